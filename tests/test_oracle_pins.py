@@ -1,0 +1,453 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Library routines (numpy's IEEE fp16 conversion, numpy textbook attention),
+closed forms (lossless quantization of grid-aligned inputs, V == 1, K == 0,
+residual-only caches), brute force on tiny inputs, invariants the pages fix
+(|x - x^| <= s/2 with the stored fp16 scale; codes in range; no INT8
+clipping) and worked numbers printed on the pages (tests/golden).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from bit_kv_cache_keyquant_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_numbers.json")
+
+
+def f16(bits):
+    return np.array(bits, dtype=np.uint16).view(np.float16)
+
+
+# --------------------------------------------------------------------------
+# fp16 conversion
+# --------------------------------------------------------------------------
+def _special_doubles(rng):
+    vals = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 70000.0, -65520.0,
+            2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -14, 2.0 ** -14 - 2.0 ** -25,
+            1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 1e-10, 3.14159]
+    vals += list(rng.standard_normal(3000) * 10.0 ** rng.uniform(-9, 5, 3000))
+    # exact ties of fp16 rounding
+    h = rng.integers(0, 0x7BFF, 500).astype(np.uint16)
+    a = f16(h).astype(np.float64)
+    b = f16(h + 1).astype(np.float64)
+    vals += list((a + b) / 2)
+    return np.array(vals, dtype=np.float64)
+
+
+def test_half_rn_matches_numpy(orc):
+    rng = np.random.default_rng(1)
+    for x in _special_doubles(rng):
+        want = np.array(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+        got = orc.double_to_half(float(x), orc.RN)
+        assert got == int(want), (x, hex(got), hex(int(want)))
+
+
+def test_half_decode_matches_numpy(orc):
+    for bits in list(range(0, 0x7C01, 7)) + [0x7BFF, 0x0001, 0x03FF, 0x0400, 0x8001, 0xFBFF]:
+        assert orc.half_to_double(bits) == float(f16(bits))
+
+
+def test_half_directed_rounding_brackets(orc):
+    rng = np.random.default_rng(2)
+    for x in _special_doubles(rng):
+        if abs(x) > 65504:
+            continue
+        lo = orc.double_to_half(float(x), orc.RD)
+        hi = orc.double_to_half(float(x), orc.RU)
+        vlo, vhi = orc.half_to_double(lo), orc.half_to_double(hi)
+        assert vlo <= x <= vhi
+        if vlo == x:
+            assert vhi == x
+        else:
+            # adjacent fp16 values
+            assert np.nextafter(np.float16(vlo), np.float16(np.inf)) == np.float16(vhi)
+
+
+# --------------------------------------------------------------------------
+# affine quantizer
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("bits", [2, 4])
+def test_affine_error_bound_and_range(orc, bits):
+    rng = np.random.default_rng(3 + bits)
+    qmax = (1 << bits) - 1
+    for trial in range(300):
+        n = int(rng.integers(2, 40))
+        scale = 10.0 ** rng.uniform(-4, 3)
+        x = (rng.standard_normal(n) * scale + rng.uniform(-3, 3) * scale).astype(np.float16)
+        if trial % 7 == 0:
+            x[:] = x[0]                      # constant group
+        s, z = orc.affine_fit(x, bits)
+        sv, zv = orc.half_to_double(s), orc.half_to_double(z)
+        xv = x.astype(np.float64)
+        assert zv <= xv.min()
+        assert zv + qmax * sv >= xv.max()
+        for xb, xx in zip(x.view(np.uint16), xv):
+            code = orc.affine_code(int(xb), s, z, bits)
+            assert 0 <= code <= qmax
+            xhat = code * sv + zv
+            assert abs(xx - xhat) <= sv / 2 * (1 + 2 ** -20) + (0 if sv else 0.0)
+        if xv.max() > xv.min():
+            # s is the fp16 round-up of the fp32 step, raised only as far as coverage needs
+            s32 = np.float32(np.float32(xv.max()) - np.float32(zv)) / np.float32(qmax)
+            assert sv >= float(s32)
+            prev = orc.half_to_double(s - 1)
+            assert prev < float(s32) or zv + qmax * prev < xv.max()
+
+
+def test_affine_grid_aligned_is_lossless(orc):
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        bits = int(rng.choice([2, 4]))
+        qmax = (1 << bits) - 1
+        s = 2.0 ** int(rng.integers(-6, 3))
+        z = s * int(rng.integers(-40, 40))
+        n = int(rng.integers(4, 33))
+        k = rng.integers(0, qmax + 1, n)
+        k[0], k[1] = 0, qmax
+        x = (z + k * s).astype(np.float16)
+        assert np.all(x.astype(np.float64) == z + k * s)
+        sb, zb = orc.affine_fit(x, bits)
+        assert orc.half_to_double(sb) == s and orc.half_to_double(zb) == z
+        for xb, kk in zip(x.view(np.uint16), k):
+            assert orc.affine_code(int(xb), sb, zb, bits) == kk
+
+
+def test_affine_brute_force_requantize(orc):
+    """All 4^4 code tuples of a 4-token 2-bit group: dequantize, refit, same codes."""
+    s = 0.25
+    z = -1.5
+    for idx in range(256):
+        k = [(idx >> (2 * i)) & 3 for i in range(4)]
+        x = np.array([z + kk * s for kk in k], dtype=np.float16)
+        sb, zb = orc.affine_fit(x, 2)
+        if min(k) == max(k):
+            assert orc.half_to_double(sb) == 0.0
+            continue
+        sv, zv = orc.half_to_double(sb), orc.half_to_double(zb)
+        codes = [orc.affine_code(int(b), sb, zb, 2) for b in x.view(np.uint16)]
+        xhat = [c * sv + zv for c in codes]
+        assert np.allclose(xhat, x.astype(np.float64), atol=sv / 2 + 1e-12)
+        if min(k) == 0 and max(k) == 3:
+            assert codes == k
+
+
+def test_kitty_step_examples(orc):
+    g = json.load(open(GOLDEN))["kitty_step_examples"]
+    for lo, hi, step, tol in g["cases"]:
+        x = np.linspace(lo, hi, 16).astype(np.float16)
+        s, z = orc.affine_fit(x, 2)
+        assert abs(orc.half_to_double(s) - step) <= tol
+        assert orc.half_to_double(z) == lo
+
+
+# --------------------------------------------------------------------------
+# packing layouts
+# --------------------------------------------------------------------------
+def test_kivi_key_layout_is_a_lane_friendly_bijection(orc):
+    seen = {}
+    for t in range(64):
+        for c in range(128):
+            off = orc.kivi_key_byte_offset(t, c)
+            seen.setdefault(off, set()).add((t // 4, c))
+            # lane 4q + c/32 of a warp finds tokens 4q..4q+3 of its 32 channels
+            # in 16-byte chunks lane and lane + 32 of the 32-token tile
+            q = (t % 32) // 4
+            lane = 4 * q + c // 32
+            chunk = (off % 1024) // 16
+            assert chunk in (lane, lane + 32)
+    assert sorted(seen) == list(range(2048))
+    assert all(len(v) == 1 for v in seen.values())
+
+
+def test_kivi_key_pack_roundtrip(orc):
+    rng = np.random.default_rng(6)
+    codes = rng.integers(0, 4, (3, 64, 128)).astype(np.uint8)
+    packed = orc.kivi_key_pack(codes)
+    for g in range(3):
+        for t in range(64):
+            for c in range(0, 128, 5):
+                b = packed[g, orc.kivi_key_byte_offset(t, c)]
+                assert (b >> (2 * (t % 4))) & 3 == codes[g, t, c]
+
+
+def test_tokenmajor_pack_matches_numpy_bitops(orc):
+    rng = np.random.default_rng(7)
+    codes = rng.integers(0, 4, (50, 128)).astype(np.uint8)
+    packed = orc.tokenmajor_pack(codes)
+    c4 = codes.reshape(50, 32, 4).astype(np.uint32)
+    want = (c4[..., 0] | (c4[..., 1] << 2) | (c4[..., 2] << 4) | (c4[..., 3] << 6)).astype(np.uint8)
+    assert np.array_equal(packed, want)
+
+
+# --------------------------------------------------------------------------
+# Kitty
+# --------------------------------------------------------------------------
+def _page(rng, G=128, D=128, heavy=True):
+    sig = 10.0 ** rng.uniform(-1, 1, D) if heavy else np.ones(D)
+    return (rng.standard_normal((G, D)) * sig).astype(np.float16)
+
+
+def test_kitty_topk_brute_force(orc):
+    rng = np.random.default_rng(8)
+    for trial in range(6):
+        x = _page(rng)
+        if trial == 1:
+            x[:, 5] = x[:, 9]                           # exact tie: lower index wins
+        score = np.abs(x.astype(np.float64)).sum(axis=0)  # exact: < 2^53 units of 2^-24
+        order = sorted(range(128), key=lambda c: (-score[c], c))
+        want = np.zeros(128, np.uint8)
+        want[order[:16]] = 1
+        assert np.array_equal(orc.kitty_select(x, 16, 0), want)
+        # variance mode, sequential fp32 sums in token order
+        s1 = np.zeros(128, np.float32)
+        s2 = np.zeros(128, np.float32)
+        for t in range(128):
+            v = x[t].astype(np.float32)
+            s1 = s1 + v
+            s2 = s2 + v * v
+        m = s1 / np.float32(128)
+        var = s2 / np.float32(128) - m * m
+        order = sorted(range(128), key=lambda c: (-float(var[c]), c))
+        want = np.zeros(128, np.uint8)
+        want[order[:16]] = 1
+        assert np.array_equal(orc.kitty_select(x, 16, 1), want)
+
+
+def test_kitty_planes_combine_to_4bit_codes(orc):
+    rng = np.random.default_rng(9)
+    x = _page(rng)
+    page = orc.kitty_key_page(x, 16)
+    assert page.size == 5248
+    codes, s, z = orc.kitty_key_page_decode(page, 128, 128, 16)
+    boosted = orc.kitty_select(x, 16, 0)
+    idx = page[4096 + 512:4096 + 512 + 128]
+    assert np.array_equal(np.flatnonzero(idx < 16), np.flatnonzero(boosted))
+    assert sorted(idx[idx < 16].tolist()) == list(range(16))
+    assert np.all(idx[boosted == 0] == 17)
+    for c in range(128):
+        bits = 4 if boosted[c] else 2
+        sc, zc = orc.affine_fit(x[:, c], bits)
+        assert (s[c], z[c]) == (sc, zc)
+        for t in range(0, 128, 3):
+            assert codes[t, c] == orc.affine_code(int(x[t, c].view(np.uint16)), sc, zc, bits)
+
+
+def test_kitty_alpha_limits(orc):
+    rng = np.random.default_rng(10)
+    x = _page(rng)
+    # alpha = 0: plain per-channel 2-bit over G = 128 tokens
+    page0 = orc.kitty_key_page(x, 0)
+    c0, s0, z0 = orc.kitty_key_page_decode(page0, 128, 128, 0)
+    kc, ksz = orc.kivi_key_codes(x[None], 2)
+    assert np.array_equal(c0, kc[0]) and np.array_equal(s0, ksz[0, :, 0]) and np.array_equal(z0, ksz[0, :, 1])
+    # alpha = 1: uniform 4-bit
+    page1 = orc.kitty_key_page(x, 128)
+    c1, s1, z1 = orc.kitty_key_page_decode(page1, 128, 128, 128)
+    kc4, ksz4 = orc.kivi_key_codes(x[None], 4)
+    assert np.array_equal(c1, kc4[0]) and np.array_equal(s1, ksz4[0, :, 0])
+
+
+def test_page_byte_accounts(orc):
+    g = json.load(open(GOLDEN))
+    D = G = 128
+    for key in ("kitty_bits_per_element", "kitty_pro_bits_per_element"):
+        a = g[key]["alpha"]
+        K = int(round(a * D))
+        code_bits = (D * G * 2 + K * G * 2) / (D * G)
+        assert code_bits == g[key]["value"]
+    assert g["kitty_boosted_channels"]["K"] == [int(a * 128) for a in g["kitty_boosted_channels"]["alpha"]]
+    assert orc.kitty_key_page_bytes(128, 128, 16) == 4096 + 512 + 128 + 512
+    assert orc.kitty_value_page_bytes(128, 128) == 4096 + 512
+    # INT8 block cache: 128 one-byte codes plus 128 fp16 scales per 256 tokens
+    assert 128 + 128 * 2 / 256 == g["int8_block_bytes_per_token_per_side"]["value"]
+    # token-granular variant: 128 codes plus one fp16 scale per 32 channels
+    assert 128 + (128 // 32) * 2 == g["int8_token_granular_bytes_per_token_per_side"]["value"]
+    assert g["kivi_group_defaults"]["R"] % g["kivi_group_defaults"]["G"] == 0
+
+
+# --------------------------------------------------------------------------
+# Philox / dither
+# --------------------------------------------------------------------------
+def test_philox_inverse_roundtrip(orc):
+    rng = np.random.default_rng(11)
+    ctrs = [[0, 0, 0, 0], [0xFFFFFFFF] * 4, [0x80000000, 1, 0xFFFFFFFF, 7]]
+    ctrs += rng.integers(0, 2 ** 32, (200, 4), dtype=np.uint64).tolist()
+    for ctr in ctrs:
+        key = rng.integers(0, 2 ** 32, 2, dtype=np.uint64)
+        out = orc.philox(ctr, key)
+        back = orc.philox_inverse(out, key)
+        assert [int(v) for v in back] == [int(v) for v in ctr]
+
+
+def test_dither_statistics_and_uniqueness(orc):
+    vals = np.array([orc.dither(0x1234, 5, 3, kv, 2, t, c)
+                     for kv in (0, 1) for t in range(64) for c in range(128)], dtype=np.float64)
+    n = vals.size
+    assert np.all(vals >= -0.5) and np.all(vals < 0.5)
+    assert abs(vals.mean()) < 5 * np.sqrt(1 / 12 / n)
+    assert abs(vals.var() - 1 / 12) < 0.004
+    # distinct five-tuples give distinct draws (collisions of 24-bit values are rare)
+    assert len(set(vals.tolist())) > 0.99 * n
+    # the K and V streams differ; changing request, layer or head changes the stream
+    a = orc.dither(7, 1, 2, 0, 3, 100, 17)
+    assert a != orc.dither(7, 1, 2, 1, 3, 100, 17)
+    assert a != orc.dither(7, 2, 2, 0, 3, 100, 17)
+    assert a != orc.dither(7, 1, 3, 0, 3, 100, 17)
+    assert a != orc.dither(7, 1, 2, 0, 4, 100, 17)
+    assert a != orc.dither(8, 1, 2, 0, 3, 100, 17)
+
+
+def test_int8_dither_no_clip_and_error_bound(orc):
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((256, 128)) * 10.0 ** rng.uniform(-2, 2, 128)).astype(np.float16)
+    x[:, 3] = 0                                    # all-zero channel: s = 0
+    codes, scale = orc.int8_quant_block(x, 99, 4, 1, 0, 2, 512)
+    assert scale[3] == 0 and np.all(codes[:, 3] == 0)
+    assert np.all(np.abs(codes.astype(np.int32)) <= 127)
+    for c in range(0, 128, 9):
+        s = orc.half_to_double(int(scale[c]))
+        amax = np.abs(x[:, c].astype(np.float64)).max()
+        assert s == float(np.float16(np.float32(amax) / np.float32(126.5)))
+        for t in range(0, 256, 17):
+            xi = orc.dither(99, 4, 1, 0, 2, 512 + t, c)
+            xhat = orc.half_to_double(0) if s == 0 else s * (int(codes[t, c]) - xi)
+            assert abs(float(x[t, c]) - xhat) <= s / 2 * (1 + 2 ** -20) + 1e-30
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+def textbook(q, K, V, sm):
+    s = (K.astype(np.float64) @ q.astype(np.float64)) * sm
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    return p @ V.astype(np.float64)
+
+
+def test_residual_only_is_textbook_attention(orc):
+    rng = np.random.default_rng(13)
+    for L in (1, 5, 77, 128):
+        K = rng.standard_normal((L, 128)).astype(np.float16)
+        V = rng.standard_normal((L, 128)).astype(np.float16)
+        q = rng.standard_normal((2, 128)).astype(np.float16)
+        parts = orc.kivi_build_one(K, V)
+        out = orc.kivi_decode_one(q, *parts, L=L)
+        for h in range(2):
+            assert np.allclose(out[h], textbook(q[h], K, V, 128 ** -0.5), atol=1e-12, rtol=0)
+
+
+def test_grid_aligned_cache_equals_fp_attention(orc):
+    """Inputs on the quantization grid: every quantized segment is lossless."""
+    rng = np.random.default_rng(14)
+    L = 300
+    kk = rng.integers(0, 4, (L, 128))
+    kk[::32][:, :] = 0
+    kk[1::32][:, :] = 3                     # every 32-token group spans codes 0..3
+    ks = 2.0 ** rng.integers(-3, 1, 128)
+    K = (ks * (kk - 1)).astype(np.float16)
+    vk = rng.integers(0, 4, (L, 128))
+    vk[:, ::32] = 0
+    vk[:, 1::32] = 3                        # every 32-channel group spans 0..3
+    V = (0.125 * vk - 0.25).astype(np.float16)
+    q = rng.standard_normal((1, 128)).astype(np.float16)
+    out = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V), L=L)
+    assert np.allclose(out[0], textbook(q[0], K, V, 128 ** -0.5), atol=1e-12, rtol=0)
+
+
+def test_constant_values_and_zero_keys(orc):
+    rng = np.random.default_rng(15)
+    L = 400
+    K = rng.standard_normal((L, 128)).astype(np.float16)
+    V = np.ones((L, 128), np.float16)
+    q = rng.standard_normal((3, 128)).astype(np.float16)
+    out = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V), L=L)
+    assert np.allclose(out, 1.0, atol=1e-12)
+    # K == 0: uniform softmax, output = mean of the dequantized values
+    K0 = np.zeros((L, 128), np.float16)
+    V2 = rng.standard_normal((L, 128)).astype(np.float16)
+    parts = orc.kivi_build_one(K0, V2)
+    out = orc.kivi_decode_one(q, *parts, L=L)
+    nkq, nvq = orc.kivi_segments(L)
+    codes, sz = orc.kivi_value_codes(V2[:nvq])
+    s = sz[..., 0].view(np.float16).astype(np.float64)
+    z = sz[..., 1].view(np.float16).astype(np.float64)
+    vhat = codes.reshape(nvq, 4, 32) * s[..., None] + z[..., None]
+    allv = np.concatenate([vhat.reshape(nvq, 128), V2[nvq:].astype(np.float64)])
+    assert np.allclose(out, allv.mean(axis=0)[None], atol=1e-12)
+
+
+def test_kitty_and_int8_short_contexts_are_textbook(orc):
+    rng = np.random.default_rng(16)
+    for L in (1, 31, 32, 33, 160):
+        K = rng.standard_normal((L, 128)).astype(np.float16)
+        V = rng.standard_normal((L, 128)).astype(np.float16)
+        q = rng.standard_normal((4, 128)).astype(np.float16)
+        out = orc.kitty_decode_one(q, *orc.kitty_build_one(K, V), L=L)
+        for h in range(4):
+            assert np.allclose(out[h], textbook(q[h], K, V, 128 ** -0.5), atol=1e-12)
+    for L in (1, 100, 256):
+        K = rng.standard_normal((L, 128)).astype(np.float16)
+        V = rng.standard_normal((L, 128)).astype(np.float16)
+        q = rng.standard_normal((2, 128)).astype(np.float16)
+        parts = orc.int8_build_one(K, V, 5, 9, 0, 1)
+        out = orc.int8_decode_one(q, *parts, L=L, seed=5, request=9, layer=0, kv_head=1)
+        for h in range(2):
+            assert np.allclose(out[h], textbook(q[h], K, V, 128 ** -0.5), atol=1e-12)
+
+
+def test_kitty_segments_match_mixed_key_workload(orc):
+    # 131072 tokens: 1023 key pages + 96 buffered keys; 1022 value pages +
+    # 96 buffered + 128 local values; 32 sink tokens each side
+    assert orc.kitty_segments(131072) == (1023, 96, 1022, 96, 128)
+    assert orc.kivi_segments(4096) == (3968, 3968)
+
+
+def test_int8_request_id_not_batch_position(orc):
+    """Permuting batch rows together with their request ids leaves outputs unchanged."""
+    rng = np.random.default_rng(17)
+    L = 600
+    rows = [(rng.standard_normal((L, 128)).astype(np.float16),
+             rng.standard_normal((L, 128)).astype(np.float16),
+             rng.standard_normal((2, 128)).astype(np.float16), rid) for rid in (11, 42)]
+    outs = {}
+    for order in ((0, 1), (1, 0)):
+        for pos, i in enumerate(order):
+            K, V, q, rid = rows[i]
+            parts = orc.int8_build_one(K, V, 3, rid, 2, 0)
+            outs[(order, rid)] = orc.int8_decode_one(q, *parts, L=L, seed=3, request=rid, layer=2, kv_head=0)
+    for rid in (11, 42):
+        assert np.array_equal(outs[((0, 1), rid)], outs[((1, 0), rid)])
+
+
+def test_int8_quantized_attention_error_is_small(orc):
+    """Dithered INT8 with the no-clip scale stays close to fp attention."""
+    rng = np.random.default_rng(18)
+    L = 700
+    K = rng.standard_normal((L, 128)).astype(np.float16)
+    V = rng.standard_normal((L, 128)).astype(np.float16)
+    q = rng.standard_normal((2, 128)).astype(np.float16)
+    parts = orc.int8_build_one(K, V, 1, 2, 3, 4)
+    out = orc.int8_decode_one(q, *parts, L=L, seed=1, request=2, layer=3, kv_head=4)
+    for h in range(2):
+        assert np.max(np.abs(out[h] - textbook(q[h], K, V, 128 ** -0.5))) < 5e-3
+
+
+# --------------------------------------------------------------------------
+# synthetic input generator
+# --------------------------------------------------------------------------
+def test_inputs_distribution_and_determinism():
+    w = I.WORKLOADS[3]
+    a = I.gen_kv_np(w, I.T_V, 5, 3, 4096)
+    b = I.gen_kv_np(w, I.T_V, 5, 3, 1000, row0=3096)
+    assert np.array_equal(a[3096:], b)
+    x = a.astype(np.float64)
+    assert abs(x.mean()) < 0.01 and abs(x.var() - 1.0) < 0.02
+    k = I.gen_kv_np(w, I.T_K, 5, 3, 512).astype(np.float64)
+    gain = I.key_channel_gain(w)[3]
+    assert np.count_nonzero(gain == 15.0) == 1
+    assert k[:, gain == 15.0].std() > 10
+    lens = I.seq_lens(I.WORKLOADS[5])
+    assert lens.min() >= 16384 and lens.max() <= 65536 and len(set(lens.tolist())) > 1
