@@ -451,3 +451,26 @@ def test_inputs_distribution_and_determinism():
     assert k[:, gain == 15.0].std() > 10
     lens = I.seq_lens(I.WORKLOADS[5])
     assert lens.min() >= 16384 and lens.max() <= 65536 and len(set(lens.tolist())) > 1
+
+
+def test_kitty_grid_aligned_long_context_equals_fp_attention(orc):
+    """Keys on {z + 5s*k} are lossless under both the 2-bit (step 5s) and the
+    4-bit (step s) fit; values on a per-token 2-bit grid are lossless.  Every
+    page, Q-buffer, local-window and sink slot must then carry its own token."""
+    rng = np.random.default_rng(19)
+    for L in (700, 32 + 128 * 2 + 128 + 1, 32 + 128 * 2 + 128):
+        s_c = 2.0 ** rng.integers(-5, -2, 128)
+        k = rng.integers(0, 4, (L, 128))
+        for p0 in range(32, L, 128):
+            k[p0, :] = 0
+            if p0 + 1 < L:
+                k[p0 + 1, :] = 3
+        K = (5 * s_c * k - 0.5).astype(np.float16)
+        vk = rng.integers(0, 4, (L, 128))
+        vk[:, 0], vk[:, 1] = 0, 3
+        st = 2.0 ** rng.integers(-4, -1, L)
+        V = (st[:, None] * vk + 0.25).astype(np.float16)
+        q = rng.standard_normal((4, 128)).astype(np.float16)
+        out = orc.kitty_decode_one(q, *orc.kitty_build_one(K, V), L=L)
+        for h in range(4):
+            assert np.allclose(out[h], textbook(q[h], K, V, 128 ** -0.5), atol=1e-12, rtol=0)
