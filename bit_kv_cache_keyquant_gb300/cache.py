@@ -1,0 +1,195 @@
+"""Device-resident KV caches in the layouts of include/kvq.h.
+
+Each class owns the torch tensors of one cache (all batch rows and kv heads
+of one layer), fills a (batch row, kv head) slice from fp16 keys and values
+through the library's quantization entry points, and exposes the C
+descriptor the decode entry points take.  Segment bookkeeping follows the
+rules stated in include/kvq.h (Kitty's insert -> attend -> quantize order).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import kvq
+
+D = 128
+
+
+def kivi_segments(L: int, R: int):
+    """(quantized keys, quantized values) at attention time with L tokens."""
+    rk = ((L - 1) % R) + 1
+    return L - rk, L - min(L, R)
+
+
+def kitty_segments(L: int, G: int, S: int, R: int):
+    """(key pages, key Q-buffer, value pages, value Q-buffer, local window)."""
+    if L > S:
+        nkb = ((L - S - 1) % G) + 1
+        pk = (L - S - nkb) // G
+    else:
+        nkb, pk = 0, 0
+    E = max(0, L - S - R)
+    nvb = ((E - 1) % G) + 1 if E > 0 else 0
+    pv = (E - nvb) // G
+    nloc = min(max(L - S, 0), R)
+    return pk, nkb, pv, nvb, nloc
+
+
+def int8_segments(L: int, T: int):
+    """(quantized blocks, fp16 tail tokens)."""
+    ntail = ((L - 1) % T) + 1
+    return (L - ntail) // T, ntail
+
+
+def _slot_copy(dst, src, slots):
+    idx = torch.as_tensor(slots, dtype=torch.int64, device=dst.device)
+    dst.index_copy_(0, idx, src)
+
+
+class KiviCache:
+    def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, device="cuda"):
+        self.cfg, self.batch, self.max_seq_len = cfg, batch, max_seq_len
+        H, G, Gv, R = cfg.n_kv_heads, cfg.group_k, cfg.group_v, cfg.residual
+        self.ngrp_cap = (max_seq_len + G - 1) // G
+        self.k_codes = torch.zeros((batch, H, self.ngrp_cap, G * D // 4), dtype=torch.uint8, device=device)
+        self.k_sz = torch.zeros((batch, H, self.ngrp_cap, D), dtype=torch.int32, device=device)
+        self.v_codes = torch.zeros((batch, H, max_seq_len, D // 4), dtype=torch.uint8, device=device)
+        self.v_sz = torch.zeros((batch, H, max_seq_len, D // Gv), dtype=torch.int32, device=device)
+        self.k_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
+        self.v_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
+        self.seq_len = torch.ones(batch, dtype=torch.int32, device=device)
+
+    def fill(self, b: int, kvh: int, K: torch.Tensor, V: torch.Tensor, stream=None):
+        """Quantize one (batch row, kv head) from fp16 K, V [L][D] on the device."""
+        cfg = self.cfg
+        L = K.shape[0]
+        assert 1 <= L <= self.max_seq_len and K.shape == V.shape == (L, D)
+        G, R = cfg.group_k, cfg.residual
+        nkq, nvq = kivi_segments(L, R)
+        if nkq:
+            kvq.kv_quant_key(cfg, K[:nkq].contiguous(), nkq // G, self.k_codes[b, kvh], self.k_sz[b, kvh], stream)
+        if nvq:
+            kvq.kv_quant_value(cfg, V[:nvq].contiguous(), nvq, self.v_codes[b, kvh], self.v_sz[b, kvh], stream)
+        _slot_copy(self.k_res[b, kvh], K[nkq:L], [t % R for t in range(nkq, L)])
+        _slot_copy(self.v_res[b, kvh], V[nvq:L], [t % R for t in range(nvq, L)])
+        self.seq_len[b] = L
+
+    def desc(self) -> kvq.kvq_kivi_cache:
+        return kvq.kvq_kivi_cache(self.batch, self.max_seq_len, self.seq_len.data_ptr(), self.k_codes.data_ptr(),
+                                  self.k_sz.data_ptr(), self.v_codes.data_ptr(), self.v_sz.data_ptr(),
+                                  self.k_res.data_ptr(), self.v_res.data_ptr())
+
+    def nbytes_read(self, lens) -> int:
+        """Algorithmic bytes one decode step reads from this cache (codes, (s, z), fp16 residual)."""
+        cfg = self.cfg
+        tot = 0
+        for L in lens:
+            nkq, nvq = kivi_segments(int(L), cfg.residual)
+            tot += nkq * D // 4 + (nkq // cfg.group_k) * D * 4          # key codes + (s, z)
+            tot += nvq * D // 4 + nvq * (D // cfg.group_v) * 4            # value codes + (s, z)
+            tot += (int(L) - nkq + int(L) - nvq) * D * 2                 # fp16 residual
+        return tot * cfg.n_kv_heads
+
+
+class KittyCache:
+    def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, device="cuda"):
+        self.cfg, self.batch, self.max_seq_len = cfg, batch, max_seq_len
+        H, G, S, R = cfg.n_kv_heads, cfg.group_k, cfg.sink, cfg.residual
+        self.kpb = kvq.kvq_kitty_key_page_bytes(cfg)
+        self.vpb = kvq.kvq_kitty_value_page_bytes(cfg)
+        self.page_cap = max(1, (max(max_seq_len - S, 0) + G - 1) // G)
+        self.k_pages = torch.zeros((batch, H, self.page_cap, self.kpb), dtype=torch.uint8, device=device)
+        self.v_pages = torch.zeros((batch, H, self.page_cap, self.vpb), dtype=torch.uint8, device=device)
+        self.k_sink = torch.zeros((batch, H, max(S, 1), D), dtype=torch.float16, device=device)
+        self.v_sink = torch.zeros((batch, H, max(S, 1), D), dtype=torch.float16, device=device)
+        self.k_qbuf = torch.zeros((batch, H, G, D), dtype=torch.float16, device=device)
+        self.v_qbuf = torch.zeros((batch, H, G, D), dtype=torch.float16, device=device)
+        self.v_local = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
+        self.seq_len = torch.ones(batch, dtype=torch.int32, device=device)
+
+    def fill(self, b: int, kvh: int, K: torch.Tensor, V: torch.Tensor, score_mode: int = 0, stream=None):
+        cfg = self.cfg
+        L = K.shape[0]
+        assert 1 <= L <= self.max_seq_len
+        G, S, R = cfg.group_k, cfg.sink, cfg.residual
+        pk, nkb, pv, nvb, nloc = kitty_segments(L, G, S, R)
+        if pk:
+            kvq.kv_quant_key_kitty(cfg, K[S:S + pk * G].contiguous(), pk, score_mode, self.k_pages[b, kvh], stream)
+        if pv:
+            kvq.kv_quant_value_kitty(cfg, V[S:S + pv * G].contiguous(), pv, self.v_pages[b, kvh], stream)
+        ns = min(L, S)
+        if ns:
+            self.k_sink[b, kvh, :ns] = K[:ns]
+            self.v_sink[b, kvh, :ns] = V[:ns]
+        k0 = S + pk * G
+        if L > k0:
+            _slot_copy(self.k_qbuf[b, kvh], K[k0:L], [(t - S) % G for t in range(k0, L)])
+        v0 = S + pv * G
+        if nvb:
+            _slot_copy(self.v_qbuf[b, kvh], V[v0:v0 + nvb], [(t - S) % G for t in range(v0, v0 + nvb)])
+        if nloc:
+            _slot_copy(self.v_local[b, kvh], V[L - nloc:L], [t % R for t in range(L - nloc, L)])
+        self.seq_len[b] = L
+
+    def desc(self) -> kvq.kvq_kitty_cache:
+        return kvq.kvq_kitty_cache(self.batch, self.max_seq_len, self.seq_len.data_ptr(), self.k_pages.data_ptr(),
+                                   self.v_pages.data_ptr(), self.k_sink.data_ptr(), self.v_sink.data_ptr(),
+                                   self.k_qbuf.data_ptr(), self.v_qbuf.data_ptr(), self.v_local.data_ptr())
+
+    def nbytes_read(self, lens) -> int:
+        cfg = self.cfg
+        tot = 0
+        for L in lens:
+            pk, nkb, pv, nvb, nloc = kitty_segments(int(L), cfg.group_k, cfg.sink, cfg.residual)
+            ns = min(int(L), cfg.sink)
+            tot += pk * self.kpb + pv * self.vpb + (2 * ns + nkb + nvb + nloc) * D * 2
+        return tot * cfg.n_kv_heads
+
+
+class Int8Cache:
+    def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, layer: int = 0, seed: int = 0,
+                 device="cuda"):
+        self.cfg, self.batch, self.max_seq_len, self.layer, self.seed = cfg, batch, max_seq_len, layer, seed
+        H, T = cfg.n_kv_heads, cfg.int8_block
+        self.blk_cap = max(1, (max_seq_len + T - 1) // T)
+        self.k_codes = torch.zeros((batch, H, max_seq_len, D), dtype=torch.int8, device=device)
+        self.v_codes = torch.zeros((batch, H, max_seq_len, D), dtype=torch.int8, device=device)
+        self.k_scale = torch.zeros((batch, H, self.blk_cap, D), dtype=torch.float16, device=device)
+        self.v_scale = torch.zeros((batch, H, self.blk_cap, D), dtype=torch.float16, device=device)
+        self.k_tail = torch.zeros((batch, H, T, D), dtype=torch.float16, device=device)
+        self.v_tail = torch.zeros((batch, H, T, D), dtype=torch.float16, device=device)
+        self.seq_len = torch.ones(batch, dtype=torch.int32, device=device)
+        self.req_id = torch.zeros(batch, dtype=torch.int32, device=device)
+
+    def fill(self, b: int, kvh: int, K: torch.Tensor, V: torch.Tensor, req_id: int, stream=None):
+        cfg = self.cfg
+        L = K.shape[0]
+        T = cfg.int8_block
+        nb, ntail = int8_segments(L, T)
+        if nb:
+            dev = K.device
+            req = torch.full((nb,), req_id, dtype=torch.int32, device=dev)
+            head = torch.full((nb,), kvh, dtype=torch.int32, device=dev)
+            tok0 = torch.arange(0, nb * T, T, dtype=torch.int32, device=dev)
+            for sel, X, codes, scale in ((0, K, self.k_codes, self.k_scale), (1, V, self.v_codes, self.v_scale)):
+                kvq.kv_quant_int8_dither(cfg, X[:nb * T].contiguous(), nb, req, head, tok0, self.layer, sel,
+                                         self.seed, codes[b, kvh], scale[b, kvh], stream)
+        q0 = nb * T
+        _slot_copy(self.k_tail[b, kvh], K[q0:L], [t % T for t in range(q0, L)])
+        _slot_copy(self.v_tail[b, kvh], V[q0:L], [t % T for t in range(q0, L)])
+        self.seq_len[b] = L
+        self.req_id[b] = req_id
+
+    def desc(self) -> kvq.kvq_int8_cache:
+        return kvq.kvq_int8_cache(self.batch, self.max_seq_len, self.seq_len.data_ptr(), self.req_id.data_ptr(),
+                                  self.layer, self.seed, self.k_codes.data_ptr(), self.v_codes.data_ptr(),
+                                  self.k_scale.data_ptr(), self.v_scale.data_ptr(), self.k_tail.data_ptr(),
+                                  self.v_tail.data_ptr())
+
+    def nbytes_read(self, lens) -> int:
+        T = self.cfg.int8_block
+        tot = 0
+        for L in lens:
+            nb, ntail = int8_segments(int(L), T)
+            tot += 2 * (nb * T * D + nb * D * 2 + ntail * D * 2)
+        return tot * self.cfg.n_kv_heads

@@ -1,0 +1,350 @@
+// extern "C" entry points of libkvq: host-side argument validation, the
+// split-KV plan, and dispatch to the kernels.  Nothing here allocates device
+// memory or synchronizes the host (except kvq_get_device_error, documented
+// as synchronous).
+#include <math.h>
+#include <string.h>
+
+#include <initializer_list>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// Device error bitmask: kernels atomically OR KVQ_DEVICE_ERR_* into it
+// instead of trapping.  Its device address is passed to every kernel that
+// can wait.
+__device__ unsigned g_device_error;
+
+static const int kMaxDevices = 64;
+
+int num_sms() {
+    static int cached[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+unsigned *device_error_ptr() {
+    static unsigned *cached[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!cached[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<unsigned *>(p);
+    }
+    return cached[dev];
+}
+
+float sm_scale_of(const kvq_config *cfg) {
+    return cfg->sm_scale > 0.f ? cfg->sm_scale : 1.0f / sqrtf((float)cfg->head_dim);
+}
+
+// Splits: 512-token chunks (a multiple of the 128-token stage), widened so
+// that no row has more than 256 splits.
+kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
+    (void)variant;
+    int chunk = 512;
+    const int min_chunk = (int)((((int64_t)max_seq_len + 255) / 256 + 127) / 128 * 128);
+    if (min_chunk > chunk) chunk = min_chunk;
+    const int splits = (max_seq_len + chunk - 1) / chunk;
+    const int64_t rows = (int64_t)batch * cfg->n_q_heads;
+    p->splits = splits < 1 ? 1 : splits;
+    p->chunk = chunk;
+    p->off_o = 256;
+    p->off_lse = p->off_o + (size_t)rows * p->splits * KVQ_D * sizeof(float);
+    p->ws_bytes = (p->off_lse + (size_t)rows * p->splits * sizeof(float) + 255) / 256 * 256;
+    return KVQ_OK;
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+// ---------------------------------------------------------------------------
+// validation helpers
+// ---------------------------------------------------------------------------
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static kvq_status check_common(const kvq_config *cfg) {
+    if (!cfg) return KVQ_ERR_INVALID_ARG;
+    if (cfg->n_q_heads < 1 || cfg->n_kv_heads < 1 || cfg->n_q_heads % cfg->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+    if (cfg->sm_scale < 0.f || !(cfg->sm_scale == cfg->sm_scale)) return KVQ_ERR_INVALID_ARG;
+    if (cfg->head_dim != KVQ_D) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+static kvq_status check_kivi(const kvq_config *cfg) {
+    kvq_status s = check_common(cfg);
+    if (s) return s;
+    if (cfg->group_k <= 0 || cfg->group_v <= 0 || cfg->residual <= 0) return KVQ_ERR_INVALID_ARG;
+    if (cfg->bits_k != 2 || cfg->bits_v != 2) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->group_k != 32 && cfg->group_k != 64 && cfg->group_k != 128) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->group_v != 32 && cfg->group_v != 64 && cfg->group_v != 128) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->residual % cfg->group_k != 0) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+static kvq_status check_kitty(const kvq_config *cfg) {
+    kvq_status s = check_common(cfg);
+    if (s) return s;
+    if (cfg->group_k <= 0 || cfg->residual <= 0 || cfg->sink < 0 || cfg->boost_k < 0 || cfg->boost_k > cfg->head_dim)
+        return KVQ_ERR_INVALID_ARG;
+    if (cfg->group_k != 128 || cfg->bits_v != 2) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+static kvq_status check_int8(const kvq_config *cfg) {
+    kvq_status s = check_common(cfg);
+    if (s) return s;
+    if (cfg->int8_block <= 0) return KVQ_ERR_INVALID_ARG;
+    if (cfg->int8_block % 128 != 0) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+static kvq_status ptrs_ok(std::initializer_list<const void *> ps) {
+    for (const void *p : ps) {
+        if (!p) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(p)) return KVQ_ERR_MISALIGNED;
+    }
+    return KVQ_OK;
+}
+
+static kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// write side
+// ---------------------------------------------------------------------------
+extern "C" kvq_status kv_quant_key(const kvq_config *cfg, const void *k, int64_t n_groups, void *codes, void *sz,
+                                   cudaStream_t stream) {
+    kvq_status s = check_kivi(cfg);
+    if (s) return s;
+    if (n_groups < 0) return KVQ_ERR_INVALID_ARG;
+    if (n_groups == 0) return KVQ_OK;
+    if ((s = ptrs_ok({k, codes, sz}))) return s;
+    return cuda_status(launch_quant_key_kivi(cfg, k, n_groups, codes, sz, stream));
+}
+
+extern "C" kvq_status kv_quant_value(const kvq_config *cfg, const void *v, int64_t n_tokens, void *codes, void *sz,
+                                     cudaStream_t stream) {
+    kvq_status s = check_kivi(cfg);
+    if (s) return s;
+    if (n_tokens < 0) return KVQ_ERR_INVALID_ARG;
+    if (n_tokens == 0) return KVQ_OK;
+    if ((s = ptrs_ok({v, codes, sz}))) return s;
+    return cuda_status(launch_quant_value_kivi(cfg, v, n_tokens, codes, sz, stream));
+}
+
+extern "C" size_t kvq_kitty_key_page_bytes(const kvq_config *cfg) {
+    if (check_kitty(cfg)) return 0;
+    return (size_t)KVQ_D * cfg->group_k / 4 + (size_t)cfg->boost_k * cfg->group_k / 4 + KVQ_D + 4 * KVQ_D;
+}
+
+extern "C" size_t kvq_kitty_value_page_bytes(const kvq_config *cfg) {
+    if (check_kitty(cfg)) return 0;
+    return (size_t)cfg->group_k * KVQ_D / 4 + 4 * (size_t)cfg->group_k;
+}
+
+extern "C" kvq_status kv_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t n_pages, int32_t score_mode,
+                                         void *pages, cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (n_pages < 0 || (score_mode != 0 && score_mode != 1)) return KVQ_ERR_INVALID_ARG;
+    if (n_pages == 0) return KVQ_OK;
+    if ((s = ptrs_ok({k, pages}))) return s;
+    return cuda_status(launch_quant_key_kitty(cfg, k, n_pages, score_mode, pages, stream));
+}
+
+extern "C" kvq_status kv_quant_value_kitty(const kvq_config *cfg, const void *v, int64_t n_pages, void *pages,
+                                           cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (n_pages < 0) return KVQ_ERR_INVALID_ARG;
+    if (n_pages == 0) return KVQ_OK;
+    if ((s = ptrs_ok({v, pages}))) return s;
+    return cuda_status(launch_quant_value_kitty(cfg, v, n_pages, pages, stream));
+}
+
+extern "C" kvq_status kv_quant_int8_dither(const kvq_config *cfg, const void *x, int64_t n_blocks,
+                                           const int32_t *req_id, const int32_t *kv_head, const int32_t *tok0,
+                                           int32_t layer, int32_t kv_sel, uint64_t seed, void *codes, void *scale,
+                                           cudaStream_t stream) {
+    kvq_status s = check_int8(cfg);
+    if (s) return s;
+    if (n_blocks < 0 || layer < 0 || layer >= (1 << 15) || (kv_sel != 0 && kv_sel != 1)) return KVQ_ERR_INVALID_ARG;
+    if (n_blocks == 0) return KVQ_OK;
+    if ((s = ptrs_ok({x, codes, scale}))) return s;
+    if (!req_id || !kv_head || !tok0) return KVQ_ERR_INVALID_ARG;
+    return cuda_status(launch_quant_int8(cfg, x, n_blocks, req_id, kv_head, tok0, layer, kv_sel, seed, codes, scale,
+                                         stream));
+}
+
+// ---------------------------------------------------------------------------
+// read side
+// ---------------------------------------------------------------------------
+extern "C" kvq_status kv_decode_attn_plan(const kvq_config *cfg, int32_t variant, int32_t batch, int32_t max_seq_len,
+                                          int32_t *n_splits, size_t *workspace_bytes) {
+    kvq_status s = variant == KVQ_VARIANT_KIVI    ? check_kivi(cfg)
+                   : variant == KVQ_VARIANT_KITTY ? check_kitty(cfg)
+                   : variant == KVQ_VARIANT_INT8  ? check_int8(cfg)
+                                                  : KVQ_ERR_INVALID_ARG;
+    if (s) return s;
+    if (batch < 1 || max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
+    DecodePlan p;
+    plan_decode(cfg, variant, batch, max_seq_len, &p);
+    if (n_splits) *n_splits = p.splits;
+    if (workspace_bytes) *workspace_bytes = p.ws_bytes;
+    return KVQ_OK;
+}
+
+static kvq_status check_ws(const kvq_config *cfg, int variant, int batch, int max_seq_len, const void *ws,
+                           size_t ws_bytes, DecodePlan *p) {
+    if (batch < 1 || max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
+    plan_decode(cfg, variant, batch, max_seq_len, p);
+    if (!ws) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return KVQ_ERR_MISALIGNED;
+    if (ws_bytes < p->ws_bytes) return KVQ_ERR_WORKSPACE;
+    return KVQ_OK;
+}
+
+static kvq_status stage1_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q, void *ws, size_t wsb,
+                              cudaStream_t st, DecodePlan *p) {
+    kvq_status s = check_kivi(cfg);
+    if (s) return s;
+    if (!c) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_ws(cfg, KVQ_VARIANT_KIVI, c->batch, c->max_seq_len, ws, wsb, p))) return s;
+    if ((s = ptrs_ok({q, c->seq_len, c->k_codes, c->k_sz, c->v_codes, c->v_sz, c->k_res, c->v_res}))) return s;
+    return cuda_status(launch_decode_kivi(cfg, c, q, *p, ws, st));
+}
+
+static kvq_status stage1_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q, void *ws, size_t wsb,
+                               cudaStream_t st, DecodePlan *p) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (!c) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_ws(cfg, KVQ_VARIANT_KITTY, c->batch, c->max_seq_len, ws, wsb, p))) return s;
+    if ((s = ptrs_ok({q, c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local}))) return s;
+    if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;
+    return cuda_status(launch_decode_kitty(cfg, c, q, *p, ws, st));
+}
+
+static kvq_status stage1_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *q, void *ws, size_t wsb,
+                              cudaStream_t st, DecodePlan *p) {
+    kvq_status s = check_int8(cfg);
+    if (s) return s;
+    if (!c) return KVQ_ERR_INVALID_ARG;
+    if (c->layer < 0 || c->layer >= (1 << 15)) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_ws(cfg, KVQ_VARIANT_INT8, c->batch, c->max_seq_len, ws, wsb, p))) return s;
+    if ((s = ptrs_ok({q, c->seq_len, c->req_id, c->k_codes, c->v_codes, c->k_scale, c->v_scale, c->k_tail,
+                      c->v_tail})))
+        return s;
+    return cuda_status(launch_decode_int8(cfg, c, q, *p, ws, st));
+}
+
+extern "C" kvq_status kv_decode_attn_stage1(const kvq_config *cfg, int32_t variant, const void *cache, const void *q,
+                                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    DecodePlan p;
+    switch (variant) {
+        case KVQ_VARIANT_KIVI:
+            return stage1_kivi(cfg, static_cast<const kvq_kivi_cache *>(cache), q, workspace, workspace_bytes, stream, &p);
+        case KVQ_VARIANT_KITTY:
+            return stage1_kitty(cfg, static_cast<const kvq_kitty_cache *>(cache), q, workspace, workspace_bytes, stream,
+                                &p);
+        case KVQ_VARIANT_INT8:
+            return stage1_int8(cfg, static_cast<const kvq_int8_cache *>(cache), q, workspace, workspace_bytes, stream, &p);
+        default:
+            return KVQ_ERR_INVALID_ARG;
+    }
+}
+
+extern "C" kvq_status kv_decode_attn_merge(const kvq_config *cfg, int32_t variant, int32_t batch, int32_t max_seq_len,
+                                           const void *workspace, size_t workspace_bytes, void *out,
+                                           cudaStream_t stream) {
+    kvq_status s = variant == KVQ_VARIANT_KIVI    ? check_kivi(cfg)
+                   : variant == KVQ_VARIANT_KITTY ? check_kitty(cfg)
+                   : variant == KVQ_VARIANT_INT8  ? check_int8(cfg)
+                                                  : KVQ_ERR_INVALID_ARG;
+    if (s) return s;
+    DecodePlan p;
+    if ((s = check_ws(cfg, variant, batch, max_seq_len, workspace, workspace_bytes, &p))) return s;
+    if ((s = ptrs_ok({out}))) return s;
+    return cuda_status(launch_merge(cfg, batch, p, workspace, out, stream));
+}
+
+extern "C" kvq_status kv_decode_attn(const kvq_config *cfg, const kvq_kivi_cache *cache, const void *q, void *out,
+                                     void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
+    DecodePlan p;
+    kvq_status s = stage1_kivi(cfg, cache, q, workspace, workspace_bytes, stream, &p);
+    if (s) return s;
+    return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
+}
+
+extern "C" kvq_status kv_decode_attn_kitty(const kvq_config *cfg, const kvq_kitty_cache *cache, const void *q,
+                                           void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
+    DecodePlan p;
+    kvq_status s = stage1_kitty(cfg, cache, q, workspace, workspace_bytes, stream, &p);
+    if (s) return s;
+    return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
+}
+
+extern "C" kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_cache *cache, const void *q,
+                                          void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
+    DecodePlan p;
+    kvq_status s = stage1_int8(cfg, cache, q, workspace, workspace_bytes, stream, &p);
+    if (s) return s;
+    return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
+}
+
+// ---------------------------------------------------------------------------
+// diagnostics
+// ---------------------------------------------------------------------------
+extern "C" kvq_status kvq_philox4x32_10(const uint32_t *ctr, const uint32_t *key, int64_t n, uint32_t *out,
+                                        cudaStream_t stream) {
+    if (n < 0) return KVQ_ERR_INVALID_ARG;
+    if (n == 0) return KVQ_OK;
+    kvq_status s = ptrs_ok({ctr, key, out});
+    if (s) return s;
+    return cuda_status(launch_philox(ctr, key, n, out, stream));
+}
+
+extern "C" kvq_status kvq_get_device_error(uint32_t *flags) {
+    if (!flags) return KVQ_ERR_INVALID_ARG;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return KVQ_ERR_CUDA;
+    *flags = v;
+    return KVQ_OK;
+}
+
+extern "C" const char *kvq_status_string(kvq_status s) {
+    switch (s) {
+        case KVQ_OK: return "ok";
+        case KVQ_ERR_INVALID_ARG: return "invalid argument";
+        case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KVQ_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case KVQ_ERR_CUDA: return "CUDA error";
+        case KVQ_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+extern "C" const char *kvq_version(void) { return "kvq 0.1 (sm_103a)"; }

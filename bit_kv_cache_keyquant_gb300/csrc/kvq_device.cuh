@@ -1,0 +1,132 @@
+// Device helpers shared by the kvq kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#define KVQ_D 128
+#define KVQ_SPIN_LIMIT (1u << 22)   // bounded mbarrier waits (each try_wait suspends a while)
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// fp16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+__device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ uint16_t f2h_rd(float f) { return __half_as_ushort(__float2half_rd(f)); }
+__device__ __forceinline__ uint16_t f2h_ru(float f) { return __half_as_ushort(__float2half_ru(f)); }
+
+// d = a * b + c with f16 a, b and an f32 accumulator (one rounding, exact product).
+__device__ __forceinline__ float fma_f16f32(uint16_t a, uint16_t b, float c) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ uint16_t lo16(uint32_t v) { return (uint16_t)(v & 0xFFFFu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t v) { return (uint16_t)(v >> 16); }
+
+// Asymmetric min-max fit for b-bit codes (same rules as the C ABI states):
+//   z = fp16 round-down(mn); s = fp16 round-up(fp32 (mx - z) / qmax), raised
+//   one fp16 step while z + qmax*s < mx (checked exactly in fp64);
+//   s = 0 when mx == mn.
+__device__ __forceinline__ void affine_fit(float mn, float mx, int qmax, uint16_t &s, uint16_t &z) {
+    z = f2h_rd(mn);
+    s = 0;
+    if (mx > mn) {
+        float zf = h2f(z);
+        float range = __fsub_rn(mx, zf);
+        float s32 = __fdiv_rn(range, (float)qmax);
+        s = f2h_ru(s32);
+        while ((double)zf + (double)h2f(s) * (double)qmax < (double)mx) s = (uint16_t)(s + 1);
+    }
+}
+
+// code = clamp(rint((x - z) / s), 0, qmax) in fp32; 0 when s == 0.
+__device__ __forceinline__ int affine_code(float x, float zf, float sf, int qmax) {
+    if (sf == 0.0f) return 0;
+    float u = __fdiv_rn(__fsub_rn(x, zf), sf);
+    float r = rintf(u);
+    r = fminf(fmaxf(r, 0.0f), (float)qmax);
+    return (int)r;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3")
+// ---------------------------------------------------------------------------
+struct philox_key { uint32_t k0, k1; };
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+    const uint32_t MA = 0xD2511F53u, MB = 0xCD9E8D57u;
+    const uint32_t WA = 0x9E3779B9u, WB = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint32_t hA = __umulhi(MA, c.x), lA = MA * c.x;
+        uint32_t hB = __umulhi(MB, c.z), lB = MB * c.z;
+        uint4 n;
+        n.x = hB ^ c.y ^ k0;
+        n.y = lB;
+        n.z = hA ^ c.w ^ k1;
+        n.w = lA;
+        c = n;
+        k0 += WA;
+        k1 += WB;
+    }
+    return c;
+}
+
+// Dither xi in [-1/2, 1/2) from one Philox output word.
+__device__ __forceinline__ float dither_from_word(uint32_t w) {
+    return __fsub_rn(__uint2float_rn(w >> 8) * 0x1.0p-24f, 0.5f);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D bulk async copy (TMA engine, no tensor map)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }"
+                 ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait: false (and the device error flag set) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+    for (uint32_t i = 0; i < KVQ_SPIN_LIMIT; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicOr(err, 1u);
+    return false;
+}
+// Global -> shared bulk copy completing on `bar`; src, dst 16-B aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+}  // namespace kvq

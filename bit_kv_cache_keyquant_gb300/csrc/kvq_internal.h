@@ -1,0 +1,49 @@
+// Host-side declarations shared by the kvq translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+struct DecodePlan {
+    int splits;        // splits per (batch row, query head)
+    int chunk;         // tokens per split (multiple of 128)
+    size_t ws_bytes;   // workspace bytes
+    size_t off_o;      // byte offset of o_s  fp32 [B][Hq][splits][D]
+    size_t off_lse;    // byte offset of lse_s fp32 [B][Hq][splits]
+};
+
+int num_sms();
+unsigned *device_error_ptr();   // device address of the error bitmask (current device)
+
+float sm_scale_of(const kvq_config *cfg);
+kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p);
+
+// launchers (return a CUDA error code; arguments already validated)
+cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t n_groups, void *codes,
+                                  void *sz, cudaStream_t st);
+cudaError_t launch_quant_value_kivi(const kvq_config *cfg, const void *v, int64_t n_tokens, void *codes,
+                                    void *sz, cudaStream_t st);
+cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t n_pages, int score_mode,
+                                   void *pages, cudaStream_t st);
+cudaError_t launch_quant_value_kitty(const kvq_config *cfg, const void *v, int64_t n_pages, void *pages,
+                                     cudaStream_t st);
+cudaError_t launch_quant_int8(const kvq_config *cfg, const void *x, int64_t n_blocks, const int32_t *req,
+                              const int32_t *head, const int32_t *tok0, int layer, int kv_sel, uint64_t seed,
+                              void *codes, void *scale, cudaStream_t st);
+
+cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q,
+                               const DecodePlan &p, void *ws, cudaStream_t st);
+cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,
+                                const DecodePlan &p, void *ws, cudaStream_t st);
+cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *q,
+                               const DecodePlan &p, void *ws, cudaStream_t st);
+cudaError_t launch_merge(const kvq_config *cfg, int batch, const DecodePlan &p, const void *ws, void *out,
+                         cudaStream_t st);
+
+cudaError_t launch_philox(const uint32_t *ctr, const uint32_t *key, int64_t n, uint32_t *out, cudaStream_t st);
+
+}  // namespace kvq

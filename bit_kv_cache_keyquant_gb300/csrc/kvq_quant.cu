@@ -1,0 +1,406 @@
+// Write-side kernels: KIVI key groups and value tokens, Kitty key / value
+// pages, WitCert INT8 subtractive dither, and the Philox diagnostic.
+//
+// Bit-exactness: every fp32 operation that decides a code is an explicit
+// round-to-nearest intrinsic (__fsub_rn, __fdiv_rn, rintf) so that no FMA
+// contraction or approximate division changes a code; scales and zeros are
+// rounded with the directed fp16 conversions the C ABI documents.
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// a1: KIVI key groups.  One CTA (4 warps) per group of G = 32*NT tokens;
+// warp w owns channels [32w, 32w+32); lane t holds token t of every 32-token
+// tile.  Per-channel min / max is a warp-shuffle reduce-scatter that leaves
+// lane l with channel 32w + l; codes are packed in registers and OR-reduced
+// across the four lanes of a token quad, then stored as 16-byte chunks in
+// the tile layout (KIVI section 3.3; Kitty Observation 1 formula).
+// ---------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
+                                                             uint8_t *__restrict__ codes, uint32_t *__restrict__ sz) {
+    const int64_t g = blockIdx.x;
+    if (g >= n_groups) return;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int G = 32 * NT;
+    const uint16_t *src = k + g * (int64_t)G * KVQ_D;
+
+    // lane's 32 channels of token lane in each tile: 4 x 16 bytes per tile
+    uint32_t xv[NT][16];
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(src + (int64_t)(tt * 32 + lane) * KVQ_D + 32 * w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 u = __ldg(p + i);
+            xv[tt][4 * i + 0] = u.x; xv[tt][4 * i + 1] = u.y; xv[tt][4 * i + 2] = u.z; xv[tt][4 * i + 3] = u.w;
+        }
+    }
+    // per-lane min / max over its NT tokens for the 32 channels
+    float mn[32], mx[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        float v = h2f((c & 1) ? hi16(xv[0][c >> 1]) : lo16(xv[0][c >> 1]));
+        mn[c] = v; mx[c] = v;
+#pragma unroll
+        for (int tt = 1; tt < NT; ++tt) {
+            float u = h2f((c & 1) ? hi16(xv[tt][c >> 1]) : lo16(xv[tt][c >> 1]));
+            mn[c] = fminf(mn[c], u); mx[c] = fmaxf(mx[c], u);
+        }
+    }
+    // reduce-scatter over the 32 lanes: after the step with offset o, a lane
+    // keeps the half of its channels selected by lane bit o
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int c = 0; c < o; ++c) {
+            float send_mn = up ? mn[c] : mn[c + o];
+            float send_mx = up ? mx[c] : mx[c + o];
+            float keep_mn = up ? mn[c + o] : mn[c];
+            float keep_mx = up ? mx[c + o] : mx[c];
+            float r_mn = __shfl_xor_sync(0xFFFFFFFFu, send_mn, o);
+            float r_mx = __shfl_xor_sync(0xFFFFFFFFu, send_mx, o);
+            mn[c] = fminf(keep_mn, r_mn);
+            mx[c] = fmaxf(keep_mx, r_mx);
+        }
+    }
+    // lane now holds channel 32w + lane in slot 0
+    uint16_t s, z;
+    affine_fit(mn[0], mx[0], 3, s, z);
+    const uint32_t my_sz = (uint32_t)s | ((uint32_t)z << 16);
+    sz[g * KVQ_D + 32 * w + lane] = my_sz;
+
+    const int q = lane >> 2, j = lane & 3;
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt) {
+        uint32_t word[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) word[i] = 0;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            uint32_t szc = __shfl_sync(0xFFFFFFFFu, my_sz, c);
+            float sf = h2f(lo16(szc)), zf = h2f(hi16(szc));
+            float x = h2f((c & 1) ? hi16(xv[tt][c >> 1]) : lo16(xv[tt][c >> 1]));
+            uint32_t code = (uint32_t)affine_code(x, zf, sf, 3);
+            word[c >> 2] |= code << (8 * (c & 3) + 2 * j);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            word[i] |= __shfl_xor_sync(0xFFFFFFFFu, word[i], 1);
+            word[i] |= __shfl_xor_sync(0xFFFFFFFFu, word[i], 2);
+        }
+        uint8_t *tile = codes + g * (int64_t)G * KVQ_D / 4 + tt * 1024;
+        if (j < 2) {
+            uint4 v = j == 0 ? make_uint4(word[0], word[1], word[2], word[3])
+                             : make_uint4(word[4], word[5], word[6], word[7]);
+            *reinterpret_cast<uint4 *>(tile + j * 512 + (4 * q + w) * 16) = v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a2 / a6: per-token value quantization over groups of GV channels.  One warp
+// per token; lane l holds channels 4l..4l+3; group min / max by xor shuffles
+// inside the GV/4 lanes of a group.  Output either KIVI (interleaved (s, z)
+// per group) or a Kitty value page (separate s[G], z[G] after the codes).
+// ---------------------------------------------------------------------------
+template <int GV, bool KITTY>
+__global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
+                                                          uint8_t *__restrict__ out, uint32_t *__restrict__ sz,
+                                                          int page_tokens, int64_t page_bytes) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    constexpr int LG = GV / 4;   // lanes per group
+    for (int64_t t = warp; t < n_tokens; t += nwarps) {
+        uint2 u = __ldg(reinterpret_cast<const uint2 *>(v + t * KVQ_D) + lane);
+        float x0 = h2f(lo16(u.x)), x1 = h2f(hi16(u.x)), x2 = h2f(lo16(u.y)), x3 = h2f(hi16(u.y));
+        float mn = fminf(fminf(x0, x1), fminf(x2, x3));
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+#pragma unroll
+        for (int o = 1; o < LG; o <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        }
+        uint16_t s, z;
+        affine_fit(mn, mx, 3, s, z);
+        float sf = h2f(s), zf = h2f(z);
+        uint32_t b = (uint32_t)affine_code(x0, zf, sf, 3) | ((uint32_t)affine_code(x1, zf, sf, 3) << 2) |
+                     ((uint32_t)affine_code(x2, zf, sf, 3) << 4) | ((uint32_t)affine_code(x3, zf, sf, 3) << 6);
+        uint32_t wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 8) | (__shfl_down_sync(0xFFFFFFFFu, b, 2) << 16) |
+                      (__shfl_down_sync(0xFFFFFFFFu, b, 3) << 24);
+        if (!KITTY) {
+            if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(out + t * (KVQ_D / 4))[lane >> 2] = wv;
+            if ((lane % LG) == 0) sz[t * (KVQ_D / GV) + lane / LG] = (uint32_t)s | ((uint32_t)z << 16);
+        } else {
+            const int64_t p = t / page_tokens;
+            const int tt = (int)(t % page_tokens);
+            uint8_t *pg = out + p * page_bytes;
+            if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(pg + (int64_t)tt * (KVQ_D / 4))[lane >> 2] = wv;
+            if (lane == 0) {
+                uint16_t *ps = reinterpret_cast<uint16_t *>(pg + (int64_t)page_tokens * KVQ_D / 4);
+                ps[tt] = s;
+                ps[page_tokens + tt] = z;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a5: Kitty key page.  One CTA of 128 threads per page (thread = channel);
+// the page is staged in shared memory.  Score: Eq. 2 as an exact integer sum
+// of |x| in units of 2^-24, or the sequential-fp32 population variance.
+// Rank = number of channels with a larger score (ties: lower channel first);
+// boosted iff rank < K; idx = boosted channels below this one.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ long long abs_units(uint16_t h) {
+    const int e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    return e == 0 ? (long long)m : ((long long)(1024 + m) << (e - 1));
+}
+
+__global__ void __launch_bounds__(128) quant_key_kitty_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
+                                                              int K, int score_mode, uint8_t *__restrict__ pages,
+                                                              int64_t page_bytes) {
+    constexpr int G = 128;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);            // [G][D]
+    long long *si = reinterpret_cast<long long *>(xs + G * KVQ_D);     // [D]
+    float *sf = reinterpret_cast<float *>(si + KVQ_D);                 // [D]
+    int *boost = reinterpret_cast<int *>(sf + KVQ_D);                   // [D]
+    const int c = threadIdx.x;
+    for (int64_t p = blockIdx.x; p < n_pages; p += gridDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(k + p * (int64_t)G * KVQ_D);
+        for (int i = c; i < G * KVQ_D / 8; i += 128) reinterpret_cast<uint4 *>(xs)[i] = __ldg(src + i);
+        __syncthreads();
+        long long a = 0;
+        float s1 = 0.f, s2 = 0.f;
+        float mn = INFINITY, mx = -INFINITY;
+        for (int t = 0; t < G; ++t) {
+            uint16_t h = xs[t * KVQ_D + c];
+            float x = h2f(h);
+            a += abs_units(h);
+            s1 = __fadd_rn(s1, x);
+            s2 = __fadd_rn(s2, __fmul_rn(x, x));
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+        }
+        float mean = __fdiv_rn(s1, (float)G);
+        float var = __fsub_rn(__fdiv_rn(s2, (float)G), __fmul_rn(mean, mean));
+        si[c] = a;
+        sf[c] = var;
+        __syncthreads();
+        int rank = 0;
+        for (int o = 0; o < KVQ_D; ++o) {
+            bool better = score_mode == 0 ? (si[o] > a || (si[o] == a && o < c))
+                                          : (sf[o] > var || (sf[o] == var && o < c));
+            rank += better ? 1 : 0;
+        }
+        const int boosted = rank < K;
+        boost[c] = boosted;
+        __syncthreads();
+        int r = 0;
+        for (int o = 0; o < c; ++o) r += boost[o];
+        const int qmax = boosted ? 15 : 3;
+        uint16_t s, z;
+        affine_fit(mn, mx, qmax, s, z);
+        const float sv = h2f(s), zv = h2f(z);
+        uint8_t *pg = pages + p * page_bytes;
+        uint8_t *low = pg;
+        uint8_t *high = pg + KVQ_D * G / 4;
+        uint8_t *idx = high + (int64_t)K * G / 4;
+        uint16_t *ps = reinterpret_cast<uint16_t *>(idx + KVQ_D);
+        uint32_t lw[8], hw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { lw[i] = 0; hw[i] = 0; }
+        for (int t = 0; t < G; ++t) {
+            uint32_t code = (uint32_t)affine_code(h2f(xs[t * KVQ_D + c]), zv, sv, qmax);
+            const int sh = 2 * (t & 15);
+            lw[t >> 4] |= (code & 3u) << sh;
+            hw[t >> 4] |= ((code >> 2) & 3u) << sh;
+        }
+        uint4 *lrow = reinterpret_cast<uint4 *>(low + c * (G / 4));
+        lrow[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        lrow[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        if (boosted) {
+            uint4 *hrow = reinterpret_cast<uint4 *>(high + (int64_t)r * (G / 4));
+            hrow[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            hrow[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        }
+        idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
+        ps[c] = s;
+        ps[KVQ_D + c] = z;
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a8: INT8 subtractive dither.  One CTA of 256 threads per block of T tokens;
+// thread (warp w, lane l) owns channels 4l..4l+3 and tokens t = w (mod 8), so
+// one Philox4x32-10 call yields the four dithers of its four channels.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_int8_kernel(const uint16_t *__restrict__ x, int64_t n_blocks, int T,
+                                                         const int32_t *__restrict__ req,
+                                                         const int32_t *__restrict__ head,
+                                                         const int32_t *__restrict__ tok0, uint32_t ctr2_layer,
+                                                         uint32_t k0, uint32_t k1, int8_t *__restrict__ codes,
+                                                         uint16_t *__restrict__ scale) {
+    __shared__ float amax_part[8][KVQ_D];
+    __shared__ float s_sh[KVQ_D];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+        const uint16_t *xb = x + b * (int64_t)T * KVQ_D;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int t = w; t < T; t += 8) {
+            uint2 u = __ldg(reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D) + lane);
+            a0 = fmaxf(a0, fabsf(h2f(lo16(u.x))));
+            a1 = fmaxf(a1, fabsf(h2f(hi16(u.x))));
+            a2 = fmaxf(a2, fabsf(h2f(lo16(u.y))));
+            a3 = fmaxf(a3, fabsf(h2f(hi16(u.y))));
+        }
+        amax_part[w][4 * lane + 0] = a0;
+        amax_part[w][4 * lane + 1] = a1;
+        amax_part[w][4 * lane + 2] = a2;
+        amax_part[w][4 * lane + 3] = a3;
+        __syncthreads();
+        if (threadIdx.x < KVQ_D) {
+            float a = amax_part[0][threadIdx.x];
+#pragma unroll
+            for (int i = 1; i < 8; ++i) a = fmaxf(a, amax_part[i][threadIdx.x]);
+            uint16_t s = f2h_rn(__fdiv_rn(a, 126.5f));
+            scale[b * KVQ_D + threadIdx.x] = s;
+            s_sh[threadIdx.x] = h2f(s);
+        }
+        __syncthreads();
+        const float s0 = s_sh[4 * lane], s1 = s_sh[4 * lane + 1], s2 = s_sh[4 * lane + 2], s3 = s_sh[4 * lane + 3];
+        const uint32_t c2 = ctr2_layer | ((uint32_t)head[b] & 0xFFFFu);
+        const uint32_t c3 = (uint32_t)req[b];
+        const int32_t t0 = tok0[b];
+        for (int t = w; t < T; t += 8) {
+            uint4 r = philox4x32_10(make_uint4((uint32_t)(t0 + t), (uint32_t)lane, c2, c3), k0, k1);
+            uint2 u = __ldg(reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D) + lane);
+            float xs[4] = {h2f(lo16(u.x)), h2f(hi16(u.x)), h2f(lo16(u.y)), h2f(hi16(u.y))};
+            float ss[4] = {s0, s1, s2, s3};
+            uint32_t wr[4] = {r.x, r.y, r.z, r.w};
+            uint32_t packed = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                int code = 0;
+                if (ss[i] != 0.0f) {
+                    float xi = dither_from_word(wr[i]);
+                    float v = __fadd_rn(__fdiv_rn(xs[i], ss[i]), xi);
+                    code = (int)fminf(fmaxf(rintf(v), -127.f), 127.f);
+                }
+                packed |= ((uint32_t)(code & 0xFF)) << (8 * i);
+            }
+            reinterpret_cast<uint32_t *>(codes + (b * (int64_t)T + t) * KVQ_D)[lane] = packed;
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void philox_kernel(const uint32_t *__restrict__ ctr, const uint32_t *__restrict__ key, int64_t n,
+                              uint32_t *__restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        uint4 c = make_uint4(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3]);
+        uint4 r = philox4x32_10(c, key[2 * i], key[2 * i + 1]);
+        out[4 * i] = r.x; out[4 * i + 1] = r.y; out[4 * i + 2] = r.z; out[4 * i + 3] = r.w;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+static int grid_cap(int64_t want, int per_sm) {
+    int64_t cap = (int64_t)num_sms() * per_sm;
+    return (int)(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t n_groups, void *codes, void *sz,
+                                  cudaStream_t st) {
+    if (n_groups == 0) return cudaSuccess;
+    const uint16_t *kp = static_cast<const uint16_t *>(k);
+    uint8_t *cp = static_cast<uint8_t *>(codes);
+    uint32_t *zp = static_cast<uint32_t *>(sz);
+    // one CTA per group; grids above 2^31-1 groups are split into launches
+    for (int64_t g0 = 0; g0 < n_groups; g0 += 0x7FFFFFFF) {
+        int64_t n = n_groups - g0 < 0x7FFFFFFF ? n_groups - g0 : 0x7FFFFFFF;
+        const int G = cfg->group_k;
+        const uint16_t *ks = kp + g0 * (int64_t)G * KVQ_D;
+        uint8_t *cs = cp + g0 * (int64_t)G * KVQ_D / 4;
+        uint32_t *zs = zp + g0 * KVQ_D;
+        if (G == 32) quant_key_kivi_kernel<1><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
+        else if (G == 64) quant_key_kivi_kernel<2><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
+        else quant_key_kivi_kernel<4><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_value_kivi(const kvq_config *cfg, const void *v, int64_t n_tokens, void *codes, void *sz,
+                                    cudaStream_t st) {
+    if (n_tokens == 0) return cudaSuccess;
+    const int grid = grid_cap((n_tokens + 7) / 8, 16);
+    const uint16_t *vp = static_cast<const uint16_t *>(v);
+    uint8_t *cp = static_cast<uint8_t *>(codes);
+    uint32_t *zp = static_cast<uint32_t *>(sz);
+    switch (cfg->group_v) {
+        case 32: quant_value_kernel<32, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0); break;
+        case 64: quant_value_kernel<64, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0); break;
+        default: quant_value_kernel<128, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_value_kitty(const kvq_config *cfg, const void *v, int64_t n_pages, void *pages,
+                                     cudaStream_t st) {
+    if (n_pages == 0) return cudaSuccess;
+    const int G = cfg->group_k;
+    const int64_t n_tokens = n_pages * G;
+    const int grid = grid_cap((n_tokens + 7) / 8, 16);
+    const int64_t pb = (int64_t)G * KVQ_D / 4 + 4LL * G;
+    quant_value_kernel<128, true><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens,
+                                                        static_cast<uint8_t *>(pages), nullptr, G, pb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t n_pages, int score_mode,
+                                   void *pages, cudaStream_t st) {
+    if (n_pages == 0) return cudaSuccess;
+    const int G = cfg->group_k, K = cfg->boost_k;
+    const int64_t pb = (int64_t)KVQ_D * G / 4 + (int64_t)K * G / 4 + KVQ_D + 4LL * KVQ_D;
+    const size_t smem = (size_t)G * KVQ_D * 2 + KVQ_D * (8 + 4 + 4);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(quant_key_kitty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int grid = grid_cap(n_pages, 4);
+    quant_key_kitty_kernel<<<grid, 128, smem, st>>>(static_cast<const uint16_t *>(k), n_pages, K, score_mode,
+                                                    static_cast<uint8_t *>(pages), pb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_int8(const kvq_config *cfg, const void *x, int64_t n_blocks, const int32_t *req,
+                              const int32_t *head, const int32_t *tok0, int layer, int kv_sel, uint64_t seed,
+                              void *codes, void *scale, cudaStream_t st) {
+    if (n_blocks == 0) return cudaSuccess;
+    const uint32_t c2 = ((uint32_t)layer << 17) | ((uint32_t)(kv_sel & 1) << 16);
+    const int grid = grid_cap(n_blocks, 8);
+    quant_int8_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(x), n_blocks, cfg->int8_block, req, head,
+                                            tok0, c2, (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32),
+                                            static_cast<int8_t *>(codes), static_cast<uint16_t *>(scale));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_philox(const uint32_t *ctr, const uint32_t *key, int64_t n, uint32_t *out, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int grid = grid_cap((n + 255) / 256, 8);
+    philox_kernel<<<grid, 256, 0, st>>>(ctr, key, n, out);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

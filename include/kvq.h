@@ -1,0 +1,274 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) low-bit KV-cache library.
+ *
+ * Write side: asymmetric min-max quantization of the KV cache
+ *   - KIVI keys per channel over groups of G tokens and values per token over
+ *     groups of Gv channels, 2-bit codes with fp16 (scale, zero)
+ *     (KIVI, zenmind.me summary, section 3.3 and section 4 steps 2-3;
+ *      the affine formula of Kitty, Observation 1);
+ *   - Kitty pages: top-K channel precision boost (Eq. 2 score), 4-bit boosted
+ *     key channels stored as two dense 2-bit planes plus a boost index, 2-bit
+ *     per-token value pages (Kitty summary, "The Channel-Wise Precision Boost
+ *     Mechanism", "Page-Centric Memory Layout and Dense-Sparse Decomposition");
+ *   - WitCert INT8 with subtractive Philox4x32-10 dither and per-256-token,
+ *     per-channel fp16 scales amax/126.5 (WitCert, arxiv 2607.28699, sec. 6).
+ * Read side: split-KV flash-decoding attention that dequantizes codes in
+ * registers, concatenates the fp16 residual / sink / buffer segments, and
+ * merges the splits by log-sum-exp (WitCert sec. 6.2.2 two-stage structure;
+ * KIVI Eq. 3; Kitty "Lightweight Attention Execution Pipeline").
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned (KVQ_ERR_MISALIGNED otherwise).  The library allocates no
+ *     memory, never synchronizes the host, and enqueues its kernels on the
+ *     given stream (0 = legacy default stream).  Calls are graph-capturable.
+ *   - Argument errors are detected on the host before anything is launched;
+ *     nothing is launched when a call returns an error.  Launch failures
+ *     return KVQ_ERR_CUDA.  No device code traps or asserts; a bounded wait
+ *     that expires inside a kernel records KVQ_DEVICE_ERR_* in a device flag
+ *     that kvq_get_device_error() reads.
+ *   - fp16 = IEEE binary16 stored as uint16; "fp16x2 (s, z)" = a pair of
+ *     fp16 values, scale first.
+ *   - head_dim must be 128 (KVQ_ERR_UNSUPPORTED otherwise).
+ *
+ * Byte layouts (D = 128):
+ *   KIVI key group (G tokens, G % 32 == 0): G*D/4 bytes made of G/32 tiles of
+ *     1024 bytes.  Token t, channel c of the group has its 2-bit code in bits
+ *     2*(t%4) of the byte at
+ *       (t/32)*1024 + ((c>>4)&1)*512 + (4*((t%32)/4) + (c>>5))*16
+ *       + ((c>>2)&3)*4 + (c&3)
+ *     so that lane 4q+j of a warp finds tokens 4q..4q+3 of channels
+ *     32j..32j+31 in the 16-byte chunks lane and lane+32 of each tile.
+ *     Parameters: fp16x2 (s, z) [D] per group.
+ *   KIVI value token: D/4 bytes, channel c in bits 2*(c%4) of byte c/4.
+ *     Parameters: fp16x2 (s, z) [D/Gv] per token.
+ *   Kitty key page (G = 128 tokens, K boosted channels), one record of
+ *     kvq_kitty_key_page_bytes() bytes: low plane [D][G/4] (byte (c, t/4),
+ *     bits 2*(t%4), code & 3), high plane [K][G/4] (row r = r-th boosted
+ *     channel in ascending channel order, code >> 2), idx uint8 [D] (r, or
+ *     K+1 for channels that are not boosted), s fp16 [D], z fp16 [D].
+ *   Kitty value page: codes [G][D/4] token-major as above, s fp16 [G],
+ *     z fp16 [G].
+ *   INT8 cache: codes int8 [tokens][D]; scale fp16 [blocks][D].
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent config */
+    KVQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, bits != 2, ...) */
+    KVQ_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    KVQ_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+    KVQ_ERR_WORKSPACE = 5      /* workspace smaller than kv_decode_attn_plan() asked for */
+} kvq_status;
+
+/* device error flags (bitmask) written by kernels instead of trapping */
+#define KVQ_DEVICE_ERR_WAIT_TIMEOUT 1u
+
+typedef enum { KVQ_VARIANT_KIVI = 0, KVQ_VARIANT_KITTY = 1, KVQ_VARIANT_INT8 = 2 } kvq_variant;
+
+typedef struct {
+    int32_t head_dim;     /* D; 128 */
+    int32_t n_q_heads;    /* Hq */
+    int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0 */
+    int32_t bits_k;       /* KIVI key bits: 2 */
+    int32_t bits_v;       /* KIVI / Kitty value bits: 2 */
+    int32_t group_k;      /* G: tokens per KIVI key group (32, 64, 128) or Kitty page (128) */
+    int32_t group_v;      /* Gv: channels per KIVI value group (32 or 128) */
+    int32_t residual;     /* R: KIVI fp16 residual (R % G == 0), Kitty value local window */
+    int32_t sink;         /* S: Kitty fp16 sink tokens */
+    int32_t boost_k;      /* K: Kitty boosted key channels, 0..head_dim */
+    int32_t int8_block;   /* INT8 dither block length in tokens: 256 */
+    float sm_scale;       /* softmax scale; 0 means 1/sqrt(head_dim) */
+} kvq_config;
+
+/* --------------------------------------------------------------------- */
+/* Write side                                                              */
+/* --------------------------------------------------------------------- */
+
+/* a1: quantize n_groups KIVI key groups.
+ *   k       fp16 [n_groups][G][D], token-major (as the K projection emits it)
+ *   codes   uint8 [n_groups][G*D/4]  (tile layout above)
+ *   sz      fp16x2 [n_groups][D]
+ * Per channel over the group's G tokens: z = fp16 round-down(min),
+ * s = fp16 round-up(fp32 (max - z) / 3), raised by one fp16 step while
+ * z + 3s < max; code = clamp(rint((x - z) / s), 0, 3) in fp32 with the
+ * stored fp16 s, z; s = 0 (all codes 0) when max == min.
+ * (KIVI section 3.3 key split; Kitty Observation 1 formula.)
+ * n_groups == 0 launches nothing and returns KVQ_OK. */
+KVQ_API kvq_status kv_quant_key(const kvq_config *cfg, const void *k, int64_t n_groups,
+                        void *codes, void *sz, cudaStream_t stream);
+
+/* a2: quantize n_tokens KIVI values, per token over groups of Gv channels.
+ *   v       fp16 [n_tokens][D]
+ *   codes   uint8 [n_tokens][D/4] (token-major)
+ *   sz      fp16x2 [n_tokens][D/Gv]
+ * Same rounding rules as kv_quant_key.  (KIVI section 3.3 value split.) */
+KVQ_API kvq_status kv_quant_value(const kvq_config *cfg, const void *v, int64_t n_tokens,
+                          void *codes, void *sz, cudaStream_t stream);
+
+/* a5: quantize n_pages Kitty key pages (G = cfg->group_k = 128 tokens).
+ *   k          fp16 [n_pages][G][D]
+ *   score_mode 0: Eq. 2 score sum_t |x| (exact integer sum in units of 2^-24);
+ *              1: population variance over the page from sequential fp32
+ *                 sums in token order (sum x^2 / G - (sum x / G)^2)
+ *   pages      [n_pages] records of kvq_kitty_key_page_bytes(cfg) bytes
+ * The K = cfg->boost_k channels with the largest score (ties to the lower
+ * channel) get 4-bit codes, the rest 2-bit; each channel has its own (s, z)
+ * with the rounding rules of kv_quant_key and 2^b - 1 = 15 or 3.
+ * (Kitty Eq. 2, "Selecting the Top-K Channels", "The Decomposition".) */
+KVQ_API kvq_status kv_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t n_pages,
+                              int32_t score_mode, void *pages, cudaStream_t stream);
+
+/* a6: quantize n_pages Kitty value pages: per token over all D channels,
+ * 2-bit.  v fp16 [n_pages][G][D]; pages [n_pages] records of
+ * kvq_kitty_value_page_bytes(cfg) bytes.  (Kitty "Value Cache Quantization".) */
+KVQ_API kvq_status kv_quant_value_kitty(const kvq_config *cfg, const void *v, int64_t n_pages,
+                                void *pages, cudaStream_t stream);
+
+/* a8: INT8 subtractive-dither quantization of n_blocks blocks of
+ * T = cfg->int8_block (256) tokens.
+ *   x        fp16 [n_blocks][T][D]
+ *   req_id, kv_head, tok0   int32 [n_blocks] (device): request id, kv head
+ *            and absolute position of the block's first token
+ *   layer    layer index (0 .. 2^15-1), kv_sel 0 for keys, 1 for values
+ *   seed     64-bit Philox key
+ *   codes    int8 [n_blocks][T][D];  scale fp16 [n_blocks][D]
+ * s_c = fp16 round-to-nearest(fp32 amax_c / 126.5); xi = Philox4x32-10 word
+ * (c % 4) of counter (token, c / 4, layer << 17 | kv_sel << 16 | kv_head,
+ * request) under key (seed lo, seed hi), xi = (word >> 8) * 2^-24 - 1/2;
+ * code = clamp(rint(x / s + xi), -127, 127) in fp32 with the stored fp16 s;
+ * s = 0 gives code 0.  (WitCert sec. 6.1 write kernel.) */
+KVQ_API kvq_status kv_quant_int8_dither(const kvq_config *cfg, const void *x, int64_t n_blocks,
+                                const int32_t *req_id, const int32_t *kv_head, const int32_t *tok0,
+                                int32_t layer, int32_t kv_sel, uint64_t seed,
+                                void *codes, void *scale, cudaStream_t stream);
+
+/* Record sizes of the Kitty pages for this config (0 on invalid config). */
+KVQ_API size_t kvq_kitty_key_page_bytes(const kvq_config *cfg);
+KVQ_API size_t kvq_kitty_value_page_bytes(const kvq_config *cfg);
+
+/* --------------------------------------------------------------------- */
+/* Read side: caches at attention time                                     */
+/* --------------------------------------------------------------------- */
+/* seq_len[b] = L_b = tokens in the cache of batch row b INCLUDING the
+ * current token (its k, v are inserted before attention; quantization of a
+ * full group happens after attention, the Kitty step order).  Every array
+ * below is dense [batch][n_kv_heads][capacity][...] with the capacity
+ * derived from max_seq_len, and 1 <= seq_len[b] <= max_seq_len. */
+
+/* KIVI: the key residual holds r_K = ((L-1) mod R) + 1 tokens and the first
+ * L - r_K keys are quantized in whole groups; the value residual holds
+ * min(L, R) tokens and the first L - min(L, R) values are quantized.
+ * Residual token t is stored at slot t % R.  (KIVI section 3.3, Eq. 3.) */
+typedef struct {
+    int32_t batch;
+    int32_t max_seq_len;
+    const int32_t *seq_len;  /* [B] */
+    const void *k_codes;     /* uint8  [B][Hkv][ceil(max_seq_len/G)][G*D/4] */
+    const void *k_sz;        /* fp16x2 [B][Hkv][ceil(max_seq_len/G)][D] */
+    const void *v_codes;     /* uint8  [B][Hkv][max_seq_len][D/4] */
+    const void *v_sz;        /* fp16x2 [B][Hkv][max_seq_len][D/Gv] */
+    const void *k_res;       /* fp16   [B][Hkv][R][D] */
+    const void *v_res;       /* fp16   [B][Hkv][R][D] */
+} kvq_kivi_cache;
+
+/* Kitty: sink tokens [0, min(L,S)) fp16; key pages, then a key Q-buffer of
+ * n_kb = ((L-S-1) mod G) + 1 tokens (slot (t-S) % G); value pages, a value
+ * Q-buffer of n_vb = ((E-1) mod G) + 1 tokens with E = L-S-R > 0 (slot
+ * (t-S) % G), then a local window of the last min(L-S, R) tokens (slot
+ * t % R).  (Kitty "Stage 1: Inserting New KV Vectors", "Stage 3".) */
+typedef struct {
+    int32_t batch;
+    int32_t max_seq_len;
+    const int32_t *seq_len;  /* [B] */
+    const void *k_pages;     /* [B][Hkv][P][key page record], P = ceil(max(max_seq_len-S,0)/G) */
+    const void *v_pages;     /* [B][Hkv][P][value page record] */
+    const void *k_sink;      /* fp16 [B][Hkv][S][D] */
+    const void *v_sink;      /* fp16 [B][Hkv][S][D] */
+    const void *k_qbuf;      /* fp16 [B][Hkv][G][D] */
+    const void *v_qbuf;      /* fp16 [B][Hkv][G][D] */
+    const void *v_local;     /* fp16 [B][Hkv][R][D] */
+} kvq_kitty_cache;
+
+/* INT8 dither: the first L - n_tail tokens are quantized in blocks of T,
+ * n_tail = ((L-1) mod T) + 1 tokens of the active block stay fp16 (slot
+ * t % T).  Dither is regenerated from (req_id[b], layer, kv head, token,
+ * channel).  (WitCert sec. 6.1 read kernel; "active block" tail.) */
+typedef struct {
+    int32_t batch;
+    int32_t max_seq_len;
+    const int32_t *seq_len;  /* [B] */
+    const int32_t *req_id;   /* [B] */
+    int32_t layer;
+    uint64_t seed;
+    const void *k_codes;     /* int8 [B][Hkv][max_seq_len][D] */
+    const void *v_codes;     /* int8 [B][Hkv][max_seq_len][D] */
+    const void *k_scale;     /* fp16 [B][Hkv][ceil(max_seq_len/T)][D] */
+    const void *v_scale;     /* fp16 [B][Hkv][ceil(max_seq_len/T)][D] */
+    const void *k_tail;      /* fp16 [B][Hkv][T][D] */
+    const void *v_tail;      /* fp16 [B][Hkv][T][D] */
+} kvq_int8_cache;
+
+/* Split-KV plan: number of splits per (batch row, query head) and the
+ * workspace bytes the decode calls need for this config, variant, batch and
+ * max_seq_len.  Deterministic: the decode calls recompute the same plan. */
+KVQ_API kvq_status kv_decode_attn_plan(const kvq_config *cfg, int32_t variant, int32_t batch,
+                               int32_t max_seq_len, int32_t *n_splits, size_t *workspace_bytes);
+
+/* a3 + a4: out fp16 [B][Hq][D] = softmax(sm_scale q K^T) V over every cached
+ * token, q fp16 [B][Hq][D]; query head h reads kv head h / (Hq / Hkv).
+ * Stage 1 writes per-split (o_s = acc / l, lse_s) into the workspace
+ * (fp32, caller-owned, at least the planned size); stage 2 merges
+ * o = sum_s exp(lse_s - LSE) o_s with LSE = log sum_s exp(lse_s). */
+KVQ_API kvq_status kv_decode_attn(const kvq_config *cfg, const kvq_kivi_cache *cache, const void *q,
+                          void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+KVQ_API kvq_status kv_decode_attn_kitty(const kvq_config *cfg, const kvq_kitty_cache *cache, const void *q,
+                                void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+KVQ_API kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_cache *cache, const void *q,
+                               void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The two stages separately (kv_decode_attn* = stage1 then merge). */
+KVQ_API kvq_status kv_decode_attn_stage1(const kvq_config *cfg, int32_t variant, const void *cache,
+                                 const void *q, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+KVQ_API kvq_status kv_decode_attn_merge(const kvq_config *cfg, int32_t variant, int32_t batch,
+                                int32_t max_seq_len, const void *workspace, size_t workspace_bytes,
+                                void *out, cudaStream_t stream);
+
+/* --------------------------------------------------------------------- */
+/* Diagnostics                                                             */
+/* --------------------------------------------------------------------- */
+
+/* The library's Philox4x32-10 on the GPU: out[i][0..3] = Philox4x32-10 of
+ * counter ctr[i][0..3] under key (key[i][0], key[i][1]); uint32 device
+ * arrays.  (Salmon et al., SC'11.) */
+KVQ_API kvq_status kvq_philox4x32_10(const uint32_t *ctr, const uint32_t *key, int64_t n,
+                             uint32_t *out, cudaStream_t stream);
+
+/* Reads and clears the device error bitmask of the current device
+ * (synchronous; not for use inside a stream capture). */
+KVQ_API kvq_status kvq_get_device_error(uint32_t *flags);
+
+KVQ_API const char *kvq_status_string(kvq_status s);
+KVQ_API const char *kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

@@ -1,0 +1,104 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def K():
+    from bit_kv_cache_keyquant_gb300 import build
+    build.build()
+    from bit_kv_cache_keyquant_gb300 import kvq
+    return kvq
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:KVQ_API\s+)?(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n.startswith(("kv_", "kvq_"))))
+
+
+def test_header_symbols_exported(K):
+    names = declared_functions()
+    assert len(names) >= 17
+    lib = ctypes.CDLL(K.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(K.EXPORTED) == names
+
+
+def test_oracle_and_library_share_no_code():
+    """Neither side imports or includes the other (inputs.py holds no method arithmetic)."""
+    pkg = os.path.join(ROOT, "bit_kv_cache_keyquant_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            src = open(os.path.join(dirpath, f), errors="ignore").read() if f.endswith((".py", ".cu", ".cuh", ".h")) else ""
+            assert not re.search(r"^\s*(from\s+oracle|import\s+oracle)", src, flags=re.M), f
+            assert not re.search(r'#include\s+[<"].*oracle', src), f
+    for f in ("oracle.py", "kvq_oracle.c"):
+        src = open(os.path.join(ROOT, "oracle", f)).read()
+        assert not re.search(r"^\s*(from|import)\s+bit_kv_cache_keyquant_gb300", src, flags=re.M), f
+        assert "#include \"../" not in src and "kvq.h" not in src.replace("kvq.h)", ""), f
+
+
+def test_status_strings(K):
+    assert K.status_string(0) == "ok"
+    assert "aligned" in K.status_string(3)
+    assert K.version().startswith("kvq")
+
+
+def _call_quant_key(K, cfg, k=16, codes=16, sz=16, n=1):
+    return K.raw_call("kv_quant_key", ctypes.byref(cfg), k, n, codes, sz, None)
+
+
+def test_validation_without_gpu(K):
+    good = K.make_config()
+    bad_d = K.make_config(head_dim=64)
+    assert _call_quant_key(K, bad_d) == K.KVQ_ERR_UNSUPPORTED
+    assert _call_quant_key(K, K.make_config(bits_k=4)) == K.KVQ_ERR_UNSUPPORTED
+    assert _call_quant_key(K, K.make_config(residual=100)) == K.KVQ_ERR_UNSUPPORTED     # R % G != 0
+    assert _call_quant_key(K, K.make_config(n_q_heads=30, n_kv_heads=8)) == K.KVQ_ERR_INVALID_ARG
+    assert _call_quant_key(K, good, k=None) == K.KVQ_ERR_INVALID_ARG
+    assert _call_quant_key(K, good, codes=0x1001) == K.KVQ_ERR_MISALIGNED
+    assert _call_quant_key(K, good, n=-1) == K.KVQ_ERR_INVALID_ARG
+    assert _call_quant_key(K, good, k=None, n=0) == K.KVQ_OK        # nothing to do, nothing launched
+    assert K.raw_call("kv_quant_key", None, 16, 1, 16, 16, None) == K.KVQ_ERR_INVALID_ARG
+    kitty = K.make_config(group_k=128, n_q_heads=32, n_kv_heads=8)
+    assert K.kvq_kitty_key_page_bytes(kitty) == 5248
+    assert K.kvq_kitty_value_page_bytes(kitty) == 4608
+    assert K.raw_call("kv_quant_key_kitty", ctypes.byref(kitty), 16, 1, 2, 16, None) == K.KVQ_ERR_INVALID_ARG
+    i8 = K.make_config(int8_block=200)
+    assert K.raw_call("kv_quant_int8_dither", ctypes.byref(i8), 16, 1, 16, 16, 16, 0, 0, 0, 16, 16,
+                      None) == K.KVQ_ERR_UNSUPPORTED
+
+
+def test_decode_plan_and_workspace_checks(K):
+    cfg = K.make_config()
+    n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, 32, 4096)
+    assert n >= 1 and wsb >= 32 * 32 * n * 129 * 4
+    n2, _ = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, 1, 131072)
+    assert n2 <= 256
+    cache = K.kvq_kivi_cache(32, 4096, 16, 16, 16, 16, 16, 16, 16)
+    st = K.raw_call("kv_decode_attn", ctypes.byref(cfg), ctypes.byref(cache), 16, 16, 16, wsb - 1, None)
+    assert st == K.KVQ_ERR_WORKSPACE
+    st = K.raw_call("kv_decode_attn", ctypes.byref(cfg), ctypes.byref(cache), 16, 16, 0x1008, wsb, None)
+    assert st == K.KVQ_ERR_MISALIGNED
+    cache.k_sz = None
+    st = K.raw_call("kv_decode_attn", ctypes.byref(cfg), ctypes.byref(cache), 16, 16, 16, wsb, None)
+    assert st == K.KVQ_ERR_INVALID_ARG
+    assert K.raw_call("kv_decode_attn_stage1", ctypes.byref(cfg), 7, ctypes.byref(cache), 16, 16, wsb,
+                      None) == K.KVQ_ERR_INVALID_ARG
+
+
+def test_segment_rules_agree_with_oracle(orc):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    for L in list(range(1, 700, 7)) + [4096, 32768, 131072]:
+        assert C.kivi_segments(L, 128) == orc.kivi_segments(L, 128)
+        assert C.kitty_segments(L, 128, 32, 128) == orc.kitty_segments(L, 128, 32, 128)

@@ -1,0 +1,243 @@
+"""GPU parity of the KIVI path and of Philox, through the C ABI.
+
+Quantization (codes, (s, z)) must match the oracle bit for bit; attention
+outputs within max-abs 2e-3 of the oracle's binary64 result (fp16 out,
+fp32 accumulate).
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_keyquant_gb300 import inputs as I
+from tests.gpu_util import curand_philox, lib, max_abs
+
+pytestmark = pytest.mark.gpu
+ATOL = 2e-3
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def K():
+    return lib()
+
+
+def _rand_fp16(rng, shape, kind):
+    if kind == "normal":
+        x = rng.standard_normal(shape)
+    elif kind == "outlier":
+        x = rng.standard_normal(shape)
+        x[..., 7] *= 40.0
+    elif kind == "wide":
+        x = rng.standard_normal(shape) * 10.0 ** rng.uniform(-6, 4, shape[-1])
+    elif kind == "tiny":
+        x = rng.standard_normal(shape) * 1e-6          # fp16 subnormals
+    elif kind == "const":
+        x = np.ones(shape) * 0.3
+    else:
+        raise ValueError(kind)
+    return x.astype(np.float16)
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+@pytest.mark.parametrize("kind", ["normal", "outlier", "wide", "tiny", "const"])
+def test_quant_key_bitexact(K, orc, G, kind):
+    rng = np.random.default_rng(100 + G)
+    n = 37
+    x = _rand_fp16(rng, (n, G, 128), kind)
+    if kind == "normal":
+        x[3, :, 11] = x[3, 0, 11]                    # a constant channel inside a group
+        x[5, 2, 4] = np.float16(65504.0)
+        x[5, 9, 4] = np.float16(-65504.0)            # widest fp16 range
+    cfg = K.make_config(group_k=G, residual=128)
+    xd = torch.from_numpy(x).to(DEV)
+    codes = torch.full((n, G * 32), 0xAB, dtype=torch.uint8, device=DEV)
+    sz = torch.full((n, 128), -1, dtype=torch.int32, device=DEV)
+    K.kv_quant_key(cfg, xd, n, codes, sz)
+    torch.cuda.synchronize()
+    ref_codes, ref_sz = orc.kivi_quant_key(x)
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, 128, 2), ref_sz)
+
+
+@pytest.mark.parametrize("Gv", [32, 64, 128])
+@pytest.mark.parametrize("kind", ["normal", "outlier", "wide", "tiny", "const"])
+def test_quant_value_bitexact(K, orc, Gv, kind):
+    rng = np.random.default_rng(200 + Gv)
+    n = 333
+    x = _rand_fp16(rng, (n, 128), kind)
+    cfg = K.make_config(group_v=Gv)
+    xd = torch.from_numpy(x).to(DEV)
+    codes = torch.full((n, 32), 0xAB, dtype=torch.uint8, device=DEV)
+    sz = torch.full((n, 128 // Gv), -1, dtype=torch.int32, device=DEV)
+    K.kv_quant_value(cfg, xd, n, codes, sz)
+    torch.cuda.synchronize()
+    ref_codes, ref_sz = orc.kivi_quant_value(x, Gv)
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, 128 // Gv, 2), ref_sz)
+
+
+def _run_decode(K, cfg, Ks, Vs, q, max_seq_len):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hkv = len(Ks), len(Ks[0])
+    cache = C.KiviCache(cfg, B, max_seq_len, device=DEV)
+    for b in range(B):
+        for h in range(Hkv):
+            cache.fill(b, h, torch.from_numpy(Ks[b][h]).to(DEV), torch.from_numpy(Vs[b][h]).to(DEV))
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, B, max_seq_len)
+    ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device=DEV)            # poisoned workspace
+    out = torch.full((B, cfg.n_q_heads, 128), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn(cfg, cache.desc(), torch.from_numpy(q).to(DEV), out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    return out.float().cpu().numpy()
+
+
+def _oracle_decode(orc, cfg, Ks, Vs, q):
+    g = cfg.n_q_heads // cfg.n_kv_heads
+    B, Hkv = len(Ks), len(Ks[0])
+    out = np.zeros((B, cfg.n_q_heads, 128))
+    for b in range(B):
+        for h in range(Hkv):
+            L = Ks[b][h].shape[0]
+            parts = orc.kivi_build_one(Ks[b][h], Vs[b][h], cfg.group_k, cfg.group_v, cfg.residual)
+            out[b, h * g:(h + 1) * g] = orc.kivi_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L, G=cfg.group_k,
+                                                            Gv=cfg.group_v, R=cfg.residual)
+    return out
+
+
+@pytest.mark.parametrize("shape", [
+    # (B, Hq, Hkv, lengths, G, Gv, R)
+    (3, 2, 2, [1, 33, 129], 32, 32, 128),
+    (2, 4, 1, [300, 1000], 32, 32, 128),
+    (2, 8, 2, [511, 512], 32, 32, 128),
+    (2, 2, 2, [640, 1537], 64, 32, 128),
+    (1, 2, 1, [2000], 128, 128, 128),
+    (2, 2, 2, [700, 900], 32, 64, 64),
+    (1, 1, 1, [128], 32, 32, 128),
+    (1, 1, 1, [4095], 32, 32, 256),
+])
+def test_decode_parity_small(K, orc, shape):
+    B, Hq, Hkv, lens, G, Gv, R = shape
+    rng = np.random.default_rng(sum(lens) + Hq)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv, group_k=G, group_v=Gv, residual=R)
+    Ks = [[(rng.standard_normal((lens[b], 128)) * (1 + 9 * (rng.random(128) < 0.03))).astype(np.float16)
+           for _ in range(Hkv)] for b in range(B)]
+    Vs = [[rng.standard_normal((lens[b], 128)).astype(np.float16) for _ in range(Hkv)] for b in range(B)]
+    q = rng.standard_normal((B, Hq, 128)).astype(np.float16)
+    got = _run_decode(K, cfg, Ks, Vs, q, max(lens) + 5)
+    want = _oracle_decode(orc, cfg, Ks, Vs, q)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_decode_capacity_and_split_invariance(K, orc):
+    """The same cache content under a larger capacity (more splits) gives the same result."""
+    rng = np.random.default_rng(7)
+    cfg = K.make_config(n_q_heads=4, n_kv_heads=2)
+    lens = [1500, 700]
+    Ks = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(2)] for L in lens]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(2)] for L in lens]
+    q = rng.standard_normal((2, 4, 128)).astype(np.float16)
+    a = _run_decode(K, cfg, Ks, Vs, q, 1500)
+    b = _run_decode(K, cfg, Ks, Vs, q, 9000)
+    assert max_abs(a, b) <= 1e-3
+    assert max_abs(a, _oracle_decode(orc, cfg, Ks, Vs, q)) <= ATOL
+
+
+def test_decode_residual_only_matches_sdpa(K):
+    """L <= R: nothing is quantized, the kernel is plain attention (torch SDPA, fp32)."""
+    rng = np.random.default_rng(8)
+    cfg = K.make_config(n_q_heads=8, n_kv_heads=2)
+    L = 100
+    Ks = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(2)]]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(2)]]
+    q = rng.standard_normal((1, 8, 128)).astype(np.float16)
+    got = _run_decode(K, cfg, Ks, Vs, q, 256)
+    kt = torch.from_numpy(np.stack(Ks[0])).float().repeat_interleave(4, 0)[None]
+    vt = torch.from_numpy(np.stack(Vs[0])).float().repeat_interleave(4, 0)[None]
+    qt = torch.from_numpy(q).float()[:, :, None, :]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, :, 0].numpy()
+    assert max_abs(got, ref) <= ATOL
+
+
+def test_workload1_tiny_full(K, orc):
+    """Tiny K2V2 workload: B=1, 4 MHA heads, 512 tokens, 4 key channels x20; every output."""
+    w = I.WORKLOADS[1]
+    cfg = K.make_config(n_q_heads=4, n_kv_heads=4)
+    Ks = [[I.gen_kv_np(w, I.T_K, 0, h, w.seq_len) for h in range(4)]]
+    Vs = [[I.gen_kv_np(w, I.T_V, 0, h, w.seq_len) for h in range(4)]]
+    q = I.gen_q_np(w)
+    got = _run_decode(K, cfg, Ks, Vs, q, w.seq_len)
+    assert max_abs(got, _oracle_decode(orc, cfg, Ks, Vs, q)) <= ATOL
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("widx", [2, 3])
+def test_workload_full_size_sampled(K, orc, widx):
+    """Full Llama-2-7B / Llama-3-8B shapes, the launch bench.py times; sampled (b, h) rows vs the oracle."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    w = I.WORKLOADS[widx]
+    cfg = K.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
+    L = w.seq_len
+    cache = C.KiviCache(cfg, w.batch, L, device=DEV)
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            cache.fill(b, h, I.gen_kv_torch(w, I.T_K, b, h, L, DEV), I.gen_kv_torch(w, I.T_V, b, h, L, DEV))
+    q = I.gen_q_torch(w, DEV)
+    n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, w.batch, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    assert np.isfinite(outn).all()
+    qn = q.cpu().numpy()
+    g = w.n_q_heads // w.n_kv_heads
+    rng = np.random.default_rng(widx)
+    for b, h in {(0, 0), (w.batch - 1, w.n_kv_heads - 1), *[(int(rng.integers(w.batch)), int(rng.integers(w.n_kv_heads))) for _ in range(3)]}:
+        parts = orc.kivi_build_one(I.gen_kv_np(w, I.T_K, b, h, L), I.gen_kv_np(w, I.T_V, b, h, L))
+        want = orc.kivi_decode_one(qn[b, h * g:(h + 1) * g], *parts, L=L)
+        assert max_abs(outn[b, h * g:(h + 1) * g], want) <= ATOL, (b, h)
+    # quantized codes of a sampled group are bit-exact at full size too
+    kc, ksz = orc.kivi_quant_key(I.gen_kv_np(w, I.T_K, 1, 0, 64)[None, :32])
+    assert np.array_equal(cache.k_codes[1, 0, 0].cpu().numpy(), kc[0])
+
+
+# ---------------------------------------------------------------------------
+# Philox
+# ---------------------------------------------------------------------------
+def _philox_cases():
+    rng = np.random.default_rng(5)
+    ctr = [[0, 0, 0, 0], [0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF], [0x80000000, 0, 0xFFFFFFFF, 1],
+           [12345, 3, 0x00020007, 99]]
+    key = [[0, 0], [0xFFFFFFFF, 0xFFFFFFFF], [0xDEADBEEF, 0x80000000], [1, 2]]
+    ctr += rng.integers(0, 2 ** 32, (60, 4), dtype=np.uint64).tolist()
+    key += rng.integers(0, 2 ** 32, (60, 2), dtype=np.uint64).tolist()
+    return np.array(ctr, np.uint32), np.array(key, np.uint32)
+
+
+def test_philox_matches_oracle(K, orc):
+    ctr, key = _philox_cases()
+    n = len(ctr)
+    out = torch.zeros((n, 4), dtype=torch.int32, device=DEV)
+    K.kvq_philox4x32_10(torch.from_numpy(ctr.view(np.int32)).to(DEV), torch.from_numpy(key.view(np.int32)).to(DEV), n,
+                        out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    for i in range(n):
+        assert np.array_equal(got[i], orc.philox(ctr[i], key[i])), i
+
+
+def test_philox_oracle_matches_curand(orc):
+    """Independent known answers: cuRAND's Philox4x32-10 at the same raw counter and key."""
+    ctr, key = _philox_cases()
+    ctr[:, 1] &= 0x3FFFFFFF                # curand_init's offset = 4 * (ctr0 | ctr1 << 32) must fit 64 bits
+    n = len(ctr)
+    c = torch.from_numpy(ctr.view(np.int32)).to(DEV)
+    k = torch.from_numpy(key.view(np.int32)).to(DEV)
+    out = torch.zeros((n, 4), dtype=torch.int32, device=DEV)
+    assert curand_philox().curand_philox_ref(c.data_ptr(), k.data_ptr(), n, out.data_ptr()) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    for i in range(n):
+        assert np.array_equal(got[i], orc.philox(ctr[i], key[i])), i
