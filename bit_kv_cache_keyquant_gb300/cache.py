@@ -50,11 +50,12 @@ class KiviCache:
     def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, device="cuda"):
         self.cfg, self.batch, self.max_seq_len = cfg, batch, max_seq_len
         H, G, Gv, R = cfg.n_kv_heads, cfg.group_k, cfg.group_v, cfg.residual
-        self.ngrp_cap = (max_seq_len + G - 1) // G
+        self.cap = (max_seq_len + 127) // 128 * 128        # token capacity (16-byte aligned rows)
+        self.ngrp_cap = self.cap // G
         self.k_codes = torch.zeros((batch, H, self.ngrp_cap, G * D // 4), dtype=torch.uint8, device=device)
         self.k_sz = torch.zeros((batch, H, self.ngrp_cap, D), dtype=torch.int32, device=device)
-        self.v_codes = torch.zeros((batch, H, max_seq_len, D // 4), dtype=torch.uint8, device=device)
-        self.v_sz = torch.zeros((batch, H, max_seq_len, D // Gv), dtype=torch.int32, device=device)
+        self.v_codes = torch.zeros((batch, H, self.cap, D // 4), dtype=torch.uint8, device=device)
+        self.v_sz = torch.zeros((batch, H, self.cap, D // Gv), dtype=torch.int32, device=device)
         self.k_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
         self.v_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
         self.seq_len = torch.ones(batch, dtype=torch.int32, device=device)

@@ -6,11 +6,17 @@
 //           = sum_c (alpha q_c s_cg) code_ct + alpha sum_c q_c z_cg
 //   o_c     = sum_t p_t (s_tj code_tc + z_tj)
 //           = sum_t (p_t s_tj) code_tc + sum_t p_t z_tj
-// with alpha = sm_scale * log2(e) (softmax in base 2).  A 2-bit code masked
-// in place out of its packed word is read as an fp16 subnormal equal to
-// code * 2^(2j-24) (j = its position in the byte), so one LOP3 yields two
-// exact operands and fma.rn.f32.f16 accumulates their products in fp32; the
-// power of two is removed once per token (keys) or channel (values).
+// with alpha = sm_scale * log2(e) (softmax in base 2).
+// Keys: a 2-bit code masked in place out of its packed word, read as an fp32
+// bit pattern, is the denormal code * 2^(k-149) (k = its bit position, kept
+// below the exponent field), so one LOP3 makes an exact fp32 operand and a
+// packed fma.rn.f32x2 multiplies it by alpha q s pre-scaled by 2^(149-k-E0);
+// every product is alpha q s code 2^(2j-E0), exact in fp32 (the fp32 weight
+// matters: a logit error is amplified by the softmax).
+// Values: the same masking read as fp16 subnormals (code * 2^(2i-24)), two
+// codes per LOP3, accumulated by fma.rn.f32.f16 with the fp16 weight
+// p_t s_tj (a weight's rounding is not amplified).
+// Powers of two are removed once per token (keys) or channel (values).
 //
 // Data movement: a producer warp streams 128-token stages (key codes, key
 // (s, z), value codes, value (s, z): 12 KiB at G = Gv = 32) with 1-D bulk
@@ -40,7 +46,7 @@ struct Smem {
     uint8_t stage[NSTAGE][STAGE_BYTES];
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
-    uint16_t qp[NCWARP][KVQ_D];           // per-warp alpha*q*s (fp16) of the current key group
+    float qk[NCWARP][KVQ_D];              // per-warp alpha*q*s*2^(149-8(c&1)-E0) of the current key group
     float st_acc[NSTATE][KVQ_D];
     float st_m[NSTATE];
     float st_l[NSTATE];
@@ -58,9 +64,11 @@ struct Params {
     float *ws_o;
     float *ws_lse;
     unsigned *err;
-    int Hq, Hkv, G, Gv, R, max_seq_len, splits, chunk;
-    int64_t kgrp_cap;
+    int Hq, Hkv, G, Gv, R, splits, chunk;
+    int64_t cap;        // token capacity per (b, kvh): max_seq_len rounded up to 128
+    int64_t kgrp_cap;   // cap / G
     float alpha;
+    int e0;             // product exponent offset: every key product is scaled by 2^-E0
 };
 
 __device__ __forceinline__ int kivi_key_byte_offset(int t, int c) {
@@ -90,8 +98,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
     const int64_t bk = (int64_t)b * P.Hkv + kvh;
     const uint8_t *kc_base = P.k_codes + bk * P.kgrp_cap * ((int64_t)G * KVQ_D / 4);
     const uint32_t *ksz_base = P.k_sz + bk * P.kgrp_cap * KVQ_D;
-    const uint8_t *vc_base = P.v_codes + bk * (int64_t)P.max_seq_len * (KVQ_D / 4);
-    const uint32_t *vsz_base = P.v_sz + bk * (int64_t)P.max_seq_len * (KVQ_D / Gv);
+    const uint8_t *vc_base = P.v_codes + bk * P.cap * (KVQ_D / 4);
+    const uint32_t *vsz_base = P.v_sz + bk * P.cap * (KVQ_D / Gv);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
@@ -159,44 +167,48 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             const uint8_t *st = S.stage[slot];
             const int gl = (32 * warp) / G;                       // key group of this tile within the stage
             const uint32_t *ksz = reinterpret_cast<const uint32_t *>(st + KC_BYTES) + gl * KVQ_D;
-            // ---- alpha*q*s for this group (fp16) and alpha*sum q z ----
-            uint4 szv = *reinterpret_cast<const uint4 *>(ksz + 4 * lane);
-            float z0 = h2f(hi16(szv.x)), z1 = h2f(hi16(szv.y)), z2 = h2f(hi16(szv.z)), z3 = h2f(hi16(szv.w));
-            uint32_t p01 = (uint32_t)f2h_rn(qa[0] * h2f(lo16(szv.x))) | ((uint32_t)f2h_rn(qa[1] * h2f(lo16(szv.y))) << 16);
-            uint32_t p23 = (uint32_t)f2h_rn(qa[2] * h2f(lo16(szv.z))) | ((uint32_t)f2h_rn(qa[3] * h2f(lo16(szv.w))) << 16);
-            *reinterpret_cast<uint2 *>(&S.qp[warp][4 * lane]) = make_uint2(p01, p23);
-            float cb = warp_sum(qa[0] * z0 + qa[1] * z1 + qa[2] * z2 + qa[3] * z3);
+            // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
+            const float4 szv = *reinterpret_cast<const float4 *>(ksz + 4 * lane);
+            const uint32_t sz0 = __float_as_uint(szv.x), sz1 = __float_as_uint(szv.y);
+            const uint32_t sz2 = __float_as_uint(szv.z), sz3 = __float_as_uint(szv.w);
+            // channel 4*lane + i has byte parity i & 1: pre-scale 2^(149-E0) or 2^(141-E0)
+            const float pe = __int_as_float((127 + 149 - P.e0) << 23), po = __int_as_float((127 + 141 - P.e0) << 23);
+            *reinterpret_cast<float4 *>(&S.qk[warp][4 * lane]) =
+                make_float4(qa[0] * h2f(lo16(sz0)) * pe, qa[1] * h2f(lo16(sz1)) * po, qa[2] * h2f(lo16(sz2)) * pe,
+                            qa[3] * h2f(lo16(sz3)) * po);
+            const float cb = warp_sum(qa[0] * h2f(hi16(sz0)) + qa[1] * h2f(hi16(sz1)) + qa[2] * h2f(hi16(sz2)) +
+                                      qa[3] * h2f(hi16(sz3)));
             __syncwarp();
-            uint32_t qh[16];
+            float qk[32];
             {
-                const uint4 *qs = reinterpret_cast<const uint4 *>(&S.qp[warp][32 * tq]);
+                const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][32 * tq]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint4 u = qs[i];
-                    qh[4 * i] = u.x; qh[4 * i + 1] = u.y; qh[4 * i + 2] = u.z; qh[4 * i + 3] = u.w;
+                for (int i = 0; i < 8; ++i) {
+                    const float4 u = qs[i];
+                    qk[4 * i] = u.x; qk[4 * i + 1] = u.y; qk[4 * i + 2] = u.z; qk[4 * i + 3] = u.w;
                 }
             }
             // ---- key codes: tokens 4qd..4qd+3 x channels 32tq..32tq+31 ----
             const uint8_t *kt = st + warp * 1024;
-            uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
-            uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
-            uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
+            const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
+            const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+            unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};     // fp32 pairs (0.0f, 0.0f)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const uint32_t w0 = kw[k], w8 = kw[k] >> 8;
-                const uint32_t qa01 = qh[2 * k], qa23 = qh[2 * k + 1];   // channels 4k+{0,1}, 4k+{2,3}
+                const uint32_t w0 = kw[k], w16 = kw[k] >> 16;          // bytes 0,1 | bytes 2,3 at bits 0..15
+                const unsigned long long q01 = pack2f(qk[4 * k], qk[4 * k + 1]);
+                const unsigned long long q23 = pack2f(qk[4 * k + 2], qk[4 * k + 3]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t m = 0x00030003u << (2 * j);
-                    const uint32_t e = w0 & m;      // bytes 0, 2: channels 4k, 4k+2
-                    const uint32_t o = w8 & m;      // bytes 1, 3: channels 4k+1, 4k+3
-                    acc[j] = fma_f16f32(lo16(e), lo16(qa01), acc[j]);
-                    acc[j] = fma_f16f32(hi16(e), lo16(qa23), acc[j]);
-                    acc[j] = fma_f16f32(lo16(o), hi16(qa01), acc[j]);
-                    acc[j] = fma_f16f32(hi16(o), hi16(qa23), acc[j]);
+                    const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
+                    acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // channels 4k, 4k+1
+                    acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);   // channels 4k+2, 4k+3
                 }
             }
+            float acc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = lo2f(acc2[j]) + hi2f(acc2[j]);
             // transpose-reduce over the 4 lanes of the quad: lane keeps token 4qd + tq
             float score;
             {
@@ -209,8 +221,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
                 float sx = h1 ? k0 : k1;
                 score = (h1 ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, sx, 1);
             }
-            // undo the 2^(2j-24) operand scaling (j = tq), add the zero-point term
-            const float logit = score * __int_as_float((127 + 24 - 2 * tq) << 23) + cb;
+            // undo the 2^(2j-E0) product scaling (j = tq), add the zero-point term
+            const float logit = score * __int_as_float((127 + P.e0 - 2 * tq) << 23) + cb;
             // ---- online softmax over the tile (warp-uniform running max) ----
             const float mt = warp_max(logit);
             if (mt > m_run) {
@@ -375,11 +387,14 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
     P.G = cfg->group_k;
     P.Gv = cfg->group_v;
     P.R = cfg->residual;
-    P.max_seq_len = c->max_seq_len;
+    P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
     P.splits = p.splits;
     P.chunk = p.chunk;
-    P.kgrp_cap = (c->max_seq_len + cfg->group_k - 1) / cfg->group_k;
+    P.kgrp_cap = P.cap / cfg->group_k;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    // |alpha q s| < alpha 2^32 (fp16 q and s): 2^(149-E0) alpha 2^32 < 2^127
+    P.e0 = 54 + (int)ceilf(log2f(P.alpha));
+    if (P.e0 < 22) P.e0 = 22;
     if (!P.err) return cudaErrorInvalidDevicePointer;
     const size_t smem = sizeof(Smem);
     static int attr_dev = -1;

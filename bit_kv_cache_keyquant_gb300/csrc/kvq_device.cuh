@@ -23,6 +23,25 @@ __device__ __forceinline__ float fma_f16f32(uint16_t a, uint16_t b, float c) {
     asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
     return d;
 }
+// packed fp32 pair helpers for fma.rn.f32x2 (two FMAs per instruction)
+__device__ __forceinline__ unsigned long long pack2f(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long pack2u(uint32_t a, uint32_t b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ float lo2f(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2f(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+// d = a * b + c elementwise on fp32 pairs (denormal inputs honoured: no ftz)
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return (uint16_t)(v & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return (uint16_t)(v >> 16); }
 

@@ -178,12 +178,12 @@ KVQ_API size_t kvq_kitty_value_page_bytes(const kvq_config *cfg);
  * Residual token t is stored at slot t % R.  (KIVI section 3.3, Eq. 3.) */
 typedef struct {
     int32_t batch;
-    int32_t max_seq_len;
+    int32_t max_seq_len;     /* token capacity CAP = max_seq_len rounded up to a multiple of 128 */
     const int32_t *seq_len;  /* [B] */
-    const void *k_codes;     /* uint8  [B][Hkv][ceil(max_seq_len/G)][G*D/4] */
-    const void *k_sz;        /* fp16x2 [B][Hkv][ceil(max_seq_len/G)][D] */
-    const void *v_codes;     /* uint8  [B][Hkv][max_seq_len][D/4] */
-    const void *v_sz;        /* fp16x2 [B][Hkv][max_seq_len][D/Gv] */
+    const void *k_codes;     /* uint8  [B][Hkv][CAP/G][G*D/4] */
+    const void *k_sz;        /* fp16x2 [B][Hkv][CAP/G][D] */
+    const void *v_codes;     /* uint8  [B][Hkv][CAP][D/4] */
+    const void *v_sz;        /* fp16x2 [B][Hkv][CAP][D/Gv] */
     const void *k_res;       /* fp16   [B][Hkv][R][D] */
     const void *v_res;       /* fp16   [B][Hkv][R][D] */
 } kvq_kivi_cache;
