@@ -1,0 +1,363 @@
+"""Benchmark of the quantized-KV decode layer-step on GB300.
+
+Default workload (N=1): Llama-2-7B-shaped MHA decode layer, batch 32,
+32 query / 32 KV heads, head_dim 128, 4096 cached tokens, K2V2 (keys per
+channel over 32-token groups, values per token over 32-channel groups),
+fp16 residual R = 128.  One step = one layer-step of the whole hot path:
+  a2  kv_quant_value  on the B*Hkv value tokens leaving the fp16 window,
+  a1  kv_quant_key    on the amortized key flush (1/R of the (b, kv head)
+                      pairs flush their R/G groups each step),
+  a3  decode stage 1  (split-KV attention over quantized + fp16 segments),
+  a4  decode merge    (LSE merge, fp16 out).
+`value` is microseconds per layer-step (whole job: time / (steps * N)),
+inputs resident in HBM; `e2e` is the same metric through the C ABI with the
+step's inputs copied from pinned host memory and the output copied back
+inside the timed region.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from bit_kv_cache_keyquant_gb300 import inputs as I  # noqa: E402
+
+METRIC = "quantized-KV decode attention: us/layer-step and HBM GB/s (% of GB300 peak)"
+UNIT = "us/layer-step"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _workload_desc(w):
+    return (f"{w.name}: batch {w.batch}, {w.n_q_heads} query / {w.n_kv_heads} KV heads, head_dim 128, "
+            f"{w.seq_len} cached tokens, K2V2 (key per-channel G=32, value per-token Gv=32), R=128")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) >= 9:
+                self.rows.append(f)
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_step_seconds(w, budget_s: float, min_pairs: int = 4):
+    """Time the oracle's layer-step on a bounded sample of (b, kv head) pairs.
+
+    Per pair: quantize the value token leaving the fp16 window, then split-free
+    fp64 attention of the pair's query heads over the quantized cache and the
+    fp16 residual.  Returns (seconds per pair, pairs timed)."""
+    from oracle import oracle as O
+    O.build()
+    g = w.n_q_heads // w.n_kv_heads
+    q = I.gen_q_np(w)
+    L = w.seq_len
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
+    rng = np.random.default_rng(0)
+    rng.shuffle(pairs)
+    spent, n = 0.0, 0
+    for b, h in pairs:
+        K = I.gen_kv_np(w, I.T_K, b, h, L)
+        V = I.gen_kv_np(w, I.T_V, b, h, L)
+        parts = O.kivi_build_one(K, V)
+        t0 = time.perf_counter()
+        O.kivi_quant_value(V[L - 129:L - 128])
+        O.kivi_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L)
+        spent += time.perf_counter() - t0
+        n += 1
+        if n >= min_pairs and spent >= budget_s:
+            break
+    return spent / n, n
+
+
+def run_reference(args, w):
+    per_pair_w, _ = oracle_step_seconds(w, 0.0, min_pairs=2)          # warm-up (builds the oracle)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_step_seconds(w, 0.0, min_pairs=1)
+    times = []
+    npairs = 0
+    for _ in range(args.steps):
+        per_pair, n = oracle_step_seconds(w, 0.2, min_pairs=2)
+        times.append(per_pair)
+        npairs += n
+    per_pair = statistics.median(times)
+    us = per_pair * w.batch * w.n_kv_heads * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_desc(w), "batch": w.batch, "seq_len": w.seq_len},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{npairs} (batch row, kv head) pairs over {args.steps} steps, each step scaled "
+                                   f"by {w.batch * w.n_kv_heads} pairs per layer-step"},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def build_kivi_state(w, device):
+    import torch
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    from bit_kv_cache_keyquant_gb300 import kvq
+    cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
+    L = w.seq_len
+    cache = C.KiviCache(cfg, w.batch, L, device=device)
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            cache.fill(b, h, I.gen_kv_torch(w, I.T_K, b, h, L, device), I.gen_kv_torch(w, I.T_V, b, h, L, device))
+    q = I.gen_q_torch(w, device)
+    # per-step write-side inputs: one value token per (b, kv head) and the amortized key flush
+    n_vtok = w.batch * w.n_kv_heads
+    n_kgrp = max(1, w.batch * w.n_kv_heads * (cfg.residual // cfg.group_k) // cfg.residual)
+    vnew = I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_vtok, 128, device)
+    knew = I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_kgrp * cfg.group_k, 128, device)
+    scratch = {
+        "vcodes": torch.empty((n_vtok, 32), dtype=torch.uint8, device=device),
+        "vsz": torch.empty((n_vtok, 128 // cfg.group_v), dtype=torch.int32, device=device),
+        "kcodes": torch.empty((n_kgrp, cfg.group_k * 32), dtype=torch.uint8, device=device),
+        "ksz": torch.empty((n_kgrp, 128), dtype=torch.int32, device=device),
+    }
+    n_splits, wsb = kvq.kv_decode_attn_plan(cfg, kvq.KVQ_VARIANT_KIVI, w.batch, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+    out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float16, device=device)
+    torch.cuda.synchronize()
+    return dict(cfg=cfg, cache=cache, desc=cache.desc(), q=q, vnew=vnew, knew=knew, n_vtok=n_vtok, n_kgrp=n_kgrp,
+                scratch=scratch, ws=ws, wsb=wsb, out=out, n_splits=n_splits)
+
+
+def kivi_step(st, stream, ev=None, q=None, vnew=None, knew=None):
+    from bit_kv_cache_keyquant_gb300 import kvq
+    cfg, sc = st["cfg"], st["scratch"]
+    if ev is not None:
+        ev[0].record(stream)
+    kvq.kv_quant_value(cfg, st["vnew"] if vnew is None else vnew, st["n_vtok"], sc["vcodes"], sc["vsz"], stream)
+    kvq.kv_quant_key(cfg, st["knew"] if knew is None else knew, st["n_kgrp"], sc["kcodes"], sc["ksz"], stream)
+    if ev is not None:
+        ev[1].record(stream)
+    kvq.kv_decode_attn_stage1(cfg, kvq.KVQ_VARIANT_KIVI, st["desc"], st["q"] if q is None else q, st["ws"],
+                              st["wsb"], stream)
+    if ev is not None:
+        ev[2].record(stream)
+    kvq.kv_decode_attn_merge(cfg, kvq.KVQ_VARIANT_KIVI, st["cache"].batch, st["cache"].max_seq_len, st["ws"],
+                             st["wsb"], st["out"], stream)
+    if ev is not None:
+        ev[3].record(stream)
+
+
+def run_gpu(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from bit_kv_cache_keyquant_gb300 import kvq
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    st = build_kivi_state(w, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- kernel-only timing: inputs resident in HBM (458 MB/step > 129 MB L2) ----
+    for _ in range(args.warmup):
+        kivi_step(st, stream)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            kivi_step(st, stream, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_end)
+    stage1_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    assert kvq.kvq_get_device_error() == 0
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end through the C ABI with host buffers ----
+    qh = st["q"].cpu().pin_memory()
+    vh = st["vnew"].cpu().pin_memory()
+    kh = st["knew"].cpu().pin_memory()
+    outh = torch.empty(st["out"].shape, dtype=torch.float16).pin_memory()
+    qd, vd, kd = torch.empty_like(st["q"]), torch.empty_like(st["vnew"]), torch.empty_like(st["knew"])
+    for _ in range(args.warmup):
+        qd.copy_(qh, non_blocking=True); vd.copy_(vh, non_blocking=True); kd.copy_(kh, non_blocking=True)
+        kivi_step(st, stream, q=qd, vnew=vd, knew=kd)
+        outh.copy_(st["out"], non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        qd.copy_(qh, non_blocking=True); vd.copy_(vh, non_blocking=True); kd.copy_(kh, non_blocking=True)
+        kivi_step(st, stream, q=qd, vnew=vd, knew=kd)
+        outh.copy_(st["out"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = qh.numel() * 2 + vh.numel() * 2 + kh.numel() * 2
+    d2h = outh.numel() * 2
+
+    if rank != 0:
+        return
+    lens = [w.seq_len] * w.batch
+    cache_bytes = st["cache"].nbytes_read(lens)
+    q_bytes = w.batch * w.n_q_heads * 128 * 2
+    alg_bytes_stage1 = cache_bytes + q_bytes
+    s1 = statistics.mean(stage1_ms)
+    achieved = alg_bytes_stage1 / (s1 * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    traffic = None
+    if os.path.exists(prof):
+        tr = json.load(open(prof)).get("kivi_decode_kernel@workload2")
+        if tr and tr.get("source_hash") == kernel_source_hash():
+            traffic = tr["bytes_per_launch"]
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        per_pair, n = oracle_step_seconds(w, args.cpu_budget)
+        cpu = {"value": per_pair * w.batch * w.n_kv_heads * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} (batch row, kv head) pairs of the workload, single thread, scaled by "
+                         f"{w.batch * w.n_kv_heads} pairs per layer-step"}
+    n_steps_total = args.steps * world
+    value = total_ms * 1e3 / n_steps_total if world > 1 else ms_per_step * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u2 codes + fp16 scales, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": _workload_desc(w), "batch": w.batch, "q_heads": w.n_q_heads,
+                   "kv_heads": w.n_kv_heads, "head_dim": 128, "seq_len": w.seq_len, "parallelism": f"replicas x{world}",
+                   "splits": st["n_splits"], "l2": "inputs larger than L2 (458 MB read per step vs 129 MB L2)"},
+        "breakdown_us": {"quant_value+key": 1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
+                         "merge": 1e3 * statistics.mean(merge_ms)},
+        "hbm_gbs_step": (alg_bytes_stage1 + d2h) / (ms_per_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "kivi_decode_kernel (a3 stage 1)",
+                     "alg_bytes_per_launch": alg_bytes_stage1},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_ms * 1e3 / args.steps / (world if world > 1 else 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kvq_decode_kivi.cu", "kvq_device.cuh"):
+        h.update(open(os.path.join(ROOT, "bit_kv_cache_keyquant_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--workload", type=int, default=2, choices=[2])
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = I.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    from bit_kv_cache_keyquant_gb300 import build
+    build.build()
+    run_gpu(args, w, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -53,17 +53,24 @@ float sm_scale_of(const kvq_config *cfg) {
     return cfg->sm_scale > 0.f ? cfg->sm_scale : 1.0f / sqrtf((float)cfg->head_dim);
 }
 
-// Splits: 512-token chunks (a multiple of the 128-token stage), widened so
-// that no row has more than 256 splits.
+// Splits: chunks of a multiple of 128 tokens (the stage), sized so that the
+// persistent decode grid (4 CTAs per SM) gets about 8 units per CTA, within
+// [128, 4096] tokens and at most 256 + 1 splits per row (the last split of
+// a row holds the tokens outside the quantized tiles, e.g. the fp16 residual).
 kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
     (void)variant;
-    int chunk = 512;
-    const int min_chunk = (int)((((int64_t)max_seq_len + 255) / 256 + 127) / 128 * 128);
-    if (min_chunk > chunk) chunk = min_chunk;
-    const int splits = (max_seq_len + chunk - 1) / chunk;
     const int64_t rows = (int64_t)batch * cfg->n_q_heads;
-    p->splits = splits < 1 ? 1 : splits;
-    p->chunk = chunk;
+    const int64_t target_units = 8LL * num_sms() * 4;
+    int64_t chunk = (rows * max_seq_len + target_units - 1) / target_units;
+    chunk = (chunk + 127) / 128 * 128;
+    if (chunk < 128) chunk = 128;
+    if (chunk > 4096) chunk = 4096;
+    const int64_t min_chunk = (((int64_t)max_seq_len + 255) / 256 + 127) / 128 * 128;
+    if (chunk < min_chunk) chunk = min_chunk;
+    // quantized-tile splits, plus one split per row for the tokens outside the tiles
+    const int splits = (int)(((int64_t)max_seq_len + chunk - 1) / chunk) + 1;
+    p->splits = splits;
+    p->chunk = (int)chunk;
     p->off_o = 256;
     p->off_lse = p->off_o + (size_t)rows * p->splits * KVQ_D * sizeof(float);
     p->ws_bytes = (p->off_lse + (size_t)rows * p->splits * sizeof(float) + 255) / 256 * 256;

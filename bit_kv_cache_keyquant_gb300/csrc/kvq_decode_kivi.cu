@@ -1,5 +1,4 @@
-// a3: KIVI split-KV decode attention, stage 1 (one CTA per (split, query
-// head, batch row)).
+// a3: KIVI split-KV decode attention, stage 1.
 //
 // Math (KIVI Eq. 3 with the dequantization folded out of the inner loops):
 //   score_t = alpha * sum_c q_c (s_cg code_ct + z_cg)
@@ -18,13 +17,17 @@
 // p_t s_tj (a weight's rounding is not amplified).
 // Powers of two are removed once per token (keys) or channel (values).
 //
-// Data movement: a producer warp streams 128-token stages (key codes, key
-// (s, z), value codes, value (s, z): 12 KiB at G = Gv = 32) with 1-D bulk
-// async copies (cp.async.bulk, the TMA engine) into a 4-slot shared-memory
-// ring guarded by mbarriers; four consumer warps each take one 32-token tile
-// of a stage.  Tokens whose key or value is not quantized (the fp16
-// residual) take a per-token path.  Each warp keeps its own online softmax
-// state; the CTA merges the eight warp states and writes (o_s, lse_s).
+// Work decomposition: a persistent grid walks the (batch row, query head,
+// split) units round-robin.  A producer warp streams every unit's 128-token
+// stages (key codes, key (s, z), value codes, value (s, z): 12 KiB at
+// G = Gv = 32) with 1-D bulk async copies (cp.async.bulk, the TMA engine)
+// into a 4-slot shared-memory ring guarded by mbarriers, without pausing at
+// unit boundaries; four consumer warps each take one 32-token tile of a
+// stage.  The last split of every row is a residual unit: tokens whose key
+// or value is not quantized (the fp16 residual, and any tile cut by a segment
+// boundary), 32 per warp straight from global memory with every load of a
+// block in flight together.  Each warp keeps an online softmax state per
+// unit; the CTA merges the four warp states and writes (o_s, lse_s).
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -40,16 +43,16 @@ constexpr int KSZ_MAX = 4 * KVQ_D * 4;                  // 2048 (G = 32)
 constexpr int VC_BYTES = STAGE_TOK * KVQ_D / 4;        // 4096
 constexpr int VSZ_MAX = STAGE_TOK * 4 * 4;             // 2048 (Gv = 32)
 constexpr int STAGE_BYTES = KC_BYTES + KSZ_MAX + VC_BYTES + VSZ_MAX;   // 12288
-constexpr int NSTATE = 2 * NCWARP;
+constexpr int QK_ROW = 36;                // 32 channels + 4 floats of padding (bank spread)
 
 struct Smem {
     uint8_t stage[NSTAGE][STAGE_BYTES];
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
-    float qk[NCWARP][KVQ_D];              // per-warp alpha*q*s*2^(149-8(c&1)-E0) of the current key group
-    float st_acc[NSTATE][KVQ_D];
-    float st_m[NSTATE];
-    float st_l[NSTATE];
+    float qk[NCWARP][4 * QK_ROW];         // per-warp alpha*q*s*2^(149-8(c&1)-E0), rows of 32 channels
+    float st_acc[NCWARP][KVQ_D];
+    float st_m[NCWARP];
+    float st_l[NCWARP];
 };
 
 struct Params {
@@ -64,15 +67,100 @@ struct Params {
     float *ws_o;
     float *ws_lse;
     unsigned *err;
-    int Hq, Hkv, G, Gv, R, splits, chunk;
+    int B, Hq, Hkv, G, Gv, R, splits, chunk;
+    int ngv;            // D / Gv: value (s, z) pairs per token
     int64_t cap;        // token capacity per (b, kvh): max_seq_len rounded up to 128
     int64_t kgrp_cap;   // cap / G
     float alpha;
-    int e0;             // product exponent offset: every key product is scaled by 2^-E0
+    int e0;             // key products are scaled by 2^-E0
 };
+
+// Geometry of one work unit.  Splits 0 .. splits-2 of a (batch row, query
+// head) cover the staged quantized tiles [0, Qf) in chunks; split splits-1
+// covers every remaining token [Qf, L) (the fp16 residual and any tokens cut
+// off by a segment boundary), read straight from global memory.
+struct Unit {
+    int b, hq, split, t0, t1, nT, nstages, nKq, nVq;
+    bool residual;
+    int64_t bk;
+};
+
+__device__ __forceinline__ Unit unit_of(const Params &P, int u) {
+    Unit U;
+    const int row = u / P.splits;
+    U.split = u - row * P.splits;
+    U.b = row / P.Hq;
+    U.hq = row - U.b * P.Hq;
+    const int L = P.seq_len[U.b];
+    const int rK = ((L - 1) % P.R) + 1;
+    U.nKq = L - rK;
+    U.nVq = L - (L < P.R ? L : P.R);
+    const int Qf = (U.nKq < U.nVq ? U.nKq : U.nVq) & ~31;
+    U.residual = U.split == P.splits - 1;
+    if (U.residual) {
+        U.t0 = Qf;
+        U.t1 = L;
+        U.nT = 0;
+    } else {
+        U.t0 = U.split * P.chunk;
+        U.t1 = max(U.t0, min(U.t0 + P.chunk, Qf));
+        U.nT = (U.t1 - U.t0) / 32;
+    }
+    U.nstages = (U.nT + NCWARP - 1) / NCWARP;
+    U.bk = (int64_t)U.b * P.Hkv + U.hq / (P.Hq / P.Hkv);
+    return U;
+}
 
 __device__ __forceinline__ int kivi_key_byte_offset(int t, int c) {
     return (t >> 5) * 1024 + ((c >> 4) & 1) * 512 + (4 * ((t & 31) >> 2) + (c >> 5)) * 16 + ((c >> 2) & 3) * 4 + (c & 3);
+}
+
+// Four dequantized key / value channels 4*lane..4*lane+3 of token t, from the
+// quantized segment or the fp16 residual (used outside the staged tiles).
+__device__ __forceinline__ void fetch_k4(const Params &P, const Unit &U, int t, int lane, float kv[4]) {
+    if (t < U.nKq) {
+        const int G = P.G, gi = t / G, tt = t - gi * G;
+        const uint8_t *grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D / 4);
+        const uint4 sz = *reinterpret_cast<const uint4 *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D + 4 * lane);
+        const uint32_t s4[4] = {sz.x, sz.y, sz.z, sz.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int code = (grp[kivi_key_byte_offset(tt, 4 * lane + i)] >> (2 * (tt & 3))) & 3;
+            kv[i] = (float)code * h2f(lo16(s4[i])) + h2f(hi16(s4[i]));
+        }
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2 *>(P.k_res + (U.bk * P.R + t % P.R) * KVQ_D + 4 * lane);
+        kv[0] = h2f(lo16(u.x)); kv[1] = h2f(hi16(u.x)); kv[2] = h2f(lo16(u.y)); kv[3] = h2f(hi16(u.y));
+    }
+}
+
+__device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, int lane, float vv[4]) {
+    if (t < U.nVq) {
+        const uint8_t byte = P.v_codes[(U.bk * P.cap + t) * (KVQ_D / 4) + lane];
+        const uint32_t sz = P.v_sz[(U.bk * P.cap + t) * P.ngv + (4 * lane) / P.Gv];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vv[i] = (float)((byte >> (2 * i)) & 3) * h2f(lo16(sz)) + h2f(hi16(sz));
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2 *>(P.v_res + (U.bk * P.R + t % P.R) * KVQ_D + 4 * lane);
+        vv[0] = h2f(lo16(u.x)); vv[1] = h2f(hi16(u.x)); vv[2] = h2f(lo16(u.y)); vv[3] = h2f(hi16(u.y));
+    }
+}
+
+// Online-softmax update of a warp state with one logit per lane (-inf for
+// empty lanes): returns p = 2^(logit - m) and rescales on a new maximum.
+__device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias, float vacc[32]) {
+    const float mt = warp_max(logit);
+    if (mt > m_run) {
+        const float sc = exp2f(m_run - mt);
+        l_part *= sc;
+        vbias *= sc;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) vacc[i] *= sc;
+        m_run = mt;
+    }
+    const float p = exp2f(logit - m_run);
+    l_part += p;
+    return p;
 }
 
 }  // namespace
@@ -80,26 +168,9 @@ __device__ __forceinline__ int kivi_key_byte_offset(int t, int c) {
 __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Params P) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
-    const int split = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
-    const int g = P.Hq / P.Hkv;
-    const int kvh = hq / g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = P.seq_len[b];
-    const int R = P.R, G = P.G, Gv = P.Gv;
-    const int rK = ((L - 1) % R) + 1;
-    const int nKq = L - rK;
-    const int nVq = L - (L < R ? L : R);
-    const int Qf = (nKq < nVq ? nKq : nVq) & ~31;         // fast tiles end here
-    const int t0 = split * P.chunk;
-    const int t1 = min(t0 + P.chunk, L);
-    const int fast_end = max(t0, min(t1, Qf));
-    const int nT = (fast_end - t0) / 32;                  // full 32-token tiles
-    const int nstages = (nT + NCWARP - 1) / NCWARP;
-    const int64_t bk = (int64_t)b * P.Hkv + kvh;
-    const uint8_t *kc_base = P.k_codes + bk * P.kgrp_cap * ((int64_t)G * KVQ_D / 4);
-    const uint32_t *ksz_base = P.k_sz + bk * P.kgrp_cap * KVQ_D;
-    const uint8_t *vc_base = P.v_codes + bk * P.cap * (KVQ_D / 4);
-    const uint32_t *vsz_base = P.v_sz + bk * P.cap * (KVQ_D / Gv);
+    const int n_units = P.B * P.Hq * P.splits;
+    const int G = P.G, Gv = P.Gv;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
@@ -111,260 +182,297 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
     __syncthreads();
 
     if (warp == NCWARP) {
-        // ---------------- producer ----------------
+        // ---------------- producer: one stream of stages across all units ----------------
         if (lane == 0) {
             bool ok = true;
-            for (int s = 0; s < nstages && ok; ++s) {
-                const int slot = s % NSTAGE;
-                if (s >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((s / NSTAGE) - 1) & 1, P.err);
-                if (!ok) break;
-                const int nt = min(NCWARP, nT - s * NCWARP);
-                const int tok = t0 + s * STAGE_TOK;
-                const uint32_t kc_b = nt * 1024;
-                const int ngrp = (nt * 32 + G - 1) / G;
-                const uint32_t ksz_b = ngrp * KVQ_D * 4;
-                const uint32_t vc_b = nt * 32 * (KVQ_D / 4);
-                const uint32_t vsz_b = nt * 32 * (KVQ_D / Gv) * 4;
-                uint8_t *st = S.stage[slot];
-                mbar_expect_tx(&S.full[slot], kc_b + ksz_b + vc_b + vsz_b);
-                bulk_g2s(st, kc_base + (int64_t)(tok >> 5) * 1024, kc_b, &S.full[slot]);
-                bulk_g2s(st + KC_BYTES, ksz_base + (int64_t)(tok / G) * KVQ_D, ksz_b, &S.full[slot]);
-                bulk_g2s(st + KC_BYTES + KSZ_MAX, vc_base + (int64_t)tok * (KVQ_D / 4), vc_b, &S.full[slot]);
-                bulk_g2s(st + KC_BYTES + KSZ_MAX + VC_BYTES, vsz_base + (int64_t)tok * (KVQ_D / Gv), vsz_b,
-                         &S.full[slot]);
+            int sg = 0;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit U = unit_of(P, u);
+                const uint8_t *kc_base = P.k_codes + U.bk * P.kgrp_cap * ((int64_t)G * KVQ_D / 4);
+                const uint32_t *ksz_base = P.k_sz + U.bk * P.kgrp_cap * KVQ_D;
+                const uint8_t *vc_base = P.v_codes + U.bk * P.cap * (KVQ_D / 4);
+                const uint32_t *vsz_base = P.v_sz + U.bk * P.cap * P.ngv;
+                for (int s = 0; s < U.nstages; ++s, ++sg) {
+                    const int slot = sg % NSTAGE;
+                    if (sg >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((sg / NSTAGE) - 1) & 1, P.err);
+                    if (!ok) break;
+                    const int nt = min(NCWARP, U.nT - s * NCWARP);
+                    const int tok = U.t0 + s * STAGE_TOK;
+                    const uint32_t kc_b = nt * 1024;
+                    const uint32_t ksz_b = ((nt * 32 + G - 1) / G) * KVQ_D * 4;
+                    const uint32_t vc_b = nt * 32 * (KVQ_D / 4);
+                    const uint32_t vsz_b = nt * 32 * P.ngv * 4;
+                    uint8_t *st = S.stage[slot];
+                    mbar_expect_tx(&S.full[slot], kc_b + ksz_b + vc_b + vsz_b);
+                    bulk_g2s(st, kc_base + (int64_t)(tok >> 5) * 1024, kc_b, &S.full[slot]);
+                    bulk_g2s(st + KC_BYTES, ksz_base + (int64_t)(tok / G) * KVQ_D, ksz_b, &S.full[slot]);
+                    bulk_g2s(st + KC_BYTES + KSZ_MAX, vc_base + (int64_t)tok * (KVQ_D / 4), vc_b, &S.full[slot]);
+                    bulk_g2s(st + KC_BYTES + KSZ_MAX + VC_BYTES, vsz_base + (int64_t)tok * P.ngv, vsz_b,
+                             &S.full[slot]);
+                }
             }
             // drain: every issued stage must have landed before the CTA exits
-            const int issued = nstages;
-            for (int s = max(0, issued - NSTAGE); s < issued; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
+            for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
         }
         return;
     }
 
     // ---------------- consumers ----------------
-    const uint16_t *qrow = P.q + ((int64_t)b * P.Hq + hq) * KVQ_D;
-    float qa[4];
-    {
-        uint2 u = *reinterpret_cast<const uint2 *>(qrow + 4 * lane);
-        qa[0] = h2f(lo16(u.x)) * P.alpha;
-        qa[1] = h2f(hi16(u.x)) * P.alpha;
-        qa[2] = h2f(lo16(u.y)) * P.alpha;
-        qa[3] = h2f(hi16(u.y)) * P.alpha;
-    }
     const int tq = lane & 3;                       // key mapping: lane = 4*(token quad) + channel block
     const int ts = lane >> 2, jg = lane & 3;       // value mapping: token slot, channel block of 32
-
-    float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
-    float vacc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) vacc[i] = 0.f;
-
+    const float pe = __int_as_float((127 + 149 - P.e0) << 23), po = __int_as_float((127 + 141 - P.e0) << 23);
+    const float lscale = __int_as_float((127 + P.e0 - 2 * tq) << 23);   // undoes 2^(2j-E0), j = tq
+    const int gl = (32 * warp) / G;                // key group of this warp's tile within a stage
+    const int ngv = P.ngv;
+    const int jv = (32 * jg) / Gv;                 // value (s, z) group of this lane's channels
     bool ok = true;
-    for (int s = 0; s < nstages; ++s) {
-        const int slot = s % NSTAGE;
-        ok = ok && mbar_wait(&S.full[slot], (s / NSTAGE) & 1, P.err);
-        const int tile = s * NCWARP + warp;
-        if (ok && tile < nT) {
-            const uint8_t *st = S.stage[slot];
-            const int gl = (32 * warp) / G;                       // key group of this tile within the stage
-            const uint32_t *ksz = reinterpret_cast<const uint32_t *>(st + KC_BYTES) + gl * KVQ_D;
-            // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
-            const float4 szv = *reinterpret_cast<const float4 *>(ksz + 4 * lane);
-            const uint32_t sz0 = __float_as_uint(szv.x), sz1 = __float_as_uint(szv.y);
-            const uint32_t sz2 = __float_as_uint(szv.z), sz3 = __float_as_uint(szv.w);
-            // channel 4*lane + i has byte parity i & 1: pre-scale 2^(149-E0) or 2^(141-E0)
-            const float pe = __int_as_float((127 + 149 - P.e0) << 23), po = __int_as_float((127 + 141 - P.e0) << 23);
-            *reinterpret_cast<float4 *>(&S.qk[warp][4 * lane]) =
-                make_float4(qa[0] * h2f(lo16(sz0)) * pe, qa[1] * h2f(lo16(sz1)) * po, qa[2] * h2f(lo16(sz2)) * pe,
-                            qa[3] * h2f(lo16(sz3)) * po);
-            const float cb = warp_sum(qa[0] * h2f(hi16(sz0)) + qa[1] * h2f(hi16(sz1)) + qa[2] * h2f(hi16(sz2)) +
-                                      qa[3] * h2f(hi16(sz3)));
-            __syncwarp();
-            float qk[32];
-            {
-                const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][32 * tq]);
+    int sg = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        float qa[4];
+        {
+            const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D + 4 * lane);
+            qa[0] = h2f(lo16(qv.x)) * P.alpha;
+            qa[1] = h2f(hi16(qv.x)) * P.alpha;
+            qa[2] = h2f(lo16(qv.y)) * P.alpha;
+            qa[3] = h2f(hi16(qv.y)) * P.alpha;
+        }
+        if (U.residual) {
+            // ---- residual unit: 32 tokens per warp, lane = token; all loads of a block issued together ----
+            float m_run = -INFINITY, l_part = 0.f, racc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int r0 = U.t0 + 32 * warp; r0 < U.t1; r0 += 32 * NCWARP) {
+                const int n = min(32, U.t1 - r0);
+                // whole block fp16 in both K and V (the usual case): unconditional loads,
+                // 8 tokens in flight per batch; indices clamped into the block
+                const bool plain = r0 >= U.nKq && r0 >= U.nVq;
+                const uint16_t *kres = P.k_res + U.bk * P.R * KVQ_D + 4 * lane;
+                const uint16_t *vres = P.v_res + U.bk * P.R * KVQ_D + 4 * lane;
+                float d[32];
+                if (plain) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 u = qs[i];
-                    qk[4 * i] = u.x; qk[4 * i + 1] = u.y; qk[4 * i + 2] = u.z; qk[4 * i + 3] = u.w;
+                    for (int hb = 0; hb < 4; ++hb) {
+                        uint2 raw[8];
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            const int t = min(r0 + 8 * hb + m, U.t1 - 1);
+                            raw[m] = __ldg(reinterpret_cast<const uint2 *>(kres + (t % P.R) * KVQ_D));
+                        }
+#pragma unroll
+                        for (int m = 0; m < 8; ++m)
+                            d[8 * hb + m] = qa[0] * h2f(lo16(raw[m].x)) + qa[1] * h2f(hi16(raw[m].x)) +
+                                             qa[2] * h2f(lo16(raw[m].y)) + qa[3] * h2f(hi16(raw[m].y));
+                    }
+                } else {
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt) {
+                        d[tt] = 0.f;
+                        if (tt < n) {
+                            float kv[4];
+                            fetch_k4(P, U, r0 + tt, lane, kv);
+                            d[tt] = qa[0] * kv[0] + qa[1] * kv[1] + qa[2] * kv[2] + qa[3] * kv[3];
+                        }
+                    }
                 }
-            }
-            // ---- key codes: tokens 4qd..4qd+3 x channels 32tq..32tq+31 ----
-            const uint8_t *kt = st + warp * 1024;
-            const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
-            const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
-            const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-            unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};     // fp32 pairs (0.0f, 0.0f)
+                // reduce-scatter over all 32 lanes: lane keeps token (bit-reversed lane index)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t w0 = kw[k], w16 = kw[k] >> 16;          // bytes 0,1 | bytes 2,3 at bits 0..15
-                const unsigned long long q01 = pack2f(qk[4 * k], qk[4 * k + 1]);
-                const unsigned long long q23 = pack2f(qk[4 * k + 2], qk[4 * k + 3]);
+                for (int o = 16, h = 16; o >= 1; o >>= 1, h >>= 1) {
+                    const bool up = (lane & o) != 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
-                    acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // channels 4k, 4k+1
-                    acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);   // channels 4k+2, 4k+3
+                    for (int m = 0; m < h; ++m) {
+                        const float send = up ? d[m] : d[m + h];
+                        d[m] = (up ? d[m + h] : d[m]) + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+                    }
                 }
-            }
-            float acc[4];
+                // lane holds token 16*b4 + 8*b3 + 4*b2 + 2*b1 + b0 = lane
+                const float logit = lane < n ? d[0] : -INFINITY;
+                const float mt = warp_max(logit);
+                if (mt > m_run) {
+                    const float sc = exp2f(m_run - mt);
+                    l_part *= sc;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[j] = lo2f(acc2[j]) + hi2f(acc2[j]);
-            // transpose-reduce over the 4 lanes of the quad: lane keeps token 4qd + tq
-            float score;
-            {
-                const bool h2 = (tq & 2) != 0;
-                float s0 = h2 ? acc[0] : acc[2], s1 = h2 ? acc[1] : acc[3];
-                float k0 = h2 ? acc[2] : acc[0], k1 = h2 ? acc[3] : acc[1];
-                k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 2);
-                k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 2);
-                const bool h1 = (tq & 1) != 0;
-                float sx = h1 ? k0 : k1;
-                score = (h1 ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, sx, 1);
-            }
-            // undo the 2^(2j-E0) product scaling (j = tq), add the zero-point term
-            const float logit = score * __int_as_float((127 + P.e0 - 2 * tq) << 23) + cb;
-            // ---- online softmax over the tile (warp-uniform running max) ----
-            const float mt = warp_max(logit);
-            if (mt > m_run) {
-                const float sc = exp2f(m_run - mt);
-                l_part *= sc;
-                vbias *= sc;
+                    for (int i = 0; i < 4; ++i) racc[i] *= sc;
+                    m_run = mt;
+                }
+                const float p = exp2f(logit - m_run);
+                l_part += p;
+                if (plain) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) vacc[i] *= sc;
-                m_run = mt;
-            }
-            const float p = exp2f(logit - m_run);
-            l_part += p;
-            // ---- values: 4 passes of 8 tokens; lane = (token slot ts, channel block jg) ----
-            const uint8_t *vc = st + KC_BYTES + KSZ_MAX + warp * 32 * (KVQ_D / 4);
-            const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + KC_BYTES + KSZ_MAX + VC_BYTES) +
-                                  warp * 32 * (KVQ_D / Gv);
-            const int jv = (32 * jg) / Gv;
+                    for (int hb = 0; hb < 4; ++hb) {
+                        uint2 raw[8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int tau = 8 * r + ts;
-                const float pt = __shfl_sync(0xFFFFFFFFu, p, tau);
-                const uint32_t szt = vsz[tau * (KVQ_D / Gv) + jv];
-                const uint16_t pp = f2h_rn(pt * h2f(lo16(szt)));
-                vbias += pt * h2f(hi16(szt));
-                const uint2 u = *reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8);
-                const uint32_t uw[2] = {u.x, u.y};
+                        for (int m = 0; m < 8; ++m) {
+                            const int t = min(r0 + 8 * hb + m, U.t1 - 1);
+                            raw[m] = __ldg(reinterpret_cast<const uint2 *>(vres + (t % P.R) * KVQ_D));
+                        }
 #pragma unroll
-                for (int wi = 0; wi < 2; ++wi) {
-                    const uint32_t w0 = uw[wi], w8 = uw[wi] >> 8;
+                        for (int m = 0; m < 8; ++m) {
+                            const float pt = __shfl_sync(0xFFFFFFFFu, p, 8 * hb + m);   // 0 beyond the block
+                            racc[0] += pt * h2f(lo16(raw[m].x));
+                            racc[1] += pt * h2f(hi16(raw[m].x));
+                            racc[2] += pt * h2f(lo16(raw[m].y));
+                            racc[3] += pt * h2f(hi16(raw[m].y));
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int tt = 0; tt < n; ++tt) {
+                        const float pt = __shfl_sync(0xFFFFFFFFu, p, tt);
+                        float vv[4];
+                        fetch_v4(P, U, r0 + tt, lane, vv);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t m = 0x00030003u << (2 * i);
-                        const uint32_t e = w0 & m, o = w8 & m;
-                        // channel 32jg + 16wi + 4b + i  ->  vacc[16wi + 4b + i]
-                        vacc[16 * wi + 0 + i] = fma_f16f32(lo16(e), pp, vacc[16 * wi + 0 + i]);
-                        vacc[16 * wi + 8 + i] = fma_f16f32(hi16(e), pp, vacc[16 * wi + 8 + i]);
-                        vacc[16 * wi + 4 + i] = fma_f16f32(lo16(o), pp, vacc[16 * wi + 4 + i]);
-                        vacc[16 * wi + 12 + i] = fma_f16f32(hi16(o), pp, vacc[16 * wi + 12 + i]);
+                        for (int i = 0; i < 4; ++i) racc[i] += pt * vv[i];
                     }
                 }
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[slot]);
-    }
-
-    // ---- fast-path state -> shared memory (channel order) ----
-    {
-        const float l_w = warp_sum(l_part);
+            const float l_w = warp_sum(l_part);
+            *reinterpret_cast<float4 *>(&S.st_acc[warp][4 * lane]) = make_float4(racc[0], racc[1], racc[2], racc[3]);
+            if (lane == 0) {
+                S.st_m[warp] = m_run;
+                S.st_l[warp] = l_w;
+            }
+        } else {
+            // query pre-scaled by the byte-parity power of two of its channel (4*lane + i has parity i & 1)
+            const float qp[4] = {qa[0] * pe, qa[1] * po, qa[2] * pe, qa[3] * po};
+            float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
+            float vacc[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            float v = vacc[i];
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-            vacc[i] = v;
-        }
-        float vb = vbias;
-        vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
-        vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 8);
-        vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 16);
-        // lane (ts, jg) writes channels 32jg + 4ts + i, i = 0..3 (idx = 16wi + 4b + i);
-        // compile-time indices keep vacc in registers
-#pragma unroll
-        for (int idx = 0; idx < 32; ++idx)
-            if ((idx >> 2) == ts)
-                S.st_acc[2 * warp][32 * jg + idx] = vacc[idx] * __int_as_float((127 + 24 - 2 * (idx & 3)) << 23) + vb;
-        if (lane == 0) {
-            S.st_m[2 * warp] = m_run;
-            S.st_l[2 * warp] = l_w;
-        }
-    }
-
-    // ---- per-token path: tokens [max(t0, Qf), t1) (fp16 residual and partial tiles) ----
-    {
-        float m_g = -INFINITY, l_g = 0.f, ag[4] = {0.f, 0.f, 0.f, 0.f};
-        const int gstart = max(t0, fast_end);
-        const uint16_t *kres = P.k_res + bk * (int64_t)R * KVQ_D;
-        const uint16_t *vres = P.v_res + bk * (int64_t)R * KVQ_D;
-        for (int t = gstart + warp; t < t1; t += NCWARP) {
-            float kv[4], vv[4];
-            if (t < nKq) {
-                const int gi = t / G, tt = t % G;
-                const uint8_t *grp = kc_base + (int64_t)gi * ((int64_t)G * KVQ_D / 4);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = 4 * lane + i;
-                    const int code = (grp[kivi_key_byte_offset(tt, c)] >> (2 * (tt & 3))) & 3;
-                    const uint32_t szc = ksz_base[(int64_t)gi * KVQ_D + c];
-                    kv[i] = (float)code * h2f(lo16(szc)) + h2f(hi16(szc));
+            for (int i = 0; i < 32; ++i) vacc[i] = 0.f;
+            for (int s = 0; s < U.nstages; ++s, ++sg) {
+                const int slot = sg % NSTAGE;
+                ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
+                const int tile = s * NCWARP + warp;
+                if (ok && tile < U.nT) {
+                    const uint8_t *st = S.stage[slot];
+                    
+                    const uint32_t *ksz = reinterpret_cast<const uint32_t *>(st + KC_BYTES) + gl * KVQ_D;
+                    // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
+                    const uint4 szv = *reinterpret_cast<const uint4 *>(ksz + 4 * lane);
+                    *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
+                        make_float4(qp[0] * h2f(lo16(szv.x)), qp[1] * h2f(lo16(szv.y)), qp[2] * h2f(lo16(szv.z)),
+                                    qp[3] * h2f(lo16(szv.w)));
+                    const float cb = warp_sum(qa[0] * h2f(hi16(szv.x)) + qa[1] * h2f(hi16(szv.y)) +
+                                              qa[2] * h2f(hi16(szv.z)) + qa[3] * h2f(hi16(szv.w)));
+                    __syncwarp();
+                    // ---- key codes: tokens 4q..4q+3 (q = lane/4) x channels 32tq..32tq+31 ----
+                    const uint8_t *kt = st + warp * 1024;
+                    const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
+                    const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
+                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                    const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][tq * QK_ROW]);
+                    unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};     // fp32 pairs
+    #pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float4 qv = qs[k];                                 // channels 32tq + 4k + 0..3
+                        const uint32_t w0 = kw[k], w16 = kw[k] >> 16;          // bytes 0,1 | bytes 2,3 at bits 0..15
+                        const unsigned long long q01 = pack2f(qv.x, qv.y), q23 = pack2f(qv.z, qv.w);
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
+                            acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // channels 4k, 4k+1
+                            acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);   // channels 4k+2, 4k+3
+                        }
+                    }
+                    // transpose-reduce over the 4 lanes of the quad: lane keeps token 4q + tq (= lane)
+                    float score;
+                    {
+                        const float a0 = lo2f(acc2[0]) + hi2f(acc2[0]), a1 = lo2f(acc2[1]) + hi2f(acc2[1]);
+                        const float a2 = lo2f(acc2[2]) + hi2f(acc2[2]), a3 = lo2f(acc2[3]) + hi2f(acc2[3]);
+                        const bool h2 = (tq & 2) != 0;
+                        float k0 = h2 ? a2 : a0, k1 = h2 ? a3 : a1;
+                        k0 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a0 : a2, 2);
+                        k1 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a1 : a3, 2);
+                        const bool h1 = (tq & 1) != 0;
+                        score = (h1 ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, h1 ? k0 : k1, 1);
+                    }
+                    const float logit = score * lscale + cb;
+                    const float p = softmax_tile(logit, m_run, l_part, vbias, vacc);
+                    // ---- values: 4 passes of 8 tokens; lane = (token slot ts, channel block jg) ----
+                    const uint8_t *vc = st + KC_BYTES + KSZ_MAX + warp * 32 * (KVQ_D / 4);
+                    const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + KC_BYTES + KSZ_MAX + VC_BYTES) +
+                                          warp * 32 * ngv;
+    #pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int tau = 8 * r + ts;
+                        const float pt = __shfl_sync(0xFFFFFFFFu, p, tau);
+                        const uint32_t szt = vsz[tau * ngv + jv];
+                        const uint16_t pp = f2h_rn(pt * h2f(lo16(szt)));
+                        vbias += pt * h2f(hi16(szt));
+                        const uint2 uu = *reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8);
+                        const uint32_t uw[2] = {uu.x, uu.y};
+    #pragma unroll
+                        for (int wi = 0; wi < 2; ++wi) {
+                            const uint32_t w0 = uw[wi], w8 = uw[wi] >> 8;
+    #pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint32_t m = 0x00030003u << (2 * i);
+                                const uint32_t e = w0 & m, o = w8 & m;
+                                // channel 32jg + 16wi + 4b + i  ->  vacc[16wi + 4b + i]
+                                vacc[16 * wi + 0 + i] = fma_f16f32(lo16(e), pp, vacc[16 * wi + 0 + i]);
+                                vacc[16 * wi + 8 + i] = fma_f16f32(hi16(e), pp, vacc[16 * wi + 8 + i]);
+                                vacc[16 * wi + 4 + i] = fma_f16f32(lo16(o), pp, vacc[16 * wi + 4 + i]);
+                                vacc[16 * wi + 12 + i] = fma_f16f32(hi16(o), pp, vacc[16 * wi + 12 + i]);
+                            }
+                        }
+                    }
                 }
-            } else {
-                uint2 u = *reinterpret_cast<const uint2 *>(kres + (int64_t)(t % R) * KVQ_D + 4 * lane);
-                kv[0] = h2f(lo16(u.x)); kv[1] = h2f(hi16(u.x)); kv[2] = h2f(lo16(u.y)); kv[3] = h2f(hi16(u.y));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
-            if (t < nVq) {
-                const uint8_t byte = vc_base[(int64_t)t * (KVQ_D / 4) + lane];
-                const uint32_t szt = vsz_base[(int64_t)t * (KVQ_D / Gv) + (4 * lane) / Gv];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) vv[i] = (float)((byte >> (2 * i)) & 3) * h2f(lo16(szt)) + h2f(hi16(szt));
-            } else {
-                uint2 u = *reinterpret_cast<const uint2 *>(vres + (int64_t)(t % R) * KVQ_D + 4 * lane);
-                vv[0] = h2f(lo16(u.x)); vv[1] = h2f(hi16(u.x)); vv[2] = h2f(lo16(u.y)); vv[3] = h2f(hi16(u.y));
-            }
-            const float logit = warp_sum(qa[0] * kv[0] + qa[1] * kv[1] + qa[2] * kv[2] + qa[3] * kv[3]);
-            const float mn = fmaxf(m_g, logit);
-            const float sc = exp2f(m_g - mn);
-            const float p = exp2f(logit - mn);
-            l_g = l_g * sc + p;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ag[i] = ag[i] * sc + p * vv[i];
-            m_g = mn;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) S.st_acc[2 * warp + 1][4 * lane + i] = ag[i];
-        if (lane == 0) {
-            S.st_m[2 * warp + 1] = m_g;
-            S.st_l[2 * warp + 1] = l_g;
-        }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
 
-    // ---- merge the eight warp states, write (o_s, lse_s) ----
-    if (warp == 0) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < NSTATE; ++i) M = fmaxf(M, S.st_m[i]);
-        float l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-        if (M > -INFINITY) {
-#pragma unroll
-            for (int i = 0; i < NSTATE; ++i) {
-                const float w = S.st_m[i] > -INFINITY ? exp2f(S.st_m[i] - M) : 0.f;
-                l += w * S.st_l[i];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o[c] += w * S.st_acc[i][4 * lane + c];
+            // ---- warp state -> shared memory (channel order) ----
+            {
+                const float l_w = warp_sum(l_part);
+    #pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float v = vacc[i];
+                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+                    vacc[i] = v;
+                }
+                float vb = vbias;
+                vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
+                vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 8);
+                vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 16);
+                // lane (ts, jg) writes channels 32jg + 4ts + i (i = 0..3): vacc[4ts + i] * 2^(24-2i) + bias
+                float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    #pragma unroll
+                for (int t8 = 0; t8 < 8; ++t8)
+                    if (ts == t8)
+                        w4 = make_float4(vacc[4 * t8 + 0] * 0x1.0p24f, vacc[4 * t8 + 1] * 0x1.0p22f,
+                                         vacc[4 * t8 + 2] * 0x1.0p20f, vacc[4 * t8 + 3] * 0x1.0p18f);
+                w4.x += vb; w4.y += vb; w4.z += vb; w4.w += vb;
+                *reinterpret_cast<float4 *>(&S.st_acc[warp][32 * jg + 4 * ts]) = w4;
+                if (lane == 0) {
+                    S.st_m[warp] = m_run;
+                    S.st_l[warp] = l_w;
+                }
             }
         }
-        const int64_t row = ((int64_t)b * P.Hq + hq) * P.splits + split;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        float4 ov = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-        *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) = ov;
-        if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+        // ---- merge the four warp states, write (o_s, lse_s) of the unit ----
+        if (warp == 0) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i]);
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NCWARP; ++i) {
+                    const float w = S.st_m[i] > -INFINITY ? exp2f(S.st_m[i] - M) : 0.f;
+                    l += w * S.st_l[i];
+                    const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][4 * lane]);
+                    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+                }
+            }
+            const int64_t row = ((int64_t)U.b * P.Hq + U.hq) * P.splits + U.split;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
     }
 }
 
@@ -382,10 +490,12 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
     P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
     P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
     P.err = device_error_ptr();
+    P.B = c->batch;
     P.Hq = cfg->n_q_heads;
     P.Hkv = cfg->n_kv_heads;
     P.G = cfg->group_k;
     P.Gv = cfg->group_v;
+    P.ngv = KVQ_D / cfg->group_v;
     P.R = cfg->residual;
     P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
     P.splits = p.splits;
@@ -405,8 +515,10 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
         if (e != cudaSuccess) return e;
         attr_dev = dev;
     }
-    dim3 grid(p.splits, cfg->n_q_heads, c->batch);
-    kivi_decode_kernel<<<grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    const int64_t n_units = (int64_t)c->batch * cfg->n_q_heads * p.splits;
+    int64_t grid = (int64_t)num_sms() * 4;
+    if (grid > n_units) grid = n_units;
+    kivi_decode_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
     return cudaGetLastError();
 }
 

@@ -5,7 +5,8 @@
 #include <stdint.h>
 
 #define KVQ_D 128
-#define KVQ_SPIN_LIMIT (1u << 22)   // bounded mbarrier waits (each try_wait suspends a while)
+#define KVQ_SUSPEND_NS 20000u      // mbarrier try_wait suspend hint (ns)
+#define KVQ_SPIN_LIMIT (1u << 16)   // bounded mbarrier waits: about 1.3 s at most
 
 namespace kvq {
 
@@ -118,13 +119,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }"
                  ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
+// try_wait with a suspend-time hint: the thread sleeps (up to the hint, in ns)
+// until the phase completes instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(KVQ_SUSPEND_NS) : "memory");
     return ok != 0;
 }
-// Bounded wait: false (and the device error flag set) if the phase never completes.
+// Bounded wait (at most about KVQ_SPIN_LIMIT * KVQ_SUSPEND_NS): false, and the
+// device error flag set, if the phase never completes.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
     for (uint32_t i = 0; i < KVQ_SPIN_LIMIT; ++i)
         if (mbar_try_wait(bar, parity)) return true;
