@@ -72,6 +72,7 @@ def _load():
         "kv_decode_attn": (S, [cfgp, ctypes.POINTER(kvq_kivi_cache), _P, _P, _P, sz, _P]),
         "kv_decode_attn_kitty": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), _P, _P, _P, sz, _P]),
         "kv_decode_attn_int8": (S, [cfgp, ctypes.POINTER(kvq_int8_cache), _P, _P, _P, sz, _P]),
+        "kv_decode_attn_noalloc": (S, [cfgp, ctypes.POINTER(kvq_kivi_cache), _P, _P, _P]),
         "kv_decode_attn_stage1": (S, [cfgp, i32, _P, _P, _P, sz, _P]),
         "kv_decode_attn_merge": (S, [cfgp, i32, i32, i32, _P, sz, _P, _P]),
         "kvq_philox4x32_10": (S, [_P, _P, i64, _P, _P]),
@@ -90,7 +91,8 @@ _lib = _load()
 
 EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither",
             "kvq_kitty_key_page_bytes", "kvq_kitty_value_page_bytes", "kv_decode_attn_plan", "kv_decode_attn",
-            "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_stage1", "kv_decode_attn_merge",
+            "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_noalloc", "kv_decode_attn_stage1",
+            "kv_decode_attn_merge",
             "kvq_philox4x32_10", "kvq_get_device_error", "kvq_status_string", "kvq_version")
 
 
@@ -195,6 +197,12 @@ def kv_decode_attn_kitty(cfg, cache, q, out, workspace, workspace_bytes, stream=
 def kv_decode_attn_int8(cfg, cache, q, out, workspace, workspace_bytes, stream=None):
     _check(_lib.kv_decode_attn_int8(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out), _ptr(workspace),
                                     workspace_bytes, _stream(stream)), "kv_decode_attn_int8")
+
+
+def kv_decode_attn_noalloc(cfg, cache, q, out, stream=None):
+    """kv_decode_attn without a caller workspace (fixed scratch inside the library)."""
+    _check(_lib.kv_decode_attn_noalloc(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out), _stream(stream)),
+           "kv_decode_attn_noalloc")
 
 
 def kv_decode_attn_stage1(cfg, variant, cache, q, workspace, workspace_bytes, stream=None):

@@ -243,6 +243,26 @@ KVQ_API kvq_status kv_decode_attn_kitty(const kvq_config *cfg, const kvq_kitty_c
 KVQ_API kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_cache *cache, const void *q,
                                void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Allocation-free kv_decode_attn (no counterpart on the pages: an addition
+ * for callers that cannot provide a workspace, such as engines whose own
+ * pool owns all device memory or deployments that allow no device
+ * allocation after start-up).  Same computation and kernels as
+ * kv_decode_attn, with the split workspace in a fixed device array of
+ * KVQ_NOALLOC_SCRATCH_BYTES compiled into the library; it holds that memory
+ * on every GPU that loads the library until the process exits.
+ *   - Returns KVQ_ERR_WORKSPACE, launching nothing, when the planned
+ *     workspace (kv_decode_attn_plan) exceeds KVQ_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress); make that first call before any stream
+ *     capture on that device.
+ *   - Every call uses the same array: calls whose kernels can overlap on the
+ *     GPU (other streams, other host threads) race and must be serialized
+ *     by the caller.  No part of the array needs clearing between calls.
+ * It calls no cudaMalloc or cudaFree. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+KVQ_API kvq_status kv_decode_attn_noalloc(const kvq_config *cfg, const kvq_kivi_cache *cache, const void *q,
+                                          void *out, cudaStream_t stream);
+
 /* The two stages separately (kv_decode_attn* = stage1 then merge). */
 KVQ_API kvq_status kv_decode_attn_stage1(const kvq_config *cfg, int32_t variant, const void *cache,
                                  const void *q, void *workspace, size_t workspace_bytes,
