@@ -54,14 +54,15 @@ float sm_scale_of(const kvq_config *cfg) {
 }
 
 // Splits: chunks of a multiple of 128 tokens (the stage), sized so that the
-// persistent decode grid (4 CTAs per SM) gets about 8 units per CTA, within
+// persistent decode grid (4 CTAs per SM, 2 for INT8) gets about 8 units per CTA, within
 // [128, 4096] tokens and at most 256 + 1 splits per row (the last split of
 // a row holds the tokens outside the quantized tiles, e.g. the fp16 residual).
 kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
-    (void)variant;
     const int64_t rows = (int64_t)batch * cfg->n_q_heads;
-    const int64_t target_units = 8LL * num_sms() * 4;
-    int64_t chunk = (rows * max_seq_len + target_units - 1) / target_units;
+    // the INT8 kernel handles all query heads of a kv head in one unit, 2 CTAs per SM
+    const int64_t unit_rows = variant == KVQ_VARIANT_INT8 ? (int64_t)batch * cfg->n_kv_heads : rows;
+    const int64_t target_units = 8LL * num_sms() * (variant == KVQ_VARIANT_INT8 ? 2 : 4);
+    int64_t chunk = (unit_rows * max_seq_len + target_units - 1) / target_units;
     chunk = (chunk + 127) / 128 * 128;
     if (chunk < 128) chunk = 128;
     if (chunk > 4096) chunk = 4096;
@@ -242,6 +243,7 @@ static kvq_status stage1_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, 
     kvq_status s = check_kitty(cfg);
     if (s) return s;
     if (!c) return KVQ_ERR_INVALID_ARG;
+    if (cfg->boost_k > 92) return KVQ_ERR_UNSUPPORTED;   // key record must fit the decode stage slot
     if ((s = check_ws(cfg, KVQ_VARIANT_KITTY, c->batch, c->max_seq_len, ws, wsb, p))) return s;
     if ((s = ptrs_ok({q, c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local}))) return s;
     if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;

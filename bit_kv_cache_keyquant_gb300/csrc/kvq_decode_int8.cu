@@ -1,8 +1,407 @@
-// placeholder until the int8 decode kernel lands
+// a9: WitCert INT8 subtractive-dither decode attention, stage 1.
+//
+// K^ = s (code - xi) with s the block's per-channel fp16 scale and xi the
+// Philox4x32-10 dither regenerated from (request, layer, kv head, token,
+// channel) exactly as the write kernel drew it (WitCert sec. 6.1: the read
+// side uses the same five-tuple Philox as the write side).  The active
+// (incomplete) 256-token block stays fp16.
+//
+// The path is bound by integer ALU work (the Philox rounds), not HBM, so the
+// kernel computes every dither once per element and shares it across all
+// g <= 8 query heads of the kv head:
+//   * one CTA per (batch row, kv head, split) unit of a persistent grid; a
+//     producer warp streams 128-token stages (int8 K and V codes, 16 KiB
+//     each, plus the block's K and V scales) with cp.async.bulk into a
+//     2-slot mbarrier ring;
+//   * a consumer warp owns 32 tokens of a stage; lane l owns channels
+//     4l..4l+3, so one Philox call (counter word 1 = l) yields its four
+//     dithers per token (the "four-output reuse");
+//   * keys: per token, 8 head partials over the lane's 4 channels are
+//     reduce-scattered across the warp until every lane holds the 8 head
+//     scores of one token; per-head online softmax in base 2;
+//   * values: the 8 head weights of each token are broadcast through shared
+//     memory and accumulated into 8 x 4 fp32 accumulators per lane.
+// The last split of every row covers the fp16 tail with the same tile code.
+#include "kvq_device.cuh"
 #include "kvq_internal.h"
+
 namespace kvq {
-cudaError_t launch_decode_int8(const kvq_config *, const kvq_int8_cache *, const void *, const DecodePlan &, void *,
-                              cudaStream_t) {
-    return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int NSTAGE = 2;
+constexpr int NCWARP = 4;
+constexpr int STAGE_TOK = 32 * NCWARP;                 // 128 tokens
+constexpr int CODES_BYTES = STAGE_TOK * KVQ_D;         // 16 KiB per side
+constexpr int STAGE_BYTES = 2 * CODES_BYTES + 2 * KVQ_D * 2;
+constexpr int GMAX = 8;
+
+struct Smem {
+    uint8_t stage[NSTAGE][STAGE_BYTES];
+    uint64_t full[NSTAGE];
+    uint64_t empty[NSTAGE];
+    float pw[NCWARP][32][GMAX];            // per-warp softmax weights of the tile's 32 tokens
+    float st_acc[NCWARP][GMAX][KVQ_D];
+    float st_m[NCWARP][GMAX];
+    float st_l[NCWARP][GMAX];
+};
+
+struct Params {
+    const int32_t *seq_len;
+    const int32_t *req_id;
+    const int8_t *k_codes, *v_codes;
+    const uint16_t *k_scale, *v_scale, *k_tail, *v_tail;
+    const uint16_t *q;
+    float *ws_o, *ws_lse;
+    unsigned *err;
+    int B, Hq, Hkv, g, T, splits, chunk, blk_cap;
+    int64_t cap;
+    uint32_t ctr2_layer, k0, k1;
+    float alpha;
+};
+
+struct Unit {
+    int b, kvh, split, t0, t1, nq, L;
+    bool residual;
+    int64_t bk;
+};
+
+__device__ __forceinline__ Unit unit_of(const Params &P, int u) {
+    Unit U;
+    const int row = u / P.splits;
+    U.split = u - row * P.splits;
+    U.b = row / P.Hkv;
+    U.kvh = row - U.b * P.Hkv;
+    U.L = P.seq_len[U.b];
+    const int ntail = ((U.L - 1) % P.T) + 1;
+    U.nq = U.L - ntail;
+    U.residual = U.split == P.splits - 1;
+    if (U.residual) {
+        U.t0 = U.nq;
+        U.t1 = U.L;
+    } else {
+        U.t0 = U.split * P.chunk;
+        U.t1 = max(U.t0, min(U.t0 + P.chunk, U.nq));
+    }
+    U.bk = (int64_t)U.b * P.Hkv + U.kvh;
+    return U;
 }
+
+// dither of the four channels 4*lane..4*lane+3 of token t (exact: (w >> 8) 2^-24 - 1/2)
+__device__ __forceinline__ void dither4(uint32_t k0, uint32_t k1, uint32_t c2, uint32_t req, int t, int lane,
+                                        float xi[4]) {
+    const uint4 r = philox4x32_10(make_uint4((uint32_t)t, (uint32_t)lane, c2, req), k0, k1);
+    xi[0] = dither_from_word(r.x);
+    xi[1] = dither_from_word(r.y);
+    xi[2] = dither_from_word(r.z);
+    xi[3] = dither_from_word(r.w);
+}
+
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float f[4]) {
+    f[0] = (float)(int8_t)(w & 0xFF);
+    f[1] = (float)(int8_t)((w >> 8) & 0xFF);
+    f[2] = (float)(int8_t)((w >> 16) & 0xFF);
+    f[3] = (float)(int8_t)(w >> 24);
+}
+
+// Per-warp online softmax state for up to GMAX heads.
+struct HeadState {
+    float m[GMAX], l[GMAX], acc[GMAX][4];
+};
+
+// One tile of n <= 32 tokens starting at t0.  kfn(tt, kv[4]) / vfn(tt, vv[4])
+// return this lane's four dequantized channels of token t0 + tt; wk are the
+// key weights alpha q_hc.
+template <typename KF, typename VF>
+__device__ __forceinline__ void tile(int n, int g, const float wk[GMAX][4], KF kfn, VF vfn, HeadState &H,
+                                     float (*pw)[GMAX], int lane) {
+    float sc[GMAX];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) sc[h] = -INFINITY;
+    // ---- keys: 8 batches of 4 tokens; reduce-scatter over lane bits 4, 3 leaves token
+    //      2*b4 + b3 of a batch in lanes 8m..8m+7, then a sum over lane bits 2..0 ----
+#pragma unroll 1
+    for (int c4 = 0; c4 < 8; ++c4) {
+        float d[4][GMAX];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            float kv[4];
+            kfn(min(4 * c4 + m, n - 1), kv);
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h)
+                d[m][h] = wk[h][0] * kv[0] + wk[h][1] * kv[1] + wk[h][2] * kv[2] + wk[h][3] * kv[3];
+        }
+#pragma unroll
+        for (int o = 16, hh = 2; o >= 8; o >>= 1, hh >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int m = 0; m < hh; ++m)
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    const float send = up ? d[m][h] : d[m + hh][h];
+                    d[m][h] = (up ? d[m + hh][h] : d[m][h]) + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+                }
+        }
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            float v = d[0][h];
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+            const float mine = __shfl_sync(0xFFFFFFFFu, v, 8 * (lane & 3));
+            if ((lane >> 2) == c4 && lane < n) sc[h] = mine;
+        }
+    }
+    // ---- per-head online softmax (lane = token) ----
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+        float p = 0.f;
+        if (h < g) {
+            const float mt = warp_max(sc[h]);
+            if (mt > H.m[h]) {
+                const float s = exp2f(H.m[h] - mt);
+                H.l[h] *= s;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) H.acc[h][i] *= s;
+                H.m[h] = mt;
+            }
+            p = exp2f(sc[h] - H.m[h]);
+            H.l[h] += p;             // lane-partial; summed over the warp at the end
+        }
+        pw[lane][h] = p;
+    }
+    __syncwarp();
+    // ---- values: lane = channels, weights broadcast from shared memory ----
+#pragma unroll 4
+    for (int tt = 0; tt < 32; ++tt) {
+        if (tt >= n) break;
+        float vv[4];
+        vfn(tt, vv);
+        const float4 p0 = *reinterpret_cast<const float4 *>(&pw[tt][0]);
+        const float4 p1 = *reinterpret_cast<const float4 *>(&pw[tt][4]);
+        const float pp[GMAX] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) H.acc[h][i] += pp[h] * vv[i];
+    }
+    __syncwarp();
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Params P) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_units = P.B * P.Hkv * P.splits;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], NCWARP);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCWARP) {
+        if (lane == 0) {
+            bool ok = true;
+            int sg = 0;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit U = unit_of(P, u);
+                const int nst = U.residual ? 0 : (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
+                for (int s = 0; s < nst; ++s, ++sg) {
+                    const int slot = sg % NSTAGE;
+                    if (sg >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((sg / NSTAGE) - 1) & 1, P.err);
+                    if (!ok) break;
+                    const int tok = U.t0 + s * STAGE_TOK;
+                    const int nt = min(STAGE_TOK, U.t1 - tok);
+                    const int blk = tok / P.T;
+                    uint8_t *st = S.stage[slot];
+                    mbar_expect_tx(&S.full[slot], (uint32_t)(2 * nt * KVQ_D + 4 * KVQ_D));
+                    bulk_g2s(st, P.k_codes + (U.bk * P.cap + tok) * KVQ_D, nt * KVQ_D, &S.full[slot]);
+                    bulk_g2s(st + CODES_BYTES, P.v_codes + (U.bk * P.cap + tok) * KVQ_D, nt * KVQ_D, &S.full[slot]);
+                    bulk_g2s(st + 2 * CODES_BYTES, P.k_scale + (U.bk * P.blk_cap + blk) * KVQ_D, 2 * KVQ_D,
+                             &S.full[slot]);
+                    bulk_g2s(st + 2 * CODES_BYTES + 2 * KVQ_D, P.v_scale + (U.bk * P.blk_cap + blk) * KVQ_D, 2 * KVQ_D,
+                             &S.full[slot]);
+                }
+            }
+            for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
+        }
+        return;
+    }
+
+    const int g = P.g;
+    bool ok = true;
+    int sg = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        // alpha q of the g heads for this lane's four channels
+        float qa[GMAX][4];
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            const int hq = U.kvh * g + min(h, g - 1);
+            const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + hq) * KVQ_D + 4 * lane);
+            const float z = h < g ? P.alpha : 0.f;
+            qa[h][0] = h2f(lo16(qv.x)) * z;
+            qa[h][1] = h2f(hi16(qv.x)) * z;
+            qa[h][2] = h2f(lo16(qv.y)) * z;
+            qa[h][3] = h2f(hi16(qv.y)) * z;
+        }
+        HeadState H;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            H.m[h] = -INFINITY;
+            H.l[h] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) H.acc[h][i] = 0.f;
+        }
+        const uint32_t c2 = P.ctr2_layer | (uint32_t)U.kvh;
+        const uint32_t req = (uint32_t)P.req_id[U.b];
+        if (U.residual) {
+            const uint16_t *kt = P.k_tail + U.bk * (int64_t)P.T * KVQ_D + 4 * lane;
+            const uint16_t *vt = P.v_tail + U.bk * (int64_t)P.T * KVQ_D + 4 * lane;
+            const int T = P.T;
+            for (int r0 = U.t0 + 32 * warp; r0 < U.t1; r0 += 32 * NCWARP) {
+                const int n = min(32, U.t1 - r0);
+                auto kfn = [=](int tt, float kv[4]) {
+                    const uint2 x = __ldg(reinterpret_cast<const uint2 *>(kt + (int64_t)((r0 + tt) % T) * KVQ_D));
+                    kv[0] = h2f(lo16(x.x)); kv[1] = h2f(hi16(x.x)); kv[2] = h2f(lo16(x.y)); kv[3] = h2f(hi16(x.y));
+                };
+                auto vfn = [=](int tt, float vv[4]) {
+                    const uint2 x = __ldg(reinterpret_cast<const uint2 *>(vt + (int64_t)((r0 + tt) % T) * KVQ_D));
+                    vv[0] = h2f(lo16(x.x)); vv[1] = h2f(hi16(x.x)); vv[2] = h2f(lo16(x.y)); vv[3] = h2f(hi16(x.y));
+                };
+                tile(n, g, qa, kfn, vfn, H, S.pw[warp], lane);
+            }
+        } else {
+            const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
+            for (int s = 0; s < nst; ++s, ++sg) {
+                const int slot = sg % NSTAGE;
+                ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
+                const int tok = U.t0 + s * STAGE_TOK;
+                const int r0 = tok + 32 * warp;
+                const int n = min(32, U.t1 - r0);
+                if (ok && n > 0) {
+                    const uint8_t *st = S.stage[slot];
+                    const uint8_t *kc = st + 32 * warp * KVQ_D + 4 * lane;
+                    const uint8_t *vc = st + CODES_BYTES + 32 * warp * KVQ_D + 4 * lane;
+                    const uint2 ks = *reinterpret_cast<const uint2 *>(st + 2 * CODES_BYTES + 8 * lane);
+                    const uint2 vs = *reinterpret_cast<const uint2 *>(st + 2 * CODES_BYTES + 2 * KVQ_D + 8 * lane);
+                    const float ks0 = h2f(lo16(ks.x)), ks1 = h2f(hi16(ks.x)), ks2 = h2f(lo16(ks.y)), ks3 = h2f(hi16(ks.y));
+                    const float vs0 = h2f(lo16(vs.x)), vs1 = h2f(hi16(vs.x)), vs2 = h2f(lo16(vs.y)), vs3 = h2f(hi16(vs.y));
+                    const uint32_t k0 = P.k0, k1 = P.k1;
+                    auto kfn = [=](int tt, float kv[4]) {
+                        float c[4], xi[4];
+                        i8x4_to_f32(*reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c);
+                        dither4(k0, k1, c2, req, r0 + tt, lane, xi);
+                        kv[0] = ks0 * (c[0] - xi[0]);
+                        kv[1] = ks1 * (c[1] - xi[1]);
+                        kv[2] = ks2 * (c[2] - xi[2]);
+                        kv[3] = ks3 * (c[3] - xi[3]);
+                    };
+                    auto vfn = [=](int tt, float vv[4]) {
+                        float c[4], xi[4];
+                        i8x4_to_f32(*reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c);
+                        dither4(k0, k1, c2 | 0x10000u, req, r0 + tt, lane, xi);
+                        vv[0] = vs0 * (c[0] - xi[0]);
+                        vv[1] = vs1 * (c[1] - xi[1]);
+                        vv[2] = vs2 * (c[2] - xi[2]);
+                        vv[3] = vs3 * (c[3] - xi[3]);
+                    };
+                    tile(n, g, qa, kfn, vfn, H, S.pw[warp], lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
+            }
+        }
+        // ---- warp states -> shared memory ----
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            const float l_w = warp_sum(H.l[h]);
+            *reinterpret_cast<float4 *>(&S.st_acc[warp][h][4 * lane]) =
+                make_float4(H.acc[h][0], H.acc[h][1], H.acc[h][2], H.acc[h][3]);
+            if (lane == 0) {
+                S.st_m[warp][h] = H.m[h];
+                S.st_l[warp][h] = l_w;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+        // ---- merge the four warp states per head: warp w writes heads w, w + 4 ----
+        for (int h = warp; h < g; h += NCWARP) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i][h]);
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NCWARP; ++i) {
+                    const float w = S.st_m[i][h] > -INFINITY ? exp2f(S.st_m[i][h] - M) : 0.f;
+                    l += w * S.st_l[i][h];
+                    const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][h][4 * lane]);
+                    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+                }
+            }
+            const int hq = U.kvh * g + h;
+            const int64_t row = ((int64_t)U.b * P.Hq + hq) * P.splits + U.split;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+    }
+}
+
+cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *q, const DecodePlan &p,
+                               void *ws, cudaStream_t st) {
+    Params P;
+    P.seq_len = c->seq_len;
+    P.req_id = c->req_id;
+    P.k_codes = static_cast<const int8_t *>(c->k_codes);
+    P.v_codes = static_cast<const int8_t *>(c->v_codes);
+    P.k_scale = static_cast<const uint16_t *>(c->k_scale);
+    P.v_scale = static_cast<const uint16_t *>(c->v_scale);
+    P.k_tail = static_cast<const uint16_t *>(c->k_tail);
+    P.v_tail = static_cast<const uint16_t *>(c->v_tail);
+    P.q = static_cast<const uint16_t *>(q);
+    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
+    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
+    P.err = device_error_ptr();
+    P.B = c->batch;
+    P.Hq = cfg->n_q_heads;
+    P.Hkv = cfg->n_kv_heads;
+    P.g = cfg->n_q_heads / cfg->n_kv_heads;
+    P.T = cfg->int8_block;
+    P.splits = p.splits;
+    P.chunk = p.chunk;
+    P.cap = c->max_seq_len;
+    P.blk_cap = (c->max_seq_len + P.T - 1) / P.T;
+    if (P.blk_cap < 1) P.blk_cap = 1;
+    P.ctr2_layer = (uint32_t)c->layer << 17;
+    P.k0 = (uint32_t)(c->seed & 0xFFFFFFFFu);
+    P.k1 = (uint32_t)(c->seed >> 32);
+    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    if (P.g > GMAX) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(Smem);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
+    int64_t grid = (int64_t)num_sms() * 2;
+    if (grid > n_units) grid = n_units;
+    int8_decode_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
+}
+
 }  // namespace kvq

@@ -1,8 +1,457 @@
-// placeholder until the kitty decode kernel lands
+// a7: Kitty split-KV decode attention, stage 1.
+//
+// The cache of one (batch row, kv head): fp16 sink tokens [0, S); key pages
+// of G = 128 tokens (two 2-bit planes, boost index, per-channel s, z),
+// value pages (2-bit per-token codes, per-token s, z); an fp16 key Q-buffer,
+// value Q-buffer and value local window (Kitty, "Page Structure for Key
+// Cache", "Page Structure for Value Cache", "Stage 1: Inserting New KV
+// Vectors").  A key code is X = low | (high << 2), high taken from row
+// idx[c] of the high plane when idx[c] < K and 0 otherwise (Algorithm 1);
+// K^ = X s + z.
+//
+// Structure (same as the KIVI stage-1 kernel): a persistent grid over
+// (batch row, query head, split) units; a producer warp streams one page
+// (key record + value record, 9856 B at K = 16) per stage with
+// cp.async.bulk into a 4-slot mbarrier ring; four consumer warps each take
+// 32 tokens of the page.  A key tile gathers, for each lane, the bytes of
+// its 32 channels x 4 tokens from the row-major low plane into packed
+// words, plus one word from the high plane (4 boosted rows, weights 4 q s),
+// and runs the exact fp32 denormal-code x fma.rn.f32x2 dot of the KIVI
+// kernel.  Values use the exact fp32 token-major path (value_token_accum)
+// with one (s, z) per token.
+// The last split of every row covers every token outside whole pages of
+// both sides (sink, buffers, local window, a key page whose values are
+// still in fp16): one token per lane for the keys (per-lane independent
+// loads), four channels per lane for the values.
+#include "kvq_device.cuh"
 #include "kvq_internal.h"
+
 namespace kvq {
-cudaError_t launch_decode_kitty(const kvq_config *, const kvq_kitty_cache *, const void *, const DecodePlan &, void *,
-                              cudaStream_t) {
-    return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int NSTAGE = 4;
+constexpr int NCWARP = 4;
+constexpr int PG = 128;                    // tokens per page
+constexpr int STAGE_BYTES = 12288;
+constexpr int VREC_OFF = 7680;             // value record offset inside a stage (key record <= 7680 B)
+constexpr int QK_ROW = 36;
+constexpr int KMAX = 92;                   // boosted channels that fit the key-record slot
+
+struct Smem {
+    uint8_t stage[NSTAGE][STAGE_BYTES];
+    uint64_t full[NSTAGE];
+    uint64_t empty[NSTAGE];
+    float qk[NCWARP][4 * QK_ROW];         // per-warp pre-scaled alpha q s (low plane)
+    float hw[NCWARP][KMAX + 4];           // per-warp pre-scaled 4 alpha q s of the boosted rows
+    float qv[KVQ_D];                       // alpha q (residual unit)
+    float st_acc[NCWARP][KVQ_D];
+    float st_m[NCWARP];
+    float st_l[NCWARP];
+};
+
+struct Params {
+    const int32_t *seq_len;
+    const uint8_t *k_pages;
+    const uint8_t *v_pages;
+    const uint16_t *k_sink, *v_sink, *k_qbuf, *v_qbuf, *v_local;
+    const uint16_t *q;
+    float *ws_o, *ws_lse;
+    unsigned *err;
+    int B, Hq, Hkv, S, R, K, splits, chunk, page_cap;
+    int kpb, vpb;
+    float alpha;
+    int e0;
+};
+
+struct Unit {
+    int b, hq, split, p0, np, nKp, nVp, nkb, nvb, L;
+    bool residual;
+    int64_t bk;
+};
+
+__device__ __forceinline__ Unit unit_of(const Params &P, int u) {
+    Unit U;
+    const int row = u / P.splits;
+    U.split = u - row * P.splits;
+    U.b = row / P.Hq;
+    U.hq = row - U.b * P.Hq;
+    const int L = P.seq_len[U.b];
+    U.L = L;
+    if (L > P.S) {
+        U.nkb = ((L - P.S - 1) % PG) + 1;
+        U.nKp = (L - P.S - U.nkb) / PG;
+    } else {
+        U.nkb = 0;
+        U.nKp = 0;
+    }
+    const int E = max(0, L - P.S - P.R);
+    U.nvb = E > 0 ? ((E - 1) % PG) + 1 : 0;
+    U.nVp = (E - U.nvb) / PG;
+    const int Pf = min(U.nKp, U.nVp);                  // pages quantized on both sides
+    U.residual = U.split == P.splits - 1;
+    if (U.residual) {
+        U.p0 = Pf;
+        U.np = 0;
+    } else {
+        const int cpp = P.chunk / PG;
+        U.p0 = U.split * cpp;
+        U.np = max(0, min(U.p0 + cpp, Pf) - U.p0);
+    }
+    U.bk = (int64_t)U.b * P.Hkv + U.hq / (P.Hq / P.Hkv);
+    return U;
 }
+
+// Key of token t (residual unit), channel c, dequantized (fp32).
+__device__ __forceinline__ const uint8_t *key_page(const Params &P, const Unit &U, int p) {
+    return P.k_pages + (U.bk * P.page_cap + p) * (int64_t)P.kpb;
+}
+
+__device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias,
+                                              unsigned long long vacc2[16]) {
+    const float mt = warp_max(logit);
+    if (mt > m_run) {
+        const float sc = exp2f(m_run - mt);
+        l_part *= sc;
+        vbias *= sc;
+        scale_pairs(vacc2, sc);
+        m_run = mt;
+    }
+    const float p = exp2f(logit - m_run);
+    l_part += p;
+    return p;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Params P) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_units = P.B * P.Hq * P.splits;
+    const int K = P.K;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], NCWARP);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCWARP) {
+        if (lane == 0) {
+            bool ok = true;
+            int sg = 0;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit U = unit_of(P, u);
+                for (int s = 0; s < U.np; ++s, ++sg) {
+                    const int slot = sg % NSTAGE;
+                    if (sg >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((sg / NSTAGE) - 1) & 1, P.err);
+                    if (!ok) break;
+                    const int p = U.p0 + s;
+                    uint8_t *st = S.stage[slot];
+                    mbar_expect_tx(&S.full[slot], (uint32_t)(P.kpb + P.vpb));
+                    bulk_g2s(st, key_page(P, U, p), (uint32_t)P.kpb, &S.full[slot]);
+                    bulk_g2s(st + VREC_OFF, P.v_pages + (U.bk * P.page_cap + p) * (int64_t)P.vpb, (uint32_t)P.vpb,
+                             &S.full[slot]);
+                }
+            }
+            for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
+        }
+        return;
+    }
+
+    const int tq = lane & 3, qd = lane >> 2;
+    const int ts = lane >> 2, jg = lane & 3;
+    const float pe = __int_as_float((127 + 149 - P.e0) << 23), po = __int_as_float((127 + 141 - P.e0) << 23);
+    const float lscale = __int_as_float((127 + P.e0 - 2 * tq) << 23);
+    const int n_hgrp = (K + 15) / 16;          // groups of 16 boosted rows (4 per channel-block lane)
+    bool ok = true;
+    int sg = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        float qa[4];
+        {
+            const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D + 4 * lane);
+            qa[0] = h2f(lo16(qv.x)) * P.alpha;
+            qa[1] = h2f(hi16(qv.x)) * P.alpha;
+            qa[2] = h2f(lo16(qv.y)) * P.alpha;
+            qa[3] = h2f(hi16(qv.y)) * P.alpha;
+        }
+        if (U.residual) {
+            // ---------------- tokens outside whole pages ----------------
+            // token list: sink [0, nA), then [S + Pf*G, L)
+            const int nA = min(U.L, P.S);
+            const int tB = P.S + U.p0 * PG;
+            const int nB = max(0, U.L - tB);
+            const int ntok = nA + nB;
+            if (warp == 0) *reinterpret_cast<float4 *>(&S.qv[4 * lane]) = make_float4(qa[0], qa[1], qa[2], qa[3]);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+            float m_run = -INFINITY, l_part = 0.f, racc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint16_t *ksink = P.k_sink + U.bk * (int64_t)P.S * KVQ_D;
+            const uint16_t *vsink = P.v_sink + U.bk * (int64_t)P.S * KVQ_D;
+            const uint16_t *kqb = P.k_qbuf + U.bk * (int64_t)PG * KVQ_D;
+            const uint16_t *vqb = P.v_qbuf + U.bk * (int64_t)PG * KVQ_D;
+            const uint16_t *vloc = P.v_local + U.bk * (int64_t)P.R * KVQ_D;
+            const int vq_end = P.S + U.nVp * PG + U.nvb;           // value Q-buffer tokens end here
+            for (int i0 = 32 * warp; i0 < ntok; i0 += 32 * NCWARP) {
+                const int n = min(32, ntok - i0);
+                // ---- keys: lane = token ----
+                const int i = i0 + min(lane, n - 1);
+                const int t = i < nA ? i : tB + (i - nA);
+                float logit = 0.f;
+                if (t < P.S || t >= P.S + U.nKp * PG) {
+                    const uint16_t *row = t < P.S ? ksink + (int64_t)t * KVQ_D : kqb + (int64_t)((t - P.S) % PG) * KVQ_D;
+#pragma unroll 4
+                    for (int c8 = 0; c8 < 16; ++c8) {
+                        const uint4 u4 = __ldg(reinterpret_cast<const uint4 *>(row) + c8);
+                        const float4 qa0 = *reinterpret_cast<const float4 *>(&S.qv[8 * c8]);
+                        const float4 qa1 = *reinterpret_cast<const float4 *>(&S.qv[8 * c8 + 4]);
+                        logit += qa0.x * h2f(lo16(u4.x)) + qa0.y * h2f(hi16(u4.x)) + qa0.z * h2f(lo16(u4.y)) +
+                                 qa0.w * h2f(hi16(u4.y)) + qa1.x * h2f(lo16(u4.z)) + qa1.y * h2f(hi16(u4.z)) +
+                                 qa1.z * h2f(lo16(u4.w)) + qa1.w * h2f(hi16(u4.w));
+                    }
+                } else {
+                    const int p = (t - P.S) / PG, tt = (t - P.S) % PG;
+                    const uint8_t *pg = key_page(P, U, p);
+                    const uint8_t *low = pg, *high = pg + KVQ_D * PG / 4, *idx = high + (int64_t)K * PG / 4;
+                    const uint16_t *ps = reinterpret_cast<const uint16_t *>(idx + KVQ_D);
+                    for (int c = 0; c < KVQ_D; ++c) {
+                        int code = (low[c * (PG / 4) + tt / 4] >> (2 * (tt & 3))) & 3;
+                        const int r = idx[c];
+                        if (r < K) code |= ((high[r * (PG / 4) + tt / 4] >> (2 * (tt & 3))) & 3) << 2;
+                        logit += S.qv[c] * ((float)code * h2f(ps[c]) + h2f(ps[KVQ_D + c]));
+                    }
+                }
+                if (lane >= n) logit = -INFINITY;
+                const float mt = warp_max(logit);
+                if (mt > m_run) {
+                    const float sc = exp2f(m_run - mt);
+                    l_part *= sc;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) racc[k] *= sc;
+                    m_run = mt;
+                }
+                const float p = exp2f(logit - m_run);
+                l_part += p;
+                // ---- values: lane = channels 4*lane..4*lane+3; every value here is fp16 ----
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int ij = i0 + min(j, n - 1);
+                    const int tj = ij < nA ? ij : tB + (ij - nA);
+                    const uint16_t *vrow = tj < P.S ? vsink + (int64_t)tj * KVQ_D
+                                         : tj < vq_end ? vqb + (int64_t)((tj - P.S) % PG) * KVQ_D
+                                                       : vloc + (int64_t)(tj % P.R) * KVQ_D;
+                    const uint2 vv = __ldg(reinterpret_cast<const uint2 *>(vrow + 4 * lane));
+                    const float pj = __shfl_sync(0xFFFFFFFFu, p, j);        // 0 for j >= n
+                    racc[0] += pj * h2f(lo16(vv.x));
+                    racc[1] += pj * h2f(hi16(vv.x));
+                    racc[2] += pj * h2f(lo16(vv.y));
+                    racc[3] += pj * h2f(hi16(vv.y));
+                }
+            }
+            const float l_w = warp_sum(l_part);
+            *reinterpret_cast<float4 *>(&S.st_acc[warp][4 * lane]) = make_float4(racc[0], racc[1], racc[2], racc[3]);
+            if (lane == 0) {
+                S.st_m[warp] = m_run;
+                S.st_l[warp] = l_w;
+            }
+        } else {
+            const float qp[4] = {qa[0] * pe, qa[1] * po, qa[2] * pe, qa[3] * po};
+            float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
+            unsigned long long vacc2[16];
+#pragma unroll
+for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
+            for (int s = 0; s < U.np; ++s, ++sg) {
+                const int slot = sg % NSTAGE;
+                ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
+                if (ok) {
+                    const uint8_t *st = S.stage[slot];
+                    const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + K * PG / 4;
+                    const uint16_t *ps = reinterpret_cast<const uint16_t *>(idx + KVQ_D);
+                    // ---- pre-scaled weights of the page: low plane (channel order) and boosted rows ----
+                    {
+                        const uint2 s4 = *reinterpret_cast<const uint2 *>(ps + 4 * lane);
+                        const uint2 z4 = *reinterpret_cast<const uint2 *>(ps + KVQ_D + 4 * lane);
+                        const float sv[4] = {h2f(lo16(s4.x)), h2f(hi16(s4.x)), h2f(lo16(s4.y)), h2f(hi16(s4.y))};
+                        *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
+                            make_float4(qp[0] * sv[0], qp[1] * sv[1], qp[2] * sv[2], qp[3] * sv[3]);
+                        const uint32_t id4 = *reinterpret_cast<const uint32_t *>(idx + 4 * lane);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = (id4 >> (8 * i)) & 0xFF;
+                            // boosted row r sits at byte r & 3 of its gathered word: parity r & 1
+                            if (r < K) S.hw[warp][r] = 4.f * qa[i] * sv[i] * ((r & 1) ? po : pe);
+                        }
+                        for (int r = K + lane; r < n_hgrp * 16; r += 32) S.hw[warp][r] = 0.f;   // rows past K
+                    }
+                    const float cb = warp_sum(qa[0] * h2f(ps[KVQ_D + 4 * lane]) + qa[1] * h2f(ps[KVQ_D + 4 * lane + 1]) +
+                                              qa[2] * h2f(ps[KVQ_D + 4 * lane + 2]) +
+                                              qa[3] * h2f(ps[KVQ_D + 4 * lane + 3]));
+                    __syncwarp();
+                    // ---- key dot: tokens 32*warp + 4*qd + j, channels 32*tq .. 32*tq+31 ----
+                    const int col = 8 * warp + qd;                  // byte column of the token quad
+                    const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][tq * QK_ROW]);
+                    unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int c0 = 32 * tq + 4 * k;
+                        const uint32_t w = (uint32_t)low[(c0 + 0) * 32 + col] | ((uint32_t)low[(c0 + 1) * 32 + col] << 8) |
+                                           ((uint32_t)low[(c0 + 2) * 32 + col] << 16) |
+                                           ((uint32_t)low[(c0 + 3) * 32 + col] << 24);
+                        const float4 qv = qs[k];
+                        const uint32_t w16 = w >> 16;
+                        const unsigned long long q01 = pack2f(qv.x, qv.y), q23 = pack2f(qv.z, qv.w);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
+                            acc2[j] = ffma2(pack2u(w & m0, w & m1), q01, acc2[j]);
+                            acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
+                        }
+                    }
+                    // boosted rows 16*hg + 4*tq + b (b = 0..3): weights 4 alpha q s, zero past K
+                    for (int hg = 0; hg < n_hgrp; ++hg) {
+                        const int r0 = 16 * hg + 4 * tq;
+                        uint32_t w = 0;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            if (r0 + b < K) w |= (uint32_t)high[(r0 + b) * 32 + col] << (8 * b);
+                        const uint32_t w16 = w >> 16;
+                        const unsigned long long q01 = pack2f(S.hw[warp][r0], S.hw[warp][r0 + 1]);
+                        const unsigned long long q23 = pack2f(S.hw[warp][r0 + 2], S.hw[warp][r0 + 3]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
+                            acc2[j] = ffma2(pack2u(w & m0, w & m1), q01, acc2[j]);
+                            acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
+                        }
+                    }
+                    float score;
+                    {
+                        const float a0 = lo2f(acc2[0]) + hi2f(acc2[0]), a1 = lo2f(acc2[1]) + hi2f(acc2[1]);
+                        const float a2 = lo2f(acc2[2]) + hi2f(acc2[2]), a3 = lo2f(acc2[3]) + hi2f(acc2[3]);
+                        const bool h2 = (tq & 2) != 0;
+                        float k0 = h2 ? a2 : a0, k1 = h2 ? a3 : a1;
+                        k0 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a0 : a2, 2);
+                        k1 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a1 : a3, 2);
+                        const bool h1 = (tq & 1) != 0;
+                        score = (h1 ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, h1 ? k0 : k1, 1);
+                    }
+                    const float logit = score * lscale + cb;
+                    const float p = softmax_tile(logit, m_run, l_part, vbias, vacc2);
+                    // ---- values (token-major page, one (s, z) per token) ----
+                    const uint8_t *vrec = st + VREC_OFF;
+                    const uint8_t *vc = vrec + warp * 32 * (KVQ_D / 4);
+                    const uint16_t *vs = reinterpret_cast<const uint16_t *>(vrec + PG * KVQ_D / 4) + 32 * warp;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int tau = 8 * r + ts;
+                        const float pt = __shfl_sync(0xFFFFFFFFu, p, tau);
+                        vbias += pt * h2f(vs[PG + tau]);
+                        value_token_accum(*reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8), pt * h2f(vs[tau]), vacc2);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
+            }
+            // ---- warp state -> shared memory ----
+            const float l_w = warp_sum(l_part);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float a = lo2f(vacc2[i]), c = hi2f(vacc2[i]);
+            #pragma unroll
+                for (int o = 4; o <= 16; o <<= 1) {
+                    a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+                    c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+                }
+                vacc2[i] = pack2f(a, c);
+            }
+            float vb = vbias;
+            vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
+            vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 8);
+            vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 16);
+            float4 w4 = value_block_channels(vacc2, ts);
+            w4.x += vb; w4.y += vb; w4.z += vb; w4.w += vb;
+            *reinterpret_cast<float4 *>(&S.st_acc[warp][32 * jg + 4 * ts]) = w4;
+            if (lane == 0) {
+                S.st_m[warp] = m_run;
+                S.st_l[warp] = l_w;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+        if (warp == 0) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i]);
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NCWARP; ++i) {
+                    const float w = S.st_m[i] > -INFINITY ? exp2f(S.st_m[i] - M) : 0.f;
+                    l += w * S.st_l[i];
+                    const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][4 * lane]);
+                    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+                }
+            }
+            const int64_t row = ((int64_t)U.b * P.Hq + U.hq) * P.splits + U.split;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+    }
+}
+
+cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q, const DecodePlan &p,
+                                void *ws, cudaStream_t st) {
+    Params P;
+    P.seq_len = c->seq_len;
+    P.k_pages = static_cast<const uint8_t *>(c->k_pages);
+    P.v_pages = static_cast<const uint8_t *>(c->v_pages);
+    P.k_sink = static_cast<const uint16_t *>(c->k_sink);
+    P.v_sink = static_cast<const uint16_t *>(c->v_sink);
+    P.k_qbuf = static_cast<const uint16_t *>(c->k_qbuf);
+    P.v_qbuf = static_cast<const uint16_t *>(c->v_qbuf);
+    P.v_local = static_cast<const uint16_t *>(c->v_local);
+    P.q = static_cast<const uint16_t *>(q);
+    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
+    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
+    P.err = device_error_ptr();
+    P.B = c->batch;
+    P.Hq = cfg->n_q_heads;
+    P.Hkv = cfg->n_kv_heads;
+    P.S = cfg->sink;
+    P.R = cfg->residual;
+    P.K = cfg->boost_k;
+    P.splits = p.splits;
+    P.chunk = p.chunk;
+    P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + PG - 1) / PG;
+    if (P.page_cap < 1) P.page_cap = 1;
+    P.kpb = KVQ_D * PG / 4 + cfg->boost_k * PG / 4 + KVQ_D + 4 * KVQ_D;
+    P.vpb = PG * KVQ_D / 4 + 4 * PG;
+    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    P.e0 = 54 + (int)ceilf(log2f(P.alpha));
+    if (P.e0 < 22) P.e0 = 22;
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    if (P.kpb > VREC_OFF || P.K > KMAX) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(Smem);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kitty_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    const int64_t n_units = (int64_t)c->batch * cfg->n_q_heads * p.splits;
+    int64_t grid = (int64_t)num_sms() * 4;
+    if (grid > n_units) grid = n_units;
+    kitty_decode_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
+}
+
 }  // namespace kvq

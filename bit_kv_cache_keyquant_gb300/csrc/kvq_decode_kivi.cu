@@ -12,10 +12,11 @@
 // packed fma.rn.f32x2 multiplies it by alpha q s pre-scaled by 2^(149-k-E0);
 // every product is alpha q s code 2^(2j-E0), exact in fp32 (the fp32 weight
 // matters: a logit error is amplified by the softmax).
-// Values: the same masking read as fp16 subnormals (code * 2^(2i-24)), two
-// codes per LOP3, accumulated by fma.rn.f32.f16 with the fp16 weight
-// p_t s_tj (a weight's rounding is not amplified).
-// Powers of two are removed once per token (keys) or channel (values).
+// Values: the same masking (value_token_accum), with the weight p_t s_tj
+// pre-scaled per bit position, so value products are exact in fp32 as well
+// (s_tj code cancels against the zero point when the token's range is wide,
+// so an fp16 weight would lose 2^-12 of a term much larger than the result).
+// Powers of two are removed once per token (keys) or per unit (values).
 //
 // Work decomposition: a persistent grid walks the (batch row, query head,
 // split) units round-robin.  A producer warp streams every unit's 128-token
@@ -148,14 +149,14 @@ __device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, 
 
 // Online-softmax update of a warp state with one logit per lane (-inf for
 // empty lanes): returns p = 2^(logit - m) and rescales on a new maximum.
-__device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias, float vacc[32]) {
+__device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias,
+                                              unsigned long long vacc2[16]) {
     const float mt = warp_max(logit);
     if (mt > m_run) {
         const float sc = exp2f(m_run - mt);
         l_part *= sc;
         vbias *= sc;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) vacc[i] *= sc;
+        scale_pairs(vacc2, sc);
         m_run = mt;
     }
     const float p = exp2f(logit - m_run);
@@ -334,9 +335,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             // query pre-scaled by the byte-parity power of two of its channel (4*lane + i has parity i & 1)
             const float qp[4] = {qa[0] * pe, qa[1] * po, qa[2] * pe, qa[3] * po};
             float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
-            float vacc[32];
+            unsigned long long vacc2[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) vacc[i] = 0.f;
+for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
             for (int s = 0; s < U.nstages; ++s, ++sg) {
                 const int slot = sg % NSTAGE;
                 ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
                         score = (h1 ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, h1 ? k0 : k1, 1);
                     }
                     const float logit = score * lscale + cb;
-                    const float p = softmax_tile(logit, m_run, l_part, vbias, vacc);
+                    const float p = softmax_tile(logit, m_run, l_part, vbias, vacc2);
                     // ---- values: 4 passes of 8 tokens; lane = (token slot ts, channel block jg) ----
                     const uint8_t *vc = st + KC_BYTES + KSZ_MAX + warp * 32 * (KVQ_D / 4);
                     const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + KC_BYTES + KSZ_MAX + VC_BYTES) +
@@ -395,24 +396,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
                         const int tau = 8 * r + ts;
                         const float pt = __shfl_sync(0xFFFFFFFFu, p, tau);
                         const uint32_t szt = vsz[tau * ngv + jv];
-                        const uint16_t pp = f2h_rn(pt * h2f(lo16(szt)));
                         vbias += pt * h2f(hi16(szt));
-                        const uint2 uu = *reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8);
-                        const uint32_t uw[2] = {uu.x, uu.y};
-    #pragma unroll
-                        for (int wi = 0; wi < 2; ++wi) {
-                            const uint32_t w0 = uw[wi], w8 = uw[wi] >> 8;
-    #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const uint32_t m = 0x00030003u << (2 * i);
-                                const uint32_t e = w0 & m, o = w8 & m;
-                                // channel 32jg + 16wi + 4b + i  ->  vacc[16wi + 4b + i]
-                                vacc[16 * wi + 0 + i] = fma_f16f32(lo16(e), pp, vacc[16 * wi + 0 + i]);
-                                vacc[16 * wi + 8 + i] = fma_f16f32(hi16(e), pp, vacc[16 * wi + 8 + i]);
-                                vacc[16 * wi + 4 + i] = fma_f16f32(lo16(o), pp, vacc[16 * wi + 4 + i]);
-                                vacc[16 * wi + 12 + i] = fma_f16f32(hi16(o), pp, vacc[16 * wi + 12 + i]);
-                            }
-                        }
+                        value_token_accum(*reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8), pt * h2f(lo16(szt)), vacc2);
                     }
                 }
                 __syncwarp();
@@ -423,24 +408,21 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             {
                 const float l_w = warp_sum(l_part);
     #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float v = vacc[i];
-                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-                    vacc[i] = v;
+                for (int i = 0; i < 16; ++i) {
+                    float a = lo2f(vacc2[i]), c = hi2f(vacc2[i]);
+                #pragma unroll
+                    for (int o = 4; o <= 16; o <<= 1) {
+                        a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+                        c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+                    }
+                    vacc2[i] = pack2f(a, c);
                 }
                 float vb = vbias;
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 8);
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 16);
-                // lane (ts, jg) writes channels 32jg + 4ts + i (i = 0..3): vacc[4ts + i] * 2^(24-2i) + bias
-                float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    #pragma unroll
-                for (int t8 = 0; t8 < 8; ++t8)
-                    if (ts == t8)
-                        w4 = make_float4(vacc[4 * t8 + 0] * 0x1.0p24f, vacc[4 * t8 + 1] * 0x1.0p22f,
-                                         vacc[4 * t8 + 2] * 0x1.0p20f, vacc[4 * t8 + 3] * 0x1.0p18f);
+                // lane (ts, jg) writes channels 32jg + 4ts + i (i = 0..3) plus the zero-point term
+                float4 w4 = value_block_channels(vacc2, ts);
                 w4.x += vb; w4.y += vb; w4.z += vb; w4.w += vb;
                 *reinterpret_cast<float4 *>(&S.st_acc[warp][32 * jg + 4 * ts]) = w4;
                 if (lane == 0) {

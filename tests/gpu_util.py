@@ -35,3 +35,23 @@ def curand_philox():
         _curand.curand_philox_ref.restype = ctypes.c_int
         _curand.curand_philox_ref.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
     return _curand
+
+
+def attn_tol(want):
+    """Per-element tolerance of an fp16 attention output against the binary64
+    oracle: max-abs 2e-3, widened to one fp16 ulp of the oracle value where the
+    fp16 output grid itself is coarser than 2e-3 (|o| >= 4)."""
+    w = np.abs(np.asarray(want, np.float64))
+    ulp = np.spacing(w.astype(np.float16)).astype(np.float64)
+    return np.maximum(2e-3, ulp)
+
+
+def assert_attn_close(got, want, what=""):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert np.isfinite(got).all(), what
+    err = np.abs(got - want)
+    tol = attn_tol(want)
+    bad = err > tol
+    assert not bad.any(), f"{what}: {bad.sum()} elements out of tolerance, worst {err.max():.3e} " \
+                          f"(|o| there {np.abs(want).flat[err.argmax()]:.3f})"

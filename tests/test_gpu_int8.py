@@ -1,0 +1,115 @@
+"""GPU parity of the INT8 subtractive-dither decode path."""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_keyquant_gb300 import inputs as I
+from tests.gpu_util import assert_attn_close, lib
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def K():
+    return lib()
+
+
+def _run(K, cfg, Ks, Vs, q, reqs, max_seq_len, layer, seed):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hkv = len(Ks), len(Ks[0])
+    cache = C.Int8Cache(cfg, B, max_seq_len, layer=layer, seed=seed, device=DEV)
+    for b in range(B):
+        for h in range(Hkv):
+            cache.fill(b, h, torch.from_numpy(Ks[b][h]).to(DEV), torch.from_numpy(Vs[b][h]).to(DEV), int(reqs[b]))
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_INT8, B, max_seq_len)
+    ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device=DEV)
+    out = torch.full((B, cfg.n_q_heads, 128), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn_int8(cfg, cache.desc(), torch.from_numpy(q).to(DEV), out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    return out.float().cpu().numpy()
+
+
+def _oracle(orc, cfg, Ks, Vs, q, reqs, layer, seed):
+    g = cfg.n_q_heads // cfg.n_kv_heads
+    B, Hkv = len(Ks), len(Ks[0])
+    out = np.zeros((B, cfg.n_q_heads, 128))
+    for b in range(B):
+        for h in range(Hkv):
+            L = Ks[b][h].shape[0]
+            parts = orc.int8_build_one(Ks[b][h], Vs[b][h], seed, int(reqs[b]), layer, h)
+            out[b, h * g:(h + 1) * g] = orc.int8_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L, seed=seed,
+                                                            request=int(reqs[b]), layer=layer, kv_head=h)
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,lens", [
+    (8, 1, [1, 100, 256]),
+    (8, 1, [257, 511, 700]),
+    (6, 2, [1500, 300]),
+    (2, 2, [1024, 999]),
+])
+def test_int8_decode_parity(K, orc, Hq, Hkv, lens):
+    rng = np.random.default_rng(sum(lens) + Hq)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    Ks = [[(rng.standard_normal((L, 128)) * 10.0 ** rng.uniform(-1, 1, 128)).astype(np.float16) for _ in range(Hkv)]
+          for L in lens]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(Hkv)] for L in lens]
+    q = rng.standard_normal((len(lens), Hq, 128)).astype(np.float16)
+    reqs = rng.integers(0, 2 ** 31 - 1, len(lens))
+    layer, seed = 7, 0x0123456789ABCDEF
+    got = _run(K, cfg, Ks, Vs, q, reqs, max(lens) + 3, layer, seed)
+    assert_attn_close(got, _oracle(orc, cfg, Ks, Vs, q, reqs, layer, seed))
+
+
+def test_int8_batch_order_invariance(K, orc):
+    """Swapping batch rows together with their request ids swaps the outputs exactly."""
+    rng = np.random.default_rng(77)
+    cfg = K.make_config(n_q_heads=8, n_kv_heads=1)
+    lens = [900, 600]
+    Ks = [[rng.standard_normal((L, 128)).astype(np.float16)] for L in lens]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16)] for L in lens]
+    q = rng.standard_normal((2, 8, 128)).astype(np.float16)
+    reqs = np.array([11, 42])
+    a = _run(K, cfg, Ks, Vs, q, reqs, 900, 3, 5)
+    b = _run(K, cfg, Ks[::-1], Vs[::-1], q[::-1].copy(), reqs[::-1].copy(), 900, 3, 5)
+    assert np.array_equal(a, b[::-1])
+
+
+@pytest.mark.slow
+def test_int8_workload_full_size_sampled(K, orc):
+    """INT8 dither workload: B8, 64q/8kv, lengths U[16384, 65536]; sampled rows vs the oracle."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    w = I.WORKLOADS[5]
+    cfg = K.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
+    lens = I.seq_lens(w)
+    reqs = I.request_ids(w)
+    layer, seed = 5, w.seed
+    Lmax = int(lens.max())
+    cache = C.Int8Cache(cfg, w.batch, Lmax, layer=layer, seed=seed, device=DEV)
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            L = int(lens[b])
+            cache.fill(b, h, I.gen_kv_torch(w, I.T_K, b, h, L, DEV), I.gen_kv_torch(w, I.T_V, b, h, L, DEV),
+                       int(reqs[b]))
+    q = I.gen_q_torch(w, DEV)
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_INT8, w.batch, Lmax)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn_int8(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    qn = q.cpu().numpy()
+    g = w.n_q_heads // w.n_kv_heads
+    for b, h in ((0, 0), (w.batch - 1, w.n_kv_heads - 1), (3, 5)):
+        L = int(lens[b])
+        parts = orc.int8_build_one(I.gen_kv_np(w, I.T_K, b, h, L), I.gen_kv_np(w, I.T_V, b, h, L), seed,
+                                   int(reqs[b]), layer, h)
+        want = orc.int8_decode_one(qn[b, h * g:(h + 1) * g], *parts, L=L, seed=seed, request=int(reqs[b]),
+                                   layer=layer, kv_head=h)
+        assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
+        # the int8 codes and scales written on the GPU are bit-exact
+        assert np.array_equal(cache.k_codes[b, h, :256].cpu().numpy(), parts[0][:256])
+        assert np.array_equal(cache.v_scale[b, h, 1].cpu().numpy().view(np.uint16), parts[3][1])

@@ -1,0 +1,98 @@
+"""GPU parity of the Kitty decode path (pages quantized on the GPU, attention
+vs the oracle's binary64 result, max-abs 2e-3)."""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_keyquant_gb300 import inputs as I
+from tests.gpu_util import assert_attn_close, lib, max_abs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def K():
+    return lib()
+
+
+def _run(K, cfg, Ks, Vs, q, max_seq_len, score_mode=0):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hkv = len(Ks), len(Ks[0])
+    cache = C.KittyCache(cfg, B, max_seq_len, device=DEV)
+    for b in range(B):
+        for h in range(Hkv):
+            cache.fill(b, h, torch.from_numpy(Ks[b][h]).to(DEV), torch.from_numpy(Vs[b][h]).to(DEV), score_mode)
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KITTY, B, max_seq_len)
+    ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device=DEV)
+    out = torch.full((B, cfg.n_q_heads, 128), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn_kitty(cfg, cache.desc(), torch.from_numpy(q).to(DEV), out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    return out.float().cpu().numpy()
+
+
+def _oracle(orc, cfg, Ks, Vs, q, score_mode=0):
+    g = cfg.n_q_heads // cfg.n_kv_heads
+    B, Hkv = len(Ks), len(Ks[0])
+    out = np.zeros((B, cfg.n_q_heads, 128))
+    for b in range(B):
+        for h in range(Hkv):
+            L = Ks[b][h].shape[0]
+            parts = orc.kitty_build_one(Ks[b][h], Vs[b][h], 128, cfg.boost_k, cfg.sink, cfg.residual, score_mode)
+            out[b, h * g:(h + 1) * g] = orc.kitty_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L, K=cfg.boost_k,
+                                                             S=cfg.sink, R=cfg.residual)
+    return out
+
+
+@pytest.mark.parametrize("lens,Kb,mode", [
+    ([1, 20, 33], 16, 0),
+    ([161, 288, 416], 16, 0),
+    ([417, 700, 2000], 16, 0),
+    ([1500, 3000], 32, 0),
+    ([1500, 2222], 16, 1),
+    ([900, 1300], 0, 0),
+])
+def test_kitty_decode_parity(K, orc, lens, Kb, mode):
+    rng = np.random.default_rng(sum(lens) + Kb + mode)
+    cfg = K.make_config(n_q_heads=8, n_kv_heads=2, group_k=128, sink=32, residual=128, boost_k=Kb)
+    sig = 10.0 ** rng.uniform(-0.3, 0.9, (2, 128))
+    Ks = [[(rng.standard_normal((L, 128)) * sig[h]).astype(np.float16) for h in range(2)] for L in lens]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for h in range(2)] for L in lens]
+    q = rng.standard_normal((len(lens), 8, 128)).astype(np.float16)
+    got = _run(K, cfg, Ks, Vs, q, max(lens) + 7, mode)
+    want = _oracle(orc, cfg, Ks, Vs, q, mode)
+    assert_attn_close(got, want)
+
+
+@pytest.mark.slow
+def test_kitty_workload_full_size_sampled(K, orc):
+    """Qwen3-8B-shaped mixed key workload (B16, 32q/8kv, L=131072); sampled rows vs the oracle."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    w = I.WORKLOADS[4]
+    cfg = K.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group_k=128, sink=32, residual=128,
+                        boost_k=16)
+    L = w.seq_len
+    cache = C.KittyCache(cfg, w.batch, L, device=DEV)
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            cache.fill(b, h, I.gen_kv_torch(w, I.T_K, b, h, L, DEV), I.gen_kv_torch(w, I.T_V, b, h, L, DEV))
+    q = I.gen_q_torch(w, DEV)
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KITTY, w.batch, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn_kitty(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    assert np.isfinite(outn).all()
+    qn = q.cpu().numpy()
+    g = w.n_q_heads // w.n_kv_heads
+    for b, h in ((0, 0), (w.batch - 1, w.n_kv_heads - 1), (7, 3)):
+        Kn = I.gen_kv_np(w, I.T_K, b, h, L)
+        Vn = I.gen_kv_np(w, I.T_V, b, h, L)
+        parts = orc.kitty_build_one(Kn, Vn)
+        want = orc.kitty_decode_one(qn[b, h * g:(h + 1) * g], *parts, L=L)
+        assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
+        # the key pages written on the GPU are bit-exact too
+        assert np.array_equal(cache.k_pages[b, h, 5].cpu().numpy(), parts[0][5])

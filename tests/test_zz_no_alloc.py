@@ -12,9 +12,8 @@ import ctypes
 import numpy as np
 import pytest
 
-from tests.gpu_util import lib, max_abs
+from tests.gpu_util import assert_attn_close, lib, max_abs
 
-ATOL = 2e-3
 
 
 @pytest.fixture(scope="module")
@@ -60,4 +59,4 @@ def test_noalloc_matches_workspace_call_twice(K):
     r = ref.float().cpu().numpy()
     for o in outs:
         assert np.isfinite(o).all()
-        assert max_abs(o, r) <= ATOL
+        assert_attn_close(o, r)
