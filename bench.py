@@ -45,8 +45,14 @@ def _peaks():
 
 
 def _workload_desc(w):
-    return (f"{w.name}: batch {w.batch}, {w.n_q_heads} query / {w.n_kv_heads} KV heads, head_dim 128, "
-            f"{w.seq_len} cached tokens, K2V2 (key per-channel G=32, value per-token Gv=32), R=128")
+    base = f"{w.name}: batch {w.batch}, {w.n_q_heads} query / {w.n_kv_heads} KV heads, head_dim 128, "
+    if w.variant == "kivi":
+        return base + f"{w.seq_len} cached tokens, K2V2 (key per-channel G=32, value per-token Gv=32), R=128"
+    if w.variant == "kitty":
+        return base + (f"{w.seq_len} cached tokens, Kitty pages G=128, 16 of 128 key channels boosted to 4 bit "
+                       f"(two 2-bit planes), value 2 bit, sink 32, local 128")
+    return base + (f"lengths U[{w.min_seq_len}, {w.seq_len}], INT8 K and V with Philox4x32-10 subtractive dither, "
+                   f"fp16 scale per 256-token block and channel, fp16 active block")
 
 
 # ---------------------------------------------------------------------------
@@ -157,53 +163,109 @@ def run_reference(args, w):
 # ---------------------------------------------------------------------------
 # GPU leg
 # ---------------------------------------------------------------------------
-def build_kivi_state(w, device):
+def build_state(w, device):
+    """Device-resident cache of the workload plus the per-step write-side inputs."""
     import torch
     from bit_kv_cache_keyquant_gb300 import cache as C
     from bit_kv_cache_keyquant_gb300 import kvq
-    cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
-    L = w.seq_len
-    cache = C.KiviCache(cfg, w.batch, L, device=device)
+    lens = I.seq_lens(w)
+    Lmax = int(lens.max())
+    if w.variant == "kivi":
+        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
+        cache = C.KiviCache(cfg, w.batch, Lmax, device=device)
+        variant = kvq.KVQ_VARIANT_KIVI
+    elif w.variant == "kitty":
+        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group_k=128, sink=32, residual=128,
+                              boost_k=16)
+        cache = C.KittyCache(cfg, w.batch, Lmax, device=device)
+        variant = kvq.KVQ_VARIANT_KITTY
+    else:
+        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
+        cache = C.Int8Cache(cfg, w.batch, Lmax, layer=5, seed=w.seed, device=device)
+        variant = kvq.KVQ_VARIANT_INT8
+    reqs = I.request_ids(w)
     for b in range(w.batch):
+        L = int(lens[b])
         for h in range(w.n_kv_heads):
-            cache.fill(b, h, I.gen_kv_torch(w, I.T_K, b, h, L, device), I.gen_kv_torch(w, I.T_V, b, h, L, device))
+            K = I.gen_kv_torch(w, I.T_K, b, h, L, device)
+            V = I.gen_kv_torch(w, I.T_V, b, h, L, device)
+            if w.variant == "int8":
+                cache.fill(b, h, K, V, int(reqs[b]))
+            else:
+                cache.fill(b, h, K, V)
     q = I.gen_q_torch(w, device)
-    # per-step write-side inputs: one value token per (b, kv head) and the amortized key flush
-    n_vtok = w.batch * w.n_kv_heads
-    n_kgrp = max(1, w.batch * w.n_kv_heads * (cfg.residual // cfg.group_k) // cfg.residual)
-    vnew = I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_vtok, 128, device)
-    knew = I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_kgrp * cfg.group_k, 128, device)
-    scratch = {
-        "vcodes": torch.empty((n_vtok, 32), dtype=torch.uint8, device=device),
-        "vsz": torch.empty((n_vtok, 128 // cfg.group_v), dtype=torch.int32, device=device),
-        "kcodes": torch.empty((n_kgrp, cfg.group_k * 32), dtype=torch.uint8, device=device),
-        "ksz": torch.empty((n_kgrp, 128), dtype=torch.int32, device=device),
-    }
-    n_splits, wsb = kvq.kv_decode_attn_plan(cfg, kvq.KVQ_VARIANT_KIVI, w.batch, L)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
-    out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float16, device=device)
+    pairs = w.batch * w.n_kv_heads
+    st = dict(w=w, cfg=cfg, cache=cache, desc=cache.desc(), q=q, lens=lens, variant=variant)
+    # per-step write-side inputs (the amortized quantization work of one decode step)
+    if w.variant == "kivi":
+        n_vtok = pairs                                                      # one value token per (b, kv head)
+        n_kgrp = max(1, pairs * (cfg.residual // cfg.group_k) // cfg.residual)   # 1/R of the key flushes
+        st.update(n_vtok=n_vtok, n_kgrp=n_kgrp,
+                  vnew=I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_vtok, 128, device),
+                  knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_kgrp * cfg.group_k, 128, device),
+                  scratch=[torch.empty((n_vtok, 32), dtype=torch.uint8, device=device),
+                           torch.empty((n_vtok, 128 // cfg.group_v), dtype=torch.int32, device=device),
+                           torch.empty((n_kgrp, cfg.group_k * 32), dtype=torch.uint8, device=device),
+                           torch.empty((n_kgrp, 128), dtype=torch.int32, device=device)])
+    elif w.variant == "kitty":
+        n_pg = max(1, pairs // 128)                                         # 1/G of the page flushes
+        st.update(n_pg=n_pg, knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_pg * 128, 128, device),
+                  vnew=I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_pg * 128, 128, device),
+                  scratch=[torch.empty((n_pg, kvq.kvq_kitty_key_page_bytes(cfg)), dtype=torch.uint8, device=device),
+                           torch.empty((n_pg, kvq.kvq_kitty_value_page_bytes(cfg)), dtype=torch.uint8,
+                                       device=device)])
+    else:
+        n_blk = max(1, (pairs + 255) // 256)                                # 1/T of the block flushes, rounded up
+        st.update(n_blk=n_blk, knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_blk * 256, 128, device),
+                  vnew=I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_blk * 256, 128, device),
+                  blk_meta=[torch.zeros(n_blk, dtype=torch.int32, device=device) for _ in range(3)],
+                  scratch=[torch.empty((n_blk, 256, 128), dtype=torch.int8, device=device),
+                           torch.empty((n_blk, 128), dtype=torch.float16, device=device)])
+    n_splits, wsb = kvq.kv_decode_attn_plan(cfg, variant, w.batch, Lmax)
+    st.update(ws=torch.empty(wsb, dtype=torch.uint8, device=device), wsb=wsb, n_splits=n_splits,
+              out=torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float16, device=device), Lmax=Lmax)
     torch.cuda.synchronize()
-    return dict(cfg=cfg, cache=cache, desc=cache.desc(), q=q, vnew=vnew, knew=knew, n_vtok=n_vtok, n_kgrp=n_kgrp,
-                scratch=scratch, ws=ws, wsb=wsb, out=out, n_splits=n_splits)
+    return st
 
 
-def kivi_step(st, stream, ev=None, q=None, vnew=None, knew=None):
+def quant_step(st, stream, vnew=None, knew=None):
+    """The step's write-side kernels (amortized quantization of the new tokens)."""
     from bit_kv_cache_keyquant_gb300 import kvq
-    cfg, sc = st["cfg"], st["scratch"]
+    w, cfg, sc = st["w"], st["cfg"], st["scratch"]
+    vnew = st["vnew"] if vnew is None else vnew
+    knew = st["knew"] if knew is None else knew
+    if w.variant == "kivi":
+        kvq.kv_quant_value(cfg, vnew, st["n_vtok"], sc[0], sc[1], stream)
+        kvq.kv_quant_key(cfg, knew, st["n_kgrp"], sc[2], sc[3], stream)
+    elif w.variant == "kitty":
+        kvq.kv_quant_key_kitty(cfg, knew, st["n_pg"], 0, sc[0], stream)
+        kvq.kv_quant_value_kitty(cfg, vnew, st["n_pg"], sc[1], stream)
+    else:
+        m = st["blk_meta"]
+        for sel, x in ((0, knew), (1, vnew)):
+            kvq.kv_quant_int8_dither(cfg, x, st["n_blk"], m[0], m[1], m[2], 5, sel, w.seed, sc[0], sc[1], stream)
+
+
+def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None):
+    from bit_kv_cache_keyquant_gb300 import kvq
+    cfg = st["cfg"]
     if ev is not None:
         ev[0].record(stream)
-    kvq.kv_quant_value(cfg, st["vnew"] if vnew is None else vnew, st["n_vtok"], sc["vcodes"], sc["vsz"], stream)
-    kvq.kv_quant_key(cfg, st["knew"] if knew is None else knew, st["n_kgrp"], sc["kcodes"], sc["ksz"], stream)
+    quant_step(st, stream, vnew, knew)
     if ev is not None:
         ev[1].record(stream)
-    kvq.kv_decode_attn_stage1(cfg, kvq.KVQ_VARIANT_KIVI, st["desc"], st["q"] if q is None else q, st["ws"],
-                              st["wsb"], stream)
+    kvq.kv_decode_attn_stage1(cfg, st["variant"], st["desc"], st["q"] if q is None else q, st["ws"], st["wsb"],
+                              stream)
     if ev is not None:
         ev[2].record(stream)
-    kvq.kv_decode_attn_merge(cfg, kvq.KVQ_VARIANT_KIVI, st["cache"].batch, st["cache"].max_seq_len, st["ws"],
-                             st["wsb"], st["out"], stream)
+    kvq.kv_decode_attn_merge(cfg, st["variant"], st["cache"].batch, st["cache"].max_seq_len, st["ws"], st["wsb"],
+                             st["out"], stream)
     if ev is not None:
         ev[3].record(stream)
+
+
+def launches_per_step(w) -> int:
+    return {"kivi": 4, "kitty": 4, "int8": 4}[w.variant]
 
 
 def run_gpu(args, w, rank, world, local_rank):
@@ -213,12 +275,12 @@ def run_gpu(args, w, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    st = build_kivi_state(w, dev)
+    st = build_state(w, dev)
     stream = torch.cuda.current_stream(dev)
 
     # ---- kernel-only timing: inputs resident in HBM (458 MB/step > 129 MB L2) ----
     for _ in range(args.warmup):
-        kivi_step(st, stream)
+        decode_step(st, stream)
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
@@ -229,7 +291,7 @@ def run_gpu(args, w, rank, world, local_rank):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(args.steps):
-            kivi_step(st, stream, evs[i])
+            decode_step(st, stream, evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
@@ -251,7 +313,7 @@ def run_gpu(args, w, rank, world, local_rank):
     qd, vd, kd = torch.empty_like(st["q"]), torch.empty_like(st["vnew"]), torch.empty_like(st["knew"])
     for _ in range(args.warmup):
         qd.copy_(qh, non_blocking=True); vd.copy_(vh, non_blocking=True); kd.copy_(kh, non_blocking=True)
-        kivi_step(st, stream, q=qd, vnew=vd, knew=kd)
+        decode_step(st, stream, q=qd, vnew=vd, knew=kd)
         outh.copy_(st["out"], non_blocking=True)
     torch.cuda.synchronize()
     if world > 1:
@@ -260,7 +322,7 @@ def run_gpu(args, w, rank, world, local_rank):
     e0.record(stream)
     for _ in range(args.steps):
         qd.copy_(qh, non_blocking=True); vd.copy_(vh, non_blocking=True); kd.copy_(kh, non_blocking=True)
-        kivi_step(st, stream, q=qd, vnew=vd, knew=kd)
+        decode_step(st, stream, q=qd, vnew=vd, knew=kd)
         outh.copy_(st["out"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -274,7 +336,7 @@ def run_gpu(args, w, rank, world, local_rank):
 
     if rank != 0:
         return
-    lens = [w.seq_len] * w.batch
+    lens = st["lens"]
     cache_bytes = st["cache"].nbytes_read(lens)
     q_bytes = w.batch * w.n_q_heads * 128 * 2
     alg_bytes_stage1 = cache_bytes + q_bytes
@@ -284,11 +346,11 @@ def run_gpu(args, w, rank, world, local_rank):
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     traffic = None
     if os.path.exists(prof):
-        tr = json.load(open(prof)).get("kivi_decode_kernel@workload2")
-        if tr and tr.get("source_hash") == kernel_source_hash():
+        tr = json.load(open(prof)).get(f"{KERNEL_NAME[w.variant]}@workload{w.index}")
+        if tr and tr.get("source_hash") == kernel_source_hash(w.variant):
             traffic = tr["bytes_per_launch"]
     cpu = None
-    if world == 1 and not args.no_cpu:
+    if world == 1 and not args.no_cpu and w.variant == "kivi":
         per_pair, n = oracle_step_seconds(w, args.cpu_budget)
         cpu = {"value": per_pair * w.batch * w.n_kv_heads * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} (batch row, kv head) pairs of the workload, single thread, scaled by "
@@ -298,29 +360,35 @@ def run_gpu(args, w, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u2 codes + fp16 scales, fp32 accumulate", "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE[w.variant], "data": "synthetic",
         "config": {"workload": _workload_desc(w), "batch": w.batch, "q_heads": w.n_q_heads,
                    "kv_heads": w.n_kv_heads, "head_dim": 128, "seq_len": w.seq_len, "parallelism": f"replicas x{world}",
-                   "splits": st["n_splits"], "l2": "inputs larger than L2 (458 MB read per step vs 129 MB L2)"},
-        "breakdown_us": {"quant_value+key": 1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
+                   "splits": st["n_splits"],
+                   "l2": f"inputs larger than L2 ({cache_bytes / 1e6:.0f} MB read per step vs 129 MB L2)"},
+        "breakdown_us": {"quant_writes": 1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
                          "merge": 1e3 * statistics.mean(merge_ms)},
         "hbm_gbs_step": (alg_bytes_stage1 + d2h) / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "kivi_decode_kernel (a3 stage 1)",
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": KERNEL_NAME[w.variant] + " (stage 1)",
                      "alg_bytes_per_launch": alg_bytes_stage1},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms * 1e3 / args.steps / (world if world > 1 else 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line))
 
 
-def kernel_source_hash() -> str:
+KERNEL_NAME = {"kivi": "kivi_decode_kernel", "kitty": "kitty_decode_kernel", "int8": "int8_decode_kernel"}
+DTYPE = {"kivi": "u2 codes + fp16 scales, fp32 accumulate", "kitty": "u2 planes + fp16 scales, fp32 accumulate",
+         "int8": "s8 codes + Philox dither + fp16 scales, fp32 accumulate"}
+
+
+def kernel_source_hash(variant: str = "kivi") -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kvq_decode_kivi.cu", "kvq_device.cuh"):
+    for f in (f"kvq_decode_{variant}.cu", "kvq_device.cuh"):
         h.update(open(os.path.join(ROOT, "bit_kv_cache_keyquant_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -331,7 +399,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=2, choices=[2])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                    help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
@@ -343,7 +412,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            run_reference(args, w)
+            if w.variant != "kivi":
+                print(json.dumps({"impl": "reference", "unavailable": "the reference leg times the KIVI workloads"}))
+            else:
+                run_reference(args, w)
         return
     import torch
     if world > 1:
