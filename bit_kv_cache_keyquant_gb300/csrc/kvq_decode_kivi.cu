@@ -112,8 +112,19 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u) {
     return U;
 }
 
+// KIVI key storage (see kv_quant_key): token t = q + 8p, channel c = 16k + cc
+// with cc = 2r + e + 8h sits in bits 2p of byte e + 2h of word k%4 of chunk
+// 4q + r of half k/4 of its 32-token tile; the group's (s, z) block is 128
+// fp16 scales then 128 fp16 zeros in the order r*32 + 4k + e + 2h.
 __device__ __forceinline__ int kivi_key_byte_offset(int t, int c) {
-    return (t >> 5) * 1024 + ((c >> 4) & 1) * 512 + (4 * ((t & 31) >> 2) + (c >> 5)) * 16 + ((c >> 2) & 3) * 4 + (c & 3);
+    const int k = c >> 4, cc = c & 15;
+    return (t >> 5) * 1024 + (k >> 2) * 512 + (4 * (t & 7) + ((cc & 7) >> 1)) * 16 + (k & 3) * 4 + (cc & 1) +
+           2 * (cc >> 3);
+}
+
+__device__ __forceinline__ int kivi_sz_index(int c) {
+    const int k = c >> 4, cc = c & 15;
+    return ((cc & 7) >> 1) * 32 + k * 4 + (cc & 1) + 2 * (cc >> 3);
 }
 
 // Four dequantized key / value channels 4*lane..4*lane+3 of token t, from the
@@ -122,12 +133,12 @@ __device__ __forceinline__ void fetch_k4(const Params &P, const Unit &U, int t, 
     if (t < U.nKq) {
         const int G = P.G, gi = t / G, tt = t - gi * G;
         const uint8_t *grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D / 4);
-        const uint4 sz = *reinterpret_cast<const uint4 *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D + 4 * lane);
-        const uint32_t s4[4] = {sz.x, sz.y, sz.z, sz.w};
+        const uint16_t *szb = reinterpret_cast<const uint16_t *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int code = (grp[kivi_key_byte_offset(tt, 4 * lane + i)] >> (2 * (tt & 3))) & 3;
-            kv[i] = (float)code * h2f(lo16(s4[i])) + h2f(hi16(s4[i]));
+            const int c = 4 * lane + i, si = kivi_sz_index(c);
+            const int code = (grp[kivi_key_byte_offset(tt, c)] >> (2 * ((tt & 31) >> 3))) & 3;
+            kv[i] = (float)code * h2f(szb[si]) + h2f(szb[KVQ_D + si]);
         }
     } else {
         const uint2 u = *reinterpret_cast<const uint2 *>(P.k_res + (U.bk * P.R + t % P.R) * KVQ_D + 4 * lane);
@@ -231,8 +242,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit U = unit_of(P, u);
         float qa[4];
+        const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D;
         {
-            const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D + 4 * lane);
+            const uint2 qv = *reinterpret_cast<const uint2 *>(qrow + 4 * lane);
             qa[0] = h2f(lo16(qv.x)) * P.alpha;
             qa[1] = h2f(hi16(qv.x)) * P.alpha;
             qa[2] = h2f(lo16(qv.y)) * P.alpha;
@@ -332,8 +344,19 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
                 S.st_l[warp] = l_w;
             }
         } else {
-            // query pre-scaled by the byte-parity power of two of its channel (4*lane + i has parity i & 1)
-            const float qp[4] = {qa[0] * pe, qa[1] * po, qa[2] * pe, qa[3] * po};
+            // lane writes weight-table entries 4*lane..4*lane+3: chunk row r = lane/8, word k = lane%8,
+            // channels 16k + 2r + {0, 1, 8, 9}; query pre-scaled by the byte-parity power of two
+            float qf[4];
+            {
+                const int c0 = 16 * (lane & 7) + 2 * (lane >> 3);
+                const uint32_t q01 = *reinterpret_cast<const uint32_t *>(qrow + c0);
+                const uint32_t q89 = *reinterpret_cast<const uint32_t *>(qrow + c0 + 8);
+                qf[0] = h2f(lo16(q01)) * P.alpha;
+                qf[1] = h2f(hi16(q01)) * P.alpha;
+                qf[2] = h2f(lo16(q89)) * P.alpha;
+                qf[3] = h2f(hi16(q89)) * P.alpha;
+            }
+            const float qp[4] = {qf[0] * pe, qf[1] * po, qf[2] * pe, qf[3] * po};
             float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
             unsigned long long vacc2[16];
 #pragma unroll
@@ -345,16 +368,17 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];
                     
-                    const uint32_t *ksz = reinterpret_cast<const uint32_t *>(st + KC_BYTES) + gl * KVQ_D;
+                    const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + KC_BYTES) + gl * 2 * KVQ_D;
                     // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
-                    const uint4 szv = *reinterpret_cast<const uint4 *>(ksz + 4 * lane);
+                    const uint2 sv = *reinterpret_cast<const uint2 *>(ksz + 4 * lane);
+                    const uint2 zv = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + 4 * lane);
                     *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
-                        make_float4(qp[0] * h2f(lo16(szv.x)), qp[1] * h2f(lo16(szv.y)), qp[2] * h2f(lo16(szv.z)),
-                                    qp[3] * h2f(lo16(szv.w)));
-                    const float cb = warp_sum(qa[0] * h2f(hi16(szv.x)) + qa[1] * h2f(hi16(szv.y)) +
-                                              qa[2] * h2f(hi16(szv.z)) + qa[3] * h2f(hi16(szv.w)));
+                        make_float4(qp[0] * h2f(lo16(sv.x)), qp[1] * h2f(hi16(sv.x)), qp[2] * h2f(lo16(sv.y)),
+                                    qp[3] * h2f(hi16(sv.y)));
+                    const float cb = warp_sum(qf[0] * h2f(lo16(zv.x)) + qf[1] * h2f(hi16(zv.x)) +
+                                              qf[2] * h2f(lo16(zv.y)) + qf[3] * h2f(hi16(zv.y)));
                     __syncwarp();
-                    // ---- key codes: tokens 4q..4q+3 (q = lane/4) x channels 32tq..32tq+31 ----
+                    // ---- key codes: tokens q + 8j (q = lane/4) x channels 16k + 2tq + {0,1,8,9} ----
                     const uint8_t *kt = st + warp * 1024;
                     const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
                     const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
@@ -363,17 +387,17 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};     // fp32 pairs
     #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float4 qv = qs[k];                                 // channels 32tq + 4k + 0..3
-                        const uint32_t w0 = kw[k], w16 = kw[k] >> 16;          // bytes 0,1 | bytes 2,3 at bits 0..15
+                        const float4 qv = qs[k];                                 // channels 16k + 2tq + {0,1,8,9}
+                        const uint32_t w0 = kw[k], w16 = kw[k] >> 16;          // channels +0,+1 | +8,+9 at bits 0..15
                         const unsigned long long q01 = pack2f(qv.x, qv.y), q23 = pack2f(qv.z, qv.w);
     #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
-                            acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // channels 4k, 4k+1
-                            acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);   // channels 4k+2, 4k+3
+                            acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // even, odd channel
+                            acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
                         }
                     }
-                    // transpose-reduce over the 4 lanes of the quad: lane keeps token 4q + tq (= lane)
+                    // transpose-reduce over the 4 lanes of the quad: lane keeps token q + 8tq
                     float score;
                     {
                         const float a0 = lo2f(acc2[0]) + hi2f(acc2[0]), a1 = lo2f(acc2[1]) + hi2f(acc2[1]);
@@ -394,7 +418,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
     #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const int tau = 8 * r + ts;
-                        const float pt = __shfl_sync(0xFFFFFFFFu, p, tau);
+                        const float pt = __shfl_sync(0xFFFFFFFFu, p, 4 * ts + r);   // token tau = ts + 8r
                         const uint32_t szt = vsz[tau * ngv + jv];
                         vbias += pt * h2f(hi16(szt));
                         value_token_accum(*reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8), pt * h2f(lo16(szt)), vacc2);

@@ -14,13 +14,22 @@ namespace kvq {
 // a1: KIVI key groups.  One CTA (4 warps) per group of G = 32*NT tokens;
 // warp w owns channels [32w, 32w+32); lane t holds token t of every 32-token
 // tile.  Per-channel min / max is a warp-shuffle reduce-scatter that leaves
-// lane l with channel 32w + l; codes are packed in registers and OR-reduced
-// across the four lanes of a token quad, then stored as 16-byte chunks in
-// the tile layout (KIVI section 3.3; Kitty Observation 1 formula).
+// lane l with channel 32w + l; codes are packed in registers, OR-reduced
+// across the four lanes t, t^8, t^16, t^24 that share a byte, and stored as
+// 8-byte pieces of the tile layout (KIVI section 3.3; Kitty Observation 1
+// formula).  Tile layout: token t = q + 8p, channel c = 16k + 2r + e + 8h
+// sits in bits 2p of byte e + 2h of word k%4 of chunk 4q + r of half k/4.
+// The (s, z) block of a group is 128 fp16 scales then 128 fp16 zeros, both
+// in the order r*32 + 4k + e + 2h.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int kivi_sz_index(int c) {
+    const int k = c >> 4, cc = c & 15;
+    return ((cc & 7) >> 1) * 32 + k * 4 + (cc & 1) + 2 * (cc >> 3);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
-                                                             uint8_t *__restrict__ codes, uint32_t *__restrict__ sz) {
+                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz) {
     const int64_t g = blockIdx.x;
     if (g >= n_groups) return;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -71,33 +80,42 @@ __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__r
     uint16_t s, z;
     affine_fit(mn[0], mx[0], 3, s, z);
     const uint32_t my_sz = (uint32_t)s | ((uint32_t)z << 16);
-    sz[g * KVQ_D + 32 * w + lane] = my_sz;
+    {
+        const int si = kivi_sz_index(32 * w + lane);
+        sz[g * 2 * KVQ_D + si] = s;
+        sz[g * 2 * KVQ_D + KVQ_D + si] = z;
+    }
 
-    const int q = lane >> 2, j = lane & 3;
+    const int q = lane & 7, p = lane >> 3;
 #pragma unroll
     for (int tt = 0; tt < NT; ++tt) {
-        uint32_t word[8];
+        // word[r][kk]: chunk row r, channel block 16*(2w+kk); byte e + 2h, bits 2p
+        uint32_t word[4][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) word[i] = 0;
+        for (int i = 0; i < 4; ++i) word[i][0] = word[i][1] = 0;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
             uint32_t szc = __shfl_sync(0xFFFFFFFFu, my_sz, c);
             float sf = h2f(lo16(szc)), zf = h2f(hi16(szc));
             float x = h2f((c & 1) ? hi16(xv[tt][c >> 1]) : lo16(xv[tt][c >> 1]));
             uint32_t code = (uint32_t)affine_code(x, zf, sf, 3);
-            word[c >> 2] |= code << (8 * (c & 3) + 2 * j);
+            const int kk = c >> 4, cc = c & 15;
+            word[(cc & 7) >> 1][kk] |= code << (8 * ((cc & 1) + 2 * (cc >> 3)) + 2 * p);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            word[i] |= __shfl_xor_sync(0xFFFFFFFFu, word[i], 1);
-            word[i] |= __shfl_xor_sync(0xFFFFFFFFu, word[i], 2);
-        }
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 8);
+                word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 16);
+            }
+        // the four lanes of token octet q store chunk rows r = p: 8 bytes each
+        uint2 v = make_uint2(word[0][0], word[0][1]);
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+            if (p == i) v = make_uint2(word[i][0], word[i][1]);
         uint8_t *tile = codes + g * (int64_t)G * KVQ_D / 4 + tt * 1024;
-        if (j < 2) {
-            uint4 v = j == 0 ? make_uint4(word[0], word[1], word[2], word[3])
-                             : make_uint4(word[4], word[5], word[6], word[7]);
-            *reinterpret_cast<uint4 *>(tile + j * 512 + (4 * q + w) * 16) = v;
-        }
+        *reinterpret_cast<uint2 *>(tile + (w >> 1) * 512 + (4 * q + p) * 16 + (w & 1) * 8) = v;
     }
 }
 
@@ -323,14 +341,14 @@ cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t 
     if (n_groups == 0) return cudaSuccess;
     const uint16_t *kp = static_cast<const uint16_t *>(k);
     uint8_t *cp = static_cast<uint8_t *>(codes);
-    uint32_t *zp = static_cast<uint32_t *>(sz);
+    uint16_t *zp = static_cast<uint16_t *>(sz);
     // one CTA per group; grids above 2^31-1 groups are split into launches
     for (int64_t g0 = 0; g0 < n_groups; g0 += 0x7FFFFFFF) {
         int64_t n = n_groups - g0 < 0x7FFFFFFF ? n_groups - g0 : 0x7FFFFFFF;
         const int G = cfg->group_k;
         const uint16_t *ks = kp + g0 * (int64_t)G * KVQ_D;
         uint8_t *cs = cp + g0 * (int64_t)G * KVQ_D / 4;
-        uint32_t *zs = zp + g0 * KVQ_D;
+        uint16_t *zs = zp + g0 * 2 * KVQ_D;
         if (G == 32) quant_key_kivi_kernel<1><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
         else if (G == 64) quant_key_kivi_kernel<2><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
         else quant_key_kivi_kernel<4><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);

@@ -33,13 +33,15 @@
  *
  * Byte layouts (D = 128):
  *   KIVI key group (G tokens, G % 32 == 0): G*D/4 bytes made of G/32 tiles of
- *     1024 bytes.  Token t, channel c of the group has its 2-bit code in bits
- *     2*(t%4) of the byte at
- *       (t/32)*1024 + ((c>>4)&1)*512 + (4*((t%32)/4) + (c>>5))*16
- *       + ((c>>2)&3)*4 + (c&3)
- *     so that lane 4q+j of a warp finds tokens 4q..4q+3 of channels
- *     32j..32j+31 in the 16-byte chunks lane and lane+32 of each tile.
- *     Parameters: fp16x2 (s, z) [D] per group.
+ *     1024 bytes.  Within a tile write token t = q + 8p (q = t%8) and
+ *     channel c = 16k + cc, cc = 2r + e + 8h (r = (cc%8)/2, e = cc%2,
+ *     h = cc/8).  The 2-bit code sits in bits 2p of the byte at
+ *       (t/32)*1024 + (k/4)*512 + (4q + r)*16 + (k%4)*4 + (e + 2h)
+ *     so a byte holds tokens q, q+8, q+16, q+24 of one channel, and lane
+ *     4q + r of a warp finds all of its tokens {q + 8p} x channels
+ *     {16k + 2r + {0,1,8,9}} in the 16-byte chunks lane and lane + 32.
+ *     Parameters: 256 fp16 per group, the 128 scales then the 128 zeros,
+ *     channel c at index r*32 + 4k + e + 2h of each half.
  *   KIVI value token: D/4 bytes, channel c in bits 2*(c%4) of byte c/4.
  *     Parameters: fp16x2 (s, z) [D/Gv] per token.
  *   Kitty key page (G = 128 tokens, K boosted channels), one record of
@@ -104,7 +106,7 @@ typedef struct {
 /* a1: quantize n_groups KIVI key groups.
  *   k       fp16 [n_groups][G][D], token-major (as the K projection emits it)
  *   codes   uint8 [n_groups][G*D/4]  (tile layout above)
- *   sz      fp16x2 [n_groups][D]
+ *   sz      fp16 [n_groups][2*D]     (scales then zeros, order above)
  * Per channel over the group's G tokens: z = fp16 round-down(min),
  * s = fp16 round-up(fp32 (max - z) / 3), raised by one fp16 step while
  * z + 3s < max; code = clamp(rint((x - z) / s), 0, 3) in fp32 with the
@@ -181,7 +183,7 @@ typedef struct {
     int32_t max_seq_len;     /* token capacity CAP = max_seq_len rounded up to a multiple of 128 */
     const int32_t *seq_len;  /* [B] */
     const void *k_codes;     /* uint8  [B][Hkv][CAP/G][G*D/4] */
-    const void *k_sz;        /* fp16x2 [B][Hkv][CAP/G][D] */
+    const void *k_sz;        /* fp16 [B][Hkv][CAP/G][2*D]: scales, then zeros (layout above) */
     const void *v_codes;     /* uint8  [B][Hkv][CAP][D/4] */
     const void *v_sz;        /* fp16x2 [B][Hkv][CAP][D/Gv] */
     const void *k_res;       /* fp16   [B][Hkv][R][D] */

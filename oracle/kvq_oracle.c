@@ -196,21 +196,30 @@ ORC_API void orc_kivi_key_codes(int D, int G, int bits, const uint16_t *x, long 
     }
 }
 
-/* Byte offset, inside one packed 2-bit KIVI key group, of the byte that
- * holds token t (bits 2*(t%4)) of channel c.  Layout (D = 128, G a
- * multiple of 32): the group is G/32 tiles of 1024 bytes; in a tile,
- * q = (t%32)/4 selects a token quad, and the bytes of quad q are spread so
- * that the 16-byte chunk (4q + c/32) of each 512-byte half holds channels
- * 32*(c/32) + 16*h + [0,16) with h = (c/16)%2 choosing the half. */
+/* Storage of a packed 2-bit KIVI key group (D = 128, G a multiple of 32).
+ * The group is G/32 tiles of 1024 bytes.  Inside a tile, token t and
+ * channel c are split as
+ *   t = q + 8p        (q = t%8, p = (t%32)/8: the code sits in bits 2p)
+ *   c = 16k + cc      (k = c/16), cc = 2r + e + 8h (r = (cc%8)/2, e = cc%2,
+ *                                                    h = cc/8)
+ * and the byte is number (e + 2h) of word k%4 in the 16-byte chunk
+ * 4q + r of the 512-byte half k/4.  A byte therefore holds four tokens
+ * q, q+8, q+16, q+24 of one channel, and the chunks 4q+r of both halves
+ * hold tokens {q, q+8, q+16, q+24} x channels {16k+2r, 16k+2r+1, 16k+2r+8,
+ * 16k+2r+9 : k = 0..7}: 32 contiguous bytes per (q, r). */
 ORC_API long orc_kivi_key_byte_offset(int t, int c)
 {
     long tile = t / 32;
-    long q = (t % 32) / 4;
-    long half = (c >> 4) & 1;
-    long chunk = 4 * q + (c >> 5);
-    long word = (c >> 2) & 3;
-    long byte = c & 3;
-    return tile * 1024 + half * 512 + chunk * 16 + word * 4 + byte;
+    long q = t % 8;
+    long k = c / 16, cc = c % 16;
+    long r = (cc % 8) / 2, e = cc % 2, h = cc / 8;
+    return tile * 1024 + (k / 4) * 512 + (4 * q + r) * 16 + (k % 4) * 4 + (e + 2 * h);
+}
+
+/* Bit position of token t inside its key byte. */
+ORC_API int orc_kivi_key_bit(int t)
+{
+    return 2 * ((t % 32) / 8);
 }
 
 ORC_API int orc_kivi_key_pack(int D, int G, const uint8_t *codes, long n_grp, uint8_t *packed)
@@ -223,14 +232,38 @@ ORC_API int orc_kivi_key_pack(int D, int G, const uint8_t *codes, long n_grp, ui
         for (int t = 0; t < G; ++t)
             for (int c = 0; c < D; ++c) {
                 int code = codes[(g * G + t) * (long)D + c] & 3;
-                packed[g * gbytes + orc_kivi_key_byte_offset(t, c)] |= (uint8_t)(code << (2 * (t % 4)));
+                packed[g * gbytes + orc_kivi_key_byte_offset(t, c)] |= (uint8_t)(code << orc_kivi_key_bit(t));
             }
+    return 0;
+}
+
+/* Storage index of channel c's scale (and, 128 entries later, its zero) in
+ * a KIVI key group's parameter block of 128 fp16 scales followed by 128
+ * fp16 zeros: the same (r, k, e + 2h) order as the code chunks, so that the
+ * 32 channels of chunk row r are 32 consecutive entries. */
+ORC_API int orc_kivi_key_sz_index(int c)
+{
+    int k = c / 16, cc = c % 16;
+    int r = (cc % 8) / 2, e = cc % 2, h = cc / 8;
+    return r * 32 + k * 4 + e + 2 * h;
+}
+
+/* sz: fp16 pairs [n_grp][D][2] -> stored blocks [n_grp][2*D]. */
+ORC_API int orc_kivi_key_sz_pack(int D, const uint16_t *sz, long n_grp, uint16_t *stored)
+{
+    if (D != 128)
+        return 1;
+    for (long g = 0; g < n_grp; ++g)
+        for (int c = 0; c < D; ++c) {
+            stored[g * 2 * D + orc_kivi_key_sz_index(c)] = sz[(g * D + c) * 2 + 0];
+            stored[g * 2 * D + D + orc_kivi_key_sz_index(c)] = sz[(g * D + c) * 2 + 1];
+        }
     return 0;
 }
 
 static int kivi_key_code_at(const uint8_t *group_bytes, int t, int c)
 {
-    return (group_bytes[orc_kivi_key_byte_offset(t, c)] >> (2 * (t % 4))) & 3;
+    return (group_bytes[orc_kivi_key_byte_offset(t, c)] >> orc_kivi_key_bit(t)) & 3;
 }
 
 /* ------------------------------------------------------------------ */

@@ -61,7 +61,10 @@ def _declare(l):
         "orc_affine_dequant": (D, [I, U16, U16]),
         "orc_kivi_key_codes": (None, [I, I, I, P, L, P, P]),
         "orc_kivi_key_byte_offset": (L, [I, I]),
+        "orc_kivi_key_bit": (I, [I]),
         "orc_kivi_key_pack": (I, [I, I, P, L, P]),
+        "orc_kivi_key_sz_index": (I, [I]),
+        "orc_kivi_key_sz_pack": (I, [I, P, L, P]),
         "orc_kivi_value_codes": (None, [I, I, I, P, L, P, P]),
         "orc_tokenmajor_pack": (None, [I, P, L, P]),
         "orc_kitty_key_page_bytes": (L, [I, I, I]),
@@ -146,6 +149,23 @@ def kivi_key_pack(codes: np.ndarray) -> np.ndarray:
 
 def kivi_key_byte_offset(t: int, c: int) -> int:
     return lib().orc_kivi_key_byte_offset(t, c)
+
+
+def kivi_key_bit(t: int) -> int:
+    return lib().orc_kivi_key_bit(t)
+
+
+def kivi_key_sz_index(c: int) -> int:
+    return lib().orc_kivi_key_sz_index(c)
+
+
+def kivi_key_sz_pack(sz: np.ndarray) -> np.ndarray:
+    """sz uint16 [n_grp][D][2] (scale, zero) -> stored blocks uint16 [n_grp][2*D]."""
+    n, Dm, _ = sz.shape
+    out = np.zeros((n, 2 * Dm), np.uint16)
+    if lib().orc_kivi_key_sz_pack(Dm, _p(np.ascontiguousarray(sz)), n, _p(out)):
+        raise ValueError("KIVI key parameter packing needs D == 128")
+    return out
 
 
 def kivi_quant_key(x: np.ndarray, bits: int = 2):

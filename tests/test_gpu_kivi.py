@@ -55,7 +55,7 @@ def test_quant_key_bitexact(K, orc, G, kind):
     torch.cuda.synchronize()
     ref_codes, ref_sz = orc.kivi_quant_key(x)
     assert np.array_equal(codes.cpu().numpy(), ref_codes)
-    assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, 128, 2), ref_sz)
+    assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, 256), orc.kivi_key_sz_pack(ref_sz))
 
 
 @pytest.mark.parametrize("Gv", [32, 64, 128])
@@ -200,6 +200,7 @@ def test_workload_full_size_sampled(K, orc, widx):
     # quantized codes of a sampled group are bit-exact at full size too
     kc, ksz = orc.kivi_quant_key(I.gen_kv_np(w, I.T_K, 1, 0, 64)[None, :32])
     assert np.array_equal(cache.k_codes[1, 0, 0].cpu().numpy(), kc[0])
+    assert np.array_equal(cache.k_sz[1, 0, 0].cpu().numpy().view(np.uint16), orc.kivi_key_sz_pack(ksz)[0])
 
 
 # ---------------------------------------------------------------------------

@@ -151,15 +151,24 @@ def test_kivi_key_layout_is_a_lane_friendly_bijection(orc):
     for t in range(64):
         for c in range(128):
             off = orc.kivi_key_byte_offset(t, c)
-            seen.setdefault(off, set()).add((t // 4, c))
-            # lane 4q + c/32 of a warp finds tokens 4q..4q+3 of its 32 channels
-            # in 16-byte chunks lane and lane + 32 of the 32-token tile
-            q = (t % 32) // 4
-            lane = 4 * q + c // 32
-            chunk = (off % 1024) // 16
-            assert chunk in (lane, lane + 32)
-    assert sorted(seen) == list(range(2048))
+            seen.setdefault((off, orc.kivi_key_bit(t)), set()).add((t, c))
+            # a byte holds tokens q, q+8, q+16, q+24 of one channel (q = t % 8);
+            # the 32 bytes of (q, r) are chunk 4q+r of each 512-byte half and
+            # cover channels 16k + 2r + {0, 1, 8, 9}, k = 0..7, in word k % 4
+            q, r, k = t % 8, (c % 8) // 2, c // 16
+            assert (off % 512) // 16 == 4 * q + r
+            assert (off % 1024) // 512 == k // 4 and (off % 16) // 4 == k % 4
+            assert off // 1024 == t // 32
+            assert orc.kivi_key_bit(t) == 2 * ((t % 32) // 8)
+    assert sorted({o for o, _ in seen}) == list(range(2048))
     assert all(len(v) == 1 for v in seen.values())
+    # (s, z) storage order: chunk row r's 32 channels are consecutive, in the code-word order
+    idx = [orc.kivi_key_sz_index(c) for c in range(128)]
+    assert sorted(idx) == list(range(128))
+    for c in range(128):
+        k, r = c // 16, (c % 8) // 2
+        byte = (orc.kivi_key_byte_offset(0, c) % 16) % 4
+        assert idx[c] == 32 * r + 4 * k + byte
 
 
 def test_kivi_key_pack_roundtrip(orc):
@@ -170,7 +179,12 @@ def test_kivi_key_pack_roundtrip(orc):
         for t in range(64):
             for c in range(0, 128, 5):
                 b = packed[g, orc.kivi_key_byte_offset(t, c)]
-                assert (b >> (2 * (t % 4))) & 3 == codes[g, t, c]
+                assert (b >> orc.kivi_key_bit(t)) & 3 == codes[g, t, c]
+    sz = rng.integers(0, 65536, (3, 128, 2)).astype(np.uint16)
+    st = orc.kivi_key_sz_pack(sz)
+    for c in range(128):
+        assert np.array_equal(st[:, orc.kivi_key_sz_index(c)], sz[:, c, 0])
+        assert np.array_equal(st[:, 128 + orc.kivi_key_sz_index(c)], sz[:, c, 1])
 
 
 def test_tokenmajor_pack_matches_numpy_bitops(orc):
