@@ -345,9 +345,10 @@ def run_gpu(args, w, rank, world, local_rank):
     peak, peak_kind = _peaks()
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     traffic = None
+    kname, kfiles = stage1_kernel(w)
     if os.path.exists(prof):
-        tr = json.load(open(prof)).get(f"{KERNEL_NAME[w.variant]}@workload{w.index}")
-        if tr and tr.get("source_hash") == kernel_source_hash(w.variant):
+        tr = json.load(open(prof)).get(f"{kname}@workload{w.index}")
+        if tr and tr.get("source_hash") == kernel_source_hash(kfiles):
             traffic = tr["bytes_per_launch"]
     cpu = None
     if world == 1 and not args.no_cpu and w.variant == "kivi":
@@ -369,7 +370,7 @@ def run_gpu(args, w, rank, world, local_rank):
                          "merge": 1e3 * statistics.mean(merge_ms)},
         "hbm_gbs_step": (alg_bytes_stage1 + d2h) / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind, "kernel": KERNEL_NAME[w.variant] + " (stage 1)",
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": kname + " (stage 1)",
                      "alg_bytes_per_launch": alg_bytes_stage1},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms * 1e3 / args.steps / (world if world > 1 else 1), "unit": UNIT,
@@ -380,15 +381,22 @@ def run_gpu(args, w, rank, world, local_rank):
     print(json.dumps(line))
 
 
-KERNEL_NAME = {"kivi": "kivi_decode_kernel", "kitty": "kitty_decode_kernel", "int8": "int8_decode_kernel"}
+def stage1_kernel(w):
+    """Name and source files of the stage-1 kernel the library runs for workload w."""
+    g = w.n_q_heads // w.n_kv_heads
+    if w.variant == "kivi" and 2 <= g <= 4:
+        return "kivi_decode_gqa_kernel", ("kvq_decode_kivi_gqa.cu", "kvq_kivi.cuh", "kvq_device.cuh")
+    if w.variant == "kivi":
+        return "kivi_decode_kernel", ("kvq_decode_kivi.cu", "kvq_kivi.cuh", "kvq_device.cuh")
+    return f"{w.variant}_decode_kernel", (f"kvq_decode_{w.variant}.cu", "kvq_device.cuh")
 DTYPE = {"kivi": "u2 codes + fp16 scales, fp32 accumulate", "kitty": "u2 planes + fp16 scales, fp32 accumulate",
          "int8": "s8 codes + Philox dither + fp16 scales, fp32 accumulate"}
 
 
-def kernel_source_hash(variant: str = "kivi") -> str:
+def kernel_source_hash(files) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in (f"kvq_decode_{variant}.cu", "kvq_device.cuh"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "bit_kv_cache_keyquant_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -403,10 +411,15 @@ def main():
                     help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller captures for profiling; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = I.WORKLOADS[args.workload]
+    if args.batch > 0:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

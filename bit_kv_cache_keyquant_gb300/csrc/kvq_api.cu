@@ -59,9 +59,12 @@ float sm_scale_of(const kvq_config *cfg) {
 // a row holds the tokens outside the quantized tiles, e.g. the fp16 residual).
 kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
     const int64_t rows = (int64_t)batch * cfg->n_q_heads;
-    // the INT8 kernel handles all query heads of a kv head in one unit, 2 CTAs per SM
-    const int64_t unit_rows = variant == KVQ_VARIANT_INT8 ? (int64_t)batch * cfg->n_kv_heads : rows;
-    const int64_t target_units = 8LL * num_sms() * (variant == KVQ_VARIANT_INT8 ? 2 : 4);
+    // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI kernel (3 CTAs per SM) handle all
+    // query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
+    const bool kv_units = variant == KVQ_VARIANT_INT8 || (variant == KVQ_VARIANT_KIVI && kivi_gqa_supported(cfg));
+    const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads : rows;
+    const int ctas = variant == KVQ_VARIANT_INT8 ? 2 : (kv_units ? 3 : 4);
+    const int64_t target_units = 8LL * num_sms() * ctas;
     int64_t chunk = (unit_rows * max_seq_len + target_units - 1) / target_units;
     chunk = (chunk + 127) / 128 * 128;
     if (chunk < 128) chunk = 128;
@@ -235,6 +238,7 @@ static kvq_status stage1_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, co
     if (!c) return KVQ_ERR_INVALID_ARG;
     if ((s = check_ws(cfg, KVQ_VARIANT_KIVI, c->batch, c->max_seq_len, ws, wsb, p))) return s;
     if ((s = ptrs_ok({q, c->seq_len, c->k_codes, c->k_sz, c->v_codes, c->v_sz, c->k_res, c->v_res}))) return s;
+    if (kivi_gqa_supported(cfg)) return cuda_status(launch_decode_kivi_gqa(cfg, c, q, *p, ws, st));
     return cuda_status(launch_decode_kivi(cfg, c, q, *p, ws, st));
 }
 

@@ -29,21 +29,13 @@
 // boundary), 32 per warp straight from global memory with every load of a
 // block in flight together.  Each warp keeps an online softmax state per
 // unit; the CTA merges the four warp states and writes (o_s, lse_s).
-#include "kvq_device.cuh"
-#include "kvq_internal.h"
+#include "kvq_kivi.cuh"
 
 namespace kvq {
 
 namespace {
 
 constexpr int NSTAGE = 4;
-constexpr int NCWARP = 4;                 // consumer warps
-constexpr int STAGE_TOK = 32 * NCWARP;    // 128 tokens per stage
-constexpr int KC_BYTES = STAGE_TOK * KVQ_D / 4;        // 4096
-constexpr int KSZ_MAX = 4 * KVQ_D * 4;                  // 2048 (G = 32)
-constexpr int VC_BYTES = STAGE_TOK * KVQ_D / 4;        // 4096
-constexpr int VSZ_MAX = STAGE_TOK * 4 * 4;             // 2048 (Gv = 32)
-constexpr int STAGE_BYTES = KC_BYTES + KSZ_MAX + VC_BYTES + VSZ_MAX;   // 12288
 constexpr int QK_ROW = 36;                // 32 channels + 4 floats of padding (bank spread)
 
 struct Smem {
@@ -55,108 +47,6 @@ struct Smem {
     float st_m[NCWARP];
     float st_l[NCWARP];
 };
-
-struct Params {
-    const int32_t *seq_len;
-    const uint8_t *k_codes;
-    const uint32_t *k_sz;
-    const uint8_t *v_codes;
-    const uint32_t *v_sz;
-    const uint16_t *k_res;
-    const uint16_t *v_res;
-    const uint16_t *q;
-    float *ws_o;
-    float *ws_lse;
-    unsigned *err;
-    int B, Hq, Hkv, G, Gv, R, splits, chunk;
-    int ngv;            // D / Gv: value (s, z) pairs per token
-    int64_t cap;        // token capacity per (b, kvh): max_seq_len rounded up to 128
-    int64_t kgrp_cap;   // cap / G
-    float alpha;
-    int e0;             // key products are scaled by 2^-E0
-};
-
-// Geometry of one work unit.  Splits 0 .. splits-2 of a (batch row, query
-// head) cover the staged quantized tiles [0, Qf) in chunks; split splits-1
-// covers every remaining token [Qf, L) (the fp16 residual and any tokens cut
-// off by a segment boundary), read straight from global memory.
-struct Unit {
-    int b, hq, split, t0, t1, nT, nstages, nKq, nVq;
-    bool residual;
-    int64_t bk;
-};
-
-__device__ __forceinline__ Unit unit_of(const Params &P, int u) {
-    Unit U;
-    const int row = u / P.splits;
-    U.split = u - row * P.splits;
-    U.b = row / P.Hq;
-    U.hq = row - U.b * P.Hq;
-    const int L = P.seq_len[U.b];
-    const int rK = ((L - 1) % P.R) + 1;
-    U.nKq = L - rK;
-    U.nVq = L - (L < P.R ? L : P.R);
-    const int Qf = (U.nKq < U.nVq ? U.nKq : U.nVq) & ~31;
-    U.residual = U.split == P.splits - 1;
-    if (U.residual) {
-        U.t0 = Qf;
-        U.t1 = L;
-        U.nT = 0;
-    } else {
-        U.t0 = U.split * P.chunk;
-        U.t1 = max(U.t0, min(U.t0 + P.chunk, Qf));
-        U.nT = (U.t1 - U.t0) / 32;
-    }
-    U.nstages = (U.nT + NCWARP - 1) / NCWARP;
-    U.bk = (int64_t)U.b * P.Hkv + U.hq / (P.Hq / P.Hkv);
-    return U;
-}
-
-// KIVI key storage (see kv_quant_key): token t = q + 8p, channel c = 16k + cc
-// with cc = 2r + e + 8h sits in bits 2p of byte e + 2h of word k%4 of chunk
-// 4q + r of half k/4 of its 32-token tile; the group's (s, z) block is 128
-// fp16 scales then 128 fp16 zeros in the order r*32 + 4k + e + 2h.
-__device__ __forceinline__ int kivi_key_byte_offset(int t, int c) {
-    const int k = c >> 4, cc = c & 15;
-    return (t >> 5) * 1024 + (k >> 2) * 512 + (4 * (t & 7) + ((cc & 7) >> 1)) * 16 + (k & 3) * 4 + (cc & 1) +
-           2 * (cc >> 3);
-}
-
-__device__ __forceinline__ int kivi_sz_index(int c) {
-    const int k = c >> 4, cc = c & 15;
-    return ((cc & 7) >> 1) * 32 + k * 4 + (cc & 1) + 2 * (cc >> 3);
-}
-
-// Four dequantized key / value channels 4*lane..4*lane+3 of token t, from the
-// quantized segment or the fp16 residual (used outside the staged tiles).
-__device__ __forceinline__ void fetch_k4(const Params &P, const Unit &U, int t, int lane, float kv[4]) {
-    if (t < U.nKq) {
-        const int G = P.G, gi = t / G, tt = t - gi * G;
-        const uint8_t *grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D / 4);
-        const uint16_t *szb = reinterpret_cast<const uint16_t *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = 4 * lane + i, si = kivi_sz_index(c);
-            const int code = (grp[kivi_key_byte_offset(tt, c)] >> (2 * ((tt & 31) >> 3))) & 3;
-            kv[i] = (float)code * h2f(szb[si]) + h2f(szb[KVQ_D + si]);
-        }
-    } else {
-        const uint2 u = *reinterpret_cast<const uint2 *>(P.k_res + (U.bk * P.R + t % P.R) * KVQ_D + 4 * lane);
-        kv[0] = h2f(lo16(u.x)); kv[1] = h2f(hi16(u.x)); kv[2] = h2f(lo16(u.y)); kv[3] = h2f(hi16(u.y));
-    }
-}
-
-__device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, int lane, float vv[4]) {
-    if (t < U.nVq) {
-        const uint8_t byte = P.v_codes[(U.bk * P.cap + t) * (KVQ_D / 4) + lane];
-        const uint32_t sz = P.v_sz[(U.bk * P.cap + t) * P.ngv + (4 * lane) / P.Gv];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) vv[i] = (float)((byte >> (2 * i)) & 3) * h2f(lo16(sz)) + h2f(hi16(sz));
-    } else {
-        const uint2 u = *reinterpret_cast<const uint2 *>(P.v_res + (U.bk * P.R + t % P.R) * KVQ_D + 4 * lane);
-        vv[0] = h2f(lo16(u.x)); vv[1] = h2f(hi16(u.x)); vv[2] = h2f(lo16(u.y)); vv[3] = h2f(hi16(u.y));
-    }
-}
 
 // Online-softmax update of a warp state with one logit per lane (-inf for
 // empty lanes): returns p = 2^(logit - m) and rescales on a new maximum.
@@ -195,37 +85,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
 
     if (warp == NCWARP) {
         // ---------------- producer: one stream of stages across all units ----------------
-        if (lane == 0) {
-            bool ok = true;
-            int sg = 0;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit U = unit_of(P, u);
-                const uint8_t *kc_base = P.k_codes + U.bk * P.kgrp_cap * ((int64_t)G * KVQ_D / 4);
-                const uint32_t *ksz_base = P.k_sz + U.bk * P.kgrp_cap * KVQ_D;
-                const uint8_t *vc_base = P.v_codes + U.bk * P.cap * (KVQ_D / 4);
-                const uint32_t *vsz_base = P.v_sz + U.bk * P.cap * P.ngv;
-                for (int s = 0; s < U.nstages; ++s, ++sg) {
-                    const int slot = sg % NSTAGE;
-                    if (sg >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((sg / NSTAGE) - 1) & 1, P.err);
-                    if (!ok) break;
-                    const int nt = min(NCWARP, U.nT - s * NCWARP);
-                    const int tok = U.t0 + s * STAGE_TOK;
-                    const uint32_t kc_b = nt * 1024;
-                    const uint32_t ksz_b = ((nt * 32 + G - 1) / G) * KVQ_D * 4;
-                    const uint32_t vc_b = nt * 32 * (KVQ_D / 4);
-                    const uint32_t vsz_b = nt * 32 * P.ngv * 4;
-                    uint8_t *st = S.stage[slot];
-                    mbar_expect_tx(&S.full[slot], kc_b + ksz_b + vc_b + vsz_b);
-                    bulk_g2s(st, kc_base + (int64_t)(tok >> 5) * 1024, kc_b, &S.full[slot]);
-                    bulk_g2s(st + KC_BYTES, ksz_base + (int64_t)(tok / G) * KVQ_D, ksz_b, &S.full[slot]);
-                    bulk_g2s(st + KC_BYTES + KSZ_MAX, vc_base + (int64_t)tok * (KVQ_D / 4), vc_b, &S.full[slot]);
-                    bulk_g2s(st + KC_BYTES + KSZ_MAX + VC_BYTES, vsz_base + (int64_t)tok * P.ngv, vsz_b,
-                             &S.full[slot]);
-                }
-            }
-            // drain: every issued stage must have landed before the CTA exits
-            for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
-        }
+        if (lane == 0) kivi_produce<NSTAGE>(P, P.Hq, S.stage, S.full, S.empty);
         return;
     }
 
@@ -240,7 +100,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit U = unit_of(P, u);
+        const Unit U = unit_of(P, u, P.Hq);
         float qa[4];
         const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D;
         {
@@ -251,92 +111,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             qa[3] = h2f(hi16(qv.y)) * P.alpha;
         }
         if (U.residual) {
-            // ---- residual unit: 32 tokens per warp, lane = token; all loads of a block issued together ----
-            float m_run = -INFINITY, l_part = 0.f, racc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int r0 = U.t0 + 32 * warp; r0 < U.t1; r0 += 32 * NCWARP) {
-                const int n = min(32, U.t1 - r0);
-                // whole block fp16 in both K and V (the usual case): unconditional loads,
-                // 8 tokens in flight per batch; indices clamped into the block
-                const bool plain = r0 >= U.nKq && r0 >= U.nVq;
-                const uint16_t *kres = P.k_res + U.bk * P.R * KVQ_D + 4 * lane;
-                const uint16_t *vres = P.v_res + U.bk * P.R * KVQ_D + 4 * lane;
-                float d[32];
-                if (plain) {
-#pragma unroll
-                    for (int hb = 0; hb < 4; ++hb) {
-                        uint2 raw[8];
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            const int t = min(r0 + 8 * hb + m, U.t1 - 1);
-                            raw[m] = __ldg(reinterpret_cast<const uint2 *>(kres + (t % P.R) * KVQ_D));
-                        }
-#pragma unroll
-                        for (int m = 0; m < 8; ++m)
-                            d[8 * hb + m] = qa[0] * h2f(lo16(raw[m].x)) + qa[1] * h2f(hi16(raw[m].x)) +
-                                             qa[2] * h2f(lo16(raw[m].y)) + qa[3] * h2f(hi16(raw[m].y));
-                    }
-                } else {
-#pragma unroll
-                    for (int tt = 0; tt < 32; ++tt) {
-                        d[tt] = 0.f;
-                        if (tt < n) {
-                            float kv[4];
-                            fetch_k4(P, U, r0 + tt, lane, kv);
-                            d[tt] = qa[0] * kv[0] + qa[1] * kv[1] + qa[2] * kv[2] + qa[3] * kv[3];
-                        }
-                    }
-                }
-                // reduce-scatter over all 32 lanes: lane keeps token (bit-reversed lane index)
-#pragma unroll
-                for (int o = 16, h = 16; o >= 1; o >>= 1, h >>= 1) {
-                    const bool up = (lane & o) != 0;
-#pragma unroll
-                    for (int m = 0; m < h; ++m) {
-                        const float send = up ? d[m] : d[m + h];
-                        d[m] = (up ? d[m + h] : d[m]) + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-                    }
-                }
-                // lane holds token 16*b4 + 8*b3 + 4*b2 + 2*b1 + b0 = lane
-                const float logit = lane < n ? d[0] : -INFINITY;
-                const float mt = warp_max(logit);
-                if (mt > m_run) {
-                    const float sc = exp2f(m_run - mt);
-                    l_part *= sc;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) racc[i] *= sc;
-                    m_run = mt;
-                }
-                const float p = exp2f(logit - m_run);
-                l_part += p;
-                if (plain) {
-#pragma unroll
-                    for (int hb = 0; hb < 4; ++hb) {
-                        uint2 raw[8];
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            const int t = min(r0 + 8 * hb + m, U.t1 - 1);
-                            raw[m] = __ldg(reinterpret_cast<const uint2 *>(vres + (t % P.R) * KVQ_D));
-                        }
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            const float pt = __shfl_sync(0xFFFFFFFFu, p, 8 * hb + m);   // 0 beyond the block
-                            racc[0] += pt * h2f(lo16(raw[m].x));
-                            racc[1] += pt * h2f(hi16(raw[m].x));
-                            racc[2] += pt * h2f(lo16(raw[m].y));
-                            racc[3] += pt * h2f(hi16(raw[m].y));
-                        }
-                    }
-                } else {
-#pragma unroll 1
-                    for (int tt = 0; tt < n; ++tt) {
-                        const float pt = __shfl_sync(0xFFFFFFFFu, p, tt);
-                        float vv[4];
-                        fetch_v4(P, U, r0 + tt, lane, vv);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) racc[i] += pt * vv[i];
-                    }
-                }
-            }
+            // ---- residual unit ----
+            float m_run, l_part, racc[4];
+            kivi_residual(P, U, qa, warp, lane, racc, m_run, l_part);
             const float l_w = warp_sum(l_part);
             *reinterpret_cast<float4 *>(&S.st_acc[warp][4 * lane]) = make_float4(racc[0], racc[1], racc[2], racc[3]);
             if (lane == 0) {
@@ -370,8 +147,9 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     
                     const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + KC_BYTES) + gl * 2 * KVQ_D;
                     // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
-                    const uint2 sv = *reinterpret_cast<const uint2 *>(ksz + 4 * lane);
-                    const uint2 zv = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + 4 * lane);
+                    const int si = (((lane & 7) >> 1) * 4 + (lane >> 3)) * 8 + (lane & 1) * 4;
+                    const uint2 sv = *reinterpret_cast<const uint2 *>(ksz + si);
+                    const uint2 zv = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + si);
                     *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
                         make_float4(qp[0] * h2f(lo16(sv.x)), qp[1] * h2f(hi16(sv.x)), qp[2] * h2f(lo16(sv.y)),
                                     qp[3] * h2f(hi16(sv.y)));

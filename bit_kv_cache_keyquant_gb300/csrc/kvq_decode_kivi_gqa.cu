@@ -1,0 +1,474 @@
+// a3 for grouped-query heads: KIVI split-KV decode attention, stage 1, with
+// all g <= 4 query heads of a kv head in one work unit and both contractions
+// on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation).
+// Each packed code is unpacked once and serves every head of its kv head.
+//
+// Keys (KIVI Eq. 3 with the dequantization folded out):
+//   S[t, n] = sum_c A[t, c] B[c, n]            n = 2h + x, x = 0 (hi), 1 (lo)
+//   A[t, c] = code_tc * 2^-9 or 2^-7: the packed byte is masked into an e4m3
+//             bit pattern (2-bit code in the low mantissa bits, or straddling
+//             the mantissa and the exponent's low bit, both linear in the
+//             code) and converted exactly with cvt.rn.f16x2.e4m3x2;
+//   B[c, n] = fp16 hi / lo parts of W = alpha q_hc s_c 2^sigma_h.  With the
+//             query split once per unit into fp16 qhi + qlo, hi = fl(qhi s)
+//             and lo = fl(qlo s + (qhi s - hi)); the bracket is the exact
+//             rounding error of hi (one fp16 FMA), so hi + lo carries W to
+//             about 2^-21 relative, and sigma_h keeps every part in range.
+//   logit_ht = (S[t, 2h] + S[t, 2h+1]) 2^(9|7 - sigma_h) + alpha sum_c q_hc z_c
+// Values:
+//   O[c, n]  = sum_t A[c, t] B[t, n]
+//   A[c, t] = code_tc * 2^-9 or 2^-7 (same unpacking, channel rows);
+//   B[t, n] = hi / lo parts of p_ht s_tg (p kept as fp16 hi + lo);
+//   o_hc     = (O[c, 2h] + O[c, 2h+1]) 2^(9|7) + sum_t p_ht z_tg.
+// Products on the tensor cores are exact (fp16 x fp16) and accumulate in
+// fp32; A operands are normal fp16 numbers (subnormal A operands lose bits).
+//
+// Work decomposition as the per-head kernel: a persistent grid walks the
+// (batch row, kv head, split) units; a producer warp streams 128-token
+// stages with bulk async copies into an mbarrier ring; four consumer warps
+// each take one 32-token tile (two 16-token m-tiles) per stage; the last
+// split of every row is the residual unit, done per head on CUDA cores.
+#include "kvq_kivi.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int GQ_NSTAGE = 4;
+constexpr int GMAX = 4;                   // query heads per unit (n = 8 tensor-core columns)
+constexpr int PB_ROW = 40;                // p exchange row: 32 tokens + 8 floats (conflict-free)
+constexpr int ACC_ROW = KVQ_D + 8;
+
+struct SmemG {
+    uint8_t stage[GQ_NSTAGE][STAGE_BYTES];
+    uint64_t full[GQ_NSTAGE];
+    uint64_t empty[GQ_NSTAGE];
+    uint32_t qhi[GMAX][64];               // fp16x2 hi parts of alpha q 2^sigma: [head][k/2][r][4]
+    uint32_t qlo[GMAX][64];               // fp16x2 lo parts, same order
+    float qz[GMAX][KVQ_D];                // alpha q (fp32): [head][k][r][4]
+    float unsig[GMAX];                    // 2^-sigma_h
+    float pbuf[NCWARP][GMAX * PB_ROW];
+    float st_acc[NCWARP][GMAX][ACC_ROW];
+    float st_m[NCWARP][GMAX];
+    float st_l[NCWARP][GMAX];
+};
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v16) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v16));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// fp16x2 product a*b as its hi part (x == 0) or its lo part (x == 1):
+// hi = fl(ah b); lo = fl(al b + fl(ah b - hi)), the inner FMA being exact.
+__device__ __forceinline__ uint32_t split_prod(uint32_t ah, uint32_t al, uint32_t b, bool x) {
+    const uint32_t hi = hmul2(ah, b);
+    return x ? hfma2(al, b, hfma2(ah, b, hi ^ 0x80008000u)) : hi;
+}
+// fp32 pair -> fp16x2 hi (x == 0) or lo = fl(v - hi) (x == 1); first value in the low half
+__device__ __forceinline__ uint32_t split_pair(float v0, float v1, bool x) {
+    uint32_t hi;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(v1), "f"(v0));
+    if (!x) return hi;
+    const float r0 = v0 - h2f(lo16(hi)), r1 = v1 - h2f(hi16(hi));
+    uint32_t lo;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(r1), "f"(r0));
+    return lo;
+}
+
+template <int N>
+__device__ __forceinline__ void load_row(const uint32_t *p, uint32_t (&v)[N]) {
+    if constexpr (N == 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    } else if constexpr (N == 2) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        v[0] = u.x; v[1] = u.y;
+    } else {
+        v[0] = *p;
+    }
+}
+
+}  // namespace
+
+template <int NGV>
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(Params P) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    SmemG &S = *reinterpret_cast<SmemG *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = P.Hq / P.Hkv;
+    const int n_units = P.B * P.Hkv * P.splits;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < GQ_NSTAGE; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], NCWARP);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCWARP) {
+        if (lane == 0) kivi_produce<GQ_NSTAGE>(P, P.Hkv, S.stage, S.full, S.empty);
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int q = lane >> 2, r = lane & 3;         // mma group id / thread in group
+    const int hB = q >> 1;                         // head of this lane's B column (n = q)
+    const bool xB = (q & 1) != 0;                  // B column holds lo parts
+    const int gl = (32 * warp) / P.G;              // key group of this warp's tile within a stage
+    // value unpacking: channel 16mt + q (+8) is byte 4mt + q/4 (+2) of a token row, bits 2(q%4)
+    const uint32_t vsel = (uint32_t)((q >> 2) | ((4 + (q >> 2)) << 4) | ((2 + (q >> 2)) << 8) | ((6 + (q >> 2)) << 12));
+    const uint32_t vshift = (q & 2) ? 4u : 0u;
+    const uint32_t vmask = (q & 1) ? 0x0C0C0C0Cu : 0x03030303u;
+    const float vscale = (q & 1) ? 128.f : 512.f;
+    bool ok = true;
+    int sg = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = unit_of(P, u, P.Hkv);     // U.hq is the kv head
+        // ---- per-unit query tables: warp w prepares head w ----
+        {
+            const int h = warp;
+            const int c0 = 16 * (lane & 7) + 2 * (lane >> 3);   // entries 4*lane..4*lane+3
+            float qv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (h < g) {
+                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+                const uint32_t q01 = *reinterpret_cast<const uint32_t *>(qrow + c0);
+                const uint32_t q89 = *reinterpret_cast<const uint32_t *>(qrow + c0 + 8);
+                qv[0] = h2f(lo16(q01)) * P.alpha;
+                qv[1] = h2f(hi16(q01)) * P.alpha;
+                qv[2] = h2f(lo16(q89)) * P.alpha;
+                qv[3] = h2f(hi16(q89)) * P.alpha;
+            }
+            const float m = warp_max(fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3]))));
+            // 2^sigma m in [1/2, 1): every |W| = |alpha q s| 2^sigma stays below 65504
+            int ex = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
+            int sigma = m > 0.f ? -ex - 1 : 0;
+            sigma = max(-120, min(120, sigma));
+            const float sc = __int_as_float((127 + sigma) << 23);
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v = qv[j] * sc;
+                hi[j] = f2h_rn(v);
+                lo[j] = f2h_rn(v - h2f(hi[j]));
+            }
+            // lane = 8r + k holds channels 16k + 2r + {0, 1, 8, 9}
+            const int tr = lane >> 3, tk = lane & 7;
+            const int pw = (tk >> 1) * 16 + tr * 4 + 2 * (tk & 1);
+            *reinterpret_cast<uint2 *>(&S.qhi[h][pw]) =
+                make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+            *reinterpret_cast<uint2 *>(&S.qlo[h][pw]) =
+                make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+            *reinterpret_cast<float4 *>(&S.qz[h][tk * 16 + tr * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+            if (lane == 0) S.unsig[h] = __int_as_float((127 - sigma) << 23);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+
+        if (U.residual) {
+            for (int h = 0; h < g; ++h) {
+                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+                const uint2 qr = *reinterpret_cast<const uint2 *>(qrow + 4 * lane);
+                const float qa[4] = {h2f(lo16(qr.x)) * P.alpha, h2f(hi16(qr.x)) * P.alpha, h2f(lo16(qr.y)) * P.alpha,
+                                     h2f(hi16(qr.y)) * P.alpha};
+                float m_run, l_part, racc[4];
+                kivi_residual(P, U, qa, warp, lane, racc, m_run, l_part);
+                const float l_w = warp_sum(l_part);
+                *reinterpret_cast<float4 *>(&S.st_acc[warp][h][4 * lane]) = make_float4(racc[0], racc[1], racc[2], racc[3]);
+                if (lane == 0) {
+                    S.st_m[warp][h] = m_run;
+                    S.st_l[warp][h] = l_w;
+                }
+            }
+        } else {
+            float m_run = -INFINITY, l_part = 0.f;        // head r
+            float vz[NGV];
+            float vacc[8][4];
+#pragma unroll
+            for (int i = 0; i < NGV; ++i) vz[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vacc[i][0] = vacc[i][1] = vacc[i][2] = vacc[i][3] = 0.f;
+            const float unsig = S.unsig[r];
+            for (int s = 0; s < U.nstages; ++s, ++sg) {
+                const int slot = sg % GQ_NSTAGE;
+                ok = ok && mbar_wait(&S.full[slot], (sg / GQ_NSTAGE) & 1, P.err);
+                const int tile = s * NCWARP + warp;
+                if (ok && tile < U.nT) {
+                    const uint8_t *st = S.stage[slot];
+                    const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + KC_BYTES) + gl * 2 * KVQ_D;
+                    // ---- key B fragments (head hB, hi or lo), channels 16k + 2r + {0,1 | 8,9} ----
+                    uint32_t bk[16];
+                    {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
+                            const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
+                            const uint4 sv = *reinterpret_cast<const uint4 *>(ksz + (4 * i + r) * 8);
+                            bk[4 * i + 0] = split_prod(a.x, l.x, sv.x, xB);
+                            bk[4 * i + 1] = split_prod(a.y, l.y, sv.y, xB);
+                            bk[4 * i + 2] = split_prod(a.z, l.z, sv.z, xB);
+                            bk[4 * i + 3] = split_prod(a.w, l.w, sv.w, xB);
+                        }
+                    }
+                    // ---- alpha sum_c q_hc z_c: the lanes of head hB split the lane's 32 channels by xB ----
+                    float zr;
+                    {
+                        float zp = 0.f;
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) {
+                            const int k = xB ? 7 - n : n;            // order keeps the two halves on distinct banks
+                            const uint2 zz = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + ((k >> 1) * 4 + r) * 8 +
+                                                                             (k & 1) * 4);
+                            const float4 qa = *reinterpret_cast<const float4 *>(&S.qz[hB][k * 16 + 4 * r]);
+                            zp = fmaf(qa.x, h2f(lo16(zz.x)), zp);
+                            zp = fmaf(qa.y, h2f(hi16(zz.x)), zp);
+                            zp = fmaf(qa.z, h2f(lo16(zz.y)), zp);
+                            zp = fmaf(qa.w, h2f(hi16(zz.y)), zp);
+                        }
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
+                        zr = __shfl_sync(0xFFFFFFFFu, zp, 8 * r);   // head r lives in lanes 8r..8r+7
+                    }
+                    // ---- key codes x B on the tensor cores: tokens q + 8p, p = 0..3 ----
+                    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                    {
+                        const uint8_t *kt = st + warp * 1024;
+                        const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
+                        const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
+                        const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t w = kw[k], w4 = kw[k] >> 4;
+                            const uint32_t m0 = w & 0x03030303u, m1 = w & 0x0C0C0C0Cu;
+                            const uint32_t m2 = w4 & 0x03030303u, m3 = w4 & 0x0C0C0C0Cu;
+                            mma16816(s0, e4m3x2_f16x2(m0), e4m3x2_f16x2(m1), e4m3x2_f16x2(m0 >> 16),
+                                     e4m3x2_f16x2(m1 >> 16), bk[2 * k], bk[2 * k + 1]);
+                            mma16816(s1, e4m3x2_f16x2(m2), e4m3x2_f16x2(m3), e4m3x2_f16x2(m2 >> 16),
+                                     e4m3x2_f16x2(m3 >> 16), bk[2 * k], bk[2 * k + 1]);
+                        }
+                    }
+                    // ---- logits of head r, tokens q, q+8, q+16, q+24; online softmax ----
+                    const float f9 = unsig * 512.f, f7 = unsig * 128.f;
+                    float lg[4];
+                    lg[0] = fmaf(s0[0] + s0[1], f9, zr);
+                    lg[1] = fmaf(s0[2] + s0[3], f7, zr);
+                    lg[2] = fmaf(s1[0] + s1[1], f9, zr);
+                    lg[3] = fmaf(s1[2] + s1[3], f7, zr);
+                    float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 4));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
+                    if (mt > m_run) {
+                        const float sc = exp2f(m_run - mt);
+                        l_part *= sc;
+#pragma unroll
+                        for (int i = 0; i < NGV; ++i) vz[i] *= sc;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            vacc[i][0] *= sc; vacc[i][1] *= sc; vacc[i][2] *= sc; vacc[i][3] *= sc;
+                        }
+                        m_run = mt;
+                    }
+                    float pr[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        pr[i] = exp2f(lg[i] - m_run);
+                        l_part += pr[i];
+                    }
+                    // token 16k + 8hk + 4e + j (k-step k, m-row pair index 2j + e + 8hk) at
+                    // position 16k + 8hk + 2j + e: each B register's two tokens are adjacent
+                    float *pb = S.pbuf[warp];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pb[r * PB_ROW + 8 * i + 2 * (q & 3) + (q >> 2)] = pr[i];
+                    // ---- value zero-point term of head r over the lane's four tokens ----
+                    const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + KC_BYTES + KSZ_MAX + VC_BYTES) +
+                                          warp * 32 * NGV;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t row[NGV];
+                        load_row<NGV>(vsz + (q + 8 * i) * NGV, row);
+#pragma unroll
+                        for (int j = 0; j < NGV; ++j) vz[j] = fmaf(pr[i], h2f(hi16(row[j])), vz[j]);
+                    }
+                    __syncwarp();
+                    // ---- values: two 16-token k-steps x eight 16-channel m-tiles; k-column 2j + e + 8hk of
+                    //      k-step k is token 16k + 8hk + 4e + j (rows of one load on distinct banks) ----
+                    const uint8_t *vc = st + KC_BYTES + KSZ_MAX + warp * 32 * (KVQ_D / 4);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int t0 = 16 * ks + r;             // tokens t0, t0+4 | t0+8, t0+12
+                        // B: p_(hB, t) s_(t, j)
+                        const float2 pa = *reinterpret_cast<const float2 *>(&pb[hB * PB_ROW + 16 * ks + 2 * r]);
+                        const float2 pc = *reinterpret_cast<const float2 *>(&pb[hB * PB_ROW + 16 * ks + 8 + 2 * r]);
+                        const uint32_t pha = split_pair(pa.x, pa.y, false), pla = split_pair(pa.x, pa.y, true);
+                        const uint32_t phc = split_pair(pc.x, pc.y, false), plc = split_pair(pc.x, pc.y, true);
+                        uint32_t bv0[NGV], bv1[NGV];
+                        {
+                            uint32_t ra[NGV], rb[NGV], rc[NGV], rd[NGV];
+                            load_row<NGV>(vsz + t0 * NGV, ra);
+                            load_row<NGV>(vsz + (t0 + 4) * NGV, rb);
+                            load_row<NGV>(vsz + (t0 + 8) * NGV, rc);
+                            load_row<NGV>(vsz + (t0 + 12) * NGV, rd);
+#pragma unroll
+                            for (int j = 0; j < NGV; ++j) {
+                                bv0[j] = split_prod(pha, pla, prmt(ra[j], rb[j], 0x5410u), xB);
+                                bv1[j] = split_prod(phc, plc, prmt(rc[j], rd[j], 0x5410u), xB);
+                            }
+                        }
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 32 + 16 * hf);
+                            const uint4 rB = *reinterpret_cast<const uint4 *>(vc + (t0 + 4) * 32 + 16 * hf);
+                            const uint4 rC = *reinterpret_cast<const uint4 *>(vc + (t0 + 8) * 32 + 16 * hf);
+                            const uint4 rD = *reinterpret_cast<const uint4 *>(vc + (t0 + 12) * 32 + 16 * hf);
+                            const uint32_t wa[4] = {rA.x, rA.y, rA.z, rA.w}, wb[4] = {rB.x, rB.y, rB.z, rB.w};
+                            const uint32_t wc[4] = {rC.x, rC.y, rC.z, rC.w}, wd[4] = {rD.x, rD.y, rD.z, rD.w};
+#pragma unroll
+                            for (int m4 = 0; m4 < 4; ++m4) {
+                                const int mt = 4 * hf + m4;
+                                const int j = (16 * mt) / (KVQ_D / NGV);       // value group of the m-tile
+                                const uint32_t y01 = (prmt(wa[m4], wb[m4], vsel) >> vshift) & vmask;
+                                const uint32_t y89 = (prmt(wc[m4], wd[m4], vsel) >> vshift) & vmask;
+                                mma16816(vacc[mt], e4m3x2_f16x2(y01), e4m3x2_f16x2(y01 >> 16), e4m3x2_f16x2(y89),
+                                         e4m3x2_f16x2(y89 >> 16), bv0[j], bv1[j]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
+            }
+            // ---- warp state (head r) -> shared memory ----
+            float l_w = l_part;
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 4);
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
+#pragma unroll
+            for (int j = 0; j < NGV; ++j) {
+                vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 4);
+                vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 8);
+                vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 16);
+            }
+            float *acc = S.st_acc[warp][r];
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int j = (16 * mt) / (KVQ_D / NGV);
+                acc[16 * mt + q] = fmaf(vacc[mt][0] + vacc[mt][1], vscale, vz[j]);
+                acc[16 * mt + q + 8] = fmaf(vacc[mt][2] + vacc[mt][3], vscale, vz[j]);
+            }
+            if (q == 0) {
+                S.st_m[warp][r] = m_run;
+                S.st_l[warp][r] = l_w;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+        // ---- warp w merges head w over the four warp states, writes (o_s, lse_s) ----
+        if (warp < g) {
+            const int h = warp;
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i][h]);
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NCWARP; ++i) {
+                    const float w = S.st_m[i][h] > -INFINITY ? exp2f(S.st_m[i][h] - M) : 0.f;
+                    l += w * S.st_l[i][h];
+                    const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][h][4 * lane]);
+                    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+                }
+            }
+            const int64_t row = (((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h)) * P.splits + U.split;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+    }
+}
+
+bool kivi_gqa_supported(const kvq_config *cfg) {
+    const int g = cfg->n_q_heads / cfg->n_kv_heads;
+    return g >= 2 && g <= GMAX;
+}
+
+cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q, const DecodePlan &p,
+                                   void *ws, cudaStream_t st) {
+    Params P;
+    P.seq_len = c->seq_len;
+    P.k_codes = static_cast<const uint8_t *>(c->k_codes);
+    P.k_sz = static_cast<const uint32_t *>(c->k_sz);
+    P.v_codes = static_cast<const uint8_t *>(c->v_codes);
+    P.v_sz = static_cast<const uint32_t *>(c->v_sz);
+    P.k_res = static_cast<const uint16_t *>(c->k_res);
+    P.v_res = static_cast<const uint16_t *>(c->v_res);
+    P.q = static_cast<const uint16_t *>(q);
+    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
+    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
+    P.err = device_error_ptr();
+    P.B = c->batch;
+    P.Hq = cfg->n_q_heads;
+    P.Hkv = cfg->n_kv_heads;
+    P.G = cfg->group_k;
+    P.Gv = cfg->group_v;
+    P.ngv = KVQ_D / cfg->group_v;
+    P.R = cfg->residual;
+    P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
+    P.splits = p.splits;
+    P.chunk = p.chunk;
+    P.kgrp_cap = P.cap / cfg->group_k;
+    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    P.e0 = 0;
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    const size_t smem = sizeof(SmemG);
+    const int ngv = P.ngv;
+    static int attr_dev[3] = {-1, -1, -1};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int ti = ngv == 4 ? 0 : (ngv == 2 ? 1 : 2);
+    if (attr_dev[ti] != dev) {
+        cudaError_t e = ngv == 4   ? cudaFuncSetAttribute(kivi_decode_gqa_kernel<4>,
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                        : ngv == 2 ? cudaFuncSetAttribute(kivi_decode_gqa_kernel<2>,
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                                   : cudaFuncSetAttribute(kivi_decode_gqa_kernel<1>,
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev[ti] = dev;
+    }
+    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
+    int64_t grid = (int64_t)num_sms() * 3;
+    if (grid > n_units) grid = n_units;
+    if (ngv == 4) kivi_decode_gqa_kernel<4><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    else if (ngv == 2) kivi_decode_gqa_kernel<2><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    else kivi_decode_gqa_kernel<1><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -20,11 +20,11 @@ namespace kvq {
 // formula).  Tile layout: token t = q + 8p, channel c = 16k + 2r + e + 8h
 // sits in bits 2p of byte e + 2h of word k%4 of chunk 4q + r of half k/4.
 // The (s, z) block of a group is 128 fp16 scales then 128 fp16 zeros, both
-// in the order r*32 + 4k + e + 2h.
+// at ((k/2)*4 + r)*8 + (k%2)*4 + e + 2h.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int kivi_sz_index(int c) {
     const int k = c >> 4, cc = c & 15;
-    return ((cc & 7) >> 1) * 32 + k * 4 + (cc & 1) + 2 * (cc >> 3);
+    return ((k >> 1) * 4 + ((cc & 7) >> 1)) * 8 + (k & 1) * 4 + (cc & 1) + 2 * (cc >> 3);
 }
 
 template <int NT>

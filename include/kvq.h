@@ -41,7 +41,7 @@
  *     4q + r of a warp finds all of its tokens {q + 8p} x channels
  *     {16k + 2r + {0,1,8,9}} in the 16-byte chunks lane and lane + 32.
  *     Parameters: 256 fp16 per group, the 128 scales then the 128 zeros,
- *     channel c at index r*32 + 4k + e + 2h of each half.
+ *     channel c at index ((k/2)*4 + r)*8 + (k%2)*4 + e + 2h of each half.
  *   KIVI value token: D/4 bytes, channel c in bits 2*(c%4) of byte c/4.
  *     Parameters: fp16x2 (s, z) [D/Gv] per token.
  *   Kitty key page (G = 128 tokens, K boosted channels), one record of

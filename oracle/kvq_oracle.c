@@ -239,13 +239,15 @@ ORC_API int orc_kivi_key_pack(int D, int G, const uint8_t *codes, long n_grp, ui
 
 /* Storage index of channel c's scale (and, 128 entries later, its zero) in
  * a KIVI key group's parameter block of 128 fp16 scales followed by 128
- * fp16 zeros: the same (r, k, e + 2h) order as the code chunks, so that the
- * 32 channels of chunk row r are 32 consecutive entries. */
+ * fp16 zeros.  With c = 16k + 2r + e + 8h as for the codes, the entry is
+ * number (k%2)*4 + e + 2h of the 8-entry chunk (k/2)*4 + r: chunk row r of
+ * the codes finds its 32 channels in the chunks r, 4+r, 8+r, 12+r, in the
+ * order of its code words. */
 ORC_API int orc_kivi_key_sz_index(int c)
 {
     int k = c / 16, cc = c % 16;
     int r = (cc % 8) / 2, e = cc % 2, h = cc / 8;
-    return r * 32 + k * 4 + e + 2 * h;
+    return ((k / 2) * 4 + r) * 8 + (k % 2) * 4 + e + 2 * h;
 }
 
 /* sz: fp16 pairs [n_grp][D][2] -> stored blocks [n_grp][2*D]. */

@@ -162,13 +162,14 @@ def test_kivi_key_layout_is_a_lane_friendly_bijection(orc):
             assert orc.kivi_key_bit(t) == 2 * ((t % 32) // 8)
     assert sorted({o for o, _ in seen}) == list(range(2048))
     assert all(len(v) == 1 for v in seen.values())
-    # (s, z) storage order: chunk row r's 32 channels are consecutive, in the code-word order
+    # (s, z) storage order: chunk row r's 32 channels are the 8-entry chunks r, 4+r, 8+r, 12+r,
+    # word k of the codes at entries (k%2)*4 + byte of chunk (k/2)*4 + r
     idx = [orc.kivi_key_sz_index(c) for c in range(128)]
     assert sorted(idx) == list(range(128))
     for c in range(128):
         k, r = c // 16, (c % 8) // 2
         byte = (orc.kivi_key_byte_offset(0, c) % 16) % 4
-        assert idx[c] == 32 * r + 4 * k + byte
+        assert idx[c] == ((k // 2) * 4 + r) * 8 + (k % 2) * 4 + byte
 
 
 def test_kivi_key_pack_roundtrip(orc):
