@@ -385,9 +385,13 @@ def stage1_kernel(w):
     """Name and source files of the stage-1 kernel the library runs for workload w."""
     g = w.n_q_heads // w.n_kv_heads
     if w.variant == "kivi" and 2 <= g <= 4:
-        return "kivi_decode_gqa_kernel", ("kvq_decode_kivi_gqa.cu", "kvq_kivi.cuh", "kvq_device.cuh")
+        return "kivi_decode_gqa_kernel", ("kvq_decode_kivi_gqa.cu", "kvq_kivi.cuh", "kvq_mma.cuh", "kvq_device.cuh")
     if w.variant == "kivi":
         return "kivi_decode_kernel", ("kvq_decode_kivi.cu", "kvq_kivi.cuh", "kvq_device.cuh")
+    if w.variant == "kitty" and 2 <= g <= 4:
+        return "kitty_decode_gqa_kernel", ("kvq_decode_kitty_gqa.cu", "kvq_kitty.cuh", "kvq_mma.cuh", "kvq_device.cuh")
+    if w.variant == "kitty":
+        return "kitty_decode_kernel", ("kvq_decode_kitty.cu", "kvq_kitty.cuh", "kvq_device.cuh")
     return f"{w.variant}_decode_kernel", (f"kvq_decode_{w.variant}.cu", "kvq_device.cuh")
 DTYPE = {"kivi": "u2 codes + fp16 scales, fp32 accumulate", "kitty": "u2 planes + fp16 scales, fp32 accumulate",
          "int8": "s8 codes + Philox dither + fp16 scales, fp32 accumulate"}

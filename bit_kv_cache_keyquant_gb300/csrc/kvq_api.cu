@@ -59,11 +59,12 @@ float sm_scale_of(const kvq_config *cfg) {
 // a row holds the tokens outside the quantized tiles, e.g. the fp16 residual).
 kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
     const int64_t rows = (int64_t)batch * cfg->n_q_heads;
-    // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI kernel (3 CTAs per SM) handle all
-    // query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
-    const bool kv_units = variant == KVQ_VARIANT_INT8 || (variant == KVQ_VARIANT_KIVI && kivi_gqa_supported(cfg));
+    // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI and Kitty kernels (4 CTAs per SM)
+    // handle all query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
+    const bool kv_units = variant == KVQ_VARIANT_INT8 || (variant == KVQ_VARIANT_KIVI && kivi_gqa_supported(cfg)) ||
+                          (variant == KVQ_VARIANT_KITTY && kitty_gqa_supported(cfg));
     const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads : rows;
-    const int ctas = variant == KVQ_VARIANT_INT8 ? 2 : (kv_units ? 3 : 4);
+    const int ctas = variant == KVQ_VARIANT_INT8 ? 2 : 4;
     const int64_t target_units = 8LL * num_sms() * ctas;
     int64_t chunk = (unit_rows * max_seq_len + target_units - 1) / target_units;
     chunk = (chunk + 127) / 128 * 128;
@@ -251,6 +252,7 @@ static kvq_status stage1_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, 
     if ((s = check_ws(cfg, KVQ_VARIANT_KITTY, c->batch, c->max_seq_len, ws, wsb, p))) return s;
     if ((s = ptrs_ok({q, c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local}))) return s;
     if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;
+    if (kitty_gqa_supported(cfg)) return cuda_status(launch_decode_kitty_gqa(cfg, c, q, *p, ws, st));
     return cuda_status(launch_decode_kitty(cfg, c, q, *p, ws, st));
 }
 

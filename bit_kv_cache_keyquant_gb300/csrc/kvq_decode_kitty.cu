@@ -23,20 +23,14 @@
 // both sides (sink, buffers, local window, a key page whose values are
 // still in fp16): one token per lane for the keys (per-lane independent
 // loads), four channels per lane for the values.
-#include "kvq_device.cuh"
-#include "kvq_internal.h"
+#include "kvq_kitty.cuh"
 
 namespace kvq {
 
 namespace {
 
 constexpr int NSTAGE = 4;
-constexpr int NCWARP = 4;
-constexpr int PG = 128;                    // tokens per page
-constexpr int STAGE_BYTES = 12288;
-constexpr int VREC_OFF = 7680;             // value record offset inside a stage (key record <= 7680 B)
 constexpr int QK_ROW = 36;
-constexpr int KMAX = 92;                   // boosted channels that fit the key-record slot
 
 struct Smem {
     uint8_t stage[NSTAGE][STAGE_BYTES];
@@ -49,63 +43,6 @@ struct Smem {
     float st_m[NCWARP];
     float st_l[NCWARP];
 };
-
-struct Params {
-    const int32_t *seq_len;
-    const uint8_t *k_pages;
-    const uint8_t *v_pages;
-    const uint16_t *k_sink, *v_sink, *k_qbuf, *v_qbuf, *v_local;
-    const uint16_t *q;
-    float *ws_o, *ws_lse;
-    unsigned *err;
-    int B, Hq, Hkv, S, R, K, splits, chunk, page_cap;
-    int kpb, vpb;
-    float alpha;
-    int e0;
-};
-
-struct Unit {
-    int b, hq, split, p0, np, nKp, nVp, nkb, nvb, L;
-    bool residual;
-    int64_t bk;
-};
-
-__device__ __forceinline__ Unit unit_of(const Params &P, int u) {
-    Unit U;
-    const int row = u / P.splits;
-    U.split = u - row * P.splits;
-    U.b = row / P.Hq;
-    U.hq = row - U.b * P.Hq;
-    const int L = P.seq_len[U.b];
-    U.L = L;
-    if (L > P.S) {
-        U.nkb = ((L - P.S - 1) % PG) + 1;
-        U.nKp = (L - P.S - U.nkb) / PG;
-    } else {
-        U.nkb = 0;
-        U.nKp = 0;
-    }
-    const int E = max(0, L - P.S - P.R);
-    U.nvb = E > 0 ? ((E - 1) % PG) + 1 : 0;
-    U.nVp = (E - U.nvb) / PG;
-    const int Pf = min(U.nKp, U.nVp);                  // pages quantized on both sides
-    U.residual = U.split == P.splits - 1;
-    if (U.residual) {
-        U.p0 = Pf;
-        U.np = 0;
-    } else {
-        const int cpp = P.chunk / PG;
-        U.p0 = U.split * cpp;
-        U.np = max(0, min(U.p0 + cpp, Pf) - U.p0);
-    }
-    U.bk = (int64_t)U.b * P.Hkv + U.hq / (P.Hq / P.Hkv);
-    return U;
-}
-
-// Key of token t (residual unit), channel c, dequantized (fp32).
-__device__ __forceinline__ const uint8_t *key_page(const Params &P, const Unit &U, int p) {
-    return P.k_pages + (U.bk * P.page_cap + p) * (int64_t)P.kpb;
-}
 
 __device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias,
                                               unsigned long long vacc2[16]) {
@@ -141,25 +78,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Para
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) {
-            bool ok = true;
-            int sg = 0;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit U = unit_of(P, u);
-                for (int s = 0; s < U.np; ++s, ++sg) {
-                    const int slot = sg % NSTAGE;
-                    if (sg >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((sg / NSTAGE) - 1) & 1, P.err);
-                    if (!ok) break;
-                    const int p = U.p0 + s;
-                    uint8_t *st = S.stage[slot];
-                    mbar_expect_tx(&S.full[slot], (uint32_t)(P.kpb + P.vpb));
-                    bulk_g2s(st, key_page(P, U, p), (uint32_t)P.kpb, &S.full[slot]);
-                    bulk_g2s(st + VREC_OFF, P.v_pages + (U.bk * P.page_cap + p) * (int64_t)P.vpb, (uint32_t)P.vpb,
-                             &S.full[slot]);
-                }
-            }
-            for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
-        }
+        if (lane == 0) kitty_produce<NSTAGE>(P, P.Hq, S.stage, S.full, S.empty);
         return;
     }
 
@@ -171,7 +90,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Para
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit U = unit_of(P, u);
+        const Unit U = unit_of(P, u, P.Hq);
         float qa[4];
         {
             const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D + 4 * lane);
@@ -182,76 +101,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Para
         }
         if (U.residual) {
             // ---------------- tokens outside whole pages ----------------
-            // token list: sink [0, nA), then [S + Pf*G, L)
-            const int nA = min(U.L, P.S);
-            const int tB = P.S + U.p0 * PG;
-            const int nB = max(0, U.L - tB);
-            const int ntok = nA + nB;
             if (warp == 0) *reinterpret_cast<float4 *>(&S.qv[4 * lane]) = make_float4(qa[0], qa[1], qa[2], qa[3]);
             asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
-            float m_run = -INFINITY, l_part = 0.f, racc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint16_t *ksink = P.k_sink + U.bk * (int64_t)P.S * KVQ_D;
-            const uint16_t *vsink = P.v_sink + U.bk * (int64_t)P.S * KVQ_D;
-            const uint16_t *kqb = P.k_qbuf + U.bk * (int64_t)PG * KVQ_D;
-            const uint16_t *vqb = P.v_qbuf + U.bk * (int64_t)PG * KVQ_D;
-            const uint16_t *vloc = P.v_local + U.bk * (int64_t)P.R * KVQ_D;
-            const int vq_end = P.S + U.nVp * PG + U.nvb;           // value Q-buffer tokens end here
-            for (int i0 = 32 * warp; i0 < ntok; i0 += 32 * NCWARP) {
-                const int n = min(32, ntok - i0);
-                // ---- keys: lane = token ----
-                const int i = i0 + min(lane, n - 1);
-                const int t = i < nA ? i : tB + (i - nA);
-                float logit = 0.f;
-                if (t < P.S || t >= P.S + U.nKp * PG) {
-                    const uint16_t *row = t < P.S ? ksink + (int64_t)t * KVQ_D : kqb + (int64_t)((t - P.S) % PG) * KVQ_D;
-#pragma unroll 4
-                    for (int c8 = 0; c8 < 16; ++c8) {
-                        const uint4 u4 = __ldg(reinterpret_cast<const uint4 *>(row) + c8);
-                        const float4 qa0 = *reinterpret_cast<const float4 *>(&S.qv[8 * c8]);
-                        const float4 qa1 = *reinterpret_cast<const float4 *>(&S.qv[8 * c8 + 4]);
-                        logit += qa0.x * h2f(lo16(u4.x)) + qa0.y * h2f(hi16(u4.x)) + qa0.z * h2f(lo16(u4.y)) +
-                                 qa0.w * h2f(hi16(u4.y)) + qa1.x * h2f(lo16(u4.z)) + qa1.y * h2f(hi16(u4.z)) +
-                                 qa1.z * h2f(lo16(u4.w)) + qa1.w * h2f(hi16(u4.w));
-                    }
-                } else {
-                    const int p = (t - P.S) / PG, tt = (t - P.S) % PG;
-                    const uint8_t *pg = key_page(P, U, p);
-                    const uint8_t *low = pg, *high = pg + KVQ_D * PG / 4, *idx = high + (int64_t)K * PG / 4;
-                    const uint16_t *ps = reinterpret_cast<const uint16_t *>(idx + KVQ_D);
-                    for (int c = 0; c < KVQ_D; ++c) {
-                        int code = (low[c * (PG / 4) + tt / 4] >> (2 * (tt & 3))) & 3;
-                        const int r = idx[c];
-                        if (r < K) code |= ((high[r * (PG / 4) + tt / 4] >> (2 * (tt & 3))) & 3) << 2;
-                        logit += S.qv[c] * ((float)code * h2f(ps[c]) + h2f(ps[KVQ_D + c]));
-                    }
-                }
-                if (lane >= n) logit = -INFINITY;
-                const float mt = warp_max(logit);
-                if (mt > m_run) {
-                    const float sc = exp2f(m_run - mt);
-                    l_part *= sc;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) racc[k] *= sc;
-                    m_run = mt;
-                }
-                const float p = exp2f(logit - m_run);
-                l_part += p;
-                // ---- values: lane = channels 4*lane..4*lane+3; every value here is fp16 ----
-#pragma unroll 8
-                for (int j = 0; j < 32; ++j) {
-                    const int ij = i0 + min(j, n - 1);
-                    const int tj = ij < nA ? ij : tB + (ij - nA);
-                    const uint16_t *vrow = tj < P.S ? vsink + (int64_t)tj * KVQ_D
-                                         : tj < vq_end ? vqb + (int64_t)((tj - P.S) % PG) * KVQ_D
-                                                       : vloc + (int64_t)(tj % P.R) * KVQ_D;
-                    const uint2 vv = __ldg(reinterpret_cast<const uint2 *>(vrow + 4 * lane));
-                    const float pj = __shfl_sync(0xFFFFFFFFu, p, j);        // 0 for j >= n
-                    racc[0] += pj * h2f(lo16(vv.x));
-                    racc[1] += pj * h2f(hi16(vv.x));
-                    racc[2] += pj * h2f(lo16(vv.y));
-                    racc[3] += pj * h2f(hi16(vv.y));
-                }
-            }
+            float m_run, l_part, racc[4];
+            kitty_residual(P, U, S.qv, warp, lane, racc, m_run, l_part);
             const float l_w = warp_sum(l_part);
             *reinterpret_cast<float4 *>(&S.st_acc[warp][4 * lane]) = make_float4(racc[0], racc[1], racc[2], racc[3]);
             if (lane == 0) {

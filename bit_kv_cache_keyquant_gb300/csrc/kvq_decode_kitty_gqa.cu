@@ -1,0 +1,441 @@
+// a7 for grouped-query heads: Kitty split-KV decode attention, stage 1, with
+// all g <= 4 query heads of a kv head in one unit and both contractions on
+// the tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation).
+//
+// A page (Kitty, "Page-Centric Memory Layout and Dense-Sparse
+// Decomposition") holds the key low plane [D][G/4] (byte (c, t/4), bits
+// 2(t%4)), the high plane of the K boosted channels, the boost index and a
+// per-channel (s, z); the value page holds token-major codes and a per-token
+// (s, z).  The key code is X = low + 4 high, so
+//   logit_ht = sum_c low_tc W_hc + sum_{r<K} high_tr 4 W_h,c(r) + alpha sum_c q_hc z_c
+// with W_hc = alpha q_hc s_c: the dense low plane is eight 16-channel
+// k-steps, the sparse high plane ceil(K/16) more k-steps whose B rows are
+// the boosted channels' weights (dense-sparse decomposition on the tensor
+// cores).  The k-steps gather the low-plane bytes of a lane's token quad
+// from four channel rows; codes become exact fp16 operands through e4m3 bit
+// patterns, weights are fp16 hi / lo pairs (see kvq_mma.cuh), with
+// 2^sigma_h |alpha q| < 1/4 so that 4 W stays in fp16 range.
+// Values are the per-token 2-bit codes of the KIVI grouped-query kernel with
+// one (s, z) per token.  Tokens outside whole pages are the residual unit,
+// per head on CUDA cores.
+#include "kvq_kitty.cuh"
+#include "kvq_mma.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int KQ_NSTAGE = 3;
+constexpr int KG_MAX = 4;                 // query heads per unit
+constexpr int KPB_ROW = 34;               // p exchange row (32 tokens + 2): conflict-free stores
+constexpr int KACC_ROW = KVQ_D + 8;
+
+struct SmemKG {
+    uint8_t stage[KQ_NSTAGE][STAGE_BYTES];
+    uint64_t full[KQ_NSTAGE];
+    uint64_t empty[KQ_NSTAGE];
+    uint32_t qhi[KG_MAX][64];             // fp16x2 hi parts of alpha q 2^sigma: [head][k/2][r][4]
+    uint32_t qlo[KG_MAX][64];
+    float qz[KG_MAX][KVQ_D];              // alpha q (fp32): [head][k][r][4]
+    float qv[KVQ_D];                      // alpha q of one head, channel order (residual unit)
+    float unsig[KG_MAX];                  // 2^-sigma_h
+    uint8_t hchan[NCWARP][KMAX + 16];     // channel of boosted row r (per warp copy)
+    float pbuf[NCWARP][KG_MAX * KPB_ROW];
+    float st_acc[NCWARP][KG_MAX][KACC_ROW];
+    float st_m[NCWARP][KG_MAX];
+    float st_l[NCWARP][KG_MAX];
+};
+
+// fragment-table word and half of channel c (tables [k/2][r][4] of fp16x2 pairs)
+__device__ __forceinline__ int qtab_word(int c) {
+    const int k = c >> 4, cc = c & 15;
+    return (k >> 1) * 16 + ((cc & 7) >> 1) * 4 + 2 * (k & 1) + (cc >> 3);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(Params P) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    SmemKG &S = *reinterpret_cast<SmemKG *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = P.Hq / P.Hkv;
+    const int n_units = P.B * P.Hkv * P.splits;
+    const int K = P.K;
+    const int n_hk = (K + 15) >> 4;               // high-plane k-steps
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < KQ_NSTAGE; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], NCWARP);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCWARP) {
+        if (lane == 0) kitty_produce<KQ_NSTAGE>(P, P.Hkv, S.stage, S.full, S.empty);
+        return;
+    }
+
+    const int q = lane >> 2, r = lane & 3;
+    const int hB = q >> 1;
+    const bool xB = (q & 1) != 0;
+    const int col = 8 * warp + q;                 // low-plane byte column: tokens 32w + 4q + p, bits 2p
+    const uint32_t bsel = (uint32_t)(col & 3) * 0x11u + 0x40u;   // bytes col%4 of a, b -> bytes 0, 1
+    const uint32_t vsel = (uint32_t)((q >> 2) | ((4 + (q >> 2)) << 4) | ((2 + (q >> 2)) << 8) | ((6 + (q >> 2)) << 12));
+    const uint32_t vshift = (q & 2) ? 4u : 0u;
+    const uint32_t vmask = (q & 1) ? 0x0C0C0C0Cu : 0x03030303u;
+    const float vscale = (q & 1) ? 128.f : 512.f;
+    bool ok = true;
+    int sg = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = unit_of(P, u, P.Hkv);     // U.hq is the kv head
+        // ---- per-unit query tables: warp w prepares head w ----
+        {
+            const int h = warp;
+            const int c0 = 16 * (lane & 7) + 2 * (lane >> 3);
+            float qv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (h < g) {
+                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+                const uint32_t q01 = *reinterpret_cast<const uint32_t *>(qrow + c0);
+                const uint32_t q89 = *reinterpret_cast<const uint32_t *>(qrow + c0 + 8);
+                qv[0] = h2f(lo16(q01)) * P.alpha;
+                qv[1] = h2f(hi16(q01)) * P.alpha;
+                qv[2] = h2f(lo16(q89)) * P.alpha;
+                qv[3] = h2f(hi16(q89)) * P.alpha;
+            }
+            const float m = warp_max(fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3]))));
+            // 2^sigma m in [1/8, 1/4): |4 W| = |4 alpha q s| 2^sigma stays below 65504
+            int ex = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
+            int sigma = m > 0.f ? -ex - 3 : 0;
+            sigma = max(-120, min(120, sigma));
+            const float sc = __int_as_float((127 + sigma) << 23);
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v = qv[j] * sc;
+                hi[j] = f2h_rn(v);
+                lo[j] = f2h_rn(v - h2f(hi[j]));
+            }
+            const int tr = lane >> 3, tk = lane & 7;
+            const int pw = (tk >> 1) * 16 + tr * 4 + 2 * (tk & 1);
+            *reinterpret_cast<uint2 *>(&S.qhi[h][pw]) =
+                make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+            *reinterpret_cast<uint2 *>(&S.qlo[h][pw]) =
+                make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+            *reinterpret_cast<float4 *>(&S.qz[h][tk * 16 + tr * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+            if (lane == 0) S.unsig[h] = __int_as_float((127 - sigma) << 23);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+
+        if (U.residual) {
+            for (int h = 0; h < g; ++h) {
+                if (warp == 0) {
+                    const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+                    const uint2 qr = *reinterpret_cast<const uint2 *>(qrow + 4 * lane);
+                    *reinterpret_cast<float4 *>(&S.qv[4 * lane]) =
+                        make_float4(h2f(lo16(qr.x)) * P.alpha, h2f(hi16(qr.x)) * P.alpha, h2f(lo16(qr.y)) * P.alpha,
+                                    h2f(hi16(qr.y)) * P.alpha);
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+                float m_run, l_part, racc[4];
+                kitty_residual(P, U, S.qv, warp, lane, racc, m_run, l_part);
+                const float l_w = warp_sum(l_part);
+                *reinterpret_cast<float4 *>(&S.st_acc[warp][h][4 * lane]) = make_float4(racc[0], racc[1], racc[2], racc[3]);
+                if (lane == 0) {
+                    S.st_m[warp][h] = m_run;
+                    S.st_l[warp][h] = l_w;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+            }
+        } else {
+            float m_run = -INFINITY, l_part = 0.f, vz = 0.f;   // head r
+            float vacc[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vacc[i][0] = vacc[i][1] = vacc[i][2] = vacc[i][3] = 0.f;
+            const float unsig = S.unsig[r];
+            for (int s = 0; s < U.np; ++s, ++sg) {
+                const int slot = sg % KQ_NSTAGE;
+                ok = ok && mbar_wait(&S.full[slot], (sg / KQ_NSTAGE) & 1, P.err);
+                if (ok) {
+                    const uint8_t *st = S.stage[slot];
+                    const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + K * PG / 4;
+                    const uint16_t *ks = reinterpret_cast<const uint16_t *>(idx + KVQ_D);   // s [D], then z [D]
+                    // ---- boosted-row channel table of this page ----
+                    {
+                        const uint32_t id4 = *reinterpret_cast<const uint32_t *>(idx + 4 * lane);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = (id4 >> (8 * i)) & 0xFF;
+                            if (rr < K) S.hchan[warp][rr] = (uint8_t)(4 * lane + i);
+                        }
+                        for (int rr = K + lane; rr < 16 * n_hk; rr += 32) S.hchan[warp][rr] = 0xFF;   // rows past K
+                    }
+                    // ---- alpha sum_c q_hc z_c: the lanes of head hB split the lane's channels by xB ----
+                    float zr;
+                    {
+                        float zp = 0.f;
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) {
+                            const int k = xB ? 7 - n : n;
+                            const int c0 = 16 * k + 2 * r;
+                            const uint32_t z01 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0);
+                            const uint32_t z89 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0 + 8);
+                            const float4 qa = *reinterpret_cast<const float4 *>(&S.qz[hB][k * 16 + 4 * r]);
+                            zp = fmaf(qa.x, h2f(lo16(z01)), zp);
+                            zp = fmaf(qa.y, h2f(hi16(z01)), zp);
+                            zp = fmaf(qa.z, h2f(lo16(z89)), zp);
+                            zp = fmaf(qa.w, h2f(hi16(z89)), zp);
+                        }
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
+                        zr = __shfl_sync(0xFFFFFFFFu, zp, 8 * r);
+                    }
+                    __syncwarp();
+                    // ---- low plane x W, then the boosted rows x 4W, on the tensor cores ----
+                    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                    {
+                        const uint32_t *lw = reinterpret_cast<const uint32_t *>(low) + 2 * warp + (q >> 2);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
+                            const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
+                            uint32_t sv[4];
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const int c0 = 16 * (2 * i + kk) + 2 * r;
+                                sv[2 * kk] = *reinterpret_cast<const uint32_t *>(ks + c0);
+                                sv[2 * kk + 1] = *reinterpret_cast<const uint32_t *>(ks + c0 + 8);
+                            }
+                            const uint32_t bk[4] = {split_prod(a.x, l.x, sv[0], xB), split_prod(a.y, l.y, sv[1], xB),
+                                                    split_prod(a.z, l.z, sv[2], xB), split_prod(a.w, l.w, sv[3], xB)};
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const int c0 = 16 * (2 * i + kk) + 2 * r;
+                                const uint32_t x01 = prmt(lw[c0 * 8], lw[(c0 + 1) * 8], bsel);
+                                const uint32_t x89 = prmt(lw[(c0 + 8) * 8], lw[(c0 + 9) * 8], bsel);
+                                const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
+                                uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
+                                e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
+                                e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
+                                e4m3x4_f16x2(w4 & 0x03030303u, a2l, a2h);
+                                e4m3x4_f16x2(w4 & 0x0C0C0C0Cu, a3l, a3h);
+                                mma16816(s0, a0l, a1l, a0h, a1h, bk[2 * kk], bk[2 * kk + 1]);
+                                mma16816(s1, a2l, a3l, a2h, a3h, bk[2 * kk], bk[2 * kk + 1]);
+                            }
+                        }
+                        // boosted rows 16hk + {2r, 2r+1, 2r+8, 2r+9}: B = 4 W of their channels, 0 past K
+                        const uint32_t *hw = reinterpret_cast<const uint32_t *>(high) + 2 * warp + (q >> 2);
+                        for (int hk = 0; hk < n_hk; ++hk) {
+                            const int r0 = 16 * hk + 2 * r;
+                            const int rows[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
+                            uint32_t qh2[2] = {0u, 0u}, ql2[2] = {0u, 0u}, s2[2] = {0u, 0u};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int ch = S.hchan[warp][rows[j]];
+                                if (ch != 0xFF) {
+                                    const int wq = qtab_word(ch), hs = 16 * (ch & 1);
+                                    const uint32_t qh = (S.qhi[hB][wq] >> hs) & 0xFFFFu, ql = (S.qlo[hB][wq] >> hs) & 0xFFFFu;
+                                    const uint32_t sh = ks[ch];
+                                    qh2[j >> 1] |= qh << (16 * (j & 1));
+                                    ql2[j >> 1] |= ql << (16 * (j & 1));
+                                    s2[j >> 1] |= sh << (16 * (j & 1));
+                                }
+                            }
+                            // 4 W = (4 qhi) s + ...: scaling the query parts by 4 is exact
+                            const uint32_t b0 = split_prod(hmul2(qh2[0], 0x44004400u), hmul2(ql2[0], 0x44004400u), s2[0], xB);
+                            const uint32_t b1 = split_prod(hmul2(qh2[1], 0x44004400u), hmul2(ql2[1], 0x44004400u), s2[1], xB);
+                            // rows past K read finite bytes; their B rows are zero
+                            const uint32_t x01 = prmt(hw[r0 * 8], hw[(r0 + 1) * 8], bsel);
+                            const uint32_t x89 = prmt(hw[(r0 + 8) * 8], hw[(r0 + 9) * 8], bsel);
+                            const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
+                            uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
+                            e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
+                            e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
+                            e4m3x4_f16x2(w4 & 0x03030303u, a2l, a2h);
+                            e4m3x4_f16x2(w4 & 0x0C0C0C0Cu, a3l, a3h);
+                            mma16816(s0, a0l, a1l, a0h, a1h, b0, b1);
+                            mma16816(s1, a2l, a3l, a2h, a3h, b0, b1);
+                        }
+                    }
+                    // ---- logits of head r, tokens 32w + 4q + p; online softmax ----
+                    const float f9 = unsig * 512.f, f7 = unsig * 128.f;
+                    float lg[4];
+                    lg[0] = fmaf(s0[0] + s0[1], f9, zr);
+                    lg[1] = fmaf(s0[2] + s0[3], f7, zr);
+                    lg[2] = fmaf(s1[0] + s1[1], f9, zr);
+                    lg[3] = fmaf(s1[2] + s1[3], f7, zr);
+                    float mt = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 4));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
+                    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
+                    if (mt > m_run) {
+                        const float sc = exp2f(m_run - mt);
+                        l_part *= sc;
+                        vz *= sc;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            vacc[i][0] *= sc; vacc[i][1] *= sc; vacc[i][2] *= sc; vacc[i][3] *= sc;
+                        }
+                        m_run = mt;
+                    }
+                    float pr[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        pr[i] = exp2f(lg[i] - m_run);
+                        l_part += pr[i];
+                    }
+                    // token t = 16k + 8hk + 4e + j of the tile sits at position 16k + 8hk + 2j + e
+                    float *pb = S.pbuf[warp];
+                    const int pbase = 16 * (q >> 2) + 8 * ((q >> 1) & 1) + (q & 1);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pb[r * KPB_ROW + pbase + 2 * i] = pr[i];
+                    // ---- value zero-point term of head r over the lane's four tokens ----
+                    const uint8_t *vrec = st + VREC_OFF;
+                    const uint16_t *vs = reinterpret_cast<const uint16_t *>(vrec + PG * KVQ_D / 4) + 32 * warp;
+                    {
+                        const uint2 z4 = *reinterpret_cast<const uint2 *>(vs + PG + 4 * q);
+                        vz = fmaf(pr[0], h2f(lo16(z4.x)), vz);
+                        vz = fmaf(pr[1], h2f(hi16(z4.x)), vz);
+                        vz = fmaf(pr[2], h2f(lo16(z4.y)), vz);
+                        vz = fmaf(pr[3], h2f(hi16(z4.y)), vz);
+                    }
+                    __syncwarp();
+                    // ---- values: k-column 2j + e + 8hk of k-step k is token 16k + 8hk + 4e + j ----
+                    const uint8_t *vc = vrec + warp * 32 * (KVQ_D / 4);
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int t0 = 16 * kv + r;             // tokens t0, t0+4 | t0+8, t0+12
+                        const float2 pa = *reinterpret_cast<const float2 *>(&pb[hB * KPB_ROW + 16 * kv + 2 * r]);
+                        const float2 pc = *reinterpret_cast<const float2 *>(&pb[hB * KPB_ROW + 16 * kv + 8 + 2 * r]);
+                        const uint32_t pha = split_pair(pa.x, pa.y, false), pla = split_pair(pa.x, pa.y, true);
+                        const uint32_t phc = split_pair(pc.x, pc.y, false), plc = split_pair(pc.x, pc.y, true);
+                        const uint32_t sa = (uint32_t)vs[t0] | ((uint32_t)vs[t0 + 4] << 16);
+                        const uint32_t sc8 = (uint32_t)vs[t0 + 8] | ((uint32_t)vs[t0 + 12] << 16);
+                        const uint32_t bv0 = split_prod(pha, pla, sa, xB);
+                        const uint32_t bv1 = split_prod(phc, plc, sc8, xB);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 32 + 16 * hf);
+                            const uint4 rB = *reinterpret_cast<const uint4 *>(vc + (t0 + 4) * 32 + 16 * hf);
+                            const uint4 rC = *reinterpret_cast<const uint4 *>(vc + (t0 + 8) * 32 + 16 * hf);
+                            const uint4 rD = *reinterpret_cast<const uint4 *>(vc + (t0 + 12) * 32 + 16 * hf);
+                            const uint32_t wa[4] = {rA.x, rA.y, rA.z, rA.w}, wb[4] = {rB.x, rB.y, rB.z, rB.w};
+                            const uint32_t wc[4] = {rC.x, rC.y, rC.z, rC.w}, wd[4] = {rD.x, rD.y, rD.z, rD.w};
+#pragma unroll
+                            for (int m4 = 0; m4 < 4; ++m4) {
+                                const int mt = 4 * hf + m4;
+                                uint32_t c0l, c0h, c8l, c8h;
+                                e4m3x4_f16x2((prmt(wa[m4], wb[m4], vsel) >> vshift) & vmask, c0l, c0h);
+                                e4m3x4_f16x2((prmt(wc[m4], wd[m4], vsel) >> vshift) & vmask, c8l, c8h);
+                                mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0, bv1);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
+            }
+            // ---- warp state (head r) -> shared memory ----
+            float l_w = l_part;
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 4);
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
+            vz += __shfl_xor_sync(0xFFFFFFFFu, vz, 4);
+            vz += __shfl_xor_sync(0xFFFFFFFFu, vz, 8);
+            vz += __shfl_xor_sync(0xFFFFFFFFu, vz, 16);
+            float *acc = S.st_acc[warp][r];
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                acc[16 * mt + q] = fmaf(vacc[mt][0] + vacc[mt][1], vscale, vz);
+                acc[16 * mt + q + 8] = fmaf(vacc[mt][2] + vacc[mt][3], vscale, vz);
+            }
+            if (q == 0) {
+                S.st_m[warp][r] = m_run;
+                S.st_l[warp][r] = l_w;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+        // ---- warp w merges head w over the four warp states, writes (o_s, lse_s) ----
+        if (warp < g) {
+            const int h = warp;
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i][h]);
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NCWARP; ++i) {
+                    const float w = S.st_m[i][h] > -INFINITY ? exp2f(S.st_m[i][h] - M) : 0.f;
+                    l += w * S.st_l[i][h];
+                    const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][h][4 * lane]);
+                    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+                }
+            }
+            const int64_t row = (((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h)) * P.splits + U.split;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+    }
+}
+
+bool kitty_gqa_supported(const kvq_config *cfg) {
+    const int g = cfg->n_q_heads / cfg->n_kv_heads;
+    return g >= 2 && g <= KG_MAX;
+}
+
+cudaError_t launch_decode_kitty_gqa(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,
+                                    const DecodePlan &p, void *ws, cudaStream_t st) {
+    Params P;
+    P.seq_len = c->seq_len;
+    P.k_pages = static_cast<const uint8_t *>(c->k_pages);
+    P.v_pages = static_cast<const uint8_t *>(c->v_pages);
+    P.k_sink = static_cast<const uint16_t *>(c->k_sink);
+    P.v_sink = static_cast<const uint16_t *>(c->v_sink);
+    P.k_qbuf = static_cast<const uint16_t *>(c->k_qbuf);
+    P.v_qbuf = static_cast<const uint16_t *>(c->v_qbuf);
+    P.v_local = static_cast<const uint16_t *>(c->v_local);
+    P.q = static_cast<const uint16_t *>(q);
+    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
+    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
+    P.err = device_error_ptr();
+    P.B = c->batch;
+    P.Hq = cfg->n_q_heads;
+    P.Hkv = cfg->n_kv_heads;
+    P.S = cfg->sink;
+    P.R = cfg->residual;
+    P.K = cfg->boost_k;
+    P.splits = p.splits;
+    P.chunk = p.chunk;
+    P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + PG - 1) / PG;
+    if (P.page_cap < 1) P.page_cap = 1;
+    P.kpb = KVQ_D * PG / 4 + cfg->boost_k * PG / 4 + KVQ_D + 4 * KVQ_D;
+    P.vpb = PG * KVQ_D / 4 + 4 * PG;
+    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    P.e0 = 0;
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    if (P.kpb > VREC_OFF || P.K > KMAX) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(SmemKG);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kitty_decode_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
+    int64_t grid = (int64_t)num_sms() * 4;
+    if (grid > n_units) grid = n_units;
+    kitty_decode_gqa_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

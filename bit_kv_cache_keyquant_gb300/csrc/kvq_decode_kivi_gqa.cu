@@ -28,13 +28,15 @@
 // stages with bulk async copies into an mbarrier ring; four consumer warps
 // each take one 32-token tile (two 16-token m-tiles) per stage; the last
 // split of every row is the residual unit, done per head on CUDA cores.
+// Four CTAs per SM with a three-stage ring keep 16 consumer warps resident.
 #include "kvq_kivi.cuh"
+#include "kvq_mma.cuh"
 
 namespace kvq {
 
 namespace {
 
-constexpr int GQ_NSTAGE = 4;
+constexpr int GQ_NSTAGE = 3;
 constexpr int GMAX = 4;                   // query heads per unit (n = 8 tensor-core columns)
 constexpr int PB_ROW = 40;                // p exchange row: 32 tokens + 8 floats (conflict-free)
 constexpr int ACC_ROW = KVQ_D + 8;
@@ -53,67 +55,10 @@ struct SmemG {
     float st_l[NCWARP][GMAX];
 };
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v16) {
-    uint32_t d;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v16));
-    return d;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// fp16x2 product a*b as its hi part (x == 0) or its lo part (x == 1):
-// hi = fl(ah b); lo = fl(al b + fl(ah b - hi)), the inner FMA being exact.
-__device__ __forceinline__ uint32_t split_prod(uint32_t ah, uint32_t al, uint32_t b, bool x) {
-    const uint32_t hi = hmul2(ah, b);
-    return x ? hfma2(al, b, hfma2(ah, b, hi ^ 0x80008000u)) : hi;
-}
-// fp32 pair -> fp16x2 hi (x == 0) or lo = fl(v - hi) (x == 1); first value in the low half
-__device__ __forceinline__ uint32_t split_pair(float v0, float v1, bool x) {
-    uint32_t hi;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(v1), "f"(v0));
-    if (!x) return hi;
-    const float r0 = v0 - h2f(lo16(hi)), r1 = v1 - h2f(hi16(hi));
-    uint32_t lo;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(r1), "f"(r0));
-    return lo;
-}
-
-template <int N>
-__device__ __forceinline__ void load_row(const uint32_t *p, uint32_t (&v)[N]) {
-    if constexpr (N == 4) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(p);
-        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
-    } else if constexpr (N == 2) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(p);
-        v[0] = u.x; v[1] = u.y;
-    } else {
-        v[0] = *p;
-    }
-}
-
 }  // namespace
 
 template <int NGV>
-__global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(Params P) {
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(Params P) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SmemG &S = *reinterpret_cast<SmemG *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -218,20 +163,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(P
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];
                     const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + KC_BYTES) + gl * 2 * KVQ_D;
-                    // ---- key B fragments (head hB, hi or lo), channels 16k + 2r + {0,1 | 8,9} ----
-                    uint32_t bk[16];
-                    {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
-                            const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
-                            const uint4 sv = *reinterpret_cast<const uint4 *>(ksz + (4 * i + r) * 8);
-                            bk[4 * i + 0] = split_prod(a.x, l.x, sv.x, xB);
-                            bk[4 * i + 1] = split_prod(a.y, l.y, sv.y, xB);
-                            bk[4 * i + 2] = split_prod(a.z, l.z, sv.z, xB);
-                            bk[4 * i + 3] = split_prod(a.w, l.w, sv.w, xB);
-                        }
-                    }
                     // ---- alpha sum_c q_hc z_c: the lanes of head hB split the lane's 32 channels by xB ----
                     float zr;
                     {
@@ -252,7 +183,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(P
                         zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
                         zr = __shfl_sync(0xFFFFFFFFu, zp, 8 * r);   // head r lives in lanes 8r..8r+7
                     }
-                    // ---- key codes x B on the tensor cores: tokens q + 8p, p = 0..3 ----
+                    // ---- key codes x B on the tensor cores: tokens q + 8p, p = 0..3; B fragments (head hB,
+                    //      hi or lo) of channels 16k + 2r + {0,1 | 8,9} made two k-steps at a time ----
                     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
                     {
                         const uint8_t *kt = st + warp * 1024;
@@ -260,14 +192,24 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(P
                         const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
                         const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint32_t w = kw[k], w4 = kw[k] >> 4;
-                            const uint32_t m0 = w & 0x03030303u, m1 = w & 0x0C0C0C0Cu;
-                            const uint32_t m2 = w4 & 0x03030303u, m3 = w4 & 0x0C0C0C0Cu;
-                            mma16816(s0, e4m3x2_f16x2(m0), e4m3x2_f16x2(m1), e4m3x2_f16x2(m0 >> 16),
-                                     e4m3x2_f16x2(m1 >> 16), bk[2 * k], bk[2 * k + 1]);
-                            mma16816(s1, e4m3x2_f16x2(m2), e4m3x2_f16x2(m3), e4m3x2_f16x2(m2 >> 16),
-                                     e4m3x2_f16x2(m3 >> 16), bk[2 * k], bk[2 * k + 1]);
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
+                            const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
+                            const uint4 sv = *reinterpret_cast<const uint4 *>(ksz + (4 * i + r) * 8);
+                            const uint32_t bk[4] = {split_prod(a.x, l.x, sv.x, xB), split_prod(a.y, l.y, sv.y, xB),
+                                                    split_prod(a.z, l.z, sv.z, xB), split_prod(a.w, l.w, sv.w, xB)};
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const int k = 2 * i + kk;
+                                const uint32_t w = kw[k], w4 = kw[k] >> 4;
+                                uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
+                                e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
+                                e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
+                                e4m3x4_f16x2(w4 & 0x03030303u, a2l, a2h);
+                                e4m3x4_f16x2(w4 & 0x0C0C0C0Cu, a3l, a3h);
+                                mma16816(s0, a0l, a1l, a0h, a1h, bk[2 * kk], bk[2 * kk + 1]);
+                                mma16816(s1, a2l, a3l, a2h, a3h, bk[2 * kk], bk[2 * kk + 1]);
+                            }
                         }
                     }
                     // ---- logits of head r, tokens q, q+8, q+16, q+24; online softmax ----
@@ -350,10 +292,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(P
                             for (int m4 = 0; m4 < 4; ++m4) {
                                 const int mt = 4 * hf + m4;
                                 const int j = (16 * mt) / (KVQ_D / NGV);       // value group of the m-tile
-                                const uint32_t y01 = (prmt(wa[m4], wb[m4], vsel) >> vshift) & vmask;
-                                const uint32_t y89 = (prmt(wc[m4], wd[m4], vsel) >> vshift) & vmask;
-                                mma16816(vacc[mt], e4m3x2_f16x2(y01), e4m3x2_f16x2(y01 >> 16), e4m3x2_f16x2(y89),
-                                         e4m3x2_f16x2(y89 >> 16), bv0[j], bv1[j]);
+                                uint32_t c0l, c0h, c8l, c8h;
+                                e4m3x4_f16x2((prmt(wa[m4], wb[m4], vsel) >> vshift) & vmask, c0l, c0h);
+                                e4m3x4_f16x2((prmt(wc[m4], wd[m4], vsel) >> vshift) & vmask, c8l, c8h);
+                                mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0[j], bv1[j]);
                             }
                         }
                     }
@@ -463,7 +405,7 @@ cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *
         attr_dev[ti] = dev;
     }
     const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
-    int64_t grid = (int64_t)num_sms() * 3;
+    int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
     if (ngv == 4) kivi_decode_gqa_kernel<4><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
     else if (ngv == 2) kivi_decode_gqa_kernel<2><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);

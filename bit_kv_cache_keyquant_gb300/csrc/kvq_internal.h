@@ -41,6 +41,10 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
 bool kivi_gqa_supported(const kvq_config *cfg);
 cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q,
                                    const DecodePlan &p, void *ws, cudaStream_t st);
+// grouped-query Kitty decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
+bool kitty_gqa_supported(const kvq_config *cfg);
+cudaError_t launch_decode_kitty_gqa(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,
+                                    const DecodePlan &p, void *ws, cudaStream_t st);
 cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,
                                 const DecodePlan &p, void *ws, cudaStream_t st);
 cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *q,
