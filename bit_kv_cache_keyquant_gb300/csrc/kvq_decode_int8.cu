@@ -57,6 +57,7 @@ struct Params {
     int B, Hq, Hkv, g, T, splits, chunk, blk_cap;
     int64_t cap;
     uint32_t ctr2_layer, k0, k1;
+    uint32_t rk0[10], rk1[10];   // Philox round keys (k0 + r*0x9E3779B9, k1 + r*0xBB67AE85)
     float alpha;
 };
 
@@ -87,10 +88,24 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u) {
     return U;
 }
 
+// Philox4x32-10 with the round keys taken from the kernel parameters (the
+// same bijection as philox4x32_10: 32x32->64 products, xor with the round
+// key; only the key schedule is precomputed).
+__device__ __forceinline__ uint4 philox_rk(uint4 c, const uint32_t *rk0, const uint32_t *rk1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        unsigned long long pa, pb;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(pa) : "r"(c.x), "r"(0xD2511F53u));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(pb) : "r"(c.z), "r"(0xCD9E8D57u));
+        c = make_uint4((uint32_t)(pb >> 32) ^ c.y ^ rk0[r], (uint32_t)pb, (uint32_t)(pa >> 32) ^ c.w ^ rk1[r],
+                       (uint32_t)pa);
+    }
+    return c;
+}
+
 // dither of the four channels 4*lane..4*lane+3 of token t (exact: (w >> 8) 2^-24 - 1/2)
-__device__ __forceinline__ void dither4(uint32_t k0, uint32_t k1, uint32_t c2, uint32_t req, int t, int lane,
-                                        float xi[4]) {
-    const uint4 r = philox4x32_10(make_uint4((uint32_t)t, (uint32_t)lane, c2, req), k0, k1);
+__device__ __forceinline__ void dither4(const Params &P, uint32_t c2, uint32_t req, int t, int lane, float xi[4]) {
+    const uint4 r = philox_rk(make_uint4((uint32_t)t, (uint32_t)lane, c2, req), P.rk0, P.rk1);
     xi[0] = dither_from_word(r.x);
     xi[1] = dither_from_word(r.y);
     xi[2] = dither_from_word(r.z);
@@ -104,74 +119,84 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t w, float f[4]) {
     f[3] = (float)(int8_t)(w >> 24);
 }
 
-// Per-warp online softmax state for up to GMAX heads.
+// Per-lane attention state: output accumulators of the lane's four channels
+// for all GMAX heads, as (head 2j, head 2j+1) pairs per channel, and the
+// online-softmax state of head lane & 7.
 struct HeadState {
-    float m[GMAX], l[GMAX], acc[GMAX][4];
+    unsigned long long acc2[GMAX / 2][4];
+    float m, l;
 };
 
-// One tile of n <= 32 tokens starting at t0.  kfn(tt, kv[4]) / vfn(tt, vv[4])
-// return this lane's four dequantized channels of token t0 + tt; wk are the
-// key weights alpha q_hc.
+// One tile of n <= 32 tokens.  kfn(tt, kv[4]) / vfn(tt, vv[4]) return this
+// lane's four dequantized channels of token tt of the tile; wk2[j][i] holds
+// the key weights (alpha q) of heads 2j, 2j+1 for channel i.
 template <typename KF, typename VF>
-__device__ __forceinline__ void tile(int n, int g, const float wk[GMAX][4], KF kfn, VF vfn, HeadState &H,
+__device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 2][4], KF kfn, VF vfn, HeadState &H,
                                      float (*pw)[GMAX], int lane) {
-    float sc[GMAX];
+    // ---- keys: 8 batches of 4 tokens; per lane 4 x 8 head partials over its 4 channels, then a
+    //      reduce-scatter over all 32 lanes leaves lane L with token 4c + L/8, head L%8 ----
+    float sc[8];
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) sc[h] = -INFINITY;
-    // ---- keys: 8 batches of 4 tokens; reduce-scatter over lane bits 4, 3 leaves token
-    //      2*b4 + b3 of a batch in lanes 8m..8m+7, then a sum over lane bits 2..0 ----
+    for (int c = 0; c < 8; ++c) sc[c] = -INFINITY;
 #pragma unroll 1
     for (int c4 = 0; c4 < 8; ++c4) {
-        float d[4][GMAX];
+        float v[32];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             float kv[4];
             kfn(min(4 * c4 + m, n - 1), kv);
 #pragma unroll
-            for (int h = 0; h < GMAX; ++h)
-                d[m][h] = wk[h][0] * kv[0] + wk[h][1] * kv[1] + wk[h][2] * kv[2] + wk[h][3] * kv[3];
+            for (int j = 0; j < GMAX / 2; ++j) {
+                unsigned long long d = 0ull;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d = ffma2(wk2[j][i], pack2f(kv[i], kv[i]), d);
+                v[8 * m + 2 * j] = lo2f(d);
+                v[8 * m + 2 * j + 1] = hi2f(d);
+            }
         }
 #pragma unroll
-        for (int o = 16, hh = 2; o >= 8; o >>= 1, hh >>= 1) {
+        for (int o = 16; o >= 1; o >>= 1) {
             const bool up = (lane & o) != 0;
 #pragma unroll
-            for (int m = 0; m < hh; ++m)
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    const float send = up ? d[m][h] : d[m + hh][h];
-                    d[m][h] = (up ? d[m + hh][h] : d[m][h]) + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-                }
+            for (int j = 0; j < o; ++j) {
+                const float send = up ? v[j] : v[j + o];
+                v[j] = (up ? v[j + o] : v[j]) + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+            }
         }
+        const float s = 4 * c4 + (lane >> 3) < n ? v[0] : -INFINITY;
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-            float v = d[0][h];
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-            const float mine = __shfl_sync(0xFFFFFFFFu, v, 8 * (lane & 3));
-            if ((lane >> 2) == c4 && lane < n) sc[h] = mine;
+        for (int c = 0; c < 8; ++c)
+            if (c == c4) sc[c] = s;
+    }
+    // ---- online softmax of head lane & 7 (its tokens live in lanes h, h+8, h+16, h+24) ----
+    float mt = sc[0];
+#pragma unroll
+    for (int c = 1; c < 8; ++c) mt = fmaxf(mt, sc[c]);
+    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
+    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
+    const float mnew = fmaxf(H.m, mt);
+    const float scl = exp2f(H.m - mnew);
+    H.m = mnew;
+    H.l *= scl;
+#pragma unroll
+    for (int j = 0; j < GMAX / 2; ++j) {
+        const unsigned long long sp =
+            pack2f(__shfl_sync(0xFFFFFFFFu, scl, 2 * j), __shfl_sync(0xFFFFFFFFu, scl, 2 * j + 1));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            unsigned long long d;
+            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(H.acc2[j][i]), "l"(sp));
+            H.acc2[j][i] = d;
         }
     }
-    // ---- per-head online softmax (lane = token) ----
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-        float p = 0.f;
-        if (h < g) {
-            const float mt = warp_max(sc[h]);
-            if (mt > H.m[h]) {
-                const float s = exp2f(H.m[h] - mt);
-                H.l[h] *= s;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) H.acc[h][i] *= s;
-                H.m[h] = mt;
-            }
-            p = exp2f(sc[h] - H.m[h]);
-            H.l[h] += p;             // lane-partial; summed over the warp at the end
-        }
-        pw[lane][h] = p;
+    for (int c = 0; c < 8; ++c) {
+        const float p = exp2f(sc[c] - mnew);
+        H.l += p;
+        pw[4 * c + (lane >> 3)][lane & 7] = p;
     }
     __syncwarp();
-    // ---- values: lane = channels, weights broadcast from shared memory ----
+    // ---- values: lane = channels, head weights broadcast from shared memory ----
 #pragma unroll 4
     for (int tt = 0; tt < 32; ++tt) {
         if (tt >= n) break;
@@ -179,11 +204,14 @@ __device__ __forceinline__ void tile(int n, int g, const float wk[GMAX][4], KF k
         vfn(tt, vv);
         const float4 p0 = *reinterpret_cast<const float4 *>(&pw[tt][0]);
         const float4 p1 = *reinterpret_cast<const float4 *>(&pw[tt][4]);
-        const float pp[GMAX] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        const unsigned long long pp[GMAX / 2] = {pack2f(p0.x, p0.y), pack2f(p0.z, p0.w), pack2f(p1.x, p1.y),
+                                                 pack2f(p1.z, p1.w)};
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h)
+        for (int i = 0; i < 4; ++i) {
+            const unsigned long long vi = pack2f(vv[i], vv[i]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) H.acc[h][i] += pp[h] * vv[i];
+            for (int j = 0; j < GMAX / 2; ++j) H.acc2[j][i] = ffma2(pp[j], vi, H.acc2[j][i]);
+        }
     }
     __syncwarp();
 }
@@ -239,26 +267,32 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit U = unit_of(P, u);
-        // alpha q of the g heads for this lane's four channels
-        float qa[GMAX][4];
+        // alpha q of the g heads for this lane's four channels, as head pairs
+        unsigned long long wk2[GMAX / 2][4];
+        {
+            float qa[GMAX][4];
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-            const int hq = U.kvh * g + min(h, g - 1);
-            const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + hq) * KVQ_D + 4 * lane);
-            const float z = h < g ? P.alpha : 0.f;
-            qa[h][0] = h2f(lo16(qv.x)) * z;
-            qa[h][1] = h2f(hi16(qv.x)) * z;
-            qa[h][2] = h2f(lo16(qv.y)) * z;
-            qa[h][3] = h2f(hi16(qv.y)) * z;
+            for (int h = 0; h < GMAX; ++h) {
+                const int hq = U.kvh * g + min(h, g - 1);
+                const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + hq) * KVQ_D + 4 * lane);
+                const float z = h < g ? P.alpha : 0.f;
+                qa[h][0] = h2f(lo16(qv.x)) * z;
+                qa[h][1] = h2f(hi16(qv.x)) * z;
+                qa[h][2] = h2f(lo16(qv.y)) * z;
+                qa[h][3] = h2f(hi16(qv.y)) * z;
+            }
+#pragma unroll
+            for (int j = 0; j < GMAX / 2; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) wk2[j][i] = pack2f(qa[2 * j][i], qa[2 * j + 1][i]);
         }
         HeadState H;
+        H.m = -INFINITY;
+        H.l = 0.f;
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-            H.m[h] = -INFINITY;
-            H.l[h] = 0.f;
+        for (int j = 0; j < GMAX / 2; ++j)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) H.acc[h][i] = 0.f;
-        }
+            for (int i = 0; i < 4; ++i) H.acc2[j][i] = 0ull;
         const uint32_t c2 = P.ctr2_layer | (uint32_t)U.kvh;
         const uint32_t req = (uint32_t)P.req_id[U.b];
         if (U.residual) {
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                     const uint2 x = __ldg(reinterpret_cast<const uint2 *>(vt + (int64_t)((r0 + tt) % T) * KVQ_D));
                     vv[0] = h2f(lo16(x.x)); vv[1] = h2f(hi16(x.x)); vv[2] = h2f(lo16(x.y)); vv[3] = h2f(hi16(x.y));
                 };
-                tile(n, g, qa, kfn, vfn, H, S.pw[warp], lane);
+                tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
             }
         } else {
             const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
@@ -293,11 +327,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                     const uint2 vs = *reinterpret_cast<const uint2 *>(st + 2 * CODES_BYTES + 2 * KVQ_D + 8 * lane);
                     const float ks0 = h2f(lo16(ks.x)), ks1 = h2f(hi16(ks.x)), ks2 = h2f(lo16(ks.y)), ks3 = h2f(hi16(ks.y));
                     const float vs0 = h2f(lo16(vs.x)), vs1 = h2f(hi16(vs.x)), vs2 = h2f(lo16(vs.y)), vs3 = h2f(hi16(vs.y));
-                    const uint32_t k0 = P.k0, k1 = P.k1;
                     auto kfn = [=](int tt, float kv[4]) {
                         float c[4], xi[4];
                         i8x4_to_f32(*reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c);
-                        dither4(k0, k1, c2, req, r0 + tt, lane, xi);
+                        dither4(P, c2, req, r0 + tt, lane, xi);
                         kv[0] = ks0 * (c[0] - xi[0]);
                         kv[1] = ks1 * (c[1] - xi[1]);
                         kv[2] = ks2 * (c[2] - xi[2]);
@@ -306,27 +339,33 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                     auto vfn = [=](int tt, float vv[4]) {
                         float c[4], xi[4];
                         i8x4_to_f32(*reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c);
-                        dither4(k0, k1, c2 | 0x10000u, req, r0 + tt, lane, xi);
+                        dither4(P, c2 | 0x10000u, req, r0 + tt, lane, xi);
                         vv[0] = vs0 * (c[0] - xi[0]);
                         vv[1] = vs1 * (c[1] - xi[1]);
                         vv[2] = vs2 * (c[2] - xi[2]);
                         vv[3] = vs3 * (c[3] - xi[3]);
                     };
-                    tile(n, g, qa, kfn, vfn, H, S.pw[warp], lane);
+                    tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
         }
         // ---- warp states -> shared memory ----
+        {
+            float l_w = H.l;
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
+            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-            const float l_w = warp_sum(H.l[h]);
-            *reinterpret_cast<float4 *>(&S.st_acc[warp][h][4 * lane]) =
-                make_float4(H.acc[h][0], H.acc[h][1], H.acc[h][2], H.acc[h][3]);
-            if (lane == 0) {
-                S.st_m[warp][h] = H.m[h];
-                S.st_l[warp][h] = l_w;
+            for (int j = 0; j < GMAX / 2; ++j) {
+                *reinterpret_cast<float4 *>(&S.st_acc[warp][2 * j][4 * lane]) =
+                    make_float4(lo2f(H.acc2[j][0]), lo2f(H.acc2[j][1]), lo2f(H.acc2[j][2]), lo2f(H.acc2[j][3]));
+                *reinterpret_cast<float4 *>(&S.st_acc[warp][2 * j + 1][4 * lane]) =
+                    make_float4(hi2f(H.acc2[j][0]), hi2f(H.acc2[j][1]), hi2f(H.acc2[j][2]), hi2f(H.acc2[j][3]));
+            }
+            if (lane < GMAX) {
+                S.st_m[warp][lane] = H.m;
+                S.st_l[warp][lane] = l_w;
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
@@ -385,6 +424,10 @@ cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, c
     P.ctr2_layer = (uint32_t)c->layer << 17;
     P.k0 = (uint32_t)(c->seed & 0xFFFFFFFFu);
     P.k1 = (uint32_t)(c->seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        P.rk0[r] = P.k0 + (uint32_t)r * 0x9E3779B9u;
+        P.rk1[r] = P.k1 + (uint32_t)r * 0xBB67AE85u;
+    }
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
     if (!P.err) return cudaErrorInvalidDevicePointer;
     if (P.g > GMAX) return cudaErrorInvalidValue;
