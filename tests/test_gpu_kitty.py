@@ -45,21 +45,26 @@ def _oracle(orc, cfg, Ks, Vs, q, score_mode=0):
     return out
 
 
-@pytest.mark.parametrize("lens,Kb,mode", [
-    ([1, 20, 33], 16, 0),
-    ([161, 288, 416], 16, 0),
-    ([417, 700, 2000], 16, 0),
-    ([1500, 3000], 32, 0),
-    ([1500, 2222], 16, 1),
-    ([900, 1300], 0, 0),
+@pytest.mark.parametrize("lens,Kb,mode,Hq,Hkv", [
+    ([1, 20, 33], 16, 0, 8, 2),
+    ([161, 288, 416], 16, 0, 8, 2),
+    ([417, 700, 2000], 16, 0, 8, 2),
+    ([1500, 3000], 32, 0, 8, 2),
+    ([1500, 2222], 16, 1, 8, 2),
+    ([900, 1300], 0, 0, 8, 2),
+    ([1700], 48, 0, 8, 2),          # three boosted k-steps
+    ([1300], 92, 0, 4, 2),          # the largest supported boost
+    ([800, 1900], 16, 0, 6, 2),     # three heads per kv head (one dead tensor-core column pair)
+    ([600, 1400], 16, 0, 2, 2),     # one head per kv head: per-head kernel
+    ([1234], 16, 0, 8, 1),          # eight heads per kv head: per-head kernel
 ])
-def test_kitty_decode_parity(K, orc, lens, Kb, mode):
-    rng = np.random.default_rng(sum(lens) + Kb + mode)
-    cfg = K.make_config(n_q_heads=8, n_kv_heads=2, group_k=128, sink=32, residual=128, boost_k=Kb)
-    sig = 10.0 ** rng.uniform(-0.3, 0.9, (2, 128))
-    Ks = [[(rng.standard_normal((L, 128)) * sig[h]).astype(np.float16) for h in range(2)] for L in lens]
-    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for h in range(2)] for L in lens]
-    q = rng.standard_normal((len(lens), 8, 128)).astype(np.float16)
+def test_kitty_decode_parity(K, orc, lens, Kb, mode, Hq, Hkv):
+    rng = np.random.default_rng(sum(lens) + Kb + mode + Hq)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv, group_k=128, sink=32, residual=128, boost_k=Kb)
+    sig = 10.0 ** rng.uniform(-0.3, 0.9, (Hkv, 128))
+    Ks = [[(rng.standard_normal((L, 128)) * sig[h]).astype(np.float16) for h in range(Hkv)] for L in lens]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for h in range(Hkv)] for L in lens]
+    q = rng.standard_normal((len(lens), Hq, 128)).astype(np.float16)
     got = _run(K, cfg, Ks, Vs, q, max(lens) + 7, mode)
     want = _oracle(orc, cfg, Ks, Vs, q, mode)
     assert_attn_close(got, want)

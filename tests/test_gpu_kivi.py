@@ -114,6 +114,12 @@ def _oracle_decode(orc, cfg, Ks, Vs, q):
     (2, 2, 2, [700, 900], 32, 64, 64),
     (1, 1, 1, [128], 32, 32, 128),
     (1, 1, 1, [4095], 32, 32, 256),
+    # grouped-query tensor-core kernel: 3 heads (one dead B column pair), Gv = 64 and 128
+    (3, 6, 2, [97, 1024, 1333], 32, 32, 128),
+    (2, 4, 2, [700, 1900], 32, 64, 64),
+    (1, 8, 4, [1025], 64, 128, 128),
+    # more than 4 query heads per kv head: per-head kernel
+    (1, 8, 1, [1200], 32, 32, 128),
 ])
 def test_decode_parity_small(K, orc, shape):
     B, Hq, Hkv, lens, G, Gv, R = shape
@@ -126,6 +132,22 @@ def test_decode_parity_small(K, orc, shape):
     got = _run_decode(K, cfg, Ks, Vs, q, max(lens) + 5)
     want = _oracle_decode(orc, cfg, Ks, Vs, q)
     assert_attn_close(got, want)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+def test_decode_wide_outlier_channels(K, orc, Hq, Hkv):
+    """Key channels x20 and a large query (the logit scale of the tiny workload): the fp16 hi / lo
+    key weights of the tensor-core path and the exact fp32 products of the per-head path both hold."""
+    rng = np.random.default_rng(Hq * 31 + Hkv)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    lens = [777, 2048]
+    gain = np.ones(128)
+    gain[[3, 40, 77, 120]] = 20.0
+    Ks = [[(rng.standard_normal((L, 128)) * gain).astype(np.float16) for _ in range(Hkv)] for L in lens]
+    Vs = [[(rng.standard_normal((L, 128)) * 3.0).astype(np.float16) for _ in range(Hkv)] for L in lens]
+    q = (rng.standard_normal((2, Hq, 128)) * 2.0).astype(np.float16)
+    got = _run_decode(K, cfg, Ks, Vs, q, 2048)
+    assert_attn_close(got, _oracle_decode(orc, cfg, Ks, Vs, q))
 
 
 def test_decode_capacity_and_split_invariance(K, orc):
