@@ -81,7 +81,11 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     const int hB = q >> 1;
     const bool xB = (q & 1) != 0;
     const int col = 8 * warp + q;                 // low-plane byte column: tokens 32w + 4q + p, bits 2p
-    const uint32_t bsel = (uint32_t)(col & 3) * 0x11u + 0x40u;   // bytes col%4 of a, b -> bytes 0, 1
+    // Lanes r >= 2 load the odd channel row of a pair first (rows 4 apart share banks); the
+    // selector puts the byte col%4 of the even row in byte 0 and of the odd row in byte 1 either way.
+    const int rsw = r >> 1;
+    const uint32_t bsel = rsw ? (uint32_t)(4 + (col & 3)) | ((uint32_t)(col & 3) << 4)
+                              : (uint32_t)(col & 3) | ((uint32_t)(4 + (col & 3)) << 4);
     const uint32_t vsel = (uint32_t)((q >> 2) | ((4 + (q >> 2)) << 4) | ((2 + (q >> 2)) << 8) | ((6 + (q >> 2)) << 12));
     const uint32_t vshift = (q & 2) ? 4u : 0u;
     const uint32_t vmask = (q & 1) ? 0x0C0C0C0Cu : 0x03030303u;
@@ -213,8 +217,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
                                 const int c0 = 16 * (2 * i + kk) + 2 * r;
-                                const uint32_t x01 = prmt(lw[c0 * 8], lw[(c0 + 1) * 8], bsel);
-                                const uint32_t x89 = prmt(lw[(c0 + 8) * 8], lw[(c0 + 9) * 8], bsel);
+                                const uint32_t x01 = prmt(lw[(c0 + rsw) * 8], lw[(c0 + 1 - rsw) * 8], bsel);
+                                const uint32_t x89 = prmt(lw[(c0 + 8 + rsw) * 8], lw[(c0 + 9 - rsw) * 8], bsel);
                                 const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
                                 uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
                                 e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
@@ -247,8 +251,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                             const uint32_t b0 = split_prod(hmul2(qh2[0], 0x44004400u), hmul2(ql2[0], 0x44004400u), s2[0], xB);
                             const uint32_t b1 = split_prod(hmul2(qh2[1], 0x44004400u), hmul2(ql2[1], 0x44004400u), s2[1], xB);
                             // rows past K read finite bytes; their B rows are zero
-                            const uint32_t x01 = prmt(hw[r0 * 8], hw[(r0 + 1) * 8], bsel);
-                            const uint32_t x89 = prmt(hw[(r0 + 8) * 8], hw[(r0 + 9) * 8], bsel);
+                            const uint32_t x01 = prmt(hw[(r0 + rsw) * 8], hw[(r0 + 1 - rsw) * 8], bsel);
+                            const uint32_t x89 = prmt(hw[(r0 + 8 + rsw) * 8], hw[(r0 + 9 - rsw) * 8], bsel);
                             const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
                             uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
                             e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);

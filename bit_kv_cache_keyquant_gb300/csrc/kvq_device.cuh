@@ -146,19 +146,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // fp32 products.  The token's 8 bytes (32 2-bit codes, channel 4b+i of byte b
 // at bits 2i) are split into 16-bit halves so that every code sits below the
 // fp32 exponent field; masked in place and read as an fp32 bit pattern a code
-// is the denormal code * 2^(k-149) (k = 2i, or 8 + 2i for odd bytes).  Each
-// weight pair ps * (2^(149-2i-EV), 2^(141-2i-EV)) turns that into
-// code * ps * 2^-EV with one packed fma.rn.f32x2; ps = p_t s_t.
+// is the denormal code * 2^(k-149) (k = 2i, or 8 + 2i for odd bytes).  One
+// weight pair ps * (2^(149-EV), 2^(141-EV)) serves every bit position, so a
+// packed fma.rn.f32x2 adds code * ps * 2^(2i-EV): accumulator i carries an
+// extra 2^(2i), removed once per unit by value_block_channels.
 // acc2[8*wi + 4*ab + i] holds channels (16 wi + 8 ab + i, 16 wi + 8 ab + 4 + i)
-// of the block, times 2^-EV.  |p s| < 2^16 keeps every weight below 2^127.
+// of the block.  |p s| < 2^16 keeps the weights below 2^127.
 // ---------------------------------------------------------------------------
 #define KVQ_EV 38
 __device__ __forceinline__ void value_token_accum(uint2 codes, float ps, unsigned long long acc2[16]) {
-    unsigned long long wt[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        wt[i] = pack2f(ps * __int_as_float((127 + 149 - KVQ_EV - 2 * i) << 23),
-                       ps * __int_as_float((127 + 141 - KVQ_EV - 2 * i) << 23));
+    const unsigned long long wt = pack2f(ps * __int_as_float((127 + 149 - KVQ_EV) << 23),
+                                         ps * __int_as_float((127 + 141 - KVQ_EV) << 23));
     const uint32_t uw[2] = {codes.x, codes.y};
 #pragma unroll
     for (int wi = 0; wi < 2; ++wi) {
@@ -166,17 +164,16 @@ __device__ __forceinline__ void value_token_accum(uint2 codes, float ps, unsigne
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t m0 = 3u << (2 * i), m1 = 3u << (8 + 2 * i);
-            acc2[8 * wi + i] = ffma2(pack2u(w0 & m0, w0 & m1), wt[i], acc2[8 * wi + i]);
-            acc2[8 * wi + 4 + i] = ffma2(pack2u(w16 & m0, w16 & m1), wt[i], acc2[8 * wi + 4 + i]);
+            acc2[8 * wi + i] = ffma2(pack2u(w0 & m0, w0 & m1), wt, acc2[8 * wi + i]);
+            acc2[8 * wi + 4 + i] = ffma2(pack2u(w16 & m0, w16 & m1), wt, acc2[8 * wi + 4 + i]);
         }
     }
 }
 
 // Channels 4*ts .. 4*ts+3 of the 32-channel block (ts = 0..7) from acc2,
-// scaled back by 2^KVQ_EV (compile-time indices only).
+// scaled back by 2^(KVQ_EV - 2i) (compile-time indices only).
 __device__ __forceinline__ float4 value_block_channels(const unsigned long long acc2[16], int ts) {
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float sc = __int_as_float((127 + KVQ_EV) << 23);
 #pragma unroll
     for (int t8 = 0; t8 < 8; ++t8) {
         if (ts == t8) {
@@ -188,7 +185,10 @@ __device__ __forceinline__ float4 value_block_channels(const unsigned long long 
                 r = make_float4(hi2f(acc2[base]), hi2f(acc2[base + 1]), hi2f(acc2[base + 2]), hi2f(acc2[base + 3]));
         }
     }
-    r.x *= sc; r.y *= sc; r.z *= sc; r.w *= sc;
+    r.x *= __int_as_float((127 + KVQ_EV) << 23);
+    r.y *= __int_as_float((127 + KVQ_EV - 2) << 23);
+    r.z *= __int_as_float((127 + KVQ_EV - 4) << 23);
+    r.w *= __int_as_float((127 + KVQ_EV - 6) << 23);
     return r;
 }
 
