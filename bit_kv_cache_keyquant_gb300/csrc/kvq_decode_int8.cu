@@ -69,8 +69,11 @@ struct Unit {
 
 __device__ __forceinline__ Unit unit_of(const Params &P, int u) {
     Unit U;
-    const int row = u / P.splits;
-    U.split = u - row * P.splits;
+    // split-major numbering (u = split * rows + row): every CTA's round-robin
+    // share mixes all splits, whose lengths differ with the rows' lengths
+    const int rows = P.B * P.Hkv;
+    U.split = u / rows;
+    const int row = u - U.split * rows;
     U.b = row / P.Hkv;
     U.kvh = row - U.b * P.Hkv;
     U.L = P.seq_len[U.b];

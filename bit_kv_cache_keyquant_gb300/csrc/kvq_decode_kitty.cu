@@ -127,7 +127,6 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     // ---- pre-scaled weights of the page: low plane (channel order) and boosted rows ----
                     {
                         const uint2 s4 = *reinterpret_cast<const uint2 *>(ps + 4 * lane);
-                        const uint2 z4 = *reinterpret_cast<const uint2 *>(ps + KVQ_D + 4 * lane);
                         const float sv[4] = {h2f(lo16(s4.x)), h2f(hi16(s4.x)), h2f(lo16(s4.y)), h2f(hi16(s4.y))};
                         *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
                             make_float4(qp[0] * sv[0], qp[1] * sv[1], qp[2] * sv[2], qp[3] * sv[3]);

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kivi_produce<GQ_NSTAGE>(P, P.Hkv, S.stage, S.full, S.empty);
+        if (lane == 0) kivi_produce<GQ_NSTAGE, true>(P, P.Hkv, S.stage, S.full, S.empty);
         return;
     }
 
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit U = unit_of(P, u, P.Hkv);     // U.hq is the kv head
+        const Unit U = unit_of<true>(P, u, P.Hkv);     // U.hq is the kv head
         // ---- per-unit query tables: warp w prepares head w ----
         {
             const int h = warp;

@@ -36,10 +36,21 @@ struct Unit {
 
 // hpr = units per batch row and split: P.Hq (one query head per unit) or
 // P.Hkv (all query heads of a kv head per unit; hq is then the kv head).
+// Row-major (u = row * splits + split) or split-major (u = split * rows +
+// row: every CTA's round-robin share mixes all splits; used by the
+// grouped-query kernel's long units).
+template <bool SPLIT_MAJOR = false>
 __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
     Unit U;
-    const int row = u / P.splits;
-    U.split = u - row * P.splits;
+    int row;
+    if (SPLIT_MAJOR) {
+        const int rows = P.B * hpr;
+        U.split = u / rows;
+        row = u - U.split * rows;
+    } else {
+        row = u / P.splits;
+        U.split = u - row * P.splits;
+    }
     U.b = row / hpr;
     U.hq = row - U.b * hpr;
     const int L = P.seq_len[U.b];
@@ -153,14 +164,14 @@ __device__ __forceinline__ void kitty_residual(const Params &P, const Unit &U, c
 
 // Producer (one lane): one page (key record, value record) per stage, in
 // unit order, into an NST-slot ring; returns after every issued copy landed.
-template <int NST>
+template <int NST, bool SPLIT_MAJOR = false>
 __device__ __forceinline__ void kitty_produce(const Params &P, int hpr, uint8_t (*stage)[STAGE_BYTES], uint64_t *full,
                                               uint64_t *empty) {
     const int n_units = P.B * hpr * P.splits;
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit U = unit_of(P, u, hpr);
+        const Unit U = unit_of<SPLIT_MAJOR>(P, u, hpr);
         for (int s = 0; s < U.np; ++s, ++sg) {
             const int slot = sg % NST;
             if (sg >= NST) ok = mbar_wait(&empty[slot], ((sg / NST) - 1) & 1, P.err);

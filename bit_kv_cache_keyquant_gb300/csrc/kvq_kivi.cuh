@@ -48,10 +48,23 @@ struct Unit {
 
 // hpr = units per batch row and split: P.Hq (one query head per unit) or
 // P.Hkv (all query heads of a kv head per unit; hq is then the kv head).
+// Units are numbered row-major (u = row * splits + split) or, for the long
+// units of the grouped-query kernels, split-major (u = split * rows + row),
+// which gives every CTA's round-robin share a mix of all splits (measured:
+// 4.5% faster on the grouped-query workload; the per-head kernel is faster
+// row-major).
+template <bool SPLIT_MAJOR = false>
 __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
     Unit U;
-    const int row = u / P.splits;
-    U.split = u - row * P.splits;
+    int row;
+    if (SPLIT_MAJOR) {
+        const int rows = P.B * hpr;
+        U.split = u / rows;
+        row = u - U.split * rows;
+    } else {
+        row = u / P.splits;
+        U.split = u - row * P.splits;
+    }
     U.b = row / hpr;
     U.hq = row - U.b * hpr;
     const int L = P.seq_len[U.b];
@@ -216,7 +229,7 @@ __device__ __forceinline__ void kivi_residual(const Params &P, const Unit &U, co
 
 // Producer (one lane): streams the stages of every unit of this CTA, in
 // unit order, into an NST-slot ring; returns after every issued copy landed.
-template <int NST>
+template <int NST, bool SPLIT_MAJOR = false>
 __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (*stage)[STAGE_BYTES], uint64_t *full,
                                              uint64_t *empty) {
     const int n_units = P.B * hpr * P.splits;
@@ -224,7 +237,7 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit U = unit_of(P, u, hpr);
+        const Unit U = unit_of<SPLIT_MAJOR>(P, u, hpr);
         const uint8_t *kc_base = P.k_codes + U.bk * P.kgrp_cap * ((int64_t)G * KVQ_D / 4);
         const uint32_t *ksz_base = P.k_sz + U.bk * P.kgrp_cap * KVQ_D;
         const uint8_t *vc_base = P.v_codes + U.bk * P.cap * (KVQ_D / 4);
