@@ -27,14 +27,12 @@ __device__ __forceinline__ int kivi_sz_index(int c) {
     return ((k >> 1) * 4 + ((cc & 7) >> 1)) * 8 + (k & 1) * 4 + (cc & 1) + 2 * (cc >> 3);
 }
 
+// One key group by a 128-thread block: src fp16 [G][D], codes the group's
+// G*D/4 bytes, sz the group's 2*D fp16 (scales, then zeros).
 template <int NT>
-__global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
-                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz) {
-    const int64_t g = blockIdx.x;
-    if (g >= n_groups) return;
+__device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src, uint8_t *__restrict__ codes,
+                                                uint16_t *__restrict__ sz) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int G = 32 * NT;
-    const uint16_t *src = k + g * (int64_t)G * KVQ_D;
 
     // lane's 32 channels of token lane in each tile: 4 x 16 bytes per tile
     uint32_t xv[NT][16];
@@ -82,8 +80,8 @@ __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__r
     const uint32_t my_sz = (uint32_t)s | ((uint32_t)z << 16);
     {
         const int si = kivi_sz_index(32 * w + lane);
-        sz[g * 2 * KVQ_D + si] = s;
-        sz[g * 2 * KVQ_D + KVQ_D + si] = z;
+        sz[si] = s;
+        sz[KVQ_D + si] = z;
     }
 
     const int q = lane & 7, p = lane >> 3;
@@ -114,9 +112,42 @@ __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__r
 #pragma unroll
         for (int i = 1; i < 4; ++i)
             if (p == i) v = make_uint2(word[i][0], word[i][1]);
-        uint8_t *tile = codes + g * (int64_t)G * KVQ_D / 4 + tt * 1024;
+        uint8_t *tile = codes + tt * 1024;
         *reinterpret_cast<uint2 *>(tile + (w >> 1) * 512 + (4 * q + p) * 16 + (w & 1) * 8) = v;
     }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
+                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz) {
+    const int64_t g = blockIdx.x;
+    if (g >= n_groups) return;
+    constexpr int G = 32 * NT;
+    key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D / 4, sz + g * 2 * KVQ_D);
+}
+
+// One value token by a warp, per token over groups of GV channels: lane l
+// reads channels 4l..4l+3 and returns in wv the packed word of its lane quad
+// (valid in lanes 4j, channels 16j..16j+15) and the (s, z) of its group.
+template <int GV>
+__device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ src, int lane, uint32_t &wv, uint16_t &s,
+                                                  uint16_t &z) {
+    constexpr int LG = GV / 4;   // lanes per group
+    uint2 u = *reinterpret_cast<const uint2 *>(src + 4 * lane);
+    float x0 = h2f(lo16(u.x)), x1 = h2f(hi16(u.x)), x2 = h2f(lo16(u.y)), x3 = h2f(hi16(u.y));
+    float mn = fminf(fminf(x0, x1), fminf(x2, x3));
+    float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+#pragma unroll
+    for (int o = 1; o < LG; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    affine_fit(mn, mx, 3, s, z);
+    float sf = h2f(s), zf = h2f(z);
+    uint32_t b = (uint32_t)affine_code(x0, zf, sf, 3) | ((uint32_t)affine_code(x1, zf, sf, 3) << 2) |
+                 ((uint32_t)affine_code(x2, zf, sf, 3) << 4) | ((uint32_t)affine_code(x3, zf, sf, 3) << 6);
+    wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 8) | (__shfl_down_sync(0xFFFFFFFFu, b, 2) << 16) |
+         (__shfl_down_sync(0xFFFFFFFFu, b, 3) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -134,22 +165,9 @@ __global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__rest
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
     constexpr int LG = GV / 4;   // lanes per group
     for (int64_t t = warp; t < n_tokens; t += nwarps) {
-        uint2 u = __ldg(reinterpret_cast<const uint2 *>(v + t * KVQ_D) + lane);
-        float x0 = h2f(lo16(u.x)), x1 = h2f(hi16(u.x)), x2 = h2f(lo16(u.y)), x3 = h2f(hi16(u.y));
-        float mn = fminf(fminf(x0, x1), fminf(x2, x3));
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-#pragma unroll
-        for (int o = 1; o < LG; o <<= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        }
+        uint32_t wv;
         uint16_t s, z;
-        affine_fit(mn, mx, 3, s, z);
-        float sf = h2f(s), zf = h2f(z);
-        uint32_t b = (uint32_t)affine_code(x0, zf, sf, 3) | ((uint32_t)affine_code(x1, zf, sf, 3) << 2) |
-                     ((uint32_t)affine_code(x2, zf, sf, 3) << 4) | ((uint32_t)affine_code(x3, zf, sf, 3) << 6);
-        uint32_t wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 8) | (__shfl_down_sync(0xFFFFFFFFu, b, 2) << 16) |
-                      (__shfl_down_sync(0xFFFFFFFFu, b, 3) << 24);
+        value_token_quant<GV>(v + t * KVQ_D, lane, wv, s, z);
         if (!KITTY) {
             if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(out + t * (KVQ_D / 4))[lane >> 2] = wv;
             if ((lane % LG) == 0) sz[t * (KVQ_D / GV) + lane / LG] = (uint32_t)s | ((uint32_t)z << 16);
@@ -411,6 +429,110 @@ cudaError_t launch_quant_int8(const kvq_config *cfg, const void *x, int64_t n_bl
     quant_int8_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(x), n_blocks, cfg->int8_block, req, head,
                                             tok0, c2, (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32),
                                             static_cast<int8_t *>(codes), static_cast<uint16_t *>(scale));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Streaming append (KIVI): one CTA of 128 threads per (batch row, kv head).
+// With L = seq_len[b] tokens cached, it first finishes the quantization that
+// follows the attention of the step with L tokens (the order is insert ->
+// attend -> quantize), then inserts token L:
+//   * keys: when L is a positive multiple of R the full key residual
+//     [L-R, L) (ring slots 0..R-1) becomes R/G quantized groups;
+//   * values: when L >= R, token L-R leaves the fp16 window and is quantized;
+//   * the new k, v are written to ring slot L % R.
+// The quantizers are the ones of kv_quant_key / kv_quant_value, so appending
+// token by token gives the bytes of a cache filled at once.  A second kernel
+// bumps seq_len once every head has read it.
+// ---------------------------------------------------------------------------
+struct AppendParams {
+    const int32_t *seq_len;
+    const uint16_t *k_new, *v_new;
+    uint8_t *k_codes, *v_codes;
+    uint16_t *k_sz;
+    uint32_t *v_sz;
+    uint16_t *k_res, *v_res;
+    unsigned *err;
+    int Hkv, R, G, ngv, max_seq_len;
+    int64_t cap, kgrp_cap;
+};
+
+template <int NT, int GV>
+__global__ void __launch_bounds__(128) append_kivi_kernel(AppendParams P) {
+    const int64_t bk = blockIdx.x;
+    const int b = (int)(bk / P.Hkv);
+    const int L = P.seq_len[b];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (L < 0 || L >= P.max_seq_len) {
+        if (threadIdx.x == 0) atomicOr(P.err, KVQ_DEVICE_ERR_CAPACITY);
+        return;
+    }
+    constexpr int G = 32 * NT;
+    const uint16_t *kres = P.k_res + bk * P.R * KVQ_D;
+    const uint16_t *vres = P.v_res + bk * P.R * KVQ_D;
+    if (L > 0 && L % P.R == 0) {
+        for (int g = 0; g < P.R / G; ++g) {
+            const int64_t gi = bk * P.kgrp_cap + (L - P.R) / G + g;
+            key_group_quant<NT>(kres + (int64_t)g * G * KVQ_D, P.k_codes + gi * (G * KVQ_D / 4), P.k_sz + gi * 2 * KVQ_D);
+        }
+    }
+    if (L >= P.R && warp == 0) {
+        const int64_t t = L - P.R;
+        uint32_t wv;
+        uint16_t s, z;
+        value_token_quant<GV>(vres + (t % P.R) * KVQ_D, lane, wv, s, z);
+        if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(P.v_codes + (bk * P.cap + t) * (KVQ_D / 4))[lane >> 2] = wv;
+        if ((lane % (GV / 4)) == 0)
+            P.v_sz[(bk * P.cap + t) * P.ngv + lane / (GV / 4)] = (uint32_t)s | ((uint32_t)z << 16);
+    }
+    __syncthreads();   // every read of the ring slot about to be overwritten is done
+    const int64_t slot = L % P.R;
+    if (threadIdx.x < 16) {
+        reinterpret_cast<uint4 *>(P.k_res + (bk * P.R + slot) * KVQ_D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(P.k_new + bk * KVQ_D)[threadIdx.x];
+    } else if (threadIdx.x < 32) {
+        reinterpret_cast<uint4 *>(P.v_res + (bk * P.R + slot) * KVQ_D)[threadIdx.x - 16] =
+            reinterpret_cast<const uint4 *>(P.v_new + bk * KVQ_D)[threadIdx.x - 16];
+    }
+}
+
+__global__ void append_bump_kernel(int32_t *seq_len, int B, int max_seq_len) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B && seq_len[b] >= 0 && seq_len[b] < max_seq_len) seq_len[b] += 1;
+}
+
+cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *k_new, const void *v_new,
+                               cudaStream_t st) {
+    AppendParams P;
+    P.seq_len = c->seq_len;
+    P.k_new = static_cast<const uint16_t *>(k_new);
+    P.v_new = static_cast<const uint16_t *>(v_new);
+    P.k_codes = static_cast<uint8_t *>(const_cast<void *>(c->k_codes));
+    P.v_codes = static_cast<uint8_t *>(const_cast<void *>(c->v_codes));
+    P.k_sz = static_cast<uint16_t *>(const_cast<void *>(c->k_sz));
+    P.v_sz = static_cast<uint32_t *>(const_cast<void *>(c->v_sz));
+    P.k_res = static_cast<uint16_t *>(const_cast<void *>(c->k_res));
+    P.v_res = static_cast<uint16_t *>(const_cast<void *>(c->v_res));
+    P.err = device_error_ptr();
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    P.Hkv = cfg->n_kv_heads;
+    P.R = cfg->residual;
+    P.G = cfg->group_k;
+    P.ngv = KVQ_D / cfg->group_v;
+    P.max_seq_len = c->max_seq_len;
+    P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
+    P.kgrp_cap = P.cap / cfg->group_k;
+    const unsigned grid = (unsigned)((int64_t)c->batch * cfg->n_kv_heads);
+#define KVQ_APPEND(NT, GV) append_kivi_kernel<NT, GV><<<grid, 128, 0, st>>>(P)
+    const int G = cfg->group_k, GV = cfg->group_v;
+    if (G == 32) { if (GV == 32) KVQ_APPEND(1, 32); else if (GV == 64) KVQ_APPEND(1, 64); else KVQ_APPEND(1, 128); }
+    else if (G == 64) { if (GV == 32) KVQ_APPEND(2, 32); else if (GV == 64) KVQ_APPEND(2, 64); else KVQ_APPEND(2, 128); }
+    else { if (GV == 32) KVQ_APPEND(4, 32); else if (GV == 64) KVQ_APPEND(4, 64); else KVQ_APPEND(4, 128); }
+#undef KVQ_APPEND
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,
+                                                                c->max_seq_len);
     return cudaGetLastError();
 }
 

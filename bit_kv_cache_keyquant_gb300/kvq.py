@@ -17,6 +17,7 @@ _LIB_PATH = _build.LIB
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_MISALIGNED, KVQ_ERR_CUDA, KVQ_ERR_WORKSPACE = range(6)
 KVQ_VARIANT_KIVI, KVQ_VARIANT_KITTY, KVQ_VARIANT_INT8 = 0, 1, 2
 KVQ_DEVICE_ERR_WAIT_TIMEOUT = 1
+KVQ_DEVICE_ERR_CAPACITY = 2
 
 
 class KvqError(RuntimeError):
@@ -63,6 +64,7 @@ def _load():
     sigs = {
         "kv_quant_key": (S, [cfgp, _P, i64, _P, _P, _P]),
         "kv_quant_value": (S, [cfgp, _P, i64, _P, _P, _P]),
+        "kv_append_kivi": (S, [cfgp, ctypes.POINTER(kvq_kivi_cache), _P, _P, _P]),
         "kv_quant_key_kitty": (S, [cfgp, _P, i64, i32, _P, _P]),
         "kv_quant_value_kitty": (S, [cfgp, _P, i64, _P, _P]),
         "kv_quant_int8_dither": (S, [cfgp, _P, i64, _P, _P, _P, i32, i32, ctypes.c_uint64, _P, _P, _P]),
@@ -89,7 +91,7 @@ def _load():
 
 _lib = _load()
 
-EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither",
+EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither",
             "kvq_kitty_key_page_bytes", "kvq_kitty_value_page_bytes", "kv_decode_attn_plan", "kv_decode_attn",
             "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_noalloc", "kv_decode_attn_stage1",
             "kv_decode_attn_merge",
@@ -150,6 +152,12 @@ def kv_quant_key(cfg, k, n_groups, codes, sz, stream=None):
 def kv_quant_value(cfg, v, n_tokens, codes, sz, stream=None):
     _check(_lib.kv_quant_value(ctypes.byref(cfg), _ptr(v), n_tokens, _ptr(codes), _ptr(sz), _stream(stream)),
            "kv_quant_value")
+
+
+def kv_append_kivi(cfg, cache, k_new, v_new, stream=None):
+    """Append one token per (batch row, kv head): k_new, v_new fp16 [B][Hkv][D]."""
+    _check(_lib.kv_append_kivi(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new), _stream(stream)),
+           "kv_append_kivi")
 
 
 def kv_quant_key_kitty(cfg, k, n_pages, score_mode, pages, stream=None):

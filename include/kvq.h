@@ -81,6 +81,7 @@ typedef enum {
 
 /* device error flags (bitmask) written by kernels instead of trapping */
 #define KVQ_DEVICE_ERR_WAIT_TIMEOUT 1u
+#define KVQ_DEVICE_ERR_CAPACITY 2u      /* kv_append_kivi on a row already at max_seq_len: nothing written */
 
 typedef enum { KVQ_VARIANT_KIVI = 0, KVQ_VARIANT_KITTY = 1, KVQ_VARIANT_INT8 = 2 } kvq_variant;
 
@@ -189,6 +190,25 @@ typedef struct {
     const void *k_res;       /* fp16   [B][Hkv][R][D] */
     const void *v_res;       /* fp16   [B][Hkv][R][D] */
 } kvq_kivi_cache;
+
+/* Streaming append of one token per (batch row, kv head) to a KIVI cache,
+ * for a decode loop that calls it before kv_decode_attn at every step.
+ *   k_new, v_new  fp16 [batch][n_kv_heads][D]: the new token's key and value
+ *   c             the cache (written: codes, (s, z), residual rings, seq_len)
+ * With L = seq_len[b] tokens cached it first completes the quantization that
+ * follows the attention of the step with L tokens (KIVI section 3.3 with the
+ * Kitty step order insert -> attend -> quantize): when L is a positive
+ * multiple of R the R keys of the full key residual become R/G quantized
+ * groups, and when L >= R value token L - R, which leaves the fp16 window,
+ * is quantized; then it writes the new token to ring slot L % R and sets
+ * seq_len[b] = L + 1.  The quantizers are those of kv_quant_key and
+ * kv_quant_value, so a cache grown token by token holds the same bytes as one
+ * filled at once.  Two kernels on `stream`, graph-capturable.  A row with
+ * seq_len[b] >= max_seq_len is left unchanged and KVQ_DEVICE_ERR_CAPACITY is
+ * recorded (kvq_get_device_error).  Beyond the pages' hot path: this is the
+ * streaming write side of their decode loop, on the dense cache layout above. */
+KVQ_API kvq_status kv_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *k_new,
+                                  const void *v_new, cudaStream_t stream);
 
 /* Kitty: sink tokens [0, min(L,S)) fp16; key pages, then a key Q-buffer of
  * n_kb = ((L-S-1) mod G) + 1 tokens (slot (t-S) % G); value pages, a value

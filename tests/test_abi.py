@@ -74,6 +74,13 @@ def test_validation_without_gpu(K):
     assert K.kvq_kitty_key_page_bytes(kitty) == 5248
     assert K.kvq_kitty_value_page_bytes(kitty) == 4608
     assert K.raw_call("kv_quant_key_kitty", ctypes.byref(kitty), 16, 1, 2, 16, None) == K.KVQ_ERR_INVALID_ARG
+    cache = K.kvq_kivi_cache(2, 512, 16, 16, 16, 16, 16, 16, 16)
+    assert K.raw_call("kv_append_kivi", ctypes.byref(good), ctypes.byref(cache), None, 16, None) == K.KVQ_ERR_INVALID_ARG
+    assert K.raw_call("kv_append_kivi", ctypes.byref(good), ctypes.byref(cache), 16, 0x1004, None) == \
+        K.KVQ_ERR_MISALIGNED
+    assert K.raw_call("kv_append_kivi", ctypes.byref(good), None, 16, 16, None) == K.KVQ_ERR_INVALID_ARG
+    assert K.raw_call("kv_append_kivi", ctypes.byref(K.make_config(bits_v=4)), ctypes.byref(cache), 16, 16,
+                      None) == K.KVQ_ERR_UNSUPPORTED
     i8 = K.make_config(int8_block=200)
     assert K.raw_call("kv_quant_int8_dither", ctypes.byref(i8), 16, 1, 16, 16, 16, 0, 0, 0, 16, 16,
                       None) == K.KVQ_ERR_UNSUPPORTED

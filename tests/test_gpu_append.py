@@ -1,0 +1,148 @@
+"""Streaming append (kv_append_kivi): a KIVI cache grown token by token must
+hold the bytes of a cache filled at once (the same quantizers, KIVI section
+3.3 with the insert -> attend -> quantize order), and decode identically."""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_util import assert_attn_close, lib
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+D = 128
+
+
+@pytest.fixture(scope="module")
+def K():
+    return lib()
+
+
+def _segments(L, R):
+    rk = (L - 1) % R + 1
+    return L - rk, L - min(L, R)
+
+
+def _fill(K, cfg, Ks, Vs, L_each, max_seq_len):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hkv = len(Ks), len(Ks[0])
+    c = C.KiviCache(cfg, B, max_seq_len, device=DEV)
+    for b in range(B):
+        for h in range(Hkv):
+            c.fill(b, h, Ks[b][h][:L_each[b]].to(DEV), Vs[b][h][:L_each[b]].to(DEV))
+    return c
+
+
+def _decode(K, cfg, c, q):
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, c.batch, c.max_seq_len)
+    ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device=DEV)
+    out = torch.full((c.batch, cfg.n_q_heads, D), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn(cfg, c.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,G,Gv,R,L0,n", [
+    (4, 2, 32, 32, 128, 1, 300),       # from one token across three key flushes
+    (2, 2, 64, 64, 128, 250, 200),
+    (8, 2, 128, 128, 128, 127, 140),   # a flush on the first append
+    (4, 4, 32, 32, 64, 500, 130),
+])
+def test_append_matches_fill(K, orc, Hq, Hkv, G, Gv, R, L0, n):
+    rng = np.random.default_rng(L0 + n + G)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv, group_k=G, group_v=Gv, residual=R)
+    B = 2
+    L_start = [L0, L0 + 7]
+    total = max(L_start) + n
+    max_seq_len = total + 3
+    gain = 1.0 + 9.0 * (rng.random(D) < 0.05)
+    Ks = [[torch.from_numpy((rng.standard_normal((total, D)) * gain).astype(np.float16)) for _ in range(Hkv)]
+          for _ in range(B)]
+    Vs = [[torch.from_numpy(rng.standard_normal((total, D)).astype(np.float16)) for _ in range(Hkv)] for _ in range(B)]
+    grown = _fill(K, cfg, Ks, Vs, L_start, max_seq_len)
+    for step in range(n):
+        kn = torch.stack([torch.stack([Ks[b][h][L_start[b] + step] for h in range(Hkv)]) for b in range(B)]).to(DEV)
+        vn = torch.stack([torch.stack([Vs[b][h][L_start[b] + step] for h in range(Hkv)]) for b in range(B)]).to(DEV)
+        K.kv_append_kivi(cfg, grown.desc(), kn, vn)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    L_end = [L + n for L in L_start]
+    full = _fill(K, cfg, Ks, Vs, L_end, max_seq_len)
+    assert grown.seq_len.cpu().tolist() == L_end
+    for b in range(B):
+        nkq, nvq = _segments(L_end[b], R)
+        ng = nkq // G
+        assert torch.equal(grown.k_codes[b, :, :ng], full.k_codes[b, :, :ng])
+        assert torch.equal(grown.k_sz[b, :, :ng], full.k_sz[b, :, :ng])
+        assert torch.equal(grown.v_codes[b, :, :nvq], full.v_codes[b, :, :nvq])
+        assert torch.equal(grown.v_sz[b, :, :nvq], full.v_sz[b, :, :nvq])
+        kslots = [t % R for t in range(nkq, L_end[b])]
+        vslots = [t % R for t in range(nvq, L_end[b])]
+        assert torch.equal(grown.k_res[b, :, kslots], full.k_res[b, :, kslots])
+        assert torch.equal(grown.v_res[b, :, vslots], full.v_res[b, :, vslots])
+    q = torch.from_numpy(rng.standard_normal((B, Hq, D)).astype(np.float16)).to(DEV)
+    a, f = _decode(K, cfg, grown, q), _decode(K, cfg, full, q)
+    assert torch.equal(a, f)
+    g = Hq // Hkv
+    want = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hkv):
+            parts = orc.kivi_build_one(Ks[b][h][:L_end[b]].numpy(), Vs[b][h][:L_end[b]].numpy(), G, Gv, R)
+            want[b, h * g:(h + 1) * g] = orc.kivi_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *parts,
+                                                             L=L_end[b], G=G, Gv=Gv, R=R)
+    assert_attn_close(a.float().cpu().numpy(), want)
+
+
+def test_append_full_row_reports_capacity(K):
+    cfg = K.make_config(n_q_heads=2, n_kv_heads=2)
+    rng = np.random.default_rng(3)
+    Ks = [[torch.from_numpy(rng.standard_normal((256, D)).astype(np.float16)) for _ in range(2)]]
+    Vs = [[torch.from_numpy(rng.standard_normal((256, D)).astype(np.float16)) for _ in range(2)]]
+    c = _fill(K, cfg, Ks, Vs, [256], 256)
+    before = (c.k_res.clone(), c.v_res.clone(), c.k_codes.clone(), c.v_codes.clone())
+    kn = torch.zeros((1, 2, D), dtype=torch.float16, device=DEV)
+    K.kv_append_kivi(cfg, c.desc(), kn, kn)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == K.KVQ_DEVICE_ERR_CAPACITY
+    assert K.kvq_get_device_error() == 0                      # reading clears it
+    assert c.seq_len.cpu().tolist() == [256]
+    after = (c.k_res, c.v_res, c.k_codes, c.v_codes)
+    assert all(torch.equal(x, y) for x, y in zip(before, after))
+
+
+def test_append_and_decode_in_one_graph(K):
+    """Append + decode captured once and replayed step by step equals the eager loop."""
+    cfg = K.make_config(n_q_heads=4, n_kv_heads=2)
+    rng = np.random.default_rng(11)
+    B, Hkv, n = 2, 2, 40
+    total = 200 + n
+    Ks = [[torch.from_numpy(rng.standard_normal((total, D)).astype(np.float16)) for _ in range(Hkv)]
+          for _ in range(B)]
+    Vs = [[torch.from_numpy(rng.standard_normal((total, D)).astype(np.float16)) for _ in range(Hkv)] for _ in range(B)]
+    q = torch.from_numpy(rng.standard_normal((B, 4, D)).astype(np.float16)).to(DEV)
+    eager = _fill(K, cfg, Ks, Vs, [200, 190], total)
+    graphed = _fill(K, cfg, Ks, Vs, [200, 190], total)
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, B, total)
+    ws = torch.zeros((wsb,), dtype=torch.uint8, device=DEV)
+    out = torch.zeros((B, 4, D), dtype=torch.float16, device=DEV)
+    kn = torch.zeros((B, Hkv, D), dtype=torch.float16, device=DEV)
+    vn = torch.zeros_like(kn)
+    stream = torch.cuda.Stream()
+    desc = graphed.desc()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        K.kv_append_kivi(cfg, desc, kn, vn, stream=torch.cuda.current_stream())
+        K.kv_decode_attn(cfg, desc, q, out, ws, wsb, stream=torch.cuda.current_stream())
+    outs_e, outs_g = [], []
+    for step in range(n):
+        cur = [200 + step, 190 + step]
+        kn.copy_(torch.stack([torch.stack([Ks[b][h][cur[b]] for h in range(Hkv)]) for b in range(B)]))
+        vn.copy_(torch.stack([torch.stack([Vs[b][h][cur[b]] for h in range(Hkv)]) for b in range(B)]))
+        graph.replay()
+        outs_g.append(out.clone())
+        K.kv_append_kivi(cfg, eager.desc(), kn, vn)
+        outs_e.append(_decode(K, cfg, eager, q))
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    for a, b in zip(outs_e, outs_g):
+        assert torch.equal(a, b)
