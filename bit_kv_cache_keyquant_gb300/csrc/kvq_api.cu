@@ -170,6 +170,18 @@ extern "C" kvq_status kv_append_kivi(const kvq_config *cfg, const kvq_kivi_cache
     return cuda_status(launch_append_kivi(cfg, c, k_new, v_new, stream));
 }
 
+extern "C" kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new,
+                                     const void *v_new, cudaStream_t stream) {
+    kvq_status s = check_int8(cfg);
+    if (s) return s;
+    if (!c || c->batch < 1 || c->max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
+    if (c->layer < 0 || c->layer >= (1 << 15)) return KVQ_ERR_INVALID_ARG;
+    if ((s = ptrs_ok({k_new, v_new, c->seq_len, c->req_id, c->k_codes, c->v_codes, c->k_scale, c->v_scale, c->k_tail,
+                      c->v_tail})))
+        return s;
+    return cuda_status(launch_append_int8(cfg, c, k_new, v_new, stream));
+}
+
 extern "C" size_t kvq_kitty_key_page_bytes(const kvq_config *cfg) {
     if (check_kitty(cfg)) return 0;
     return (size_t)KVQ_D * cfg->group_k / 4 + (size_t)cfg->boost_k * cfg->group_k / 4 + KVQ_D + 4 * KVQ_D;

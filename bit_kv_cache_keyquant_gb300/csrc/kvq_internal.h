@@ -37,6 +37,8 @@ cudaError_t launch_quant_int8(const kvq_config *cfg, const void *x, int64_t n_bl
 
 cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *k_new, const void *v_new,
                                cudaStream_t st);
+cudaError_t launch_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new, const void *v_new,
+                               cudaStream_t st);
 cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q,
                                const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query KIVI decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)

@@ -277,6 +277,59 @@ __global__ void __launch_bounds__(128) quant_key_kitty_kernel(const uint16_t *__
 // thread (warp w, lane l) owns channels 4l..4l+3 and tokens t = w (mod 8), so
 // one Philox4x32-10 call yields the four dithers of its four channels.
 // ---------------------------------------------------------------------------
+// One INT8 block of T tokens by a 256-thread block: per-channel amax ->
+// s = fp16_RN(amax / 126.5); code = clamp(rint(x / s + xi), -127, 127) with
+// the Philox dither of (token t0 + t, channel, c2, c3) (WitCert section 6.1).
+__device__ __forceinline__ void int8_block_quant(const uint16_t *__restrict__ xb, int T, uint32_t c2, uint32_t c3,
+                                                 int32_t t0, uint32_t k0, uint32_t k1, int8_t *__restrict__ codes,
+                                                 uint16_t *__restrict__ scale, float (*amax_part)[KVQ_D],
+                                                 float *s_sh) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int t = w; t < T; t += 8) {
+        uint2 u = *reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D + 4 * lane);
+        a0 = fmaxf(a0, fabsf(h2f(lo16(u.x))));
+        a1 = fmaxf(a1, fabsf(h2f(hi16(u.x))));
+        a2 = fmaxf(a2, fabsf(h2f(lo16(u.y))));
+        a3 = fmaxf(a3, fabsf(h2f(hi16(u.y))));
+    }
+    amax_part[w][4 * lane + 0] = a0;
+    amax_part[w][4 * lane + 1] = a1;
+    amax_part[w][4 * lane + 2] = a2;
+    amax_part[w][4 * lane + 3] = a3;
+    __syncthreads();
+    if (threadIdx.x < KVQ_D) {
+        float a = amax_part[0][threadIdx.x];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) a = fmaxf(a, amax_part[i][threadIdx.x]);
+        uint16_t s = f2h_rn(__fdiv_rn(a, 126.5f));
+        scale[threadIdx.x] = s;
+        s_sh[threadIdx.x] = h2f(s);
+    }
+    __syncthreads();
+    const float s0 = s_sh[4 * lane], s1 = s_sh[4 * lane + 1], s2 = s_sh[4 * lane + 2], s3 = s_sh[4 * lane + 3];
+    for (int t = w; t < T; t += 8) {
+        uint4 r = philox4x32_10(make_uint4((uint32_t)(t0 + t), (uint32_t)lane, c2, c3), k0, k1);
+        uint2 u = *reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D + 4 * lane);
+        float xs[4] = {h2f(lo16(u.x)), h2f(hi16(u.x)), h2f(lo16(u.y)), h2f(hi16(u.y))};
+        float ss[4] = {s0, s1, s2, s3};
+        uint32_t wr[4] = {r.x, r.y, r.z, r.w};
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int code = 0;
+            if (ss[i] != 0.0f) {
+                float xi = dither_from_word(wr[i]);
+                float v = __fadd_rn(__fdiv_rn(xs[i], ss[i]), xi);
+                code = (int)fminf(fmaxf(rintf(v), -127.f), 127.f);
+            }
+            packed |= ((uint32_t)(code & 0xFF)) << (8 * i);
+        }
+        reinterpret_cast<uint32_t *>(codes + (int64_t)t * KVQ_D)[lane] = packed;
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(256) quant_int8_kernel(const uint16_t *__restrict__ x, int64_t n_blocks, int T,
                                                          const int32_t *__restrict__ req,
                                                          const int32_t *__restrict__ head,
@@ -285,55 +338,10 @@ __global__ void __launch_bounds__(256) quant_int8_kernel(const uint16_t *__restr
                                                          uint16_t *__restrict__ scale) {
     __shared__ float amax_part[8][KVQ_D];
     __shared__ float s_sh[KVQ_D];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
-        const uint16_t *xb = x + b * (int64_t)T * KVQ_D;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        for (int t = w; t < T; t += 8) {
-            uint2 u = __ldg(reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D) + lane);
-            a0 = fmaxf(a0, fabsf(h2f(lo16(u.x))));
-            a1 = fmaxf(a1, fabsf(h2f(hi16(u.x))));
-            a2 = fmaxf(a2, fabsf(h2f(lo16(u.y))));
-            a3 = fmaxf(a3, fabsf(h2f(hi16(u.y))));
-        }
-        amax_part[w][4 * lane + 0] = a0;
-        amax_part[w][4 * lane + 1] = a1;
-        amax_part[w][4 * lane + 2] = a2;
-        amax_part[w][4 * lane + 3] = a3;
-        __syncthreads();
-        if (threadIdx.x < KVQ_D) {
-            float a = amax_part[0][threadIdx.x];
-#pragma unroll
-            for (int i = 1; i < 8; ++i) a = fmaxf(a, amax_part[i][threadIdx.x]);
-            uint16_t s = f2h_rn(__fdiv_rn(a, 126.5f));
-            scale[b * KVQ_D + threadIdx.x] = s;
-            s_sh[threadIdx.x] = h2f(s);
-        }
-        __syncthreads();
-        const float s0 = s_sh[4 * lane], s1 = s_sh[4 * lane + 1], s2 = s_sh[4 * lane + 2], s3 = s_sh[4 * lane + 3];
         const uint32_t c2 = ctr2_layer | ((uint32_t)head[b] & 0xFFFFu);
-        const uint32_t c3 = (uint32_t)req[b];
-        const int32_t t0 = tok0[b];
-        for (int t = w; t < T; t += 8) {
-            uint4 r = philox4x32_10(make_uint4((uint32_t)(t0 + t), (uint32_t)lane, c2, c3), k0, k1);
-            uint2 u = __ldg(reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D) + lane);
-            float xs[4] = {h2f(lo16(u.x)), h2f(hi16(u.x)), h2f(lo16(u.y)), h2f(hi16(u.y))};
-            float ss[4] = {s0, s1, s2, s3};
-            uint32_t wr[4] = {r.x, r.y, r.z, r.w};
-            uint32_t packed = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                int code = 0;
-                if (ss[i] != 0.0f) {
-                    float xi = dither_from_word(wr[i]);
-                    float v = __fadd_rn(__fdiv_rn(xs[i], ss[i]), xi);
-                    code = (int)fminf(fmaxf(rintf(v), -127.f), 127.f);
-                }
-                packed |= ((uint32_t)(code & 0xFF)) << (8 * i);
-            }
-            reinterpret_cast<uint32_t *>(codes + (b * (int64_t)T + t) * KVQ_D)[lane] = packed;
-        }
-        __syncthreads();
+        int8_block_quant(x + b * (int64_t)T * KVQ_D, T, c2, (uint32_t)req[b], tok0[b], k0, k1,
+                         codes + b * (int64_t)T * KVQ_D, scale + b * KVQ_D, amax_part, s_sh);
     }
 }
 
@@ -529,6 +537,87 @@ cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
     else if (G == 64) { if (GV == 32) KVQ_APPEND(2, 32); else if (GV == 64) KVQ_APPEND(2, 64); else KVQ_APPEND(2, 128); }
     else { if (GV == 32) KVQ_APPEND(4, 32); else if (GV == 64) KVQ_APPEND(4, 64); else KVQ_APPEND(4, 128); }
 #undef KVQ_APPEND
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,
+                                                                c->max_seq_len);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Streaming append (INT8): one CTA of 256 threads per (batch row, kv head).
+// With L = seq_len[b] cached: when L is a positive multiple of T the fp16
+// tail [L-T, L) (ring slots 0..T-1) becomes the INT8 block (L-T)/T of K and V
+// (the write kernel's quantizer and dither streams); then token L goes to tail
+// slot L % T.  seq_len is bumped by a second kernel.
+// ---------------------------------------------------------------------------
+struct AppendInt8Params {
+    const int32_t *seq_len, *req_id;
+    const uint16_t *k_new, *v_new;
+    int8_t *k_codes, *v_codes;
+    uint16_t *k_scale, *v_scale, *k_tail, *v_tail;
+    unsigned *err;
+    int Hkv, T, max_seq_len, blk_cap;
+    uint32_t ctr2_layer, k0, k1;
+};
+
+__global__ void __launch_bounds__(256) append_int8_kernel(AppendInt8Params P) {
+    __shared__ float amax_part[8][KVQ_D];
+    __shared__ float s_sh[KVQ_D];
+    const int64_t bk = blockIdx.x;
+    const int b = (int)(bk / P.Hkv), h = (int)(bk % P.Hkv);
+    const int L = P.seq_len[b];
+    if (L < 0 || L >= P.max_seq_len) {
+        if (threadIdx.x == 0) atomicOr(P.err, KVQ_DEVICE_ERR_CAPACITY);
+        return;
+    }
+    const int T = P.T;
+    if (L > 0 && L % T == 0) {
+        const int blk = (L - T) / T;
+        const uint32_t c2 = P.ctr2_layer | ((uint32_t)h & 0xFFFFu);
+        const uint32_t c3 = (uint32_t)P.req_id[b];
+        int8_block_quant(P.k_tail + bk * T * KVQ_D, T, c2, c3, L - T, P.k0, P.k1,
+                         P.k_codes + (bk * P.max_seq_len + (L - T)) * KVQ_D, P.k_scale + (bk * P.blk_cap + blk) * KVQ_D,
+                         amax_part, s_sh);
+        int8_block_quant(P.v_tail + bk * T * KVQ_D, T, c2 | 0x10000u, c3, L - T, P.k0, P.k1,
+                         P.v_codes + (bk * P.max_seq_len + (L - T)) * KVQ_D, P.v_scale + (bk * P.blk_cap + blk) * KVQ_D,
+                         amax_part, s_sh);
+    }
+    __syncthreads();
+    const int64_t slot = L % T;
+    if (threadIdx.x < 16) {
+        reinterpret_cast<uint4 *>(P.k_tail + (bk * T + slot) * KVQ_D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(P.k_new + bk * KVQ_D)[threadIdx.x];
+    } else if (threadIdx.x < 32) {
+        reinterpret_cast<uint4 *>(P.v_tail + (bk * T + slot) * KVQ_D)[threadIdx.x - 16] =
+            reinterpret_cast<const uint4 *>(P.v_new + bk * KVQ_D)[threadIdx.x - 16];
+    }
+}
+
+cudaError_t launch_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new, const void *v_new,
+                               cudaStream_t st) {
+    AppendInt8Params P;
+    P.seq_len = c->seq_len;
+    P.req_id = c->req_id;
+    P.k_new = static_cast<const uint16_t *>(k_new);
+    P.v_new = static_cast<const uint16_t *>(v_new);
+    P.k_codes = static_cast<int8_t *>(const_cast<void *>(c->k_codes));
+    P.v_codes = static_cast<int8_t *>(const_cast<void *>(c->v_codes));
+    P.k_scale = static_cast<uint16_t *>(const_cast<void *>(c->k_scale));
+    P.v_scale = static_cast<uint16_t *>(const_cast<void *>(c->v_scale));
+    P.k_tail = static_cast<uint16_t *>(const_cast<void *>(c->k_tail));
+    P.v_tail = static_cast<uint16_t *>(const_cast<void *>(c->v_tail));
+    P.err = device_error_ptr();
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    P.Hkv = cfg->n_kv_heads;
+    P.T = cfg->int8_block;
+    P.max_seq_len = c->max_seq_len;
+    P.blk_cap = (c->max_seq_len + P.T - 1) / P.T;
+    if (P.blk_cap < 1) P.blk_cap = 1;
+    P.ctr2_layer = (uint32_t)c->layer << 17;
+    P.k0 = (uint32_t)(c->seed & 0xFFFFFFFFu);
+    P.k1 = (uint32_t)(c->seed >> 32);
+    append_int8_kernel<<<(unsigned)((int64_t)c->batch * cfg->n_kv_heads), 256, 0, st>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,

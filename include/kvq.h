@@ -247,6 +247,19 @@ typedef struct {
     const void *v_tail;      /* fp16 [B][Hkv][T][D] */
 } kvq_int8_cache;
 
+/* Streaming append of one token per (batch row, kv head) to an INT8 cache,
+ * called before kv_decode_attn_int8 at every step.
+ *   k_new, v_new  fp16 [batch][n_kv_heads][D]
+ * With L = seq_len[b] cached: when L is a positive multiple of T the fp16
+ * tail becomes INT8 block (L-T)/T of keys and values with the same scales,
+ * codes and Philox dither streams as kv_quant_int8_dither (WitCert section
+ * 6.1, active-block tail); then the new token goes to tail slot L % T and
+ * seq_len[b] = L + 1.  Two kernels on `stream`, graph-capturable.  A row
+ * with seq_len[b] >= max_seq_len is left unchanged and
+ * KVQ_DEVICE_ERR_CAPACITY is recorded. */
+KVQ_API kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new,
+                                  const void *v_new, cudaStream_t stream);
+
 /* Split-KV plan: number of splits per (batch row, query head) and the
  * workspace bytes the decode calls need for this config, variant, batch and
  * max_seq_len.  Deterministic: the decode calls recompute the same plan. */

@@ -1,6 +1,7 @@
-"""Streaming append (kv_append_kivi): a KIVI cache grown token by token must
-hold the bytes of a cache filled at once (the same quantizers, KIVI section
-3.3 with the insert -> attend -> quantize order), and decode identically."""
+"""Streaming append (kv_append_kivi, kv_append_int8): a cache grown token by token must
+hold the bytes of a cache filled at once (the same quantizers; KIVI section
+3.3 with the insert -> attend -> quantize order, WitCert section 6.1 tail blocks),
+and decode identically."""
 import numpy as np
 import pytest
 import torch
@@ -146,3 +147,66 @@ def test_append_and_decode_in_one_graph(K):
     assert K.kvq_get_device_error() == 0
     for a, b in zip(outs_e, outs_g):
         assert torch.equal(a, b)
+
+
+def _fill_int8(cfg, Ks, Vs, L_each, max_seq_len, reqs, layer, seed):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hkv = len(Ks), len(Ks[0])
+    c = C.Int8Cache(cfg, B, max_seq_len, layer=layer, seed=seed, device=DEV)
+    for b in range(B):
+        for h in range(Hkv):
+            c.fill(b, h, Ks[b][h][:L_each[b]].to(DEV), Vs[b][h][:L_each[b]].to(DEV), int(reqs[b]))
+    return c
+
+
+@pytest.mark.parametrize("Hq,Hkv,L0,n", [(8, 2, 1, 600), (4, 4, 255, 300), (8, 1, 700, 100)])
+def test_append_int8_matches_fill(K, orc, Hq, Hkv, L0, n):
+    rng = np.random.default_rng(L0 + n)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    B, T, layer, seed = 2, cfg.int8_block, 3, 0xABCDEF0123
+    reqs = rng.integers(0, 2 ** 31 - 1, B)
+    L_start = [L0, L0 + 31]
+    total = max(L_start) + n
+    max_seq_len = total + 5
+    Ks = [[torch.from_numpy((rng.standard_normal((total, D)) * 10.0 ** rng.uniform(-1, 1, D)).astype(np.float16))
+           for _ in range(Hkv)] for _ in range(B)]
+    Vs = [[torch.from_numpy(rng.standard_normal((total, D)).astype(np.float16)) for _ in range(Hkv)] for _ in range(B)]
+    grown = _fill_int8(cfg, Ks, Vs, L_start, max_seq_len, reqs, layer, seed)
+    for step in range(n):
+        kn = torch.stack([torch.stack([Ks[b][h][L_start[b] + step] for h in range(Hkv)]) for b in range(B)]).to(DEV)
+        vn = torch.stack([torch.stack([Vs[b][h][L_start[b] + step] for h in range(Hkv)]) for b in range(B)]).to(DEV)
+        K.kv_append_int8(cfg, grown.desc(), kn, vn)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    L_end = [L + n for L in L_start]
+    full = _fill_int8(cfg, Ks, Vs, L_end, max_seq_len, reqs, layer, seed)
+    assert grown.seq_len.cpu().tolist() == L_end
+    for b in range(B):
+        nq = L_end[b] - ((L_end[b] - 1) % T + 1)
+        assert torch.equal(grown.k_codes[b, :, :nq], full.k_codes[b, :, :nq])
+        assert torch.equal(grown.v_codes[b, :, :nq], full.v_codes[b, :, :nq])
+        assert torch.equal(grown.k_scale[b, :, :nq // T], full.k_scale[b, :, :nq // T])
+        assert torch.equal(grown.v_scale[b, :, :nq // T], full.v_scale[b, :, :nq // T])
+        slots = [t % T for t in range(nq, L_end[b])]
+        assert torch.equal(grown.k_tail[b, :, slots], full.k_tail[b, :, slots])
+        assert torch.equal(grown.v_tail[b, :, slots], full.v_tail[b, :, slots])
+    q = torch.from_numpy(rng.standard_normal((B, Hq, D)).astype(np.float16)).to(DEV)
+    outs = []
+    for c in (grown, full):
+        _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_INT8, B, max_seq_len)
+        ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device=DEV)
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float16, device=DEV)
+        K.kv_decode_attn_int8(cfg, c.desc(), q, out, ws, wsb)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    g = Hq // Hkv
+    want = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hkv):
+            parts = orc.int8_build_one(Ks[b][h][:L_end[b]].numpy(), Vs[b][h][:L_end[b]].numpy(), seed, int(reqs[b]),
+                                       layer, h)
+            want[b, h * g:(h + 1) * g] = orc.int8_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *parts,
+                                                             L=L_end[b], seed=seed, request=int(reqs[b]), layer=layer,
+                                                             kv_head=h)
+    assert_attn_close(outs[0].float().cpu().numpy(), want)
