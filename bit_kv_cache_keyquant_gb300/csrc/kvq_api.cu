@@ -182,6 +182,17 @@ extern "C" kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache
     return cuda_status(launch_append_int8(cfg, c, k_new, v_new, stream));
 }
 
+extern "C" kvq_status kv_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new,
+                                      const void *v_new, int score_mode, cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (score_mode != 0 && score_mode != 1) return KVQ_ERR_INVALID_ARG;
+    if (!c || c->batch < 1 || c->max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
+    if ((s = ptrs_ok({k_new, v_new, c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local}))) return s;
+    if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;
+    return cuda_status(launch_append_kitty(cfg, c, k_new, v_new, score_mode, stream));
+}
+
 extern "C" size_t kvq_kitty_key_page_bytes(const kvq_config *cfg) {
     if (check_kitty(cfg)) return 0;
     return (size_t)KVQ_D * cfg->group_k / 4 + (size_t)cfg->boost_k * cfg->group_k / 4 + KVQ_D + 4 * KVQ_D;

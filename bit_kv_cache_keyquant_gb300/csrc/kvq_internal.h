@@ -39,6 +39,8 @@ cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
                                cudaStream_t st);
 cudaError_t launch_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new, const void *v_new,
                                cudaStream_t st);
+cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new, const void *v_new,
+                                int score_mode, cudaStream_t st);
 cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q,
                                const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query KIVI decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)

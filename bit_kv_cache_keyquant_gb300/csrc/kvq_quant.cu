@@ -197,79 +197,85 @@ __device__ __forceinline__ long long abs_units(uint16_t h) {
     return e == 0 ? (long long)m : ((long long)(1024 + m) << (e - 1));
 }
 
-__global__ void __launch_bounds__(128) quant_key_kitty_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
-                                                              int K, int score_mode, uint8_t *__restrict__ pages,
-                                                              int64_t page_bytes) {
+// One Kitty key page (G = 128 tokens) by a 128-thread block (thread =
+// channel), staged through `smem` (G*D fp16 plus three D-sized arrays).
+__device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict__ src, int K, int score_mode,
+                                                     uint8_t *__restrict__ pg, uint8_t *smem) {
     constexpr int G = 128;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);            // [G][D]
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);                 // [G][D]
     long long *si = reinterpret_cast<long long *>(xs + G * KVQ_D);     // [D]
     float *sf = reinterpret_cast<float *>(si + KVQ_D);                 // [D]
     int *boost = reinterpret_cast<int *>(sf + KVQ_D);                   // [D]
     const int c = threadIdx.x;
-    for (int64_t p = blockIdx.x; p < n_pages; p += gridDim.x) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(k + p * (int64_t)G * KVQ_D);
-        for (int i = c; i < G * KVQ_D / 8; i += 128) reinterpret_cast<uint4 *>(xs)[i] = __ldg(src + i);
-        __syncthreads();
-        long long a = 0;
-        float s1 = 0.f, s2 = 0.f;
-        float mn = INFINITY, mx = -INFINITY;
-        for (int t = 0; t < G; ++t) {
-            uint16_t h = xs[t * KVQ_D + c];
-            float x = h2f(h);
-            a += abs_units(h);
-            s1 = __fadd_rn(s1, x);
-            s2 = __fadd_rn(s2, __fmul_rn(x, x));
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
-        }
-        float mean = __fdiv_rn(s1, (float)G);
-        float var = __fsub_rn(__fdiv_rn(s2, (float)G), __fmul_rn(mean, mean));
-        si[c] = a;
-        sf[c] = var;
-        __syncthreads();
-        int rank = 0;
-        for (int o = 0; o < KVQ_D; ++o) {
-            bool better = score_mode == 0 ? (si[o] > a || (si[o] == a && o < c))
-                                          : (sf[o] > var || (sf[o] == var && o < c));
-            rank += better ? 1 : 0;
-        }
-        const int boosted = rank < K;
-        boost[c] = boosted;
-        __syncthreads();
-        int r = 0;
-        for (int o = 0; o < c; ++o) r += boost[o];
-        const int qmax = boosted ? 15 : 3;
-        uint16_t s, z;
-        affine_fit(mn, mx, qmax, s, z);
-        const float sv = h2f(s), zv = h2f(z);
-        uint8_t *pg = pages + p * page_bytes;
-        uint8_t *low = pg;
-        uint8_t *high = pg + KVQ_D * G / 4;
-        uint8_t *idx = high + (int64_t)K * G / 4;
-        uint16_t *ps = reinterpret_cast<uint16_t *>(idx + KVQ_D);
-        uint32_t lw[8], hw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { lw[i] = 0; hw[i] = 0; }
-        for (int t = 0; t < G; ++t) {
-            uint32_t code = (uint32_t)affine_code(h2f(xs[t * KVQ_D + c]), zv, sv, qmax);
-            const int sh = 2 * (t & 15);
-            lw[t >> 4] |= (code & 3u) << sh;
-            hw[t >> 4] |= ((code >> 2) & 3u) << sh;
-        }
-        uint4 *lrow = reinterpret_cast<uint4 *>(low + c * (G / 4));
-        lrow[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        lrow[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-        if (boosted) {
-            uint4 *hrow = reinterpret_cast<uint4 *>(high + (int64_t)r * (G / 4));
-            hrow[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            hrow[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-        }
-        idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
-        ps[c] = s;
-        ps[KVQ_D + c] = z;
-        __syncthreads();
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    for (int i = c; i < G * KVQ_D / 8; i += 128) reinterpret_cast<uint4 *>(xs)[i] = s4[i];
+    __syncthreads();
+    long long a = 0;
+    float s1 = 0.f, s2 = 0.f;
+    float mn = INFINITY, mx = -INFINITY;
+    for (int t = 0; t < G; ++t) {
+        uint16_t h = xs[t * KVQ_D + c];
+        float x = h2f(h);
+        a += abs_units(h);
+        s1 = __fadd_rn(s1, x);
+        s2 = __fadd_rn(s2, __fmul_rn(x, x));
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
     }
+    float mean = __fdiv_rn(s1, (float)G);
+    float var = __fsub_rn(__fdiv_rn(s2, (float)G), __fmul_rn(mean, mean));
+    si[c] = a;
+    sf[c] = var;
+    __syncthreads();
+    int rank = 0;
+    for (int o = 0; o < KVQ_D; ++o) {
+        bool better = score_mode == 0 ? (si[o] > a || (si[o] == a && o < c)) : (sf[o] > var || (sf[o] == var && o < c));
+        rank += better ? 1 : 0;
+    }
+    const int boosted = rank < K;
+    boost[c] = boosted;
+    __syncthreads();
+    int r = 0;
+    for (int o = 0; o < c; ++o) r += boost[o];
+    const int qmax = boosted ? 15 : 3;
+    uint16_t s, z;
+    affine_fit(mn, mx, qmax, s, z);
+    const float sv = h2f(s), zv = h2f(z);
+    uint8_t *low = pg;
+    uint8_t *high = pg + KVQ_D * G / 4;
+    uint8_t *idx = high + (int64_t)K * G / 4;
+    uint16_t *ps = reinterpret_cast<uint16_t *>(idx + KVQ_D);
+    uint32_t lw[8], hw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { lw[i] = 0; hw[i] = 0; }
+    for (int t = 0; t < G; ++t) {
+        uint32_t code = (uint32_t)affine_code(h2f(xs[t * KVQ_D + c]), zv, sv, qmax);
+        const int sh = 2 * (t & 15);
+        lw[t >> 4] |= (code & 3u) << sh;
+        hw[t >> 4] |= ((code >> 2) & 3u) << sh;
+    }
+    uint4 *lrow = reinterpret_cast<uint4 *>(low + c * (G / 4));
+    lrow[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    lrow[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    if (boosted) {
+        uint4 *hrow = reinterpret_cast<uint4 *>(high + (int64_t)r * (G / 4));
+        hrow[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        hrow[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    }
+    idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
+    ps[c] = s;
+    ps[KVQ_D + c] = z;
+    __syncthreads();
+}
+
+constexpr size_t KITTY_KEY_SMEM = (size_t)128 * KVQ_D * 2 + KVQ_D * (8 + 4 + 4);
+
+__global__ void __launch_bounds__(128) quant_key_kitty_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
+                                                              int K, int score_mode, uint8_t *__restrict__ pages,
+                                                              int64_t page_bytes) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    for (int64_t p = blockIdx.x; p < n_pages; p += gridDim.x)
+        kitty_key_page_quant(k + p * (int64_t)128 * KVQ_D, K, score_mode, pages + p * page_bytes, smem_raw);
 }
 
 // ---------------------------------------------------------------------------
@@ -414,13 +420,15 @@ cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t
     if (n_pages == 0) return cudaSuccess;
     const int G = cfg->group_k, K = cfg->boost_k;
     const int64_t pb = (int64_t)KVQ_D * G / 4 + (int64_t)K * G / 4 + KVQ_D + 4LL * KVQ_D;
-    const size_t smem = (size_t)G * KVQ_D * 2 + KVQ_D * (8 + 4 + 4);
-    static bool attr_set = false;
-    if (!attr_set) {
+    const size_t smem = KITTY_KEY_SMEM;
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(quant_key_kitty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_dev = dev;
     }
     const int grid = grid_cap(n_pages, 4);
     quant_key_kitty_kernel<<<grid, 128, smem, st>>>(static_cast<const uint16_t *>(k), n_pages, K, score_mode,
@@ -618,6 +626,127 @@ cudaError_t launch_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, c
     P.k0 = (uint32_t)(c->seed & 0xFFFFFFFFu);
     P.k1 = (uint32_t)(c->seed >> 32);
     append_int8_kernel<<<(unsigned)((int64_t)c->batch * cfg->n_kv_heads), 256, 0, st>>>(P);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,
+                                                                c->max_seq_len);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Streaming append (Kitty): one CTA of 128 threads per (batch row, kv head).
+// With L = seq_len[b] cached it completes the quantization that follows the
+// attention of the step with L tokens, then inserts token L (Kitty, "Stage 1:
+// Inserting New KV Vectors" and "Stage 3" of the pipeline):
+//   * keys: when (L - S) is a positive multiple of G the full key Q-buffer
+//     becomes key page (L - S)/G - 1;
+//   * values: when E = L - S - R is a positive multiple of G the full value
+//     Q-buffer becomes value page E/G - 1; when L - R >= S, token L - R leaves
+//     the local window for value Q-buffer slot (L - R - S) % G;
+//   * token L goes to the sink (L < S) or to key Q-buffer slot (L - S) % G
+//     and local window slot L % R.
+// ---------------------------------------------------------------------------
+struct AppendKittyParams {
+    const int32_t *seq_len;
+    const uint16_t *k_new, *v_new;
+    uint8_t *k_pages, *v_pages;
+    uint16_t *k_sink, *v_sink, *k_qbuf, *v_qbuf, *v_local;
+    unsigned *err;
+    int Hkv, S, R, K, score_mode, max_seq_len, page_cap;
+    int64_t kpb, vpb;
+};
+
+__global__ void __launch_bounds__(128) append_kitty_kernel(AppendKittyParams P) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    constexpr int G = 128;
+    const int64_t bk = blockIdx.x;
+    const int b = (int)(bk / P.Hkv);
+    const int L = P.seq_len[b];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (L < 0 || L >= P.max_seq_len) {
+        if (threadIdx.x == 0) atomicOr(P.err, KVQ_DEVICE_ERR_CAPACITY);
+        return;
+    }
+    const int S = P.S, R = P.R;
+    uint16_t *kqb = P.k_qbuf + bk * G * KVQ_D;
+    uint16_t *vqb = P.v_qbuf + bk * G * KVQ_D;
+    uint16_t *vloc = P.v_local + bk * (int64_t)R * KVQ_D;
+    if (L > S && (L - S) % G == 0) {
+        const int p = (L - S) / G - 1;
+        kitty_key_page_quant(kqb, P.K, P.score_mode, P.k_pages + (bk * P.page_cap + p) * P.kpb, smem_raw);
+    }
+    const int E = L - S - R;
+    if (E > 0 && E % G == 0) {
+        uint8_t *pg = P.v_pages + (bk * P.page_cap + (E / G - 1)) * P.vpb;
+        uint16_t *ps = reinterpret_cast<uint16_t *>(pg + (int64_t)G * KVQ_D / 4);
+        for (int tt = warp; tt < G; tt += 4) {
+            uint32_t wv;
+            uint16_t sv, zv;
+            value_token_quant<128>(vqb + (int64_t)tt * KVQ_D, lane, wv, sv, zv);
+            if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(pg + (int64_t)tt * (KVQ_D / 4))[lane >> 2] = wv;
+            if (lane == 0) {
+                ps[tt] = sv;
+                ps[G + tt] = zv;
+            }
+        }
+    }
+    __syncthreads();
+    if (L - R >= S && threadIdx.x < 16) {
+        const int te = L - R;
+        reinterpret_cast<uint4 *>(vqb + (int64_t)((te - S) % G) * KVQ_D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(vloc + (int64_t)(te % R) * KVQ_D)[threadIdx.x];
+    }
+    __syncthreads();
+    const uint4 *kn = reinterpret_cast<const uint4 *>(P.k_new + bk * KVQ_D);
+    const uint4 *vn = reinterpret_cast<const uint4 *>(P.v_new + bk * KVQ_D);
+    if (L < S) {
+        if (threadIdx.x < 16)
+            reinterpret_cast<uint4 *>(P.k_sink + (bk * S + L) * KVQ_D)[threadIdx.x] = kn[threadIdx.x];
+        else if (threadIdx.x < 32)
+            reinterpret_cast<uint4 *>(P.v_sink + (bk * S + L) * KVQ_D)[threadIdx.x - 16] = vn[threadIdx.x - 16];
+    } else {
+        if (threadIdx.x < 16)
+            reinterpret_cast<uint4 *>(kqb + (int64_t)((L - S) % G) * KVQ_D)[threadIdx.x] = kn[threadIdx.x];
+        else if (threadIdx.x < 32)
+            reinterpret_cast<uint4 *>(vloc + (int64_t)(L % R) * KVQ_D)[threadIdx.x - 16] = vn[threadIdx.x - 16];
+    }
+}
+
+cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new, const void *v_new,
+                                int score_mode, cudaStream_t st) {
+    AppendKittyParams P;
+    P.seq_len = c->seq_len;
+    P.k_new = static_cast<const uint16_t *>(k_new);
+    P.v_new = static_cast<const uint16_t *>(v_new);
+    P.k_pages = static_cast<uint8_t *>(const_cast<void *>(c->k_pages));
+    P.v_pages = static_cast<uint8_t *>(const_cast<void *>(c->v_pages));
+    P.k_sink = static_cast<uint16_t *>(const_cast<void *>(c->k_sink));
+    P.v_sink = static_cast<uint16_t *>(const_cast<void *>(c->v_sink));
+    P.k_qbuf = static_cast<uint16_t *>(const_cast<void *>(c->k_qbuf));
+    P.v_qbuf = static_cast<uint16_t *>(const_cast<void *>(c->v_qbuf));
+    P.v_local = static_cast<uint16_t *>(const_cast<void *>(c->v_local));
+    P.err = device_error_ptr();
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    P.Hkv = cfg->n_kv_heads;
+    P.S = cfg->sink;
+    P.R = cfg->residual;
+    P.K = cfg->boost_k;
+    P.score_mode = score_mode;
+    P.max_seq_len = c->max_seq_len;
+    P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + 127) / 128;
+    if (P.page_cap < 1) P.page_cap = 1;
+    P.kpb = (int64_t)KVQ_D * 128 / 4 + (int64_t)cfg->boost_k * 128 / 4 + KVQ_D + 4LL * KVQ_D;
+    P.vpb = 128LL * KVQ_D / 4 + 4LL * 128;
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(append_kitty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)KITTY_KEY_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    append_kitty_kernel<<<(unsigned)((int64_t)c->batch * cfg->n_kv_heads), 128, KITTY_KEY_SMEM, st>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,

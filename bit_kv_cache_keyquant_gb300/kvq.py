@@ -66,6 +66,7 @@ def _load():
         "kv_quant_value": (S, [cfgp, _P, i64, _P, _P, _P]),
         "kv_append_kivi": (S, [cfgp, ctypes.POINTER(kvq_kivi_cache), _P, _P, _P]),
         "kv_append_int8": (S, [cfgp, ctypes.POINTER(kvq_int8_cache), _P, _P, _P]),
+        "kv_append_kitty": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), _P, _P, i32, _P]),
         "kv_quant_key_kitty": (S, [cfgp, _P, i64, i32, _P, _P]),
         "kv_quant_value_kitty": (S, [cfgp, _P, i64, _P, _P]),
         "kv_quant_int8_dither": (S, [cfgp, _P, i64, _P, _P, _P, i32, i32, ctypes.c_uint64, _P, _P, _P]),
@@ -92,7 +93,7 @@ def _load():
 
 _lib = _load()
 
-EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_append_int8", "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither",
+EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_append_int8", "kv_append_kitty", "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither",
             "kvq_kitty_key_page_bytes", "kvq_kitty_value_page_bytes", "kv_decode_attn_plan", "kv_decode_attn",
             "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_noalloc", "kv_decode_attn_stage1",
             "kv_decode_attn_merge",
@@ -165,6 +166,12 @@ def kv_append_int8(cfg, cache, k_new, v_new, stream=None):
     """Append one token per (batch row, kv head) to an INT8 cache: k_new, v_new fp16 [B][Hkv][D]."""
     _check(_lib.kv_append_int8(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new), _stream(stream)),
            "kv_append_int8")
+
+
+def kv_append_kitty(cfg, cache, k_new, v_new, score_mode=0, stream=None):
+    """Append one token per (batch row, kv head) to a Kitty cache: k_new, v_new fp16 [B][Hkv][D]."""
+    _check(_lib.kv_append_kitty(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new), score_mode,
+                                _stream(stream)), "kv_append_kitty")
 
 
 def kv_quant_key_kitty(cfg, k, n_pages, score_mode, pages, stream=None):

@@ -228,6 +228,24 @@ typedef struct {
     const void *v_local;     /* fp16 [B][Hkv][R][D] */
 } kvq_kitty_cache;
 
+/* Streaming append of one token per (batch row, kv head) to a Kitty cache,
+ * called before kv_decode_attn_kitty at every step.
+ *   k_new, v_new  fp16 [batch][n_kv_heads][D]
+ *   score_mode    as kv_quant_key_kitty
+ * With L = seq_len[b] cached it completes the quantization that follows the
+ * attention of the step with L tokens: a full key Q-buffer ((L-S) a positive
+ * multiple of G) becomes key page (L-S)/G - 1, a full value Q-buffer (E = L-S-R
+ * a positive multiple of G) becomes value page E/G - 1, and token L-R leaves
+ * the local window for value Q-buffer slot (L-R-S) % G; then token L goes to
+ * the sink (L < S) or to key Q-buffer slot (L-S) % G and local slot L % R,
+ * and seq_len[b] = L + 1 (Kitty "Stage 1: Inserting New KV Vectors",
+ * "Stage 3").  The page quantizers are those of kv_quant_key_kitty and
+ * kv_quant_value_kitty.  Two kernels on `stream`, graph-capturable; a row
+ * with seq_len[b] >= max_seq_len is left unchanged and
+ * KVQ_DEVICE_ERR_CAPACITY is recorded. */
+KVQ_API kvq_status kv_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new,
+                                   const void *v_new, int score_mode, cudaStream_t stream);
+
 /* INT8 dither: the first L - n_tail tokens are quantized in blocks of T,
  * n_tail = ((L-1) mod T) + 1 tokens of the active block stay fp16 (slot
  * t % T).  Dither is regenerated from (req_id[b], layer, kv head, token,

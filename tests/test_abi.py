@@ -81,6 +81,15 @@ def test_validation_without_gpu(K):
     assert K.raw_call("kv_append_kivi", ctypes.byref(good), None, 16, 16, None) == K.KVQ_ERR_INVALID_ARG
     assert K.raw_call("kv_append_kivi", ctypes.byref(K.make_config(bits_v=4)), ctypes.byref(cache), 16, 16,
                       None) == K.KVQ_ERR_UNSUPPORTED
+    kc = K.kvq_kitty_cache(2, 512, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert K.raw_call("kv_append_kitty", ctypes.byref(kitty), ctypes.byref(kc), 16, 16, 2, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert K.raw_call("kv_append_kitty", ctypes.byref(kitty), ctypes.byref(kc), 16, None, 0, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert K.raw_call("kv_append_kitty", ctypes.byref(kitty), ctypes.byref(kc), 0x1004, 16, 0, None) == \
+        K.KVQ_ERR_MISALIGNED
+    assert K.raw_call("kv_append_kitty", ctypes.byref(K.make_config(group_k=64)), ctypes.byref(kc), 16, 16, 0,
+                      None) == K.KVQ_ERR_UNSUPPORTED
     i8 = K.make_config(int8_block=200)
     assert K.raw_call("kv_quant_int8_dither", ctypes.byref(i8), 16, 1, 16, 16, 16, 0, 0, 0, 16, 16,
                       None) == K.KVQ_ERR_UNSUPPORTED

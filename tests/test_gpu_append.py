@@ -1,6 +1,7 @@
-"""Streaming append (kv_append_kivi, kv_append_int8): a cache grown token by token must
+"""Streaming append (kv_append_kivi, kv_append_int8, kv_append_kitty): a cache grown token by token must
 hold the bytes of a cache filled at once (the same quantizers; KIVI section
-3.3 with the insert -> attend -> quantize order, WitCert section 6.1 tail blocks),
+3.3 with the insert -> attend -> quantize order, Kitty "Stage 1" and "Stage 3" of its
+pipeline, WitCert section 6.1 tail blocks),
 and decode identically."""
 import numpy as np
 import pytest
@@ -210,3 +211,93 @@ def test_append_int8_matches_fill(K, orc, Hq, Hkv, L0, n):
                                                              L=L_end[b], seed=seed, request=int(reqs[b]), layer=layer,
                                                              kv_head=h)
     assert_attn_close(outs[0].float().cpu().numpy(), want)
+
+
+def _fill_kitty(cfg, Ks, Vs, L_each, max_seq_len, score_mode):
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hkv = len(Ks), len(Ks[0])
+    c = C.KittyCache(cfg, B, max_seq_len, device=DEV)
+    for b in range(B):
+        for h in range(Hkv):
+            c.fill(b, h, Ks[b][h][:L_each[b]].to(DEV), Vs[b][h][:L_each[b]].to(DEV), score_mode)
+    return c
+
+
+@pytest.mark.parametrize("Hq,Hkv,Kb,mode,L0,n", [
+    (4, 2, 16, 0, 1, 450),      # sink, then two key-page and two value-page flushes
+    (8, 2, 48, 1, 150, 300),
+    (2, 1, 0, 0, 287, 140),     # a value-page flush on the first append
+])
+def test_append_kitty_matches_fill(K, orc, Hq, Hkv, Kb, mode, L0, n):
+    from bit_kv_cache_keyquant_gb300.cache import kitty_segments
+    rng = np.random.default_rng(L0 + n + Kb)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv, group_k=128, boost_k=Kb)
+    G, S, R = cfg.group_k, cfg.sink, cfg.residual
+    B = 2
+    L_start = [L0, L0 + 5]
+    total = max(L_start) + n
+    max_seq_len = total + 2
+    gain = 1.0 + 9.0 * (rng.random(D) < 0.1)
+    Ks = [[torch.from_numpy((rng.standard_normal((total, D)) * gain).astype(np.float16)) for _ in range(Hkv)]
+          for _ in range(B)]
+    Vs = [[torch.from_numpy(rng.standard_normal((total, D)).astype(np.float16)) for _ in range(Hkv)] for _ in range(B)]
+    grown = _fill_kitty(cfg, Ks, Vs, L_start, max_seq_len, mode)
+    for step in range(n):
+        kn = torch.stack([torch.stack([Ks[b][h][L_start[b] + step] for h in range(Hkv)]) for b in range(B)]).to(DEV)
+        vn = torch.stack([torch.stack([Vs[b][h][L_start[b] + step] for h in range(Hkv)]) for b in range(B)]).to(DEV)
+        K.kv_append_kitty(cfg, grown.desc(), kn, vn, mode)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    L_end = [L + n for L in L_start]
+    full = _fill_kitty(cfg, Ks, Vs, L_end, max_seq_len, mode)
+    assert grown.seq_len.cpu().tolist() == L_end
+    for b in range(B):
+        L = L_end[b]
+        pk, nkb, pv, nvb, nloc = kitty_segments(L, G, S, R)
+        ns = min(L, S)
+        assert torch.equal(grown.k_pages[b, :, :pk], full.k_pages[b, :, :pk])
+        assert torch.equal(grown.v_pages[b, :, :pv], full.v_pages[b, :, :pv])
+        assert torch.equal(grown.k_sink[b, :, :ns], full.k_sink[b, :, :ns])
+        assert torch.equal(grown.v_sink[b, :, :ns], full.v_sink[b, :, :ns])
+        k0, v0 = S + pk * G, S + pv * G
+        kslots = [(t - S) % G for t in range(k0, L)]
+        vslots = [(t - S) % G for t in range(v0, v0 + nvb)]
+        lslots = [t % R for t in range(L - nloc, L)]
+        assert torch.equal(grown.k_qbuf[b, :, kslots], full.k_qbuf[b, :, kslots])
+        assert torch.equal(grown.v_qbuf[b, :, vslots], full.v_qbuf[b, :, vslots])
+        assert torch.equal(grown.v_local[b, :, lslots], full.v_local[b, :, lslots])
+    q = torch.from_numpy(rng.standard_normal((B, Hq, D)).astype(np.float16)).to(DEV)
+    outs = []
+    for c in (grown, full):
+        _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KITTY, B, max_seq_len)
+        ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device=DEV)
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float16, device=DEV)
+        K.kv_decode_attn_kitty(cfg, c.desc(), q, out, ws, wsb)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    g = Hq // Hkv
+    want = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hkv):
+            parts = orc.kitty_build_one(Ks[b][h][:L_end[b]].numpy(), Vs[b][h][:L_end[b]].numpy(), G, Kb, S, R, mode)
+            want[b, h * g:(h + 1) * g] = orc.kitty_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *parts,
+                                                              L=L_end[b], K=Kb, S=S, R=R)
+    assert_attn_close(outs[0].float().cpu().numpy(), want)
+
+
+def test_append_kitty_full_row_reports_capacity(K):
+    cfg = K.make_config(n_q_heads=2, n_kv_heads=1, group_k=128)
+    rng = np.random.default_rng(5)
+    L = 300
+    Ks = [[torch.from_numpy(rng.standard_normal((L, D)).astype(np.float16))]]
+    Vs = [[torch.from_numpy(rng.standard_normal((L, D)).astype(np.float16))]]
+    c = _fill_kitty(cfg, Ks, Vs, [L], L, 0)
+    before = [t.clone() for t in (c.k_pages, c.v_pages, c.k_qbuf, c.v_qbuf, c.v_local, c.k_sink)]
+    kn = torch.zeros((1, 1, D), dtype=torch.float16, device=DEV)
+    K.kv_append_kitty(cfg, c.desc(), kn, kn, 0)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == K.KVQ_DEVICE_ERR_CAPACITY
+    assert c.seq_len.cpu().tolist() == [L]
+    after = (c.k_pages, c.v_pages, c.k_qbuf, c.v_qbuf, c.v_local, c.k_sink)
+    assert all(torch.equal(x, y) for x, y in zip(before, after))
