@@ -17,7 +17,10 @@
  *   WitCert (arxiv 2607.28699, section 6): INT8 subtractive dither
  *     x^ = s(round(x/s + xi) - xi), Philox4x32-10 keyed by (request, layer,
  *     KV head, token, channel), block scale s = amax/126.5 stored in fp16 and
- *     used for quantization, split-free softmax.
+ *     used for quantization, split-free softmax.  Its token-granular form
+ *     for a slot-paged pool (the SGLang storage subsection): one scale per
+ *     token and group of Gc channels, Philox keyed by (layer, KV head, slot,
+ *     channel), every token quantized when it is written.
  *   Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *     Easy as 1, 2, 3", SC'11 (the published round function and constants).
  *
@@ -34,6 +37,9 @@
  *                       on the CPU by its inverse and by uniformity statistics
  *   attention           pinned (R >= L equals textbook softmax attention,
  *                       V == 1, K == 0, permutation invariance)
+ *   token-granular INT8 pinned (error bound, no clipping, group locality,
+ *                       unbiased and uniform dither error over slots,
+ *                       one-token attention, K == 0, slot gather)
  */
 #include <math.h>
 #include <stdint.h>
@@ -749,6 +755,91 @@ ORC_API void orc_int8_decode_one(int D, int T, int L, int n_heads, double sm_sca
                 v[(long)t * D + c] = orc_half_to_double(vtail[(long)(t % T) * D + c]);
             }
         }
+    double *qd = (double *)malloc(sizeof(double) * D);
+    for (int h = 0; h < n_heads; ++h) {
+        for (int c = 0; c < D; ++c) qd[c] = orc_half_to_double(q[(long)h * D + c]);
+        attend_f64(D, L, qd, k, v, sm_scale, out + (long)h * D);
+    }
+    free(qd); free(k); free(v);
+}
+
+/* ------------------------------------------------------------------ */
+/* Token-granular INT8 over a slot pool (WitCert, SGLang storage)        */
+/* ------------------------------------------------------------------ */
+
+/* Dither of the slot-keyed stream.  The tuple is (layer, KV head, slot,
+ * channel); counter = (slot, channel/4, (layer << 17) | (kv_sel << 16) |
+ * kv_head, 0), key and output word as orc_dither. */
+ORC_API float orc_dither_slot(uint64_t seed, int32_t layer, int kv_sel, int32_t kv_head, int32_t slot,
+                              int32_t channel)
+{
+    uint32_t ctr[4], key[2], out[4];
+    ctr[0] = (uint32_t)slot;
+    ctr[1] = (uint32_t)channel >> 2;
+    ctr[2] = ((uint32_t)layer << 17) | ((uint32_t)(kv_sel & 1) << 16) | ((uint32_t)kv_head & 0xFFFFu);
+    ctr[3] = 0u;
+    key[0] = (uint32_t)(seed & 0xFFFFFFFFu);
+    key[1] = (uint32_t)(seed >> 32);
+    orc_philox4x32_10(ctr, key, out);
+    float u = (float)(out[channel & 3] >> 8) * 0x1.0p-24f;
+    return u - 0.5f;
+}
+
+/* Quantize one token of one kv head written to `slot`: x fp16 [D].  For
+ * every group of Gc consecutive channels s = fp16_RN(amax / 126.5) (binary32
+ * division); code = clamp(rint(x/s + xi), -127, 127) in binary32 with the
+ * stored scale; s == 0 gives code 0.  codes int8 [D], scale fp16 [D/Gc]. */
+ORC_API void orc_int8t_quant_token(int D, int Gc, const uint16_t *x, uint64_t seed, int32_t layer, int kv_sel,
+                                   int32_t kv_head, int32_t slot, int8_t *codes, uint16_t *scale)
+{
+    for (int g = 0; g < D / Gc; ++g) {
+        double amax = 0.0;
+        for (int i = 0; i < Gc; ++i) {
+            double v = fabs(orc_half_to_double(x[g * Gc + i]));
+            if (v > amax) amax = v;
+        }
+        float s32 = (float)amax / 126.5f;
+        uint16_t s = orc_double_to_half((double)s32, ORC_RN);
+        scale[g] = s;
+        float sf = (float)orc_half_to_double(s);
+        for (int i = 0; i < Gc; ++i) {
+            int c = g * Gc + i;
+            int code = 0;
+            if (sf != 0.0f) {
+                float xf = (float)orc_half_to_double(x[c]);
+                float xi = orc_dither_slot(seed, layer, kv_sel, kv_head, slot, c);
+                float u = xf / sf;
+                float w = u + xi;
+                float r = rintf(w);
+                if (r < -127.0f) r = -127.0f;
+                if (r > 127.0f) r = 127.0f;
+                code = (int)r;
+            }
+            codes[c] = (int8_t)code;
+        }
+    }
+}
+
+/* Decode of one (request, kv head) over a slot pool: token t of the request
+ * lives in slot table[t]; kc, vc int8 [n_slots][Hkv][D]; ks, vs fp16
+ * [n_slots][Hkv][D/Gc].  Every token is dequantized as s (code - xi) with the
+ * dither of its slot, then softmax attention in binary64 over the L tokens. */
+ORC_API void orc_int8t_decode_one(int D, int Gc, int Hkv, int L, int n_heads, double sm_scale, uint64_t seed,
+                                  int32_t layer, int32_t kv_head, const int32_t *table, const uint16_t *q,
+                                  const int8_t *kc, const int8_t *vc, const uint16_t *ks, const uint16_t *vs,
+                                  double *out)
+{
+    double *k = (double *)malloc(sizeof(double) * (size_t)L * D + 8);
+    double *v = (double *)malloc(sizeof(double) * (size_t)L * D + 8);
+    for (int t = 0; t < L; ++t) {
+        long rec = (long)table[t] * Hkv + kv_head;
+        for (int c = 0; c < D; ++c) {
+            float xk = orc_dither_slot(seed, layer, 0, kv_head, table[t], c);
+            float xv = orc_dither_slot(seed, layer, 1, kv_head, table[t], c);
+            k[(long)t * D + c] = orc_int8_dequant(kc[rec * D + c], ks[rec * (D / Gc) + c / Gc], xk);
+            v[(long)t * D + c] = orc_int8_dequant(vc[rec * D + c], vs[rec * (D / Gc) + c / Gc], xv);
+        }
+    }
     double *qd = (double *)malloc(sizeof(double) * D);
     for (int h = 0; h < n_heads; ++h) {
         for (int c = 0; c < D; ++c) qd[c] = orc_half_to_double(q[(long)h * D + c]);

@@ -82,6 +82,9 @@ def _declare(l):
         "orc_kivi_decode_one": (None, [I, I, I, I, I, I, D, P, P, P, P, P, P, P, P]),
         "orc_kitty_decode_one": (None, [I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P, P]),
         "orc_int8_decode_one": (None, [I, I, I, I, D, U64, I32, I32, I32, P, P, P, P, P, P, P, P]),
+        "orc_dither_slot": (ctypes.c_float, [U64, I32, I, I32, I32, I32]),
+        "orc_int8t_quant_token": (None, [I, I, P, U64, I32, I, I32, I32, P, P]),
+        "orc_int8t_decode_one": (None, [I, I, I, I, I, D, U64, I32, I32, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(l, name)
@@ -266,6 +269,43 @@ def int8_quant_block(x: np.ndarray, seed: int, request: int, layer: int, kv_sel:
     lib().orc_int8_quant_block(Dm, T, _p(_h16(x)), seed, request, layer, kv_sel, kv_head, tok0,
                                _p(codes), _p(scale))
     return codes, scale
+
+
+def dither_slot(seed: int, layer: int, kv_sel: int, kv_head: int, slot: int, channel: int) -> float:
+    return lib().orc_dither_slot(seed, layer, kv_sel, kv_head, slot, channel)
+
+
+def int8t_quant_token(x: np.ndarray, Gc: int, seed: int, layer: int, kv_sel: int, kv_head: int, slot: int):
+    """One token of one kv head written to `slot`: fp16 [D] -> (int8 codes [D], fp16 bits scales [D/Gc])."""
+    Dm = x.shape[0]
+    codes = np.zeros(Dm, np.int8)
+    scale = np.zeros(Dm // Gc, np.uint16)
+    lib().orc_int8t_quant_token(Dm, Gc, _p(_h16(x)), seed, layer, kv_sel, kv_head, slot, _p(codes), _p(scale))
+    return codes, scale
+
+
+def int8t_write(pool, K: np.ndarray, V: np.ndarray, slots, kv_head: int, Gc: int, seed: int, layer: int):
+    """Quantize tokens K[i], V[i] ([n][D] fp16) of one kv head into pool slots slots[i].
+
+    pool = (kc, vc, ks, vs): int8 [n_slots][Hkv][D] and uint16 [n_slots][Hkv][D/Gc], updated in place."""
+    kc, vc, ks, vs = pool
+    for i, s in enumerate(slots):
+        kc[s, kv_head], ks[s, kv_head] = int8t_quant_token(K[i], Gc, seed, layer, 0, kv_head, int(s))
+        vc[s, kv_head], vs[s, kv_head] = int8t_quant_token(V[i], Gc, seed, layer, 1, kv_head, int(s))
+
+
+def int8t_decode_one(q, pool, table, kv_head: int, seed: int, layer: int, Gc: int = 32, sm_scale=None):
+    """One (request, kv head) whose token t sits in slot table[t]: q fp16 [g][D] -> binary64 [g][D]."""
+    kc, vc, ks, vs = pool
+    g, Dm = q.shape
+    Hkv = kc.shape[1]
+    tab = np.ascontiguousarray(table, dtype=np.int32)
+    sm = (1.0 / np.sqrt(Dm)) if sm_scale is None else sm_scale
+    out = np.zeros((g, Dm), np.float64)
+    lib().orc_int8t_decode_one(Dm, Gc, Hkv, len(tab), g, sm, seed, layer, kv_head, _p(tab), _p(_h16(q)),
+                               _p(np.ascontiguousarray(kc)), _p(np.ascontiguousarray(vc)), _p(_h16(ks)),
+                               _p(_h16(vs)), _p(out))
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -451,6 +451,148 @@ def test_int8_quantized_attention_error_is_small(orc):
 
 
 # --------------------------------------------------------------------------
+# token-granular INT8 over a slot pool (WitCert, SGLang storage subsection)
+# --------------------------------------------------------------------------
+def _int8t_xhat(orc, codes, scale, Gc, seed, layer, kv_sel, kv_head, slot):
+    return np.array([orc.half_to_double(int(scale[c // Gc])) *
+                     (int(codes[c]) - orc.dither_slot(seed, layer, kv_sel, kv_head, slot, c))
+                     for c in range(len(codes))])
+
+
+@pytest.mark.parametrize("Gc", [32, 64, 128])
+def test_int8t_scale_per_token_group_bound_and_no_clip(orc, Gc):
+    rng = np.random.default_rng(40 + Gc)
+    for trial in range(6):
+        x = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 3, 128)).astype(np.float16)
+        if trial == 0:
+            x[:Gc] = 0                                  # an all-zero group: s = 0, codes 0
+        slot = int(rng.integers(0, 2 ** 31 - 1))
+        codes, scale = orc.int8t_quant_token(x, Gc, 77, 5, trial & 1, 3, slot)
+        assert scale.shape == (128 // Gc,)
+        for g in range(128 // Gc):
+            amax = np.abs(x[g * Gc:(g + 1) * Gc].astype(np.float64)).max()
+            assert scale[g] == np.float16(np.float32(amax) / np.float32(126.5)).view(np.uint16)
+        # no clipping: |x/s + xi| < 127.07 always rounds inside [-127, 127]; the extreme codes stay reachable
+        assert np.all(np.abs(codes.astype(np.int32)) <= 127)
+        xhat = _int8t_xhat(orc, codes, scale, Gc, 77, 5, trial & 1, 3, slot)
+        s = np.array([orc.half_to_double(int(scale[c // Gc])) for c in range(128)])
+        assert np.all(np.abs(x.astype(np.float64) - xhat) <= s / 2 * (1 + 2 ** -20) + 1e-30)
+        if trial == 0:
+            assert np.all(codes[:Gc] == 0) and scale[0] == 0 and np.all(xhat[:Gc] == 0)
+
+
+def test_int8t_groups_are_independent(orc):
+    """Changing one group's channels leaves every other group's scale and codes unchanged."""
+    rng = np.random.default_rng(47)
+    x = rng.standard_normal(128).astype(np.float16)
+    a_codes, a_scale = orc.int8t_quant_token(x, 32, 1, 0, 0, 0, 1234)
+    y = x.copy()
+    y[64:96] *= np.float16(40)
+    b_codes, b_scale = orc.int8t_quant_token(y, 32, 1, 0, 0, 0, 1234)
+    keep = np.r_[0:64, 96:128]
+    assert np.array_equal(a_codes[keep], b_codes[keep])
+    assert a_scale[0] == b_scale[0] and a_scale[1] == b_scale[1] and a_scale[3] == b_scale[3]
+    assert a_scale[2] != b_scale[2]
+
+
+def test_int8t_dither_is_keyed_by_slot_unbiased_and_uniform(orc):
+    """Subtractive dither: over many slots the error x^ - x of a fixed value is uniform on
+    [-s/2, s/2) (mean 0, variance s^2/12) whatever x is; the stream depends on the slot only."""
+    x = np.zeros(128, np.float16)
+    x[0] = np.float16(126.5 * 0.01)                     # fixes s of group 0 near 0.01
+    x[1:32] = np.linspace(-1.2, 1.2, 31).astype(np.float16)
+    errs = []
+    for slot in range(1500):
+        codes, scale = orc.int8t_quant_token(x, 32, 9, 1, 0, 2, slot)
+        s = orc.half_to_double(int(scale[0]))
+        xhat = _int8t_xhat(orc, codes[:32], scale, 32, 9, 1, 0, 2, slot)
+        errs.append((xhat - x[:32].astype(np.float64)) / s)
+    e = np.array(errs)
+    assert np.all(np.abs(e) <= 0.5 * (1 + 2 ** -20))
+    n = e.shape[0]
+    assert np.all(np.abs(e.mean(axis=0)) < 4 * np.sqrt(1 / 12 / n))
+    assert np.all(np.abs(e.var(axis=0) - 1 / 12) < 0.012)
+    # the counter carries the slot, not the position: the same slot gives the same codes
+    c1, _ = orc.int8t_quant_token(x, 32, 9, 1, 0, 2, 700)
+    c2, _ = orc.int8t_quant_token(x, 32, 9, 1, 0, 2, 700)
+    c3, _ = orc.int8t_quant_token(x, 32, 9, 1, 0, 2, 701)
+    assert np.array_equal(c1, c2) and not np.array_equal(c1, c3)
+    # distinct (layer, kv_sel, kv_head, slot) give distinct streams
+    seen = {tuple(orc.dither_slot(9, la, ks, h, sl, c) for c in range(4))
+            for la in range(3) for ks in range(2) for h in range(3) for sl in (0, 1, 2 ** 31 - 1)}
+    assert len(seen) == 3 * 2 * 3 * 3
+
+
+def _int8t_pool(n_slots, Hkv, Gc=32):
+    return (np.zeros((n_slots, Hkv, 128), np.int8), np.zeros((n_slots, Hkv, 128), np.int8),
+            np.zeros((n_slots, Hkv, 128 // Gc), np.uint16), np.zeros((n_slots, Hkv, 128 // Gc), np.uint16))
+
+
+def test_int8t_decode_gathers_by_slot(orc):
+    """One token: attention returns its dequantized value (within s/2 of v); K == 0 gives the mean of
+    the dequantized values of the request's own slots, even with other slots holding large values."""
+    rng = np.random.default_rng(48)
+    Hkv, n_slots = 2, 300
+    pool = _int8t_pool(n_slots, Hkv)
+    junk = (rng.standard_normal((n_slots, 128)) * 1000).astype(np.float16)
+    for h in range(Hkv):
+        orc.int8t_write(pool, junk, junk, range(n_slots), h, 32, 5, 7)
+    # one token at slot 123 of kv head 1
+    k1 = rng.standard_normal((1, 128)).astype(np.float16)
+    v1 = rng.standard_normal((1, 128)).astype(np.float16)
+    orc.int8t_write(pool, k1, v1, [123], 1, 32, 5, 7)
+    q = rng.standard_normal((2, 128)).astype(np.float16)
+    o = orc.int8t_decode_one(q, pool, [123], 1, 5, 7)
+    s = np.repeat([orc.half_to_double(int(z)) for z in pool[3][123, 1]], 32)
+    for h in range(2):
+        assert np.all(np.abs(o[h] - v1[0].astype(np.float64)) <= s / 2 * (1 + 2 ** -20))
+    # K == 0 over a scattered request
+    L = 40
+    slots = rng.permutation(n_slots)[:L]
+    V = rng.standard_normal((L, 128)).astype(np.float16)
+    orc.int8t_write(pool, np.zeros((L, 128), np.float16), V, slots, 0, 32, 5, 7)
+    o = orc.int8t_decode_one(q, pool, slots, 0, 5, 7)
+    vhat = np.array([_int8t_xhat(orc, pool[1][s_, 0], pool[3][s_, 0], 32, 5, 7, 1, 0, int(s_)) for s_ in slots])
+    for h in range(2):
+        assert np.allclose(o[h], vhat.mean(axis=0), rtol=0, atol=1e-12)
+        assert np.max(np.abs(o[h] - V.astype(np.float64).mean(axis=0))) < 0.02
+
+
+def test_int8t_decode_equals_attention_over_slot_dequantized_tokens(orc):
+    """The decode equals textbook attention over keys and values dequantized element by element from
+    the request's slots with the dither of each slot (s (code - xi), evaluated here in numpy)."""
+    rng = np.random.default_rng(50)
+    Hkv, n_slots, L = 3, 400, 60
+    pool = _int8t_pool(n_slots, Hkv)
+    slots = rng.permutation(n_slots)[:L]
+    K = (rng.standard_normal((L, 128)) * 4).astype(np.float16)
+    V = rng.standard_normal((L, 128)).astype(np.float16)
+    orc.int8t_write(pool, K, V, slots, 2, 32, 21, 4)
+    q = rng.standard_normal((2, 128)).astype(np.float16)
+    o = orc.int8t_decode_one(q, pool, slots, 2, 21, 4)
+    khat = np.array([_int8t_xhat(orc, pool[0][s_, 2], pool[2][s_, 2], 32, 21, 4, 0, 2, int(s_)) for s_ in slots])
+    vhat = np.array([_int8t_xhat(orc, pool[1][s_, 2], pool[3][s_, 2], 32, 21, 4, 1, 2, int(s_)) for s_ in slots])
+    for h in range(2):
+        sc = khat @ q[h].astype(np.float64) * 128 ** -0.5
+        p = np.exp(sc - sc.max())
+        assert np.allclose(o[h], (p / p.sum()) @ vhat, rtol=0, atol=1e-12)
+
+
+def test_int8t_attention_close_to_fp(orc):
+    rng = np.random.default_rng(49)
+    L, n_slots = 500, 2048
+    pool = _int8t_pool(n_slots, 1)
+    K = rng.standard_normal((L, 128)).astype(np.float16)
+    V = rng.standard_normal((L, 128)).astype(np.float16)
+    slots = rng.permutation(n_slots)[:L]
+    orc.int8t_write(pool, K, V, slots, 0, 32, 11, 2)
+    q = rng.standard_normal((3, 128)).astype(np.float16)
+    out = orc.int8t_decode_one(q, pool, slots, 0, 11, 2)
+    for h in range(3):
+        assert np.max(np.abs(out[h] - textbook(q[h], K, V, 128 ** -0.5))) < 5e-3
+
+
+# --------------------------------------------------------------------------
 # synthetic input generator
 # --------------------------------------------------------------------------
 def test_inputs_distribution_and_determinism():
