@@ -194,3 +194,61 @@ class Int8Cache:
             nb, ntail = int8_segments(int(L), T)
             tot += 2 * (nb * T * D + nb * D * 2 + ntail * D * 2)
         return tot * self.cfg.n_kv_heads
+
+
+class Int8TokenCache:
+    """Token-granular INT8 KV pool of one layer: n_slots token slots shared by
+    all requests, a per-request slot table and a free-slot stack (the device
+    state of kv_append_int8_token / kv_release_int8_token)."""
+
+    def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, n_slots: int, layer: int = 0,
+                 seed: int = 0, device="cuda"):
+        self.cfg, self.batch, self.max_seq_len, self.n_slots = cfg, batch, max_seq_len, n_slots
+        self.layer, self.seed = layer, seed
+        H, Gc = cfg.n_kv_heads, cfg.int8_group
+        self.k_codes = torch.zeros((n_slots, H, D), dtype=torch.int8, device=device)
+        self.v_codes = torch.zeros((n_slots, H, D), dtype=torch.int8, device=device)
+        self.k_scale = torch.zeros((n_slots, H, D // Gc), dtype=torch.float16, device=device)
+        self.v_scale = torch.zeros((n_slots, H, D // Gc), dtype=torch.float16, device=device)
+        self.slot_table = torch.full((batch, max_seq_len), -1, dtype=torch.int32, device=device)
+        self.seq_len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.free_slots = torch.empty(n_slots, dtype=torch.int32, device=device)
+        self.top = torch.zeros(4, dtype=torch.int32, device=device)
+        kvq.kv_slot_pool_init(self.pool())
+
+    def pool(self) -> kvq.kvq_slot_pool:
+        return kvq.kvq_slot_pool(self.n_slots, self.free_slots.data_ptr(), self.top.data_ptr())
+
+    def desc(self) -> kvq.kvq_int8_token_cache:
+        return kvq.kvq_int8_token_cache(self.batch, self.max_seq_len, self.seq_len.data_ptr(),
+                                        self.slot_table.data_ptr(), self.n_slots, self.layer, self.seed,
+                                        self.k_codes.data_ptr(), self.v_codes.data_ptr(), self.k_scale.data_ptr(),
+                                        self.v_scale.data_ptr())
+
+    def shuffle_free(self, perm_pages, page: int = 16):
+        """Reorder the free stack by pages of `page` slots (a permutation of the pages, host setup), so that
+        later pops hand out scattered pages as a long-running allocator would."""
+        top = int(self.top[0].item())
+        free = self.free_slots[:top].flip(0)                      # pop order
+        n = top // page * page
+        idx = torch.as_tensor(perm_pages, dtype=torch.int64, device=free.device)
+        pages = free[:n].view(-1, page)[idx].reshape(-1)
+        self.free_slots[:top] = torch.cat([pages, free[n:]]).flip(0)
+
+    def fill(self, b: int, K: torch.Tensor, V: torch.Tensor, stream=None):
+        """Append L tokens K, V fp16 [L][Hkv][D] to request b (slots popped from the free stack)."""
+        L = K.shape[0]
+        L0 = int(self.seq_len[b].item())
+        top = int(self.top[0].item())
+        assert L0 + L <= self.max_seq_len and L <= top
+        slots = self.free_slots[top - L:top].flip(0).contiguous()
+        self.top[0] = top - L
+        kvq.kv_quant_int8_token(self.cfg, self.desc(), K.contiguous(), L, slots, 0, stream)
+        kvq.kv_quant_int8_token(self.cfg, self.desc(), V.contiguous(), L, slots, 1, stream)
+        self.slot_table[b, L0:L0 + L] = slots
+        self.seq_len[b] = L0 + L
+
+    def nbytes_read(self, lens) -> int:
+        """Bytes a decode must read: codes and scales of K and V per (token, kv head), plus the slot table."""
+        per_tok = self.cfg.n_kv_heads * 2 * (D + 2 * (D // self.cfg.int8_group)) + 4
+        return int(sum(int(L) for L in lens)) * per_tok

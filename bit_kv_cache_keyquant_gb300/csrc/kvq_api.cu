@@ -56,15 +56,17 @@ float sm_scale_of(const kvq_config *cfg) {
 // Splits: chunks of a multiple of 128 tokens (the stage), sized so that the
 // persistent decode grid (4 CTAs per SM, 2 for INT8) gets about 8 units per CTA, within
 // [128, 4096] tokens and at most 256 + 1 splits per row (the last split of
-// a row holds the tokens outside the quantized tiles, e.g. the fp16 residual).
+// a row holds the tokens outside the quantized tiles, e.g. the fp16 residual;
+// the token-granular INT8 cache has none and leaves that split empty).
 kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
     const int64_t rows = (int64_t)batch * cfg->n_q_heads;
     // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI and Kitty kernels (4 CTAs per SM)
     // handle all query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
-    const bool kv_units = variant == KVQ_VARIANT_INT8 || (variant == KVQ_VARIANT_KIVI && kivi_gqa_supported(cfg)) ||
+    const bool int8 = variant == KVQ_VARIANT_INT8 || variant == KVQ_VARIANT_INT8_TOKEN;
+    const bool kv_units = int8 || (variant == KVQ_VARIANT_KIVI && kivi_gqa_supported(cfg)) ||
                           (variant == KVQ_VARIANT_KITTY && kitty_gqa_supported(cfg));
     const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads : rows;
-    const int ctas = variant == KVQ_VARIANT_INT8 ? 2 : 4;
+    const int ctas = int8 ? 2 : 4;
     const int64_t target_units = 8LL * num_sms() * ctas;
     int64_t chunk = (unit_rows * max_seq_len + target_units - 1) / target_units;
     chunk = (chunk + 127) / 128 * 128;
@@ -124,6 +126,15 @@ static kvq_status check_int8(const kvq_config *cfg) {
     if (s) return s;
     if (cfg->int8_block <= 0) return KVQ_ERR_INVALID_ARG;
     if (cfg->int8_block % 128 != 0) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+static kvq_status check_int8_token(const kvq_config *cfg) {
+    kvq_status s = check_common(cfg);
+    if (s) return s;
+    if (cfg->int8_group <= 0) return KVQ_ERR_INVALID_ARG;
+    if (cfg->int8_group != 32 && cfg->int8_group != 64 && cfg->int8_group != 128) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->n_q_heads / cfg->n_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
 }
 
@@ -193,6 +204,55 @@ extern "C" kvq_status kv_append_kitty(const kvq_config *cfg, const kvq_kitty_cac
     return cuda_status(launch_append_kitty(cfg, c, k_new, v_new, score_mode, stream));
 }
 
+static kvq_status check_int8_token_cache(const kvq_int8_token_cache *c) {
+    if (!c || c->batch < 1 || c->max_seq_len < 1 || c->n_slots < 1) return KVQ_ERR_INVALID_ARG;
+    if (c->layer < 0 || c->layer >= (1 << 15)) return KVQ_ERR_INVALID_ARG;
+    if ((int64_t)c->batch * c->max_seq_len > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+    return ptrs_ok({c->seq_len, c->slot_table, c->k_codes, c->v_codes, c->k_scale, c->v_scale});
+}
+
+static kvq_status check_pool(const kvq_slot_pool *pool) {
+    if (!pool || pool->capacity < 1) return KVQ_ERR_INVALID_ARG;
+    return ptrs_ok({pool->slots, pool->top});
+}
+
+extern "C" kvq_status kv_quant_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *x,
+                                          int64_t n, const int32_t *slots, int32_t kv_sel, cudaStream_t stream) {
+    kvq_status s = check_int8_token(cfg);
+    if (s) return s;
+    if (n < 0 || (kv_sel != 0 && kv_sel != 1)) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_int8_token_cache(c))) return s;
+    if (n == 0) return KVQ_OK;
+    if ((s = ptrs_ok({x, slots}))) return s;
+    return cuda_status(launch_quant_int8_token(cfg, c, x, n, slots, kv_sel, stream));
+}
+
+extern "C" kvq_status kv_slot_pool_init(const kvq_slot_pool *pool, cudaStream_t stream) {
+    kvq_status s = check_pool(pool);
+    if (s) return s;
+    return cuda_status(launch_slot_pool_init(pool, stream));
+}
+
+extern "C" kvq_status kv_append_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c,
+                                           const kvq_slot_pool *pool, const void *k_new, const void *v_new,
+                                           cudaStream_t stream) {
+    kvq_status s = check_int8_token(cfg);
+    if (s) return s;
+    if ((s = check_int8_token_cache(c))) return s;
+    if ((s = check_pool(pool))) return s;
+    if ((s = ptrs_ok({k_new, v_new}))) return s;
+    return cuda_status(launch_append_int8_token(cfg, c, pool, k_new, v_new, stream));
+}
+
+extern "C" kvq_status kv_release_int8_token(const kvq_int8_token_cache *c, int32_t row, const kvq_slot_pool *pool,
+                                            cudaStream_t stream) {
+    kvq_status s = check_int8_token_cache(c);
+    if (s) return s;
+    if (row < 0 || row >= c->batch) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_pool(pool))) return s;
+    return cuda_status(launch_release_int8_token(c, row, pool, stream));
+}
+
 extern "C" size_t kvq_kitty_key_page_bytes(const kvq_config *cfg) {
     if (check_kitty(cfg)) return 0;
     return (size_t)KVQ_D * cfg->group_k / 4 + (size_t)cfg->boost_k * cfg->group_k / 4 + KVQ_D + 4 * KVQ_D;
@@ -245,6 +305,7 @@ extern "C" kvq_status kv_decode_attn_plan(const kvq_config *cfg, int32_t variant
     kvq_status s = variant == KVQ_VARIANT_KIVI    ? check_kivi(cfg)
                    : variant == KVQ_VARIANT_KITTY ? check_kitty(cfg)
                    : variant == KVQ_VARIANT_INT8  ? check_int8(cfg)
+                   : variant == KVQ_VARIANT_INT8_TOKEN ? check_int8_token(cfg)
                                                   : KVQ_ERR_INVALID_ARG;
     if (s) return s;
     if (batch < 1 || max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
@@ -302,6 +363,16 @@ static kvq_status stage1_int8(const kvq_config *cfg, const kvq_int8_cache *c, co
     return cuda_status(launch_decode_int8(cfg, c, q, *p, ws, st));
 }
 
+static kvq_status stage1_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *q, void *ws,
+                                    size_t wsb, cudaStream_t st, DecodePlan *p) {
+    kvq_status s = check_int8_token(cfg);
+    if (s) return s;
+    if ((s = check_int8_token_cache(c))) return s;
+    if ((s = check_ws(cfg, KVQ_VARIANT_INT8_TOKEN, c->batch, c->max_seq_len, ws, wsb, p))) return s;
+    if ((s = ptrs_ok({q}))) return s;
+    return cuda_status(launch_decode_int8_token(cfg, c, q, *p, ws, st));
+}
+
 extern "C" kvq_status kv_decode_attn_stage1(const kvq_config *cfg, int32_t variant, const void *cache, const void *q,
                                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     DecodePlan p;
@@ -313,6 +384,9 @@ extern "C" kvq_status kv_decode_attn_stage1(const kvq_config *cfg, int32_t varia
                                 &p);
         case KVQ_VARIANT_INT8:
             return stage1_int8(cfg, static_cast<const kvq_int8_cache *>(cache), q, workspace, workspace_bytes, stream, &p);
+        case KVQ_VARIANT_INT8_TOKEN:
+            return stage1_int8_token(cfg, static_cast<const kvq_int8_token_cache *>(cache), q, workspace,
+                                     workspace_bytes, stream, &p);
         default:
             return KVQ_ERR_INVALID_ARG;
     }
@@ -324,6 +398,7 @@ extern "C" kvq_status kv_decode_attn_merge(const kvq_config *cfg, int32_t varian
     kvq_status s = variant == KVQ_VARIANT_KIVI    ? check_kivi(cfg)
                    : variant == KVQ_VARIANT_KITTY ? check_kitty(cfg)
                    : variant == KVQ_VARIANT_INT8  ? check_int8(cfg)
+                   : variant == KVQ_VARIANT_INT8_TOKEN ? check_int8_token(cfg)
                                                   : KVQ_ERR_INVALID_ARG;
     if (s) return s;
     DecodePlan p;
@@ -358,6 +433,17 @@ extern "C" kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_
     if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
     DecodePlan p;
     kvq_status s = stage1_int8(cfg, cache, q, workspace, workspace_bytes, stream, &p);
+    if (s) return s;
+    return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
+}
+
+extern "C" kvq_status kv_decode_attn_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *cache,
+                                                const void *q, void *out, void *workspace, size_t workspace_bytes,
+                                                cudaStream_t stream) {
+    if (!out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
+    DecodePlan p;
+    kvq_status s = stage1_int8_token(cfg, cache, q, workspace, workspace_bytes, stream, &p);
     if (s) return s;
     return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
 }

@@ -106,9 +106,11 @@ __device__ __forceinline__ uint4 philox_rk(uint4 c, const uint32_t *rk0, const u
     return c;
 }
 
-// dither of the four channels 4*lane..4*lane+3 of token t (exact: (w >> 8) 2^-24 - 1/2)
-__device__ __forceinline__ void dither4(const Params &P, uint32_t c2, uint32_t req, int t, int lane, float xi[4]) {
-    const uint4 r = philox_rk(make_uint4((uint32_t)t, (uint32_t)lane, c2, req), P.rk0, P.rk1);
+// dither of the four channels 4*lane..4*lane+3 for counter word 0 = t (the
+// token, or the slot) and word 3 = w3 (exact: (w >> 8) 2^-24 - 1/2)
+template <typename PP>
+__device__ __forceinline__ void dither4(const PP &P, uint32_t c2, uint32_t w3, int t, int lane, float xi[4]) {
+    const uint4 r = philox_rk(make_uint4((uint32_t)t, (uint32_t)lane, c2, w3), P.rk0, P.rk1);
     xi[0] = dither_from_word(r.x);
     xi[1] = dither_from_word(r.y);
     xi[2] = dither_from_word(r.z);
@@ -129,6 +131,85 @@ struct HeadState {
     unsigned long long acc2[GMAX / 2][4];
     float m, l;
 };
+
+// alpha q of the g <= GMAX query heads of kv head kvh (q_row = the batch
+// row's [Hq][D] queries) for this lane's four channels, as head pairs;
+// heads >= g get weight 0
+__device__ __forceinline__ void load_key_weights(const uint16_t *q_row, int kvh, int g, float alpha, int lane,
+                                                 unsigned long long wk2[GMAX / 2][4]) {
+    float qa[GMAX][4];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+        const int hq = kvh * g + min(h, g - 1);
+        const uint2 qv = *reinterpret_cast<const uint2 *>(q_row + (int64_t)hq * KVQ_D + 4 * lane);
+        const float z = h < g ? alpha : 0.f;
+        qa[h][0] = h2f(lo16(qv.x)) * z;
+        qa[h][1] = h2f(hi16(qv.x)) * z;
+        qa[h][2] = h2f(lo16(qv.y)) * z;
+        qa[h][3] = h2f(hi16(qv.y)) * z;
+    }
+#pragma unroll
+    for (int j = 0; j < GMAX / 2; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wk2[j][i] = pack2f(qa[2 * j][i], qa[2 * j + 1][i]);
+}
+
+__device__ __forceinline__ void head_state_init(HeadState &H) {
+    H.m = -INFINITY;
+    H.l = 0.f;
+#pragma unroll
+    for (int j = 0; j < GMAX / 2; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) H.acc2[j][i] = 0ull;
+}
+
+// Merge the NCWARP consumer warps' states of one unit and write (o_s, lse_s)
+// of its g query heads (workspace rows head_row0 .. head_row0 + g - 1).
+template <typename SM>
+__device__ __forceinline__ void write_unit(SM &S, const HeadState &H, float *ws_o, float *ws_lse, int64_t head_row0,
+                                           int g, int splits, int split, int warp, int lane) {
+    // ---- warp states -> shared memory ----
+    {
+        float l_w = H.l;
+        l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
+        l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
+#pragma unroll
+        for (int j = 0; j < GMAX / 2; ++j) {
+            *reinterpret_cast<float4 *>(&S.st_acc[warp][2 * j][4 * lane]) =
+                make_float4(lo2f(H.acc2[j][0]), lo2f(H.acc2[j][1]), lo2f(H.acc2[j][2]), lo2f(H.acc2[j][3]));
+            *reinterpret_cast<float4 *>(&S.st_acc[warp][2 * j + 1][4 * lane]) =
+                make_float4(hi2f(H.acc2[j][0]), hi2f(H.acc2[j][1]), hi2f(H.acc2[j][2]), hi2f(H.acc2[j][3]));
+        }
+        if (lane < GMAX) {
+            S.st_m[warp][lane] = H.m;
+            S.st_l[warp][lane] = l_w;
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+    // ---- merge the four warp states per head: warp w writes heads w, w + 4 ----
+    for (int h = warp; h < g; h += NCWARP) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i][h]);
+        float l = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M > -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < NCWARP; ++i) {
+                const float w = S.st_m[i][h] > -INFINITY ? exp2f(S.st_m[i][h] - M) : 0.f;
+                l += w * S.st_l[i][h];
+                const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][h][4 * lane]);
+                o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+            }
+        }
+        const int64_t row = (head_row0 + h) * splits + split;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        *reinterpret_cast<float4 *>(ws_o + row * KVQ_D + 4 * lane) =
+            make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        if (lane == 0) ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+}
 
 // One tile of n <= 32 tokens.  kfn(tt, kv[4]) / vfn(tt, vv[4]) return this
 // lane's four dequantized channels of token tt of the tile; wk2[j][i] holds
@@ -270,32 +351,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit U = unit_of(P, u);
-        // alpha q of the g heads for this lane's four channels, as head pairs
         unsigned long long wk2[GMAX / 2][4];
-        {
-            float qa[GMAX][4];
-#pragma unroll
-            for (int h = 0; h < GMAX; ++h) {
-                const int hq = U.kvh * g + min(h, g - 1);
-                const uint2 qv = *reinterpret_cast<const uint2 *>(P.q + ((int64_t)U.b * P.Hq + hq) * KVQ_D + 4 * lane);
-                const float z = h < g ? P.alpha : 0.f;
-                qa[h][0] = h2f(lo16(qv.x)) * z;
-                qa[h][1] = h2f(hi16(qv.x)) * z;
-                qa[h][2] = h2f(lo16(qv.y)) * z;
-                qa[h][3] = h2f(hi16(qv.y)) * z;
-            }
-#pragma unroll
-            for (int j = 0; j < GMAX / 2; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) wk2[j][i] = pack2f(qa[2 * j][i], qa[2 * j + 1][i]);
-        }
+        load_key_weights(P.q + (int64_t)U.b * P.Hq * KVQ_D, U.kvh, g, P.alpha, lane, wk2);
         HeadState H;
-        H.m = -INFINITY;
-        H.l = 0.f;
-#pragma unroll
-        for (int j = 0; j < GMAX / 2; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) H.acc2[j][i] = 0ull;
+        head_state_init(H);
         const uint32_t c2 = P.ctr2_layer | (uint32_t)U.kvh;
         const uint32_t req = (uint32_t)P.req_id[U.b];
         if (U.residual) {
@@ -354,48 +413,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
         }
-        // ---- warp states -> shared memory ----
-        {
-            float l_w = H.l;
-            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
-            l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
-#pragma unroll
-            for (int j = 0; j < GMAX / 2; ++j) {
-                *reinterpret_cast<float4 *>(&S.st_acc[warp][2 * j][4 * lane]) =
-                    make_float4(lo2f(H.acc2[j][0]), lo2f(H.acc2[j][1]), lo2f(H.acc2[j][2]), lo2f(H.acc2[j][3]));
-                *reinterpret_cast<float4 *>(&S.st_acc[warp][2 * j + 1][4 * lane]) =
-                    make_float4(hi2f(H.acc2[j][0]), hi2f(H.acc2[j][1]), hi2f(H.acc2[j][2]), hi2f(H.acc2[j][3]));
-            }
-            if (lane < GMAX) {
-                S.st_m[warp][lane] = H.m;
-                S.st_l[warp][lane] = l_w;
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
-        // ---- merge the four warp states per head: warp w writes heads w, w + 4 ----
-        for (int h = warp; h < g; h += NCWARP) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < NCWARP; ++i) M = fmaxf(M, S.st_m[i][h]);
-            float l = 0.f;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M > -INFINITY) {
-#pragma unroll
-                for (int i = 0; i < NCWARP; ++i) {
-                    const float w = S.st_m[i][h] > -INFINITY ? exp2f(S.st_m[i][h] - M) : 0.f;
-                    l += w * S.st_l[i][h];
-                    const float4 a = *reinterpret_cast<const float4 *>(&S.st_acc[i][h][4 * lane]);
-                    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
-                }
-            }
-            const int hq = U.kvh * g + h;
-            const int64_t row = ((int64_t)U.b * P.Hq + hq) * P.splits + U.split;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
-                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-            if (lane == 0) P.ws_lse[row] = l > 0.f ? M + log2f(l) : -INFINITY;
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+        write_unit(S, H, P.ws_o, P.ws_lse, (int64_t)U.b * P.Hq + U.kvh * g, g, P.splits, U.split, warp, lane);
     }
 }
 
@@ -447,6 +465,238 @@ cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, c
     int64_t grid = (int64_t)num_sms() * 2;
     if (grid > n_units) grid = n_units;
     int8_decode_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Token-granular INT8 over a slot pool (WitCert, SGLang storage subsection):
+// token t of request b lives in slot table[b][t]; its codes are one 128-byte
+// row of the pool and its scales one fp16 per Gc channels.  Same tile code as
+// above; the producer warp gathers a stage's rows by slot: each of its 32
+// lanes reads the slots of four tokens, copies their scales (plain loads, 2-8
+// bytes) and slot ids into shared memory, arrives on the stage barrier with
+// the byte count of its code rows and then issues those 128-byte bulk copies.
+// Every token is quantized, so there is no fp16 tail and no residual unit.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct SmemT {
+    uint8_t kc[NSTAGE][CODES_BYTES];
+    uint8_t vc[NSTAGE][CODES_BYTES];
+    uint16_t ks[NSTAGE][STAGE_TOK][4];     // per-token scales, D/Gc <= 4 used
+    uint16_t vs[NSTAGE][STAGE_TOK][4];
+    int32_t slot[NSTAGE][STAGE_TOK];
+    uint64_t full[NSTAGE];
+    uint64_t empty[NSTAGE];
+    float pw[NCWARP][32][GMAX];
+    float st_acc[NCWARP][GMAX][KVQ_D];
+    float st_m[NCWARP][GMAX];
+    float st_l[NCWARP][GMAX];
+};
+
+struct ParamsT {
+    const int32_t *seq_len, *table;
+    const int8_t *k_codes, *v_codes;
+    const uint16_t *k_scale, *v_scale;
+    const uint16_t *q;
+    float *ws_o, *ws_lse;
+    unsigned *err;
+    int B, Hq, Hkv, g, splits, chunk, cap, n_slots, nsc, gshift;
+    uint32_t ctr2_layer;
+    uint32_t rk0[10], rk1[10];
+    float alpha;
+};
+
+struct UnitT {
+    int b, kvh, split, t0, t1;
+};
+
+__device__ __forceinline__ UnitT unit_of_t(const ParamsT &P, int u) {
+    UnitT U;
+    const int rows = P.B * P.Hkv;
+    U.split = u / rows;
+    const int row = u - U.split * rows;
+    U.b = row / P.Hkv;
+    U.kvh = row - U.b * P.Hkv;
+    const int L = min(P.seq_len[U.b], P.cap);   // a length above the table's row is read as the full row
+    U.t0 = U.split * P.chunk;
+    U.t1 = max(U.t0, min(U.t0 + P.chunk, L));
+    return U;
+}
+
+// nsc fp16 scales of one record (nsc = 4, 2 or 1; 8-, 4- or 2-byte aligned)
+__device__ __forceinline__ uint2 load_scales(const uint16_t *p, int nsc) {
+    if (nsc == 4) return __ldg(reinterpret_cast<const uint2 *>(p));
+    if (nsc == 2) return make_uint2(__ldg(reinterpret_cast<const unsigned *>(p)), 0u);
+    return make_uint2((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)), 0u);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel(ParamsT P) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    SmemT &S = *reinterpret_cast<SmemT *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_units = P.B * P.Hkv * P.splits;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&S.full[i], 32);
+            mbar_init(&S.empty[i], NCWARP);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCWARP) {
+        bool ok = true;
+        int sg = 0;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const UnitT U = unit_of_t(P, u);
+            const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
+            const int32_t *trow = P.table + (int64_t)U.b * P.cap;
+            for (int s = 0; s < nst; ++s, ++sg) {
+                const int buf = sg % NSTAGE;
+                if (sg >= NSTAGE) ok = mbar_wait(&S.empty[buf], ((sg / NSTAGE) - 1) & 1, P.err);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                const int tok = U.t0 + s * STAGE_TOK;
+                const int nt = min(STAGE_TOK, U.t1 - tok);
+                int64_t rec[4];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = lane + 32 * j;
+                    rec[j] = -1;
+                    if (i < nt) {
+                        int32_t sl = __ldg(trow + tok + i);
+                        if (sl < 0 || sl >= P.n_slots) {   // a table entry outside the pool: read slot 0, flag it
+                            atomicOr(P.err, KVQ_DEVICE_ERR_POOL);
+                            sl = 0;
+                        }
+                        rec[j] = (int64_t)sl * P.Hkv + U.kvh;
+                        S.slot[buf][i] = sl;
+                        const uint2 a = load_scales(P.k_scale + rec[j] * P.nsc, P.nsc);
+                        const uint2 b = load_scales(P.v_scale + rec[j] * P.nsc, P.nsc);
+                        *reinterpret_cast<uint2 *>(&S.ks[buf][i][0]) = a;
+                        *reinterpret_cast<uint2 *>(&S.vs[buf][i][0]) = b;
+                        bytes += 2 * KVQ_D;
+                    }
+                }
+                mbar_expect_tx(&S.full[buf], bytes);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (rec[j] >= 0) {
+                        const int i = lane + 32 * j;
+                        bulk_g2s(S.kc[buf] + i * KVQ_D, P.k_codes + rec[j] * KVQ_D, KVQ_D, &S.full[buf]);
+                        bulk_g2s(S.vc[buf] + i * KVQ_D, P.v_codes + rec[j] * KVQ_D, KVQ_D, &S.full[buf]);
+                    }
+                }
+            }
+        }
+        // no copy may be in flight when the CTA exits
+        for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
+        return;
+    }
+
+    const int g = P.g;
+    const int gi = lane >> P.gshift;       // the lane's channel group
+    bool ok = true;
+    int sg = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const UnitT U = unit_of_t(P, u);
+        unsigned long long wk2[GMAX / 2][4];
+        load_key_weights(P.q + (int64_t)U.b * P.Hq * KVQ_D, U.kvh, g, P.alpha, lane, wk2);
+        HeadState H;
+        head_state_init(H);
+        const uint32_t c2 = P.ctr2_layer | (uint32_t)U.kvh;
+        const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
+        for (int s = 0; s < nst; ++s, ++sg) {
+            const int buf = sg % NSTAGE;
+            ok = ok && mbar_wait(&S.full[buf], (sg / NSTAGE) & 1, P.err);
+            const int r0 = U.t0 + s * STAGE_TOK + 32 * warp;
+            const int n = min(32, U.t1 - r0);
+            if (ok && n > 0) {
+                const uint8_t *kc = S.kc[buf] + 32 * warp * KVQ_D + 4 * lane;
+                const uint8_t *vc = S.vc[buf] + 32 * warp * KVQ_D + 4 * lane;
+                const uint16_t(*ks)[4] = S.ks[buf] + 32 * warp;
+                const uint16_t(*vs)[4] = S.vs[buf] + 32 * warp;
+                const int32_t *sl = S.slot[buf] + 32 * warp;
+                auto kfn = [=](int tt, float kv[4]) {
+                    float c[4], xi[4];
+                    i8x4_to_f32(*reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c);
+                    dither4(P, c2, 0u, sl[tt], lane, xi);
+                    const float sc = h2f(ks[tt][gi]);
+                    kv[0] = sc * (c[0] - xi[0]);
+                    kv[1] = sc * (c[1] - xi[1]);
+                    kv[2] = sc * (c[2] - xi[2]);
+                    kv[3] = sc * (c[3] - xi[3]);
+                };
+                auto vfn = [=](int tt, float vv[4]) {
+                    float c[4], xi[4];
+                    i8x4_to_f32(*reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c);
+                    dither4(P, c2 | 0x10000u, 0u, sl[tt], lane, xi);
+                    const float sc = h2f(vs[tt][gi]);
+                    vv[0] = sc * (c[0] - xi[0]);
+                    vv[1] = sc * (c[1] - xi[1]);
+                    vv[2] = sc * (c[2] - xi[2]);
+                    vv[3] = sc * (c[3] - xi[3]);
+                };
+                tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[buf]);
+        }
+        write_unit(S, H, P.ws_o, P.ws_lse, (int64_t)U.b * P.Hq + U.kvh * g, g, P.splits, U.split, warp, lane);
+    }
+}
+
+cudaError_t launch_decode_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *q,
+                                     const DecodePlan &p, void *ws, cudaStream_t st) {
+    ParamsT P;
+    P.seq_len = c->seq_len;
+    P.table = c->slot_table;
+    P.k_codes = static_cast<const int8_t *>(c->k_codes);
+    P.v_codes = static_cast<const int8_t *>(c->v_codes);
+    P.k_scale = static_cast<const uint16_t *>(c->k_scale);
+    P.v_scale = static_cast<const uint16_t *>(c->v_scale);
+    P.q = static_cast<const uint16_t *>(q);
+    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
+    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
+    P.err = device_error_ptr();
+    P.B = c->batch;
+    P.Hq = cfg->n_q_heads;
+    P.Hkv = cfg->n_kv_heads;
+    P.g = cfg->n_q_heads / cfg->n_kv_heads;
+    P.splits = p.splits;
+    P.chunk = p.chunk;
+    P.cap = c->max_seq_len;
+    P.n_slots = c->n_slots;
+    P.nsc = KVQ_D / cfg->int8_group;
+    P.gshift = cfg->int8_group == 32 ? 3 : cfg->int8_group == 64 ? 4 : 5;
+    P.ctr2_layer = (uint32_t)c->layer << 17;
+    const uint32_t k0 = (uint32_t)(c->seed & 0xFFFFFFFFu), k1 = (uint32_t)(c->seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        P.rk0[r] = k0 + (uint32_t)r * 0x9E3779B9u;
+        P.rk1[r] = k1 + (uint32_t)r * 0xBB67AE85u;
+    }
+    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    if (!P.err) return cudaErrorInvalidDevicePointer;
+    if (P.g > GMAX) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(SmemT);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(int8_token_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
+    int64_t grid = (int64_t)num_sms() * 2;
+    if (grid > n_units) grid = n_units;
+    int8_token_decode_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
     return cudaGetLastError();
 }
 

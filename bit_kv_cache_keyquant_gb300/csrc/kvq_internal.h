@@ -55,6 +55,15 @@ cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
                                 const DecodePlan &p, void *ws, cudaStream_t st);
 cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *q,
                                const DecodePlan &p, void *ws, cudaStream_t st);
+cudaError_t launch_decode_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *q,
+                                     const DecodePlan &p, void *ws, cudaStream_t st);
+cudaError_t launch_quant_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *x, int64_t n,
+                                    const int32_t *slots, int kv_sel, cudaStream_t st);
+cudaError_t launch_slot_pool_init(const kvq_slot_pool *pool, cudaStream_t st);
+cudaError_t launch_append_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const kvq_slot_pool *pool,
+                                     const void *k_new, const void *v_new, cudaStream_t st);
+cudaError_t launch_release_int8_token(const kvq_int8_token_cache *c, int row, const kvq_slot_pool *pool,
+                                      cudaStream_t st);
 cudaError_t launch_merge(const kvq_config *cfg, int batch, const DecodePlan &p, const void *ws, void *out,
                          cudaStream_t st);
 

@@ -39,7 +39,7 @@ _C2 = 0xC2B2AE35
 _GOLD = 0x9E3779B1
 
 # tensor ids of the hash streams
-T_K, T_V, T_Q, T_SCALE, T_LEN, T_REQ, T_OUTLIER = 1, 2, 3, 4, 5, 6, 7
+T_K, T_V, T_Q, T_SCALE, T_LEN, T_REQ, T_OUTLIER, T_SLOT = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 @dataclasses.dataclass(frozen=True)
@@ -51,7 +51,7 @@ class Workload:
     n_q_heads: int
     n_kv_heads: int
     seq_len: int                 # fixed length, or the upper bound when ragged
-    variant: str                 # "kivi", "kitty", "int8"
+    variant: str                 # "kivi", "kitty", "int8", "int8t" (token-granular slot pool)
     head_dim: int = 128
     outlier_channels: int = 0    # per kv head, seeded
     outlier_gain: float = 1.0
@@ -74,6 +74,8 @@ WORKLOADS = {
                 131072, "kitty", channel_sigma=True),
     5: Workload(5, "INT8 dither B8 64q/8kv L~U[16384,65536]", 8, 64, 8, 65536,
                 "int8", min_seq_len=16384),
+    6: Workload(6, "INT8 token-granular slot pool B8 64q/8kv L~U[16384,65536]", 8, 64, 8, 65536,
+                "int8t", min_seq_len=16384),
 }
 
 
@@ -143,6 +145,13 @@ def request_ids(w: Workload) -> np.ndarray:
     hv = hash_np(key, np.arange(w.batch, dtype=np.uint64))
     ids = (hv & np.uint64(0x7FFFFF00)).astype(np.int64) + np.arange(w.batch)
     return ids.astype(np.int32)
+
+
+def page_permutation(w: Workload, n_pages: int) -> np.ndarray:
+    """Seeded permutation of a slot pool's pages: the order in which a long-running
+    allocator hands pages out, so a request's tokens land on scattered pages."""
+    hv = hash_np(stream_key(w.seed, T_SLOT, 0, 0), np.arange(n_pages, dtype=np.uint64))
+    return np.argsort(hv, kind="stable")
 
 
 def key_channel_gain(w: Workload) -> np.ndarray:

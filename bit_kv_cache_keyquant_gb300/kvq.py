@@ -15,9 +15,10 @@ from . import build as _build
 _LIB_PATH = _build.LIB
 
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_MISALIGNED, KVQ_ERR_CUDA, KVQ_ERR_WORKSPACE = range(6)
-KVQ_VARIANT_KIVI, KVQ_VARIANT_KITTY, KVQ_VARIANT_INT8 = 0, 1, 2
+KVQ_VARIANT_KIVI, KVQ_VARIANT_KITTY, KVQ_VARIANT_INT8, KVQ_VARIANT_INT8_TOKEN = 0, 1, 2, 3
 KVQ_DEVICE_ERR_WAIT_TIMEOUT = 1
 KVQ_DEVICE_ERR_CAPACITY = 2
+KVQ_DEVICE_ERR_POOL = 4
 
 
 class KvqError(RuntimeError):
@@ -30,7 +31,8 @@ class kvq_config(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("bits_k", ctypes.c_int32), ("bits_v", ctypes.c_int32), ("group_k", ctypes.c_int32),
                 ("group_v", ctypes.c_int32), ("residual", ctypes.c_int32), ("sink", ctypes.c_int32),
-                ("boost_k", ctypes.c_int32), ("int8_block", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
+                ("boost_k", ctypes.c_int32), ("int8_block", ctypes.c_int32), ("sm_scale", ctypes.c_float),
+                ("int8_group", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -45,6 +47,16 @@ class kvq_kitty_cache(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("seq_len", _P),
                 ("k_pages", _P), ("v_pages", _P), ("k_sink", _P), ("v_sink", _P), ("k_qbuf", _P),
                 ("v_qbuf", _P), ("v_local", _P)]
+
+
+class kvq_slot_pool(ctypes.Structure):
+    _fields_ = [("capacity", ctypes.c_int32), ("slots", _P), ("top", _P)]
+
+
+class kvq_int8_token_cache(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("seq_len", _P), ("slot_table", _P),
+                ("n_slots", ctypes.c_int32), ("layer", ctypes.c_int32), ("seed", ctypes.c_uint64),
+                ("k_codes", _P), ("v_codes", _P), ("k_scale", _P), ("v_scale", _P)]
 
 
 class kvq_int8_cache(ctypes.Structure):
@@ -67,6 +79,12 @@ def _load():
         "kv_append_kivi": (S, [cfgp, ctypes.POINTER(kvq_kivi_cache), _P, _P, _P]),
         "kv_append_int8": (S, [cfgp, ctypes.POINTER(kvq_int8_cache), _P, _P, _P]),
         "kv_append_kitty": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), _P, _P, i32, _P]),
+        "kv_quant_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), _P, i64, _P, i32, _P]),
+        "kv_slot_pool_init": (S, [ctypes.POINTER(kvq_slot_pool), _P]),
+        "kv_append_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), ctypes.POINTER(kvq_slot_pool), _P,
+                                     _P, _P]),
+        "kv_release_int8_token": (S, [ctypes.POINTER(kvq_int8_token_cache), i32, ctypes.POINTER(kvq_slot_pool), _P]),
+        "kv_decode_attn_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), _P, _P, _P, sz, _P]),
         "kv_quant_key_kitty": (S, [cfgp, _P, i64, i32, _P, _P]),
         "kv_quant_value_kitty": (S, [cfgp, _P, i64, _P, _P]),
         "kv_quant_int8_dither": (S, [cfgp, _P, i64, _P, _P, _P, i32, i32, ctypes.c_uint64, _P, _P, _P]),
@@ -93,10 +111,12 @@ def _load():
 
 _lib = _load()
 
-EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_append_int8", "kv_append_kitty", "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither",
+EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_append_int8", "kv_append_kitty",
+            "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither", "kv_quant_int8_token",
+            "kv_slot_pool_init", "kv_append_int8_token", "kv_release_int8_token",
             "kvq_kitty_key_page_bytes", "kvq_kitty_value_page_bytes", "kv_decode_attn_plan", "kv_decode_attn",
-            "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_noalloc", "kv_decode_attn_stage1",
-            "kv_decode_attn_merge",
+            "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_int8_token", "kv_decode_attn_noalloc",
+            "kv_decode_attn_stage1", "kv_decode_attn_merge",
             "kvq_philox4x32_10", "kvq_get_device_error", "kvq_status_string", "kvq_version")
 
 
@@ -138,9 +158,9 @@ def _check(status: int, what: str):
 
 
 def make_config(head_dim=128, n_q_heads=32, n_kv_heads=32, bits_k=2, bits_v=2, group_k=32, group_v=32,
-                residual=128, sink=32, boost_k=16, int8_block=256, sm_scale=0.0) -> kvq_config:
+                residual=128, sink=32, boost_k=16, int8_block=256, sm_scale=0.0, int8_group=32) -> kvq_config:
     return kvq_config(head_dim, n_q_heads, n_kv_heads, bits_k, bits_v, group_k, group_v, residual, sink, boost_k,
-                      int8_block, sm_scale)
+                      int8_block, sm_scale, int8_group)
 
 
 # ---------------------------------------------------------------------------
@@ -172,6 +192,27 @@ def kv_append_kitty(cfg, cache, k_new, v_new, score_mode=0, stream=None):
     """Append one token per (batch row, kv head) to a Kitty cache: k_new, v_new fp16 [B][Hkv][D]."""
     _check(_lib.kv_append_kitty(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new), score_mode,
                                 _stream(stream)), "kv_append_kitty")
+
+
+def kv_quant_int8_token(cfg, cache, x, n, slots, kv_sel, stream=None):
+    """Quantize n tokens x fp16 [n][Hkv][D] into pool slots slots int32 [n] (keys: kv_sel 0, values: 1)."""
+    _check(_lib.kv_quant_int8_token(ctypes.byref(cfg), ctypes.byref(cache), _ptr(x), n, _ptr(slots), kv_sel,
+                                    _stream(stream)), "kv_quant_int8_token")
+
+
+def kv_slot_pool_init(pool, stream=None):
+    _check(_lib.kv_slot_pool_init(ctypes.byref(pool), _stream(stream)), "kv_slot_pool_init")
+
+
+def kv_append_int8_token(cfg, cache, pool, k_new, v_new, stream=None):
+    """Append one token per request (fp16 [B][Hkv][D]) into slots taken from the pool."""
+    _check(_lib.kv_append_int8_token(ctypes.byref(cfg), ctypes.byref(cache), ctypes.byref(pool), _ptr(k_new),
+                                     _ptr(v_new), _stream(stream)), "kv_append_int8_token")
+
+
+def kv_release_int8_token(cache, row, pool, stream=None):
+    _check(_lib.kv_release_int8_token(ctypes.byref(cache), row, ctypes.byref(pool), _stream(stream)),
+           "kv_release_int8_token")
 
 
 def kv_quant_key_kitty(cfg, k, n_pages, score_mode, pages, stream=None):
@@ -219,6 +260,12 @@ def kv_decode_attn_kitty(cfg, cache, q, out, workspace, workspace_bytes, stream=
 def kv_decode_attn_int8(cfg, cache, q, out, workspace, workspace_bytes, stream=None):
     _check(_lib.kv_decode_attn_int8(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out), _ptr(workspace),
                                     workspace_bytes, _stream(stream)), "kv_decode_attn_int8")
+
+
+def kv_decode_attn_int8_token(cfg, cache, q, out, workspace, workspace_bytes, stream=None):
+    _check(_lib.kv_decode_attn_int8_token(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out),
+                                          _ptr(workspace), workspace_bytes, _stream(stream)),
+           "kv_decode_attn_int8_token")
 
 
 def kv_decode_attn_noalloc(cfg, cache, q, out, stream=None):

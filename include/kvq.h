@@ -11,7 +11,10 @@
  *     per-token value pages (Kitty summary, "The Channel-Wise Precision Boost
  *     Mechanism", "Page-Centric Memory Layout and Dense-Sparse Decomposition");
  *   - WitCert INT8 with subtractive Philox4x32-10 dither and per-256-token,
- *     per-channel fp16 scales amax/126.5 (WitCert, arxiv 2607.28699, sec. 6).
+ *     per-channel fp16 scales amax/126.5 (WitCert, arxiv 2607.28699, sec. 6),
+ *     and its token-granular form for a slot-paged pool: one fp16 scale per
+ *     token and group of Gc channels, dither keyed by the slot (WitCert, the
+ *     SGLang storage subsection of sec. 6.2).
  * Read side: split-KV flash-decoding attention that dequantizes codes in
  * registers, concatenates the fp16 residual / sink / buffer segments, and
  * merges the splits by log-sum-exp (WitCert sec. 6.2.2 two-stage structure;
@@ -52,6 +55,8 @@
  *   Kitty value page: codes [G][D/4] token-major as above, s fp16 [G],
  *     z fp16 [G].
  *   INT8 cache: codes int8 [tokens][D]; scale fp16 [blocks][D].
+ *   Token-granular INT8 slot pool: codes int8 [n_slots][Hkv][D]; scale fp16
+ *     [n_slots][Hkv][D/Gc] (136 bytes per token, kv head and side at Gc = 32).
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -81,9 +86,15 @@ typedef enum {
 
 /* device error flags (bitmask) written by kernels instead of trapping */
 #define KVQ_DEVICE_ERR_WAIT_TIMEOUT 1u
-#define KVQ_DEVICE_ERR_CAPACITY 2u      /* kv_append_kivi on a row already at max_seq_len: nothing written */
+#define KVQ_DEVICE_ERR_CAPACITY 2u      /* kv_append_* on a row already at max_seq_len: nothing written */
+#define KVQ_DEVICE_ERR_POOL 4u          /* slot pool exhausted (or overfilled by a release): nothing written */
 
-typedef enum { KVQ_VARIANT_KIVI = 0, KVQ_VARIANT_KITTY = 1, KVQ_VARIANT_INT8 = 2 } kvq_variant;
+typedef enum {
+    KVQ_VARIANT_KIVI = 0,
+    KVQ_VARIANT_KITTY = 1,
+    KVQ_VARIANT_INT8 = 2,
+    KVQ_VARIANT_INT8_TOKEN = 3
+} kvq_variant;
 
 typedef struct {
     int32_t head_dim;     /* D; 128 */
@@ -98,6 +109,7 @@ typedef struct {
     int32_t boost_k;      /* K: Kitty boosted key channels, 0..head_dim */
     int32_t int8_block;   /* INT8 dither block length in tokens: 256 */
     float sm_scale;       /* softmax scale; 0 means 1/sqrt(head_dim) */
+    int32_t int8_group;   /* Gc: channels per token-granular INT8 scale (32, 64 or 128) */
 } kvq_config;
 
 /* --------------------------------------------------------------------- */
@@ -278,6 +290,76 @@ typedef struct {
 KVQ_API kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new,
                                   const void *v_new, cudaStream_t stream);
 
+/* --------------------------------------------------------------------- */
+/* Token-granular INT8 over a slot pool                                     */
+/* --------------------------------------------------------------------- */
+/* The form WitCert gives for an engine whose KV pool is paged at token-slot
+ * granularity (the SGLang storage subsection of sec. 6.2): a token's slot is
+ * any free slot of the pool, a request's tokens need not be contiguous, and
+ * a token is quantized when it is written, with
+ *   s = fp16_RN(amax / 126.5) per token and group of Gc channels,
+ *   code = clamp(rint(x/s + xi), -127, 127) with the stored s (0 if s == 0),
+ *   x^ = s (code - xi),
+ * and xi = (w >> 8) 2^-24 - 1/2 from Philox4x32-10 keyed by (layer, kv head,
+ * slot, channel): counter (slot, channel/4, layer << 17 | kv_sel << 16 |
+ * kv_head, 0), key (seed low, seed high), word channel % 4; kv_sel 0 = K,
+ * 1 = V.  The dither follows the slot, so moving a request never changes
+ * what a written slot decodes to. */
+
+/* Free-slot pool: a stack of free slot ids.  slots int32 [capacity] and top
+ * int32 [1] are device memory owned by the caller; the slots below *top are
+ * free. */
+typedef struct {
+    int32_t capacity;
+    int32_t *slots;
+    int32_t *top;
+} kvq_slot_pool;
+
+typedef struct {
+    int32_t batch;
+    int32_t max_seq_len;      /* row stride of slot_table */
+    const int32_t *seq_len;   /* [B] tokens per request (0 allowed) */
+    const int32_t *slot_table; /* int32 [B][max_seq_len]: slot of token t of request b */
+    int32_t n_slots;
+    int32_t layer;            /* 0 .. 2^15 - 1 */
+    uint64_t seed;
+    const void *k_codes;      /* int8 [n_slots][Hkv][D] */
+    const void *v_codes;      /* int8 [n_slots][Hkv][D] */
+    const void *k_scale;      /* fp16 [n_slots][Hkv][D/Gc] */
+    const void *v_scale;      /* fp16 [n_slots][Hkv][D/Gc] */
+} kvq_int8_token_cache;
+
+/* Quantize n tokens (all kv heads) into their slots.
+ *   x      fp16 [n][Hkv][D]
+ *   slots  int32 [n] device array of distinct slots in [0, n_slots)
+ *   kv_sel 0 for keys (writes k_codes / k_scale of c), 1 for values
+ * Slots outside [0, n_slots) are skipped. */
+KVQ_API kvq_status kv_quant_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *x,
+                                       int64_t n, const int32_t *slots, int32_t kv_sel, cudaStream_t stream);
+
+/* Fill the pool with every slot 0 .. capacity-1 (pops then return 0, 1, 2, ...). */
+KVQ_API kvq_status kv_slot_pool_init(const kvq_slot_pool *pool, cudaStream_t stream);
+
+/* Streaming append of one token per request: k_new, v_new fp16 [B][Hkv][D].
+ * Every row b with seq_len[b] < max_seq_len takes one slot from the pool
+ * (rows in order of b take the slots from the top of the stack down, so the
+ * assignment is deterministic and a replayed graph writes the same slots),
+ * records it in slot_table[b][seq_len[b]], quantizes the token into it and
+ * sets seq_len[b] += 1.  Rows already at max_seq_len record
+ * KVQ_DEVICE_ERR_CAPACITY and are left unchanged; if the pool holds fewer
+ * free slots than rows that need one, KVQ_DEVICE_ERR_POOL is recorded and
+ * no row is changed.  Two kernels on `stream`, graph-capturable. */
+KVQ_API kvq_status kv_append_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c,
+                                        const kvq_slot_pool *pool, const void *k_new, const void *v_new,
+                                        cudaStream_t stream);
+
+/* Return the slots of request `row` (slot_table[row][0 .. seq_len[row])) to
+ * the pool and set seq_len[row] = 0.  A release that would overfill the pool
+ * records KVQ_DEVICE_ERR_POOL and changes nothing.  Slots shared between
+ * requests are not reference-counted: release each slot once. */
+KVQ_API kvq_status kv_release_int8_token(const kvq_int8_token_cache *c, int32_t row, const kvq_slot_pool *pool,
+                                         cudaStream_t stream);
+
 /* Split-KV plan: number of splits per (batch row, query head) and the
  * workspace bytes the decode calls need for this config, variant, batch and
  * max_seq_len.  Deterministic: the decode calls recompute the same plan. */
@@ -295,6 +377,12 @@ KVQ_API kvq_status kv_decode_attn_kitty(const kvq_config *cfg, const kvq_kitty_c
                                 void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 KVQ_API kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_cache *cache, const void *q,
                                void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+/* Token-granular INT8: every token t < seq_len[b] is read from slot
+ * slot_table[b][t] and dequantized with its slot's dither; a row with
+ * seq_len[b] == 0 gets out = 0. */
+KVQ_API kvq_status kv_decode_attn_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *cache,
+                                             const void *q, void *out, void *workspace, size_t workspace_bytes,
+                                             cudaStream_t stream);
 
 /* Allocation-free kv_decode_attn (no counterpart on the pages: an addition
  * for callers that cannot provide a workspace, such as engines whose own

@@ -95,6 +95,38 @@ def test_validation_without_gpu(K):
                       None) == K.KVQ_ERR_UNSUPPORTED
 
 
+def test_int8_token_validation_without_gpu(K):
+    cfg = K.make_config(n_q_heads=64, n_kv_heads=8)
+    c = K.kvq_int8_token_cache(4, 1024, 16, 16, 4096, 3, 7, 16, 16, 16, 16)
+    pool = K.kvq_slot_pool(4096, 16, 16)
+    call = K.raw_call
+    assert call("kv_quant_int8_token", ctypes.byref(cfg), ctypes.byref(c), 16, 5, 16, 2, None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_quant_int8_token", ctypes.byref(cfg), ctypes.byref(c), 16, -1, 16, 0, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert call("kv_quant_int8_token", ctypes.byref(cfg), ctypes.byref(c), 0x1008, 5, 16, 0, None) == \
+        K.KVQ_ERR_MISALIGNED
+    assert call("kv_quant_int8_token", ctypes.byref(cfg), ctypes.byref(c), 16, 0, None, 0, None) == K.KVQ_OK
+    assert call("kv_quant_int8_token", ctypes.byref(K.make_config(int8_group=48)), ctypes.byref(c), 16, 5, 16, 0,
+                None) == K.KVQ_ERR_UNSUPPORTED
+    assert call("kv_quant_int8_token", ctypes.byref(K.make_config(int8_group=0)), ctypes.byref(c), 16, 5, 16, 0,
+                None) == K.KVQ_ERR_INVALID_ARG
+    bad_layer = K.kvq_int8_token_cache(4, 1024, 16, 16, 4096, 1 << 15, 7, 16, 16, 16, 16)
+    assert call("kv_append_int8_token", ctypes.byref(cfg), ctypes.byref(bad_layer), ctypes.byref(pool), 16, 16,
+                None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_append_int8_token", ctypes.byref(cfg), ctypes.byref(c), ctypes.byref(K.kvq_slot_pool(0, 16, 16)),
+                16, 16, None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_append_int8_token", ctypes.byref(cfg), ctypes.byref(c), None, 16, 16, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert call("kv_release_int8_token", ctypes.byref(c), 4, ctypes.byref(pool), None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_slot_pool_init", ctypes.byref(K.kvq_slot_pool(8, 16, 0x1004)), None) == K.KVQ_ERR_MISALIGNED
+    wide = K.make_config(n_q_heads=72, n_kv_heads=8)                 # 9 query heads per kv head
+    assert call("kv_decode_attn_int8_token", ctypes.byref(wide), ctypes.byref(c), 16, 16, 16, 1 << 30, None) == \
+        K.KVQ_ERR_UNSUPPORTED
+    n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_INT8_TOKEN, 4, 1024)
+    assert call("kv_decode_attn_int8_token", ctypes.byref(cfg), ctypes.byref(c), 16, 16, 16, wsb - 1, None) == \
+        K.KVQ_ERR_WORKSPACE
+
+
 def test_decode_plan_and_workspace_checks(K):
     cfg = K.make_config()
     n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, 32, 4096)
