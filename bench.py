@@ -51,6 +51,10 @@ def _workload_desc(w):
     if w.variant == "kitty":
         return base + (f"{w.seq_len} cached tokens, Kitty pages G=128, 16 of 128 key channels boosted to 4 bit "
                        f"(two 2-bit planes), value 2 bit, sink 32, local 128")
+    if w.variant == "int8t":
+        return base + (f"lengths U[{w.min_seq_len}, {w.seq_len}], token-granular INT8 slot pool (scattered 16-slot "
+                       f"pages), fp16 scale per token and 32 channels, Philox4x32-10 dither keyed by slot, "
+                       f"one token appended per request per step")
     return base + (f"lengths U[{w.min_seq_len}, {w.seq_len}], INT8 K and V with Philox4x32-10 subtractive dither, "
                    f"fp16 scale per 256-token block and channel, fp16 active block")
 
@@ -163,7 +167,7 @@ def run_reference(args, w):
 # ---------------------------------------------------------------------------
 # GPU leg
 # ---------------------------------------------------------------------------
-def build_state(w, device):
+def build_state(w, device, appends: int = 1024):
     """Device-resident cache of the workload plus the per-step write-side inputs."""
     import torch
     from bit_kv_cache_keyquant_gb300 import cache as C
@@ -179,12 +183,24 @@ def build_state(w, device):
                               boost_k=16)
         cache = C.KittyCache(cfg, w.batch, Lmax, device=device)
         variant = kvq.KVQ_VARIANT_KITTY
+    elif w.variant == "int8t":
+        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, int8_group=32)
+        margin = (appends + 15) // 16 * 16                                  # tokens appended per request, at most
+        n_slots = (int(lens.sum()) + w.batch * margin + 15) // 16 * 16
+        cache = C.Int8TokenCache(cfg, w.batch, Lmax + margin, n_slots, layer=5, seed=w.seed, device=device)
+        cache.shuffle_free(I.page_permutation(w, n_slots // 16), 16)
+        variant = kvq.KVQ_VARIANT_INT8_TOKEN
     else:
         cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
         cache = C.Int8Cache(cfg, w.batch, Lmax, layer=5, seed=w.seed, device=device)
         variant = kvq.KVQ_VARIANT_INT8
     reqs = I.request_ids(w)
     for b in range(w.batch):
+        if w.variant == "int8t":
+            L = int(lens[b])
+            cache.fill(b, torch.stack([I.gen_kv_torch(w, I.T_K, b, h, L, device) for h in range(w.n_kv_heads)], 1),
+                       torch.stack([I.gen_kv_torch(w, I.T_V, b, h, L, device) for h in range(w.n_kv_heads)], 1))
+            continue
         L = int(lens[b])
         for h in range(w.n_kv_heads):
             K = I.gen_kv_torch(w, I.T_K, b, h, L, device)
@@ -214,6 +230,11 @@ def build_state(w, device):
                   scratch=[torch.empty((n_pg, kvq.kvq_kitty_key_page_bytes(cfg)), dtype=torch.uint8, device=device),
                            torch.empty((n_pg, kvq.kvq_kitty_value_page_bytes(cfg)), dtype=torch.uint8,
                                        device=device)])
+    elif w.variant == "int8t":
+        # one new token per request, appended (slot from the pool, quantized) before the attention reads it
+        st.update(pool=cache.pool(),
+                  knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, pairs, 128, device).view(w.batch, w.n_kv_heads, 128),
+                  vnew=I.gen_slice_torch(w.seed, I.T_V, 9999, 0, pairs, 128, device).view(w.batch, w.n_kv_heads, 128))
     else:
         n_blk = max(1, (pairs + 255) // 256)                                # 1/T of the block flushes, rounded up
         st.update(n_blk=n_blk, knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_blk * 256, 128, device),
@@ -231,7 +252,7 @@ def build_state(w, device):
 def quant_step(st, stream, vnew=None, knew=None):
     """The step's write-side kernels (amortized quantization of the new tokens)."""
     from bit_kv_cache_keyquant_gb300 import kvq
-    w, cfg, sc = st["w"], st["cfg"], st["scratch"]
+    w, cfg, sc = st["w"], st["cfg"], st.get("scratch")
     vnew = st["vnew"] if vnew is None else vnew
     knew = st["knew"] if knew is None else knew
     if w.variant == "kivi":
@@ -240,6 +261,8 @@ def quant_step(st, stream, vnew=None, knew=None):
     elif w.variant == "kitty":
         kvq.kv_quant_key_kitty(cfg, knew, st["n_pg"], 0, sc[0], stream)
         kvq.kv_quant_value_kitty(cfg, vnew, st["n_pg"], sc[1], stream)
+    elif w.variant == "int8t":
+        kvq.kv_append_int8_token(cfg, st["desc"], st["pool"], knew, vnew, stream)
     else:
         m = st["blk_meta"]
         for sel, x in ((0, knew), (1, vnew)):
@@ -253,6 +276,8 @@ def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None):
     cache slots that this step's attention does not read."""
     from bit_kv_cache_keyquant_gb300 import kvq
     cfg, side = st["cfg"], st["side"]
+    if st["w"].variant == "int8t":
+        side = stream                  # the token is quantized on insert: the attention reads it
     st["fork"].record(stream)
     side.wait_event(st["fork"])
     if ev is not None:
@@ -275,7 +300,7 @@ def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None):
 
 
 def launches_per_step(w) -> int:
-    return {"kivi": 4, "kitty": 4, "int8": 4}[w.variant]
+    return {"kivi": 4, "kitty": 4, "int8": 4, "int8t": 4}[w.variant]
 
 
 def run_gpu(args, w, rank, world, local_rank):
@@ -285,7 +310,7 @@ def run_gpu(args, w, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    st = build_state(w, dev)
+    st = build_state(w, dev, appends=2 * (args.warmup + args.steps) + 16)
     stream = torch.cuda.current_stream(dev)
     st["side"] = torch.cuda.Stream(device=dev)
     st["fork"], st["join"] = torch.cuda.Event(), torch.cuda.Event()
@@ -349,6 +374,8 @@ def run_gpu(args, w, rank, world, local_rank):
     if rank != 0:
         return
     lens = st["lens"]
+    if w.variant == "int8t":       # one token appended per request before every timed attention
+        lens = lens + args.warmup + (args.steps + 1) // 2
     cache_bytes = st["cache"].nbytes_read(lens)
     q_bytes = w.batch * w.n_q_heads * 128 * 2
     alg_bytes_stage1 = cache_bytes + q_bytes
@@ -378,7 +405,8 @@ def run_gpu(args, w, rank, world, local_rank):
                    "kv_heads": w.n_kv_heads, "head_dim": 128, "seq_len": w.seq_len, "parallelism": f"replicas x{world}",
                    "splits": st["n_splits"],
                    "l2": f"inputs larger than L2 ({cache_bytes / 1e6:.0f} MB read per step vs 129 MB L2)"},
-        "breakdown_us": {"quant_writes_side_stream_span": 1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
+        "breakdown_us": {("append_before_attention" if w.variant == "int8t" else "quant_writes_side_stream_span"):
+                         1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
                          "merge": 1e3 * statistics.mean(merge_ms)},
         "hbm_gbs_step": (alg_bytes_stage1 + d2h) / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -404,9 +432,12 @@ def stage1_kernel(w):
         return "kitty_decode_gqa_kernel", ("kvq_decode_kitty_gqa.cu", "kvq_kitty.cuh", "kvq_mma.cuh", "kvq_device.cuh")
     if w.variant == "kitty":
         return "kitty_decode_kernel", ("kvq_decode_kitty.cu", "kvq_kitty.cuh", "kvq_device.cuh")
+    if w.variant == "int8t":
+        return "int8_token_decode_kernel", ("kvq_decode_int8.cu", "kvq_device.cuh")
     return f"{w.variant}_decode_kernel", (f"kvq_decode_{w.variant}.cu", "kvq_device.cuh")
 DTYPE = {"kivi": "u2 codes + fp16 scales, fp32 accumulate", "kitty": "u2 planes + fp16 scales, fp32 accumulate",
-         "int8": "s8 codes + Philox dither + fp16 scales, fp32 accumulate"}
+         "int8": "s8 codes + Philox dither + fp16 scales, fp32 accumulate",
+         "int8t": "s8 codes + Philox dither + fp16 token scales, fp32 accumulate"}
 
 
 def kernel_source_hash(files) -> str:
@@ -423,7 +454,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5],
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6],
                     help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
