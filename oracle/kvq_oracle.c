@@ -228,19 +228,44 @@ ORC_API int orc_kivi_key_bit(int t)
     return 2 * ((t % 32) / 8);
 }
 
-ORC_API int orc_kivi_key_pack(int D, int G, const uint8_t *codes, long n_grp, uint8_t *packed)
+/* The same layout for b-bit codes (b = 2 or 4; KIVI-4 of the KIVI summary's
+ * section 4): a byte holds 8/b codes, so a 32-token tile takes 1024 * b/2
+ * bytes, made of b/2 planes of 1024 bytes.  Token t = q + 8p goes to plane
+ * p / (8/b), at bits b * (p % (8/b)) of the byte that the 2-bit layout gives
+ * inside the plane.  For b = 2 this is the layout above. */
+ORC_API long orc_kivi_key_byte_offset_w(int bits, int t, int c)
 {
-    if (D != 128 || G % 32 != 0)
+    long cpb = 8 / bits;
+    long p = (t % 32) / 8;
+    return (t / 32) * (1024L * bits / 2) + (p / cpb) * 1024 + orc_kivi_key_byte_offset(t % 8, c);
+}
+
+ORC_API int orc_kivi_key_bit_w(int bits, int t)
+{
+    int cpb = 8 / bits;
+    return bits * (((t % 32) / 8) % cpb);
+}
+
+ORC_API int orc_kivi_key_pack_w(int D, int G, int bits, const uint8_t *codes, long n_grp, uint8_t *packed)
+{
+    if (D != 128 || G % 32 != 0 || (bits != 2 && bits != 4))
         return 1;
-    long gbytes = (long)G * D / 4;
+    long gbytes = (long)G * D * bits / 8;
+    int mask = (1 << bits) - 1;
     memset(packed, 0, (size_t)(gbytes * n_grp));
     for (long g = 0; g < n_grp; ++g)
         for (int t = 0; t < G; ++t)
             for (int c = 0; c < D; ++c) {
-                int code = codes[(g * G + t) * (long)D + c] & 3;
-                packed[g * gbytes + orc_kivi_key_byte_offset(t, c)] |= (uint8_t)(code << orc_kivi_key_bit(t));
+                int code = codes[(g * G + t) * (long)D + c] & mask;
+                packed[g * gbytes + orc_kivi_key_byte_offset_w(bits, t, c)] |=
+                    (uint8_t)(code << orc_kivi_key_bit_w(bits, t));
             }
     return 0;
+}
+
+ORC_API int orc_kivi_key_pack(int D, int G, const uint8_t *codes, long n_grp, uint8_t *packed)
+{
+    return orc_kivi_key_pack_w(D, G, 2, codes, n_grp, packed);
 }
 
 /* Storage index of channel c's scale (and, 128 entries later, its zero) in
@@ -269,9 +294,9 @@ ORC_API int orc_kivi_key_sz_pack(int D, const uint16_t *sz, long n_grp, uint16_t
     return 0;
 }
 
-static int kivi_key_code_at(const uint8_t *group_bytes, int t, int c)
+static int kivi_key_code_at(int bits, const uint8_t *group_bytes, int t, int c)
 {
-    return (group_bytes[orc_kivi_key_byte_offset(t, c)] >> orc_kivi_key_bit(t)) & 3;
+    return (group_bytes[orc_kivi_key_byte_offset_w(bits, t, c)] >> orc_kivi_key_bit_w(bits, t)) & ((1 << bits) - 1);
 }
 
 /* ------------------------------------------------------------------ */
@@ -295,18 +320,27 @@ ORC_API void orc_kivi_value_codes(int D, int Gv, int bits, const uint16_t *x, lo
         }
 }
 
-/* Token-major 2-bit packing: byte c/4 of the token's D/4 bytes, bits 2*(c%4). */
-ORC_API void orc_tokenmajor_pack(int D, const uint8_t *codes, long n_tok, uint8_t *packed)
+/* Token-major b-bit packing (b = 2 or 4): byte c/(8/b) of the token's D*b/8
+ * bytes, bits b*(c % (8/b)). */
+ORC_API void orc_tokenmajor_pack_w(int D, int bits, const uint8_t *codes, long n_tok, uint8_t *packed)
 {
-    memset(packed, 0, (size_t)(n_tok * D / 4));
+    int cpb = 8 / bits, mask = (1 << bits) - 1;
+    long tb = (long)D * bits / 8;
+    memset(packed, 0, (size_t)(n_tok * tb));
     for (long t = 0; t < n_tok; ++t)
         for (int c = 0; c < D; ++c)
-            packed[t * (D / 4) + c / 4] |= (uint8_t)((codes[t * D + c] & 3) << (2 * (c % 4)));
+            packed[t * tb + c / cpb] |= (uint8_t)((codes[t * D + c] & mask) << (bits * (c % cpb)));
 }
 
-static int tokenmajor_code_at(const uint8_t *tok_bytes, int c)
+ORC_API void orc_tokenmajor_pack(int D, const uint8_t *codes, long n_tok, uint8_t *packed)
 {
-    return (tok_bytes[c / 4] >> (2 * (c % 4))) & 3;
+    orc_tokenmajor_pack_w(D, 2, codes, n_tok, packed);
+}
+
+static int tokenmajor_code_at(int bits, const uint8_t *tok_bytes, int c)
+{
+    int cpb = 8 / bits;
+    return (tok_bytes[c / cpb] >> (bits * (c % cpb))) & ((1 << bits) - 1);
 }
 
 /* ------------------------------------------------------------------ */
@@ -615,15 +649,15 @@ ORC_API void orc_attend_fp16(int D, int n, const uint16_t *q, const uint16_t *k,
  *   keys are quantized in groups of G; value residual holds min(L, R)
  *   tokens, the first L - min(L, R) values are quantized per token.
  *   Residual token t lives at slot t % R.
- * Arrays (this (b, kvh) only):
- *   kc   packed key groups, G*D/4 bytes each     ksz fp16 [grp][D][2]
- *   vc   packed value tokens, D/4 bytes each     vsz fp16 [tok][D/Gv][2]
+ * Arrays (this (b, kvh) only), b_K / b_V-bit codes:
+ *   kc   packed key groups, G*D*b_K/8 bytes each   ksz fp16 [grp][D][2]
+ *   vc   packed value tokens, D*b_V/8 bytes each   vsz fp16 [tok][D/Gv][2]
  *   kres, vres fp16 [R][D]
  * out: binary64 [g][D] for the g query heads q fp16 [g][D]. */
-ORC_API void orc_kivi_decode_one(int D, int G, int Gv, int R, int L, int n_heads, double sm_scale,
-                                 const uint16_t *q, const uint8_t *kc, const uint16_t *ksz,
-                                 const uint8_t *vc, const uint16_t *vsz,
-                                 const uint16_t *kres, const uint16_t *vres, double *out)
+ORC_API void orc_kivi_decode_one_w(int D, int G, int Gv, int R, int L, int bits_k, int bits_v, int n_heads,
+                                   double sm_scale, const uint16_t *q, const uint8_t *kc, const uint16_t *ksz,
+                                   const uint8_t *vc, const uint16_t *vsz,
+                                   const uint16_t *kres, const uint16_t *vres, double *out)
 {
     int rK = ((L - 1) % R) + 1;
     int nKq = L - rK;
@@ -636,14 +670,14 @@ ORC_API void orc_kivi_decode_one(int D, int G, int Gv, int R, int L, int n_heads
         for (int c = 0; c < D; ++c) {
             if (t < nKq) {
                 long g = t / G;
-                const uint8_t *gb = kc + g * ((long)G * D / 4);
-                int code = kivi_key_code_at(gb, t % G, c);
+                const uint8_t *gb = kc + g * ((long)G * D * bits_k / 8);
+                int code = kivi_key_code_at(bits_k, gb, t % G, c);
                 k[(long)t * D + c] = orc_affine_dequant(code, ksz[(g * D + c) * 2], ksz[(g * D + c) * 2 + 1]);
             } else {
                 k[(long)t * D + c] = orc_half_to_double(kres[(long)(t % R) * D + c]);
             }
             if (t < nVq) {
-                int code = tokenmajor_code_at(vc + (long)t * (D / 4), c);
+                int code = tokenmajor_code_at(bits_v, vc + (long)t * ((long)D * bits_v / 8), c);
                 long j = (long)t * ngv + c / Gv;
                 v[(long)t * D + c] = orc_affine_dequant(code, vsz[j * 2], vsz[j * 2 + 1]);
             } else {
@@ -657,6 +691,14 @@ ORC_API void orc_kivi_decode_one(int D, int G, int Gv, int R, int L, int n_heads
         attend_f64(D, L, qd, k, v, sm_scale, out + (long)h * D);
     }
     free(qd); free(k); free(v);
+}
+
+ORC_API void orc_kivi_decode_one(int D, int G, int Gv, int R, int L, int n_heads, double sm_scale,
+                                 const uint16_t *q, const uint8_t *kc, const uint16_t *ksz,
+                                 const uint8_t *vc, const uint16_t *vsz,
+                                 const uint16_t *kres, const uint16_t *vres, double *out)
+{
+    orc_kivi_decode_one_w(D, G, Gv, R, L, 2, 2, n_heads, sm_scale, q, kc, ksz, vc, vsz, kres, vres, out);
 }
 
 /* Kitty cache of one (batch row, kv head) with L tokens, sink S, page G,
@@ -710,7 +752,7 @@ ORC_API void orc_kitty_decode_one(int D, int G, int K, int S, int R, int L, int 
                 int p = (t - S) / G, tt = (t - S) % G;
                 const uint8_t *pg = vp + p * vpb;
                 const uint16_t *ps = (const uint16_t *)(pg + (long)G * D / 4);
-                int code = tokenmajor_code_at(pg + (long)tt * (D / 4), c);
+                int code = tokenmajor_code_at(2, pg + (long)tt * (D / 4), c);
                 val = orc_affine_dequant(code, ps[tt], ps[G + tt]);
             } else if (t < S + PV * G + nvb) {
                 val = orc_half_to_double(vqbuf[(long)((t - S) % G) * D + c]);

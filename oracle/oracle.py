@@ -63,6 +63,11 @@ def _declare(l):
         "orc_kivi_key_byte_offset": (L, [I, I]),
         "orc_kivi_key_bit": (I, [I]),
         "orc_kivi_key_pack": (I, [I, I, P, L, P]),
+        "orc_kivi_key_byte_offset_w": (L, [I, I, I]),
+        "orc_kivi_key_bit_w": (I, [I, I]),
+        "orc_kivi_key_pack_w": (I, [I, I, I, P, L, P]),
+        "orc_tokenmajor_pack_w": (None, [I, I, P, L, P]),
+        "orc_kivi_decode_one_w": (None, [I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P]),
         "orc_kivi_key_sz_index": (I, [I]),
         "orc_kivi_key_sz_pack": (I, [I, P, L, P]),
         "orc_kivi_value_codes": (None, [I, I, I, P, L, P, P]),
@@ -141,21 +146,21 @@ def kivi_key_codes(x: np.ndarray, bits: int = 2):
     return codes, sz
 
 
-def kivi_key_pack(codes: np.ndarray) -> np.ndarray:
+def kivi_key_pack(codes: np.ndarray, bits: int = 2) -> np.ndarray:
     n, G, Dm = codes.shape
-    out = np.zeros((n, G * Dm // 4), np.uint8)
-    rc = lib().orc_kivi_key_pack(Dm, G, _p(np.ascontiguousarray(codes)), n, _p(out))
+    out = np.zeros((n, G * Dm * bits // 8), np.uint8)
+    rc = lib().orc_kivi_key_pack_w(Dm, G, bits, _p(np.ascontiguousarray(codes)), n, _p(out))
     if rc:
-        raise ValueError("KIVI key packing needs D == 128 and G % 32 == 0")
+        raise ValueError("KIVI key packing needs D == 128, G % 32 == 0 and 2 or 4 bits")
     return out
 
 
-def kivi_key_byte_offset(t: int, c: int) -> int:
-    return lib().orc_kivi_key_byte_offset(t, c)
+def kivi_key_byte_offset(t: int, c: int, bits: int = 2) -> int:
+    return lib().orc_kivi_key_byte_offset_w(bits, t, c)
 
 
-def kivi_key_bit(t: int) -> int:
-    return lib().orc_kivi_key_bit(t)
+def kivi_key_bit(t: int, bits: int = 2) -> int:
+    return lib().orc_kivi_key_bit_w(bits, t)
 
 
 def kivi_key_sz_index(c: int) -> int:
@@ -174,7 +179,7 @@ def kivi_key_sz_pack(sz: np.ndarray) -> np.ndarray:
 def kivi_quant_key(x: np.ndarray, bits: int = 2):
     """Full a1 step: fp16 [n_grp][G][D] -> (packed codes, sz)."""
     codes, sz = kivi_key_codes(x, bits)
-    return kivi_key_pack(codes), sz
+    return kivi_key_pack(codes, bits), sz
 
 
 def kivi_value_codes(x: np.ndarray, group: int = 32, bits: int = 2):
@@ -186,16 +191,16 @@ def kivi_value_codes(x: np.ndarray, group: int = 32, bits: int = 2):
     return codes, sz
 
 
-def tokenmajor_pack(codes: np.ndarray) -> np.ndarray:
+def tokenmajor_pack(codes: np.ndarray, bits: int = 2) -> np.ndarray:
     n, Dm = codes.shape
-    out = np.zeros((n, Dm // 4), np.uint8)
-    lib().orc_tokenmajor_pack(Dm, _p(np.ascontiguousarray(codes)), n, _p(out))
+    out = np.zeros((n, Dm * bits // 8), np.uint8)
+    lib().orc_tokenmajor_pack_w(Dm, bits, _p(np.ascontiguousarray(codes)), n, _p(out))
     return out
 
 
 def kivi_quant_value(x: np.ndarray, group: int = 32, bits: int = 2):
     codes, sz = kivi_value_codes(x, group, bits)
-    return tokenmajor_pack(codes), sz
+    return tokenmajor_pack(codes, bits), sz
 
 
 # ---------------------------------------------------------------------------
@@ -318,14 +323,14 @@ def attend_fp16(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: float) ->
     return out
 
 
-def kivi_decode_one(q, kc, ksz, vc, vsz, kres, vres, L, G=32, Gv=32, R=128, sm_scale=None):
+def kivi_decode_one(q, kc, ksz, vc, vsz, kres, vres, L, G=32, Gv=32, R=128, sm_scale=None, bits_k=2, bits_v=2):
     """One (batch row, kv head): q fp16 [g][D] -> binary64 [g][D]."""
     g, Dm = q.shape
     sm = (1.0 / np.sqrt(Dm)) if sm_scale is None else sm_scale
     out = np.zeros((g, Dm), np.float64)
-    lib().orc_kivi_decode_one(Dm, G, Gv, R, L, g, sm, _p(_h16(q)), _p(np.ascontiguousarray(kc)),
-                              _p(_h16(ksz)), _p(np.ascontiguousarray(vc)), _p(_h16(vsz)),
-                              _p(_h16(kres)), _p(_h16(vres)), _p(out))
+    lib().orc_kivi_decode_one_w(Dm, G, Gv, R, L, bits_k, bits_v, g, sm, _p(_h16(q)), _p(np.ascontiguousarray(kc)),
+                                _p(_h16(ksz)), _p(np.ascontiguousarray(vc)), _p(_h16(vsz)),
+                                _p(_h16(kres)), _p(_h16(vres)), _p(out))
     return out
 
 
@@ -364,20 +369,21 @@ def kivi_segments(L: int, R: int = 128):
     return L - rk, L - rv
 
 
-def kivi_build_one(K: np.ndarray, V: np.ndarray, G: int = 32, Gv: int = 32, R: int = 128):
+def kivi_build_one(K: np.ndarray, V: np.ndarray, G: int = 32, Gv: int = 32, R: int = 128, bits_k: int = 2,
+                   bits_v: int = 2):
     """fp16 K, V [L][D] -> (kc, ksz, vc, vsz, kres, vres) for one (b, kvh)."""
     L, Dm = K.shape
     nkq, nvq = kivi_segments(L, R)
     ng = nkq // G
     if ng:
-        kc, ksz = kivi_quant_key(K[:ng * G].reshape(ng, G, Dm))
+        kc, ksz = kivi_quant_key(K[:ng * G].reshape(ng, G, Dm), bits_k)
     else:
-        kc = np.zeros((0, G * Dm // 4), np.uint8)
+        kc = np.zeros((0, G * Dm * bits_k // 8), np.uint8)
         ksz = np.zeros((0, Dm, 2), np.uint16)
     if nvq:
-        vc, vsz = kivi_quant_value(V[:nvq], Gv)
+        vc, vsz = kivi_quant_value(V[:nvq], Gv, bits_v)
     else:
-        vc = np.zeros((0, Dm // 4), np.uint8)
+        vc = np.zeros((0, Dm * bits_v // 8), np.uint8)
         vsz = np.zeros((0, Dm // Gv, 2), np.uint16)
     kres = np.zeros((R, Dm), np.float16)
     vres = np.zeros((R, Dm), np.float16)

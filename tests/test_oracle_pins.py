@@ -172,6 +172,69 @@ def test_kivi_key_layout_is_a_lane_friendly_bijection(orc):
         assert idx[c] == ((k // 2) * 4 + r) * 8 + (k % 2) * 4 + byte
 
 
+def test_kivi_key_layout_4bit_is_a_lane_friendly_bijection(orc):
+    """4-bit keys: a 32-token tile is two 1024-byte planes; plane p // 2 holds the tokens q + 8p of the
+    2-bit byte at bits 4 (p % 2), so a lane still finds its tokens x channels in the same chunks."""
+    seen = {}
+    for t in range(64):
+        for c in range(128):
+            off, bit = orc.kivi_key_byte_offset(t, c, 4), orc.kivi_key_bit(t, 4)
+            seen.setdefault((off, bit), set()).add((t, c))
+            p = (t % 32) // 8
+            assert off // 2048 == t // 32 and (off % 2048) // 1024 == p // 2
+            assert off % 1024 == orc.kivi_key_byte_offset(t % 8, c) and bit == 4 * (p % 2)
+    assert sorted({o for o, _ in seen}) == list(range(4096))
+    assert all(len(v) == 1 for v in seen.values()) and len(seen) == 64 * 128
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_kivi_key_pack_roundtrip_any_width(orc, bits):
+    rng = np.random.default_rng(60 + bits)
+    codes = rng.integers(0, 1 << bits, (3, 64, 128)).astype(np.uint8)
+    packed = orc.kivi_key_pack(codes, bits)
+    assert packed.shape == (3, 64 * 128 * bits // 8)
+    for g in range(3):
+        for t in range(0, 64, 5):
+            for c in range(0, 128, 3):
+                byte = int(packed[g, orc.kivi_key_byte_offset(t, c, bits)])
+                assert (byte >> orc.kivi_key_bit(t, bits)) & ((1 << bits) - 1) == codes[g, t, c]
+
+
+def test_tokenmajor_pack_4bit_matches_numpy_nibbles(orc):
+    rng = np.random.default_rng(64)
+    codes = rng.integers(0, 16, (9, 128)).astype(np.uint8)
+    packed = orc.tokenmajor_pack(codes, 4)
+    assert np.array_equal(packed, (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8))
+
+
+@pytest.mark.parametrize("bk,bv", [(4, 4), (4, 2), (2, 4)])
+def test_grid_aligned_cache_equals_fp_attention_any_width(orc, bk, bv):
+    """Inputs on the b-bit grid are lossless at both widths, which pins the 4-bit unpacking of
+    keys and values in the decode."""
+    rng = np.random.default_rng(70 + 10 * bk + bv)
+    L = 300
+    kmax, vmax = (1 << bk) - 1, (1 << bv) - 1
+    kk = rng.integers(0, kmax + 1, (L, 128))
+    kk[::32][:, :] = 0
+    kk[1::32][:, :] = kmax                  # every 32-token group spans codes 0..kmax
+    ks = 2.0 ** rng.integers(-4, -1, 128)
+    K = (ks * (kk - 2)).astype(np.float16)
+    vk = rng.integers(0, vmax + 1, (L, 128))
+    vk[:, ::32] = 0
+    vk[:, 1::32] = vmax
+    V = (0.0625 * vk - 0.25).astype(np.float16)
+    q = rng.standard_normal((2, 128)).astype(np.float16)
+    parts = orc.kivi_build_one(K, V, bits_k=bk, bits_v=bv)
+    assert parts[0].shape[1] == 32 * 128 * bk // 8 and parts[2].shape[1] == 128 * bv // 8
+    out = orc.kivi_decode_one(q, *parts, L=L, bits_k=bk, bits_v=bv)
+    for h in range(2):
+        assert np.allclose(out[h], textbook(q[h], K, V, 128 ** -0.5), atol=1e-12, rtol=0)
+    # and the 2-bit reading of the same 4-bit bytes is not the same cache
+    if bk == 4:
+        wrong = orc.kivi_decode_one(q, *parts, L=L, bits_k=2, bits_v=bv) if parts[0].size else None
+        assert wrong is None or not np.allclose(wrong, out, atol=1e-6)
+
+
 def test_kivi_key_pack_roundtrip(orc):
     rng = np.random.default_rng(6)
     codes = rng.integers(0, 4, (3, 64, 128)).astype(np.uint8)
