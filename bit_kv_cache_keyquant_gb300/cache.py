@@ -52,9 +52,10 @@ class KiviCache:
         H, G, Gv, R = cfg.n_kv_heads, cfg.group_k, cfg.group_v, cfg.residual
         self.cap = (max_seq_len + 127) // 128 * 128        # token capacity (16-byte aligned rows)
         self.ngrp_cap = self.cap // G
-        self.k_codes = torch.zeros((batch, H, self.ngrp_cap, G * D // 4), dtype=torch.uint8, device=device)
+        bk, bv = cfg.bits_k, cfg.bits_v
+        self.k_codes = torch.zeros((batch, H, self.ngrp_cap, G * D * bk // 8), dtype=torch.uint8, device=device)
         self.k_sz = torch.zeros((batch, H, self.ngrp_cap, D), dtype=torch.int32, device=device)
-        self.v_codes = torch.zeros((batch, H, self.cap, D // 4), dtype=torch.uint8, device=device)
+        self.v_codes = torch.zeros((batch, H, self.cap, D * bv // 8), dtype=torch.uint8, device=device)
         self.v_sz = torch.zeros((batch, H, self.cap, D // Gv), dtype=torch.int32, device=device)
         self.k_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
         self.v_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
@@ -86,8 +87,8 @@ class KiviCache:
         tot = 0
         for L in lens:
             nkq, nvq = kivi_segments(int(L), cfg.residual)
-            tot += nkq * D // 4 + (nkq // cfg.group_k) * D * 4          # key codes + (s, z)
-            tot += nvq * D // 4 + nvq * (D // cfg.group_v) * 4            # value codes + (s, z)
+            tot += nkq * D * cfg.bits_k // 8 + (nkq // cfg.group_k) * D * 4     # key codes + (s, z)
+            tot += nvq * D * cfg.bits_v // 8 + nvq * (D // cfg.group_v) * 4     # value codes + (s, z)
             tot += (int(L) - nkq + int(L) - nvq) * D * 2                 # fp16 residual
         return tot * cfg.n_kv_heads
 

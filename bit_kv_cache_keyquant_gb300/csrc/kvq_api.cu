@@ -105,7 +105,7 @@ static kvq_status check_kivi(const kvq_config *cfg) {
     kvq_status s = check_common(cfg);
     if (s) return s;
     if (cfg->group_k <= 0 || cfg->group_v <= 0 || cfg->residual <= 0) return KVQ_ERR_INVALID_ARG;
-    if (cfg->bits_k != 2 || cfg->bits_v != 2) return KVQ_ERR_UNSUPPORTED;
+    if ((cfg->bits_k != 2 && cfg->bits_k != 4) || (cfg->bits_v != 2 && cfg->bits_v != 4)) return KVQ_ERR_UNSUPPORTED;
     if (cfg->group_k != 32 && cfg->group_k != 64 && cfg->group_k != 128) return KVQ_ERR_UNSUPPORTED;
     if (cfg->group_v != 32 && cfg->group_v != 64 && cfg->group_v != 128) return KVQ_ERR_UNSUPPORTED;
     if (cfg->residual % cfg->group_k != 0) return KVQ_ERR_UNSUPPORTED;

@@ -35,11 +35,11 @@ namespace kvq {
 
 namespace {
 
-constexpr int NSTAGE = 4;
 constexpr int QK_ROW = 36;                // 32 channels + 4 floats of padding (bank spread)
 
+template <int BK, int BV, int NSTAGE>
 struct Smem {
-    uint8_t stage[NSTAGE][STAGE_BYTES];
+    uint8_t stage[NSTAGE][Geo<BK, BV>::BYTES];
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
     float qk[NCWARP][4 * QK_ROW];         // per-warp alpha*q*s*2^(149-8(c&1)-E0), rows of 32 channels
@@ -67,9 +67,14 @@ __device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &
 
 }  // namespace
 
+// BK-bit keys and BV-bit values (2 or 4) in an NSTAGE-slot ring.
+template <int BK, int BV, int NSTAGE>
 __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Params P) {
+    using GG = Geo<BK, BV>;
+    constexpr int CPB = 8 / BK;                    // key codes per byte
+    constexpr int NPL = BK / 2;                    // 1024-byte planes per 32-token key tile
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    Smem<BK, BV, NSTAGE> &S = *reinterpret_cast<Smem<BK, BV, NSTAGE> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_units = P.B * P.Hq * P.splits;
     const int G = P.G, Gv = P.Gv;
@@ -85,7 +90,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
 
     if (warp == NCWARP) {
         // ---------------- producer: one stream of stages across all units ----------------
-        if (lane == 0) kivi_produce<NSTAGE>(P, P.Hq, S.stage, S.full, S.empty);
+        if (lane == 0) kivi_produce<NSTAGE, false, BK, BV>(P, P.Hq, S.stage, S.full, S.empty);
         return;
     }
 
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
     const int tq = lane & 3;                       // key mapping: lane = 4*(token quad) + channel block
     const int ts = lane >> 2, jg = lane & 3;       // value mapping: token slot, channel block of 32
     const float pe = __int_as_float((127 + 149 - P.e0) << 23), po = __int_as_float((127 + 141 - P.e0) << 23);
-    const float lscale = __int_as_float((127 + P.e0 - 2 * tq) << 23);   // undoes 2^(2j-E0), j = tq
+    const float lscale = __int_as_float((127 + P.e0 - BK * (tq % CPB)) << 23);   // undoes 2^(BK(j % CPB)-E0), j = tq
     const int gl = (32 * warp) / G;                // key group of this warp's tile within a stage
     const int ngv = P.ngv;
     const int jv = (32 * jg) / Gv;                 // value (s, z) group of this lane's channels
@@ -145,7 +150,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];
                     
-                    const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + KC_BYTES) + gl * 2 * KVQ_D;
+                    const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + GG::KC) + gl * 2 * KVQ_D;
                     // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
                     const int si = (((lane & 7) >> 1) * 4 + (lane >> 3)) * 8 + (lane & 1) * 4;
                     const uint2 sv = *reinterpret_cast<const uint2 *>(ksz + si);
@@ -156,23 +161,33 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     const float cb = warp_sum(qf[0] * h2f(lo16(zv.x)) + qf[1] * h2f(hi16(zv.x)) +
                                               qf[2] * h2f(lo16(zv.y)) + qf[3] * h2f(hi16(zv.y)));
                     __syncwarp();
-                    // ---- key codes: tokens q + 8j (q = lane/4) x channels 16k + 2tq + {0,1,8,9} ----
-                    const uint8_t *kt = st + warp * 1024;
-                    const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
-                    const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
-                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                    // ---- key codes: tokens q + 8j (q = lane/4) x channels 16k + 2tq + {0,1,8,9};
+                    //      token j sits in plane j / CPB at bits BK * (j % CPB) ----
+                    const uint8_t *kt = st + warp * 512 * BK;
+                    uint32_t kw[NPL][8];
+    #pragma unroll
+                    for (int pl = 0; pl < NPL; ++pl) {
+                        const uint4 ka = *reinterpret_cast<const uint4 *>(kt + pl * 1024 + lane * 16);
+                        const uint4 kb = *reinterpret_cast<const uint4 *>(kt + pl * 1024 + 512 + lane * 16);
+                        kw[pl][0] = ka.x; kw[pl][1] = ka.y; kw[pl][2] = ka.z; kw[pl][3] = ka.w;
+                        kw[pl][4] = kb.x; kw[pl][5] = kb.y; kw[pl][6] = kb.z; kw[pl][7] = kb.w;
+                    }
                     const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][tq * QK_ROW]);
                     unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};     // fp32 pairs
     #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const float4 qv = qs[k];                                 // channels 16k + 2tq + {0,1,8,9}
-                        const uint32_t w0 = kw[k], w16 = kw[k] >> 16;          // channels +0,+1 | +8,+9 at bits 0..15
                         const unsigned long long q01 = pack2f(qv.x, qv.y), q23 = pack2f(qv.z, qv.w);
     #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t m0 = 3u << (2 * j), m1 = 3u << (8 + 2 * j);
-                            acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // even, odd channel
-                            acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
+                        for (int pl = 0; pl < NPL; ++pl) {
+                            const uint32_t w0 = kw[pl][k], w16 = kw[pl][k] >> 16;   // channels +0,+1 | +8,+9
+    #pragma unroll
+                            for (int jj = 0; jj < CPB; ++jj) {
+                                const int j = pl * CPB + jj;
+                                const uint32_t m0 = ((1u << BK) - 1) << (BK * jj), m1 = m0 << 8;
+                                acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // even, odd channel
+                                acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
+                            }
                         }
                     }
                     // transpose-reduce over the 4 lanes of the quad: lane keeps token q + 8tq
@@ -190,8 +205,8 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     const float logit = score * lscale + cb;
                     const float p = softmax_tile(logit, m_run, l_part, vbias, vacc2);
                     // ---- values: 4 passes of 8 tokens; lane = (token slot ts, channel block jg) ----
-                    const uint8_t *vc = st + KC_BYTES + KSZ_MAX + warp * 32 * (KVQ_D / 4);
-                    const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + KC_BYTES + KSZ_MAX + VC_BYTES) +
+                    const uint8_t *vc = st + GG::KC + GG::KSZ + warp * 32 * (KVQ_D * BV / 8);
+                    const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + GG::KC + GG::KSZ + GG::VC) +
                                           warp * 32 * ngv;
     #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -199,7 +214,12 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                         const float pt = __shfl_sync(0xFFFFFFFFu, p, 4 * ts + r);   // token tau = ts + 8r
                         const uint32_t szt = vsz[tau * ngv + jv];
                         vbias += pt * h2f(hi16(szt));
-                        value_token_accum(*reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8), pt * h2f(lo16(szt)), vacc2);
+                        if (BV == 2)
+                            value_token_accum(*reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8),
+                                              pt * h2f(lo16(szt)), vacc2);
+                        else
+                            value_token_accum4(*reinterpret_cast<const uint4 *>(vc + tau * (KVQ_D / 2) + jg * 16),
+                                               pt * h2f(lo16(szt)), vacc2);
                     }
                 }
                 __syncwarp();
@@ -224,7 +244,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 8);
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 16);
                 // lane (ts, jg) writes channels 32jg + 4ts + i (i = 0..3) plus the zero-point term
-                float4 w4 = value_block_channels(vacc2, ts);
+                float4 w4 = BV == 2 ? value_block_channels(vacc2, ts) : value_block_channels4(vacc2, ts);
                 w4.x += vb; w4.y += vb; w4.z += vb; w4.w += vb;
                 *reinterpret_cast<float4 *>(&S.st_acc[warp][32 * jg + 4 * ts]) = w4;
                 if (lane == 0) {
@@ -260,6 +280,22 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
     }
 }
 
+template <int BK, int BV, int NST>
+static cudaError_t launch_kivi_variant(const Params &P, int64_t grid, cudaStream_t st) {
+    const size_t smem = sizeof(Smem<BK, BV, NST>);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kivi_decode_kernel<BK, BV, NST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    kivi_decode_kernel<BK, BV, NST><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q, const DecodePlan &p,
                                void *ws, cudaStream_t st) {
     Params P;
@@ -289,21 +325,18 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
     // |alpha q s| < alpha 2^32 (fp16 q and s): 2^(149-E0) alpha 2^32 < 2^127
     P.e0 = 54 + (int)ceilf(log2f(P.alpha));
     if (P.e0 < 22) P.e0 = 22;
+    P.bits_k = cfg->bits_k;
+    P.bits_v = cfg->bits_v;
     if (!P.err) return cudaErrorInvalidDevicePointer;
-    const size_t smem = sizeof(Smem);
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kivi_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
     const int64_t n_units = (int64_t)c->batch * cfg->n_q_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
-    kivi_decode_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
-    return cudaGetLastError();
+    // the ring holds 4 stages of 12 KiB at 2/2 bits, 3 of 16 KiB at 4/2 or 2/4, 2 of 20 KiB at 4/4
+    // (4 CTAs per SM)
+    if (cfg->bits_k == 2 && cfg->bits_v == 2) return launch_kivi_variant<2, 2, 4>(P, grid, st);
+    if (cfg->bits_k == 4 && cfg->bits_v == 2) return launch_kivi_variant<4, 2, 3>(P, grid, st);
+    if (cfg->bits_k == 2 && cfg->bits_v == 4) return launch_kivi_variant<2, 4, 3>(P, grid, st);
+    return launch_kivi_variant<4, 4, 2>(P, grid, st);
 }
 
 }  // namespace kvq

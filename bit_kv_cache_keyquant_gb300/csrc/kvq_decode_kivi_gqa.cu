@@ -355,9 +355,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     }
 }
 
+// 2-bit keys and values only (4-bit widths run on the per-head kernel)
 bool kivi_gqa_supported(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;
-    return g >= 2 && g <= GMAX;
+    return g >= 2 && g <= GMAX && cfg->bits_k == 2 && cfg->bits_v == 2;
 }
 
 cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q, const DecodePlan &p,
@@ -387,6 +388,8 @@ cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *
     P.kgrp_cap = P.cap / cfg->group_k;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
     P.e0 = 0;
+    P.bits_k = 2;
+    P.bits_v = 2;
     if (!P.err) return cudaErrorInvalidDevicePointer;
     const size_t smem = sizeof(SmemG);
     const int ngv = P.ngv;

@@ -192,6 +192,43 @@ __device__ __forceinline__ float4 value_block_channels(const unsigned long long 
     return r;
 }
 
+// The 4-bit form: the token's 16 bytes (32 4-bit codes, channel 2b + i of
+// byte b at bits 4i).  Halves of each word are masked the same way; channel
+// 2b + i carries an extra 2^(4i), and acc2[4*wi + 2*ab + i] holds channels
+// (8 wi + 4 ab + i, 8 wi + 4 ab + 2 + i).  Codes stay below bit 16, so every
+// masked word is still a denormal and every product exact.
+__device__ __forceinline__ void value_token_accum4(uint4 codes, float ps, unsigned long long acc2[16]) {
+    const unsigned long long wt = pack2f(ps * __int_as_float((127 + 149 - KVQ_EV) << 23),
+                                         ps * __int_as_float((127 + 141 - KVQ_EV) << 23));
+    const uint32_t uw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        const uint32_t w0 = uw[wi], w16 = uw[wi] >> 16;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t m0 = 15u << (4 * i), m1 = 15u << (8 + 4 * i);
+            acc2[4 * wi + i] = ffma2(pack2u(w0 & m0, w0 & m1), wt, acc2[4 * wi + i]);
+            acc2[4 * wi + 2 + i] = ffma2(pack2u(w16 & m0, w16 & m1), wt, acc2[4 * wi + 2 + i]);
+        }
+    }
+}
+
+// Channels 4*ts .. 4*ts+3 of the block from the 4-bit accumulators: channel
+// 4ts + x is acc2[2ts + (x & 1)], low half for x < 2, scaled by 2^(KVQ_EV - 4(x & 1)).
+__device__ __forceinline__ float4 value_block_channels4(const unsigned long long acc2[16], int ts) {
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int t8 = 0; t8 < 8; ++t8) {
+        if (ts == t8)
+            r = make_float4(lo2f(acc2[2 * t8]), lo2f(acc2[2 * t8 + 1]), hi2f(acc2[2 * t8]), hi2f(acc2[2 * t8 + 1]));
+    }
+    r.x *= __int_as_float((127 + KVQ_EV) << 23);
+    r.y *= __int_as_float((127 + KVQ_EV - 4) << 23);
+    r.z *= __int_as_float((127 + KVQ_EV) << 23);
+    r.w *= __int_as_float((127 + KVQ_EV - 4) << 23);
+    return r;
+}
+
 __device__ __forceinline__ void scale_pairs(unsigned long long acc2[16], float sc) {
     const unsigned long long s2 = pack2f(sc, sc);
 #pragma unroll

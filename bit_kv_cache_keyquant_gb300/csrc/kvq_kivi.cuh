@@ -16,6 +16,19 @@ constexpr int KSZ_MAX = 4 * KVQ_D * 4;                  // 2048 (G = 32)
 constexpr int VC_BYTES = STAGE_TOK * KVQ_D / 4;        // 4096
 constexpr int VSZ_MAX = STAGE_TOK * 4 * 4;             // 2048 (Gv = 32)
 constexpr int STAGE_BYTES = KC_BYTES + KSZ_MAX + VC_BYTES + VSZ_MAX;   // 12288
+
+// Stage geometry for BK-bit keys and BV-bit values (2 or 4): key codes, key
+// (s, z), value codes, value (s, z), in that order.
+template <int BK, int BV>
+struct Geo {
+    static constexpr int KC = STAGE_TOK * KVQ_D * BK / 8;
+    static constexpr int KSZ = KSZ_MAX;
+    static constexpr int VC = STAGE_TOK * KVQ_D * BV / 8;
+    static constexpr int VSZ = VSZ_MAX;
+    static constexpr int BYTES = KC + KSZ + VC + VSZ;
+};
+static_assert(Geo<2, 2>::BYTES == STAGE_BYTES, "2-bit stage geometry");
+
 struct Params {
     const int32_t *seq_len;
     const uint8_t *k_codes;
@@ -34,6 +47,7 @@ struct Params {
     int64_t kgrp_cap;   // cap / G
     float alpha;
     int e0;             // key products are scaled by 2^-E0
+    int bits_k, bits_v; // code widths (2 or 4)
 };
 
 // Geometry of one work unit.  Splits 0 .. splits-2 of a (batch row, query
@@ -97,6 +111,15 @@ __device__ __forceinline__ int kivi_key_byte_offset(int t, int c) {
            2 * (cc >> 3);
 }
 
+// The same layout at b bits: a 32-token tile is b/2 planes of 1024 bytes and
+// token q + 8p sits in plane p / (8/b) at bits b * (p % (8/b)).
+__device__ __forceinline__ int kivi_key_byte_offset_w(int bits, int t, int c) {
+    const int cpb = 8 / bits, p = (t & 31) >> 3;
+    return (t >> 5) * 512 * bits + (p / cpb) * 1024 + kivi_key_byte_offset(t & 7, c);
+}
+
+__device__ __forceinline__ int kivi_key_bit_w(int bits, int t) { return bits * (((t & 31) >> 3) % (8 / bits)); }
+
 __device__ __forceinline__ int kivi_sz_index(int c) {
     const int k = c >> 4, cc = c & 15;
     return ((k >> 1) * 4 + ((cc & 7) >> 1)) * 8 + (k & 1) * 4 + (cc & 1) + 2 * (cc >> 3);
@@ -107,12 +130,13 @@ __device__ __forceinline__ int kivi_sz_index(int c) {
 __device__ __forceinline__ void fetch_k4(const Params &P, const Unit &U, int t, int lane, float kv[4]) {
     if (t < U.nKq) {
         const int G = P.G, gi = t / G, tt = t - gi * G;
-        const uint8_t *grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D / 4);
+        const int bits = P.bits_k;
+        const uint8_t *grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D * bits / 8);
         const uint16_t *szb = reinterpret_cast<const uint16_t *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int c = 4 * lane + i, si = kivi_sz_index(c);
-            const int code = (grp[kivi_key_byte_offset(tt, c)] >> (2 * ((tt & 31) >> 3))) & 3;
+            const int code = (grp[kivi_key_byte_offset_w(bits, tt, c)] >> kivi_key_bit_w(bits, tt)) & ((1 << bits) - 1);
             kv[i] = (float)code * h2f(szb[si]) + h2f(szb[KVQ_D + si]);
         }
     } else {
@@ -123,10 +147,14 @@ __device__ __forceinline__ void fetch_k4(const Params &P, const Unit &U, int t, 
 
 __device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, int lane, float vv[4]) {
     if (t < U.nVq) {
-        const uint8_t byte = P.v_codes[(U.bk * P.cap + t) * (KVQ_D / 4) + lane];
+        // the lane's 4 channels: one byte at 2 bits, two at 4 bits (channel c at bits bits*(c % (8/bits)))
+        const int bits = P.bits_v;
+        const uint8_t *tb = P.v_codes + (U.bk * P.cap + t) * (KVQ_D * bits / 8);
+        const uint32_t w = bits == 2 ? (uint32_t)tb[lane] : (uint32_t)reinterpret_cast<const uint16_t *>(tb)[lane];
         const uint32_t sz = P.v_sz[(U.bk * P.cap + t) * P.ngv + (4 * lane) / P.Gv];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) vv[i] = (float)((byte >> (2 * i)) & 3) * h2f(lo16(sz)) + h2f(hi16(sz));
+        for (int i = 0; i < 4; ++i)
+            vv[i] = (float)((w >> (bits * i)) & ((1u << bits) - 1)) * h2f(lo16(sz)) + h2f(hi16(sz));
     } else {
         const uint2 u = *reinterpret_cast<const uint2 *>(P.v_res + (U.bk * P.R + t % P.R) * KVQ_D + 4 * lane);
         vv[0] = h2f(lo16(u.x)); vv[1] = h2f(hi16(u.x)); vv[2] = h2f(lo16(u.y)); vv[3] = h2f(hi16(u.y));
@@ -229,18 +257,19 @@ __device__ __forceinline__ void kivi_residual(const Params &P, const Unit &U, co
 
 // Producer (one lane): streams the stages of every unit of this CTA, in
 // unit order, into an NST-slot ring; returns after every issued copy landed.
-template <int NST, bool SPLIT_MAJOR = false>
-__device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (*stage)[STAGE_BYTES], uint64_t *full,
-                                             uint64_t *empty) {
+template <int NST, bool SPLIT_MAJOR = false, int BK = 2, int BV = 2>
+__device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (*stage)[Geo<BK, BV>::BYTES],
+                                             uint64_t *full, uint64_t *empty) {
+    using GG = Geo<BK, BV>;
     const int n_units = P.B * hpr * P.splits;
     const int G = P.G;
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit U = unit_of<SPLIT_MAJOR>(P, u, hpr);
-        const uint8_t *kc_base = P.k_codes + U.bk * P.kgrp_cap * ((int64_t)G * KVQ_D / 4);
+        const uint8_t *kc_base = P.k_codes + U.bk * P.kgrp_cap * ((int64_t)G * KVQ_D * BK / 8);
         const uint32_t *ksz_base = P.k_sz + U.bk * P.kgrp_cap * KVQ_D;
-        const uint8_t *vc_base = P.v_codes + U.bk * P.cap * (KVQ_D / 4);
+        const uint8_t *vc_base = P.v_codes + U.bk * P.cap * (KVQ_D * BV / 8);
         const uint32_t *vsz_base = P.v_sz + U.bk * P.cap * P.ngv;
         for (int s = 0; s < U.nstages; ++s, ++sg) {
             const int slot = sg % NST;
@@ -248,16 +277,16 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
             if (!ok) break;
             const int nt = min(NCWARP, U.nT - s * NCWARP);
             const int tok = U.t0 + s * STAGE_TOK;
-            const uint32_t kc_b = nt * 1024;
+            const uint32_t kc_b = nt * 512 * BK;
             const uint32_t ksz_b = ((nt * 32 + G - 1) / G) * KVQ_D * 4;
-            const uint32_t vc_b = nt * 32 * (KVQ_D / 4);
+            const uint32_t vc_b = nt * 32 * (KVQ_D * BV / 8);
             const uint32_t vsz_b = nt * 32 * P.ngv * 4;
             uint8_t *st = stage[slot];
             mbar_expect_tx(&full[slot], kc_b + ksz_b + vc_b + vsz_b);
-            bulk_g2s(st, kc_base + (int64_t)(tok >> 5) * 1024, kc_b, &full[slot]);
-            bulk_g2s(st + KC_BYTES, ksz_base + (int64_t)(tok / G) * KVQ_D, ksz_b, &full[slot]);
-            bulk_g2s(st + KC_BYTES + KSZ_MAX, vc_base + (int64_t)tok * (KVQ_D / 4), vc_b, &full[slot]);
-            bulk_g2s(st + KC_BYTES + KSZ_MAX + VC_BYTES, vsz_base + (int64_t)tok * P.ngv, vsz_b, &full[slot]);
+            bulk_g2s(st, kc_base + (int64_t)(tok >> 5) * 512 * BK, kc_b, &full[slot]);
+            bulk_g2s(st + GG::KC, ksz_base + (int64_t)(tok / G) * KVQ_D, ksz_b, &full[slot]);
+            bulk_g2s(st + GG::KC + GG::KSZ, vc_base + (int64_t)tok * (KVQ_D * BV / 8), vc_b, &full[slot]);
+            bulk_g2s(st + GG::KC + GG::KSZ + GG::VC, vsz_base + (int64_t)tok * P.ngv, vsz_b, &full[slot]);
         }
     }
     // drain: every issued stage must have landed before the CTA exits

@@ -28,10 +28,12 @@ __device__ __forceinline__ int kivi_sz_index(int c) {
 }
 
 // One key group by a 128-thread block: src fp16 [G][D], codes the group's
-// G*D/4 bytes, sz the group's 2*D fp16 (scales, then zeros).
+// G*D*bits/8 bytes, sz the group's 2*D fp16 (scales, then zeros).  bits = 2
+// or 4: a 32-token tile is bits/2 planes of 1024 bytes, token q + 8p in plane
+// p / (8/bits) at bits bits*(p % (8/bits)) of its 2-bit-layout byte.
 template <int NT>
 __device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src, uint8_t *__restrict__ codes,
-                                                uint16_t *__restrict__ sz) {
+                                                uint16_t *__restrict__ sz, int bits = 2) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // lane's 32 channels of token lane in each tile: 4 x 16 bytes per tile
@@ -76,7 +78,8 @@ __device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src
     }
     // lane now holds channel 32w + lane in slot 0
     uint16_t s, z;
-    affine_fit(mn[0], mx[0], 3, s, z);
+    const int qmax = (1 << bits) - 1;
+    affine_fit(mn[0], mx[0], qmax, s, z);
     const uint32_t my_sz = (uint32_t)s | ((uint32_t)z << 16);
     {
         const int si = kivi_sz_index(32 * w + lane);
@@ -85,9 +88,11 @@ __device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src
     }
 
     const int q = lane & 7, p = lane >> 3;
+    const int cpb = 8 / bits;                      // codes per byte; lanes p sharing a plane: p / cpb
+    const int shift = bits * (p % cpb);
 #pragma unroll
     for (int tt = 0; tt < NT; ++tt) {
-        // word[r][kk]: chunk row r, channel block 16*(2w+kk); byte e + 2h, bits 2p
+        // word[r][kk]: chunk row r, channel block 16*(2w+kk); byte e + 2h, bits `shift`
         uint32_t word[4][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i) word[i][0] = word[i][1] = 0;
@@ -96,34 +101,41 @@ __device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src
             uint32_t szc = __shfl_sync(0xFFFFFFFFu, my_sz, c);
             float sf = h2f(lo16(szc)), zf = h2f(hi16(szc));
             float x = h2f((c & 1) ? hi16(xv[tt][c >> 1]) : lo16(xv[tt][c >> 1]));
-            uint32_t code = (uint32_t)affine_code(x, zf, sf, 3);
+            uint32_t code = (uint32_t)affine_code(x, zf, sf, qmax);
             const int kk = c >> 4, cc = c & 15;
-            word[(cc & 7) >> 1][kk] |= code << (8 * ((cc & 1) + 2 * (cc >> 3)) + 2 * p);
+            word[(cc & 7) >> 1][kk] |= code << (8 * ((cc & 1) + 2 * (cc >> 3)) + shift);
         }
+        // OR the codes of the lanes that share a byte: tokens q + 8p of one plane
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 8);
-                word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 16);
+                if (bits == 2) word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 16);
             }
-        // the four lanes of token octet q store chunk rows r = p: 8 bytes each
-        uint2 v = make_uint2(word[0][0], word[0][1]);
+        // the cpb lanes of a plane store its four chunk rows, 4 / cpb rows of 8 bytes each
+        uint8_t *tile = codes + tt * 512 * bits + (p / cpb) * 1024;
+        const int nrow = 4 / cpb;
+        for (int rr = 0; rr < nrow; ++rr) {
+            const int r = (p % cpb) * nrow + rr;
+            uint2 v = make_uint2(word[0][0], word[0][1]);
 #pragma unroll
-        for (int i = 1; i < 4; ++i)
-            if (p == i) v = make_uint2(word[i][0], word[i][1]);
-        uint8_t *tile = codes + tt * 1024;
-        *reinterpret_cast<uint2 *>(tile + (w >> 1) * 512 + (4 * q + p) * 16 + (w & 1) * 8) = v;
+            for (int i = 1; i < 4; ++i)
+                if (r == i) v = make_uint2(word[i][0], word[i][1]);
+            *reinterpret_cast<uint2 *>(tile + (w >> 1) * 512 + (4 * q + r) * 16 + (w & 1) * 8) = v;
+        }
     }
 }
 
 template <int NT>
 __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
-                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz) {
+                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz,
+                                                             int bits) {
     const int64_t g = blockIdx.x;
     if (g >= n_groups) return;
     constexpr int G = 32 * NT;
-    key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D / 4, sz + g * 2 * KVQ_D);
+    key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D * bits / 8, sz + g * 2 * KVQ_D,
+                        bits);
 }
 
 // One value token by a warp, per token over groups of GV channels: lane l
@@ -131,7 +143,7 @@ __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__r
 // (valid in lanes 4j, channels 16j..16j+15) and the (s, z) of its group.
 template <int GV>
 __device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ src, int lane, uint32_t &wv, uint16_t &s,
-                                                  uint16_t &z) {
+                                                  uint16_t &z, int bits = 2) {
     constexpr int LG = GV / 4;   // lanes per group
     uint2 u = *reinterpret_cast<const uint2 *>(src + 4 * lane);
     float x0 = h2f(lo16(u.x)), x1 = h2f(hi16(u.x)), x2 = h2f(lo16(u.y)), x3 = h2f(hi16(u.y));
@@ -142,12 +154,26 @@ __device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ s
         mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
     }
-    affine_fit(mn, mx, 3, s, z);
+    const int qmax = (1 << bits) - 1;
+    affine_fit(mn, mx, qmax, s, z);
     float sf = h2f(s), zf = h2f(z);
-    uint32_t b = (uint32_t)affine_code(x0, zf, sf, 3) | ((uint32_t)affine_code(x1, zf, sf, 3) << 2) |
-                 ((uint32_t)affine_code(x2, zf, sf, 3) << 4) | ((uint32_t)affine_code(x3, zf, sf, 3) << 6);
-    wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 8) | (__shfl_down_sync(0xFFFFFFFFu, b, 2) << 16) |
-         (__shfl_down_sync(0xFFFFFFFFu, b, 3) << 24);
+    const uint32_t b = (uint32_t)affine_code(x0, zf, sf, qmax) | ((uint32_t)affine_code(x1, zf, sf, qmax) << bits) |
+                       ((uint32_t)affine_code(x2, zf, sf, qmax) << (2 * bits)) |
+                       ((uint32_t)affine_code(x3, zf, sf, qmax) << (3 * bits));
+    if (bits == 2)       // lanes 4j: channels 16j..16j+15
+        wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 8) | (__shfl_down_sync(0xFFFFFFFFu, b, 2) << 16) |
+             (__shfl_down_sync(0xFFFFFFFFu, b, 3) << 24);
+    else                 // lanes 2j: channels 8j..8j+7, channel c at nibble c % 2 of byte c / 2
+        wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 16);
+}
+
+// Store of one token's packed codes by the lanes that hold a full word.
+__device__ __forceinline__ void value_token_store(uint8_t *__restrict__ tok, int lane, uint32_t wv, int bits) {
+    if (bits == 2) {
+        if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(tok)[lane >> 2] = wv;
+    } else {
+        if ((lane & 1) == 0) reinterpret_cast<uint32_t *>(tok)[lane >> 1] = wv;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -159,7 +185,7 @@ __device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ s
 template <int GV, bool KITTY>
 __global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
                                                           uint8_t *__restrict__ out, uint32_t *__restrict__ sz,
-                                                          int page_tokens, int64_t page_bytes) {
+                                                          int page_tokens, int64_t page_bytes, int bits) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -167,9 +193,9 @@ __global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__rest
     for (int64_t t = warp; t < n_tokens; t += nwarps) {
         uint32_t wv;
         uint16_t s, z;
-        value_token_quant<GV>(v + t * KVQ_D, lane, wv, s, z);
+        value_token_quant<GV>(v + t * KVQ_D, lane, wv, s, z, KITTY ? 2 : bits);
         if (!KITTY) {
-            if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(out + t * (KVQ_D / 4))[lane >> 2] = wv;
+            value_token_store(out + t * (KVQ_D * bits / 8), lane, wv, bits);
             if ((lane % LG) == 0) sz[t * (KVQ_D / GV) + lane / LG] = (uint32_t)s | ((uint32_t)z << 16);
         } else {
             const int64_t p = t / page_tokens;
@@ -379,11 +405,12 @@ cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t 
         int64_t n = n_groups - g0 < 0x7FFFFFFF ? n_groups - g0 : 0x7FFFFFFF;
         const int G = cfg->group_k;
         const uint16_t *ks = kp + g0 * (int64_t)G * KVQ_D;
-        uint8_t *cs = cp + g0 * (int64_t)G * KVQ_D / 4;
+        uint8_t *cs = cp + g0 * (int64_t)G * KVQ_D * cfg->bits_k / 8;
         uint16_t *zs = zp + g0 * 2 * KVQ_D;
-        if (G == 32) quant_key_kivi_kernel<1><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
-        else if (G == 64) quant_key_kivi_kernel<2><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
-        else quant_key_kivi_kernel<4><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs);
+        const int bits = cfg->bits_k;
+        if (G == 32) quant_key_kivi_kernel<1><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs, bits);
+        else if (G == 64) quant_key_kivi_kernel<2><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs, bits);
+        else quant_key_kivi_kernel<4><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs, bits);
     }
     return cudaGetLastError();
 }
@@ -396,9 +423,9 @@ cudaError_t launch_quant_value_kivi(const kvq_config *cfg, const void *v, int64_
     uint8_t *cp = static_cast<uint8_t *>(codes);
     uint32_t *zp = static_cast<uint32_t *>(sz);
     switch (cfg->group_v) {
-        case 32: quant_value_kernel<32, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0); break;
-        case 64: quant_value_kernel<64, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0); break;
-        default: quant_value_kernel<128, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0); break;
+        case 32: quant_value_kernel<32, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, cfg->bits_v); break;
+        case 64: quant_value_kernel<64, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, cfg->bits_v); break;
+        default: quant_value_kernel<128, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, cfg->bits_v); break;
     }
     return cudaGetLastError();
 }
@@ -411,7 +438,7 @@ cudaError_t launch_quant_value_kitty(const kvq_config *cfg, const void *v, int64
     const int grid = grid_cap((n_tokens + 7) / 8, 16);
     const int64_t pb = (int64_t)G * KVQ_D / 4 + 4LL * G;
     quant_value_kernel<128, true><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens,
-                                                        static_cast<uint8_t *>(pages), nullptr, G, pb);
+                                                        static_cast<uint8_t *>(pages), nullptr, G, pb, 2);
     return cudaGetLastError();
 }
 
@@ -469,7 +496,7 @@ struct AppendParams {
     uint32_t *v_sz;
     uint16_t *k_res, *v_res;
     unsigned *err;
-    int Hkv, R, G, ngv, max_seq_len;
+    int Hkv, R, G, ngv, max_seq_len, bits_k, bits_v;
     int64_t cap, kgrp_cap;
 };
 
@@ -489,15 +516,16 @@ __global__ void __launch_bounds__(128) append_kivi_kernel(AppendParams P) {
     if (L > 0 && L % P.R == 0) {
         for (int g = 0; g < P.R / G; ++g) {
             const int64_t gi = bk * P.kgrp_cap + (L - P.R) / G + g;
-            key_group_quant<NT>(kres + (int64_t)g * G * KVQ_D, P.k_codes + gi * (G * KVQ_D / 4), P.k_sz + gi * 2 * KVQ_D);
+            key_group_quant<NT>(kres + (int64_t)g * G * KVQ_D, P.k_codes + gi * (G * KVQ_D * P.bits_k / 8),
+                                P.k_sz + gi * 2 * KVQ_D, P.bits_k);
         }
     }
     if (L >= P.R && warp == 0) {
         const int64_t t = L - P.R;
         uint32_t wv;
         uint16_t s, z;
-        value_token_quant<GV>(vres + (t % P.R) * KVQ_D, lane, wv, s, z);
-        if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(P.v_codes + (bk * P.cap + t) * (KVQ_D / 4))[lane >> 2] = wv;
+        value_token_quant<GV>(vres + (t % P.R) * KVQ_D, lane, wv, s, z, P.bits_v);
+        value_token_store(P.v_codes + (bk * P.cap + t) * (KVQ_D * P.bits_v / 8), lane, wv, P.bits_v);
         if ((lane % (GV / 4)) == 0)
             P.v_sz[(bk * P.cap + t) * P.ngv + lane / (GV / 4)] = (uint32_t)s | ((uint32_t)z << 16);
     }
@@ -535,6 +563,8 @@ cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
     P.R = cfg->residual;
     P.G = cfg->group_k;
     P.ngv = KVQ_D / cfg->group_v;
+    P.bits_k = cfg->bits_k;
+    P.bits_v = cfg->bits_v;
     P.max_seq_len = c->max_seq_len;
     P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
     P.kgrp_cap = P.cap / cfg->group_k;

@@ -45,8 +45,11 @@
  *     {16k + 2r + {0,1,8,9}} in the 16-byte chunks lane and lane + 32.
  *     Parameters: 256 fp16 per group, the 128 scales then the 128 zeros,
  *     channel c at index ((k/2)*4 + r)*8 + (k%2)*4 + e + 2h of each half.
- *   KIVI value token: D/4 bytes, channel c in bits 2*(c%4) of byte c/4.
- *     Parameters: fp16x2 (s, z) [D/Gv] per token.
+ *     At 4 bits (KIVI-4) a tile is 2048 bytes, two planes of 1024: token
+ *     q + 8p goes to plane p/2, at bits 4*(p%2) of the byte that the 2-bit
+ *     layout above gives inside the plane (t%8 in place of t).
+ *   KIVI value token: D*b/8 bytes for b-bit codes, channel c in bits
+ *     b*(c % (8/b)) of byte c/(8/b).  Parameters: fp16x2 (s, z) [D/Gv] per token.
  *   Kitty key page (G = 128 tokens, K boosted channels), one record of
  *     kvq_kitty_key_page_bytes() bytes: low plane [D][G/4] (byte (c, t/4),
  *     bits 2*(t%4), code & 3), high plane [K][G/4] (row r = r-th boosted
@@ -78,7 +81,7 @@ extern "C" {
 typedef enum {
     KVQ_OK = 0,
     KVQ_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent config */
-    KVQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, bits != 2, ...) */
+    KVQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, bits not 2 or 4, ...) */
     KVQ_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
     KVQ_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
     KVQ_ERR_WORKSPACE = 5      /* workspace smaller than kv_decode_attn_plan() asked for */
@@ -100,8 +103,8 @@ typedef struct {
     int32_t head_dim;     /* D; 128 */
     int32_t n_q_heads;    /* Hq */
     int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0 */
-    int32_t bits_k;       /* KIVI key bits: 2 */
-    int32_t bits_v;       /* KIVI / Kitty value bits: 2 */
+    int32_t bits_k;       /* KIVI key bits: 2 or 4 */
+    int32_t bits_v;       /* KIVI value bits: 2 or 4; Kitty value bits: 2 */
     int32_t group_k;      /* G: tokens per KIVI key group (32, 64, 128) or Kitty page (128) */
     int32_t group_v;      /* Gv: channels per KIVI value group (32 or 128) */
     int32_t residual;     /* R: KIVI fp16 residual (R % G == 0), Kitty value local window */
@@ -116,22 +119,24 @@ typedef struct {
 /* Write side                                                              */
 /* --------------------------------------------------------------------- */
 
-/* a1: quantize n_groups KIVI key groups.
+/* a1: quantize n_groups KIVI key groups at b = cfg->bits_k bits (2 or 4).
  *   k       fp16 [n_groups][G][D], token-major (as the K projection emits it)
- *   codes   uint8 [n_groups][G*D/4]  (tile layout above)
- *   sz      fp16 [n_groups][2*D]     (scales then zeros, order above)
- * Per channel over the group's G tokens: z = fp16 round-down(min),
- * s = fp16 round-up(fp32 (max - z) / 3), raised by one fp16 step while
- * z + 3s < max; code = clamp(rint((x - z) / s), 0, 3) in fp32 with the
- * stored fp16 s, z; s = 0 (all codes 0) when max == min.
- * (KIVI section 3.3 key split; Kitty Observation 1 formula.)
+ *   codes   uint8 [n_groups][G*D*b/8]  (tile layout above)
+ *   sz      fp16 [n_groups][2*D]       (scales then zeros, order above)
+ * Per channel over the group's G tokens, with Q = 2^b - 1: z = fp16
+ * round-down(min), s = fp16 round-up(fp32 (max - z) / Q), raised by one fp16
+ * step while z + Q s < max; code = clamp(rint((x - z) / s), 0, Q) in fp32
+ * with the stored fp16 s, z; s = 0 (all codes 0) when max == min.
+ * (KIVI section 3.3 key split, section 4 KIVI-2 / KIVI-4; Kitty Observation 1
+ * formula.)
  * n_groups == 0 launches nothing and returns KVQ_OK. */
 KVQ_API kvq_status kv_quant_key(const kvq_config *cfg, const void *k, int64_t n_groups,
                         void *codes, void *sz, cudaStream_t stream);
 
-/* a2: quantize n_tokens KIVI values, per token over groups of Gv channels.
+/* a2: quantize n_tokens KIVI values, per token over groups of Gv channels,
+ * at b = cfg->bits_v bits (2 or 4).
  *   v       fp16 [n_tokens][D]
- *   codes   uint8 [n_tokens][D/4] (token-major)
+ *   codes   uint8 [n_tokens][D*b/8] (token-major)
  *   sz      fp16x2 [n_tokens][D/Gv]
  * Same rounding rules as kv_quant_key.  (KIVI section 3.3 value split.) */
 KVQ_API kvq_status kv_quant_value(const kvq_config *cfg, const void *v, int64_t n_tokens,
@@ -195,9 +200,9 @@ typedef struct {
     int32_t batch;
     int32_t max_seq_len;     /* token capacity CAP = max_seq_len rounded up to a multiple of 128 */
     const int32_t *seq_len;  /* [B] */
-    const void *k_codes;     /* uint8  [B][Hkv][CAP/G][G*D/4] */
+    const void *k_codes;     /* uint8  [B][Hkv][CAP/G][G*D*bits_k/8] */
     const void *k_sz;        /* fp16 [B][Hkv][CAP/G][2*D]: scales, then zeros (layout above) */
-    const void *v_codes;     /* uint8  [B][Hkv][CAP][D/4] */
+    const void *v_codes;     /* uint8  [B][Hkv][CAP][D*bits_v/8] */
     const void *v_sz;        /* fp16x2 [B][Hkv][CAP][D/Gv] */
     const void *k_res;       /* fp16   [B][Hkv][R][D] */
     const void *v_res;       /* fp16   [B][Hkv][R][D] */

@@ -62,7 +62,9 @@ def test_validation_without_gpu(K):
     good = K.make_config()
     bad_d = K.make_config(head_dim=64)
     assert _call_quant_key(K, bad_d) == K.KVQ_ERR_UNSUPPORTED
-    assert _call_quant_key(K, K.make_config(bits_k=4)) == K.KVQ_ERR_UNSUPPORTED
+    assert _call_quant_key(K, K.make_config(bits_k=3)) == K.KVQ_ERR_UNSUPPORTED
+    assert _call_quant_key(K, K.make_config(bits_k=8)) == K.KVQ_ERR_UNSUPPORTED
+    assert _call_quant_key(K, K.make_config(bits_k=4), k=None) == K.KVQ_ERR_INVALID_ARG   # 4 bits is accepted
     assert _call_quant_key(K, K.make_config(residual=100)) == K.KVQ_ERR_UNSUPPORTED     # R % G != 0
     assert _call_quant_key(K, K.make_config(n_q_heads=30, n_kv_heads=8)) == K.KVQ_ERR_INVALID_ARG
     assert _call_quant_key(K, good, k=None) == K.KVQ_ERR_INVALID_ARG
@@ -79,7 +81,7 @@ def test_validation_without_gpu(K):
     assert K.raw_call("kv_append_kivi", ctypes.byref(good), ctypes.byref(cache), 16, 0x1004, None) == \
         K.KVQ_ERR_MISALIGNED
     assert K.raw_call("kv_append_kivi", ctypes.byref(good), None, 16, 16, None) == K.KVQ_ERR_INVALID_ARG
-    assert K.raw_call("kv_append_kivi", ctypes.byref(K.make_config(bits_v=4)), ctypes.byref(cache), 16, 16,
+    assert K.raw_call("kv_append_kivi", ctypes.byref(K.make_config(bits_v=1)), ctypes.byref(cache), 16, 16,
                       None) == K.KVQ_ERR_UNSUPPORTED
     kc = K.kvq_kitty_cache(2, 512, 16, 16, 16, 16, 16, 16, 16, 16)
     assert K.raw_call("kv_append_kitty", ctypes.byref(kitty), ctypes.byref(kc), 16, 16, 2, None) == \
