@@ -47,7 +47,8 @@ def _peaks():
 def _workload_desc(w):
     base = f"{w.name}: batch {w.batch}, {w.n_q_heads} query / {w.n_kv_heads} KV heads, head_dim 128, "
     if w.variant == "kivi":
-        return base + f"{w.seq_len} cached tokens, K2V2 (key per-channel G=32, value per-token Gv=32), R=128"
+        return base + (f"{w.seq_len} cached tokens, K{w.bits_k}V{w.bits_v} (key per-channel G=32, value per-token "
+                       f"Gv=32), R=128")
     if w.variant == "kitty":
         return base + (f"{w.seq_len} cached tokens, Kitty pages G=128, 16 of 128 key channels boosted to 4 bit "
                        f"(two 2-bit planes), value 2 bit, sink 32, local 128")
@@ -128,10 +129,10 @@ def oracle_step_seconds(w, budget_s: float, min_pairs: int = 4):
     for b, h in pairs:
         K = I.gen_kv_np(w, I.T_K, b, h, L)
         V = I.gen_kv_np(w, I.T_V, b, h, L)
-        parts = O.kivi_build_one(K, V)
+        parts = O.kivi_build_one(K, V, bits_k=w.bits_k, bits_v=w.bits_v)
         t0 = time.perf_counter()
-        O.kivi_quant_value(V[L - 129:L - 128])
-        O.kivi_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L)
+        O.kivi_quant_value(V[L - 129:L - 128], 32, w.bits_v)
+        O.kivi_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L, bits_k=w.bits_k, bits_v=w.bits_v)
         spent += time.perf_counter() - t0
         n += 1
         if n >= min_pairs and spent >= budget_s:
@@ -175,7 +176,7 @@ def build_state(w, device, appends: int = 1024):
     lens = I.seq_lens(w)
     Lmax = int(lens.max())
     if w.variant == "kivi":
-        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads)
+        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, bits_k=w.bits_k, bits_v=w.bits_v)
         cache = C.KiviCache(cfg, w.batch, Lmax, device=device)
         variant = kvq.KVQ_VARIANT_KIVI
     elif w.variant == "kitty":
@@ -219,9 +220,10 @@ def build_state(w, device, appends: int = 1024):
         st.update(n_vtok=n_vtok, n_kgrp=n_kgrp,
                   vnew=I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_vtok, 128, device),
                   knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_kgrp * cfg.group_k, 128, device),
-                  scratch=[torch.empty((n_vtok, 32), dtype=torch.uint8, device=device),
+                  scratch=[torch.empty((n_vtok, 128 * w.bits_v // 8), dtype=torch.uint8, device=device),
                            torch.empty((n_vtok, 128 // cfg.group_v), dtype=torch.int32, device=device),
-                           torch.empty((n_kgrp, cfg.group_k * 32), dtype=torch.uint8, device=device),
+                           torch.empty((n_kgrp, cfg.group_k * 128 * w.bits_k // 8), dtype=torch.uint8,
+                                       device=device),
                            torch.empty((n_kgrp, 128), dtype=torch.int32, device=device)])
     elif w.variant == "kitty":
         n_pg = max(1, pairs // 128)                                         # 1/G of the page flushes
@@ -407,7 +409,8 @@ def run_gpu(args, w, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": DTYPE[w.variant], "data": "synthetic",
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": DTYPE["kivi4" if w.variant == "kivi" and w.bits_k == 4 else w.variant],
         "config": {"workload": _workload_desc(w), "batch": w.batch, "q_heads": w.n_q_heads,
                    "kv_heads": w.n_kv_heads, "head_dim": 128, "seq_len": w.seq_len, "parallelism": f"replicas x{world}",
                    "splits": st["n_splits"],
@@ -432,7 +435,7 @@ def run_gpu(args, w, rank, world, local_rank):
 def stage1_kernel(w):
     """Name and source files of the stage-1 kernel the library runs for workload w."""
     g = w.n_q_heads // w.n_kv_heads
-    if w.variant == "kivi" and 2 <= g <= 4:
+    if w.variant == "kivi" and 2 <= g <= 4 and w.bits_k == 2 and w.bits_v == 2:
         return "kivi_decode_gqa_kernel", ("kvq_decode_kivi_gqa.cu", "kvq_kivi.cuh", "kvq_mma.cuh", "kvq_device.cuh")
     if w.variant == "kivi":
         return "kivi_decode_kernel", ("kvq_decode_kivi.cu", "kvq_kivi.cuh", "kvq_device.cuh")
@@ -443,7 +446,7 @@ def stage1_kernel(w):
     if w.variant == "int8t":
         return "int8_token_decode_kernel", ("kvq_decode_int8.cu", "kvq_device.cuh")
     return f"{w.variant}_decode_kernel", (f"kvq_decode_{w.variant}.cu", "kvq_device.cuh")
-DTYPE = {"kivi": "u2 codes + fp16 scales, fp32 accumulate", "kitty": "u2 planes + fp16 scales, fp32 accumulate",
+DTYPE = {"kivi": "u2 codes + fp16 scales, fp32 accumulate", "kivi4": "u4 codes + fp16 scales, fp32 accumulate", "kitty": "u2 planes + fp16 scales, fp32 accumulate",
          "int8": "s8 codes + Philox dither + fp16 scales, fp32 accumulate",
          "int8t": "s8 codes + Philox dither + fp16 token scales, fp32 accumulate"}
 
@@ -462,7 +465,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6],
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7],
                     help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")

@@ -58,6 +58,8 @@ class Workload:
     channel_sigma: bool = False  # per-(kv head, channel) sigma, log-uniform [0.5, 8]
     min_seq_len: int = 0         # >0: lengths ~ U{min..seq_len}
     fixed_outliers: bool = False  # same outlier channels for every kv head
+    bits_k: int = 2              # KIVI code widths
+    bits_v: int = 2
 
     @property
     def seed(self) -> int:
@@ -76,6 +78,7 @@ WORKLOADS = {
                 "int8", min_seq_len=16384),
     6: Workload(6, "INT8 token-granular slot pool B8 64q/8kv L~U[16384,65536]", 8, 64, 8, 65536,
                 "int8t", min_seq_len=16384),
+    7: Workload(7, "KIVI-4 Llama-2-7B-shaped MHA B32 H32 L4096", 32, 32, 32, 4096, "kivi", bits_k=4, bits_v=4),
 }
 
 
