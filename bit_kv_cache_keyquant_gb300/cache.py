@@ -93,6 +93,74 @@ class KiviCache:
         return tot * cfg.n_kv_heads
 
 
+class KiviPagedCache:
+    """Paged KIVI cache of one layer: n_pages page records of 128 tokens x Hkv heads shared by all
+    requests, a page table per request, a free-page stack, and per-(row, kv head) fp16 residual rings."""
+
+    def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, n_pages: int, device="cuda"):
+        self.cfg, self.batch, self.max_seq_len, self.n_pages = cfg, batch, max_seq_len, n_pages
+        H, R = cfg.n_kv_heads, cfg.residual
+        self.page_bytes = kvq.kvq_kivi_page_bytes(cfg)
+        self.pt_stride = (max_seq_len + 127) // 128
+        self.pages = torch.zeros((n_pages, H, self.page_bytes), dtype=torch.uint8, device=device)
+        self.page_table = torch.full((batch, self.pt_stride), -1, dtype=torch.int32, device=device)
+        self.seq_len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.k_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
+        self.v_res = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
+        self.free_pages = torch.empty(n_pages, dtype=torch.int32, device=device)
+        self.top = torch.zeros(4, dtype=torch.int32, device=device)
+        kvq.kv_slot_pool_init(self.pool())
+
+    def pool(self) -> kvq.kvq_slot_pool:
+        return kvq.kvq_slot_pool(self.n_pages, self.free_pages.data_ptr(), self.top.data_ptr())
+
+    def desc(self) -> kvq.kvq_kivi_paged_cache:
+        return kvq.kvq_kivi_paged_cache(self.batch, self.max_seq_len, self.seq_len.data_ptr(),
+                                        self.page_table.data_ptr(), self.n_pages, self.pages.data_ptr(),
+                                        self.k_res.data_ptr(), self.v_res.data_ptr())
+
+    def shuffle_free(self, perm):
+        """Reorder the free stack by a permutation of its entries (host setup), so that later pops hand
+        out scattered pages."""
+        top = int(self.top[0].item())
+        free = self.free_pages[:top].flip(0)
+        idx = torch.as_tensor(perm, dtype=torch.int64, device=free.device)
+        self.free_pages[:top] = free[idx].flip(0)
+
+    def fill(self, b: int, K: torch.Tensor, V: torch.Tensor, stream=None):
+        """Request b from fp16 K, V [Hkv][L][D]: pops ceil(L/128) pages, quantizes every head into them."""
+        cfg = self.cfg
+        H, L = K.shape[0], K.shape[1]
+        assert 1 <= L <= self.max_seq_len and int(self.seq_len[b].item()) == 0
+        G, R = cfg.group_k, cfg.residual
+        npg = (L + 127) // 128
+        top = int(self.top[0].item())
+        assert npg <= top
+        self.page_table[b, :npg] = self.free_pages[top - npg:top].flip(0)
+        self.top[0] = top - npg
+        nkq, nvq = kivi_segments(L, R)
+        d = self.desc()
+        for h in range(H):
+            if nkq:
+                kvq.kv_quant_key_paged(cfg, d, K[h, :nkq].contiguous(), nkq // G, 0, b, h, stream)
+            if nvq:
+                kvq.kv_quant_value_paged(cfg, d, V[h, :nvq].contiguous(), nvq, 0, b, h, stream)
+            _slot_copy(self.k_res[b, h], K[h, nkq:L], [t % R for t in range(nkq, L)])
+            _slot_copy(self.v_res[b, h], V[h, nvq:L], [t % R for t in range(nvq, L)])
+        self.seq_len[b] = L
+
+    def nbytes_read(self, lens) -> int:
+        """Algorithmic bytes of one decode step (as the dense cache: codes, (s, z), fp16 residual)."""
+        cfg = self.cfg
+        tot = 0
+        for L in lens:
+            nkq, nvq = kivi_segments(int(L), cfg.residual)
+            tot += nkq * D * cfg.bits_k // 8 + (nkq // cfg.group_k) * D * 4
+            tot += nvq * D * cfg.bits_v // 8 + nvq * (D // cfg.group_v) * 4
+            tot += (int(L) - nkq + int(L) - nvq) * D * 2
+        return tot * cfg.n_kv_heads
+
+
 class KittyCache:
     def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, device="cuda"):
         self.cfg, self.batch, self.max_seq_len = cfg, batch, max_seq_len

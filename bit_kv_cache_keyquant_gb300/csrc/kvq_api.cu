@@ -63,7 +63,8 @@ kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_se
     // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI and Kitty kernels (4 CTAs per SM)
     // handle all query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
     const bool int8 = variant == KVQ_VARIANT_INT8 || variant == KVQ_VARIANT_INT8_TOKEN;
-    const bool kv_units = int8 || (variant == KVQ_VARIANT_KIVI && kivi_gqa_supported(cfg)) ||
+    const bool kivi = variant == KVQ_VARIANT_KIVI || variant == KVQ_VARIANT_KIVI_PAGED;
+    const bool kv_units = int8 || (kivi && kivi_gqa_supported(cfg)) ||
                           (variant == KVQ_VARIANT_KITTY && kitty_gqa_supported(cfg));
     const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads : rows;
     const int ctas = int8 ? 2 : 4;
@@ -148,6 +149,16 @@ static kvq_status ptrs_ok(std::initializer_list<const void *> ps) {
 
 static kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+static kvq_status check_pool(const kvq_slot_pool *pool) {
+    if (!pool || pool->capacity < 1) return KVQ_ERR_INVALID_ARG;
+    return ptrs_ok({pool->slots, pool->top});
+}
+
+static kvq_status check_kivi_paged_cache(const kvq_kivi_paged_cache *c) {
+    if (!c || c->batch < 1 || c->max_seq_len < 1 || c->n_pages < 1) return KVQ_ERR_INVALID_ARG;
+    return ptrs_ok({c->seq_len, c->page_table, c->pages, c->k_res, c->v_res});
+}
+
 // ---------------------------------------------------------------------------
 // write side
 // ---------------------------------------------------------------------------
@@ -181,6 +192,65 @@ extern "C" kvq_status kv_append_kivi(const kvq_config *cfg, const kvq_kivi_cache
     return cuda_status(launch_append_kivi(cfg, c, k_new, v_new, stream));
 }
 
+extern "C" size_t kvq_kivi_page_bytes(const kvq_config *cfg) {
+    if (check_kivi(cfg)) return 0;
+    return (size_t)kivi_page_bytes(cfg->bits_k, cfg->bits_v);
+}
+
+static kvq_status check_kivi_paged_write(const kvq_config *cfg, const kvq_kivi_paged_cache *c, int64_t n,
+                                         int64_t first, int64_t unit, int32_t row, int32_t kv_head) {
+    kvq_status s = check_kivi(cfg);
+    if (s) return s;
+    if (!c || c->batch < 1 || c->max_seq_len < 1 || c->n_pages < 1) return KVQ_ERR_INVALID_ARG;
+    if (n < 0 || first < 0 || row < 0 || row >= c->batch || kv_head < 0 || kv_head >= cfg->n_kv_heads)
+        return KVQ_ERR_INVALID_ARG;
+    const int64_t row_tokens = ((int64_t)c->max_seq_len + 127) / 128 * 128;
+    if ((first + n) * unit > row_tokens) return KVQ_ERR_INVALID_ARG;
+    return ptrs_ok({c->page_table, c->pages});
+}
+
+extern "C" kvq_status kv_quant_key_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *k,
+                                         int64_t n_groups, int32_t group0, int32_t row, int32_t kv_head,
+                                         cudaStream_t stream) {
+    kvq_status s = check_kivi_paged_write(cfg, c, n_groups, group0, cfg ? cfg->group_k : 1, row, kv_head);
+    if (s) return s;
+    if (n_groups == 0) return KVQ_OK;
+    if ((s = ptrs_ok({k}))) return s;
+    return cuda_status(launch_quant_key_paged(cfg, c, k, n_groups, group0, row, kv_head, stream));
+}
+
+extern "C" kvq_status kv_quant_value_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *v,
+                                           int64_t n_tokens, int32_t tok0, int32_t row, int32_t kv_head,
+                                           cudaStream_t stream) {
+    kvq_status s = check_kivi_paged_write(cfg, c, n_tokens, tok0, 1, row, kv_head);
+    if (s) return s;
+    if (n_tokens == 0) return KVQ_OK;
+    if ((s = ptrs_ok({v}))) return s;
+    return cuda_status(launch_quant_value_paged(cfg, c, v, n_tokens, tok0, row, kv_head, stream));
+}
+
+extern "C" kvq_status kv_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c,
+                                           const kvq_slot_pool *pool, const void *k_new, const void *v_new,
+                                           cudaStream_t stream) {
+    kvq_status s = check_kivi(cfg);
+    if (s) return s;
+    if ((s = check_kivi_paged_cache(c))) return s;
+    if ((s = check_pool(pool))) return s;
+    if ((s = ptrs_ok({k_new, v_new}))) return s;
+    return cuda_status(launch_append_kivi_paged(cfg, c, pool, k_new, v_new, stream));
+}
+
+extern "C" kvq_status kv_release_kivi_paged(const kvq_kivi_paged_cache *c, int32_t row, const kvq_slot_pool *pool,
+                                            cudaStream_t stream) {
+    kvq_status s = check_kivi_paged_cache(c);
+    if (s) return s;
+    if (row < 0 || row >= c->batch) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_pool(pool))) return s;
+    const int stride = (int)(((int64_t)c->max_seq_len + 127) / 128);
+    return cuda_status(launch_release_ids(const_cast<int32_t *>(c->seq_len), c->page_table, row, c->max_seq_len, 128,
+                                          stride, pool, stream));
+}
+
 extern "C" kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new,
                                      const void *v_new, cudaStream_t stream) {
     kvq_status s = check_int8(cfg);
@@ -211,10 +281,6 @@ static kvq_status check_int8_token_cache(const kvq_int8_token_cache *c) {
     return ptrs_ok({c->seq_len, c->slot_table, c->k_codes, c->v_codes, c->k_scale, c->v_scale});
 }
 
-static kvq_status check_pool(const kvq_slot_pool *pool) {
-    if (!pool || pool->capacity < 1) return KVQ_ERR_INVALID_ARG;
-    return ptrs_ok({pool->slots, pool->top});
-}
 
 extern "C" kvq_status kv_quant_int8_token(const kvq_config *cfg, const kvq_int8_token_cache *c, const void *x,
                                           int64_t n, const int32_t *slots, int32_t kv_sel, cudaStream_t stream) {
@@ -306,6 +372,7 @@ extern "C" kvq_status kv_decode_attn_plan(const kvq_config *cfg, int32_t variant
                    : variant == KVQ_VARIANT_KITTY ? check_kitty(cfg)
                    : variant == KVQ_VARIANT_INT8  ? check_int8(cfg)
                    : variant == KVQ_VARIANT_INT8_TOKEN ? check_int8_token(cfg)
+                   : variant == KVQ_VARIANT_KIVI_PAGED ? check_kivi(cfg)
                                                   : KVQ_ERR_INVALID_ARG;
     if (s) return s;
     if (batch < 1 || max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
@@ -333,8 +400,20 @@ static kvq_status stage1_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, co
     if (!c) return KVQ_ERR_INVALID_ARG;
     if ((s = check_ws(cfg, KVQ_VARIANT_KIVI, c->batch, c->max_seq_len, ws, wsb, p))) return s;
     if ((s = ptrs_ok({q, c->seq_len, c->k_codes, c->k_sz, c->v_codes, c->v_sz, c->k_res, c->v_res}))) return s;
-    if (kivi_gqa_supported(cfg)) return cuda_status(launch_decode_kivi_gqa(cfg, c, q, *p, ws, st));
-    return cuda_status(launch_decode_kivi(cfg, c, q, *p, ws, st));
+    if (kivi_gqa_supported(cfg)) return cuda_status(launch_decode_kivi_gqa(cfg, kivi_src(c), q, *p, ws, st));
+    return cuda_status(launch_decode_kivi(cfg, kivi_src(c), q, *p, ws, st));
+}
+
+
+static kvq_status stage1_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *q, void *ws,
+                                    size_t wsb, cudaStream_t st, DecodePlan *p) {
+    kvq_status s = check_kivi(cfg);
+    if (s) return s;
+    if ((s = check_kivi_paged_cache(c))) return s;
+    if ((s = check_ws(cfg, KVQ_VARIANT_KIVI_PAGED, c->batch, c->max_seq_len, ws, wsb, p))) return s;
+    if ((s = ptrs_ok({q}))) return s;
+    if (kivi_gqa_supported(cfg)) return cuda_status(launch_decode_kivi_gqa(cfg, kivi_src(c), q, *p, ws, st));
+    return cuda_status(launch_decode_kivi(cfg, kivi_src(c), q, *p, ws, st));
 }
 
 static kvq_status stage1_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q, void *ws, size_t wsb,
@@ -387,6 +466,9 @@ extern "C" kvq_status kv_decode_attn_stage1(const kvq_config *cfg, int32_t varia
         case KVQ_VARIANT_INT8_TOKEN:
             return stage1_int8_token(cfg, static_cast<const kvq_int8_token_cache *>(cache), q, workspace,
                                      workspace_bytes, stream, &p);
+        case KVQ_VARIANT_KIVI_PAGED:
+            return stage1_kivi_paged(cfg, static_cast<const kvq_kivi_paged_cache *>(cache), q, workspace,
+                                     workspace_bytes, stream, &p);
         default:
             return KVQ_ERR_INVALID_ARG;
     }
@@ -399,6 +481,7 @@ extern "C" kvq_status kv_decode_attn_merge(const kvq_config *cfg, int32_t varian
                    : variant == KVQ_VARIANT_KITTY ? check_kitty(cfg)
                    : variant == KVQ_VARIANT_INT8  ? check_int8(cfg)
                    : variant == KVQ_VARIANT_INT8_TOKEN ? check_int8_token(cfg)
+                   : variant == KVQ_VARIANT_KIVI_PAGED ? check_kivi(cfg)
                                                   : KVQ_ERR_INVALID_ARG;
     if (s) return s;
     DecodePlan p;
@@ -433,6 +516,17 @@ extern "C" kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_
     if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
     DecodePlan p;
     kvq_status s = stage1_int8(cfg, cache, q, workspace, workspace_bytes, stream, &p);
+    if (s) return s;
+    return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
+}
+
+extern "C" kvq_status kv_decode_attn_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *cache,
+                                                const void *q, void *out, void *workspace, size_t workspace_bytes,
+                                                cudaStream_t stream) {
+    if (!out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return KVQ_ERR_MISALIGNED;
+    DecodePlan p;
+    kvq_status s = stage1_kivi_paged(cfg, cache, q, workspace, workspace_bytes, stream, &p);
     if (s) return s;
     return cuda_status(launch_merge(cfg, cache->batch, p, workspace, out, stream));
 }

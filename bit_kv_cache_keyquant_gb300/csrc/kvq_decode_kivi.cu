@@ -296,39 +296,14 @@ static cudaError_t launch_kivi_variant(const Params &P, int64_t grid, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q, const DecodePlan &p,
+cudaError_t launch_decode_kivi(const kvq_config *cfg, const KiviSrc &c, const void *q, const DecodePlan &p,
                                void *ws, cudaStream_t st) {
-    Params P;
-    P.seq_len = c->seq_len;
-    P.k_codes = static_cast<const uint8_t *>(c->k_codes);
-    P.k_sz = static_cast<const uint32_t *>(c->k_sz);
-    P.v_codes = static_cast<const uint8_t *>(c->v_codes);
-    P.v_sz = static_cast<const uint32_t *>(c->v_sz);
-    P.k_res = static_cast<const uint16_t *>(c->k_res);
-    P.v_res = static_cast<const uint16_t *>(c->v_res);
-    P.q = static_cast<const uint16_t *>(q);
-    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
-    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
-    P.err = device_error_ptr();
-    P.B = c->batch;
-    P.Hq = cfg->n_q_heads;
-    P.Hkv = cfg->n_kv_heads;
-    P.G = cfg->group_k;
-    P.Gv = cfg->group_v;
-    P.ngv = KVQ_D / cfg->group_v;
-    P.R = cfg->residual;
-    P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
-    P.splits = p.splits;
-    P.chunk = p.chunk;
-    P.kgrp_cap = P.cap / cfg->group_k;
-    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    Params P = kivi_params(cfg, c, q, p, ws);
     // |alpha q s| < alpha 2^32 (fp16 q and s): 2^(149-E0) alpha 2^32 < 2^127
     P.e0 = 54 + (int)ceilf(log2f(P.alpha));
     if (P.e0 < 22) P.e0 = 22;
-    P.bits_k = cfg->bits_k;
-    P.bits_v = cfg->bits_v;
     if (!P.err) return cudaErrorInvalidDevicePointer;
-    const int64_t n_units = (int64_t)c->batch * cfg->n_q_heads * p.splits;
+    const int64_t n_units = (int64_t)c.batch * cfg->n_q_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
     // the ring holds 4 stages of 12 KiB at 2/2 bits, 3 of 16 KiB at 4/2 or 2/4, 2 of 20 KiB at 4/4

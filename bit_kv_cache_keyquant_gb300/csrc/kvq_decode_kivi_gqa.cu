@@ -361,35 +361,9 @@ bool kivi_gqa_supported(const kvq_config *cfg) {
     return g >= 2 && g <= GMAX && cfg->bits_k == 2 && cfg->bits_v == 2;
 }
 
-cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q, const DecodePlan &p,
+cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, const void *q, const DecodePlan &p,
                                    void *ws, cudaStream_t st) {
-    Params P;
-    P.seq_len = c->seq_len;
-    P.k_codes = static_cast<const uint8_t *>(c->k_codes);
-    P.k_sz = static_cast<const uint32_t *>(c->k_sz);
-    P.v_codes = static_cast<const uint8_t *>(c->v_codes);
-    P.v_sz = static_cast<const uint32_t *>(c->v_sz);
-    P.k_res = static_cast<const uint16_t *>(c->k_res);
-    P.v_res = static_cast<const uint16_t *>(c->v_res);
-    P.q = static_cast<const uint16_t *>(q);
-    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
-    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
-    P.err = device_error_ptr();
-    P.B = c->batch;
-    P.Hq = cfg->n_q_heads;
-    P.Hkv = cfg->n_kv_heads;
-    P.G = cfg->group_k;
-    P.Gv = cfg->group_v;
-    P.ngv = KVQ_D / cfg->group_v;
-    P.R = cfg->residual;
-    P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
-    P.splits = p.splits;
-    P.chunk = p.chunk;
-    P.kgrp_cap = P.cap / cfg->group_k;
-    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
-    P.e0 = 0;
-    P.bits_k = 2;
-    P.bits_v = 2;
+    Params P = kivi_params(cfg, c, q, p, ws);
     if (!P.err) return cudaErrorInvalidDevicePointer;
     const size_t smem = sizeof(SmemG);
     const int ngv = P.ngv;
@@ -407,7 +381,7 @@ cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *
         if (e != cudaSuccess) return e;
         attr_dev[ti] = dev;
     }
-    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
+    const int64_t n_units = (int64_t)c.batch * cfg->n_kv_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
     if (ngv == 4) kivi_decode_gqa_kernel<4><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);

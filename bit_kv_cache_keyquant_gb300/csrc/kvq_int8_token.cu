@@ -117,9 +117,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total)
     return r;
 }
 
+// Rows b with 0 <= L = seq_len[b] < cap and L % unit == 0 take one id each
+// (token slots: unit 1; pages of 128 tokens: unit 128) for table[b][L / unit].
 __global__ void __launch_bounds__(1024) slot_alloc_kernel(const int32_t *__restrict__ seq_len,
-                                                          int32_t *__restrict__ table, int B, int cap,
-                                                          const int32_t *__restrict__ free_slots,
+                                                          int32_t *__restrict__ table, int B, int cap, int unit,
+                                                          int stride, const int32_t *__restrict__ free_slots,
                                                           int32_t *__restrict__ top, int capacity,
                                                           unsigned *err) {
     __shared__ int warp_tot[33];
@@ -130,7 +132,7 @@ __global__ void __launch_bounds__(1024) slot_alloc_kernel(const int32_t *__restr
     bool full = false;
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int L = seq_len[b];
-        if (L >= 0 && L < cap) ++cnt;
+        if (L >= 0 && L < cap) cnt += L % unit == 0 ? 1 : 0;
         else full = true;
     }
     if (full) atomicOr(err, KVQ_DEVICE_ERR_CAPACITY);
@@ -144,10 +146,10 @@ __global__ void __launch_bounds__(1024) slot_alloc_kernel(const int32_t *__restr
     for (int c0 = 0; c0 < B; c0 += blockDim.x) {
         const int b = c0 + threadIdx.x;
         const int L = b < B ? seq_len[b] : -1;
-        const int f = (L >= 0 && L < cap) ? 1 : 0;
+        const int f = (L >= 0 && L < cap && L % unit == 0) ? 1 : 0;
         int tot;
         const int r = block_excl_scan(f, warp_tot, tot) + base;
-        if (f) table[(int64_t)b * cap + L] = fail ? -1 : free_slots[t0 - 1 - r];
+        if (f) table[(int64_t)b * stride + L / unit] = fail ? -1 : free_slots[t0 - 1 - r];
         base += tot;
     }
     __syncthreads();
@@ -187,17 +189,19 @@ __global__ void __launch_bounds__(256) append_int8_token_kernel(AppendT P) {
     if (threadIdx.x == 0) P.seq_len[b] = L + 1;
 }
 
+// Push the ids of request `row` (table[row][0 .. ceil(seq_len[row] / unit))) back.
 __global__ void __launch_bounds__(1024) slot_release_kernel(int32_t *__restrict__ seq_len,
                                                             const int32_t *__restrict__ table, int row, int cap,
-                                                            int32_t *__restrict__ free_slots,
+                                                            int unit, int stride, int32_t *__restrict__ free_slots,
                                                             int32_t *__restrict__ top, int capacity, unsigned *err) {
-    const int n = seq_len[row];
+    const int L = seq_len[row];
+    const int n = L >= 0 && L <= cap ? (L + unit - 1) / unit : -1;
     const int t0 = *top;
-    if (n < 0 || n > cap || t0 < 0 || t0 + n > capacity) {
+    if (n < 0 || t0 < 0 || t0 + n > capacity) {
         if (threadIdx.x == 0) atomicOr(err, KVQ_DEVICE_ERR_POOL);
         return;
     }
-    for (int i = threadIdx.x; i < n; i += blockDim.x) free_slots[t0 + i] = table[(int64_t)row * cap + i];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) free_slots[t0 + i] = table[(int64_t)row * stride + i];
     __syncthreads();
     if (threadIdx.x == 0) {
         *top = t0 + n;
@@ -252,9 +256,7 @@ cudaError_t launch_append_int8_token(const kvq_config *cfg, const kvq_int8_token
     if (!err) return cudaErrorInvalidDevicePointer;
     int32_t *table = const_cast<int32_t *>(c->slot_table);
     int32_t *seq_len = const_cast<int32_t *>(c->seq_len);
-    slot_alloc_kernel<<<1, 1024, 0, st>>>(seq_len, table, c->batch, c->max_seq_len, pool->slots, pool->top,
-                                          pool->capacity, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_alloc_ids(seq_len, table, c->batch, c->max_seq_len, 1, c->max_seq_len, pool, st);
     if (e != cudaSuccess) return e;
     AppendT P;
     P.seq_len = seq_len;
@@ -281,10 +283,25 @@ cudaError_t launch_append_int8_token(const kvq_config *cfg, const kvq_int8_token
 
 cudaError_t launch_release_int8_token(const kvq_int8_token_cache *c, int row, const kvq_slot_pool *pool,
                                       cudaStream_t st) {
+    return launch_release_ids(const_cast<int32_t *>(c->seq_len), c->slot_table, row, c->max_seq_len, 1,
+                              c->max_seq_len, pool, st);
+}
+
+cudaError_t launch_alloc_ids(const int32_t *seq_len, int32_t *table, int batch, int cap, int unit, int stride,
+                             const kvq_slot_pool *pool, cudaStream_t st) {
     unsigned *err = device_error_ptr();
     if (!err) return cudaErrorInvalidDevicePointer;
-    slot_release_kernel<<<1, 1024, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->slot_table, row, c->max_seq_len,
-                                            pool->slots, pool->top, pool->capacity, err);
+    slot_alloc_kernel<<<1, 1024, 0, st>>>(seq_len, table, batch, cap, unit, stride, pool->slots, pool->top,
+                                          pool->capacity, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_release_ids(int32_t *seq_len, const int32_t *table, int row, int cap, int unit, int stride,
+                               const kvq_slot_pool *pool, cudaStream_t st) {
+    unsigned *err = device_error_ptr();
+    if (!err) return cudaErrorInvalidDevicePointer;
+    slot_release_kernel<<<1, 1024, 0, st>>>(seq_len, table, row, cap, unit, stride, pool->slots, pool->top,
+                                            pool->capacity, err);
     return cudaGetLastError();
 }
 

@@ -16,6 +16,50 @@ struct DecodePlan {
     size_t off_lse;    // byte offset of lse_s fp32 [B][Hq][splits]
 };
 
+// A dense or a paged KIVI cache as the decode kernels read it: dense caches
+// set the four code / parameter arrays, paged caches the page table and pool.
+struct KiviSrc {
+    int batch = 0, max_seq_len = 0;
+    const int32_t *seq_len = nullptr;
+    const void *k_codes = nullptr, *k_sz = nullptr, *v_codes = nullptr, *v_sz = nullptr;
+    const int32_t *page_table = nullptr;
+    const void *pages = nullptr;
+    int n_pages = 0;
+    const void *k_res = nullptr, *v_res = nullptr;
+};
+
+inline KiviSrc kivi_src(const kvq_kivi_cache *c) {
+    KiviSrc s;
+    s.batch = c->batch;
+    s.max_seq_len = c->max_seq_len;
+    s.seq_len = c->seq_len;
+    s.k_codes = c->k_codes;
+    s.k_sz = c->k_sz;
+    s.v_codes = c->v_codes;
+    s.v_sz = c->v_sz;
+    s.k_res = c->k_res;
+    s.v_res = c->v_res;
+    return s;
+}
+
+inline KiviSrc kivi_src(const kvq_kivi_paged_cache *c) {
+    KiviSrc s;
+    s.batch = c->batch;
+    s.max_seq_len = c->max_seq_len;
+    s.seq_len = c->seq_len;
+    s.page_table = c->page_table;
+    s.pages = c->pages;
+    s.n_pages = c->n_pages;
+    s.k_res = c->k_res;
+    s.v_res = c->v_res;
+    return s;
+}
+
+// bytes of one paged KIVI page record: key codes, key (s, z), value codes, value (s, z) of 128 tokens
+inline int64_t kivi_page_bytes(int bits_k, int bits_v) {
+    return 16LL * 128 * bits_k + 2048 + 16LL * 128 * bits_v + 2048;   // D = 128
+}
+
 int num_sms();
 unsigned *device_error_ptr();   // device address of the error bitmask (current device)
 
@@ -41,11 +85,11 @@ cudaError_t launch_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, c
                                cudaStream_t st);
 cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new, const void *v_new,
                                 int score_mode, cudaStream_t st);
-cudaError_t launch_decode_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q,
+cudaError_t launch_decode_kivi(const kvq_config *cfg, const KiviSrc &c, const void *q,
                                const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query KIVI decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
 bool kivi_gqa_supported(const kvq_config *cfg);
-cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const kvq_kivi_cache *c, const void *q,
+cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, const void *q,
                                    const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query Kitty decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
 bool kitty_gqa_supported(const kvq_config *cfg);
@@ -64,6 +108,19 @@ cudaError_t launch_append_int8_token(const kvq_config *cfg, const kvq_int8_token
                                      const void *k_new, const void *v_new, cudaStream_t st);
 cudaError_t launch_release_int8_token(const kvq_int8_token_cache *c, int row, const kvq_slot_pool *pool,
                                       cudaStream_t st);
+// paged KIVI write side
+cudaError_t launch_quant_key_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *k, int64_t n,
+                                   int group0, int row, int kvh, cudaStream_t st);
+cudaError_t launch_quant_value_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *v, int64_t n,
+                                     int tok0, int row, int kvh, cudaStream_t st);
+cudaError_t launch_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const kvq_slot_pool *pool,
+                                     const void *k_new, const void *v_new, cudaStream_t st);
+// free-id stack (token slots: unit 1; pages: unit 128): rows with seq_len % unit == 0 take an id for
+// table[b][seq_len / unit]; release pushes table[row][0 .. ceil(seq_len / unit)) back
+cudaError_t launch_alloc_ids(const int32_t *seq_len, int32_t *table, int batch, int cap, int unit, int stride,
+                             const kvq_slot_pool *pool, cudaStream_t st);
+cudaError_t launch_release_ids(int32_t *seq_len, const int32_t *table, int row, int cap, int unit, int stride,
+                               const kvq_slot_pool *pool, cudaStream_t st);
 cudaError_t launch_merge(const kvq_config *cfg, int batch, const DecodePlan &p, const void *ws, void *out,
                          cudaStream_t st);
 

@@ -48,6 +48,13 @@ struct Params {
     float alpha;
     int e0;             // key products are scaled by 2^-E0
     int bits_k, bits_v; // code widths (2 or 4)
+    // paged cache (page_table non-null): token t of row b is in page record
+    // pages + (page_table[b * pt_stride + t / 128] * Hkv + kv head) * rec_bytes
+    const int32_t *page_table;
+    const uint8_t *pages;
+    int pt_stride, n_pages;
+    int64_t rec_bytes;
+    int kc_bytes, vc_bytes;   // page record sections: key codes, key (s, z) (2048 B), value codes, value (s, z)
 };
 
 // Geometry of one work unit.  Splits 0 .. splits-2 of a (batch row, query
@@ -55,7 +62,7 @@ struct Params {
 // covers every remaining token [Qf, L) (the fp16 residual and any tokens cut
 // off by a segment boundary), read straight from global memory.
 struct Unit {
-    int b, hq, split, t0, t1, nT, nstages, nKq, nVq;
+    int b, hq, kvh, split, t0, t1, nT, nstages, nKq, nVq;
     bool residual;
     int64_t bk;
 };
@@ -97,8 +104,20 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
         U.nT = (U.t1 - U.t0) / 32;
     }
     U.nstages = (U.nT + NCWARP - 1) / NCWARP;
-    U.bk = (int64_t)U.b * P.Hkv + (hpr == P.Hkv ? U.hq : U.hq / (P.Hq / P.Hkv));
+    U.kvh = hpr == P.Hkv ? U.hq : U.hq / (P.Hq / P.Hkv);
+    U.bk = (int64_t)U.b * P.Hkv + U.kvh;
     return U;
+}
+
+// Page record holding token t of the unit's (row, kv head) in a paged cache;
+// a table entry outside the pool reads page 0 and records KVQ_DEVICE_ERR_POOL.
+__device__ __forceinline__ const uint8_t *kivi_page(const Params &P, const Unit &U, int t) {
+    int pg = P.page_table[(int64_t)U.b * P.pt_stride + (t >> 7)];
+    if (pg < 0 || pg >= P.n_pages) {
+        atomicOr(P.err, KVQ_DEVICE_ERR_POOL);
+        pg = 0;
+    }
+    return P.pages + ((int64_t)pg * P.Hkv + U.kvh) * P.rec_bytes;
 }
 
 // KIVI key storage (see kv_quant_key): token t = q + 8p, channel c = 16k + cc
@@ -131,8 +150,17 @@ __device__ __forceinline__ void fetch_k4(const Params &P, const Unit &U, int t, 
     if (t < U.nKq) {
         const int G = P.G, gi = t / G, tt = t - gi * G;
         const int bits = P.bits_k;
-        const uint8_t *grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D * bits / 8);
-        const uint16_t *szb = reinterpret_cast<const uint16_t *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D);
+        const uint8_t *grp;
+        const uint16_t *szb;
+        if (P.page_table) {
+            const uint8_t *rec = kivi_page(P, U, t);
+            const int gp = (t & 127) / G;                       // group within the page
+            grp = rec + gp * (G * KVQ_D * bits / 8);
+            szb = reinterpret_cast<const uint16_t *>(rec + P.kc_bytes + gp * 512);
+        } else {
+            grp = P.k_codes + (U.bk * P.kgrp_cap + gi) * ((int64_t)G * KVQ_D * bits / 8);
+            szb = reinterpret_cast<const uint16_t *>(P.k_sz + (U.bk * P.kgrp_cap + gi) * KVQ_D);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int c = 4 * lane + i, si = kivi_sz_index(c);
@@ -149,9 +177,19 @@ __device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, 
     if (t < U.nVq) {
         // the lane's 4 channels: one byte at 2 bits, two at 4 bits (channel c at bits bits*(c % (8/bits)))
         const int bits = P.bits_v;
-        const uint8_t *tb = P.v_codes + (U.bk * P.cap + t) * (KVQ_D * bits / 8);
+        const uint8_t *tb;
+        const uint32_t *szr;
+        if (P.page_table) {
+            const uint8_t *rec = kivi_page(P, U, t);
+            const int tp = t & 127;
+            tb = rec + P.kc_bytes + 2048 + tp * (KVQ_D * bits / 8);
+            szr = reinterpret_cast<const uint32_t *>(rec + P.kc_bytes + 2048 + P.vc_bytes) + tp * P.ngv;
+        } else {
+            tb = P.v_codes + (U.bk * P.cap + t) * (KVQ_D * bits / 8);
+            szr = P.v_sz + (U.bk * P.cap + t) * P.ngv;
+        }
         const uint32_t w = bits == 2 ? (uint32_t)tb[lane] : (uint32_t)reinterpret_cast<const uint16_t *>(tb)[lane];
-        const uint32_t sz = P.v_sz[(U.bk * P.cap + t) * P.ngv + (4 * lane) / P.Gv];
+        const uint32_t sz = szr[(4 * lane) / P.Gv];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             vv[i] = (float)((w >> (bits * i)) & ((1u << bits) - 1)) * h2f(lo16(sz)) + h2f(hi16(sz));
@@ -282,6 +320,12 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
             const uint32_t vc_b = nt * 32 * (KVQ_D * BV / 8);
             const uint32_t vsz_b = nt * 32 * P.ngv * 4;
             uint8_t *st = stage[slot];
+            if (P.page_table) {
+                // the page record is the stage: one copy (the tiles past nt are not read)
+                mbar_expect_tx(&full[slot], (uint32_t)GG::BYTES);
+                bulk_g2s(st, kivi_page(P, U, tok), (uint32_t)GG::BYTES, &full[slot]);
+                continue;
+            }
             mbar_expect_tx(&full[slot], kc_b + ksz_b + vc_b + vsz_b);
             bulk_g2s(st, kc_base + (int64_t)(tok >> 5) * 512 * BK, kc_b, &full[slot]);
             bulk_g2s(st + GG::KC, ksz_base + (int64_t)(tok / G) * KVQ_D, ksz_b, &full[slot]);
@@ -291,6 +335,45 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
     }
     // drain: every issued stage must have landed before the CTA exits
     for (int s = max(0, sg - NST); s < sg; ++s) mbar_wait(&full[s % NST], (s / NST) & 1, P.err);
+}
+
+// Kernel parameters common to the KIVI decode kernels, from a dense or paged cache.
+inline Params kivi_params(const kvq_config *cfg, const KiviSrc &c, const void *q, const DecodePlan &p, void *ws) {
+    Params P;
+    P.seq_len = c.seq_len;
+    P.k_codes = static_cast<const uint8_t *>(c.k_codes);
+    P.k_sz = static_cast<const uint32_t *>(c.k_sz);
+    P.v_codes = static_cast<const uint8_t *>(c.v_codes);
+    P.v_sz = static_cast<const uint32_t *>(c.v_sz);
+    P.k_res = static_cast<const uint16_t *>(c.k_res);
+    P.v_res = static_cast<const uint16_t *>(c.v_res);
+    P.q = static_cast<const uint16_t *>(q);
+    P.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_o);
+    P.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + p.off_lse);
+    P.err = device_error_ptr();
+    P.B = c.batch;
+    P.Hq = cfg->n_q_heads;
+    P.Hkv = cfg->n_kv_heads;
+    P.G = cfg->group_k;
+    P.Gv = cfg->group_v;
+    P.ngv = KVQ_D / cfg->group_v;
+    P.R = cfg->residual;
+    P.cap = ((int64_t)c.max_seq_len + 127) / 128 * 128;
+    P.splits = p.splits;
+    P.chunk = p.chunk;
+    P.kgrp_cap = P.cap / cfg->group_k;
+    P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
+    P.e0 = 0;
+    P.bits_k = cfg->bits_k;
+    P.bits_v = cfg->bits_v;
+    P.page_table = c.page_table;
+    P.pages = static_cast<const uint8_t *>(c.pages);
+    P.pt_stride = (int)(P.cap / 128);
+    P.n_pages = c.n_pages;
+    P.rec_bytes = kivi_page_bytes(cfg->bits_k, cfg->bits_v);
+    P.kc_bytes = 16 * KVQ_D * cfg->bits_k;
+    P.vc_bytes = 16 * KVQ_D * cfg->bits_v;
+    return P;
 }
 
 }  // namespace

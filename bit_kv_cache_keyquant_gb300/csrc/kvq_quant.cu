@@ -583,6 +583,216 @@ cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
 }
 
 // ---------------------------------------------------------------------------
+// Paged KIVI: a page record holds 128 tokens of one kv head in decode-stage
+// order (key codes, key (s, z) 2048 B, value codes, value (s, z) 2048 B).
+// The write side quantizes with the same device functions as the dense
+// cache and only addresses through the page table.
+// ---------------------------------------------------------------------------
+struct PagedDst {
+    const int32_t *page_table;
+    uint8_t *pages;
+    int pt_stride, n_pages, Hkv;
+    int64_t rec_bytes;
+    int kc_bytes, vc_bytes;
+    unsigned *err;
+};
+
+// Record of logical page lp of row b, kv head h; null (KVQ_DEVICE_ERR_POOL
+// recorded) when the table entry is outside the pool.
+__device__ __forceinline__ uint8_t *paged_record(const PagedDst &D, int b, int lp, int h) {
+    const int pg = D.page_table[(int64_t)b * D.pt_stride + lp];
+    if (pg < 0 || pg >= D.n_pages) {
+        if (threadIdx.x == 0) atomicOr(D.err, KVQ_DEVICE_ERR_POOL);
+        return nullptr;
+    }
+    return D.pages + ((int64_t)pg * D.Hkv + h) * D.rec_bytes;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(128) quant_key_paged_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
+                                                              int group0, int row, int kvh, PagedDst D, int bits) {
+    const int64_t g = blockIdx.x;
+    if (g >= n_groups) return;
+    constexpr int G = 32 * NT;
+    const int gl = group0 + (int)g;
+    uint8_t *rec = paged_record(D, row, gl * G / 128, kvh);
+    if (!rec) return;
+    const int gp = gl % (128 / G);
+    key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, rec + gp * (G * KVQ_D * bits / 8),
+                        reinterpret_cast<uint16_t *>(rec + D.kc_bytes + gp * 512), bits);
+}
+
+// value token tg of the row (fp16 src) into its page record, by one warp
+template <int GV>
+__device__ __forceinline__ void value_token_paged(const uint16_t *__restrict__ src, uint8_t *rec, int tg,
+                                                  const PagedDst &D, int ngv, int lane, int bits) {
+    constexpr int LG = GV / 4;
+    uint32_t wv;
+    uint16_t s, z;
+    value_token_quant<GV>(src, lane, wv, s, z, bits);
+    const int tp = tg & 127;
+    value_token_store(rec + D.kc_bytes + 2048 + tp * (KVQ_D * bits / 8), lane, wv, bits);
+    if ((lane % LG) == 0)
+        reinterpret_cast<uint32_t *>(rec + D.kc_bytes + 2048 + D.vc_bytes)[tp * ngv + lane / LG] =
+            (uint32_t)s | ((uint32_t)z << 16);
+}
+
+template <int GV>
+__global__ void __launch_bounds__(256) quant_value_paged_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
+                                                                int tok0, int row, int kvh, PagedDst D, int ngv,
+                                                                int bits) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tokens; t += nwarps) {
+        const int tg = tok0 + (int)t;
+        const int pg = D.page_table[(int64_t)row * D.pt_stride + (tg >> 7)];
+        if (pg < 0 || pg >= D.n_pages) {
+            if (lane == 0) atomicOr(D.err, KVQ_DEVICE_ERR_POOL);
+            continue;
+        }
+        value_token_paged<GV>(v + t * KVQ_D, D.pages + ((int64_t)pg * D.Hkv + kvh) * D.rec_bytes, tg, D, ngv, lane,
+                              bits);
+    }
+}
+
+static PagedDst paged_dst(const kvq_config *cfg, const kvq_kivi_paged_cache *c) {
+    PagedDst D;
+    D.page_table = c->page_table;
+    D.pages = static_cast<uint8_t *>(const_cast<void *>(c->pages));
+    D.pt_stride = (int)(((int64_t)c->max_seq_len + 127) / 128);
+    D.n_pages = c->n_pages;
+    D.Hkv = cfg->n_kv_heads;
+    D.rec_bytes = kivi_page_bytes(cfg->bits_k, cfg->bits_v);
+    D.kc_bytes = 16 * KVQ_D * cfg->bits_k;
+    D.vc_bytes = 16 * KVQ_D * cfg->bits_v;
+    D.err = device_error_ptr();
+    return D;
+}
+
+cudaError_t launch_quant_key_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *k, int64_t n,
+                                   int group0, int row, int kvh, cudaStream_t st) {
+    const PagedDst D = paged_dst(cfg, c);
+    if (!D.err) return cudaErrorInvalidDevicePointer;
+    const uint16_t *kp = static_cast<const uint16_t *>(k);
+    const int G = cfg->group_k, bits = cfg->bits_k;
+    if (G == 32) quant_key_paged_kernel<1><<<(unsigned)n, 128, 0, st>>>(kp, n, group0, row, kvh, D, bits);
+    else if (G == 64) quant_key_paged_kernel<2><<<(unsigned)n, 128, 0, st>>>(kp, n, group0, row, kvh, D, bits);
+    else quant_key_paged_kernel<4><<<(unsigned)n, 128, 0, st>>>(kp, n, group0, row, kvh, D, bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_value_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *v, int64_t n,
+                                     int tok0, int row, int kvh, cudaStream_t st) {
+    const PagedDst D = paged_dst(cfg, c);
+    if (!D.err) return cudaErrorInvalidDevicePointer;
+    const uint16_t *vp = static_cast<const uint16_t *>(v);
+    int64_t grid = (n + 7) / 8;
+    if (grid > (int64_t)num_sms() * 16) grid = (int64_t)num_sms() * 16;
+    const int ngv = KVQ_D / cfg->group_v, bits = cfg->bits_v;
+    switch (cfg->group_v) {
+        case 32: quant_value_paged_kernel<32><<<(unsigned)grid, 256, 0, st>>>(vp, n, tok0, row, kvh, D, ngv, bits); break;
+        case 64: quant_value_paged_kernel<64><<<(unsigned)grid, 256, 0, st>>>(vp, n, tok0, row, kvh, D, ngv, bits); break;
+        default: quant_value_paged_kernel<128><<<(unsigned)grid, 256, 0, st>>>(vp, n, tok0, row, kvh, D, ngv, bits); break;
+    }
+    return cudaGetLastError();
+}
+
+// Streaming append into a paged cache: as append_kivi_kernel, with the key
+// groups and the value token written into the row's page records.  A row
+// whose new page could not be allocated (table entry -1) is left unchanged.
+template <int NT, int GV>
+__global__ void __launch_bounds__(128) append_kivi_paged_kernel(AppendParams P, PagedDst D) {
+    const int64_t bk = blockIdx.x;
+    const int b = (int)(bk / P.Hkv), h = (int)(bk % P.Hkv);
+    const int L = P.seq_len[b];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (L < 0 || L >= P.max_seq_len) return;                // the allocator recorded the capacity error
+    if ((L & 127) == 0 && D.page_table[(int64_t)b * D.pt_stride + (L >> 7)] < 0) return;
+    constexpr int G = 32 * NT;
+    const uint16_t *kres = P.k_res + bk * P.R * KVQ_D;
+    const uint16_t *vres = P.v_res + bk * P.R * KVQ_D;
+    if (L > 0 && L % P.R == 0) {
+        for (int g = 0; g < P.R / G; ++g) {
+            const int gl = (L - P.R) / G + g;
+            uint8_t *rec = paged_record(D, b, gl * G / 128, h);
+            if (!rec) continue;
+            const int gp = gl % (128 / G);
+            key_group_quant<NT>(kres + (int64_t)g * G * KVQ_D, rec + gp * (G * KVQ_D * P.bits_k / 8),
+                                reinterpret_cast<uint16_t *>(rec + D.kc_bytes + gp * 512), P.bits_k);
+        }
+    }
+    if (L >= P.R && warp == 0) {
+        const int t = L - P.R;
+        const int pg = D.page_table[(int64_t)b * D.pt_stride + (t >> 7)];
+        if (pg >= 0 && pg < D.n_pages)
+            value_token_paged<GV>(vres + (int64_t)(t % P.R) * KVQ_D, D.pages + ((int64_t)pg * D.Hkv + h) * D.rec_bytes,
+                                  t, D, P.ngv, lane, P.bits_v);
+        else if (lane == 0)
+            atomicOr(D.err, KVQ_DEVICE_ERR_POOL);
+    }
+    __syncthreads();   // every read of the ring slot about to be overwritten is done
+    const int64_t slot = L % P.R;
+    if (threadIdx.x < 16) {
+        reinterpret_cast<uint4 *>(P.k_res + (bk * P.R + slot) * KVQ_D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(P.k_new + bk * KVQ_D)[threadIdx.x];
+    } else if (threadIdx.x < 32) {
+        reinterpret_cast<uint4 *>(P.v_res + (bk * P.R + slot) * KVQ_D)[threadIdx.x - 16] =
+            reinterpret_cast<const uint4 *>(P.v_new + bk * KVQ_D)[threadIdx.x - 16];
+    }
+}
+
+__global__ void append_bump_paged_kernel(int32_t *seq_len, const int32_t *table, int stride, int B, int max_seq_len) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int L = seq_len[b];
+    if (L < 0 || L >= max_seq_len) return;
+    if ((L & 127) == 0 && table[(int64_t)b * stride + (L >> 7)] < 0) return;
+    seq_len[b] = L + 1;
+}
+
+cudaError_t launch_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const kvq_slot_pool *pool,
+                                     const void *k_new, const void *v_new, cudaStream_t st) {
+    const PagedDst D = paged_dst(cfg, c);
+    if (!D.err) return cudaErrorInvalidDevicePointer;
+    int32_t *seq_len = const_cast<int32_t *>(c->seq_len);
+    cudaError_t e = launch_alloc_ids(seq_len, const_cast<int32_t *>(c->page_table), c->batch, c->max_seq_len, 128,
+                                     D.pt_stride, pool, st);
+    if (e != cudaSuccess) return e;
+    AppendParams P;
+    P.seq_len = c->seq_len;
+    P.k_new = static_cast<const uint16_t *>(k_new);
+    P.v_new = static_cast<const uint16_t *>(v_new);
+    P.k_codes = nullptr;
+    P.v_codes = nullptr;
+    P.k_sz = nullptr;
+    P.v_sz = nullptr;
+    P.k_res = static_cast<uint16_t *>(const_cast<void *>(c->k_res));
+    P.v_res = static_cast<uint16_t *>(const_cast<void *>(c->v_res));
+    P.err = D.err;
+    P.Hkv = cfg->n_kv_heads;
+    P.R = cfg->residual;
+    P.G = cfg->group_k;
+    P.ngv = KVQ_D / cfg->group_v;
+    P.bits_k = cfg->bits_k;
+    P.bits_v = cfg->bits_v;
+    P.max_seq_len = c->max_seq_len;
+    P.cap = 0;
+    P.kgrp_cap = 0;
+    const int64_t grid = (int64_t)c->batch * cfg->n_kv_heads;
+#define KVQ_APPEND_PAGED(NT, GV) append_kivi_paged_kernel<NT, GV><<<(unsigned)grid, 128, 0, st>>>(P, D)
+    const int G = cfg->group_k, GV = cfg->group_v;
+    if (G == 32) { if (GV == 32) KVQ_APPEND_PAGED(1, 32); else if (GV == 64) KVQ_APPEND_PAGED(1, 64); else KVQ_APPEND_PAGED(1, 128); }
+    else if (G == 64) { if (GV == 32) KVQ_APPEND_PAGED(2, 32); else if (GV == 64) KVQ_APPEND_PAGED(2, 64); else KVQ_APPEND_PAGED(2, 128); }
+    else { if (GV == 32) KVQ_APPEND_PAGED(4, 32); else if (GV == 64) KVQ_APPEND_PAGED(4, 64); else KVQ_APPEND_PAGED(4, 128); }
+#undef KVQ_APPEND_PAGED
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    append_bump_paged_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(seq_len, c->page_table, D.pt_stride, c->batch,
+                                                                      c->max_seq_len);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Streaming append (INT8): one CTA of 256 threads per (batch row, kv head).
 // With L = seq_len[b] cached: when L is a positive multiple of T the fp16
 // tail [L-T, L) (ring slots 0..T-1) becomes the INT8 block (L-T)/T of K and V

@@ -15,7 +15,7 @@ from . import build as _build
 _LIB_PATH = _build.LIB
 
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_MISALIGNED, KVQ_ERR_CUDA, KVQ_ERR_WORKSPACE = range(6)
-KVQ_VARIANT_KIVI, KVQ_VARIANT_KITTY, KVQ_VARIANT_INT8, KVQ_VARIANT_INT8_TOKEN = 0, 1, 2, 3
+KVQ_VARIANT_KIVI, KVQ_VARIANT_KITTY, KVQ_VARIANT_INT8, KVQ_VARIANT_INT8_TOKEN, KVQ_VARIANT_KIVI_PAGED = 0, 1, 2, 3, 4
 KVQ_DEVICE_ERR_WAIT_TIMEOUT = 1
 KVQ_DEVICE_ERR_CAPACITY = 2
 KVQ_DEVICE_ERR_POOL = 4
@@ -41,6 +41,11 @@ _P = ctypes.c_void_p
 class kvq_kivi_cache(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("seq_len", _P),
                 ("k_codes", _P), ("k_sz", _P), ("v_codes", _P), ("v_sz", _P), ("k_res", _P), ("v_res", _P)]
+
+
+class kvq_kivi_paged_cache(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("seq_len", _P), ("page_table", _P),
+                ("n_pages", ctypes.c_int32), ("pages", _P), ("k_res", _P), ("v_res", _P)]
 
 
 class kvq_kitty_cache(ctypes.Structure):
@@ -79,6 +84,13 @@ def _load():
         "kv_append_kivi": (S, [cfgp, ctypes.POINTER(kvq_kivi_cache), _P, _P, _P]),
         "kv_append_int8": (S, [cfgp, ctypes.POINTER(kvq_int8_cache), _P, _P, _P]),
         "kv_append_kitty": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), _P, _P, i32, _P]),
+        "kvq_kivi_page_bytes": (sz, [cfgp]),
+        "kv_quant_key_paged": (S, [cfgp, ctypes.POINTER(kvq_kivi_paged_cache), _P, i64, i32, i32, i32, _P]),
+        "kv_quant_value_paged": (S, [cfgp, ctypes.POINTER(kvq_kivi_paged_cache), _P, i64, i32, i32, i32, _P]),
+        "kv_append_kivi_paged": (S, [cfgp, ctypes.POINTER(kvq_kivi_paged_cache), ctypes.POINTER(kvq_slot_pool), _P,
+                                     _P, _P]),
+        "kv_release_kivi_paged": (S, [ctypes.POINTER(kvq_kivi_paged_cache), i32, ctypes.POINTER(kvq_slot_pool), _P]),
+        "kv_decode_attn_kivi_paged": (S, [cfgp, ctypes.POINTER(kvq_kivi_paged_cache), _P, _P, _P, sz, _P]),
         "kv_quant_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), _P, i64, _P, i32, _P]),
         "kv_slot_pool_init": (S, [ctypes.POINTER(kvq_slot_pool), _P]),
         "kv_append_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), ctypes.POINTER(kvq_slot_pool), _P,
@@ -113,7 +125,9 @@ _lib = _load()
 
 EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_append_int8", "kv_append_kitty",
             "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither", "kv_quant_int8_token",
-            "kv_slot_pool_init", "kv_append_int8_token", "kv_release_int8_token",
+            "kv_slot_pool_init", "kv_append_int8_token", "kv_release_int8_token", "kvq_kivi_page_bytes",
+            "kv_quant_key_paged", "kv_quant_value_paged", "kv_append_kivi_paged", "kv_release_kivi_paged",
+            "kv_decode_attn_kivi_paged",
             "kvq_kitty_key_page_bytes", "kvq_kitty_value_page_bytes", "kv_decode_attn_plan", "kv_decode_attn",
             "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_int8_token", "kv_decode_attn_noalloc",
             "kv_decode_attn_stage1", "kv_decode_attn_merge",
@@ -192,6 +206,36 @@ def kv_append_kitty(cfg, cache, k_new, v_new, score_mode=0, stream=None):
     """Append one token per (batch row, kv head) to a Kitty cache: k_new, v_new fp16 [B][Hkv][D]."""
     _check(_lib.kv_append_kitty(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new), score_mode,
                                 _stream(stream)), "kv_append_kitty")
+
+
+def kvq_kivi_page_bytes(cfg) -> int:
+    return int(_lib.kvq_kivi_page_bytes(ctypes.byref(cfg)))
+
+
+def kv_quant_key_paged(cfg, cache, k, n_groups, group0, row, kv_head, stream=None):
+    _check(_lib.kv_quant_key_paged(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k), n_groups, group0, row, kv_head,
+                                   _stream(stream)), "kv_quant_key_paged")
+
+
+def kv_quant_value_paged(cfg, cache, v, n_tokens, tok0, row, kv_head, stream=None):
+    _check(_lib.kv_quant_value_paged(ctypes.byref(cfg), ctypes.byref(cache), _ptr(v), n_tokens, tok0, row, kv_head,
+                                     _stream(stream)), "kv_quant_value_paged")
+
+
+def kv_append_kivi_paged(cfg, cache, pool, k_new, v_new, stream=None):
+    _check(_lib.kv_append_kivi_paged(ctypes.byref(cfg), ctypes.byref(cache), ctypes.byref(pool), _ptr(k_new),
+                                     _ptr(v_new), _stream(stream)), "kv_append_kivi_paged")
+
+
+def kv_release_kivi_paged(cache, row, pool, stream=None):
+    _check(_lib.kv_release_kivi_paged(ctypes.byref(cache), row, ctypes.byref(pool), _stream(stream)),
+           "kv_release_kivi_paged")
+
+
+def kv_decode_attn_kivi_paged(cfg, cache, q, out, workspace, workspace_bytes, stream=None):
+    _check(_lib.kv_decode_attn_kivi_paged(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out),
+                                          _ptr(workspace), workspace_bytes, _stream(stream)),
+           "kv_decode_attn_kivi_paged")
 
 
 def kv_quant_int8_token(cfg, cache, x, n, slots, kv_sel, stream=None):

@@ -96,8 +96,18 @@ typedef enum {
     KVQ_VARIANT_KIVI = 0,
     KVQ_VARIANT_KITTY = 1,
     KVQ_VARIANT_INT8 = 2,
-    KVQ_VARIANT_INT8_TOKEN = 3
+    KVQ_VARIANT_INT8_TOKEN = 3,
+    KVQ_VARIANT_KIVI_PAGED = 4
 } kvq_variant;
+
+/* Free-slot (or free-page) pool: a stack of free ids.  slots int32
+ * [capacity] and top int32 [1] are device memory owned by the caller; the
+ * ids below *top are free. */
+typedef struct {
+    int32_t capacity;
+    int32_t *slots;
+    int32_t *top;
+} kvq_slot_pool;
 
 typedef struct {
     int32_t head_dim;     /* D; 128 */
@@ -227,6 +237,62 @@ typedef struct {
 KVQ_API kvq_status kv_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, const void *k_new,
                                   const void *v_new, cudaStream_t stream);
 
+/* Paged KIVI cache: the quantized part of every request lives in pages of
+ * 128 tokens taken from a shared pool (a page table per request, a free-page
+ * stack: kvq_slot_pool with page ids), the fp16 residual stays per (batch
+ * row, kv head).  A page record holds one kv head's 128 tokens in the order a
+ * decode stage uses them:
+ *   key codes   128*D*bits_k/8 bytes  (128/G key groups in the tile layout)
+ *   key (s, z)  2048 bytes            (128/G blocks of 256 fp16, order above)
+ *   value codes 128*D*bits_v/8 bytes  (token-major)
+ *   value (s,z) 2048 bytes            (fp16x2 [128][D/Gv])
+ * so a decode stage is one contiguous copy of kvq_kivi_page_bytes(cfg)
+ * bytes.  Token t of request b is in logical page t/128, physical page
+ * page_table[b][t/128], record pages + (page * Hkv + kv_head) * page_bytes. */
+typedef struct {
+    int32_t batch;
+    int32_t max_seq_len;       /* page_table row stride = ceil(max_seq_len / 128) */
+    const int32_t *seq_len;    /* [B] */
+    const int32_t *page_table; /* int32 [B][ceil(max_seq_len/128)] */
+    int32_t n_pages;           /* pages in the pool */
+    const void *pages;         /* [n_pages][Hkv][kvq_kivi_page_bytes(cfg)] */
+    const void *k_res;         /* fp16 [B][Hkv][R][D] */
+    const void *v_res;         /* fp16 [B][Hkv][R][D] */
+} kvq_kivi_paged_cache;
+
+/* Bytes of one paged KIVI page record for cfg (0 for an invalid cfg). */
+KVQ_API size_t kvq_kivi_page_bytes(const kvq_config *cfg);
+
+/* a1 / a2 into pages: quantize n_groups key groups (fp16 [n_groups][G][D]
+ * of kv head kv_head) that are groups group0 .. group0 + n_groups - 1 of
+ * request `row`, or n_tokens value tokens (fp16 [n_tokens][D]) that are its
+ * tokens tok0 .., into the pages page_table[row] names.  Same arithmetic as
+ * kv_quant_key / kv_quant_value. */
+KVQ_API kvq_status kv_quant_key_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *k,
+                                      int64_t n_groups, int32_t group0, int32_t row, int32_t kv_head,
+                                      cudaStream_t stream);
+KVQ_API kvq_status kv_quant_value_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const void *v,
+                                        int64_t n_tokens, int32_t tok0, int32_t row, int32_t kv_head,
+                                        cudaStream_t stream);
+
+/* Streaming append to a paged KIVI cache, as kv_append_kivi: a row with
+ * L = seq_len[b] a multiple of 128 first takes a page from the pool for
+ * logical page L/128 (rows in order of b take pages from the top of the free
+ * stack, deterministic under graph replay); then the pending flush and value
+ * quantization write into the row's pages, token L goes to ring slot L % R,
+ * and seq_len[b] = L + 1.  A row that needs a page when the pool has too few
+ * is left unchanged and KVQ_DEVICE_ERR_POOL is recorded; a full row records
+ * KVQ_DEVICE_ERR_CAPACITY.  Three kernels on `stream`, graph-capturable. */
+KVQ_API kvq_status kv_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c,
+                                        const kvq_slot_pool *pool, const void *k_new, const void *v_new,
+                                        cudaStream_t stream);
+
+/* Return the pages of request `row` (logical pages 0 .. ceil(seq_len/128)-1)
+ * to the pool and set seq_len[row] = 0; overfilling the pool records
+ * KVQ_DEVICE_ERR_POOL and changes nothing. */
+KVQ_API kvq_status kv_release_kivi_paged(const kvq_kivi_paged_cache *c, int32_t row, const kvq_slot_pool *pool,
+                                         cudaStream_t stream);
+
 /* Kitty: sink tokens [0, min(L,S)) fp16; key pages, then a key Q-buffer of
  * n_kb = ((L-S-1) mod G) + 1 tokens (slot (t-S) % G); value pages, a value
  * Q-buffer of n_vb = ((E-1) mod G) + 1 tokens with E = L-S-R > 0 (slot
@@ -311,14 +377,6 @@ KVQ_API kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c
  * 1 = V.  The dither follows the slot, so moving a request never changes
  * what a written slot decodes to. */
 
-/* Free-slot pool: a stack of free slot ids.  slots int32 [capacity] and top
- * int32 [1] are device memory owned by the caller; the slots below *top are
- * free. */
-typedef struct {
-    int32_t capacity;
-    int32_t *slots;
-    int32_t *top;
-} kvq_slot_pool;
 
 typedef struct {
     int32_t batch;
@@ -382,6 +440,11 @@ KVQ_API kvq_status kv_decode_attn_kitty(const kvq_config *cfg, const kvq_kitty_c
                                 void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 KVQ_API kvq_status kv_decode_attn_int8(const kvq_config *cfg, const kvq_int8_cache *cache, const void *q,
                                void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+/* Paged KIVI: the quantized tiles are read page by page through the page
+ * table (one copy per 128-token stage). */
+KVQ_API kvq_status kv_decode_attn_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *cache,
+                                             const void *q, void *out, void *workspace, size_t workspace_bytes,
+                                             cudaStream_t stream);
 /* Token-granular INT8: every token t < seq_len[b] is read from slot
  * slot_table[b][t] and dequantized with its slot's dither; a row with
  * seq_len[b] == 0 gets out = 0. */

@@ -129,6 +129,33 @@ def test_int8_token_validation_without_gpu(K):
         K.KVQ_ERR_WORKSPACE
 
 
+def test_kivi_paged_validation_without_gpu(K):
+    cfg = K.make_config(n_q_heads=8, n_kv_heads=2)
+    assert K.kvq_kivi_page_bytes(cfg) == 4096 + 2048 + 4096 + 2048
+    assert K.kvq_kivi_page_bytes(K.make_config(bits_k=4, bits_v=4)) == 8192 + 2048 + 8192 + 2048
+    c = K.kvq_kivi_paged_cache(2, 1000, 16, 16, 64, 16, 16, 16)
+    call = K.raw_call
+    assert call("kv_quant_key_paged", ctypes.byref(cfg), ctypes.byref(c), 16, 4, 0, 2, 0, None) == \
+        K.KVQ_ERR_INVALID_ARG                                           # row out of range
+    assert call("kv_quant_key_paged", ctypes.byref(cfg), ctypes.byref(c), 16, 4, 0, 0, 2, None) == \
+        K.KVQ_ERR_INVALID_ARG                                           # kv head out of range
+    assert call("kv_quant_key_paged", ctypes.byref(cfg), ctypes.byref(c), 16, 33, 0, 0, 0, None) == \
+        K.KVQ_ERR_INVALID_ARG                                           # 33 groups of 32 > 1024 tokens
+    assert call("kv_quant_value_paged", ctypes.byref(cfg), ctypes.byref(c), 16, 10, 1020, 0, 0, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert call("kv_quant_value_paged", ctypes.byref(cfg), ctypes.byref(c), 0x1002, 10, 0, 0, 0, None) == \
+        K.KVQ_ERR_MISALIGNED
+    assert call("kv_append_kivi_paged", ctypes.byref(cfg), ctypes.byref(c), None, 16, 16, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert call("kv_release_kivi_paged", ctypes.byref(c), -1, ctypes.byref(K.kvq_slot_pool(8, 16, 16)), None) == \
+        K.KVQ_ERR_INVALID_ARG
+    n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI_PAGED, 2, 1000)
+    assert call("kv_decode_attn_kivi_paged", ctypes.byref(cfg), ctypes.byref(c), 16, 16, 16, wsb - 1, None) == \
+        K.KVQ_ERR_WORKSPACE
+    assert call("kv_decode_attn_kivi_paged", ctypes.byref(K.make_config(bits_k=3)), ctypes.byref(c), 16, 16, 16, wsb,
+                None) == K.KVQ_ERR_UNSUPPORTED
+
+
 def test_decode_plan_and_workspace_checks(K):
     cfg = K.make_config()
     n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, 32, 4096)
