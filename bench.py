@@ -48,7 +48,8 @@ def _workload_desc(w):
     base = f"{w.name}: batch {w.batch}, {w.n_q_heads} query / {w.n_kv_heads} KV heads, head_dim 128, "
     if w.variant == "kivi":
         return base + (f"{w.seq_len} cached tokens, K{w.bits_k}V{w.bits_v} (key per-channel G=32, value per-token "
-                       f"Gv=32), R=128")
+                       f"Gv=32), R=128" + (", paged: 128-token pages in a hashed order from a shared pool"
+                                           if w.paged else ""))
     if w.variant == "kitty":
         return base + (f"{w.seq_len} cached tokens, Kitty pages G=128, 16 of 128 key channels boosted to 4 bit "
                        f"(two 2-bit planes), value 2 bit, sink 32, local 128")
@@ -175,7 +176,13 @@ def build_state(w, device, appends: int = 1024):
     from bit_kv_cache_keyquant_gb300 import kvq
     lens = I.seq_lens(w)
     Lmax = int(lens.max())
-    if w.variant == "kivi":
+    if w.variant == "kivi" and w.paged:
+        cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, bits_k=w.bits_k, bits_v=w.bits_v)
+        n_pages = int(sum((int(L) + 127) // 128 for L in lens)) + 64
+        cache = C.KiviPagedCache(cfg, w.batch, Lmax, n_pages, device=device)
+        cache.shuffle_free(I.page_permutation(w, n_pages))
+        variant = kvq.KVQ_VARIANT_KIVI_PAGED
+    elif w.variant == "kivi":
         cfg = kvq.make_config(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, bits_k=w.bits_k, bits_v=w.bits_v)
         cache = C.KiviCache(cfg, w.batch, Lmax, device=device)
         variant = kvq.KVQ_VARIANT_KIVI
@@ -197,8 +204,12 @@ def build_state(w, device, appends: int = 1024):
         variant = kvq.KVQ_VARIANT_INT8
     reqs = I.request_ids(w)
     for b in range(w.batch):
-        if w.variant == "int8t":
+        if w.variant == "int8t" or (w.variant == "kivi" and w.paged):
             L = int(lens[b])
+            if w.variant == "kivi":
+                cache.fill(b, torch.stack([I.gen_kv_torch(w, I.T_K, b, h, L, device) for h in range(w.n_kv_heads)]),
+                           torch.stack([I.gen_kv_torch(w, I.T_V, b, h, L, device) for h in range(w.n_kv_heads)]))
+                continue
             cache.fill(b, torch.stack([I.gen_kv_torch(w, I.T_K, b, h, L, device) for h in range(w.n_kv_heads)], 1),
                        torch.stack([I.gen_kv_torch(w, I.T_V, b, h, L, device) for h in range(w.n_kv_heads)], 1))
             continue
@@ -465,7 +476,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7],
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8],
                     help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")

@@ -60,6 +60,7 @@ class Workload:
     fixed_outliers: bool = False  # same outlier channels for every kv head
     bits_k: int = 2              # KIVI code widths
     bits_v: int = 2
+    paged: bool = False          # KIVI: pages of 128 tokens from a shared pool through a page table
 
     @property
     def seed(self) -> int:
@@ -79,6 +80,7 @@ WORKLOADS = {
     6: Workload(6, "INT8 token-granular slot pool B8 64q/8kv L~U[16384,65536]", 8, 64, 8, 65536,
                 "int8t", min_seq_len=16384),
     7: Workload(7, "KIVI-4 Llama-2-7B-shaped MHA B32 H32 L4096", 32, 32, 32, 4096, "kivi", bits_k=4, bits_v=4),
+    8: Workload(8, "paged KIVI Llama-2-7B-shaped MHA B32 H32 L4096", 32, 32, 32, 4096, "kivi", paged=True),
 }
 
 
