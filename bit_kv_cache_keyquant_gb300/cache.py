@@ -216,6 +216,91 @@ class KittyCache:
         return tot * cfg.n_kv_heads
 
 
+class KittyPagedCache:
+    """Paged Kitty cache of one layer: key and value page records in pools of n_pages pages shared by all
+    requests (one page id per 128 tokens after the sink, for every kv head), a page table per request, a
+    free-page stack, and per-(row, kv head) fp16 sink, Q-buffers and local window."""
+
+    def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, n_pages: int, device="cuda"):
+        self.cfg, self.batch, self.max_seq_len, self.n_pages = cfg, batch, max_seq_len, n_pages
+        H, G, S, R = cfg.n_kv_heads, cfg.group_k, cfg.sink, cfg.residual
+        self.kpb = kvq.kvq_kitty_key_page_bytes(cfg)
+        self.vpb = kvq.kvq_kitty_value_page_bytes(cfg)
+        self.page_cap = max(1, (max(max_seq_len - S, 0) + G - 1) // G)
+        self.k_pages = torch.zeros((n_pages, H, self.kpb), dtype=torch.uint8, device=device)
+        self.v_pages = torch.zeros((n_pages, H, self.vpb), dtype=torch.uint8, device=device)
+        self.page_table = torch.full((batch, self.page_cap), -1, dtype=torch.int32, device=device)
+        self.k_sink = torch.zeros((batch, H, max(S, 1), D), dtype=torch.float16, device=device)
+        self.v_sink = torch.zeros((batch, H, max(S, 1), D), dtype=torch.float16, device=device)
+        self.k_qbuf = torch.zeros((batch, H, G, D), dtype=torch.float16, device=device)
+        self.v_qbuf = torch.zeros((batch, H, G, D), dtype=torch.float16, device=device)
+        self.v_local = torch.zeros((batch, H, R, D), dtype=torch.float16, device=device)
+        self.seq_len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.free_pages = torch.empty(n_pages, dtype=torch.int32, device=device)
+        self.top = torch.zeros(4, dtype=torch.int32, device=device)
+        kvq.kv_slot_pool_init(self.pool())
+
+    def pool(self) -> kvq.kvq_slot_pool:
+        return kvq.kvq_slot_pool(self.n_pages, self.free_pages.data_ptr(), self.top.data_ptr())
+
+    def desc(self) -> kvq.kvq_kitty_cache:
+        return kvq.kvq_kitty_cache(self.batch, self.max_seq_len, self.seq_len.data_ptr(), self.k_pages.data_ptr(),
+                                   self.v_pages.data_ptr(), self.k_sink.data_ptr(), self.v_sink.data_ptr(),
+                                   self.k_qbuf.data_ptr(), self.v_qbuf.data_ptr(), self.v_local.data_ptr(),
+                                   self.page_table.data_ptr(), self.n_pages)
+
+    def shuffle_free(self, perm):
+        """Reorder the free stack by a permutation of its entries (host setup)."""
+        top = int(self.top[0].item())
+        free = self.free_pages[:top].flip(0)
+        idx = torch.as_tensor(perm, dtype=torch.int64, device=free.device)
+        self.free_pages[:top] = free[idx].flip(0)
+
+    def fill(self, b: int, K: torch.Tensor, V: torch.Tensor, score_mode: int = 0, stream=None):
+        """Request b from fp16 K, V [Hkv][L][D]: pops a page for every 128 tokens after the sink that hold
+        a token, quantizes the full key / value pages of every head into them."""
+        cfg = self.cfg
+        H, L = K.shape[0], K.shape[1]
+        G, S, R = cfg.group_k, cfg.sink, cfg.residual
+        assert 1 <= L <= self.max_seq_len and int(self.seq_len[b].item()) == 0
+        npg = (max(L - S, 0) + G - 1) // G
+        top = int(self.top[0].item())
+        assert npg <= top
+        if npg:
+            self.page_table[b, :npg] = self.free_pages[top - npg:top].flip(0)
+            self.top[0] = top - npg
+        pk, nkb, pv, nvb, nloc = kitty_segments(L, G, S, R)
+        d = self.desc()
+        for h in range(H):
+            if pk:
+                kvq.kv_quant_key_kitty_paged(cfg, d, K[h, S:S + pk * G].contiguous(), pk, 0, b, h, score_mode,
+                                             stream)
+            if pv:
+                kvq.kv_quant_value_kitty_paged(cfg, d, V[h, S:S + pv * G].contiguous(), pv, 0, b, h, stream)
+            ns = min(L, S)
+            if ns:
+                self.k_sink[b, h, :ns] = K[h, :ns]
+                self.v_sink[b, h, :ns] = V[h, :ns]
+            k0 = S + pk * G
+            if L > k0:
+                _slot_copy(self.k_qbuf[b, h], K[h, k0:L], [(t - S) % G for t in range(k0, L)])
+            v0 = S + pv * G
+            if nvb:
+                _slot_copy(self.v_qbuf[b, h], V[h, v0:v0 + nvb], [(t - S) % G for t in range(v0, v0 + nvb)])
+            if nloc:
+                _slot_copy(self.v_local[b, h], V[h, L - nloc:L], [t % R for t in range(L - nloc, L)])
+        self.seq_len[b] = L
+
+    def nbytes_read(self, lens) -> int:
+        cfg = self.cfg
+        tot = 0
+        for L in lens:
+            pk, nkb, pv, nvb, nloc = kitty_segments(int(L), cfg.group_k, cfg.sink, cfg.residual)
+            ns = min(int(L), cfg.sink)
+            tot += pk * self.kpb + pv * self.vpb + (2 * ns + nkb + nvb + nloc) * D * 2
+        return tot * cfg.n_kv_heads
+
+
 class Int8Cache:
     def __init__(self, cfg: kvq.kvq_config, batch: int, max_seq_len: int, layer: int = 0, seed: int = 0,
                  device="cuda"):

@@ -248,7 +248,7 @@ extern "C" kvq_status kv_release_kivi_paged(const kvq_kivi_paged_cache *c, int32
     if ((s = check_pool(pool))) return s;
     const int stride = (int)(((int64_t)c->max_seq_len + 127) / 128);
     return cuda_status(launch_release_ids(const_cast<int32_t *>(c->seq_len), c->page_table, row, c->max_seq_len, 128,
-                                          stride, pool, stream));
+                                          stride, 0, pool, stream));
 }
 
 extern "C" kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, const void *k_new,
@@ -263,12 +263,81 @@ extern "C" kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache
     return cuda_status(launch_append_int8(cfg, c, k_new, v_new, stream));
 }
 
+static int kitty_page_cap(const kvq_config *cfg, const kvq_kitty_cache *c) {
+    const int pc = (int)(((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + 127) / 128);
+    return pc < 1 ? 1 : pc;
+}
+
+static kvq_status check_kitty_cache(const kvq_config *cfg, const kvq_kitty_cache *c, bool paged) {
+    if (!c || c->batch < 1 || c->max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
+    if (paged != (c->page_table != nullptr)) return KVQ_ERR_INVALID_ARG;
+    if (paged && c->n_pages < 1) return KVQ_ERR_INVALID_ARG;
+    kvq_status s = ptrs_ok({c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local});
+    if (s) return s;
+    if (paged && (s = ptrs_ok({c->page_table}))) return s;
+    if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;
+    return KVQ_OK;
+}
+
+extern "C" kvq_status kv_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k,
+                                               int64_t n_pages, int32_t page0, int32_t row, int32_t kv_head,
+                                               int32_t score_mode, cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (score_mode != 0 && score_mode != 1) return KVQ_ERR_INVALID_ARG;
+    if (!c || !c->page_table || c->batch < 1 || c->max_seq_len < 1 || c->n_pages < 1) return KVQ_ERR_INVALID_ARG;
+    if (n_pages < 0 || page0 < 0 || row < 0 || row >= c->batch || kv_head < 0 || kv_head >= cfg->n_kv_heads ||
+        page0 + n_pages > kitty_page_cap(cfg, c))
+        return KVQ_ERR_INVALID_ARG;
+    if (n_pages == 0) return KVQ_OK;
+    if ((s = ptrs_ok({k, c->k_pages, c->page_table}))) return s;
+    return cuda_status(launch_quant_key_kitty_paged(cfg, c, k, n_pages, page0, row, kv_head, score_mode, stream));
+}
+
+extern "C" kvq_status kv_quant_value_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *v,
+                                                 int64_t n_pages, int32_t page0, int32_t row, int32_t kv_head,
+                                                 cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (!c || !c->page_table || c->batch < 1 || c->max_seq_len < 1 || c->n_pages < 1) return KVQ_ERR_INVALID_ARG;
+    if (n_pages < 0 || page0 < 0 || row < 0 || row >= c->batch || kv_head < 0 || kv_head >= cfg->n_kv_heads ||
+        page0 + n_pages > kitty_page_cap(cfg, c))
+        return KVQ_ERR_INVALID_ARG;
+    if (n_pages == 0) return KVQ_OK;
+    if ((s = ptrs_ok({v, c->v_pages, c->page_table}))) return s;
+    return cuda_status(launch_quant_value_kitty_paged(cfg, c, v, n_pages, page0, row, kv_head, stream));
+}
+
+extern "C" kvq_status kv_append_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const kvq_slot_pool *pool,
+                                            const void *k_new, const void *v_new, int32_t score_mode,
+                                            cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if (score_mode != 0 && score_mode != 1) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_kitty_cache(cfg, c, true))) return s;
+    if ((s = check_pool(pool))) return s;
+    if ((s = ptrs_ok({k_new, v_new}))) return s;
+    return cuda_status(launch_append_kitty_paged(cfg, c, pool, k_new, v_new, score_mode, stream));
+}
+
+extern "C" kvq_status kv_release_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, int32_t row,
+                                       const kvq_slot_pool *pool, cudaStream_t stream) {
+    kvq_status s = check_kitty(cfg);
+    if (s) return s;
+    if ((s = check_kitty_cache(cfg, c, true))) return s;
+    if (row < 0 || row >= c->batch) return KVQ_ERR_INVALID_ARG;
+    if ((s = check_pool(pool))) return s;
+    return cuda_status(launch_release_ids(const_cast<int32_t *>(c->seq_len), c->page_table, row, c->max_seq_len, 128,
+                                          kitty_page_cap(cfg, c), cfg->sink, pool, stream));
+}
+
 extern "C" kvq_status kv_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new,
                                       const void *v_new, int score_mode, cudaStream_t stream) {
     kvq_status s = check_kitty(cfg);
     if (s) return s;
     if (score_mode != 0 && score_mode != 1) return KVQ_ERR_INVALID_ARG;
     if (!c || c->batch < 1 || c->max_seq_len < 1) return KVQ_ERR_INVALID_ARG;
+    if (c->page_table) return KVQ_ERR_INVALID_ARG;          // a paged cache appends through kv_append_kitty_paged
     if ((s = ptrs_ok({k_new, v_new, c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local}))) return s;
     if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;
     return cuda_status(launch_append_kitty(cfg, c, k_new, v_new, score_mode, stream));
@@ -423,8 +492,8 @@ static kvq_status stage1_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, 
     if (!c) return KVQ_ERR_INVALID_ARG;
     if (cfg->boost_k > 92) return KVQ_ERR_UNSUPPORTED;   // key record must fit the decode stage slot
     if ((s = check_ws(cfg, KVQ_VARIANT_KITTY, c->batch, c->max_seq_len, ws, wsb, p))) return s;
-    if ((s = ptrs_ok({q, c->seq_len, c->k_pages, c->v_pages, c->k_qbuf, c->v_qbuf, c->v_local}))) return s;
-    if (cfg->sink > 0 && (s = ptrs_ok({c->k_sink, c->v_sink}))) return s;
+    if ((s = check_kitty_cache(cfg, c, c->page_table != nullptr))) return s;
+    if ((s = ptrs_ok({q}))) return s;
     if (kitty_gqa_supported(cfg)) return cuda_status(launch_decode_kitty_gqa(cfg, c, q, *p, ws, st));
     return cuda_status(launch_decode_kitty(cfg, c, q, *p, ws, st));
 }

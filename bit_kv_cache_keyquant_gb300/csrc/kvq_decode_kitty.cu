@@ -264,6 +264,8 @@ cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
     P.seq_len = c->seq_len;
     P.k_pages = static_cast<const uint8_t *>(c->k_pages);
     P.v_pages = static_cast<const uint8_t *>(c->v_pages);
+    P.page_table = c->page_table;
+    P.n_pages = c->n_pages;
     P.k_sink = static_cast<const uint16_t *>(c->k_sink);
     P.v_sink = static_cast<const uint16_t *>(c->v_sink);
     P.k_qbuf = static_cast<const uint16_t *>(c->k_qbuf);

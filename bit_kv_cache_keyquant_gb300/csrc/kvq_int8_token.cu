@@ -117,11 +117,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total)
     return r;
 }
 
-// Rows b with 0 <= L = seq_len[b] < cap and L % unit == 0 take one id each
-// (token slots: unit 1; pages of 128 tokens: unit 128) for table[b][L / unit].
+// Rows b with base <= L = seq_len[b] < cap and (L - base) % unit == 0 take one
+// id each (token slots: unit 1; pages of 128 tokens: unit 128; Kitty pages
+// start after the base = S sink tokens) for table[b][(L - base) / unit].
 __global__ void __launch_bounds__(1024) slot_alloc_kernel(const int32_t *__restrict__ seq_len,
                                                           int32_t *__restrict__ table, int B, int cap, int unit,
-                                                          int stride, const int32_t *__restrict__ free_slots,
+                                                          int stride, int base,
+                                                          const int32_t *__restrict__ free_slots,
                                                           int32_t *__restrict__ top, int capacity,
                                                           unsigned *err) {
     __shared__ int warp_tot[33];
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(1024) slot_alloc_kernel(const int32_t *__restr
     bool full = false;
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int L = seq_len[b];
-        if (L >= 0 && L < cap) cnt += L % unit == 0 ? 1 : 0;
+        if (L >= 0 && L < cap) cnt += (L >= base && (L - base) % unit == 0) ? 1 : 0;
         else full = true;
     }
     if (full) atomicOr(err, KVQ_DEVICE_ERR_CAPACITY);
@@ -142,15 +144,15 @@ __global__ void __launch_bounds__(1024) slot_alloc_kernel(const int32_t *__restr
     const int t0 = *top;
     const bool fail = need > t0 || t0 > capacity;
     if (fail && threadIdx.x == 0) atomicOr(err, KVQ_DEVICE_ERR_POOL);
-    int base = 0;
+    int done = 0;
     for (int c0 = 0; c0 < B; c0 += blockDim.x) {
         const int b = c0 + threadIdx.x;
         const int L = b < B ? seq_len[b] : -1;
-        const int f = (L >= 0 && L < cap && L % unit == 0) ? 1 : 0;
+        const int f = (L >= base && L < cap && (L - base) % unit == 0) ? 1 : 0;
         int tot;
-        const int r = block_excl_scan(f, warp_tot, tot) + base;
-        if (f) table[(int64_t)b * stride + L / unit] = fail ? -1 : free_slots[t0 - 1 - r];
-        base += tot;
+        const int r = block_excl_scan(f, warp_tot, tot) + done;
+        if (f) table[(int64_t)b * stride + (L - base) / unit] = fail ? -1 : free_slots[t0 - 1 - r];
+        done += tot;
     }
     __syncthreads();
     if (threadIdx.x == 0 && !fail) *top = t0 - need;
@@ -189,13 +191,14 @@ __global__ void __launch_bounds__(256) append_int8_token_kernel(AppendT P) {
     if (threadIdx.x == 0) P.seq_len[b] = L + 1;
 }
 
-// Push the ids of request `row` (table[row][0 .. ceil(seq_len[row] / unit))) back.
+// Push the ids of request `row` (table[row][0 .. ceil(max(seq_len[row] - base, 0) / unit))) back.
 __global__ void __launch_bounds__(1024) slot_release_kernel(int32_t *__restrict__ seq_len,
                                                             const int32_t *__restrict__ table, int row, int cap,
-                                                            int unit, int stride, int32_t *__restrict__ free_slots,
+                                                            int unit, int stride, int base,
+                                                            int32_t *__restrict__ free_slots,
                                                             int32_t *__restrict__ top, int capacity, unsigned *err) {
     const int L = seq_len[row];
-    const int n = L >= 0 && L <= cap ? (L + unit - 1) / unit : -1;
+    const int n = L >= 0 && L <= cap ? (max(L - base, 0) + unit - 1) / unit : -1;
     const int t0 = *top;
     if (n < 0 || t0 < 0 || t0 + n > capacity) {
         if (threadIdx.x == 0) atomicOr(err, KVQ_DEVICE_ERR_POOL);
@@ -256,7 +259,7 @@ cudaError_t launch_append_int8_token(const kvq_config *cfg, const kvq_int8_token
     if (!err) return cudaErrorInvalidDevicePointer;
     int32_t *table = const_cast<int32_t *>(c->slot_table);
     int32_t *seq_len = const_cast<int32_t *>(c->seq_len);
-    cudaError_t e = launch_alloc_ids(seq_len, table, c->batch, c->max_seq_len, 1, c->max_seq_len, pool, st);
+    cudaError_t e = launch_alloc_ids(seq_len, table, c->batch, c->max_seq_len, 1, c->max_seq_len, 0, pool, st);
     if (e != cudaSuccess) return e;
     AppendT P;
     P.seq_len = seq_len;
@@ -284,23 +287,23 @@ cudaError_t launch_append_int8_token(const kvq_config *cfg, const kvq_int8_token
 cudaError_t launch_release_int8_token(const kvq_int8_token_cache *c, int row, const kvq_slot_pool *pool,
                                       cudaStream_t st) {
     return launch_release_ids(const_cast<int32_t *>(c->seq_len), c->slot_table, row, c->max_seq_len, 1,
-                              c->max_seq_len, pool, st);
+                              c->max_seq_len, 0, pool, st);
 }
 
 cudaError_t launch_alloc_ids(const int32_t *seq_len, int32_t *table, int batch, int cap, int unit, int stride,
-                             const kvq_slot_pool *pool, cudaStream_t st) {
+                             int base, const kvq_slot_pool *pool, cudaStream_t st) {
     unsigned *err = device_error_ptr();
     if (!err) return cudaErrorInvalidDevicePointer;
-    slot_alloc_kernel<<<1, 1024, 0, st>>>(seq_len, table, batch, cap, unit, stride, pool->slots, pool->top,
+    slot_alloc_kernel<<<1, 1024, 0, st>>>(seq_len, table, batch, cap, unit, stride, base, pool->slots, pool->top,
                                           pool->capacity, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_release_ids(int32_t *seq_len, const int32_t *table, int row, int cap, int unit, int stride,
-                               const kvq_slot_pool *pool, cudaStream_t st) {
+                               int base, const kvq_slot_pool *pool, cudaStream_t st) {
     unsigned *err = device_error_ptr();
     if (!err) return cudaErrorInvalidDevicePointer;
-    slot_release_kernel<<<1, 1024, 0, st>>>(seq_len, table, row, cap, unit, stride, pool->slots, pool->top,
+    slot_release_kernel<<<1, 1024, 0, st>>>(seq_len, table, row, cap, unit, stride, base, pool->slots, pool->top,
                                             pool->capacity, err);
     return cudaGetLastError();
 }

@@ -115,12 +115,19 @@ cudaError_t launch_quant_value_paged(const kvq_config *cfg, const kvq_kivi_paged
                                      int tok0, int row, int kvh, cudaStream_t st);
 cudaError_t launch_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged_cache *c, const kvq_slot_pool *pool,
                                      const void *k_new, const void *v_new, cudaStream_t st);
-// free-id stack (token slots: unit 1; pages: unit 128): rows with seq_len % unit == 0 take an id for
-// table[b][seq_len / unit]; release pushes table[row][0 .. ceil(seq_len / unit)) back
+// free-id stack (token slots: unit 1; pages: unit 128, after `base` sink tokens for Kitty): rows with
+// seq_len >= base and (seq_len - base) % unit == 0 take an id for table[b][(seq_len - base) / unit];
+// release pushes table[row][0 .. ceil(max(seq_len - base, 0) / unit)) back
 cudaError_t launch_alloc_ids(const int32_t *seq_len, int32_t *table, int batch, int cap, int unit, int stride,
-                             const kvq_slot_pool *pool, cudaStream_t st);
+                             int base, const kvq_slot_pool *pool, cudaStream_t st);
 cudaError_t launch_release_ids(int32_t *seq_len, const int32_t *table, int row, int cap, int unit, int stride,
-                               const kvq_slot_pool *pool, cudaStream_t st);
+                               int base, const kvq_slot_pool *pool, cudaStream_t st);
+cudaError_t launch_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k, int64_t n,
+                                         int page0, int row, int kvh, int score_mode, cudaStream_t st);
+cudaError_t launch_quant_value_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *v, int64_t n,
+                                           int page0, int row, int kvh, cudaStream_t st);
+cudaError_t launch_append_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const kvq_slot_pool *pool,
+                                      const void *k_new, const void *v_new, int score_mode, cudaStream_t st);
 cudaError_t launch_merge(const kvq_config *cfg, int batch, const DecodePlan &p, const void *ws, void *out,
                          cudaStream_t st);
 

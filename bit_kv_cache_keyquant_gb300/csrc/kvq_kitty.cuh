@@ -26,10 +26,14 @@ struct Params {
     int kpb, vpb;
     float alpha;
     int e0;
+    // paged cache (page_table non-null): logical page p of row b is pool page
+    // page_table[b * page_cap + p] of k_pages / v_pages ([n_pages][Hkv][record])
+    const int32_t *page_table;
+    int n_pages;
 };
 
 struct Unit {
-    int b, hq, split, p0, np, nKp, nVp, nkb, nvb, L;
+    int b, hq, kvh, split, p0, np, nKp, nVp, nkb, nvb, L;
     bool residual;
     int64_t bk;
 };
@@ -75,13 +79,30 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
         U.p0 = U.split * cpp;
         U.np = max(0, min(U.p0 + cpp, Pf) - U.p0);
     }
-    U.bk = (int64_t)U.b * P.Hkv + (hpr == P.Hkv ? U.hq : U.hq / (P.Hq / P.Hkv));
+    U.kvh = hpr == P.Hkv ? U.hq : U.hq / (P.Hq / P.Hkv);
+    U.bk = (int64_t)U.b * P.Hkv + U.kvh;
     return U;
 }
 
-// Key of token t (residual unit), channel c, dequantized (fp32).
+// Record index of logical page p of the unit's (row, kv head): the dense
+// per-request arrays, or the pool page the page table names (an entry
+// outside the pool reads page 0 and records KVQ_DEVICE_ERR_POOL).
+__device__ __forceinline__ int64_t page_record(const Params &P, const Unit &U, int p) {
+    if (!P.page_table) return U.bk * P.page_cap + p;
+    int pg = P.page_table[(int64_t)U.b * P.page_cap + p];
+    if (pg < 0 || pg >= P.n_pages) {
+        atomicOr(P.err, KVQ_DEVICE_ERR_POOL);
+        pg = 0;
+    }
+    return (int64_t)pg * P.Hkv + U.kvh;
+}
+
 __device__ __forceinline__ const uint8_t *key_page(const Params &P, const Unit &U, int p) {
-    return P.k_pages + (U.bk * P.page_cap + p) * (int64_t)P.kpb;
+    return P.k_pages + page_record(P, U, p) * (int64_t)P.kpb;
+}
+
+__device__ __forceinline__ const uint8_t *value_page(const Params &P, const Unit &U, int p) {
+    return P.v_pages + page_record(P, U, p) * (int64_t)P.vpb;
 }
 
 // Tokens of one query head outside whole pages (sink, Q-buffers, local
@@ -180,7 +201,7 @@ __device__ __forceinline__ void kitty_produce(const Params &P, int hpr, uint8_t 
             uint8_t *st = stage[slot];
             mbar_expect_tx(&full[slot], (uint32_t)(P.kpb + P.vpb));
             bulk_g2s(st, key_page(P, U, p), (uint32_t)P.kpb, &full[slot]);
-            bulk_g2s(st + VREC_OFF, P.v_pages + (U.bk * P.page_cap + p) * (int64_t)P.vpb, (uint32_t)P.vpb, &full[slot]);
+            bulk_g2s(st + VREC_OFF, value_page(P, U, p), (uint32_t)P.vpb, &full[slot]);
         }
     }
     for (int s = max(0, sg - NST); s < sg; ++s) mbar_wait(&full[s % NST], (s / NST) & 1, P.err);

@@ -741,12 +741,15 @@ __global__ void __launch_bounds__(128) append_kivi_paged_kernel(AppendParams P, 
     }
 }
 
-__global__ void append_bump_paged_kernel(int32_t *seq_len, const int32_t *table, int stride, int B, int max_seq_len) {
+// seq_len += 1 for every row that could append: not full, and not waiting
+// for a page the allocator could not give (pages start after `base` tokens)
+__global__ void append_bump_paged_kernel(int32_t *seq_len, const int32_t *table, int stride, int base, int B,
+                                         int max_seq_len) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const int L = seq_len[b];
     if (L < 0 || L >= max_seq_len) return;
-    if ((L & 127) == 0 && table[(int64_t)b * stride + (L >> 7)] < 0) return;
+    if (L >= base && ((L - base) & 127) == 0 && table[(int64_t)b * stride + ((L - base) >> 7)] < 0) return;
     seq_len[b] = L + 1;
 }
 
@@ -756,7 +759,7 @@ cudaError_t launch_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged
     if (!D.err) return cudaErrorInvalidDevicePointer;
     int32_t *seq_len = const_cast<int32_t *>(c->seq_len);
     cudaError_t e = launch_alloc_ids(seq_len, const_cast<int32_t *>(c->page_table), c->batch, c->max_seq_len, 128,
-                                     D.pt_stride, pool, st);
+                                     D.pt_stride, 0, pool, st);
     if (e != cudaSuccess) return e;
     AppendParams P;
     P.seq_len = c->seq_len;
@@ -787,8 +790,8 @@ cudaError_t launch_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged
 #undef KVQ_APPEND_PAGED
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    append_bump_paged_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(seq_len, c->page_table, D.pt_stride, c->batch,
-                                                                      c->max_seq_len);
+    append_bump_paged_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(seq_len, c->page_table, D.pt_stride, 0,
+                                                                      c->batch, c->max_seq_len);
     return cudaGetLastError();
 }
 
@@ -874,6 +877,109 @@ cudaError_t launch_append_int8(const kvq_config *cfg, const kvq_int8_cache *c, c
 }
 
 // ---------------------------------------------------------------------------
+// Paged Kitty bulk writes: whole key / value pages of one kv head into the
+// pool pages of a request's page table (the same page quantizers).
+// ---------------------------------------------------------------------------
+struct KittyPagedDst {
+    const int32_t *page_table;
+    uint8_t *pool;
+    int page_cap, n_pages, Hkv, row, kvh, page0;
+    int64_t rec_bytes;
+    unsigned *err;
+};
+
+__device__ __forceinline__ uint8_t *kitty_paged_record(const KittyPagedDst &D, int p) {
+    const int pg = D.page_table[(int64_t)D.row * D.page_cap + D.page0 + p];
+    if (pg < 0 || pg >= D.n_pages) return nullptr;
+    return D.pool + ((int64_t)pg * D.Hkv + D.kvh) * D.rec_bytes;
+}
+
+__global__ void __launch_bounds__(128) quant_key_kitty_paged_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
+                                                                    int K, int score_mode, KittyPagedDst D) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    for (int64_t p = blockIdx.x; p < n_pages; p += gridDim.x) {
+        uint8_t *rec = kitty_paged_record(D, (int)p);
+        if (!rec) {
+            if (threadIdx.x == 0) atomicOr(D.err, KVQ_DEVICE_ERR_POOL);
+            continue;
+        }
+        kitty_key_page_quant(k + p * (int64_t)128 * KVQ_D, K, score_mode, rec, smem_raw);
+    }
+}
+
+__global__ void __launch_bounds__(256) quant_value_kitty_paged_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
+                                                                      KittyPagedDst D) {
+    constexpr int G = 128;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tokens; t += nwarps) {
+        uint8_t *pg = kitty_paged_record(D, (int)(t / G));
+        if (!pg) {
+            if (lane == 0) atomicOr(D.err, KVQ_DEVICE_ERR_POOL);
+            continue;
+        }
+        const int tt = (int)(t % G);
+        uint32_t wv;
+        uint16_t sv, zv;
+        value_token_quant<128>(v + t * KVQ_D, lane, wv, sv, zv);
+        if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(pg + (int64_t)tt * (KVQ_D / 4))[lane >> 2] = wv;
+        if (lane == 0) {
+            uint16_t *ps = reinterpret_cast<uint16_t *>(pg + (int64_t)G * KVQ_D / 4);
+            ps[tt] = sv;
+            ps[G + tt] = zv;
+        }
+    }
+}
+
+static KittyPagedDst kitty_paged_dst(const kvq_config *cfg, const kvq_kitty_cache *c, const void *pool, int64_t rec,
+                                     int page0, int row, int kvh) {
+    KittyPagedDst D;
+    D.page_table = c->page_table;
+    D.pool = static_cast<uint8_t *>(const_cast<void *>(pool));
+    D.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + 127) / 128;
+    if (D.page_cap < 1) D.page_cap = 1;
+    D.n_pages = c->n_pages;
+    D.Hkv = cfg->n_kv_heads;
+    D.row = row;
+    D.kvh = kvh;
+    D.page0 = page0;
+    D.rec_bytes = rec;
+    D.err = device_error_ptr();
+    return D;
+}
+
+cudaError_t launch_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k, int64_t n,
+                                         int page0, int row, int kvh, int score_mode, cudaStream_t st) {
+    const int64_t kpb = (int64_t)KVQ_D * 128 / 4 + (int64_t)cfg->boost_k * 128 / 4 + KVQ_D + 4LL * KVQ_D;
+    const KittyPagedDst D = kitty_paged_dst(cfg, c, c->k_pages, kpb, page0, row, kvh);
+    if (!D.err) return cudaErrorInvalidDevicePointer;
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(quant_key_kitty_paged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)KITTY_KEY_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    const int grid = grid_cap(n, 4);
+    quant_key_kitty_paged_kernel<<<grid, 128, KITTY_KEY_SMEM, st>>>(static_cast<const uint16_t *>(k), n, cfg->boost_k,
+                                                                    score_mode, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_value_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *v, int64_t n,
+                                           int page0, int row, int kvh, cudaStream_t st) {
+    const int64_t vpb = 128LL * KVQ_D / 4 + 4LL * 128;
+    const KittyPagedDst D = kitty_paged_dst(cfg, c, c->v_pages, vpb, page0, row, kvh);
+    if (!D.err) return cudaErrorInvalidDevicePointer;
+    const int64_t n_tokens = n * 128;
+    const int grid = grid_cap((n_tokens + 7) / 8, 16);
+    quant_value_kitty_paged_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens, D);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Streaming append (Kitty): one CTA of 128 threads per (batch row, kv head).
 // With L = seq_len[b] cached it completes the quantization that follows the
 // attention of the step with L tokens, then inserts token L (Kitty, "Stage 1:
@@ -894,7 +1000,22 @@ struct AppendKittyParams {
     unsigned *err;
     int Hkv, S, R, K, score_mode, max_seq_len, page_cap;
     int64_t kpb, vpb;
+    const int32_t *page_table;   // paged cache: pools [n_pages][Hkv][record]; null: per-request arrays
+    int n_pages;
 };
+
+// Record index of logical page p of (row b, kv head h): per-request arrays,
+// or the pool page of the page table (-1, KVQ_DEVICE_ERR_POOL recorded, for
+// an entry outside the pool).
+__device__ __forceinline__ int64_t kitty_record(const AppendKittyParams &P, int b, int h, int p) {
+    if (!P.page_table) return ((int64_t)b * P.Hkv + h) * P.page_cap + p;
+    const int pg = P.page_table[(int64_t)b * P.page_cap + p];
+    if (pg < 0 || pg >= P.n_pages) {
+        if (threadIdx.x == 0) atomicOr(P.err, KVQ_DEVICE_ERR_POOL);
+        return -1;
+    }
+    return (int64_t)pg * P.Hkv + h;
+}
 
 __global__ void __launch_bounds__(128) append_kitty_kernel(AppendKittyParams P) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -908,16 +1029,20 @@ __global__ void __launch_bounds__(128) append_kitty_kernel(AppendKittyParams P) 
         return;
     }
     const int S = P.S, R = P.R;
+    const int h = (int)(bk - (int64_t)b * P.Hkv);
+    // paged: a row whose next page could not be allocated is left unchanged
+    if (P.page_table && L >= S && (L - S) % G == 0 && P.page_table[(int64_t)b * P.page_cap + (L - S) / G] < 0) return;
     uint16_t *kqb = P.k_qbuf + bk * G * KVQ_D;
     uint16_t *vqb = P.v_qbuf + bk * G * KVQ_D;
     uint16_t *vloc = P.v_local + bk * (int64_t)R * KVQ_D;
     if (L > S && (L - S) % G == 0) {
-        const int p = (L - S) / G - 1;
-        kitty_key_page_quant(kqb, P.K, P.score_mode, P.k_pages + (bk * P.page_cap + p) * P.kpb, smem_raw);
+        const int64_t rec = kitty_record(P, b, h, (L - S) / G - 1);
+        if (rec >= 0) kitty_key_page_quant(kqb, P.K, P.score_mode, P.k_pages + rec * P.kpb, smem_raw);
     }
     const int E = L - S - R;
-    if (E > 0 && E % G == 0) {
-        uint8_t *pg = P.v_pages + (bk * P.page_cap + (E / G - 1)) * P.vpb;
+    const int64_t vrec = E > 0 && E % G == 0 ? kitty_record(P, b, h, E / G - 1) : -1;
+    if (vrec >= 0) {
+        uint8_t *pg = P.v_pages + vrec * P.vpb;
         uint16_t *ps = reinterpret_cast<uint16_t *>(pg + (int64_t)G * KVQ_D / 4);
         for (int tt = warp; tt < G; tt += 4) {
             uint32_t wv;
@@ -952,8 +1077,8 @@ __global__ void __launch_bounds__(128) append_kitty_kernel(AppendKittyParams P) 
     }
 }
 
-cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new, const void *v_new,
-                                int score_mode, cudaStream_t st) {
+static cudaError_t launch_append_kitty_impl(const kvq_config *cfg, const kvq_kitty_cache *c, const kvq_slot_pool *pool,
+                                           const void *k_new, const void *v_new, int score_mode, cudaStream_t st) {
     AppendKittyParams P;
     P.seq_len = c->seq_len;
     P.k_new = static_cast<const uint16_t *>(k_new);
@@ -972,6 +1097,8 @@ cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
     P.R = cfg->residual;
     P.K = cfg->boost_k;
     P.score_mode = score_mode;
+    P.page_table = c->page_table;
+    P.n_pages = c->n_pages;
     P.max_seq_len = c->max_seq_len;
     P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + 127) / 128;
     if (P.page_cap < 1) P.page_cap = 1;
@@ -986,12 +1113,31 @@ cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
         if (e != cudaSuccess) return e;
         attr_dev = dev;
     }
+    if (c->page_table) {
+        cudaError_t e = launch_alloc_ids(c->seq_len, const_cast<int32_t *>(c->page_table), c->batch, c->max_seq_len,
+                                         128, P.page_cap, cfg->sink, pool, st);
+        if (e != cudaSuccess) return e;
+    }
     append_kitty_kernel<<<(unsigned)((int64_t)c->batch * cfg->n_kv_heads), 128, KITTY_KEY_SMEM, st>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,
-                                                                c->max_seq_len);
+    if (c->page_table)
+        append_bump_paged_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(
+            const_cast<int32_t *>(c->seq_len), c->page_table, P.page_cap, cfg->sink, c->batch, c->max_seq_len);
+    else
+        append_bump_kernel<<<(c->batch + 127) / 128, 128, 0, st>>>(const_cast<int32_t *>(c->seq_len), c->batch,
+                                                                    c->max_seq_len);
     return cudaGetLastError();
+}
+
+cudaError_t launch_append_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const kvq_slot_pool *pool,
+                                      const void *k_new, const void *v_new, int score_mode, cudaStream_t st) {
+    return launch_append_kitty_impl(cfg, c, pool, k_new, v_new, score_mode, st);
+}
+
+cudaError_t launch_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new, const void *v_new,
+                                int score_mode, cudaStream_t st) {
+    return launch_append_kitty_impl(cfg, c, nullptr, k_new, v_new, score_mode, st);
 }
 
 cudaError_t launch_philox(const uint32_t *ctr, const uint32_t *key, int64_t n, uint32_t *out, cudaStream_t st) {

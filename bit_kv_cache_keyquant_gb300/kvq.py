@@ -51,7 +51,8 @@ class kvq_kivi_paged_cache(ctypes.Structure):
 class kvq_kitty_cache(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("seq_len", _P),
                 ("k_pages", _P), ("v_pages", _P), ("k_sink", _P), ("v_sink", _P), ("k_qbuf", _P),
-                ("v_qbuf", _P), ("v_local", _P)]
+                ("v_qbuf", _P), ("v_local", _P), ("page_table", _P),
+                ("n_pages", ctypes.c_int32)]
 
 
 class kvq_slot_pool(ctypes.Structure):
@@ -91,6 +92,11 @@ def _load():
                                      _P, _P]),
         "kv_release_kivi_paged": (S, [ctypes.POINTER(kvq_kivi_paged_cache), i32, ctypes.POINTER(kvq_slot_pool), _P]),
         "kv_decode_attn_kivi_paged": (S, [cfgp, ctypes.POINTER(kvq_kivi_paged_cache), _P, _P, _P, sz, _P]),
+        "kv_quant_key_kitty_paged": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), _P, i64, i32, i32, i32, i32, _P]),
+        "kv_quant_value_kitty_paged": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), _P, i64, i32, i32, i32, _P]),
+        "kv_append_kitty_paged": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), ctypes.POINTER(kvq_slot_pool), _P, _P,
+                                      i32, _P]),
+        "kv_release_kitty": (S, [cfgp, ctypes.POINTER(kvq_kitty_cache), i32, ctypes.POINTER(kvq_slot_pool), _P]),
         "kv_quant_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), _P, i64, _P, i32, _P]),
         "kv_slot_pool_init": (S, [ctypes.POINTER(kvq_slot_pool), _P]),
         "kv_append_int8_token": (S, [cfgp, ctypes.POINTER(kvq_int8_token_cache), ctypes.POINTER(kvq_slot_pool), _P,
@@ -127,7 +133,8 @@ EXPORTED = ("kv_quant_key", "kv_quant_value", "kv_append_kivi", "kv_append_int8"
             "kv_quant_key_kitty", "kv_quant_value_kitty", "kv_quant_int8_dither", "kv_quant_int8_token",
             "kv_slot_pool_init", "kv_append_int8_token", "kv_release_int8_token", "kvq_kivi_page_bytes",
             "kv_quant_key_paged", "kv_quant_value_paged", "kv_append_kivi_paged", "kv_release_kivi_paged",
-            "kv_decode_attn_kivi_paged",
+            "kv_decode_attn_kivi_paged", "kv_quant_key_kitty_paged", "kv_quant_value_kitty_paged",
+            "kv_append_kitty_paged", "kv_release_kitty",
             "kvq_kitty_key_page_bytes", "kvq_kitty_value_page_bytes", "kv_decode_attn_plan", "kv_decode_attn",
             "kv_decode_attn_kitty", "kv_decode_attn_int8", "kv_decode_attn_int8_token", "kv_decode_attn_noalloc",
             "kv_decode_attn_stage1", "kv_decode_attn_merge",
@@ -236,6 +243,26 @@ def kv_decode_attn_kivi_paged(cfg, cache, q, out, workspace, workspace_bytes, st
     _check(_lib.kv_decode_attn_kivi_paged(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out),
                                           _ptr(workspace), workspace_bytes, _stream(stream)),
            "kv_decode_attn_kivi_paged")
+
+
+def kv_quant_key_kitty_paged(cfg, cache, k, n_pages, page0, row, kv_head, score_mode=0, stream=None):
+    _check(_lib.kv_quant_key_kitty_paged(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k), n_pages, page0, row, kv_head,
+                                         score_mode, _stream(stream)), "kv_quant_key_kitty_paged")
+
+
+def kv_quant_value_kitty_paged(cfg, cache, v, n_pages, page0, row, kv_head, stream=None):
+    _check(_lib.kv_quant_value_kitty_paged(ctypes.byref(cfg), ctypes.byref(cache), _ptr(v), n_pages, page0, row,
+                                           kv_head, _stream(stream)), "kv_quant_value_kitty_paged")
+
+
+def kv_append_kitty_paged(cfg, cache, pool, k_new, v_new, score_mode=0, stream=None):
+    _check(_lib.kv_append_kitty_paged(ctypes.byref(cfg), ctypes.byref(cache), ctypes.byref(pool), _ptr(k_new),
+                                      _ptr(v_new), score_mode, _stream(stream)), "kv_append_kitty_paged")
+
+
+def kv_release_kitty(cfg, cache, row, pool, stream=None):
+    _check(_lib.kv_release_kitty(ctypes.byref(cfg), ctypes.byref(cache), row, ctypes.byref(pool), _stream(stream)),
+           "kv_release_kitty")
 
 
 def kv_quant_int8_token(cfg, cache, x, n, slots, kv_sel, stream=None):

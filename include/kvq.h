@@ -309,6 +309,13 @@ typedef struct {
     const void *k_qbuf;      /* fp16 [B][Hkv][G][D] */
     const void *v_qbuf;      /* fp16 [B][Hkv][G][D] */
     const void *v_local;     /* fp16 [B][Hkv][R][D] */
+    /* Paged form (page_table non-null): key and value page records come from
+     * shared pools k_pages [n_pages][Hkv][key page record] and v_pages
+     * [n_pages][Hkv][value page record]; logical page j of request b (tokens
+     * S + G j .. S + G j + G - 1, keys and values) is physical page
+     * page_table[b][j], int32 [B][P].  NULL: the per-request arrays above. */
+    const int32_t *page_table;
+    int32_t n_pages;
 } kvq_kitty_cache;
 
 /* Streaming append of one token per (batch row, kv head) to a Kitty cache,
@@ -328,6 +335,31 @@ typedef struct {
  * KVQ_DEVICE_ERR_CAPACITY is recorded. */
 KVQ_API kvq_status kv_append_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k_new,
                                    const void *v_new, int score_mode, cudaStream_t stream);
+
+/* a5 / a6 into a paged Kitty cache: n_pages key (value) pages, fp16
+ * [n_pages][G][D] of kv head kv_head, that are logical pages page0 .. of
+ * request `row`, quantized into the pool pages page_table[row] names.  Same
+ * arithmetic as kv_quant_key_kitty / kv_quant_value_kitty. */
+KVQ_API kvq_status kv_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k,
+                                            int64_t n_pages, int32_t page0, int32_t row, int32_t kv_head,
+                                            int32_t score_mode, cudaStream_t stream);
+KVQ_API kvq_status kv_quant_value_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *v,
+                                              int64_t n_pages, int32_t page0, int32_t row, int32_t kv_head,
+                                              cudaStream_t stream);
+
+/* Streaming append to a paged Kitty cache, as kv_append_kitty: a row whose
+ * L = seq_len[b] is S + G j first takes pool page j for its next tokens
+ * (rows in order of b, from the top of the free stack; deterministic under
+ * graph replay).  A row that needs a page when too few are free is left
+ * unchanged and KVQ_DEVICE_ERR_POOL is recorded.  Three kernels. */
+KVQ_API kvq_status kv_append_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const kvq_slot_pool *pool,
+                                         const void *k_new, const void *v_new, int32_t score_mode,
+                                         cudaStream_t stream);
+
+/* Return the pages of request `row` (logical pages 0 .. ceil(max(seq_len-S, 0)/G) - 1)
+ * of a paged Kitty cache to the pool and set seq_len[row] = 0. */
+KVQ_API kvq_status kv_release_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, int32_t row,
+                                    const kvq_slot_pool *pool, cudaStream_t stream);
 
 /* INT8 dither: the first L - n_tail tokens are quantized in blocks of T,
  * n_tail = ((L-1) mod T) + 1 tokens of the active block stay fp16 (slot

@@ -156,6 +156,27 @@ def test_kivi_paged_validation_without_gpu(K):
                 None) == K.KVQ_ERR_UNSUPPORTED
 
 
+def test_kitty_paged_validation_without_gpu(K):
+    cfg = K.make_config(n_q_heads=8, n_kv_heads=2, group_k=128)
+    dense = K.kvq_kitty_cache(2, 1000, 16, 16, 16, 16, 16, 16, 16, 16)
+    paged = K.kvq_kitty_cache(2, 1000, 16, 16, 16, 16, 16, 16, 16, 16, 16, 8)
+    pool = K.kvq_slot_pool(8, 16, 16)
+    call = K.raw_call
+    assert call("kv_append_kitty", ctypes.byref(cfg), ctypes.byref(paged), 16, 16, 0, None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_append_kitty_paged", ctypes.byref(cfg), ctypes.byref(dense), ctypes.byref(pool), 16, 16, 0,
+                None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_append_kitty_paged", ctypes.byref(cfg), ctypes.byref(paged), ctypes.byref(pool), 16, 16, 3,
+                None) == K.KVQ_ERR_INVALID_ARG
+    assert call("kv_quant_key_kitty_paged", ctypes.byref(cfg), ctypes.byref(paged), 0x1008, 8, 0, 0, 0, 0, None) == \
+        K.KVQ_ERR_MISALIGNED                                           # 8 = ceil((1000 - 32) / 128) pages fit
+    assert call("kv_quant_key_kitty_paged", ctypes.byref(cfg), ctypes.byref(paged), 16, 9, 0, 0, 0, 0, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert call("kv_quant_value_kitty_paged", ctypes.byref(cfg), ctypes.byref(paged), 16, 1, 0, 0, 2, None) == \
+        K.KVQ_ERR_INVALID_ARG
+    assert call("kv_release_kitty", ctypes.byref(cfg), ctypes.byref(dense), 0, ctypes.byref(pool), None) == \
+        K.KVQ_ERR_INVALID_ARG
+
+
 def test_decode_plan_and_workspace_checks(K):
     cfg = K.make_config()
     n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, 32, 4096)
