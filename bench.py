@@ -316,6 +316,22 @@ def launches_per_step(w) -> int:
     return {"kivi": 4, "kitty": 4, "int8": 4, "int8t": 4}[w.variant]
 
 
+def job_time_ms(local_ms: float, world: int, device=None) -> float:
+    """The job's timed-region length: the max over ranks of each rank's (one collective, the only one)."""
+    if world == 1:
+        return local_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_step(job_ms: float, steps: int, world: int) -> float:
+    """us per layer-step of the whole job: `world` replicas each ran `steps` layer-steps in job_ms."""
+    return job_ms * 1e3 / (steps * world)
+
+
 def run_gpu(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -356,10 +372,7 @@ def run_gpu(args, w, rank, world, local_rank):
     quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
     merge_ms = [e[3].elapsed_time(e[4]) for e in evs]
     assert kvq.kvq_get_device_error() == 0
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = job_time_ms(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
 
     # ---- end to end through the C ABI with host buffers ----
@@ -383,11 +396,7 @@ def run_gpu(args, w, rank, world, local_rank):
         outh.copy_(st["out"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = job_time_ms(e0.elapsed_time(e1), world, dev)
     h2d = qh.numel() * 2 + vh.numel() * 2 + kh.numel() * 2
     d2h = outh.numel() * 2
 
@@ -415,8 +424,7 @@ def run_gpu(args, w, rank, world, local_rank):
         cpu = {"value": per_pair * w.batch * w.n_kv_heads * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} (batch row, kv head) pairs of the workload, single thread, scaled by "
                          f"{w.batch * w.n_kv_heads} pairs per layer-step"}
-    n_steps_total = args.steps * world
-    value = total_ms * 1e3 / n_steps_total if world > 1 else ms_per_step * 1e3
+    value = whole_job_us_per_step(total_ms, args.steps, world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
@@ -435,7 +443,7 @@ def run_gpu(args, w, rank, world, local_rank):
                      "traffic": traffic, "peak_kind": peak_kind, "kernel": kname + " (stage 1)",
                      "alg_bytes_per_launch": alg_bytes_stage1},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_ms * 1e3 / args.steps / (world if world > 1 else 1), "unit": UNIT,
+        "e2e": {"value": whole_job_us_per_step(e2e_ms, args.steps, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
