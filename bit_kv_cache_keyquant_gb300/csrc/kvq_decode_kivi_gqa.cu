@@ -36,15 +36,15 @@ namespace kvq {
 
 namespace {
 
-constexpr int GQ_NSTAGE = 3;
 constexpr int GMAX = 4;                   // query heads per unit (n = 8 tensor-core columns)
 constexpr int PB_ROW = 40;                // p exchange row: 32 tokens + 8 floats (conflict-free)
 constexpr int ACC_ROW = KVQ_D + 8;
 
+template <int BK, int BV, int NST>
 struct SmemG {
-    uint8_t stage[GQ_NSTAGE][STAGE_BYTES];
-    uint64_t full[GQ_NSTAGE];
-    uint64_t empty[GQ_NSTAGE];
+    uint8_t stage[NST][Geo<BK, BV>::BYTES];
+    uint64_t full[NST];
+    uint64_t empty[NST];
     uint32_t qhi[GMAX][64];               // fp16x2 hi parts of alpha q 2^sigma: [head][k/2][r][4]
     uint32_t qlo[GMAX][64];               // fp16x2 lo parts, same order
     float qz[GMAX][KVQ_D];                // alpha q (fp32): [head][k][r][4]
@@ -57,10 +57,13 @@ struct SmemG {
 
 }  // namespace
 
-template <int NGV>
+// BK-bit keys and BV-bit values (2 or 4) in an NST-stage ring.
+template <int NGV, int BK, int BV, int NST>
 __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(Params P) {
+    using GG = Geo<BK, BV>;
+    constexpr int GQ_NSTAGE = NST;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    SmemG &S = *reinterpret_cast<SmemG *>(smem_raw);
+    SmemG<BK, BV, NST> &S = *reinterpret_cast<SmemG<BK, BV, NST> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = P.Hq / P.Hkv;
     const int n_units = P.B * P.Hkv * P.splits;
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kivi_produce<GQ_NSTAGE, true>(P, P.Hkv, S.stage, S.full, S.empty);
+        if (lane == 0) kivi_produce<GQ_NSTAGE, true, BK, BV>(P, P.Hkv, S.stage, S.full, S.empty);
         return;
     }
 
@@ -88,7 +91,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     const uint32_t vsel = (uint32_t)((q >> 2) | ((4 + (q >> 2)) << 4) | ((2 + (q >> 2)) << 8) | ((6 + (q >> 2)) << 12));
     const uint32_t vshift = (q & 2) ? 4u : 0u;
     const uint32_t vmask = (q & 1) ? 0x0C0C0C0Cu : 0x03030303u;
-    const float vscale = (q & 1) ? 128.f : 512.f;
+    // 4-bit values: channel 16mt + q (+8) is byte q/2 of the m-tile's first (second) word, bits 4(q%2)
+    const uint32_t vsel4 = (uint32_t)((q >> 1) | ((4 + (q >> 1)) << 4));
+    const uint32_t vshift4 = (q & 1) ? 4u : 0u;
+    const float vscale = BV == 4 ? 512.f : ((q & 1) ? 128.f : 512.f);
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                 const int tile = s * NCWARP + warp;
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];
-                    const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + KC_BYTES) + gl * 2 * KVQ_D;
+                    const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + GG::KC) + gl * 2 * KVQ_D;
                     // ---- alpha sum_c q_hc z_c: the lanes of head hB split the lane's 32 channels by xB ----
                     float zr;
                     {
@@ -187,10 +193,18 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     //      hi or lo) of channels 16k + 2r + {0,1 | 8,9} made two k-steps at a time ----
                     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
                     {
-                        const uint8_t *kt = st + warp * 1024;
+                        // BK = 4: plane 0 holds tokens p = 0, 1, plane 1 tokens p = 2, 3, a nibble each
+                        const uint8_t *kt = st + warp * 512 * BK;
                         const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
                         const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
                         const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                        uint32_t kw1[8];
+                        if (BK == 4) {
+                            const uint4 kc = *reinterpret_cast<const uint4 *>(kt + 1024 + lane * 16);
+                            const uint4 kd = *reinterpret_cast<const uint4 *>(kt + 1536 + lane * 16);
+                            kw1[0] = kc.x; kw1[1] = kc.y; kw1[2] = kc.z; kw1[3] = kc.w;
+                            kw1[4] = kd.x; kw1[5] = kd.y; kw1[6] = kd.z; kw1[7] = kd.w;
+                        }
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
@@ -203,17 +217,25 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                                 const int k = 2 * i + kk;
                                 const uint32_t w = kw[k], w4 = kw[k] >> 4;
                                 uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
-                                e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
-                                e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
-                                e4m3x4_f16x2(w4 & 0x03030303u, a2l, a2h);
-                                e4m3x4_f16x2(w4 & 0x0C0C0C0Cu, a3l, a3h);
+                                if (BK == 2) {
+                                    e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
+                                    e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
+                                    e4m3x4_f16x2(w4 & 0x03030303u, a2l, a2h);
+                                    e4m3x4_f16x2(w4 & 0x0C0C0C0Cu, a3l, a3h);
+                                } else {
+                                    // a nibble in bits 0-3 is the e4m3 pattern of code * 2^-9 (exact, linear)
+                                    e4m3x4_f16x2(w & 0x0F0F0F0Fu, a0l, a0h);
+                                    e4m3x4_f16x2(w4 & 0x0F0F0F0Fu, a1l, a1h);
+                                    e4m3x4_f16x2(kw1[k] & 0x0F0F0F0Fu, a2l, a2h);
+                                    e4m3x4_f16x2((kw1[k] >> 4) & 0x0F0F0F0Fu, a3l, a3h);
+                                }
                                 mma16816(s0, a0l, a1l, a0h, a1h, bk[2 * kk], bk[2 * kk + 1]);
                                 mma16816(s1, a2l, a3l, a2h, a3h, bk[2 * kk], bk[2 * kk + 1]);
                             }
                         }
                     }
                     // ---- logits of head r, tokens q, q+8, q+16, q+24; online softmax ----
-                    const float f9 = unsig * 512.f, f7 = unsig * 128.f;
+                    const float f9 = unsig * 512.f, f7 = BK == 4 ? f9 : unsig * 128.f;
                     float lg[4];
                     lg[0] = fmaf(s0[0] + s0[1], f9, zr);
                     lg[1] = fmaf(s0[2] + s0[3], f7, zr);
@@ -246,7 +268,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pb[r * PB_ROW + 8 * i + 2 * (q & 3) + (q >> 2)] = pr[i];
                     // ---- value zero-point term of head r over the lane's four tokens ----
-                    const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + KC_BYTES + KSZ_MAX + VC_BYTES) +
+                    const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + GG::KC + GG::KSZ + GG::VC) +
                                           warp * 32 * NGV;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -258,7 +280,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     __syncwarp();
                     // ---- values: two 16-token k-steps x eight 16-channel m-tiles; k-column 2j + e + 8hk of
                     //      k-step k is token 16k + 8hk + 4e + j (rows of one load on distinct banks) ----
-                    const uint8_t *vc = st + KC_BYTES + KSZ_MAX + warp * 32 * (KVQ_D / 4);
+                    const uint8_t *vc = st + GG::KC + GG::KSZ + warp * 32 * (KVQ_D * BV / 8);
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const int t0 = 16 * ks + r;             // tokens t0, t0+4 | t0+8, t0+12
@@ -280,6 +302,32 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                                 bv1[j] = split_prod(phc, plc, prmt(rc[j], rd[j], 0x5410u), xB);
                             }
                         }
+                        if (BV == 4) {
+                            // 32 channels (two m-tiles) per quarter: 16 bytes of each of the lane's token rows
+#pragma unroll
+                            for (int qt = 0; qt < 4; ++qt) {
+                                const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 64 + 16 * qt);
+                                const uint4 rB = *reinterpret_cast<const uint4 *>(vc + (t0 + 4) * 64 + 16 * qt);
+                                const uint4 rC = *reinterpret_cast<const uint4 *>(vc + (t0 + 8) * 64 + 16 * qt);
+                                const uint4 rD = *reinterpret_cast<const uint4 *>(vc + (t0 + 12) * 64 + 16 * qt);
+                                const uint32_t wa[4] = {rA.x, rA.y, rA.z, rA.w}, wb[4] = {rB.x, rB.y, rB.z, rB.w};
+                                const uint32_t wc[4] = {rC.x, rC.y, rC.z, rC.w}, wd[4] = {rD.x, rD.y, rD.z, rD.w};
+#pragma unroll
+                                for (int m2 = 0; m2 < 2; ++m2) {
+                                    const int mt = 2 * qt + m2;
+                                    const int j = (16 * mt) / (KVQ_D / NGV);
+                                    // channel q of tokens (a, b) | channel q + 8 of tokens (a, b)
+                                    const uint32_t x0 = prmt(prmt(wa[2 * m2], wb[2 * m2], vsel4),
+                                                             prmt(wa[2 * m2 + 1], wb[2 * m2 + 1], vsel4), 0x5410u);
+                                    const uint32_t x1 = prmt(prmt(wc[2 * m2], wd[2 * m2], vsel4),
+                                                             prmt(wc[2 * m2 + 1], wd[2 * m2 + 1], vsel4), 0x5410u);
+                                    uint32_t c0l, c0h, c8l, c8h;
+                                    e4m3x4_f16x2((x0 >> vshift4) & 0x0F0F0F0Fu, c0l, c0h);
+                                    e4m3x4_f16x2((x1 >> vshift4) & 0x0F0F0F0Fu, c8l, c8h);
+                                    mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0[j], bv1[j]);
+                                }
+                            }
+                        } else
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
                             const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 32 + 16 * hf);
@@ -355,39 +403,48 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     }
 }
 
-// 2-bit keys and values only (4-bit widths run on the per-head kernel)
+// any value group at 2/2 bits; with a 4-bit width the value group must be 32 channels (other
+// 4-bit configurations run on the per-head kernel)
 bool kivi_gqa_supported(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;
-    return g >= 2 && g <= GMAX && cfg->bits_k == 2 && cfg->bits_v == 2;
+    if (g < 2 || g > GMAX) return false;
+    if (cfg->bits_k == 2 && cfg->bits_v == 2) return true;
+    return cfg->group_v == 32;
+}
+
+template <int NGV, int BK, int BV, int NST>
+static cudaError_t launch_gqa_variant(const Params &P, int64_t grid, cudaStream_t st) {
+    const size_t smem = sizeof(SmemG<BK, BV, NST>);
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kivi_decode_gqa_kernel<NGV, BK, BV, NST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    kivi_decode_gqa_kernel<NGV, BK, BV, NST><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, const void *q, const DecodePlan &p,
                                    void *ws, cudaStream_t st) {
     Params P = kivi_params(cfg, c, q, p, ws);
     if (!P.err) return cudaErrorInvalidDevicePointer;
-    const size_t smem = sizeof(SmemG);
-    const int ngv = P.ngv;
-    static int attr_dev[3] = {-1, -1, -1};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int ti = ngv == 4 ? 0 : (ngv == 2 ? 1 : 2);
-    if (attr_dev[ti] != dev) {
-        cudaError_t e = ngv == 4   ? cudaFuncSetAttribute(kivi_decode_gqa_kernel<4>,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                        : ngv == 2 ? cudaFuncSetAttribute(kivi_decode_gqa_kernel<2>,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                                   : cudaFuncSetAttribute(kivi_decode_gqa_kernel<1>,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev[ti] = dev;
-    }
     const int64_t n_units = (int64_t)c.batch * cfg->n_kv_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
-    if (ngv == 4) kivi_decode_gqa_kernel<4><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
-    else if (ngv == 2) kivi_decode_gqa_kernel<2><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
-    else kivi_decode_gqa_kernel<1><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
-    return cudaGetLastError();
+    const int ngv = P.ngv;
+    // 2/2 bits: three 12 KiB stages; with 4-bit codes (Gv = 32 only) two stages of up to 20 KiB
+    if (cfg->bits_k == 2 && cfg->bits_v == 2) {
+        if (ngv == 4) return launch_gqa_variant<4, 2, 2, 3>(P, grid, st);
+        if (ngv == 2) return launch_gqa_variant<2, 2, 2, 3>(P, grid, st);
+        return launch_gqa_variant<1, 2, 2, 3>(P, grid, st);
+    }
+    if (cfg->bits_k == 4 && cfg->bits_v == 4) return launch_gqa_variant<4, 4, 4, 2>(P, grid, st);
+    if (cfg->bits_k == 4) return launch_gqa_variant<4, 4, 2, 2>(P, grid, st);
+    return launch_gqa_variant<4, 2, 4, 2>(P, grid, st);
 }
 
 }  // namespace kvq

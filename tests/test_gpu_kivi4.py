@@ -96,7 +96,10 @@ def _oracle(orc, cfg, Ks, Vs, q, lens):
 @pytest.mark.parametrize("shape", [
     # (Hq, Hkv, lengths, G, Gv, R)
     (2, 2, [1, 33, 129, 700], 32, 32, 128),
-    (4, 1, [1000, 1537], 64, 32, 128),        # grouped query heads: per-head kernel at 4 bits
+    (4, 1, [1000, 1537], 64, 32, 128),        # grouped query heads, Gv = 32: tensor-core kernel at 4 bits
+    (8, 2, [97, 2049], 32, 32, 128),
+    (6, 2, [700, 1300], 128, 32, 256),        # 3 heads per kv head (one dead column pair)
+    (4, 2, [800, 1100], 32, 64, 128),         # Gv = 64 at 4 bits: per-head kernel
     (2, 2, [640, 2000], 128, 128, 128),
     (3, 3, [900, 257], 32, 64, 64),
 ])
