@@ -454,7 +454,7 @@ def run_gpu(args, w, rank, world, local_rank):
 def stage1_kernel(w):
     """Name and source files of the stage-1 kernel the library runs for workload w."""
     g = w.n_q_heads // w.n_kv_heads
-    if w.variant == "kivi" and 2 <= g <= 4 and w.bits_k == 2 and w.bits_v == 2:
+    if w.variant == "kivi" and 2 <= g <= 4:
         return "kivi_decode_gqa_kernel", ("kvq_decode_kivi_gqa.cu", "kvq_kivi.cuh", "kvq_mma.cuh", "kvq_device.cuh")
     if w.variant == "kivi":
         return "kivi_decode_kernel", ("kvq_decode_kivi.cu", "kvq_kivi.cuh", "kvq_device.cuh")
@@ -484,7 +484,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8],
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
                     help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
