@@ -113,3 +113,47 @@ def test_int8_workload_full_size_sampled(K, orc):
         # the int8 codes and scales written on the GPU are bit-exact
         assert np.array_equal(cache.k_codes[b, h, :256].cpu().numpy(), parts[0][:256])
         assert np.array_equal(cache.v_scale[b, h, 1].cpu().numpy().view(np.uint16), parts[3][1])
+
+
+@pytest.mark.slow
+def test_int8_offsets_beyond_2gib(K, orc):
+    """Maximum-size addressing: int8 code arrays of 2.3 GB each (B16, 64 query / 16 kv heads, 69632 tokens).
+    Random codes and scales fill every row; the first and the last (row, kv head) hold real data (the last
+    at byte offsets beyond 2^31) and are checked against the oracle."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hq, Hkv, L = 16, 64, 16, 69632
+    layer, seed = 2, 0x1234567890
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    cache = C.Int8Cache(cfg, B, L, layer=layer, seed=seed, device=DEV)
+    assert (B * Hkv - 1) * L * 128 > 2 ** 31          # the last (row, kv head) starts past 2^31 bytes
+    gen = torch.Generator(device=DEV).manual_seed(4)
+    cache.k_codes.random_(-127, 128, generator=gen)
+    cache.v_codes.random_(-127, 128, generator=gen)
+    cache.k_scale.uniform_(0.0, 0.05, generator=gen)
+    cache.v_scale.uniform_(0.0, 0.05, generator=gen)
+    cache.k_tail.normal_(generator=gen)
+    cache.v_tail.normal_(generator=gen)
+    cache.seq_len.fill_(L)
+    rng = np.random.default_rng(13)
+    reqs = [11, 12]
+    rows = {}
+    for (b, h), rid in zip(((0, 0), (B - 1, Hkv - 1)), reqs):
+        Kh = (rng.standard_normal((L, 128)) * 10.0 ** rng.uniform(-1, 1, 128)).astype(np.float16)
+        Vh = rng.standard_normal((L, 128)).astype(np.float16)
+        cache.fill(b, h, torch.from_numpy(Kh).to(DEV), torch.from_numpy(Vh).to(DEV), rid)
+        rows[(b, h)] = (Kh, Vh, rid)
+    q = torch.from_numpy(rng.standard_normal((B, Hq, 128)).astype(np.float16)).to(DEV)
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_INT8, B, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn_int8(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    assert np.isfinite(outn).all()
+    g = Hq // Hkv
+    for (b, h), (Kh, Vh, rid) in rows.items():
+        parts = orc.int8_build_one(Kh, Vh, seed, rid, layer, h)
+        want = orc.int8_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *parts, L=L, seed=seed, request=rid,
+                                   layer=layer, kv_head=h)
+        assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")

@@ -101,3 +101,48 @@ def test_kitty_workload_full_size_sampled(K, orc):
         assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
         # the key pages written on the GPU are bit-exact too
         assert np.array_equal(cache.k_pages[b, h, 5].cpu().numpy(), parts[0][5])
+
+
+@pytest.mark.slow
+def test_kitty_offsets_beyond_2gib(K, orc):
+    """Maximum-size addressing: key page records spanning 2.2 GB (B32, 64 query / 16 kv heads, 104992 tokens).
+    Random bytes fill every page; the first and the last (row, kv head) hold real data (the last at byte
+    offsets beyond 2^31) and are checked against the oracle."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hq, Hkv, L = 32, 64, 16, 32 + 820 * 128
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv, group_k=128, sink=32, residual=128, boost_k=16)
+    cache = C.KittyCache(cfg, B, L, device=DEV)
+    assert (B * Hkv - 1) * 820 * cache.kpb > 2 ** 31   # the last (row, kv head) starts past 2^31 bytes
+    gen = torch.Generator(device=DEV).manual_seed(3)
+    # random codes; s, z of every page set to small fp16 values; idx left 0 (boost rank 0)
+    cache.k_pages.random_(0, 256, generator=gen)
+    cache.v_pages.random_(0, 256, generator=gen)
+    kpb, vpb = cache.kpb, cache.vpb
+    cache.k_pages[..., kpb - 512:].view(torch.float16).uniform_(0.0, 0.2, generator=gen)
+    cache.k_pages[..., kpb - 512 - 128:kpb - 512].fill_(17)            # idx: no channel boosted
+    cache.v_pages[..., vpb - 512:].view(torch.float16).uniform_(0.0, 0.2, generator=gen)
+    for t in (cache.k_sink, cache.v_sink, cache.k_qbuf, cache.v_qbuf, cache.v_local):
+        t.normal_(generator=gen)
+    cache.seq_len.fill_(L)
+    rng = np.random.default_rng(12)
+    rows = {}
+    for b, h in ((0, 0), (B - 1, Hkv - 1)):
+        sig = 0.5 * 16.0 ** rng.random(128)
+        Kh = (rng.standard_normal((L, 128)) * sig).astype(np.float16)
+        Vh = rng.standard_normal((L, 128)).astype(np.float16)
+        cache.fill(b, h, torch.from_numpy(Kh).to(DEV), torch.from_numpy(Vh).to(DEV))
+        rows[(b, h)] = (Kh, Vh)
+    q = torch.from_numpy(rng.standard_normal((B, Hq, 128)).astype(np.float16)).to(DEV)
+    _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KITTY, B, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn_kitty(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    assert np.isfinite(outn).all()
+    g = Hq // Hkv
+    for (b, h), (Kh, Vh) in rows.items():
+        parts = orc.kitty_build_one(Kh, Vh)
+        want = orc.kitty_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *parts, L=L)
+        assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")

@@ -225,6 +225,46 @@ def test_workload_full_size_sampled(K, orc, widx):
     assert np.array_equal(cache.k_sz[1, 0, 0].cpu().numpy().view(np.uint16), orc.kivi_key_sz_pack(ksz)[0])
 
 
+@pytest.mark.slow
+def test_decode_offsets_beyond_2gib(K, orc):
+    """Maximum-size addressing: a cache whose code and parameter arrays span 4.3 GB (B32, 64 query / 16 kv
+    heads, 262144 tokens).  Random bytes fill every row; the first and the last (row, kv head) hold real
+    data (the last at byte offsets far beyond 2^31) and are checked against the oracle."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    B, Hq, Hkv, L = 32, 64, 16, 262144
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    cache = C.KiviCache(cfg, B, L, device=DEV)
+    gen = torch.Generator(device=DEV).manual_seed(5)
+    cache.k_codes.random_(0, 256, generator=gen)
+    cache.v_codes.random_(0, 256, generator=gen)
+    cache.k_sz.view(torch.float16).uniform_(0.0, 0.25, generator=gen)
+    cache.v_sz.view(torch.float16).uniform_(0.0, 0.25, generator=gen)
+    cache.k_res.normal_(generator=gen)
+    cache.v_res.normal_(generator=gen)
+    cache.seq_len.fill_(L)
+    assert (B * Hkv - 1) * L * 32 > 2 ** 31          # the last (row, kv head) starts past 2^31 bytes
+    rng = np.random.default_rng(9)
+    rows = {}
+    for b, h in ((0, 0), (B - 1, Hkv - 1)):
+        Kh = (rng.standard_normal((L, 128)) * (1 + 9 * (rng.random(128) < 0.02))).astype(np.float16)
+        Vh = rng.standard_normal((L, 128)).astype(np.float16)
+        cache.fill(b, h, torch.from_numpy(Kh).to(DEV), torch.from_numpy(Vh).to(DEV))
+        rows[(b, h)] = (Kh, Vh)
+    q = torch.from_numpy(rng.standard_normal((B, Hq, 128)).astype(np.float16)).to(DEV)
+    n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, B, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    assert np.isfinite(outn).all()
+    g = Hq // Hkv
+    for (b, h), (Kh, Vh) in rows.items():
+        want = orc.kivi_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *orc.kivi_build_one(Kh, Vh), L=L)
+        assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
+
+
 # ---------------------------------------------------------------------------
 # Philox
 # ---------------------------------------------------------------------------
