@@ -36,6 +36,24 @@ METRIC = "quantized-KV decode attention: us/layer-step and HBM GB/s (% of GB300 
 UNIT = "us/layer-step"
 
 
+# Pure Philox4x32-10 throughput of this GPU (blocks of 4 words per second): a probe kernel running the
+# decode kernels' Philox form (round keys precomputed, 32x32->64 products) over 152 x 8 CTAs x 256 threads
+# x 4 independent streams, CUDA events, 2070 MHz: 519.2 G blocks/s, i.e. 1.65 blocks (33 wide products)
+# per clock per SM.  The INT8 decode paths are bound by this arithmetic, not by HBM.
+PHILOX_PEAK_GBLOCKS = 519.2
+
+
+def philox_blocks(w, lens) -> int:
+    """Philox4x32-10 blocks one INT8 decode launch must run: one per (quantized token, kv head, side,
+    4 channels)."""
+    if w.variant == "int8":
+        T = 256
+        nq = sum(int(L) - ((int(L) - 1) % T + 1) for L in lens)
+    else:
+        nq = sum(int(L) for L in lens)
+    return nq * w.n_kv_heads * 2 * (128 // 4)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -418,6 +436,17 @@ def run_gpu(args, w, rank, world, local_rank):
         tr = json.load(open(prof)).get(f"{kname}@workload{w.index}")
         if tr and tr.get("source_hash") == kernel_source_hash(kfiles):
             traffic = tr["bytes_per_launch"]
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_kind": peak_kind, "kernel": kname + " (stage 1)",
+            "alg_bytes_per_launch": alg_bytes_stage1}
+    if w.variant in ("int8", "int8t"):
+        nb = philox_blocks(w, lens)
+        ach = nb / (s1 * 1e-3) / 1e9
+        roof = {"bound": "alu", "achieved": ach, "peak": PHILOX_PEAK_GBLOCKS, "unit": "G Philox4x32-10 blocks/s",
+                "frac": ach / PHILOX_PEAK_GBLOCKS, "traffic": traffic,
+                "peak_kind": "measured (pure Philox4x32-10 probe kernel on this GPU)",
+                "kernel": kname + " (stage 1)", "alg_philox_blocks_per_launch": nb,
+                "alg_bytes_per_launch": alg_bytes_stage1, "hbm_gbs": achieved, "hbm_frac": achieved / peak}
     cpu = None
     if world == 1 and not args.no_cpu and w.variant == "kivi":
         per_pair, n = oracle_step_seconds(w, args.cpu_budget)
@@ -439,9 +468,7 @@ def run_gpu(args, w, rank, world, local_rank):
                          "merge": 1e3 * statistics.mean(merge_ms),
                          "timing": "a second pass of the K steps with CUDA events around every kernel"},
         "hbm_gbs_step": (alg_bytes_stage1 + d2h) / (ms_per_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind, "kernel": kname + " (stage 1)",
-                     "alg_bytes_per_launch": alg_bytes_stage1},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_us_per_step(e2e_ms, args.steps, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
