@@ -300,7 +300,7 @@ def quant_step(st, stream, vnew=None, knew=None):
             kvq.kv_quant_int8_dither(cfg, x, st["n_blk"], m[0], m[1], m[2], 5, sel, w.seed, sc[0], sc[1], stream)
 
 
-def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None):
+def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None, out=None):
     """One layer-step.  The write side (quantizing the tokens that leave the
     fp16 window) runs on a second stream beside the attention: in the
     insert -> attend -> quantize order it reads only the new tokens and writes
@@ -324,7 +324,7 @@ def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None):
     if ev is not None:
         ev[3].record(stream)
     kvq.kv_decode_attn_merge(cfg, st["variant"], st["cache"].batch, st["cache"].max_seq_len, st["ws"], st["wsb"],
-                             st["out"], stream)
+                             st["out"] if out is None else out, stream)
     if ev is not None:
         ev[4].record(stream)
     stream.wait_event(st["join"])
@@ -393,30 +393,54 @@ def run_gpu(args, w, rank, world, local_rank):
     total_ms = job_time_ms(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
 
-    # ---- end to end through the C ABI with host buffers ----
+    # ---- end to end through the C ABI with host buffers: every step copies its inputs from pinned host
+    #      memory and reads its output back; a serving loop overlaps these copies with the neighbouring
+    #      steps' compute (inputs of step i+1 and the output of step i on two copy streams, two device
+    #      buffer sets) ----
     qh = st["q"].cpu().pin_memory()
     vh = st["vnew"].cpu().pin_memory()
     kh = st["knew"].cpu().pin_memory()
-    outh = torch.empty(st["out"].shape, dtype=torch.float16).pin_memory()
-    qd, vd, kd = torch.empty_like(st["q"]), torch.empty_like(st["vnew"]), torch.empty_like(st["knew"])
-    for _ in range(args.warmup):
-        qd.copy_(qh, non_blocking=True); vd.copy_(vh, non_blocking=True); kd.copy_(kh, non_blocking=True)
-        decode_step(st, stream, q=qd, vnew=vd, knew=kd)
-        outh.copy_(st["out"], non_blocking=True)
+    outh = [torch.empty(st["out"].shape, dtype=torch.float16).pin_memory() for _ in range(2)]
+    bufs = [dict(q=torch.empty_like(st["q"]), v=torch.empty_like(st["vnew"]), k=torch.empty_like(st["knew"]),
+                 out=torch.empty_like(st["out"])) for _ in range(2)]
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_free = [torch.cuda.Event() for _ in range(2)]      # the step that read buffer set s has finished
+    in_ready = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer set s copied
+    out_free = [torch.cuda.Event() for _ in range(2)]     # output of buffer set s read back
+
+    def e2e_step(i):
+        k = i % 2
+        b = bufs[k]
+        h2d_s.wait_event(in_free[k])
+        with torch.cuda.stream(h2d_s):
+            b["q"].copy_(qh, non_blocking=True)
+            b["v"].copy_(vh, non_blocking=True)
+            b["k"].copy_(kh, non_blocking=True)
+        in_ready[k].record(h2d_s)
+        stream.wait_event(in_ready[k])
+        stream.wait_event(out_free[k])
+        decode_step(st, stream, q=b["q"], vnew=b["v"], knew=b["k"], out=b["out"])
+        in_free[k].record(stream)
+        d2h_s.wait_event(in_free[k])
+        with torch.cuda.stream(d2h_s):
+            outh[k].copy_(b["out"], non_blocking=True)
+        out_free[k].record(d2h_s)
+
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        qd.copy_(qh, non_blocking=True); vd.copy_(vh, non_blocking=True); kd.copy_(kh, non_blocking=True)
-        decode_step(st, stream, q=qd, vnew=vd, knew=kd)
-        outh.copy_(st["out"], non_blocking=True)
+    e0.record(h2d_s)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_event(out_free[(args.steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = job_time_ms(e0.elapsed_time(e1), world, dev)
     h2d = qh.numel() * 2 + vh.numel() * 2 + kh.numel() * 2
-    d2h = outh.numel() * 2
+    d2h = outh[0].numel() * 2
 
     if rank != 0:
         return
@@ -471,7 +495,9 @@ def run_gpu(args, w, rank, world, local_rank):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_us_per_step(e2e_ms, args.steps, world), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "every step's inputs from pinned host memory and its output back, on two copy streams "
+                          "overlapping the neighbouring steps (two device buffer sets)"},
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
     }
