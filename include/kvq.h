@@ -116,7 +116,7 @@ typedef struct {
     int32_t bits_k;       /* KIVI key bits: 2 or 4 */
     int32_t bits_v;       /* KIVI value bits: 2 or 4; Kitty value bits: 2 */
     int32_t group_k;      /* G: tokens per KIVI key group (32, 64, 128) or Kitty page (128) */
-    int32_t group_v;      /* Gv: channels per KIVI value group (32 or 128) */
+    int32_t group_v;      /* Gv: channels per KIVI value group (32, 64 or 128) */
     int32_t residual;     /* R: KIVI fp16 residual (R % G == 0), Kitty value local window */
     int32_t sink;         /* S: Kitty fp16 sink tokens */
     int32_t boost_k;      /* K: Kitty boosted key channels, 0..head_dim */
@@ -198,9 +198,11 @@ KVQ_API size_t kvq_kitty_value_page_bytes(const kvq_config *cfg);
 /* --------------------------------------------------------------------- */
 /* seq_len[b] = L_b = tokens in the cache of batch row b INCLUDING the
  * current token (its k, v are inserted before attention; quantization of a
- * full group happens after attention, the Kitty step order).  Every array
- * below is dense [batch][n_kv_heads][capacity][...] with the capacity
- * derived from max_seq_len, and 1 <= seq_len[b] <= max_seq_len. */
+ * full group happens after attention, the Kitty step order).  The dense
+ * caches are [batch][n_kv_heads][capacity][...] with the capacity derived
+ * from max_seq_len, and 1 <= seq_len[b] <= max_seq_len; the paged caches
+ * and the token-granular slot pool state their own layouts below (a slot-pool
+ * request may be empty, seq_len[b] = 0). */
 
 /* KIVI: the key residual holds r_K = ((L-1) mod R) + 1 tokens and the first
  * L - r_K keys are quantized in whole groups; the value residual holds
@@ -248,7 +250,10 @@ KVQ_API kvq_status kv_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c
  *   value (s,z) 2048 bytes            (fp16x2 [128][D/Gv])
  * so a decode stage is one contiguous copy of kvq_kivi_page_bytes(cfg)
  * bytes.  Token t of request b is in logical page t/128, physical page
- * page_table[b][t/128], record pages + (page * Hkv + kv_head) * page_bytes. */
+ * page_table[b][t/128], record pages + (page * Hkv + kv_head) * page_bytes.
+ * (Page management as in Kitty's "Page-Centric Memory Layout and
+ * Dense-Sparse Decomposition": fixed-size pages in a pool addressed through
+ * a page table, PagedAttention style; applied here to the KIVI segments.) */
 typedef struct {
     int32_t batch;
     int32_t max_seq_len;       /* page_table row stride = ceil(max_seq_len / 128) */
@@ -408,8 +413,6 @@ KVQ_API kvq_status kv_append_int8(const kvq_config *cfg, const kvq_int8_cache *c
  * kv_head, 0), key (seed low, seed high), word channel % 4; kv_sel 0 = K,
  * 1 = V.  The dither follows the slot, so moving a request never changes
  * what a written slot decodes to. */
-
-
 typedef struct {
     int32_t batch;
     int32_t max_seq_len;      /* row stride of slot_table */
