@@ -37,11 +37,18 @@ __device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, u
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ uint32_t hneg2(uint32_t a) {
+    uint32_t d;
+    asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
 // fp16x2 product a*b as its hi part (x == 0) or its lo part (x == 1):
 // hi = fl(ah b); lo = fl(al b + fl(ah b - hi)), the inner FMA being exact.
+// The negation is a floating-point one, which the FMA can take as an
+// operand modifier.
 __device__ __forceinline__ uint32_t split_prod(uint32_t ah, uint32_t al, uint32_t b, bool x) {
     uint32_t d = hmul2(ah, b);
-    if (x) d = hfma2(al, b, hfma2(ah, b, d ^ 0x80008000u));
+    if (x) d = hfma2(al, b, hfma2(ah, b, hneg2(d)));
     return d;
 }
 // fp32 pair -> fp16x2 hi (x == 0) or lo = fl(v - hi) (x == 1); first value in the low half
