@@ -10,9 +10,10 @@ fp16 residual R = 128.  One step = one layer-step of the whole hot path:
   a3  decode stage 1  (split-KV attention over quantized + fp16 segments),
   a4  decode merge    (LSE merge, fp16 out).
 `value` is microseconds per layer-step (whole job: time / (steps * N)),
-inputs resident in HBM; `e2e` is the same metric through the C ABI with the
-step's inputs copied from pinned host memory and the output copied back
-inside the timed region.  `--impl reference` times the CPU oracle on a
+inputs resident in HBM, the K steps captured into a CUDA graph and timed
+over one replay; `e2e` is the same metric through the C ABI with the step's
+inputs copied from pinned host memory and the output copied back inside the
+timed region, the steps launched one by one from the host.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -372,7 +373,7 @@ def run_gpu(args, w, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    st = build_state(w, dev, appends=2 * args.warmup + 3 * args.steps + 16)
+    st = build_state(w, dev, appends=2 * args.warmup + 4 * args.steps + 16)
     stream = torch.cuda.current_stream(dev)
     st["side"] = torch.cuda.Stream(device=dev)
     st["fork"], st["join"] = torch.cuda.Event(), torch.cuda.Event()
@@ -381,22 +382,33 @@ def run_gpu(args, w, rank, world, local_rank):
     for _ in range(args.warmup):
         decode_step(st, stream)
     torch.cuda.synchronize()
+    # The K timed steps are captured once into a CUDA graph and replayed, as a serving loop would run
+    # them: the library's calls are stream-ordered, allocate nothing and never synchronize, so they
+    # capture as they are (the merge's programmatic early launch becomes a programmatic graph edge).
+    # One untimed replay uploads the graph; the timed replay runs exactly K steps with no host launch
+    # between them and no event between their kernels.
+    gs = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for i in range(args.steps):
+            decode_step(st, gs)
+    with torch.cuda.stream(gs):
+        graph.replay()
+    torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with Clocks(local_rank) as clk:
-        # the K timed steps, with no event between their kernels (an event between stage 1 and
-        # the merge would stop the merge's programmatic early launch)
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            decode_step(st, stream)
-        t_end.record(stream)
+        t_start.record(gs)
+        with torch.cuda.stream(gs):
+            graph.replay()
+        t_end.record(gs)
         torch.cuda.synchronize()
-        # a second pass of K steps with events around every kernel: the per-kernel breakdown
-        # and the stage-1 duration of the roofline
+        # a second pass of K steps, launched one by one with events around every kernel: the
+        # per-kernel breakdown and the stage-1 duration of the roofline
         for i in range(args.steps):
             decode_step(st, stream, evs[i])
         torch.cuda.synchronize()
@@ -441,6 +453,10 @@ def run_gpu(args, w, rank, world, local_rank):
             outh[k].copy_(b["out"], non_blocking=True)
         out_free[k].record(d2h_s)
 
+    # launched step by step from the host (a graph of the K steps with their copies measured 7-35 us
+    # per step slower on the large workloads: its copies did not overlap the neighbouring steps' kernels
+    # as the stream-launched ones do; on the tiny workload 1, whose steps are host-launch bound, the
+    # graph form was 17 us per step against 70-80)
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -461,7 +477,7 @@ def run_gpu(args, w, rank, world, local_rank):
         return
     lens = st["lens"]
     if w.variant == "int8t":       # one token appended per request before every attention
-        lens = lens + args.warmup + args.steps + (args.steps + 1) // 2
+        lens = lens + args.warmup + 2 * args.steps + (args.steps + 1) // 2   # mid-point of the per-kernel pass
     cache_bytes = st["cache"].nbytes_read(lens)
     q_bytes = w.batch * w.n_q_heads * 128 * 2
     alg_bytes_stage1 = cache_bytes + q_bytes
@@ -501,7 +517,8 @@ def run_gpu(args, w, rank, world, local_rank):
         "config": {"workload": _workload_desc(w), "batch": w.batch, "q_heads": w.n_q_heads,
                    "kv_heads": w.n_kv_heads, "head_dim": 128, "seq_len": w.seq_len, "parallelism": f"replicas x{world}",
                    "splits": st["n_splits"],
-                   "l2": f"inputs larger than L2 ({cache_bytes / 1e6:.0f} MB read per step vs 129 MB L2)"},
+                   "l2": f"inputs larger than L2 ({cache_bytes / 1e6:.0f} MB read per step vs 129 MB L2)",
+                   "timed": "K steps captured once into a CUDA graph; one untimed replay, then one timed replay"},
         "breakdown_us": {("append_before_attention" if w.variant == "int8t" else "quant_writes_side_stream_span"):
                          1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
                          "merge": 1e3 * statistics.mean(merge_ms),
@@ -512,7 +529,8 @@ def run_gpu(args, w, rank, world, local_rank):
         "e2e": {"value": whole_job_us_per_step(e2e_ms, args.steps, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "every step's inputs from pinned host memory and its output back, on two copy streams "
-                          "overlapping the neighbouring steps (two device buffer sets)"},
+                          "overlapping the neighbouring steps (two device buffer sets); steps launched one by one "
+                          "from the host"},
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
     }

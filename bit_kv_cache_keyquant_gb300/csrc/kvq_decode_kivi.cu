@@ -6,17 +6,26 @@
 //   o_c     = sum_t p_t (s_tj code_tc + z_tj)
 //           = sum_t (p_t s_tj) code_tc + sum_t p_t z_tj
 // with alpha = sm_scale * log2(e) (softmax in base 2).
-// Keys: a 2-bit code masked in place out of its packed word, read as an fp32
-// bit pattern, is the denormal code * 2^(k-149) (k = its bit position, kept
-// below the exponent field), so one LOP3 makes an exact fp32 operand and a
-// packed fma.rn.f32x2 multiplies it by alpha q s pre-scaled by 2^(149-k-E0);
-// every product is alpha q s code 2^(2j-E0), exact in fp32 (the fp32 weight
-// matters: a logit error is amplified by the softmax).
-// Values: the same masking (value_token_accum), with the weight p_t s_tj
-// pre-scaled per bit position, so value products are exact in fp32 as well
-// (s_tj code cancels against the zero point when the token's range is wide,
-// so an fp16 weight would lose 2^-12 of a term much larger than the result).
-// Powers of two are removed once per token (keys) or per unit (values).
+// Keys: the weights alpha q_c s_cg of a 32-token group are put in 22-bit
+// fixed point against the group's largest |weight| (one power-of-two scale
+// per tile) and split into three bytes; a packed word of key codes, masked
+// in place, is four unsigned bytes code * 2^(b j) (b the code width, j the
+// token's slot in the byte), so dp4a (four byte products summed into an
+// int32) multiplies four channels' codes by one weight byte exactly.  Three
+// dp4a per mask (one per weight byte) and the integer sums are exact; the
+// only key rounding is the weights' fixed-point rounding (at most 2^-22 of
+// the group's largest) and the final int -> fp32 conversion.  dp4a issues on
+// the FMA-heavy pipe, beside the ALU pipe that the masks load (two LOP3 and
+// one fma.rn.f32x2 per pair of codes loaded the ALU pipe alone: the dp4a form
+// measured 9% faster on the MHA decode layer).
+// Values: a 2-bit code masked in place out of its packed word, read as an
+// fp32 bit pattern, is the denormal code * 2^(k-149) (k = its bit position,
+// kept below the exponent field), so one LOP3 makes an exact fp32 operand
+// and a packed fma.rn.f32x2 multiplies it by p_t s_tj pre-scaled per bit
+// position (value_token_accum): the value products are exact in fp32 (s_tj
+// code cancels against the zero point when the token's range is wide, so an
+// fp16 weight would lose 2^-12 of a term much larger than the result).
+// Powers of two are removed once per unit.
 //
 // Work decomposition: a persistent grid walks the (batch row, query head,
 // split) units round-robin.  A producer warp streams every unit's 128-token
@@ -42,7 +51,7 @@ struct Smem {
     uint8_t stage[NSTAGE][Geo<BK, BV>::BYTES];
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
-    float qk[NCWARP][4 * QK_ROW];         // per-warp alpha*q*s*2^(149-8(c&1)-E0), rows of 32 channels
+    uint32_t qk[NCWARP][4 * QK_ROW];      // per-warp key weight bytes: row tq, (k: byte 0, 1, 2 of 4 channels, pad)
     float st_acc[NCWARP][KVQ_D];
     float st_m[NCWARP];
     float st_l[NCWARP];
@@ -63,6 +72,41 @@ __device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &
     const float p = exp2f(logit - m_run);
     l_part += p;
     return p;
+}
+
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Fixed-point exponent fx of a group whose largest |weight| is wm: wm 2^fx
+// lies in [2^21, 2^22), so every rounded weight is below 2^22 in magnitude
+// and its top byte (bits 16-23, two's complement) is a signed byte in
+// [-64, 64].  Clamped so that 2^fx and 2^-(fx + 6) stay normal fp32.
+__device__ __forceinline__ int key_fixed_exp(float wm) {
+    const int ex = (int)((__float_as_uint(wm) >> 23) & 255u);    // biased exponent, 0 for 0 and denormals
+    return max(-100, min(100, 148 - ex));
+}
+// Four channels' weights in fixed point (rint(w 2^fx)), as three words of
+// bytes: word i holds byte i of each channel's two's-complement value
+// (channel order = the code word's byte order).
+__device__ __forceinline__ uint4 key_weight_bytes(const float w[4], float scale) {
+    const int w0 = __float2int_rn(w[0] * scale), w1 = __float2int_rn(w[1] * scale);
+    const int w2 = __float2int_rn(w[2] * scale), w3 = __float2int_rn(w[3] * scale);
+    uint32_t t01, t23, u01, u23, b0, b1, b2;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t01) : "r"(w0), "r"(w1));   // w0.b0 w1.b0 w0.b1 w1.b1
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t23) : "r"(w2), "r"(w3));
+    asm("prmt.b32 %0, %1, %2, 0x0062;" : "=r"(u01) : "r"(w0), "r"(w1));   // w0.b2 w1.b2
+    asm("prmt.b32 %0, %1, %2, 0x0062;" : "=r"(u23) : "r"(w2), "r"(w3));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(b0) : "r"(t01), "r"(t23));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(b1) : "r"(t01), "r"(t23));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(b2) : "r"(u01), "r"(u23));
+    return make_uint4(b0, b1, b2, 0u);
 }
 
 }  // namespace
@@ -97,8 +141,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
     // ---------------- consumers ----------------
     const int tq = lane & 3;                       // key mapping: lane = 4*(token quad) + channel block
     const int ts = lane >> 2, jg = lane & 3;       // value mapping: token slot, channel block of 32
-    const float pe = __int_as_float((127 + 149 - P.e0) << 23), po = __int_as_float((127 + 141 - P.e0) << 23);
-    const float lscale = __int_as_float((127 + P.e0 - BK * (tq % CPB)) << 23);   // undoes 2^(BK(j % CPB)-E0), j = tq
     const int gl = (32 * warp) / G;                // key group of this warp's tile within a stage
     const int ngv = P.ngv;
     const int jv = (32 * jg) / Gv;                 // value (s, z) group of this lane's channels
@@ -138,7 +180,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
                 qf[2] = h2f(lo16(q89)) * P.alpha;
                 qf[3] = h2f(hi16(q89)) * P.alpha;
             }
-            const float qp[4] = {qf[0] * pe, qf[1] * po, qf[2] * pe, qf[3] * po};
             float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
             unsigned long long vacc2[16];
 #pragma unroll
@@ -151,15 +192,24 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     const uint8_t *st = S.stage[slot];
                     
                     const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + GG::KC) + gl * 2 * KVQ_D;
-                    // ---- pre-scaled alpha*q*s of this group (fp32) and alpha*sum q z ----
+                    // ---- this group's key weights alpha q s in 22-bit fixed point, and alpha sum q z ----
                     const int si = (((lane & 7) >> 1) * 4 + (lane >> 3)) * 8 + (lane & 1) * 4;
                     const uint2 sv = *reinterpret_cast<const uint2 *>(ksz + si);
                     const uint2 zv = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + si);
-                    *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
-                        make_float4(qp[0] * h2f(lo16(sv.x)), qp[1] * h2f(hi16(sv.x)), qp[2] * h2f(lo16(sv.y)),
-                                    qp[3] * h2f(hi16(sv.y)));
-                    const float cb = warp_sum(qf[0] * h2f(lo16(zv.x)) + qf[1] * h2f(hi16(zv.x)) +
-                                              qf[2] * h2f(lo16(zv.y)) + qf[3] * h2f(hi16(zv.y)));
+                    const float w[4] = {qf[0] * h2f(lo16(sv.x)), qf[1] * h2f(hi16(sv.x)), qf[2] * h2f(lo16(sv.y)),
+                                        qf[3] * h2f(hi16(sv.y))};
+                    // the zero-point dot and the largest |weight|, reduced over the warp together
+                    float cb = qf[0] * h2f(lo16(zv.x)) + qf[1] * h2f(hi16(zv.x)) + qf[2] * h2f(lo16(zv.y)) +
+                               qf[3] * h2f(hi16(zv.y));
+                    float wm = fmaxf(fmaxf(fabsf(w[0]), fabsf(w[1])), fmaxf(fabsf(w[2]), fabsf(w[3])));
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        cb += __shfl_xor_sync(0xFFFFFFFFu, cb, o);
+                        wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
+                    }
+                    const int fx = key_fixed_exp(wm);
+                    *reinterpret_cast<uint4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
+                        key_weight_bytes(w, __int_as_float((127 + fx) << 23));
                     __syncwarp();
                     // ---- key codes: tokens q + 8j (q = lane/4) x channels 16k + 2tq + {0,1,8,9};
                     //      token j sits in plane j / CPB at bits BK * (j % CPB) ----
@@ -172,37 +222,40 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                         kw[pl][0] = ka.x; kw[pl][1] = ka.y; kw[pl][2] = ka.z; kw[pl][3] = ka.w;
                         kw[pl][4] = kb.x; kw[pl][5] = kb.y; kw[pl][6] = kb.z; kw[pl][7] = kb.w;
                     }
-                    const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][tq * QK_ROW]);
-                    unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};     // fp32 pairs
+                    const uint4 *qd = reinterpret_cast<const uint4 *>(&S.qk[warp][tq * QK_ROW]);
+                    int acc[4][3];                                              // token j, weight byte
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = 0;
     #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float4 qv = qs[k];                                 // channels 16k + 2tq + {0,1,8,9}
-                        const unsigned long long q01 = pack2f(qv.x, qv.y), q23 = pack2f(qv.z, qv.w);
+                        const uint4 d = qd[k];                                  // channels 16k + 2tq + {0,1,8,9}
     #pragma unroll
                         for (int pl = 0; pl < NPL; ++pl) {
-                            const uint32_t w0 = kw[pl][k], w16 = kw[pl][k] >> 16;   // channels +0,+1 | +8,+9
     #pragma unroll
                             for (int jj = 0; jj < CPB; ++jj) {
                                 const int j = pl * CPB + jj;
-                                const uint32_t m0 = ((1u << BK) - 1) << (BK * jj), m1 = m0 << 8;
-                                acc2[j] = ffma2(pack2u(w0 & m0, w0 & m1), q01, acc2[j]);     // even, odd channel
-                                acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
+                                const uint32_t x = kw[pl][k] & ((((1u << BK) - 1) * 0x01010101u) << (BK * jj));
+                                acc[j][0] = dp4a_uu(x, d.x, acc[j][0]);
+                                acc[j][1] = dp4a_uu(x, d.y, acc[j][1]);
+                                acc[j][2] = dp4a_us(x, d.z, acc[j][2]);
                             }
                         }
                     }
+                    // weight bytes 0 + 1 fit an int32 (< 2^29); the sum is code * 2^(BK (j % CPB)) * W 2^fx
+                    float a[4];
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) a[j] = fmaf((float)acc[j][2], 65536.f, (float)(acc[j][0] + (acc[j][1] << 8)));
                     // transpose-reduce over the 4 lanes of the quad: lane keeps token q + 8tq
                     float score;
                     {
-                        const float a0 = lo2f(acc2[0]) + hi2f(acc2[0]), a1 = lo2f(acc2[1]) + hi2f(acc2[1]);
-                        const float a2 = lo2f(acc2[2]) + hi2f(acc2[2]), a3 = lo2f(acc2[3]) + hi2f(acc2[3]);
                         const bool h2 = (tq & 2) != 0;
-                        float k0 = h2 ? a2 : a0, k1 = h2 ? a3 : a1;
-                        k0 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a0 : a2, 2);
-                        k1 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a1 : a3, 2);
+                        float k0 = h2 ? a[2] : a[0], k1 = h2 ? a[3] : a[1];
+                        k0 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a[0] : a[2], 2);
+                        k1 += __shfl_xor_sync(0xFFFFFFFFu, h2 ? a[1] : a[3], 2);
                         const bool h1 = (tq & 1) != 0;
                         score = (h1 ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, h1 ? k0 : k1, 1);
                     }
-                    const float logit = score * lscale + cb;
+                    const float logit = fmaf(score, __int_as_float((127 - fx - BK * (tq % CPB)) << 23), cb);
                     const float p = softmax_tile(logit, m_run, l_part, vbias, vacc2);
                     // ---- values: 4 passes of 8 tokens; lane = (token slot ts, channel block jg) ----
                     const uint8_t *vc = st + GG::KC + GG::KSZ + warp * 32 * (KVQ_D * BV / 8);
@@ -299,9 +352,6 @@ static cudaError_t launch_kivi_variant(const Params &P, int64_t grid, cudaStream
 cudaError_t launch_decode_kivi(const kvq_config *cfg, const KiviSrc &c, const void *q, const DecodePlan &p,
                                void *ws, cudaStream_t st) {
     Params P = kivi_params(cfg, c, q, p, ws);
-    // |alpha q s| < alpha 2^32 (fp16 q and s): 2^(149-E0) alpha 2^32 < 2^127
-    P.e0 = 54 + (int)ceilf(log2f(P.alpha));
-    if (P.e0 < 22) P.e0 = 22;
     if (!P.err) return cudaErrorInvalidDevicePointer;
     const int64_t n_units = (int64_t)c.batch * cfg->n_q_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;

@@ -46,7 +46,6 @@ struct Params {
     int64_t cap;        // token capacity per (b, kvh): max_seq_len rounded up to 128
     int64_t kgrp_cap;   // cap / G
     float alpha;
-    int e0;             // key products are scaled by 2^-E0
     int bits_k, bits_v; // code widths (2 or 4)
     // paged cache (page_table non-null): token t of row b is in page record
     // pages + (page_table[b * pt_stride + t / 128] * Hkv + kv head) * rec_bytes
@@ -363,7 +362,6 @@ inline Params kivi_params(const kvq_config *cfg, const KiviSrc &c, const void *q
     P.chunk = p.chunk;
     P.kgrp_cap = P.cap / cfg->group_k;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
-    P.e0 = 0;
     P.bits_k = cfg->bits_k;
     P.bits_v = cfg->bits_v;
     P.page_table = c.page_table;
