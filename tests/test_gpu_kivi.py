@@ -150,6 +150,49 @@ def test_decode_wide_outlier_channels(K, orc, Hq, Hkv):
     assert_attn_close(got, _oracle_decode(orc, cfg, Ks, Vs, q))
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+@pytest.mark.parametrize("case", ["zero_query", "wide_channels", "const_groups", "huge_query"])
+def test_decode_key_weight_extremes(K, orc, Hq, Hkv, case):
+    """Key weights alpha q s at the edges of the per-head kernel's fixed-point form (one power-of-two
+    scale per 32-token group, set by the group's largest |weight|) and of the tensor-core hi / lo
+    split: an all-zero query (every weight 0), channel ranges from 1e-4 to 3e4 in one group, groups
+    whose channels are constant (s = 0), and a query of +-300 in one channel over channels of about
+    0.02, a range of 2^14 (the grouped-query path keeps every channel's weight a normal fp16 number
+    up to that range; beyond it the smallest channels fall to fp16 subnormals and lose their key
+    contributions, and the logits' ties on the large channel are then broken without them)."""
+    rng = np.random.default_rng({"zero_query": 11, "wide_channels": 12, "const_groups": 13, "huge_query": 14}[case] + Hq)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    lens = [700, 1300]
+    Ks, Vs = [], []
+    for L in lens:
+        kr, vr = [], []
+        for _ in range(Hkv):
+            k = rng.standard_normal((L, 128))
+            if case == "wide_channels":
+                k = np.clip(k * 10.0 ** rng.uniform(-4, 4.4, 128), -6.0e4, 6.0e4)
+            if case == "const_groups":
+                for g0 in range(0, L - 31, 64):                    # every other 32-token group constant
+                    k[g0:g0 + 32] = k[g0]
+            kr.append(k.astype(np.float16))
+            vr.append(rng.standard_normal((L, 128)).astype(np.float16))
+        Ks.append(kr)
+        Vs.append(vr)
+    q = rng.standard_normal((2, Hq, 128))
+    if case == "zero_query":
+        q[0, 0] = 0.0
+        q[1, :] = 0.0
+    if case == "wide_channels":
+        q *= 10.0 ** rng.uniform(-3, 2, 128)
+    if case == "huge_query":
+        q *= 0.02
+        q[:, :, 5] = 300.0
+        q[1, 0, 5] = -300.0
+    q = q.astype(np.float16)
+    got = _run_decode(K, cfg, Ks, Vs, q, 1300)
+    assert np.isfinite(got).all()
+    assert_attn_close(got, _oracle_decode(orc, cfg, Ks, Vs, q))
+
+
 def test_decode_capacity_and_split_invariance(K, orc):
     """The same cache content under a larger capacity (more splits) gives the same result."""
     rng = np.random.default_rng(7)
