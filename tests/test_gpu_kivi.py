@@ -137,7 +137,7 @@ def test_decode_parity_small(K, orc, shape):
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
 def test_decode_wide_outlier_channels(K, orc, Hq, Hkv):
     """Key channels x20 and a large query (the logit scale of the tiny workload): the fp16 hi / lo
-    key weights of the tensor-core path and the exact fp32 products of the per-head path both hold."""
+    key weights of the tensor-core path and the fixed-point dp4a key products of the per-head path both hold."""
     rng = np.random.default_rng(Hq * 31 + Hkv)
     cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
     lens = [777, 2048]
