@@ -377,6 +377,69 @@ def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None, out=None):
     stream.wait_event(st["join"])
 
 
+def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
+    """The workload's quantization kernels on their own, outside the timed step, at 256 MB of fp16 input
+    per call (twice the L2): us per call, and HBM GB/s of the bytes each call must move (fp16 input read,
+    codes and scales written) against the measured copy peak."""
+    import torch
+    from bit_kv_cache_keyquant_gb300 import kvq
+    peak, _ = _peaks()
+    total = 256 << 20
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def entry(us, units, unit, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us_per_call": us, "units": units, "unit": unit, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak}
+
+    x = torch.randn(total // 2, generator=gen, device=dev).half()
+    out = {}
+    with torch.cuda.stream(stream):
+        if w.variant == "kivi":
+            G, Gv = cfg.group_k, cfg.group_v
+            ng = total // (G * 128 * 2)
+            kc = torch.empty(ng * G * 128 * w.bits_k // 8, dtype=torch.uint8, device=dev)
+            ks = torch.empty((ng, 128), dtype=torch.int32, device=dev)
+            us = timed(lambda: kvq.kv_quant_key(cfg, x, ng, kc, ks, stream))
+            out["kv_quant_key"] = entry(us, ng, f"{G}-token key groups", total + kc.numel() + ks.numel() * 4)
+            nt = total // 256
+            vc = torch.empty(nt * 128 * w.bits_v // 8, dtype=torch.uint8, device=dev)
+            vs = torch.empty((nt, 128 // Gv), dtype=torch.int32, device=dev)
+            us = timed(lambda: kvq.kv_quant_value(cfg, x, nt, vc, vs, stream))
+            out["kv_quant_value"] = entry(us, nt, "value tokens", total + vc.numel() + vs.numel() * 4)
+        elif w.variant == "kitty":
+            npg = total // (128 * 128 * 2)
+            kp = torch.empty(npg * kvq.kvq_kitty_key_page_bytes(cfg), dtype=torch.uint8, device=dev)
+            us = timed(lambda: kvq.kv_quant_key_kitty(cfg, x, npg, 0, kp, stream))
+            out["kv_quant_key_kitty"] = entry(us, npg, "128-token key pages", total + kp.numel())
+            vp = torch.empty(npg * kvq.kvq_kitty_value_page_bytes(cfg), dtype=torch.uint8, device=dev)
+            us = timed(lambda: kvq.kv_quant_value_kitty(cfg, x, npg, vp, stream))
+            out["kv_quant_value_kitty"] = entry(us, npg, "128-token value pages", total + vp.numel())
+        elif w.variant == "int8":
+            nb = total // (256 * 128 * 2)
+            blk = torch.arange(nb, dtype=torch.int32, device=dev)
+            meta = [blk // w.n_kv_heads, blk % w.n_kv_heads, 256 * (blk // w.n_kv_heads)]   # request, kv head, tok0
+            codes = torch.empty(nb * 256 * 128, dtype=torch.int8, device=dev)
+            scale = torch.empty((nb, 128), dtype=torch.float16, device=dev)
+            us = timed(lambda: kvq.kv_quant_int8_dither(cfg, x, nb, meta[0], meta[1], meta[2], 5, 0, w.seed, codes,
+                                                        scale, stream))
+            out["kv_quant_int8_dither"] = entry(us, nb, "256-token blocks", total + codes.numel() + scale.numel() * 2)
+    torch.cuda.synchronize()
+    return out
+
+
 def launches_per_step(w) -> int:
     return {"kivi": 4, "kitty": 4, "int8": 4, "int8t": 4}[w.variant]
 
@@ -504,6 +567,7 @@ def run_gpu(args, w, rank, world, local_rank):
     h2d = qh.numel() * 2 + vh.numel() * 2 + kh.numel() * 2
     d2h = outh[0].numel() * 2
 
+    quant = quant_kernels_bench(w, st["cfg"], dev, stream) if rank == 0 else None
     if rank != 0:
         return
     lens = st["lens"]
@@ -569,6 +633,7 @@ def run_gpu(args, w, rank, world, local_rank):
                 "copies": "every step's inputs from pinned host memory and its output back, on two copy streams "
                           "overlapping the neighbouring steps (two device buffer sets); steps launched one by one "
                           "from the host"},
+        "quant_kernels": quant,
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
     }

@@ -31,121 +31,94 @@ __device__ __forceinline__ int kivi_sz_index(int c) {
 // G*D*bits/8 bytes, sz the group's 2*D fp16 (scales, then zeros).  bits = 2
 // or 4: a 32-token tile is bits/2 planes of 1024 bytes, token q + 8p in plane
 // p / (8/bits) at bits bits*(p % (8/bits)) of its 2-bit-layout byte.
+// One key group by a 128-thread block, thread c = channel c: src fp16 [G][D],
+// codes the group's G*D*BITS/8 bytes, sz the group's 2*D fp16 (scales, then
+// zeros).  The group is staged in shared memory (xs) with 16-byte loads; each
+// thread reads its channel's column (min / max, fit, codes) and writes its
+// code bytes into a shared copy of the tile layout (cw), which the block then
+// stores with 16-byte stores.  BITS = 2 or 4: a 32-token tile is BITS/2
+// planes of 1024 bytes, token q + 8p in plane p / (8/BITS) at bits
+// BITS*(p % (8/BITS)) of its 2-bit-layout byte.  Every thread of the block
+// calls it (block barriers inside).
+template <int NT, int BITS>
+__device__ __forceinline__ void key_group_quant_b(const uint16_t *__restrict__ src, uint8_t *__restrict__ codes,
+                                                  uint16_t *__restrict__ sz, uint16_t *xs, uint32_t *cw) {
+    constexpr int G = 32 * NT, CPB = 8 / BITS, NPL = BITS / 2, QMAX = (1 << BITS) - 1;
+    const int c = threadIdx.x;
+    __syncthreads();                                               // the block's previous group is stored
+    {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+        uint4 *x4 = reinterpret_cast<uint4 *>(xs);
+#pragma unroll
+        for (int i = 0; i < 4 * NT; ++i) x4[c + 128 * i] = __ldg(s4 + c + 128 * i);
+    }
+    __syncthreads();
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 8
+    for (int t = 0; t < G; ++t) {
+        const float v = h2f(xs[t * KVQ_D + c]);
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+    }
+    uint16_t s, z;
+    affine_fit(mn, mx, QMAX, s, z);
+    const int si = kivi_sz_index(c);
+    sz[si] = s;
+    sz[KVQ_D + si] = z;
+    const float sf = h2f(s), zf = h2f(z), rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+    // channel c = 16k + 2r + e + 8h: half k/4, chunk row 4q + r, word k%4, byte e + 2h of the tile layout
+    const int k = c >> 4, cc = c & 15;
+    const int pos = (k >> 2) * 512 + ((cc & 7) >> 1) * 16 + (k & 3) * 4 + (cc & 1) + 2 * (cc >> 3);
+    uint8_t *cb = reinterpret_cast<uint8_t *>(cw);
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt)
+#pragma unroll 2
+        for (int q = 0; q < 8; ++q) {
+            uint32_t byte[NPL];
+#pragma unroll
+            for (int pl = 0; pl < NPL; ++pl) byte[pl] = 0u;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t code = (uint32_t)affine_code(h2f(xs[(tt * 32 + q + 8 * p) * KVQ_D + c]), zf, sf, rf, QMAX);
+                byte[p / CPB] |= code << (BITS * (p % CPB));
+            }
+#pragma unroll
+            for (int pl = 0; pl < NPL; ++pl) cb[(tt * NPL + pl) * 1024 + q * 64 + pos] = (uint8_t)byte[pl];
+        }
+    __syncthreads();
+    const uint4 *c4 = reinterpret_cast<const uint4 *>(cw);
+    uint4 *o4 = reinterpret_cast<uint4 *>(codes);
+#pragma unroll
+    for (int i = c; i < NT * NPL * 64; i += 128) o4[i] = c4[i];
+}
+
 template <int NT>
 __device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src, uint8_t *__restrict__ codes,
                                                 uint16_t *__restrict__ sz, int bits = 2) {
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // lane's 32 channels of token lane in each tile: 4 x 16 bytes per tile
-    uint32_t xv[NT][16];
-#pragma unroll
-    for (int tt = 0; tt < NT; ++tt) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(src + (int64_t)(tt * 32 + lane) * KVQ_D + 32 * w);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 u = __ldg(p + i);
-            xv[tt][4 * i + 0] = u.x; xv[tt][4 * i + 1] = u.y; xv[tt][4 * i + 2] = u.z; xv[tt][4 * i + 3] = u.w;
-        }
-    }
-    // per-lane min / max over its NT tokens for the 32 channels
-    float mn[32], mx[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        float v = h2f((c & 1) ? hi16(xv[0][c >> 1]) : lo16(xv[0][c >> 1]));
-        mn[c] = v; mx[c] = v;
-#pragma unroll
-        for (int tt = 1; tt < NT; ++tt) {
-            float u = h2f((c & 1) ? hi16(xv[tt][c >> 1]) : lo16(xv[tt][c >> 1]));
-            mn[c] = fminf(mn[c], u); mx[c] = fmaxf(mx[c], u);
-        }
-    }
-    // reduce-scatter over the 32 lanes: after the step with offset o, a lane
-    // keeps the half of its channels selected by lane bit o
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int c = 0; c < o; ++c) {
-            float send_mn = up ? mn[c] : mn[c + o];
-            float send_mx = up ? mx[c] : mx[c + o];
-            float keep_mn = up ? mn[c + o] : mn[c];
-            float keep_mx = up ? mx[c + o] : mx[c];
-            float r_mn = __shfl_xor_sync(0xFFFFFFFFu, send_mn, o);
-            float r_mx = __shfl_xor_sync(0xFFFFFFFFu, send_mx, o);
-            mn[c] = fminf(keep_mn, r_mn);
-            mx[c] = fmaxf(keep_mx, r_mx);
-        }
-    }
-    // lane now holds channel 32w + lane in slot 0
-    uint16_t s, z;
-    const int qmax = (1 << bits) - 1;
-    affine_fit(mn[0], mx[0], qmax, s, z);
-    const uint32_t my_sz = (uint32_t)s | ((uint32_t)z << 16);
-    {
-        const int si = kivi_sz_index(32 * w + lane);
-        sz[si] = s;
-        sz[KVQ_D + si] = z;
-    }
-
-    const int q = lane & 7, p = lane >> 3;
-    const int cpb = 8 / bits;                      // codes per byte; lanes p sharing a plane: p / cpb
-    const int shift = bits * (p % cpb);
-#pragma unroll
-    for (int tt = 0; tt < NT; ++tt) {
-        // word[r][kk]: chunk row r, channel block 16*(2w+kk); byte e + 2h, bits `shift`
-        uint32_t word[4][2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) word[i][0] = word[i][1] = 0;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            uint32_t szc = __shfl_sync(0xFFFFFFFFu, my_sz, c);
-            float sf = h2f(lo16(szc)), zf = h2f(hi16(szc));
-            float x = h2f((c & 1) ? hi16(xv[tt][c >> 1]) : lo16(xv[tt][c >> 1]));
-            uint32_t code = (uint32_t)affine_code(x, zf, sf, qmax);
-            const int kk = c >> 4, cc = c & 15;
-            word[(cc & 7) >> 1][kk] |= code << (8 * ((cc & 1) + 2 * (cc >> 3)) + shift);
-        }
-        // OR the codes of the lanes that share a byte: tokens q + 8p of one plane
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 8);
-                if (bits == 2) word[i][kk] |= __shfl_xor_sync(0xFFFFFFFFu, word[i][kk], 16);
-            }
-        // the cpb lanes of a plane store its four chunk rows, 4 / cpb rows of 8 bytes each
-        uint8_t *tile = codes + tt * 512 * bits + (p / cpb) * 1024;
-        const int nrow = 4 / cpb;
-        for (int rr = 0; rr < nrow; ++rr) {
-            const int r = (p % cpb) * nrow + rr;
-            uint2 v = make_uint2(word[0][0], word[0][1]);
-#pragma unroll
-            for (int i = 1; i < 4; ++i)
-                if (r == i) v = make_uint2(word[i][0], word[i][1]);
-            *reinterpret_cast<uint2 *>(tile + (w >> 1) * 512 + (4 * q + r) * 16 + (w & 1) * 8) = v;
-        }
-    }
+    __shared__ __align__(16) uint16_t xs[32 * NT * KVQ_D];
+    __shared__ __align__(16) uint32_t cw[NT * 2 * 256];           // NT tiles x up to 2 planes x 1024 bytes
+    if (bits == 4) key_group_quant_b<NT, 4>(src, codes, sz, xs, cw);
+    else key_group_quant_b<NT, 2>(src, codes, sz, xs, cw);
 }
 
+// Bulk key groups: a grid of resident blocks walks the groups.
 template <int NT>
 __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
                                                              uint8_t *__restrict__ codes, uint16_t *__restrict__ sz,
                                                              int bits) {
-    const int64_t g = blockIdx.x;
-    if (g >= n_groups) return;
     constexpr int G = 32 * NT;
-    key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D * bits / 8, sz + g * 2 * KVQ_D,
-                        bits);
+    for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x)
+        key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D * bits / 8, sz + g * 2 * KVQ_D,
+                            bits);
 }
 
 // One value token by a warp, per token over groups of GV channels: lane l
 // reads channels 4l..4l+3 and returns in wv the packed word of its lane quad
 // (valid in lanes 4j, channels 16j..16j+15) and the (s, z) of its group.
 template <int GV>
-__device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ src, int lane, uint32_t &wv, uint16_t &s,
-                                                  uint16_t &z, int bits = 2) {
+__device__ __forceinline__ void value_token_quant_x(uint2 u, int lane, uint32_t &wv, uint16_t &s, uint16_t &z,
+                                                    int bits = 2) {
     constexpr int LG = GV / 4;   // lanes per group
-    uint2 u = *reinterpret_cast<const uint2 *>(src + 4 * lane);
     float x0 = h2f(lo16(u.x)), x1 = h2f(hi16(u.x)), x2 = h2f(lo16(u.y)), x3 = h2f(hi16(u.y));
     float mn = fminf(fminf(x0, x1), fminf(x2, x3));
     float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
@@ -156,15 +129,21 @@ __device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ s
     }
     const int qmax = (1 << bits) - 1;
     affine_fit(mn, mx, qmax, s, z);
-    float sf = h2f(s), zf = h2f(z);
-    const uint32_t b = (uint32_t)affine_code(x0, zf, sf, qmax) | ((uint32_t)affine_code(x1, zf, sf, qmax) << bits) |
-                       ((uint32_t)affine_code(x2, zf, sf, qmax) << (2 * bits)) |
-                       ((uint32_t)affine_code(x3, zf, sf, qmax) << (3 * bits));
+    const float sf = h2f(s), zf = h2f(z), rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+    const uint32_t b = (uint32_t)affine_code(x0, zf, sf, rf, qmax) |
+                       ((uint32_t)affine_code(x1, zf, sf, rf, qmax) << bits) |
+                       ((uint32_t)affine_code(x2, zf, sf, rf, qmax) << (2 * bits)) |
+                       ((uint32_t)affine_code(x3, zf, sf, rf, qmax) << (3 * bits));
     if (bits == 2)       // lanes 4j: channels 16j..16j+15
         wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 8) | (__shfl_down_sync(0xFFFFFFFFu, b, 2) << 16) |
              (__shfl_down_sync(0xFFFFFFFFu, b, 3) << 24);
     else                 // lanes 2j: channels 8j..8j+7, channel c at nibble c % 2 of byte c / 2
         wv = b | (__shfl_down_sync(0xFFFFFFFFu, b, 1) << 16);
+}
+template <int GV>
+__device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ src, int lane, uint32_t &wv, uint16_t &s,
+                                                  uint16_t &z, int bits = 2) {
+    value_token_quant_x<GV>(*reinterpret_cast<const uint2 *>(src + 4 * lane), lane, wv, s, z, bits);
 }
 
 // Store of one token's packed codes by the lanes that hold a full word.
@@ -177,32 +156,72 @@ __device__ __forceinline__ void value_token_store(uint8_t *__restrict__ tok, int
 }
 
 // ---------------------------------------------------------------------------
-// a2 / a6: per-token value quantization over groups of GV channels.  One warp
-// per token; lane l holds channels 4l..4l+3; group min / max by xor shuffles
-// inside the GV/4 lanes of a group.  Output either KIVI (interleaved (s, z)
-// per group) or a Kitty value page (separate s[G], z[G] after the codes).
+// a2 / a6: per-token value quantization over groups of GV channels, in bulk.
+// A warp takes four tokens at once: lane = 8 * token slot + channel block,
+// the block's 16 channels (two 16-byte loads) in registers; group min / max
+// by xor shuffles inside the GV/16 lanes of a group.  A lane's 16 codes are
+// one word (2-bit: channel c at bits 2(c % 4) of byte c / 4) or two (4-bit:
+// nibble c % 2 of byte c / 2) of the token's code row.  Output either KIVI
+// (interleaved (s, z) per group) or a Kitty value page (separate s[G], z[G]
+// after the codes).
 // ---------------------------------------------------------------------------
-template <int GV, bool KITTY>
+template <int GV, bool KITTY, int BITS>
 __global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
                                                           uint8_t *__restrict__ out, uint32_t *__restrict__ sz,
-                                                          int page_tokens, int64_t page_bytes, int bits) {
-    const int lane = threadIdx.x & 31;
+                                                          int page_tokens, int64_t page_bytes) {
+    constexpr int LG = GV / 16, QMAX = (1 << BITS) - 1;   // lanes per group
+    const int lane = threadIdx.x & 31, ts = lane >> 3, cb = lane & 7;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    constexpr int LG = GV / 4;   // lanes per group
-    for (int64_t t = warp; t < n_tokens; t += nwarps) {
-        uint32_t wv;
+    for (int64_t t0 = 4 * warp; t0 < n_tokens; t0 += 4 * nwarps) {
+        const int64_t t = t0 + ts;
+        const bool live = t < n_tokens;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+        if (live) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(v + t * KVQ_D + 16 * cb);
+            a = __ldg(p);
+            b = __ldg(p + 1);
+        }
+        const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[2 * i] = h2f(lo16(h[i]));
+            x[2 * i + 1] = h2f(hi16(h[i]));
+        }
+        float mn = x[0], mx = x[0];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            mn = fminf(mn, x[i]);
+            mx = fmaxf(mx, x[i]);
+        }
+#pragma unroll
+        for (int o = 1; o < LG; o <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        }
         uint16_t s, z;
-        value_token_quant<GV>(v + t * KVQ_D, lane, wv, s, z, KITTY ? 2 : bits);
+        affine_fit(mn, mx, QMAX, s, z);
+        const float sf = h2f(s), zf = h2f(z), rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+        uint32_t w[BITS / 2] = {};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t code = (uint32_t)affine_code(x[i], zf, sf, rf, QMAX);
+            if (BITS == 2) w[0] |= code << (2 * i);
+            else w[i / 8] |= code << (4 * (i % 8));
+        }
+        if (!live) continue;
         if (!KITTY) {
-            value_token_store(out + t * (KVQ_D * bits / 8), lane, wv, bits);
-            if ((lane % LG) == 0) sz[t * (KVQ_D / GV) + lane / LG] = (uint32_t)s | ((uint32_t)z << 16);
+            uint8_t *row = out + t * (KVQ_D * BITS / 8);
+            if (BITS == 2) reinterpret_cast<uint32_t *>(row)[cb] = w[0];
+            else reinterpret_cast<uint2 *>(row)[cb] = make_uint2(w[0], w[BITS / 2 - 1]);
+            if (cb % LG == 0) sz[t * (KVQ_D / GV) + cb / LG] = (uint32_t)s | ((uint32_t)z << 16);
         } else {
             const int64_t p = t / page_tokens;
             const int tt = (int)(t % page_tokens);
             uint8_t *pg = out + p * page_bytes;
-            if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(pg + (int64_t)tt * (KVQ_D / 4))[lane >> 2] = wv;
-            if (lane == 0) {
+            reinterpret_cast<uint32_t *>(pg + (int64_t)tt * (KVQ_D / 4))[cb] = w[0];
+            if (cb == 0) {
                 uint16_t *ps = reinterpret_cast<uint16_t *>(pg + (int64_t)page_tokens * KVQ_D / 4);
                 ps[tt] = s;
                 ps[page_tokens + tt] = z;
@@ -266,7 +285,7 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
     const int qmax = boosted ? 15 : 3;
     uint16_t s, z;
     affine_fit(mn, mx, qmax, s, z);
-    const float sv = h2f(s), zv = h2f(z);
+    const float sv = h2f(s), zv = h2f(z), rv = sv != 0.0f ? __frcp_rn(sv) : 0.0f;
     uint8_t *low = pg;
     uint8_t *high = pg + KVQ_D * G / 4;
     uint8_t *idx = high + (int64_t)K * G / 4;
@@ -275,7 +294,7 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
 #pragma unroll
     for (int i = 0; i < 8; ++i) { lw[i] = 0; hw[i] = 0; }
     for (int t = 0; t < G; ++t) {
-        uint32_t code = (uint32_t)affine_code(h2f(xs[t * KVQ_D + c]), zv, sv, qmax);
+        uint32_t code = (uint32_t)affine_code(h2f(xs[t * KVQ_D + c]), zv, sv, rv, qmax);
         const int sh = 2 * (t & 15);
         lw[t >> 4] |= (code & 3u) << sh;
         hw[t >> 4] |= ((code >> 2) & 3u) << sh;
@@ -408,9 +427,10 @@ cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t 
         uint8_t *cs = cp + g0 * (int64_t)G * KVQ_D * cfg->bits_k / 8;
         uint16_t *zs = zp + g0 * 2 * KVQ_D;
         const int bits = cfg->bits_k;
-        if (G == 32) quant_key_kivi_kernel<1><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs, bits);
-        else if (G == 64) quant_key_kivi_kernel<2><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs, bits);
-        else quant_key_kivi_kernel<4><<<(unsigned)n, 128, 0, st>>>(ks, n, cs, zs, bits);
+        const unsigned grid = (unsigned)grid_cap(n, G == 32 ? 16 : G == 64 ? 8 : 4);   // resident blocks per SM
+        if (G == 32) quant_key_kivi_kernel<1><<<grid, 128, 0, st>>>(ks, n, cs, zs, bits);
+        else if (G == 64) quant_key_kivi_kernel<2><<<grid, 128, 0, st>>>(ks, n, cs, zs, bits);
+        else quant_key_kivi_kernel<4><<<grid, 128, 0, st>>>(ks, n, cs, zs, bits);
     }
     return cudaGetLastError();
 }
@@ -418,15 +438,18 @@ cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t 
 cudaError_t launch_quant_value_kivi(const kvq_config *cfg, const void *v, int64_t n_tokens, void *codes, void *sz,
                                     cudaStream_t st) {
     if (n_tokens == 0) return cudaSuccess;
-    const int grid = grid_cap((n_tokens + 7) / 8, 16);
+    const int grid = grid_cap((n_tokens + 31) / 32, 8);           // 32 tokens per 8-warp block pass
     const uint16_t *vp = static_cast<const uint16_t *>(v);
     uint8_t *cp = static_cast<uint8_t *>(codes);
     uint32_t *zp = static_cast<uint32_t *>(sz);
+#define KVQ_QV(GV, B) quant_value_kernel<GV, false, B><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0)
+    const bool b4 = cfg->bits_v == 4;
     switch (cfg->group_v) {
-        case 32: quant_value_kernel<32, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, cfg->bits_v); break;
-        case 64: quant_value_kernel<64, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, cfg->bits_v); break;
-        default: quant_value_kernel<128, false><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, cfg->bits_v); break;
+        case 32: if (b4) KVQ_QV(32, 4); else KVQ_QV(32, 2); break;
+        case 64: if (b4) KVQ_QV(64, 4); else KVQ_QV(64, 2); break;
+        default: if (b4) KVQ_QV(128, 4); else KVQ_QV(128, 2); break;
     }
+#undef KVQ_QV
     return cudaGetLastError();
 }
 
@@ -435,10 +458,10 @@ cudaError_t launch_quant_value_kitty(const kvq_config *cfg, const void *v, int64
     if (n_pages == 0) return cudaSuccess;
     const int G = cfg->group_k;
     const int64_t n_tokens = n_pages * G;
-    const int grid = grid_cap((n_tokens + 7) / 8, 16);
+    const int grid = grid_cap((n_tokens + 31) / 32, 8);
     const int64_t pb = (int64_t)G * KVQ_D / 4 + 4LL * G;
-    quant_value_kernel<128, true><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens,
-                                                        static_cast<uint8_t *>(pages), nullptr, G, pb, 2);
+    quant_value_kernel<128, true, 2><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens,
+                                                           static_cast<uint8_t *>(pages), nullptr, G, pb);
     return cudaGetLastError();
 }
 
