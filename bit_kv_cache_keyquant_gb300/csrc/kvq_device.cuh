@@ -84,6 +84,18 @@ __device__ __forceinline__ int affine_code(float x, float zf, float sf, float ri
     return (int)r;
 }
 
+// INT8 dithered code = clamp(rint(fl(x / s) + xi), -127, 127) in fp32 with
+// rounding to nearest (the definition), s != 0, rinv = fl(1 / s).  With
+// |x / s| < 127 the product x * rinv is within 2^-15.4 of fl(x / s), so the
+// sums with xi differ by at most 2^-15 and round to the same integer unless
+// they lie within 2^-13.3 of a half-integer; only then is the quotient formed.
+__device__ __forceinline__ int dither_code(float x, float s, float rinv, float xi) {
+    const float va = __fadd_rn(__fmul_rn(x, rinv), xi);
+    float r = rintf(va);
+    if (fabsf(__fsub_rn(va, r)) > 0.4999f) r = rintf(__fadd_rn(__fdiv_rn(x, s), xi));
+    return (int)fminf(fmaxf(r, -127.f), 127.f);
+}
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3")
 // ---------------------------------------------------------------------------

@@ -39,17 +39,14 @@ __device__ __forceinline__ void int8t_token_quant(const uint16_t *__restrict__ s
 #pragma unroll
     for (int o = 1; o < LG; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
     s = f2h_rn(__fdiv_rn(a, 126.5f));
-    const float sf = h2f(s);
+    const float sf = h2f(s), rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
     const uint4 r = philox4x32_10(make_uint4(slot, (uint32_t)lane, c2, 0u), k0, k1);
     const uint32_t wr[4] = {r.x, r.y, r.z, r.w};
     word = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         int code = 0;
-        if (sf != 0.0f) {
-            const float v = __fadd_rn(__fdiv_rn(xs[i], sf), dither_from_word(wr[i]));
-            code = (int)fminf(fmaxf(rintf(v), -127.f), 127.f);
-        }
+        if (sf != 0.0f) code = dither_code(xs[i], sf, rf, dither_from_word(wr[i]));
         word |= ((uint32_t)(code & 0xFF)) << (8 * i);
     }
 }

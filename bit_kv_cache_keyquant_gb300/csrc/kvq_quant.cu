@@ -256,19 +256,28 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
     for (int i = c; i < G * KVQ_D / 8; i += 128) reinterpret_cast<uint4 *>(xs)[i] = s4[i];
     __syncthreads();
     long long a = 0;
-    float s1 = 0.f, s2 = 0.f;
-    float mn = INFINITY, mx = -INFINITY;
-    for (int t = 0; t < G; ++t) {
-        uint16_t h = xs[t * KVQ_D + c];
-        float x = h2f(h);
-        a += abs_units(h);
-        s1 = __fadd_rn(s1, x);
-        s2 = __fadd_rn(s2, __fmul_rn(x, x));
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
+    float mn = INFINITY, mx = -INFINITY, var = 0.f;
+    if (score_mode == 0) {
+#pragma unroll 4
+        for (int t = 0; t < G; ++t) {
+            uint16_t h = xs[t * KVQ_D + c];
+            float x = h2f(h);
+            a += abs_units(h);
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+        }
+    } else {
+        float s1 = 0.f, s2 = 0.f;
+        for (int t = 0; t < G; ++t) {
+            float x = h2f(xs[t * KVQ_D + c]);
+            s1 = __fadd_rn(s1, x);
+            s2 = __fadd_rn(s2, __fmul_rn(x, x));
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+        }
+        float mean = __fdiv_rn(s1, (float)G);
+        var = __fsub_rn(__fdiv_rn(s2, (float)G), __fmul_rn(mean, mean));
     }
-    float mean = __fdiv_rn(s1, (float)G);
-    float var = __fsub_rn(__fdiv_rn(s2, (float)G), __fmul_rn(mean, mean));
     si[c] = a;
     sf[c] = var;
     __syncthreads();
@@ -278,10 +287,12 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
         rank += better ? 1 : 0;
     }
     const int boosted = rank < K;
-    boost[c] = boosted;
+    // r = boosted channels below c: a ballot within the warp plus the counts of the warps below
+    const unsigned bm = __ballot_sync(0xFFFFFFFFu, boosted);
+    if ((c & 31) == 0) boost[c >> 5] = __popc(bm);
     __syncthreads();
-    int r = 0;
-    for (int o = 0; o < c; ++o) r += boost[o];
+    int r = __popc(bm & ((1u << (c & 31)) - 1u));
+    for (int w = 0; w < (c >> 5); ++w) r += boost[w];
     const int qmax = boosted ? 15 : 3;
     uint16_t s, z;
     affine_fit(mn, mx, qmax, s, z);
@@ -359,6 +370,8 @@ __device__ __forceinline__ void int8_block_quant(const uint16_t *__restrict__ xb
     }
     __syncthreads();
     const float s0 = s_sh[4 * lane], s1 = s_sh[4 * lane + 1], s2 = s_sh[4 * lane + 2], s3 = s_sh[4 * lane + 3];
+    const float ri[4] = {s0 != 0.f ? __frcp_rn(s0) : 0.f, s1 != 0.f ? __frcp_rn(s1) : 0.f,
+                         s2 != 0.f ? __frcp_rn(s2) : 0.f, s3 != 0.f ? __frcp_rn(s3) : 0.f};
     for (int t = w; t < T; t += 8) {
         uint4 r = philox4x32_10(make_uint4((uint32_t)(t0 + t), (uint32_t)lane, c2, c3), k0, k1);
         uint2 u = *reinterpret_cast<const uint2 *>(xb + (int64_t)t * KVQ_D + 4 * lane);
@@ -369,11 +382,7 @@ __device__ __forceinline__ void int8_block_quant(const uint16_t *__restrict__ xb
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             int code = 0;
-            if (ss[i] != 0.0f) {
-                float xi = dither_from_word(wr[i]);
-                float v = __fadd_rn(__fdiv_rn(xs[i], ss[i]), xi);
-                code = (int)fminf(fmaxf(rintf(v), -127.f), 127.f);
-            }
+            if (ss[i] != 0.0f) code = dither_code(xs[i], ss[i], ri[i], dither_from_word(wr[i]));
             packed |= ((uint32_t)(code & 0xFF)) << (8 * i);
         }
         reinterpret_cast<uint32_t *>(codes + (int64_t)t * KVQ_D)[lane] = packed;
