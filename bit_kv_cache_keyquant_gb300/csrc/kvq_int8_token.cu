@@ -20,6 +20,7 @@
 #include <type_traits>
 
 #include "kvq_device.cuh"
+#include "kvq_quant.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {

@@ -6,6 +6,7 @@
 // contraction or approximate division changes a code; scales and zeros are
 // rounded with the directed fp16 conversions the C ABI documents.
 #include "kvq_device.cuh"
+#include "kvq_quant.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
