@@ -13,7 +13,8 @@ fp16 residual R = 128.  One step = one layer-step of the whole hot path:
 inputs resident in HBM, the K steps captured into a CUDA graph and timed
 over one replay; `e2e` is the same metric through the C ABI with the step's
 inputs copied from pinned host memory and the output copied back inside the
-timed region, the steps launched one by one from the host.  `--impl reference` times the CPU oracle on a
+timed region, the copies launched per step from the host and each step's
+kernels replayed as one CUDA graph.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -529,6 +530,17 @@ def run_gpu(args, w, rank, world, local_rank):
     in_ready = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer set s copied
     out_free = [torch.cuda.Event() for _ in range(2)]     # output of buffer set s read back
 
+    # each buffer set's decode step is captured once into a CUDA graph (kernels only; the copies stay on
+    # the copy streams, launched per step from the host)
+    step_graphs = []
+    for kk in range(2):
+        gk = torch.cuda.CUDAGraph()
+        bk = bufs[kk]
+        with torch.cuda.graph(gk, stream=gs):
+            decode_step(st, gs, q=bk["q"], vnew=bk["v"], knew=bk["k"], out=bk["out"])
+        step_graphs.append(gk)
+    torch.cuda.synchronize()
+
     def e2e_step(i):
         k = i % 2
         b = bufs[k]
@@ -540,17 +552,18 @@ def run_gpu(args, w, rank, world, local_rank):
         in_ready[k].record(h2d_s)
         stream.wait_event(in_ready[k])
         stream.wait_event(out_free[k])
-        decode_step(st, stream, q=b["q"], vnew=b["v"], knew=b["k"], out=b["out"])
+        with torch.cuda.stream(stream):
+            step_graphs[k].replay()
         in_free[k].record(stream)
         d2h_s.wait_event(in_free[k])
         with torch.cuda.stream(d2h_s):
             outh[k].copy_(b["out"], non_blocking=True)
         out_free[k].record(d2h_s)
 
-    # launched step by step from the host (a graph of the K steps with their copies measured 7-35 us
-    # per step slower on the large workloads: its copies did not overlap the neighbouring steps' kernels
-    # as the stream-launched ones do; on the tiny workload 1, whose steps are host-launch bound, the
-    # graph form was 17 us per step against 70-80)
+    # the copies launched step by step from the host (a graph of the K steps with their copies measured
+    # 7-35 us per step slower on the large workloads: its copies did not overlap the neighbouring steps'
+    # kernels as the stream-launched ones do; on the tiny workload 1, whose steps are host-launch bound,
+    # it gave 17 us per step, the per-step graphs 57 and step-by-step launches 78)
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -631,8 +644,8 @@ def run_gpu(args, w, rank, world, local_rank):
         "e2e": {"value": whole_job_us_per_step(e2e_ms, args.steps, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "every step's inputs from pinned host memory and its output back, on two copy streams "
-                          "overlapping the neighbouring steps (two device buffer sets); steps launched one by one "
-                          "from the host"},
+                          "overlapping the neighbouring steps (two device buffer sets), launched per step from "
+                          "the host; each step's kernels one CUDA graph replay"},
         "quant_kernels": quant,
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
