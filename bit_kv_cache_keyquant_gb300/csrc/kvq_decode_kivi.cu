@@ -57,11 +57,21 @@ struct Smem {
     float st_l[NCWARP];
 };
 
+// Warp maximum of a float in one redux instruction: the bit patterns are
+// mapped to unsigned integers in the floats' order (negative patterns
+// complemented, non-negative ones given the top bit) and back.
+__device__ __forceinline__ float warp_max_redux(float v) {
+    uint32_t b = __float_as_uint(v);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    b = __reduce_max_sync(0xFFFFFFFFu, b);
+    return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
+}
+
 // Online-softmax update of a warp state with one logit per lane (-inf for
 // empty lanes): returns p = 2^(logit - m) and rescales on a new maximum.
 __device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias,
                                               unsigned long long vacc2[16]) {
-    const float mt = warp_max(logit);
+    const float mt = warp_max_redux(logit);
     if (mt > m_run) {
         const float sc = exp2f(m_run - mt);
         l_part *= sc;
@@ -198,15 +208,11 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     const uint2 zv = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + si);
                     const float w[4] = {qf[0] * h2f(lo16(sv.x)), qf[1] * h2f(hi16(sv.x)), qf[2] * h2f(lo16(sv.y)),
                                         qf[3] * h2f(hi16(sv.y))};
-                    // the zero-point dot and the largest |weight|, reduced over the warp together
-                    float cb = qf[0] * h2f(lo16(zv.x)) + qf[1] * h2f(hi16(zv.x)) + qf[2] * h2f(lo16(zv.y)) +
-                               qf[3] * h2f(hi16(zv.y));
-                    float wm = fmaxf(fmaxf(fabsf(w[0]), fabsf(w[1])), fmaxf(fabsf(w[2]), fabsf(w[3])));
-    #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        cb += __shfl_xor_sync(0xFFFFFFFFu, cb, o);
-                        wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
-                    }
+                    // the zero-point dot, and the largest |weight| (non-negative floats order as their bits)
+                    const float cb = warp_sum(qf[0] * h2f(lo16(zv.x)) + qf[1] * h2f(hi16(zv.x)) +
+                                              qf[2] * h2f(lo16(zv.y)) + qf[3] * h2f(hi16(zv.y)));
+                    const float wm = __uint_as_float(__reduce_max_sync(
+                        0xFFFFFFFFu, __float_as_uint(fmaxf(fmaxf(fabsf(w[0]), fabsf(w[1])), fmaxf(fabsf(w[2]), fabsf(w[3]))))));
                     const int fx = key_fixed_exp(wm);
                     *reinterpret_cast<uint4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
                         key_weight_bytes(w, __int_as_float((127 + fx) << 23));
