@@ -65,3 +65,4 @@ def test_reference_arm_runs_on_rank_zero_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["higher_is_better"] is False and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["cores"] == (os.cpu_count() or 1)       # the oracle on every host core
