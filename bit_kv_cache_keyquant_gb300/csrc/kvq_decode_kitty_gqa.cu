@@ -36,6 +36,7 @@ struct SmemKG {
     uint64_t empty[KQ_NSTAGE];
     uint32_t qhi[KG_MAX][64];             // fp16x2 hi parts of alpha q 2^sigma: [head][k/2][r][4]
     uint32_t qlo[KG_MAX][64];
+    uint32_t qhl[KG_MAX][KVQ_D];          // channel order: fp16 hi | lo << 16 (the boosted rows' lookups)
     float qz[KG_MAX][KVQ_D];              // alpha q (fp32): [head][k][r][4]
     float qv[KVQ_D];                      // alpha q of one head, channel order (residual unit)
     float unsig[KG_MAX];                  // 2^-sigma_h
@@ -45,12 +46,6 @@ struct SmemKG {
     float st_m[NCWARP][KG_MAX];
     float st_l[NCWARP][KG_MAX];
 };
-
-// fragment-table word and half of channel c (tables [k/2][r][4] of fp16x2 pairs)
-__device__ __forceinline__ int qtab_word(int c) {
-    const int k = c >> 4, cc = c & 15;
-    return (k >> 1) * 16 + ((cc & 7) >> 1) * 4 + 2 * (k & 1) + (cc >> 3);
-}
 
 }  // namespace
 
@@ -128,6 +123,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
             *reinterpret_cast<uint2 *>(&S.qlo[h][pw]) =
                 make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
             *reinterpret_cast<float4 *>(&S.qz[h][tk * 16 + tr * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+            S.qhl[h][c0] = (uint32_t)hi[0] | ((uint32_t)lo[0] << 16);
+            S.qhl[h][c0 + 1] = (uint32_t)hi[1] | ((uint32_t)lo[1] << 16);
+            S.qhl[h][c0 + 8] = (uint32_t)hi[2] | ((uint32_t)lo[2] << 16);
+            S.qhl[h][c0 + 9] = (uint32_t)hi[3] | ((uint32_t)lo[3] << 16);
             if (lane == 0) S.unsig[h] = __int_as_float((127 - sigma) << 23);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
@@ -234,18 +233,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                         for (int hk = 0; hk < n_hk; ++hk) {
                             const int r0 = 16 * hk + 2 * r;
                             const int rows[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
-                            uint32_t qh2[2] = {0u, 0u}, ql2[2] = {0u, 0u}, s2[2] = {0u, 0u};
+                            uint32_t qh2[2], ql2[2], s2[2];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int ch = S.hchan[warp][rows[j]];
-                                if (ch != 0xFF) {
-                                    const int wq = qtab_word(ch), hs = 16 * (ch & 1);
-                                    const uint32_t qh = (S.qhi[hB][wq] >> hs) & 0xFFFFu, ql = (S.qlo[hB][wq] >> hs) & 0xFFFFu;
-                                    const uint32_t sh = ks[ch];
-                                    qh2[j >> 1] |= qh << (16 * (j & 1));
-                                    ql2[j >> 1] |= ql << (16 * (j & 1));
-                                    s2[j >> 1] |= sh << (16 * (j & 1));
-                                }
+                            for (int jp = 0; jp < 2; ++jp) {
+                                // rows past K (channel 0xFF) take weight 0
+                                const int ca = S.hchan[warp][rows[2 * jp]], cb = S.hchan[warp][rows[2 * jp + 1]];
+                                const uint32_t ha = ca < KVQ_D ? S.qhl[hB][ca] : 0u, hb = cb < KVQ_D ? S.qhl[hB][cb] : 0u;
+                                const uint32_t sa = ca < KVQ_D ? (uint32_t)ks[ca] : 0u, sb = cb < KVQ_D ? (uint32_t)ks[cb] : 0u;
+                                qh2[jp] = prmt(ha, hb, 0x5410u);
+                                ql2[jp] = prmt(ha, hb, 0x7632u);
+                                s2[jp] = sa | (sb << 16);
                             }
                             // 4 W = (4 qhi) s + ...: scaling the query parts by 4 is exact
                             const uint32_t b0 = split_prod(hmul2(qh2[0], 0x44004400u), hmul2(ql2[0], 0x44004400u), s2[0], xB);
