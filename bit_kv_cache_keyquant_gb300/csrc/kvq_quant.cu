@@ -41,19 +41,48 @@ __device__ __forceinline__ int kivi_sz_index(int c) {
 // planes of 1024 bytes, token q + 8p in plane p / (8/BITS) at bits
 // BITS*(p % (8/BITS)) of its 2-bit-layout byte.  Every thread of the block
 // calls it (block barriers inside).
-template <int NT, int BITS>
-__device__ __forceinline__ void key_group_quant_b(const uint16_t *__restrict__ src, uint8_t *__restrict__ codes,
-                                                  uint16_t *__restrict__ sz, uint16_t *xs, uint32_t *cw) {
-    constexpr int G = 32 * NT, CPB = 8 / BITS, NPL = BITS / 2, QMAX = (1 << BITS) - 1;
-    const int c = threadIdx.x;
-    __syncthreads();                                               // the block's previous group is stored
-    {
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-        uint4 *x4 = reinterpret_cast<uint4 *>(xs);
+// The codes of the thread's channel over the group staged in xs, as bytes of
+// the tile layout in cb (product form, or the quotient when EXACT); returns
+// whether the product form met a near-tie.
+template <int NT, int BITS, bool EXACT>
+__device__ __forceinline__ bool key_group_codes(const uint16_t *xs, uint8_t *cb, int c, int pos, float zf, float sf,
+                                                float rf) {
+    constexpr int CPB = 8 / BITS, NPL = BITS / 2, QMAX = (1 << BITS) - 1;
+    bool tie = false;
 #pragma unroll
-        for (int i = 0; i < 4 * NT; ++i) x4[c + 128 * i] = __ldg(s4 + c + 128 * i);
-    }
-    __syncthreads();
+    for (int tt = 0; tt < NT; ++tt)
+#pragma unroll 2
+        for (int q = 0; q < 8; ++q) {
+            uint32_t byte[NPL];
+#pragma unroll
+            for (int pl = 0; pl < NPL; ++pl) byte[pl] = 0u;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float x = h2f(xs[(tt * 32 + q + 8 * p) * KVQ_D + c]);
+                const uint32_t code = EXACT ? (uint32_t)affine_code(x, zf, sf, rf, QMAX)
+                                            : (uint32_t)affine_code_fast(x, zf, rf, tie);
+                byte[p / CPB] |= code << (BITS * (p % CPB));
+            }
+#pragma unroll
+            for (int pl = 0; pl < NPL; ++pl) cb[(tt * NPL + pl) * 1024 + q * 64 + pos] = (uint8_t)byte[pl];
+        }
+    return tie;
+}
+
+// One key group staged in xs (visible to the whole block) by a 128-thread
+// block, thread c = channel c: codes the group's G*D*BITS/8 bytes, sz its
+// 2*D fp16 (scales, then zeros).  Each thread reads its channel's column
+// (min / max, fit, codes) and writes its code bytes into a shared copy of
+// the tile layout (cw), which the block then stores with 16-byte stores.
+// BITS = 2 or 4: a 32-token tile is BITS/2 planes of 1024 bytes, token
+// q + 8p in plane p / (8/BITS) at bits BITS*(p % (8/BITS)) of its
+// 2-bit-layout byte.  Every thread of the block calls it (a block barrier
+// inside; cw is read by the block until its next barrier).
+template <int NT, int BITS>
+__device__ __forceinline__ void key_group_code_b(const uint16_t *xs, uint8_t *__restrict__ codes,
+                                                 uint16_t *__restrict__ sz, uint32_t *cw) {
+    constexpr int G = 32 * NT, NPL = BITS / 2, QMAX = (1 << BITS) - 1;
+    const int c = threadIdx.x;
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll 8
     for (int t = 0; t < G; ++t) {
@@ -71,26 +100,30 @@ __device__ __forceinline__ void key_group_quant_b(const uint16_t *__restrict__ s
     const int k = c >> 4, cc = c & 15;
     const int pos = (k >> 2) * 512 + ((cc & 7) >> 1) * 16 + (k & 3) * 4 + (cc & 1) + 2 * (cc >> 3);
     uint8_t *cb = reinterpret_cast<uint8_t *>(cw);
-#pragma unroll
-    for (int tt = 0; tt < NT; ++tt)
-#pragma unroll 2
-        for (int q = 0; q < 8; ++q) {
-            uint32_t byte[NPL];
-#pragma unroll
-            for (int pl = 0; pl < NPL; ++pl) byte[pl] = 0u;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const uint32_t code = (uint32_t)affine_code(h2f(xs[(tt * 32 + q + 8 * p) * KVQ_D + c]), zf, sf, rf, QMAX);
-                byte[p / CPB] |= code << (BITS * (p % CPB));
-            }
-#pragma unroll
-            for (int pl = 0; pl < NPL; ++pl) cb[(tt * NPL + pl) * 1024 + q * 64 + pos] = (uint8_t)byte[pl];
-        }
+    // the product form; a thread that met a near-tie redoes its column with the quotient
+    if (key_group_codes<NT, BITS, false>(xs, cb, c, pos, zf, sf, rf))
+        key_group_codes<NT, BITS, true>(xs, cb, c, pos, zf, sf, rf);
     __syncthreads();
     const uint4 *c4 = reinterpret_cast<const uint4 *>(cw);
     uint4 *o4 = reinterpret_cast<uint4 *>(codes);
 #pragma unroll
     for (int i = c; i < NT * NPL * 64; i += 128) o4[i] = c4[i];
+}
+
+// One key group from global memory: staged with 16-byte loads, then coded.
+template <int NT, int BITS>
+__device__ __forceinline__ void key_group_quant_b(const uint16_t *__restrict__ src, uint8_t *__restrict__ codes,
+                                                  uint16_t *__restrict__ sz, uint16_t *xs, uint32_t *cw) {
+    const int c = threadIdx.x;
+    __syncthreads();                                               // the block's previous group is stored
+    {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+        uint4 *x4 = reinterpret_cast<uint4 *>(xs);
+#pragma unroll
+        for (int i = 0; i < 4 * NT; ++i) x4[c + 128 * i] = __ldg(s4 + c + 128 * i);
+    }
+    __syncthreads();
+    key_group_code_b<NT, BITS>(xs, codes, sz, cw);
 }
 
 template <int NT>
@@ -102,15 +135,45 @@ __device__ __forceinline__ void key_group_quant(const uint16_t *__restrict__ src
     else key_group_quant_b<NT, 2>(src, codes, sz, xs, cw);
 }
 
-// Bulk key groups: a grid of resident blocks walks the groups.
-template <int NT>
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Bulk key groups: a grid of resident blocks walks the groups; with G <= 64
+// each block copies its next group (cp.async) into a second buffer while it
+// codes the current one.
+template <int NT, int BITS>
 __global__ void __launch_bounds__(128) quant_key_kivi_kernel(const uint16_t *__restrict__ k, int64_t n_groups,
-                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz,
-                                                             int bits) {
+                                                             uint8_t *__restrict__ codes, uint16_t *__restrict__ sz) {
     constexpr int G = 32 * NT;
-    for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x)
-        key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D * bits / 8, sz + g * 2 * KVQ_D,
-                            bits);
+    int64_t g = blockIdx.x;
+    if (g >= n_groups) return;
+    if constexpr (NT <= 2) {
+        __shared__ __align__(16) uint16_t xs[2][G * KVQ_D];
+        __shared__ __align__(16) uint32_t cw[NT * 2 * 256];
+        const int c = threadIdx.x;
+        auto issue = [&](int64_t gg, int b) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(k + gg * (int64_t)G * KVQ_D);
+            uint4 *dst = reinterpret_cast<uint4 *>(xs[b]);
+#pragma unroll
+            for (int i = 0; i < 4 * NT; ++i) cp_async16(dst + c + 128 * i, src + c + 128 * i);
+        };
+        issue(g, 0);
+        cp_async_commit();
+        for (int b = 0; g < n_groups; g += gridDim.x, b ^= 1) {
+            if (g + gridDim.x < n_groups) issue(g + gridDim.x, b ^ 1);
+            cp_async_commit();                                     // (an empty group past the end)
+            cp_async_wait_prev();                                  // this thread's copies of group g are in
+            __syncthreads();                                       // and every thread's; cw free again
+            key_group_code_b<NT, BITS>(xs[b], codes + g * (int64_t)G * KVQ_D * BITS / 8, sz + g * 2 * KVQ_D, cw);
+        }
+    } else {
+        for (; g < n_groups; g += gridDim.x)
+            key_group_quant<NT>(k + g * (int64_t)G * KVQ_D, codes + g * (int64_t)G * KVQ_D * BITS / 8,
+                                sz + g * 2 * KVQ_D, BITS);
+    }
 }
 
 // One value token by a warp, per token over groups of GV channels: lane l
@@ -167,22 +230,30 @@ __device__ __forceinline__ void value_token_store(uint8_t *__restrict__ tok, int
 // after the codes).
 // ---------------------------------------------------------------------------
 template <int GV, bool KITTY, int BITS>
-__global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
+__global__ void __launch_bounds__(256, 3) quant_value_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
                                                           uint8_t *__restrict__ out, uint32_t *__restrict__ sz,
                                                           int page_tokens, int64_t page_bytes) {
     constexpr int LG = GV / 16, QMAX = (1 << BITS) - 1;   // lanes per group
     const int lane = threadIdx.x & 31, ts = lane >> 3, cb = lane & 7;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t t0 = 4 * warp; t0 < n_tokens; t0 += 4 * nwarps) {
-        const int64_t t = t0 + ts;
-        const bool live = t < n_tokens;
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        if (live) {
+    // the lane's 16 channels of token t, zeros past the end
+    auto load = [&](int64_t t, uint4 &a, uint4 &b) {
+        a = make_uint4(0u, 0u, 0u, 0u);
+        b = a;
+        if (t < n_tokens) {
             const uint4 *p = reinterpret_cast<const uint4 *>(v + t * KVQ_D + 16 * cb);
             a = __ldg(p);
             b = __ldg(p + 1);
         }
+    };
+    uint4 na, nb;                                   // the next pass's tokens, loaded while this pass codes
+    load(4 * warp + ts, na, nb);
+    for (int64_t t0 = 4 * warp; t0 < n_tokens; t0 += 4 * nwarps) {
+        const int64_t t = t0 + ts;
+        const bool live = t < n_tokens;
+        const uint4 a = na, b = nb;
+        load(t + 4 * nwarps, na, nb);
         const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float x[16];
 #pragma unroll
@@ -205,11 +276,22 @@ __global__ void __launch_bounds__(256) quant_value_kernel(const uint16_t *__rest
         affine_fit(mn, mx, QMAX, s, z);
         const float sf = h2f(s), zf = h2f(z), rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
         uint32_t w[BITS / 2] = {};
+        bool tie = false;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const uint32_t code = (uint32_t)affine_code(x[i], zf, sf, rf, QMAX);
+            const uint32_t code = (uint32_t)affine_code_fast(x[i], zf, rf, tie);
             if (BITS == 2) w[0] |= code << (2 * i);
             else w[i / 8] |= code << (4 * (i % 8));
+        }
+        if (tie) {                       // a near-tie: the lane's codes again with the quotient
+#pragma unroll
+            for (int i = 0; i < BITS / 2; ++i) w[i] = 0u;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t code = (uint32_t)affine_code(x[i], zf, sf, rf, QMAX);
+                if (BITS == 2) w[0] |= code << (2 * i);
+                else w[i / 8] |= code << (4 * (i % 8));
+            }
         }
         if (!live) continue;
         if (!KITTY) {
@@ -305,19 +387,37 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
     uint32_t lw[8], hw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) { lw[i] = 0; hw[i] = 0; }
-    for (int t = 0; t < G; ++t) {
-        uint32_t code = (uint32_t)affine_code(h2f(xs[t * KVQ_D + c]), zv, sv, rv, qmax);
-        const int sh = 2 * (t & 15);
-        lw[t >> 4] |= (code & 3u) << sh;
-        hw[t >> 4] |= ((code >> 2) & 3u) << sh;
-    }
+    // word i of the planes holds tokens 16i..16i+15 (indices fixed at compile time: no local memory)
+    bool tie = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t code = (uint32_t)affine_code_fast(h2f(xs[(16 * i + j) * KVQ_D + c]), zv, rv, tie);
+            lw[i] |= (code & 3u) << (2 * j);
+            hw[i] |= ((code >> 2) & 3u) << (2 * j);
+        }
+
     uint4 *lrow = reinterpret_cast<uint4 *>(low + c * (G / 4));
     lrow[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     lrow[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    uint4 *hrow = reinterpret_cast<uint4 *>(high + (int64_t)r * (G / 4));
     if (boosted) {
-        uint4 *hrow = reinterpret_cast<uint4 *>(high + (int64_t)r * (G / 4));
         hrow[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         hrow[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    }
+    if (tie) {                           // a near-tie: the channel's rows again with the quotient
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            uint32_t l = 0u, hh = 0u;
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t code = (uint32_t)affine_code(h2f(xs[(16 * i + j) * KVQ_D + c]), zv, sv, rv, qmax);
+                l |= (code & 3u) << (2 * j);
+                hh |= ((code >> 2) & 3u) << (2 * j);
+            }
+            reinterpret_cast<uint32_t *>(lrow)[i] = l;
+            if (boosted) reinterpret_cast<uint32_t *>(hrow)[i] = hh;
+        }
     }
     idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
     ps[c] = s;
@@ -437,10 +537,18 @@ cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t 
         uint8_t *cs = cp + g0 * (int64_t)G * KVQ_D * cfg->bits_k / 8;
         uint16_t *zs = zp + g0 * 2 * KVQ_D;
         const int bits = cfg->bits_k;
-        const unsigned grid = (unsigned)grid_cap(n, G == 32 ? 16 : G == 64 ? 8 : 4);   // resident blocks per SM
-        if (G == 32) quant_key_kivi_kernel<1><<<grid, 128, 0, st>>>(ks, n, cs, zs, bits);
-        else if (G == 64) quant_key_kivi_kernel<2><<<grid, 128, 0, st>>>(ks, n, cs, zs, bits);
-        else quant_key_kivi_kernel<4><<<grid, 128, 0, st>>>(ks, n, cs, zs, bits);
+        const unsigned grid = (unsigned)grid_cap(n, G == 32 ? 12 : G == 64 ? 6 : 4);   // resident blocks per SM
+        const bool b4 = bits == 4;
+        if (G == 32) {
+            if (b4) quant_key_kivi_kernel<1, 4><<<grid, 128, 0, st>>>(ks, n, cs, zs);
+            else quant_key_kivi_kernel<1, 2><<<grid, 128, 0, st>>>(ks, n, cs, zs);
+        } else if (G == 64) {
+            if (b4) quant_key_kivi_kernel<2, 4><<<grid, 128, 0, st>>>(ks, n, cs, zs);
+            else quant_key_kivi_kernel<2, 2><<<grid, 128, 0, st>>>(ks, n, cs, zs);
+        } else {
+            if (b4) quant_key_kivi_kernel<4, 4><<<grid, 128, 0, st>>>(ks, n, cs, zs);
+            else quant_key_kivi_kernel<4, 2><<<grid, 128, 0, st>>>(ks, n, cs, zs);
+        }
     }
     return cudaGetLastError();
 }
@@ -448,7 +556,7 @@ cudaError_t launch_quant_key_kivi(const kvq_config *cfg, const void *k, int64_t 
 cudaError_t launch_quant_value_kivi(const kvq_config *cfg, const void *v, int64_t n_tokens, void *codes, void *sz,
                                     cudaStream_t st) {
     if (n_tokens == 0) return cudaSuccess;
-    const int grid = grid_cap((n_tokens + 31) / 32, 8);           // 32 tokens per 8-warp block pass
+    const int grid = grid_cap((n_tokens + 31) / 32, 3);           // 32 tokens per 8-warp block pass; 3 resident
     const uint16_t *vp = static_cast<const uint16_t *>(v);
     uint8_t *cp = static_cast<uint8_t *>(codes);
     uint32_t *zp = static_cast<uint32_t *>(sz);
@@ -468,7 +576,7 @@ cudaError_t launch_quant_value_kitty(const kvq_config *cfg, const void *v, int64
     if (n_pages == 0) return cudaSuccess;
     const int G = cfg->group_k;
     const int64_t n_tokens = n_pages * G;
-    const int grid = grid_cap((n_tokens + 31) / 32, 8);
+    const int grid = grid_cap((n_tokens + 31) / 32, 3);
     const int64_t pb = (int64_t)G * KVQ_D / 4 + 4LL * G;
     quant_value_kernel<128, true, 2><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens,
                                                            static_cast<uint8_t *>(pages), nullptr, G, pb);

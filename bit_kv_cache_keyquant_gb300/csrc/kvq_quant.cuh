@@ -45,6 +45,20 @@ __device__ __forceinline__ int affine_code(float x, float zf, float sf, float ri
     return (int)r;
 }
 
+// The code of an element of a group fitted by affine_fit, without the
+// quotient: rint(d * rinv).  For x in [mn, mx], d = fl(x - z) lies in
+// [0, qmax*s] (z <= mn, and qmax*s is an fp32 number >= mx - z), so the
+// result lies in [0, qmax] and needs no clamp; with s = 0 (rinv = 0, every
+// x = z) it is 0.  `tie` is set when the product lies within 2^-16.6 of a
+// half-integer, where only affine_code's quotient decides: callers then
+// recompute that element (or their whole set) with affine_code.
+__device__ __forceinline__ int affine_code_fast(float x, float zf, float rinv, bool &tie) {
+    const float qa = __fmul_rn(__fsub_rn(x, zf), rinv);
+    const float r = rintf(qa);
+    tie |= fabsf(__fsub_rn(qa, r)) > 0.49999f;
+    return (int)r;
+}
+
 // INT8 dithered code = clamp(rint(fl(x / s) + xi), -127, 127) in fp32 with
 // rounding to nearest (the definition), s != 0, rinv = fl(1 / s).  With
 // |x / s| < 127 the product x * rinv is within 2^-15.4 of fl(x / s), so the
