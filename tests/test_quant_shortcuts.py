@@ -1,0 +1,88 @@
+"""CPU checks of the two arithmetic shortcuts the write-side kernels take, in numpy float32 (IEEE
+binary32, round to nearest) against float64 references; no GPU and no oracle code involved.
+
+1. The fit's fix-up test: for fp16 mn <= mx, z = fp16_RD(mn) and an fp16 step s, the exact test
+   z + qmax*s < mx equals the fp32 test fl(qmax*s) < fl_up(mx - z) (qmax*s is an fp32 number; no fp32
+   number lies strictly between mx - z and its round-up).
+2. The element code: rint(fl(d * fl(1/s))) equals rint(fl(d / s)) whenever the product is farther than
+   0.5 - 1e-5 from a half-integer (|d / s| <= 32), so only near-ties need the quotient.
+"""
+import numpy as np
+
+
+def _f32_round_up(x64):
+    """Least float32 >= x64 (x64 a float64 holding an exact value)."""
+    f = x64.astype(np.float32)
+    lo = f.astype(np.float64) < x64
+    f[lo] = np.nextafter(f[lo], np.float32(np.inf))
+    return f
+
+
+def _fp16_rd(x):
+    h = x.astype(np.float16)
+    hi = h.astype(np.float64) > x
+    h[hi] = np.nextafter(h[hi], np.float16(-np.inf))
+    return h
+
+
+def test_fixup_test_exact_in_fp32():
+    np.seterr(over="ignore", invalid="ignore")
+    rng = np.random.default_rng(1)
+    n = 400000
+    scale = 10.0 ** rng.uniform(-6, 4.5, n)
+    a = (rng.standard_normal(n) * scale).astype(np.float16)
+    b = (a.astype(np.float64) + np.abs(rng.standard_normal(n)) * scale * 10.0 ** rng.uniform(-4, 0, n)).astype(np.float16)
+    ok = np.isfinite(a) & np.isfinite(b) & (b > a)
+    mn, mx = a[ok].astype(np.float64), b[ok].astype(np.float64)
+    z = _fp16_rd(mn).astype(np.float64)
+    for qmax in (3, 15):
+        # candidate steps around the fitted one, as the loop meets them
+        s0 = ((mx - z) / qmax).astype(np.float16)
+        for k in (-2, -1, 0, 1, 2):
+            s = s0.copy()
+            for _ in range(abs(k)):
+                s = np.nextafter(s, np.float16(np.inf if k > 0 else -np.inf))
+            s64 = s.astype(np.float64)
+            good = np.isfinite(s64) & (s64 > 0)
+            exact = z[good] + qmax * s64[good] < mx[good]
+            p32 = (np.float32(qmax) * s[good].astype(np.float32))
+            assert np.all(p32.astype(np.float64) == qmax * s64[good])            # p is an fp32 number
+            up = _f32_round_up(mx[good] - z[good])
+            assert np.array_equal(exact, p32 < up)
+
+
+def test_fixup_test_at_the_boundary():
+    """mx - z one fp16 subnormal above qmax*s: only the rounded-up difference keeps the test exact."""
+    np.seterr(over="ignore", invalid="ignore")
+    rng = np.random.default_rng(3)
+    s = (10.0 ** rng.uniform(-2, 3, 20000)).astype(np.float16)
+    for qmax in (3, 15):
+        p64 = qmax * s.astype(np.float64)
+        mx = p64.astype(np.float16)
+        keep = np.isfinite(mx) & (mx.astype(np.float64) == p64)          # qmax*s itself an fp16 number
+        for zt in (-2.0 ** -24, -2.0 ** -20, -2.0 ** -14):
+            z = np.full(keep.sum(), zt)
+            mxk, sk = mx[keep].astype(np.float64), s[keep]
+            exact = z + qmax * sk.astype(np.float64) < mxk                  # true: z < 0
+            p32 = np.float32(qmax) * sk.astype(np.float32)
+            assert exact.all()
+            assert np.array_equal(exact, p32 < _f32_round_up(mxk - z))
+
+
+def test_product_form_code_matches_quotient_off_ties():
+    rng = np.random.default_rng(2)
+    n = 2000000
+    s = (10.0 ** rng.uniform(-7, 4, n) * rng.uniform(0.5, 1.0, n)).astype(np.float16).astype(np.float32)
+    s = s[(s > 0) & np.isfinite(s)]
+    q = rng.uniform(0.0, 15.5, s.size)
+    # quotients spread over [0, 15.5], with a share placed near half-integers
+    near = rng.random(s.size) < 0.3
+    q[near] = np.floor(q[near]) + 0.5 + rng.uniform(-3e-5, 3e-5, near.sum())
+    d = (q * s.astype(np.float64)).astype(np.float32)
+    exact = np.rint((d / s).astype(np.float32))
+    rinv = (np.float32(1.0) / s).astype(np.float32)
+    qa = (d * rinv).astype(np.float32)
+    r = np.rint(qa)
+    tie = np.abs((qa - r).astype(np.float32)) > np.float32(0.49999)
+    assert tie.any() and (~tie).any()
+    assert np.array_equal(r[~tie], exact[~tie])
