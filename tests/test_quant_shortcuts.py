@@ -1,11 +1,12 @@
-"""CPU checks of the two arithmetic shortcuts the write-side kernels take, in numpy float32 (IEEE
-binary32, round to nearest) against float64 references; no GPU and no oracle code involved.
+"""CPU checks of the arithmetic shortcuts the kernels take, in numpy float32 (IEEE binary32, round to
+nearest) and integers against float64 references; no GPU and no oracle code involved.
 
 1. The fit's fix-up test: for fp16 mn <= mx, z = fp16_RD(mn) and an fp16 step s, the exact test
    z + qmax*s < mx equals the fp32 test fl(qmax*s) < fl_up(mx - z) (qmax*s is an fp32 number; no fp32
    number lies strictly between mx - z and its round-up).
 2. The element code: rint(fl(d * fl(1/s))) equals rint(fl(d / s)) whenever the product is farther than
    0.5 - 1e-5 from a half-integer (|d / s| <= 32), so only near-ties need the quotient.
+3. The per-head decode kernel's dp4a key products (below).
 """
 import numpy as np
 
@@ -86,3 +87,40 @@ def test_product_form_code_matches_quotient_off_ties():
     tie = np.abs((qa - r).astype(np.float32)) > np.float32(0.49999)
     assert tie.any() and (~tie).any()
     assert np.array_equal(r[~tie], exact[~tie])
+
+
+def _key_fixed_exp(wm):
+    """The per-head kernel's fixed-point exponent: wm 2^fx in [2^21, 2^22), clamped to [-100, 100]."""
+    ex = (np.asarray(wm, dtype=np.float32).view(np.uint32) >> 23) & 255
+    return np.clip(148 - ex.astype(np.int64), -100, 100)
+
+
+def test_dp4a_key_products_reconstruct_the_fixed_point_dot():
+    """3. The per-head kernel's key scores: weights alpha q s in 22-bit fixed point against the group's
+    largest |weight|, split into two unsigned bytes and a signed top byte; dp4a sums of four
+    (u8 code byte) x (weight byte) products, combined as (A0 + 256 A1) + 65536 A2, equal the integer
+    dot product exactly, and the result is within 128 * 3 * 2^-22 * max|W| (the weights' rounding) of
+    the binary64 dot product."""
+    rng = np.random.default_rng(4)
+    for trial in range(300):
+        w = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 3, 128)).astype(np.float32)
+        if trial % 7 == 0:
+            w[:] = 0.0                                     # an all-zero query: every weight 0
+        fx = int(_key_fixed_exp(np.max(np.abs(w))))
+        wi = np.rint(w.astype(np.float64) * 2.0 ** fx).astype(np.int64)      # fl(w 2^fx) is exact here
+        assert np.all(np.abs(wi) <= 2 ** 22)
+        b0, b1 = wi & 0xFF, (wi >> 8) & 0xFF
+        b2 = ((wi >> 16) & 0xFF).astype(np.int8).astype(np.int64)            # signed top byte
+        assert np.array_equal(b0 + 256 * b1 + 65536 * b2, wi)
+        for bits in (2, 4):
+            codes = rng.integers(0, 2 ** bits, size=128)
+            for slot in range(8 // bits):                  # the code's position in its byte
+                x = codes << (bits * slot)                 # the masked byte, an unsigned value
+                a0, a1, a2 = (int(np.sum(x * b)) for b in (b0, b1, b2))   # four-byte sums, accumulated
+                assert (a0 + (a1 << 8)) < 2 ** 31 and abs(a2) < 2 ** 24
+                combined = float(np.float32(a2)) * 65536.0 + float(np.float32(a0 + (a1 << 8)))
+                assert a0 + 256 * a1 + 65536 * a2 == int(np.sum(x * wi))
+                got = combined * 2.0 ** (-fx - bits * slot)
+                want = float(np.sum(codes.astype(np.float64) * w.astype(np.float64)))
+                bound = 128 * (2 ** bits - 1) * 0.5 * 2.0 ** -fx + 2 ** -22 * abs(want) + 1e-300
+                assert abs(got - want) <= bound
