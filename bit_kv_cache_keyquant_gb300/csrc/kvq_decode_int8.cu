@@ -106,22 +106,19 @@ __device__ __forceinline__ uint4 philox_rk(uint4 c, const uint32_t *rk0, const u
     return c;
 }
 
-// dither of the four channels 4*lane..4*lane+3 for counter word 0 = t (the
-// token, or the slot) and word 3 = w3 (exact: (w >> 8) 2^-24 - 1/2)
+// code - xi of the four channels 4*lane..4*lane+3 (codes: the int8 bytes of
+// w), with the dither of counter word 0 = t (the token, or the slot) and
+// word 3 = w3: xi = (r >> 8) 2^-24 - 1/2 exactly, so code - xi is
+// (code + 1/2) - (r >> 8) 2^-24 before its one rounding, formed by one FMA
+// (the same fp32 number as fl(code - xi)).
 template <typename PP>
-__device__ __forceinline__ void dither4(const PP &P, uint32_t c2, uint32_t w3, int t, int lane, float xi[4]) {
+__device__ __forceinline__ void code_minus_dither4(const PP &P, uint32_t w, uint32_t c2, uint32_t w3, int t, int lane,
+                                                   float d[4]) {
     const uint4 r = philox_rk(make_uint4((uint32_t)t, (uint32_t)lane, c2, w3), P.rk0, P.rk1);
-    xi[0] = dither_from_word(r.x);
-    xi[1] = dither_from_word(r.y);
-    xi[2] = dither_from_word(r.z);
-    xi[3] = dither_from_word(r.w);
-}
-
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float f[4]) {
-    f[0] = (float)(int8_t)(w & 0xFF);
-    f[1] = (float)(int8_t)((w >> 8) & 0xFF);
-    f[2] = (float)(int8_t)((w >> 16) & 0xFF);
-    f[3] = (float)(int8_t)(w >> 24);
+    const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        d[i] = fmaf(__uint2float_rn(rr[i] >> 8), -0x1.0p-24f, (float)(int8_t)((w >> (8 * i)) & 0xFFu) + 0.5f);
 }
 
 // Per-lane attention state: output accumulators of the lane's four channels
@@ -390,22 +387,22 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                     const float ks0 = h2f(lo16(ks.x)), ks1 = h2f(hi16(ks.x)), ks2 = h2f(lo16(ks.y)), ks3 = h2f(hi16(ks.y));
                     const float vs0 = h2f(lo16(vs.x)), vs1 = h2f(hi16(vs.x)), vs2 = h2f(lo16(vs.y)), vs3 = h2f(hi16(vs.y));
                     auto kfn = [=](int tt, float kv[4]) {
-                        float c[4], xi[4];
-                        i8x4_to_f32(*reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c);
-                        dither4(P, c2, req, r0 + tt, lane, xi);
-                        kv[0] = ks0 * (c[0] - xi[0]);
-                        kv[1] = ks1 * (c[1] - xi[1]);
-                        kv[2] = ks2 * (c[2] - xi[2]);
-                        kv[3] = ks3 * (c[3] - xi[3]);
+                        float d[4];
+                        code_minus_dither4(P, *reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c2, req, r0 + tt,
+                                           lane, d);
+                        kv[0] = ks0 * d[0];
+                        kv[1] = ks1 * d[1];
+                        kv[2] = ks2 * d[2];
+                        kv[3] = ks3 * d[3];
                     };
                     auto vfn = [=](int tt, float vv[4]) {
-                        float c[4], xi[4];
-                        i8x4_to_f32(*reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c);
-                        dither4(P, c2 | 0x10000u, req, r0 + tt, lane, xi);
-                        vv[0] = vs0 * (c[0] - xi[0]);
-                        vv[1] = vs1 * (c[1] - xi[1]);
-                        vv[2] = vs2 * (c[2] - xi[2]);
-                        vv[3] = vs3 * (c[3] - xi[3]);
+                        float d[4];
+                        code_minus_dither4(P, *reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c2 | 0x10000u, req,
+                                           r0 + tt, lane, d);
+                        vv[0] = vs0 * d[0];
+                        vv[1] = vs1 * d[1];
+                        vv[2] = vs2 * d[2];
+                        vv[3] = vs3 * d[3];
                     };
                     tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
                 }
@@ -623,24 +620,23 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
                 const uint16_t(*vs)[4] = S.vs[buf] + 32 * warp;
                 const int32_t *sl = S.slot[buf] + 32 * warp;
                 auto kfn = [=](int tt, float kv[4]) {
-                    float c[4], xi[4];
-                    i8x4_to_f32(*reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c);
-                    dither4(P, c2, 0u, sl[tt], lane, xi);
+                    float d[4];
+                    code_minus_dither4(P, *reinterpret_cast<const uint32_t *>(kc + tt * KVQ_D), c2, 0u, sl[tt], lane, d);
                     const float sc = h2f(ks[tt][gi]);
-                    kv[0] = sc * (c[0] - xi[0]);
-                    kv[1] = sc * (c[1] - xi[1]);
-                    kv[2] = sc * (c[2] - xi[2]);
-                    kv[3] = sc * (c[3] - xi[3]);
+                    kv[0] = sc * d[0];
+                    kv[1] = sc * d[1];
+                    kv[2] = sc * d[2];
+                    kv[3] = sc * d[3];
                 };
                 auto vfn = [=](int tt, float vv[4]) {
-                    float c[4], xi[4];
-                    i8x4_to_f32(*reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c);
-                    dither4(P, c2 | 0x10000u, 0u, sl[tt], lane, xi);
+                    float d[4];
+                    code_minus_dither4(P, *reinterpret_cast<const uint32_t *>(vc + tt * KVQ_D), c2 | 0x10000u, 0u,
+                                       sl[tt], lane, d);
                     const float sc = h2f(vs[tt][gi]);
-                    vv[0] = sc * (c[0] - xi[0]);
-                    vv[1] = sc * (c[1] - xi[1]);
-                    vv[2] = sc * (c[2] - xi[2]);
-                    vv[3] = sc * (c[3] - xi[3]);
+                    vv[0] = sc * d[0];
+                    vv[1] = sc * d[1];
+                    vv[2] = sc * d[2];
+                    vv[3] = sc * d[3];
                 };
                 tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
             }
