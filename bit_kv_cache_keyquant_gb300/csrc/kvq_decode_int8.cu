@@ -41,7 +41,10 @@ struct Smem {
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
     float pw[NCWARP][32][GMAX];            // per-warp softmax weights of the tile's 32 tokens
-    float st_acc[NCWARP][GMAX][KVQ_D];
+    union {                                // a warp's region: key partials inside a tile, its state at the unit end
+        float st_acc[NCWARP][GMAX][KVQ_D];
+        float red[NCWARP][32][32];
+    };
     float st_m[NCWARP][GMAX];
     float st_l[NCWARP][GMAX];
 };
@@ -166,6 +169,7 @@ template <typename SM>
 __device__ __forceinline__ void write_unit(SM &S, const HeadState &H, float *ws_o, float *ws_lse, int64_t head_row0,
                                            int g, int splits, int split, int warp, int lane) {
     // ---- warp states -> shared memory ----
+    __syncwarp();                        // the last tile's reads of this warp's reduction rows are done
     {
         float l_w = H.l;
         l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
@@ -213,7 +217,7 @@ __device__ __forceinline__ void write_unit(SM &S, const HeadState &H, float *ws_
 // the key weights (alpha q) of heads 2j, 2j+1 for channel i.
 template <typename KF, typename VF>
 __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 2][4], KF kfn, VF vfn, HeadState &H,
-                                     float (*pw)[GMAX], int lane) {
+                                     float (*pw)[GMAX], float (*red)[32], int lane) {
     // ---- keys: 8 batches of 4 tokens; per lane 4 x 8 head partials over its 4 channels, then a
     //      reduce-scatter over all 32 lanes leaves lane L with token 4c + L/8, head L%8 ----
     float sc[8];
@@ -235,16 +239,19 @@ __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 
                 v[8 * m + 2 * j + 1] = hi2f(d);
             }
         }
+        // sum over the 32 lanes through shared memory: lane l stores its 32 partials as row l (16-byte
+        // chunk k at k ^ (l & 7): four wavefronts a store), then lane L sums column L (conflict-free)
+        __syncwarp();                                              // the previous batch's columns are read
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const bool up = (lane & o) != 0;
+        for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4 *>(&red[lane][4 * (k ^ (lane & 7))]) =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        __syncwarp();
+        float acc = 0.f;
+        const int col = lane & 3, chunk = lane >> 2;
 #pragma unroll
-            for (int j = 0; j < o; ++j) {
-                const float send = up ? v[j] : v[j + o];
-                v[j] = (up ? v[j + o] : v[j]) + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-            }
-        }
-        const float s = 4 * c4 + (lane >> 3) < n ? v[0] : -INFINITY;
+        for (int l = 0; l < 32; ++l) acc += red[l][4 * (chunk ^ (l & 7)) + col];
+        const float s = 4 * c4 + (lane >> 3) < n ? acc : -INFINITY;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
             if (c == c4) sc[c] = s;
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                     const uint2 x = __ldg(reinterpret_cast<const uint2 *>(vt + (int64_t)((r0 + tt) % T) * KVQ_D));
                     vv[0] = h2f(lo16(x.x)); vv[1] = h2f(hi16(x.x)); vv[2] = h2f(lo16(x.y)); vv[3] = h2f(hi16(x.y));
                 };
-                tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
+                tile(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
             }
         } else {
             const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
@@ -404,7 +411,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                         vv[2] = vs2 * d[2];
                         vv[3] = vs3 * d[3];
                     };
-                    tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
+                    tile(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -486,7 +493,10 @@ struct SmemT {
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
     float pw[NCWARP][32][GMAX];
-    float st_acc[NCWARP][GMAX][KVQ_D];
+    union {
+        float st_acc[NCWARP][GMAX][KVQ_D];
+        float red[NCWARP][32][32];
+    };
     float st_m[NCWARP][GMAX];
     float st_l[NCWARP][GMAX];
 };
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
                     vv[2] = sc * d[2];
                     vv[3] = sc * d[3];
                 };
-                tile(n, wk2, kfn, vfn, H, S.pw[warp], lane);
+                tile(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[buf]);
