@@ -219,7 +219,7 @@ template <typename KF, typename VF>
 __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 2][4], KF kfn, VF vfn, HeadState &H,
                                      float (*pw)[GMAX], float (*red)[32], int lane) {
     // ---- keys: 8 batches of 4 tokens; per lane 4 x 8 head partials over its 4 channels, then a
-    //      reduce-scatter over all 32 lanes leaves lane L with token 4c + L/8, head L%8 ----
+    //      sum over all 32 lanes leaves lane L with token 4c + L/8, head L%8 ----
     float sc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) sc[c] = -INFINITY;
@@ -247,11 +247,11 @@ __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 
             *reinterpret_cast<float4 *>(&red[lane][4 * (k ^ (lane & 7))]) =
                 make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         __syncwarp();
-        float acc = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};                      // four chains of eight dependent adds
         const int col = lane & 3, chunk = lane >> 2;
 #pragma unroll
-        for (int l = 0; l < 32; ++l) acc += red[l][4 * (chunk ^ (l & 7)) + col];
-        const float s = 4 * c4 + (lane >> 3) < n ? acc : -INFINITY;
+        for (int l = 0; l < 32; ++l) acc[l & 3] += red[l][4 * (chunk ^ (l & 7)) + col];
+        const float s = 4 * c4 + (lane >> 3) < n ? (acc[0] + acc[1]) + (acc[2] + acc[3]) : -INFINITY;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
             if (c == c4) sc[c] = s;
