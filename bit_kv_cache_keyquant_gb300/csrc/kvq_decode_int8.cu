@@ -16,9 +16,11 @@
 //   * a consumer warp owns 32 tokens of a stage; lane l owns channels
 //     4l..4l+3, so one Philox call (counter word 1 = l) yields its four
 //     dithers per token (the "four-output reuse");
-//   * keys: per token, 8 head partials over the lane's 4 channels are
-//     reduce-scattered across the warp until every lane holds the 8 head
-//     scores of one token; per-head online softmax in base 2;
+//   * keys: per token, 8 head partials over the lane's 4 channels; for 4
+//     tokens at a time each lane writes its 32 partials as one row of a
+//     per-warp shared-memory block and then sums one column over the 32
+//     rows, so that lane L holds head L%8 of token L/8 of the four;
+//     per-head online softmax in base 2;
 //   * values: the 8 head weights of each token are broadcast through shared
 //     memory and accumulated into 8 x 4 fp32 accumulators per lane.
 // The last split of every row covers the fp16 tail with the same tile code.
