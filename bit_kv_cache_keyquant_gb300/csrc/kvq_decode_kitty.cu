@@ -213,7 +213,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 float a = lo2f(vacc2[i]), c = hi2f(vacc2[i]);
-            #pragma unroll
+#pragma unroll
                 for (int o = 4; o <= 16; o <<= 1) {
                     a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
                     c += __shfl_xor_sync(0xFFFFFFFFu, c, o);

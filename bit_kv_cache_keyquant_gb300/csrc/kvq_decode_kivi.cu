@@ -193,14 +193,13 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
             unsigned long long vacc2[16];
 #pragma unroll
-for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
+            for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
             for (int s = 0; s < U.nstages; ++s, ++sg) {
                 const int slot = sg % NSTAGE;
                 ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
                 const int tile = s * NCWARP + warp;
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];
-                    
                     const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + GG::KC) + gl * 2 * KVQ_D;
                     // ---- this group's key weights alpha q s in 22-bit fixed point, and alpha sum q z ----
                     const int si = (((lane & 7) >> 1) * 4 + (lane >> 3)) * 8 + (lane & 1) * 4;
@@ -221,7 +220,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     //      token j sits in plane j / CPB at bits BK * (j % CPB) ----
                     const uint8_t *kt = st + warp * 512 * BK;
                     uint32_t kw[NPL][8];
-    #pragma unroll
+#pragma unroll
                     for (int pl = 0; pl < NPL; ++pl) {
                         const uint4 ka = *reinterpret_cast<const uint4 *>(kt + pl * 1024 + lane * 16);
                         const uint4 kb = *reinterpret_cast<const uint4 *>(kt + pl * 1024 + 512 + lane * 16);
@@ -230,14 +229,14 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     }
                     const uint4 *qd = reinterpret_cast<const uint4 *>(&S.qk[warp][tq * QK_ROW]);
                     int acc[4][3];                                              // token j, weight byte
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = 0;
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint4 d = qd[k];                                  // channels 16k + 2tq + {0,1,8,9}
-    #pragma unroll
+#pragma unroll
                         for (int pl = 0; pl < NPL; ++pl) {
-    #pragma unroll
+#pragma unroll
                             for (int jj = 0; jj < CPB; ++jj) {
                                 const int j = pl * CPB + jj;
                                 const uint32_t x = kw[pl][k] & ((((1u << BK) - 1) * 0x01010101u) << (BK * jj));
@@ -249,7 +248,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     }
                     // weight bytes 0 + 1 fit an int32 (< 2^29); the sum is code * 2^(BK (j % CPB)) * W 2^fx
                     float a[4];
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 4; ++j) a[j] = fmaf((float)acc[j][2], 65536.f, (float)(acc[j][0] + (acc[j][1] << 8)));
                     // transpose-reduce over the 4 lanes of the quad: lane keeps token q + 8tq
                     float score;
@@ -267,7 +266,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                     const uint8_t *vc = st + GG::KC + GG::KSZ + warp * 32 * (KVQ_D * BV / 8);
                     const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + GG::KC + GG::KSZ + GG::VC) +
                                           warp * 32 * ngv;
-    #pragma unroll
+#pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const int tau = 8 * r + ts;
                         const float pt = __shfl_sync(0xFFFFFFFFu, p, 4 * ts + r);   // token tau = ts + 8r
@@ -288,10 +287,10 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
             // ---- warp state -> shared memory (channel order) ----
             {
                 const float l_w = warp_sum(l_part);
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float a = lo2f(vacc2[i]), c = hi2f(vacc2[i]);
-                #pragma unroll
+#pragma unroll
                     for (int o = 4; o <= 16; o <<= 1) {
                         a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
                         c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
