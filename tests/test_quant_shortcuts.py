@@ -7,6 +7,7 @@ nearest) and integers against float64 references; no GPU and no oracle code invo
 2. The element code: rint(fl(d * fl(1/s))) equals rint(fl(d / s)) whenever the product is farther than
    0.5 - 1e-5 from a half-integer (|d / s| <= 32), so only near-ties need the quotient.
 3. The per-head decode kernel's dp4a key products (below).
+4. The INT8 decode kernel's warp sum through shared memory (below).
 """
 import numpy as np
 
@@ -124,3 +125,34 @@ def test_dp4a_key_products_reconstruct_the_fixed_point_dot():
                 want = float(np.sum(codes.astype(np.float64) * w.astype(np.float64)))
                 bound = 128 * (2 ** bits - 1) * 0.5 * 2.0 ** -fx + 2 ** -22 * abs(want) + 1e-300
                 assert abs(got - want) <= bound
+
+
+def test_int8_swizzled_column_sum():
+    """The INT8 decode kernel sums 32 partials per lane over the warp by storing lane l's 32 floats as
+    row l of a 32 x 32 float block, its 16-byte chunk k at chunk position k ^ (l & 7), and letting lane
+    L read column L: element (4 * (L >> 2) + (L & 3)) of every row, found at chunk (L >> 2) ^ (l & 7).
+    Checked here: the read gives lane L the sum over lanes of partial L (what the register
+    reduce-scatter gave), every row is written whole and once, each 16-byte store of a chunk index k
+    by the warp touches every one of the 32 banks exactly four times (four wavefronts, the minimum for
+    512 bytes), and each column load touches 32 distinct banks (one wavefront)."""
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal((32, 32)).astype(np.float32)        # v[lane, k]: lane's partial k
+    smem = np.full((32, 32), np.nan, dtype=np.float32)
+    written = np.zeros((32, 32), dtype=int)
+    for k in range(8):                                          # store instruction k, all lanes
+        banks = np.zeros(32, dtype=int)
+        for lane in range(32):
+            pos = 4 * (k ^ (lane & 7))
+            smem[lane, pos:pos + 4] = v[lane, 4 * k:4 * k + 4]
+            written[lane, pos:pos + 4] += 1
+            for w in range(4):
+                banks[(lane * 32 + pos + w) % 32] += 1
+        assert (banks == 4).all()
+    assert (written == 1).all()
+    got = np.zeros(32, dtype=np.float64)
+    for row in range(32):                                       # load instruction row, all lanes
+        addr = [row * 32 + 4 * ((L >> 2) ^ (row & 7)) + (L & 3) for L in range(32)]
+        assert len({a % 32 for a in addr}) == 32
+        for L in range(32):
+            got[L] += smem.reshape(-1)[addr[L]]
+    np.testing.assert_allclose(got, v.astype(np.float64).sum(axis=0), rtol=1e-5, atol=1e-5)
