@@ -81,7 +81,7 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u) {
     const int row = u - U.split * rows;
     U.b = row / P.Hkv;
     U.kvh = row - U.b * P.Hkv;
-    U.L = P.seq_len[U.b];
+    U.L = clamp_len(P.seq_len[U.b], (int)P.cap, P.err);
     const int ntail = ((U.L - 1) % P.T) + 1;
     U.nq = U.L - ntail;
     U.residual = U.split == P.splits - 1;
@@ -459,14 +459,8 @@ cudaError_t launch_decode_int8(const kvq_config *cfg, const kvq_int8_cache *c, c
     if (!P.err) return cudaErrorInvalidDevicePointer;
     if (P.g > GMAX) return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(int8_decode_kernel, smem, attr_done)) return e;
     const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 2;
     if (grid > n_units) grid = n_units;
@@ -527,7 +521,7 @@ __device__ __forceinline__ UnitT unit_of_t(const ParamsT &P, int u) {
     const int row = u - U.split * rows;
     U.b = row / P.Hkv;
     U.kvh = row - U.b * P.Hkv;
-    const int L = min(P.seq_len[U.b], P.cap);   // a length above the table's row is read as the full row
+    const int L = clamp_len(P.seq_len[U.b], P.cap, P.err);   // a length above the table's row: the full row
     U.t0 = U.split * P.chunk;
     U.t1 = max(U.t0, min(U.t0 + P.chunk, L));
     return U;
@@ -692,15 +686,8 @@ cudaError_t launch_decode_int8_token(const kvq_config *cfg, const kvq_int8_token
     if (!P.err) return cudaErrorInvalidDevicePointer;
     if (P.g > GMAX) return cudaErrorInvalidValue;
     const size_t smem = sizeof(SmemT);
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(int8_token_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(int8_token_decode_kernel, smem, attr_done)) return e;
     const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 2;
     if (grid > n_units) grid = n_units;

@@ -285,6 +285,7 @@ cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
     P.chunk = p.chunk;
     P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + PG - 1) / PG;
     if (P.page_cap < 1) P.page_cap = 1;
+    P.max_len = c->max_seq_len;
     P.kpb = KVQ_D * PG / 4 + cfg->boost_k * PG / 4 + KVQ_D + 4 * KVQ_D;
     P.vpb = PG * KVQ_D / 4 + 4 * PG;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
@@ -293,14 +294,8 @@ cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
     if (!P.err) return cudaErrorInvalidDevicePointer;
     if (P.kpb > VREC_OFF || P.K > KMAX) return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kitty_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(kitty_decode_kernel, smem, attr_done)) return e;
     const int64_t n_units = (int64_t)c->batch * cfg->n_q_heads * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;

@@ -341,15 +341,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
 template <int BK, int BV, int NST>
 static cudaError_t launch_kivi_variant(const Params &P, int64_t grid, cudaStream_t st) {
     const size_t smem = sizeof(Smem<BK, BV, NST>);
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kivi_decode_kernel<BK, BV, NST>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(kivi_decode_kernel<BK, BV, NST>, smem, attr_done)) return e;
     kivi_decode_kernel<BK, BV, NST><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
     return cudaGetLastError();
 }

@@ -415,15 +415,8 @@ bool kivi_gqa_supported(const kvq_config *cfg) {
 template <int NGV, int BK, int BV, int NST>
 static cudaError_t launch_gqa_variant(const Params &P, int64_t grid, cudaStream_t st) {
     const size_t smem = sizeof(SmemG<BK, BV, NST>);
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kivi_decode_gqa_kernel<NGV, BK, BV, NST>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(kivi_decode_gqa_kernel<NGV, BK, BV, NST>, smem, attr_done)) return e;
     kivi_decode_gqa_kernel<NGV, BK, BV, NST><<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);
     return cudaGetLastError();
 }

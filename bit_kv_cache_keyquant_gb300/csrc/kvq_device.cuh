@@ -4,6 +4,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "../../include/kvq.h"
+
 #define KVQ_D 128
 #define KVQ_SUSPEND_NS 20000u      // mbarrier try_wait suspend hint (ns)
 #define KVQ_SPIN_LIMIT (1u << 16)   // bounded mbarrier waits: about 1.3 s at most
@@ -212,6 +214,17 @@ __device__ __forceinline__ void scale_pairs(unsigned long long acc2[16], float s
         asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(acc2[i]), "l"(s2));
         acc2[i] = d;
     }
+}
+
+// A cached length as the decode kernels use it: seq_len[b] clamped into
+// [0, max_len], so that a corrupt length can never move a read outside the
+// caller's arrays; a clamped length records KVQ_DEVICE_ERR_CAPACITY.
+__device__ __forceinline__ int clamp_len(int L, int max_len, unsigned *err) {
+    if (L < 0 || L > max_len) {
+        atomicOr(err, KVQ_DEVICE_ERR_CAPACITY);
+        L = L < 0 ? 0 : max_len;
+    }
+    return L;
 }
 
 __device__ __forceinline__ float warp_max(float v) {

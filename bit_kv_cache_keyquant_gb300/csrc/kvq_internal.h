@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -58,6 +60,22 @@ inline KiviSrc kivi_src(const kvq_kivi_paged_cache *c) {
 // bytes of one paged KIVI page record: key codes, key (s, z), value codes, value (s, z) of 128 tokens
 inline int64_t kivi_page_bytes(int bits_k, int bits_v) {
     return 16LL * 128 * bits_k + 2048 + 16LL * 128 * bits_v + 2048;   // D = 128
+}
+
+// Opts a kernel into `smem` bytes of dynamic shared memory, once per device:
+// `done` is that kernel's own bitmask of devices already set up.  Host
+// threads that make a first launch together may both set the attribute (it
+// is idempotent); none can skip it.
+template <typename Kern>
+inline cudaError_t smem_opt_in(Kern *kernel, size_t smem, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
 }
 
 int num_sms();

@@ -23,6 +23,7 @@ struct Params {
     float *ws_o, *ws_lse;
     unsigned *err;
     int B, Hq, Hkv, S, R, K, splits, chunk, page_cap;
+    int max_len;        // max_seq_len: seq_len[b] is read clamped into [0, max_len]
     int kpb, vpb;
     float alpha;
     int e0;
@@ -57,7 +58,7 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
     }
     U.b = row / hpr;
     U.hq = row - U.b * hpr;
-    const int L = P.seq_len[U.b];
+    const int L = clamp_len(P.seq_len[U.b], P.max_len, P.err);
     U.L = L;
     if (L > P.S) {
         U.nkb = ((L - P.S - 1) % PG) + 1;

@@ -43,6 +43,7 @@ struct Params {
     unsigned *err;
     int B, Hq, Hkv, G, Gv, R, splits, chunk;
     int ngv;            // D / Gv: value (s, z) pairs per token
+    int max_len;        // max_seq_len: seq_len[b] is read clamped into [0, max_len]
     int64_t cap;        // token capacity per (b, kvh): max_seq_len rounded up to 128
     int64_t kgrp_cap;   // cap / G
     float alpha;
@@ -87,7 +88,7 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
     }
     U.b = row / hpr;
     U.hq = row - U.b * hpr;
-    const int L = P.seq_len[U.b];
+    const int L = clamp_len(P.seq_len[U.b], P.max_len, P.err);
     const int rK = ((L - 1) % P.R) + 1;
     U.nKq = L - rK;
     U.nVq = L - (L < P.R ? L : P.R);
@@ -357,6 +358,7 @@ inline Params kivi_params(const kvq_config *cfg, const KiviSrc &c, const void *q
     P.Gv = cfg->group_v;
     P.ngv = KVQ_D / cfg->group_v;
     P.R = cfg->residual;
+    P.max_len = c.max_seq_len;
     P.cap = ((int64_t)c.max_seq_len + 127) / 128 * 128;
     P.splits = p.splits;
     P.chunk = p.chunk;

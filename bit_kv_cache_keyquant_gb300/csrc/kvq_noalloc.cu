@@ -25,23 +25,50 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCR
 namespace {
 constexpr int kMaxDev = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDev] = {nullptr};
+struct ScratchEntry {
+    void *ctx;    // the context the address belongs to
+    void *ptr;
+};
+ScratchEntry g_scratch[kMaxDev] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (host code cannot use the array's name as a device pointer).
+// The calling thread's current CUDA context (null if none, or if the driver
+// does not hand out cuCtxGetCurrent), reached through the runtime's driver
+// entry-point query so that the library needs no link to the driver library.
+void *current_context() {
+    typedef int (*ctx_get_t)(void **);
+    static ctx_get_t fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (ctx_get_t) nullptr;
+        return reinterpret_cast<ctx_get_t>(p);
+    }();
+    void *ctx = nullptr;
+    if (!fn || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
+
+// Device address of the scratch array in the current device's context
+// (host code cannot use the array's name as a device pointer).  Looked up
+// once per device and context: after a device reset the context, and with it
+// the array's address, changes, and the next call looks it up again.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchEntry &ent = g_scratch[dev];
+    void *ctx = current_context();
+    if (!ent.ptr || !ctx || ent.ctx != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
+        ent.ptr = p;
+        ent.ctx = current_context();     // the lookup makes the device's primary context current
     }
-    *out = g_scratch_ptr[dev];
+    *out = ent.ptr;
     return cudaSuccess;
 }
 }  // namespace

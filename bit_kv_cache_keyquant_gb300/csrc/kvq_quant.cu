@@ -589,15 +589,8 @@ cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t
     const int G = cfg->group_k, K = cfg->boost_k;
     const int64_t pb = (int64_t)KVQ_D * G / 4 + (int64_t)K * G / 4 + KVQ_D + 4LL * KVQ_D;
     const size_t smem = KITTY_KEY_SMEM;
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(quant_key_kitty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(quant_key_kitty_kernel, smem, attr_done)) return e;
     const int grid = grid_cap(n_pages, 4);
     quant_key_kitty_kernel<<<grid, 128, smem, st>>>(static_cast<const uint16_t *>(k), n_pages, K, score_mode,
                                                     static_cast<uint8_t *>(pages), pb);
@@ -1094,15 +1087,8 @@ cudaError_t launch_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_
     const int64_t kpb = (int64_t)KVQ_D * 128 / 4 + (int64_t)cfg->boost_k * 128 / 4 + KVQ_D + 4LL * KVQ_D;
     const KittyPagedDst D = kitty_paged_dst(cfg, c, c->k_pages, kpb, page0, row, kvh);
     if (!D.err) return cudaErrorInvalidDevicePointer;
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(quant_key_kitty_paged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)KITTY_KEY_SMEM);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(quant_key_kitty_paged_kernel, KITTY_KEY_SMEM, attr_done)) return e;
     const int grid = grid_cap(n, 4);
     quant_key_kitty_paged_kernel<<<grid, 128, KITTY_KEY_SMEM, st>>>(static_cast<const uint16_t *>(k), n, cfg->boost_k,
                                                                     score_mode, D);
@@ -1245,15 +1231,8 @@ static cudaError_t launch_append_kitty_impl(const kvq_config *cfg, const kvq_kit
     if (P.page_cap < 1) P.page_cap = 1;
     P.kpb = (int64_t)KVQ_D * 128 / 4 + (int64_t)cfg->boost_k * 128 / 4 + KVQ_D + 4LL * KVQ_D;
     P.vpb = 128LL * KVQ_D / 4 + 4LL * 128;
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(append_kitty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)KITTY_KEY_SMEM);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_opt_in(append_kitty_kernel, KITTY_KEY_SMEM, attr_done)) return e;
     if (c->page_table) {
         cudaError_t e = launch_alloc_ids(c->seq_len, const_cast<int32_t *>(c->page_table), c->batch, c->max_seq_len,
                                          128, P.page_cap, cfg->sink, pool, st);

@@ -498,7 +498,9 @@ KVQ_API kvq_status kv_decode_attn_int8_token(const kvq_config *cfg, const kvq_in
  *     workspace (kv_decode_attn_plan) exceeds KVQ_NOALLOC_SCRATCH_BYTES.
  *   - The first call on each device looks the array's device address up
  *     (cudaGetSymbolAddress); make that first call before any stream
- *     capture on that device.
+ *     capture on that device.  The address is kept per device and context:
+ *     after a device reset the next call looks it up again (so, again,
+ *     outside a capture).
  *   - Every call uses the same array: calls whose kernels can overlap on the
  *     GPU (other streams, other host threads) race and must be serialized
  *     by the caller.  No part of the array needs clearing between calls.

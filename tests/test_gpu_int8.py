@@ -63,6 +63,32 @@ def test_int8_decode_parity(K, orc, Hq, Hkv, lens):
     assert_attn_close(got, _oracle(orc, cfg, Ks, Vs, q, reqs, layer, seed))
 
 
+def test_int8_dither_dominated_parity(K, orc):
+    """Cases whose outputs the dither moves far beyond the tolerance, so that a read side regenerating
+    the wrong stream (K / V swapped, token index off by the block start, another head's tuple) fails by
+    orders of magnitude: row 0 has K = 0 (uniform softmax: o = mean of the dequantized values over one
+    quantized block and one fp16 token), row 1 large keys (a peaked softmax over two quantized blocks);
+    values x100 make the dither part s * xi about 0.4 per element."""
+    rng = np.random.default_rng(91)
+    Hq, Hkv, lens = 8, 2, [257, 600]
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
+    Ks = [[np.zeros((257, 128), np.float16) for _ in range(Hkv)],
+          [(rng.standard_normal((600, 128)) * 30).astype(np.float16) for _ in range(Hkv)]]
+    Vs = [[(rng.standard_normal((L, 128)) * 100).astype(np.float16) for _ in range(Hkv)] for L in lens]
+    q = rng.standard_normal((2, Hq, 128)).astype(np.float16)
+    reqs = np.array([1234567, 89])
+    layer, seed = 9, 0xFEDCBA9876543210
+    want = _oracle(orc, cfg, Ks, Vs, q, reqs, layer, seed)
+    got = _run(K, cfg, Ks, Vs, q, reqs, 600, layer, seed)
+    assert_attn_close(got, want)
+    # the same quantized cache read without its dither (x^ = s code) is far outside the tolerance
+    g = Hq // Hkv
+    parts = orc.int8_build_one(Ks[0][1], Vs[0][1], seed, int(reqs[0]), layer, 1)
+    vs = np.array([[orc.half_to_double(int(x)) for x in parts[3][0]]])
+    v_plain = np.concatenate([parts[1][:256].astype(np.float64) * vs, Vs[0][1][256:].astype(np.float64)])
+    assert np.max(np.abs(v_plain.mean(axis=0) - want[0, g])) > 0.02
+
+
 def test_int8_batch_order_invariance(K, orc):
     """Swapping batch rows together with their request ids swaps the outputs exactly."""
     rng = np.random.default_rng(77)

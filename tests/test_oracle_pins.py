@@ -513,6 +513,51 @@ def test_int8_quantized_attention_error_is_small(orc):
         assert np.max(np.abs(out[h] - textbook(q[h], K, V, 128 ** -0.5))) < 5e-3
 
 
+def _int8_block_xhat(orc, codes, scale, X, nq, seed, request, layer, kv_sel, kv_head, T=256):
+    """Dequantized tokens of one side of a block-INT8 cache, element by element: s (code - xi) with the
+    writer's five-tuple dither (request, layer, kv_sel, kv head, absolute token, channel) for the quantized
+    tokens, the fp16 token itself for the active block."""
+    out = X.astype(np.float64).copy()
+    for t in range(nq):
+        for c in range(128):
+            s = orc.half_to_double(int(scale[t // T, c]))
+            out[t, c] = s * (int(codes[t, c]) - orc.dither(seed, request, layer, kv_sel, kv_head, t, c))
+    return out
+
+
+def test_int8_decode_equals_attention_over_block_dequantized_tokens(orc):
+    """WitCert sec. 6.1 read side: the block-INT8 decode equals textbook attention over keys and values
+    dequantized element by element as s (code - xi), xi regenerated from the writer's tuple, over two
+    quantized 256-token blocks and an fp16 active block (L = 700: 512 quantized + 188 fp16)."""
+    rng = np.random.default_rng(51)
+    L, seed, request, layer, kv_head = 700, 0x0123456789AB, 77, 3, 5
+    K = (rng.standard_normal((L, 128)) * 3).astype(np.float16)
+    V = (rng.standard_normal((L, 128)) * 2).astype(np.float16)
+    q = rng.standard_normal((3, 128)).astype(np.float16)
+    kc, vc, ks, vs, kt, vt = orc.int8_build_one(K, V, seed, request, layer, kv_head)
+    nq = 512                                       # ((L - 1) mod 256) + 1 = 188 tokens stay fp16
+    out = orc.int8_decode_one(q, kc, vc, ks, vs, kt, vt, L=L, seed=seed, request=request, layer=layer,
+                              kv_head=kv_head)
+    khat = _int8_block_xhat(orc, kc, ks, K, nq, seed, request, layer, 0, kv_head)
+    vhat = _int8_block_xhat(orc, vc, vs, V, nq, seed, request, layer, 1, kv_head)
+    # the fp16 active block is read as is; the quantized tokens are not (the dither moves them)
+    assert np.array_equal(khat[nq:], K[nq:].astype(np.float64))
+    assert np.max(np.abs(khat[:nq] - K[:nq].astype(np.float64))) > 1e-3
+    for h in range(3):
+        assert np.allclose(out[h], textbook(q[h], khat, vhat, 128 ** -0.5), rtol=0, atol=1e-12)
+    # the pin has the power to see a wrong read-side stream: the K / V streams swapped, or the token index
+    # taken relative to its block, each move the textbook result far beyond 1e-12
+    k_swap = _int8_block_xhat(orc, kc, ks, K, nq, seed, request, layer, 1, kv_head)
+    v_swap = _int8_block_xhat(orc, vc, vs, V, nq, seed, request, layer, 0, kv_head)
+    assert np.max(np.abs(textbook(q[0], k_swap, v_swap, 128 ** -0.5) - out[0])) > 1e-6
+    v_rel = vhat.copy()
+    for t in range(256, nq):
+        for c in range(128):
+            s = orc.half_to_double(int(vs[1, c]))
+            v_rel[t, c] = s * (int(vc[t, c]) - orc.dither(seed, request, layer, 1, kv_head, t - 256, c))
+    assert np.max(np.abs(textbook(q[0], khat, v_rel, 128 ** -0.5) - out[0])) > 1e-6
+
+
 # --------------------------------------------------------------------------
 # token-granular INT8 over a slot pool (WitCert, SGLang storage subsection)
 # --------------------------------------------------------------------------

@@ -31,32 +31,51 @@ def test_noalloc_rejects_problems_beyond_its_scratch(K):
     assert st == K.KVQ_ERR_WORKSPACE
 
 
-@pytest.mark.gpu
-def test_noalloc_matches_workspace_call_twice(K):
+def _kivi_cache(K, rng, cfg, B, L, step):
     import torch
     from bit_kv_cache_keyquant_gb300 import cache as C
+    cache = C.KiviCache(cfg, B, L, device="cuda")
+    for b in range(B):
+        for h in range(cfg.n_kv_heads):
+            Lb = L - step * b
+            cache.fill(b, h, torch.from_numpy(rng.standard_normal((Lb, 128)).astype(np.float16)).cuda(),
+                       torch.from_numpy(rng.standard_normal((Lb, 128)).astype(np.float16)).cuda())
+    q = torch.from_numpy(rng.standard_normal((B, cfg.n_q_heads, 128)).astype(np.float16)).cuda()
+    return cache, q
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_call_twice(K):
+    """Two calls in a row give the workspace call's output.  Between them a call on another problem
+    (more rows, more splits, other lengths) fills the shared scratch with its own partial results, so
+    the second call shows that nothing a previous call left in the array is read."""
+    import torch
     rng = np.random.default_rng(41)
     cfg = K.make_config(n_q_heads=8, n_kv_heads=4)
     B, L = 3, 1500
-    cache = C.KiviCache(cfg, B, L, device="cuda")
-    for b in range(B):
-        for h in range(4):
-            Lb = L - 311 * b
-            cache.fill(b, h, torch.from_numpy(rng.standard_normal((Lb, 128)).astype(np.float16)).cuda(),
-                       torch.from_numpy(rng.standard_normal((Lb, 128)).astype(np.float16)).cuda())
-    q = torch.from_numpy(rng.standard_normal((B, 8, 128)).astype(np.float16)).cuda()
+    cache, q = _kivi_cache(K, rng, cfg, B, L, 311)
     _, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, B, L)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     ref = torch.empty((B, 8, 128), dtype=torch.float16, device="cuda")
     K.kv_decode_attn(cfg, cache.desc(), q, ref, ws, wsb)
+    other_cfg = K.make_config(n_q_heads=4, n_kv_heads=4)
+    other, other_q = _kivi_cache(K, rng, other_cfg, 5, 9000, 977)
+    n_a, _ = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, B, L)
+    n_b, _ = K.kv_decode_attn_plan(other_cfg, K.KVQ_VARIANT_KIVI, 5, 9000)
+    assert n_b > n_a
     outs = []
-    for _ in range(2):
+    for i in range(2):
         out = torch.full((B, 8, 128), float("nan"), dtype=torch.float16, device="cuda")
         K.kv_decode_attn_noalloc(cfg, cache.desc(), q, out)
         torch.cuda.synchronize()
         outs.append(out.float().cpu().numpy())
+        if i == 0:
+            junk = torch.empty((5, 4, 128), dtype=torch.float16, device="cuda")
+            K.kv_decode_attn_noalloc(other_cfg, other.desc(), other_q, junk)
+            torch.cuda.synchronize()
     assert K.kvq_get_device_error() == 0
     r = ref.float().cpu().numpy()
     for o in outs:
         assert np.isfinite(o).all()
         assert_attn_close(o, r)
+        assert np.array_equal(o, r)          # the same kernels on the same plan: identical bits
