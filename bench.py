@@ -1,9 +1,11 @@
 """Benchmark of the quantized-KV decode layer-step on GB300.
 
-Default workload (N=1): Llama-2-7B-shaped MHA decode layer, batch 32,
-32 query / 32 KV heads, head_dim 128, 4096 cached tokens, K2V2 (keys per
-channel over 32-token groups, values per token over 32-channel groups),
-fp16 residual R = 128.  One step = one layer-step of the whole hot path:
+Headline workload (N=1, the largest single-GPU configuration): Llama-3-8B-
+shaped grouped-query decode layer, batch 64, 32 query / 8 KV heads,
+head_dim 128, 32768 cached tokens, K2V2 (keys per channel over 32-token
+groups, values per token over 32-channel groups), fp16 residual R = 128,
+one seeded key channel per kv head x15.  One step = one layer-step of the
+whole hot path:
   a2  kv_quant_value  on the B*Hkv value tokens leaving the fp16 window,
   a1  kv_quant_key    on the amortized key flush (1/R of the (b, kv head)
                       pairs flush their R/G groups each step),
@@ -11,10 +13,14 @@ fp16 residual R = 128.  One step = one layer-step of the whole hot path:
   a4  decode merge    (LSE merge, fp16 out).
 `value` is microseconds per layer-step (whole job: time / (steps * N)),
 inputs resident in HBM, the K steps captured into a CUDA graph and timed
-over one replay; `e2e` is the same metric through the C ABI with the step's
-inputs copied from pinned host memory and the output copied back inside the
-timed region, the copies launched per step from the host and each step's
-kernels replayed as one CUDA graph.  `--impl reference` times the CPU oracle on a
+over one replay; the roofline's stage-1 time comes from the same kind of
+replay of a graph of K stage-1 launches.  `e2e` is the same metric through
+the C ABI with the step's inputs copied from pinned host memory and the
+output copied back inside the timed region, the copies launched per step
+from the host and each step's kernels replayed as one CUDA graph.  At N=1
+the other workloads (the MHA layer, the mixed-key layer in both boost
+selections, the INT8 dither layer, the tiny case) are measured the same way
+and reported under `configs`.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -72,8 +78,9 @@ def _workload_desc(w):
                        f"Gv=32), R=128" + (", paged: 128-token pages in a hashed order from a shared pool"
                                            if w.paged else ""))
     if w.variant == "kitty":
+        sel = "by variance over the page (score_mode 1)" if w.score_mode else "by the Eq. 2 sum of |x| (score_mode 0)"
         return base + (f"{w.seq_len} cached tokens, Kitty pages G=128, 16 of 128 key channels boosted to 4 bit "
-                       f"(two 2-bit planes), value 2 bit, sink 32, local 128")
+                       f"{sel} (two 2-bit planes), value 2 bit, sink 32, local 128")
     if w.variant == "int8t":
         return base + (f"lengths U[{w.min_seq_len}, {w.seq_len}], token-granular INT8 slot pool (scattered 16-slot "
                        f"pages), fp16 scale per token and 32 channels, Philox4x32-10 dither keyed by slot, "
@@ -133,12 +140,29 @@ class Clocks:
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
+_PAIRS = {}     # per process: (workload, batch row, kv head) -> the pair's quantized cache, built once
+
+
+def _pair(w, b, h):
+    """The oracle's cache of one (batch row, kv head) of workload w and the value token that leaves the fp16
+    window this step (built on first use, outside any timing)."""
+    from oracle import oracle as O
+    key = (w, b, h)
+    if key not in _PAIRS:
+        L = w.seq_len
+        K = I.gen_kv_np(w, I.T_K, b, h, L)
+        V = I.gen_kv_np(w, I.T_V, b, h, L)
+        _PAIRS[key] = (V[L - 129:L - 128].copy(), O.kivi_build_one(K, V, bits_k=w.bits_k, bits_v=w.bits_v))
+    return _PAIRS[key]
+
+
 def oracle_step_seconds(w, budget_s: float, min_pairs: int = 4, seed: int = 0):
     """Time the oracle's layer-step on a bounded sample of (b, kv head) pairs.
 
     Per pair: quantize the value token leaving the fp16 window, then split-free
     fp64 attention of the pair's query heads over the quantized cache and the
-    fp16 residual.  Returns (seconds per pair, pairs timed)."""
+    fp16 residual.  The sample is the seed's shuffle of the pairs; each pair's
+    cache is built once per process.  Returns (seconds per pair, pairs timed)."""
     from oracle import oracle as O
     O.build()
     g = w.n_q_heads // w.n_kv_heads
@@ -149,11 +173,9 @@ def oracle_step_seconds(w, budget_s: float, min_pairs: int = 4, seed: int = 0):
     rng.shuffle(pairs)
     spent, n = 0.0, 0
     for b, h in pairs:
-        K = I.gen_kv_np(w, I.T_K, b, h, L)
-        V = I.gen_kv_np(w, I.T_V, b, h, L)
-        parts = O.kivi_build_one(K, V, bits_k=w.bits_k, bits_v=w.bits_v)
+        vtok, parts = _pair(w, b, h)
         t0 = time.perf_counter()
-        O.kivi_quant_value(V[L - 129:L - 128], 32, w.bits_v)
+        O.kivi_quant_value(vtok, 32, w.bits_v)
         O.kivi_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L, bits_k=w.bits_k, bits_v=w.bits_v)
         spent += time.perf_counter() - t0
         n += 1
@@ -164,9 +186,8 @@ def oracle_step_seconds(w, budget_s: float, min_pairs: int = 4, seed: int = 0):
 
 def _oracle_worker(job):
     """One host process of the all-cores CPU leg (a spawned process: it never touches the GPU)."""
-    widx, batch, budget_s, min_pairs, seed = job
-    wk = dataclasses.replace(I.WORKLOADS[widx], batch=batch)
-    return oracle_step_seconds(wk, budget_s, min_pairs, seed)
+    w, budget_s, min_pairs, seed = job
+    return oracle_step_seconds(w, budget_s, min_pairs, seed)
 
 
 def oracle_pool(procs: int = 0):
@@ -179,12 +200,12 @@ def oracle_pool(procs: int = 0):
     return mp.get_context("spawn").Pool(procs), procs
 
 
-def oracle_step_seconds_all_cores(w, widx: int, budget_s: float, pool, procs: int, seed: int = 1):
+def oracle_step_seconds_all_cores(w, budget_s: float, pool, procs: int, seed: int = 1):
     """The oracle on every host core at once: `procs` processes, each timing its own shuffled sample of
     (b, kv head) pairs for about budget_s / procs seconds.  Returns (layer-step seconds at the aggregate
     throughput, pairs timed)."""
-    jobs = [(widx, w.batch, budget_s / procs, 2, seed + i) for i in range(procs)]
-    res = pool.map(_oracle_worker, jobs)
+    jobs = [(w, budget_s / procs, 2, seed + i) for i in range(procs)]
+    res = pool.map(_oracle_worker, jobs, chunksize=1)
     rate = sum(1.0 / per_pair for per_pair, _ in res)  # pairs per second, all processes together
     return w.batch * w.n_kv_heads / rate, sum(n for _, n in res)
 
@@ -194,12 +215,12 @@ def run_reference(args, w):
     each a bounded sample of the workload's (b, kv head) pairs at the processes' summed throughput."""
     pool, procs = oracle_pool()
     with pool:
+        # the warm-up steps build every process's sample pairs; the timed steps time the same samples
         for i in range(max(1, args.warmup)):
-            oracle_step_seconds_all_cores(w, args.workload, 0.0, pool, procs, seed=1000 * (i + 1))
+            oracle_step_seconds_all_cores(w, 0.0, pool, procs, seed=1)
         times, npairs = [], 0
         for i in range(args.steps):
-            step_s, n = oracle_step_seconds_all_cores(w, args.workload, 0.1 * procs, pool, procs,
-                                                      seed=100000 * (i + 1))
+            step_s, n = oracle_step_seconds_all_cores(w, 0.1 * procs, pool, procs, seed=1)
             times.append(step_s)
             npairs += n
     us = statistics.median(times) * 1e6
@@ -270,6 +291,8 @@ def build_state(w, device, appends: int = 1024):
             V = I.gen_kv_torch(w, I.T_V, b, h, L, device)
             if w.variant == "int8":
                 cache.fill(b, h, K, V, int(reqs[b]))
+            elif w.variant == "kitty":
+                cache.fill(b, h, K, V, score_mode=w.score_mode)
             else:
                 cache.fill(b, h, K, V)
     q = I.gen_q_torch(w, device)
@@ -323,7 +346,7 @@ def quant_step(st, stream, vnew=None, knew=None):
         kvq.kv_quant_value(cfg, vnew, st["n_vtok"], sc[0], sc[1], stream)
         kvq.kv_quant_key(cfg, knew, st["n_kgrp"], sc[2], sc[3], stream)
     elif w.variant == "kitty":
-        kvq.kv_quant_key_kitty(cfg, knew, st["n_pg"], 0, sc[0], stream)
+        kvq.kv_quant_key_kitty(cfg, knew, st["n_pg"], w.score_mode, sc[0], stream)
         kvq.kv_quant_value_kitty(cfg, vnew, st["n_pg"], sc[1], stream)
     elif w.variant == "int8t":
         kvq.kv_append_int8_token(cfg, st["desc"], st["pool"], knew, vnew, stream)
@@ -423,8 +446,9 @@ def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
         elif w.variant == "kitty":
             npg = total // (128 * 128 * 2)
             kp = torch.empty(npg * kvq.kvq_kitty_key_page_bytes(cfg), dtype=torch.uint8, device=dev)
-            us = timed(lambda: kvq.kv_quant_key_kitty(cfg, x, npg, 0, kp, stream))
+            us = timed(lambda: kvq.kv_quant_key_kitty(cfg, x, npg, w.score_mode, kp, stream))
             out["kv_quant_key_kitty"] = entry(us, npg, "128-token key pages", total + kp.numel())
+            out["kv_quant_key_kitty"]["score_mode"] = w.score_mode
             vp = torch.empty(npg * kvq.kvq_kitty_value_page_bytes(cfg), dtype=torch.uint8, device=dev)
             us = timed(lambda: kvq.kv_quant_value_kitty(cfg, x, npg, vp, stream))
             out["kv_quant_value_kitty"] = entry(us, npg, "128-token value pages", total + vp.numel())
@@ -461,19 +485,22 @@ def whole_job_us_per_step(job_ms: float, steps: int, world: int) -> float:
     return job_ms * 1e3 / (steps * world)
 
 
-def run_gpu(args, w, rank, world, local_rank):
+def measure(args, w, rank, world, local_rank, steps: int, want_quant: bool = True, want_cpu: bool = True):
+    """Time workload w on this rank: the step, its stage 1 and the write side, e2e through host buffers.
+    Returns the measurement (rank 0; None on the other ranks)."""
     import torch
     import torch.distributed as dist
     from bit_kv_cache_keyquant_gb300 import kvq
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    st = build_state(w, dev, appends=2 * args.warmup + 4 * args.steps + 16)
+    st = build_state(w, dev, appends=2 * args.warmup + 4 * steps + 16)
     stream = torch.cuda.current_stream(dev)
     st["side"] = torch.cuda.Stream(device=dev)
     st["fork"], st["join"] = torch.cuda.Event(), torch.cuda.Event()
 
-    # ---- kernel-only timing: inputs resident in HBM (458 MB/step > 129 MB L2) ----
+    # ---- kernel-only timing: inputs resident in HBM (every workload but the tiny one reads more than the
+    #      129 MB L2 per step) ----
     for _ in range(args.warmup):
         decode_step(st, stream)
     torch.cuda.synchronize()
@@ -481,39 +508,50 @@ def run_gpu(args, w, rank, world, local_rank):
     # them: the library's calls are stream-ordered, allocate nothing and never synchronize, so they
     # capture as they are (the merge's programmatic early launch becomes a programmatic graph edge).
     # One untimed replay uploads the graph; the timed replay runs exactly K steps with no host launch
-    # between them and no event between their kernels.
+    # between them and no event between their kernels.  A second graph holds K stage-1 launches alone:
+    # its replay, timed the same way, gives the stage-1 duration of the roofline.
     gs = torch.cuda.Stream(device=dev)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=gs):
-        for i in range(args.steps):
+        for i in range(steps):
             decode_step(st, gs)
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=gs):
+        for i in range(steps):
+            kvq.kv_decode_attn_stage1(st["cfg"], st["variant"], st["desc"], st["q"], st["ws"], st["wsb"], gs)
     with torch.cuda.stream(gs):
         graph.replay()
+        g1.replay()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     with Clocks(local_rank) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(gs)
+        ev[0].record(gs)
         with torch.cuda.stream(gs):
             graph.replay()
-        t_end.record(gs)
+        ev[1].record(gs)
         torch.cuda.synchronize()
-        # a second pass of K steps, launched one by one with events around every kernel: the
-        # per-kernel breakdown and the stage-1 duration of the roofline
-        for i in range(args.steps):
+        ev[2].record(gs)
+        with torch.cuda.stream(gs):
+            g1.replay()
+        ev[3].record(gs)
+        torch.cuda.synchronize()
+        # a third pass of K steps, launched one by one with events around every kernel: the per-kernel
+        # breakdown (the write side's span and the merge)
+        for i in range(steps):
             decode_step(st, stream, evs[i])
         torch.cuda.synchronize()
-    total_ms = t_start.elapsed_time(t_end)
-    stage1_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = ev[0].elapsed_time(ev[1])
+    s1 = ev[2].elapsed_time(ev[3]) / steps
+    stage1_evt_ms = [e[2].elapsed_time(e[3]) for e in evs]
     quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
     merge_ms = [e[3].elapsed_time(e[4]) for e in evs]
     assert kvq.kvq_get_device_error() == 0
     total_ms = job_time_ms(total_ms, world, dev)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / steps
 
     # ---- end to end through the C ABI with host buffers: every step copies its inputs from pinned host
     #      memory and reads its output back; a serving loop overlaps these copies with the neighbouring
@@ -571,25 +609,24 @@ def run_gpu(args, w, rank, world, local_rank):
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(h2d_s)
-    for i in range(args.steps):
+    for i in range(steps):
         e2e_step(i)
-    stream.wait_event(out_free[(args.steps - 1) % 2])
+    stream.wait_event(out_free[(steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = job_time_ms(e0.elapsed_time(e1), world, dev)
     h2d = qh.numel() * 2 + vh.numel() * 2 + kh.numel() * 2
     d2h = outh[0].numel() * 2
 
-    quant = quant_kernels_bench(w, st["cfg"], dev, stream) if rank == 0 else None
+    quant = quant_kernels_bench(w, st["cfg"], dev, stream) if (rank == 0 and want_quant) else None
     if rank != 0:
-        return
+        return None
     lens = st["lens"]
     if w.variant == "int8t":       # one token appended per request before every attention
-        lens = lens + args.warmup + 2 * args.steps + (args.steps + 1) // 2   # mid-point of the per-kernel pass
+        lens = lens + args.warmup + steps                                  # at the stage-1 graph's replay
     cache_bytes = st["cache"].nbytes_read(lens)
     q_bytes = w.batch * w.n_q_heads * 128 * 2
     alg_bytes_stage1 = cache_bytes + q_bytes
-    s1 = statistics.mean(stage1_ms)
     achieved = alg_bytes_stage1 / (s1 * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     prof = os.path.join(ROOT, "profiles", "traffic.json")
@@ -599,9 +636,10 @@ def run_gpu(args, w, rank, world, local_rank):
         tr = json.load(open(prof)).get(f"{kname}@workload{w.index}")
         if tr and tr.get("source_hash") == kernel_source_hash(kfiles):
             traffic = tr["bytes_per_launch"]
+    timing = f"a CUDA graph of {steps} stage-1 launches, one timed replay (CUDA events on its stream)"
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic, "peak_kind": peak_kind, "kernel": kname + " (stage 1)",
-            "alg_bytes_per_launch": alg_bytes_stage1}
+            "alg_bytes_per_launch": alg_bytes_stage1, "stage1_us": 1e3 * s1, "stage1_timing": timing}
     if w.variant in ("int8", "int8t"):
         nb = philox_blocks(w, lens)
         ach = nb / (s1 * 1e-3) / 1e9
@@ -609,13 +647,14 @@ def run_gpu(args, w, rank, world, local_rank):
                 "frac": ach / PHILOX_PEAK_GBLOCKS, "traffic": traffic,
                 "peak_kind": "measured (pure Philox4x32-10 probe kernel on this GPU)",
                 "kernel": kname + " (stage 1)", "alg_philox_blocks_per_launch": nb,
-                "alg_bytes_per_launch": alg_bytes_stage1, "hbm_gbs": achieved, "hbm_frac": achieved / peak}
+                "alg_bytes_per_launch": alg_bytes_stage1, "hbm_gbs": achieved, "hbm_frac": achieved / peak,
+                "stage1_us": 1e3 * s1, "stage1_timing": timing}
     cpu = None
-    if world == 1 and not args.no_cpu and w.variant == "kivi":
+    if world == 1 and want_cpu and not args.no_cpu and w.variant == "kivi":
         # the oracle on every host core (the reference arm's form), and on one thread
         pool, procs = oracle_pool()
         with pool:
-            step_s, n_all = oracle_step_seconds_all_cores(w, args.workload, args.cpu_budget, pool, procs)
+            step_s, n_all = oracle_step_seconds_all_cores(w, args.cpu_budget, pool, procs)
         per_pair, n = oracle_step_seconds(w, args.cpu_budget / 2)
         cpu = {"value": step_s * 1e6, "unit": UNIT, "cores": procs, "kind": "oracle",
                "sample": f"{n_all} (batch row, kv head) pairs of the workload over {procs} spawned processes "
@@ -623,33 +662,70 @@ def run_gpu(args, w, rank, world, local_rank):
                          f"pairs) at their summed throughput",
                "single_thread": {"value": per_pair * w.batch * w.n_kv_heads * 1e6, "unit": UNIT, "cores": 1,
                                  "sample": f"{n} pairs, one thread, scaled by {w.batch * w.n_kv_heads} pairs"}}
-    value = whole_job_us_per_step(total_ms, args.steps, world)
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "data": "synthetic",
+    out = {
+        "value": whole_job_us_per_step(total_ms, steps, world), "unit": UNIT, "ms_per_step": ms_per_step,
+        "steps": steps,
         "dtype": DTYPE["kivi4" if w.variant == "kivi" and w.bits_k == 4 else w.variant],
         "config": {"workload": _workload_desc(w), "batch": w.batch, "q_heads": w.n_q_heads,
                    "kv_heads": w.n_kv_heads, "head_dim": 128, "seq_len": w.seq_len, "parallelism": f"replicas x{world}",
                    "splits": st["n_splits"],
-                   "l2": f"inputs larger than L2 ({cache_bytes / 1e6:.0f} MB read per step vs 129 MB L2)",
+                   "l2": (f"inputs larger than L2 ({cache_bytes / 1e6:.0f} MB read per step vs 129 MB L2)"
+                          if cache_bytes > 129e6 else
+                          f"L2-resident ({cache_bytes / 1e6:.2f} MB read per step): launch-latency bound"),
                    "timed": "K steps captured once into a CUDA graph; one untimed replay, then one timed replay"},
         "breakdown_us": {("append_before_attention" if w.variant == "int8t" else "quant_writes_side_stream_span"):
                          1e3 * statistics.mean(quant_ms), "decode_stage1": 1e3 * s1,
+                         "decode_stage1_launched_one_by_one": 1e3 * statistics.mean(stage1_evt_ms),
                          "merge": 1e3 * statistics.mean(merge_ms),
-                         "timing": "a second pass of the K steps with CUDA events around every kernel"},
+                         "timing": "stage 1 from the stage-1 graph; the write side, the merge and the "
+                                   "one-by-one stage 1 from a pass of the K steps with events around every kernel"},
         "hbm_gbs_step": (alg_bytes_stage1 + d2h) / (ms_per_step * 1e-3) / 1e9,
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": whole_job_us_per_step(e2e_ms, args.steps, world), "unit": UNIT,
+        "e2e": {"value": whole_job_us_per_step(e2e_ms, steps, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "every step's inputs from pinned host memory and its output back, on two copy streams "
                           "overlapping the neighbouring steps (two device buffer sets), launched per step from "
                           "the host; each step's kernels one CUDA graph replay"},
         "quant_kernels": quant,
-        "gpu_launches": launches_per_step(w) * args.steps,
+        "gpu_launches": launches_per_step(w) * steps,
         "clocks": clk.summary(),
     }
+    del st, graph, g1, step_graphs, bufs
+    torch.cuda.empty_cache()
+    return out
+
+
+# The other workloads measured beside the headline at N=1: (key, workload index, field overrides)
+EXTRA_CONFIGS = (
+    ("2", 2, {}),
+    ("4", 4, {}),
+    ("4_variance", 4, {"score_mode": 1}),
+    ("5", 5, {}),
+    ("1", 1, {}),
+)
+
+
+def run_gpu(args, w, rank, world, local_rank):
+    head = measure(args, w, rank, world, local_rank, args.steps)
+    extras = None
+    if world == 1 and not args.only and args.batch == 0:
+        extras = {}
+        for key, idx, over in EXTRA_CONFIGS:
+            if idx == args.workload and not over:
+                continue
+            wk = dataclasses.replace(I.WORKLOADS[idx], **over)
+            m = measure(args, wk, rank, world, local_rank, min(args.steps, 20), want_quant=True, want_cpu=False)
+            m.pop("cpu_baseline", None)
+            extras[key] = m
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": head.pop("value"), "unit": head.pop("unit"), "n_gpus": world,
+            "steps": head.pop("steps"), "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
+    line.update(head)
+    if extras is not None:
+        line["configs"] = extras
     print(json.dumps(line))
 
 
@@ -686,8 +762,14 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
-                    help="2 (default, the headline line); 1, 3, 4, 5 are the other synthetic workloads")
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
+                    help="3 (default: the headline line, the largest single-GPU workload); 1, 2, 4, 5 are the "
+                         "other synthetic workloads, 6-9 the variants (token-granular INT8, KIVI-4, paged KIVI, "
+                         "KIVI-4 grouped-query)")
+    ap.add_argument("--score-mode", type=int, default=0, choices=[0, 1],
+                    help="Kitty boost selection of workload 4: 0 = Eq. 2 sum of |x|, 1 = variance")
+    ap.add_argument("--only", action="store_true",
+                    help="measure the chosen workload alone (no `configs` entries for the other workloads)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
@@ -695,9 +777,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = I.WORKLOADS[args.workload]
+    w = dataclasses.replace(I.WORKLOADS[args.workload], score_mode=args.score_mode)
     if args.batch > 0:
-        import dataclasses
         w = dataclasses.replace(w, batch=args.batch)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

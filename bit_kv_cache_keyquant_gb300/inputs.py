@@ -61,6 +61,7 @@ class Workload:
     bits_k: int = 2              # KIVI code widths
     bits_v: int = 2
     paged: bool = False          # KIVI: pages of 128 tokens from a shared pool through a page table
+    score_mode: int = 0          # Kitty boost selection: 0 = Eq. 2 sum of |x|, 1 = variance over the page
 
     @property
     def seed(self) -> int:
@@ -87,15 +88,16 @@ WORKLOADS = {
 
 
 # ----------------------------------------------------------------------------
-# counter-based hash (numpy, uint64 lanes holding 32-bit values)
+# counter-based hash (numpy: uint32 lanes, wrapping products)
 # ----------------------------------------------------------------------------
 def _fmix32_np(h):
-    h = h & MASK32
-    h ^= h >> np.uint64(16)
-    h = (h * np.uint64(_C1)) & np.uint64(MASK32)
-    h ^= h >> np.uint64(13)
-    h = (h * np.uint64(_C2)) & np.uint64(MASK32)
-    h ^= h >> np.uint64(16)
+    """murmur3 finaliser on uint32 arrays (products wrap modulo 2**32)."""
+    h = h.astype(np.uint32, copy=True)
+    h ^= h >> np.uint32(16)
+    h *= np.uint32(_C1)
+    h ^= h >> np.uint32(13)
+    h *= np.uint32(_C2)
+    h ^= h >> np.uint32(16)
     return h
 
 
@@ -119,10 +121,10 @@ def stream_key(seed: int, tensor: int, b: int, h: int) -> int:
 
 
 def hash_np(key: int, index: np.ndarray) -> np.ndarray:
-    """32-bit hash of (key, index) for a uint64 index array (index < 2**32)."""
-    idx = index.astype(np.uint64)
-    h = (idx * np.uint64(_GOLD) + np.uint64(key)) & np.uint64(MASK32)
-    return _fmix32_np(h)
+    """32-bit hash of (key, index) for an index array (index < 2**32), as uint64 values."""
+    idx = np.asarray(index).astype(np.uint32)
+    h = idx * np.uint32(_GOLD) + np.uint32(key)
+    return _fmix32_np(h).astype(np.uint64)
 
 
 def irwin_hall_np(hv: np.ndarray) -> np.ndarray:
