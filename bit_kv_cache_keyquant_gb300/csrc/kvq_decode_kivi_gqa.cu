@@ -14,12 +14,16 @@
 //             and lo = fl(qlo s + (qhi s - hi)); the bracket is the exact
 //             rounding error of hi (one fp16 FMA), so hi + lo carries W to
 //             about 2^-21 relative, and sigma_h keeps every part in range.
-//   logit_ht = (S[t, 2h] + S[t, 2h+1]) 2^(9|7 - sigma_h) + alpha sum_c q_hc z_c
+//   logit_ht = (S[t, 2h] + S[t, 2h+1]) 2^(9|7 - sigma_h) + alpha sum_c q_hc z_c,
+//   the zero-point term as one more product per k-step: A = the group's z_c
+//   (fp16, exact) in every row, B = the hi / lo parts of alpha q_hc 2^sigma_h.
 // Values:
 //   O[c, n]  = sum_t A[c, t] B[t, n]
 //   A[c, t] = code_tc * 2^-9 or 2^-7 (same unpacking, channel rows);
 //   B[t, n] = hi / lo parts of p_ht s_tg (p kept as fp16 hi + lo);
-//   o_hc     = (O[c, 2h] + O[c, 2h+1]) 2^(9|7) + sum_t p_ht z_tg.
+//   o_hc     = (O[c, 2h] + O[c, 2h+1]) 2^(9|7) + sum_t p_ht z_tg,
+//   the zero-point term again on the tensor cores: A row g = z_tg (rows
+//   repeat the D/Gv groups), B = the hi / lo parts of p_ht.
 // Products on the tensor cores are exact (fp16 x fp16) and accumulate in
 // fp32; A operands are normal fp16 numbers (subnormal A operands lose bits).
 //
@@ -46,8 +50,9 @@ struct SmemG {
     uint64_t full[NST];
     uint64_t empty[NST];
     uint32_t qhi[GMAX][64];               // fp16x2 hi parts of alpha q 2^sigma: [head][k/2][r][4]
+    uint32_t qpad[16];                    // puts qlo's chunks on the other half of the banks
     uint32_t qlo[GMAX][64];               // fp16x2 lo parts, same order
-    float qz[GMAX][KVQ_D];                // alpha q (fp32): [head][k][r][4]
+    float qz[GMAX][KVQ_D];                // alpha q (fp32): [head][k][r][4] (4-bit widths' zero-point dots)
     float unsig[GMAX];                    // 2^-sigma_h
     float pbuf[NCWARP][GMAX * PB_ROW];
     float st_acc[NCWARP][GMAX][ACC_ROW];
@@ -62,6 +67,9 @@ template <int NGV, int BK, int BV, int NST>
 __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(Params P) {
     using GG = Geo<BK, BV>;
     constexpr int GQ_NSTAGE = NST;
+    // zero-point terms as tensor-core products (2-bit widths) or as CUDA-core dots (4-bit widths: the
+    // products' extra registers cost the 4-bit variants more in spills than they save)
+    constexpr bool ZMMA = BK == 2 && BV == 2;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SmemG<BK, BV, NST> &S = *reinterpret_cast<SmemG<BK, BV, NST> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,6 +103,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     const uint32_t vsel4 = (uint32_t)((q >> 1) | ((4 + (q >> 1)) << 4));
     const uint32_t vshift4 = (q & 1) ? 4u : 0u;
     const float vscale = BV == 4 ? 512.f : ((q & 1) ? 128.f : 512.f);
+    const uint32_t *qown = xB ? S.qlo[hB] : S.qhi[hB];   // the part of B column n = q (zero-point products)
+    const int jz = q % NGV;                               // value group of rows q, q + 8 of the zero-point product
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                 make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
             *reinterpret_cast<uint2 *>(&S.qlo[h][pw]) =
                 make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
-            *reinterpret_cast<float4 *>(&S.qz[h][tk * 16 + tr * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+            if (!ZMMA) *reinterpret_cast<float4 *>(&S.qz[h][tk * 16 + tr * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
             if (lane == 0) S.unsig[h] = __int_as_float((127 - sigma) << 23);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
@@ -155,10 +165,11 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
             }
         } else {
             float m_run = -INFINITY, l_part = 0.f;        // head r
-            float vz[NGV];
-            float vacc[8][4];
+            float vzacc[4] = {0.f, 0.f, 0.f, 0.f};        // sum_t p z_t,jz of head r (hi, lo; rows q, q + 8)
+            float vzc[NGV];                               // the CUDA-core form: sum_t p z_t,j of head r
 #pragma unroll
-            for (int i = 0; i < NGV; ++i) vz[i] = 0.f;
+            for (int i = 0; i < NGV; ++i) vzc[i] = 0.f;
+            float vacc[8][4];
 #pragma unroll
             for (int i = 0; i < 8; ++i) vacc[i][0] = vacc[i][1] = vacc[i][2] = vacc[i][3] = 0.f;
             const float unsig = S.unsig[r];
@@ -169,29 +180,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];
                     const uint16_t *ksz = reinterpret_cast<const uint16_t *>(st + GG::KC) + gl * 2 * KVQ_D;
-                    // ---- alpha sum_c q_hc z_c: the lanes of head hB split the lane's 32 channels by xB ----
-                    float zr;
-                    {
-                        float zp = 0.f;
-#pragma unroll
-                        for (int n = 0; n < 4; ++n) {
-                            const int k = xB ? 7 - n : n;            // order keeps the two halves on distinct banks
-                            const uint2 zz = *reinterpret_cast<const uint2 *>(ksz + KVQ_D + ((k >> 1) * 4 + r) * 8 +
-                                                                             (k & 1) * 4);
-                            const float4 qa = *reinterpret_cast<const float4 *>(&S.qz[hB][k * 16 + 4 * r]);
-                            zp = fmaf(qa.x, h2f(lo16(zz.x)), zp);
-                            zp = fmaf(qa.y, h2f(hi16(zz.x)), zp);
-                            zp = fmaf(qa.z, h2f(lo16(zz.y)), zp);
-                            zp = fmaf(qa.w, h2f(hi16(zz.y)), zp);
-                        }
-                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
-                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
-                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
-                        zr = __shfl_sync(0xFFFFFFFFu, zp, 8 * r);   // head r lives in lanes 8r..8r+7
-                    }
                     // ---- key codes x B on the tensor cores: tokens q + 8p, p = 0..3; B fragments (head hB,
                     //      hi or lo) of channels 16k + 2r + {0,1 | 8,9} made two k-steps at a time ----
                     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                    float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
                     {
                         // BK = 4: plane 0 holds tokens p = 0, 1, plane 1 tokens p = 2, 3, a nibble each
                         const uint8_t *kt = st + warp * 512 * BK;
@@ -210,6 +202,25 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                             const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
                             const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
                             const uint4 sv = *reinterpret_cast<const uint4 *>(ksz + (4 * i + r) * 8);
+                            const uint4 zv = *reinterpret_cast<const uint4 *>(ksz + KVQ_D + (4 * i + r) * 8);
+                            const uint4 qo = *reinterpret_cast<const uint4 *>(qown + 16 * i + 4 * r);
+                            if (!ZMMA) {
+                                // CUDA-core form: lane (q, r) adds its head hB's products over the lane's
+                                // channels of k-steps 2i, 2i+1 (hi lanes the first, lo lanes the second)
+                                const int k = 2 * i + (xB ? 1 : 0);
+                                const uint2 zz = make_uint2(xB ? zv.z : zv.x, xB ? zv.w : zv.y);
+                                const float4 qa = *reinterpret_cast<const float4 *>(&S.qz[hB][k * 16 + 4 * r]);
+                                z0[0] = fmaf(qa.x, h2f(lo16(zz.x)), z0[0]);
+                                z0[0] = fmaf(qa.y, h2f(hi16(zz.x)), z0[0]);
+                                z0[0] = fmaf(qa.z, h2f(lo16(zz.y)), z0[0]);
+                                z0[0] = fmaf(qa.w, h2f(hi16(zz.y)), z0[0]);
+                            } else if (i & 1) {
+                                mma16816(z1, zv.x, zv.x, zv.y, zv.y, qo.x, qo.y);
+                                mma16816(z1, zv.z, zv.z, zv.w, zv.w, qo.z, qo.w);
+                            } else {
+                                mma16816(z0, zv.x, zv.x, zv.y, zv.y, qo.x, qo.y);
+                                mma16816(z0, zv.z, zv.z, zv.w, zv.w, qo.z, qo.w);
+                            }
                             const uint32_t bk[4] = {split_prod(a.x, l.x, sv.x, xB), split_prod(a.y, l.y, sv.y, xB),
                                                     split_prod(a.z, l.z, sv.z, xB), split_prod(a.w, l.w, sv.w, xB)};
 #pragma unroll
@@ -236,6 +247,17 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     }
                     // ---- logits of head r, tokens q, q+8, q+16, q+24; online softmax ----
                     const float f9 = unsig * 512.f, f7 = BK == 4 ? f9 : unsig * 128.f;
+                    float zr;
+                    if (ZMMA) {
+                        zr = ((z0[0] + z1[0]) + (z0[1] + z1[1])) * unsig;
+                    } else {
+                        // the 8 lanes of head hB hold its partial dots; head r's sum sits in lane 8r
+                        float zp = z0[0];
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
+                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
+                        zr = __shfl_sync(0xFFFFFFFFu, zp, 8 * r);
+                    }
                     float lg[4];
                     lg[0] = fmaf(s0[0] + s0[1], f9, zr);
                     lg[1] = fmaf(s0[2] + s0[3], f7, zr);
@@ -246,20 +268,19 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
                     if (mt > m_run) {
-                        const float sc = exp2f(m_run - mt);
+                        const float sc = ex2_ftz(m_run - mt);
                         l_part *= sc;
+                        scale4(vzacc, sc);
 #pragma unroll
-                        for (int i = 0; i < NGV; ++i) vz[i] *= sc;
+                        for (int i = 0; i < NGV; ++i) vzc[i] *= sc;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            vacc[i][0] *= sc; vacc[i][1] *= sc; vacc[i][2] *= sc; vacc[i][3] *= sc;
-                        }
+                        for (int i = 0; i < 8; ++i) scale4(vacc[i], sc);
                         m_run = mt;
                     }
                     float pr[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        pr[i] = exp2f(lg[i] - m_run);
+                        pr[i] = ex2_ftz(lg[i] - m_run);
                         l_part += pr[i];
                     }
                     // token 16k + 8hk + 4e + j (k-step k, m-row pair index 2j + e + 8hk) at
@@ -267,15 +288,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     float *pb = S.pbuf[warp];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pb[r * PB_ROW + 8 * i + 2 * (q & 3) + (q >> 2)] = pr[i];
-                    // ---- value zero-point term of head r over the lane's four tokens ----
                     const uint32_t *vsz = reinterpret_cast<const uint32_t *>(st + GG::KC + GG::KSZ + GG::VC) +
                                           warp * 32 * NGV;
+                    if (!ZMMA) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t row[NGV];
-                        load_row<NGV>(vsz + (q + 8 * i) * NGV, row);
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t row[NGV];
+                            load_row<NGV>(vsz + (q + 8 * i) * NGV, row);
 #pragma unroll
-                        for (int j = 0; j < NGV; ++j) vz[j] = fmaf(pr[i], h2f(hi16(row[j])), vz[j]);
+                            for (int j = 0; j < NGV; ++j) vzc[j] = fmaf(pr[i], h2f(hi16(row[j])), vzc[j]);
+                        }
                     }
                     __syncwarp();
                     // ---- values: two 16-token k-steps x eight 16-channel m-tiles; k-column 2j + e + 8hk of
@@ -289,6 +311,13 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                         const float2 pc = *reinterpret_cast<const float2 *>(&pb[hB * PB_ROW + 16 * ks + 8 + 2 * r]);
                         const uint32_t pha = split_pair(pa.x, pa.y, false), pla = split_pair(pa.x, pa.y, true);
                         const uint32_t phc = split_pair(pc.x, pc.y, false), plc = split_pair(pc.x, pc.y, true);
+                        if (ZMMA) {
+                            // value zero-point product: A rows hold z of group jz for the k-step's tokens (the
+                            // high halves of the (s, z) words), B the lane's part of p
+                            const uint32_t za = prmt(vsz[t0 * NGV + jz], vsz[(t0 + 4) * NGV + jz], 0x7632u);
+                            const uint32_t zc = prmt(vsz[(t0 + 8) * NGV + jz], vsz[(t0 + 12) * NGV + jz], 0x7632u);
+                            mma16816(vzacc, za, za, zc, zc, xB ? pla : pha, xB ? plc : phc);
+                        }
                         uint32_t bv0[NGV], bv1[NGV];
                         {
                             uint32_t ra[NGV], rb[NGV], rc[NGV], rd[NGV];
@@ -357,11 +386,20 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 4);
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
+            float vz[NGV];
+            if (ZMMA) {
+                // group j's zero-point sum of head r sits in the lanes with q % NGV == j
+                const float vzs = vzacc[0] + vzacc[1];
 #pragma unroll
-            for (int j = 0; j < NGV; ++j) {
-                vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 4);
-                vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 8);
-                vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 16);
+                for (int j = 0; j < NGV; ++j) vz[j] = __shfl_sync(0xFFFFFFFFu, vzs, 4 * j + r);
+            } else {
+#pragma unroll
+                for (int j = 0; j < NGV; ++j) {
+                    vz[j] = vzc[j];
+                    vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 4);
+                    vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 8);
+                    vz[j] += __shfl_xor_sync(0xFFFFFFFFu, vz[j], 16);
+                }
             }
             float *acc = S.st_acc[warp][r];
 #pragma unroll

@@ -62,6 +62,21 @@ __device__ __forceinline__ uint32_t split_pair(float v0, float v1, bool x) {
     return lo;
 }
 
+// 2^x, approximate, with results below 2^-126 flushed to zero (softmax weights that small add nothing)
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// four accumulators times sc, as two packed fp32 multiplies
+__device__ __forceinline__ void scale4(float d[4], float sc) {
+    const unsigned long long s2 = pack2f(sc, sc);
+    unsigned long long a = pack2f(d[0], d[1]), b = pack2f(d[2], d[3]);
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(s2));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(b) : "l"(s2));
+    d[0] = lo2f(a); d[1] = hi2f(a); d[2] = lo2f(b); d[3] = hi2f(b);
+}
+
 template <int N>
 __device__ __forceinline__ void load_row(const uint32_t *p, uint32_t (&v)[N]) {
     if constexpr (N == 4) {
