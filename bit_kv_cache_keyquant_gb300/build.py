@@ -48,12 +48,25 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    return _build_into(BUILD, LIB, [], verbose, ptxas_info)
+
+
+def build_test_lib(out_dir: str) -> str:
+    """A separate copy of the library for the tests of the failure paths only: built with
+    KVQ_FAULT_INJECT, which adds the kvq_test_inject_wait hook (a KIVI decode stage left unfilled,
+    shortened wait limits).  The product library (build()) never defines it."""
+    os.makedirs(out_dir, exist_ok=True)
+    return _build_into(os.path.join(out_dir, "obj"), os.path.join(out_dir, "libkvq_test.so"),
+                       ["-DKVQ_FAULT_INJECT"], False, False)
+
+
+def _build_into(obj_dir: str, lib: str, defines, verbose: bool, ptxas_info: bool) -> str:
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + list(defines)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, err in results:
             if err:
                 print(err)
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -628,6 +628,18 @@ extern "C" kvq_status kvq_philox4x32_10(const uint32_t *ctr, const uint32_t *key
     return cuda_status(launch_philox(ctr, key, n, out, stream));
 }
 
+#ifdef KVQ_FAULT_INJECT
+namespace kvq {
+TestInject g_test_inject;
+}
+// Test builds only: arm (skip_stage >= 0) or disarm (-1) the KIVI decode
+// wait injection; spin_limit 0 restores the product limit.
+extern "C" KVQ_API void kvq_test_inject_wait(int skip_stage, unsigned spin_limit) {
+    kvq::g_test_inject.skip_stage = skip_stage;
+    kvq::g_test_inject.spin_limit = spin_limit;
+}
+#endif
+
 extern "C" kvq_status kvq_get_device_error(uint32_t *flags) {
     if (!flags) return KVQ_ERR_INVALID_ARG;
     unsigned v = 0, zero = 0;

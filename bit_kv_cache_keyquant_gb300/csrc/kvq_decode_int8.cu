@@ -49,7 +49,10 @@ struct Smem {
     };
     float st_m[NCWARP][GMAX];
     float st_l[NCWARP][GMAX];
+    int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
+                                          // members before it keep their 16-byte alignment)
 };
+static_assert(offsetof(Smem, pw) % 16 == 0 && offsetof(Smem, st_acc) % 16 == 0, "16-byte aligned tables");
 
 struct Params {
     const int32_t *seq_len;
@@ -319,6 +322,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], NCWARP);
         }
+        S.abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -327,17 +331,22 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
         if (lane == 0) {
             bool ok = true;
             int sg = 0;
+            int armed[NSTAGE];
+#pragma unroll
+            for (int j = 0; j < NSTAGE; ++j) armed[j] = 0;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit U = unit_of(P, u);
                 const int nst = U.residual ? 0 : (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
                 for (int s = 0; s < nst; ++s, ++sg) {
                     const int slot = sg % NSTAGE;
                     if (sg >= NSTAGE) ok = mbar_wait(&S.empty[slot], ((sg / NSTAGE) - 1) & 1, P.err);
+                    ok = ok && !ring_aborted(&S.abort_flag);
                     if (!ok) break;
                     const int tok = U.t0 + s * STAGE_TOK;
                     const int nt = min(STAGE_TOK, U.t1 - tok);
                     const int blk = tok / P.T;
                     uint8_t *st = S.stage[slot];
+                    ++armed[slot];
                     mbar_expect_tx(&S.full[slot], (uint32_t)(2 * nt * KVQ_D + 4 * KVQ_D));
                     bulk_g2s(st, P.k_codes + (U.bk * P.cap + tok) * KVQ_D, nt * KVQ_D, &S.full[slot]);
                     bulk_g2s(st + CODES_BYTES, P.v_codes + (U.bk * P.cap + tok) * KVQ_D, nt * KVQ_D, &S.full[slot]);
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                              &S.full[slot]);
                 }
             }
-            for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
+            producer_drain<NSTAGE>(S.full, armed, P.err);
         }
         return;
     }
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
             const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
             for (int s = 0; s < nst; ++s, ++sg) {
                 const int slot = sg % NSTAGE;
-                ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
+                ok = consumer_stage_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err, KVQ_SPIN_LIMIT, ok, &S.abort_flag);
                 const int tok = U.t0 + s * STAGE_TOK;
                 const int r0 = tok + 32 * warp;
                 const int n = min(32, U.t1 - r0);
@@ -495,7 +504,10 @@ struct SmemT {
     };
     float st_m[NCWARP][GMAX];
     float st_l[NCWARP][GMAX];
+    int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
+                                          // members before it keep their 16-byte alignment)
 };
+static_assert(offsetof(SmemT, pw) % 16 == 0 && offsetof(SmemT, st_acc) % 16 == 0, "16-byte aligned tables");
 
 struct ParamsT {
     const int32_t *seq_len, *table;
@@ -547,6 +559,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
             mbar_init(&S.full[i], 32);
             mbar_init(&S.empty[i], NCWARP);
         }
+        S.abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -554,6 +567,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
     if (warp == NCWARP) {
         bool ok = true;
         int sg = 0;
+        int armed[NSTAGE];
+#pragma unroll
+        for (int j = 0; j < NSTAGE; ++j) armed[j] = 0;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const UnitT U = unit_of_t(P, u);
             const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
@@ -561,8 +577,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
             for (int s = 0; s < nst; ++s, ++sg) {
                 const int buf = sg % NSTAGE;
                 if (sg >= NSTAGE) ok = mbar_wait(&S.empty[buf], ((sg / NSTAGE) - 1) & 1, P.err);
-                ok = __all_sync(0xFFFFFFFFu, ok);
+                ok = __all_sync(0xFFFFFFFFu, ok && !ring_aborted(&S.abort_flag));
                 if (!ok) break;
+                ++armed[buf];
                 const int tok = U.t0 + s * STAGE_TOK;
                 const int nt = min(STAGE_TOK, U.t1 - tok);
                 int64_t rec[4];
@@ -598,7 +615,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
             }
         }
         // no copy may be in flight when the CTA exits
-        for (int s = max(0, sg - NSTAGE); s < sg; ++s) mbar_wait(&S.full[s % NSTAGE], (s / NSTAGE) & 1, P.err);
+        producer_drain<NSTAGE>(S.full, armed, P.err);
         return;
     }
 
@@ -616,7 +633,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
         const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
         for (int s = 0; s < nst; ++s, ++sg) {
             const int buf = sg % NSTAGE;
-            ok = ok && mbar_wait(&S.full[buf], (sg / NSTAGE) & 1, P.err);
+            ok = consumer_stage_wait(&S.full[buf], (sg / NSTAGE) & 1, P.err, KVQ_SPIN_LIMIT, ok, &S.abort_flag);
             const int r0 = U.t0 + s * STAGE_TOK + 32 * warp;
             const int n = min(32, U.t1 - r0);
             if (ok && n > 0) {

@@ -42,7 +42,10 @@ struct Smem {
     float st_acc[NCWARP][KVQ_D];
     float st_m[NCWARP];
     float st_l[NCWARP];
+    int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
+                                          // members before it keep their 16-byte alignment)
 };
+static_assert(offsetof(Smem, qk) % 16 == 0 && offsetof(Smem, st_acc) % 16 == 0, "16-byte aligned tables");
 
 __device__ __forceinline__ float softmax_tile(float logit, float &m_run, float &l_part, float &vbias,
                                               unsigned long long vacc2[16]) {
@@ -73,12 +76,13 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Para
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], NCWARP);
         }
+        S.abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kitty_produce<NSTAGE>(P, P.Hq, S.stage, S.full, S.empty);
+        if (lane == 0) kitty_produce<NSTAGE>(P, P.Hq, S.stage, S.full, S.empty, &S.abort_flag);
         return;
     }
 
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Para
 for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
             for (int s = 0; s < U.np; ++s, ++sg) {
                 const int slot = sg % NSTAGE;
-                ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
+                ok = consumer_stage_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err, KVQ_SPIN_LIMIT, ok, &S.abort_flag);
                 if (ok) {
                     const uint8_t *st = S.stage[slot];
                     const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + K * PG / 4;

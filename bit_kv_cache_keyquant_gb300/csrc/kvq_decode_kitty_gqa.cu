@@ -45,7 +45,12 @@ struct SmemKG {
     float st_acc[NCWARP][KG_MAX][KACC_ROW];
     float st_m[NCWARP][KG_MAX];
     float st_l[NCWARP][KG_MAX];
+    int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
+                                          // members before it keep their 16-byte alignment)
 };
+static_assert(offsetof(SmemKG, qhi) % 16 == 0 && offsetof(SmemKG, qlo) % 16 == 0 && offsetof(SmemKG, qz) % 16 == 0 &&
+                  offsetof(SmemKG, st_acc) % 16 == 0,
+              "16-byte aligned tables");
 
 }  // namespace
 
@@ -63,12 +68,13 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], NCWARP);
         }
+        S.abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kitty_produce<KQ_NSTAGE, true>(P, P.Hkv, S.stage, S.full, S.empty);
+        if (lane == 0) kitty_produce<KQ_NSTAGE, true>(P, P.Hkv, S.stage, S.full, S.empty, &S.abort_flag);
         return;
     }
 
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
             const float unsig = S.unsig[r];
             for (int s = 0; s < U.np; ++s, ++sg) {
                 const int slot = sg % KQ_NSTAGE;
-                ok = ok && mbar_wait(&S.full[slot], (sg / KQ_NSTAGE) & 1, P.err);
+                ok = consumer_stage_wait(&S.full[slot], (sg / KQ_NSTAGE) & 1, P.err, KVQ_SPIN_LIMIT, ok, &S.abort_flag);
                 if (ok) {
                     const uint8_t *st = S.stage[slot];
                     const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + K * PG / 4;

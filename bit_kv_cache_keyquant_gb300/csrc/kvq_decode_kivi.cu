@@ -55,7 +55,15 @@ struct Smem {
     float st_acc[NCWARP][KVQ_D];
     float st_m[NCWARP];
     float st_l[NCWARP];
+    int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
+                                          // members before it keep their 16-byte alignment)
 };
+// members read with 16-byte vector loads stay 16-byte aligned
+using Smem_223 = Smem<2, 2, 3>;
+using Smem_442 = Smem<4, 4, 2>;
+static_assert(offsetof(Smem_223, qk) % 16 == 0 && offsetof(Smem_223, st_acc) % 16 == 0 &&
+                  offsetof(Smem_442, qk) % 16 == 0 && offsetof(Smem_442, st_acc) % 16 == 0,
+              "16-byte aligned shared-memory tables");
 
 // Warp maximum of a float in one redux instruction: the bit patterns are
 // mapped to unsigned integers in the floats' order (negative patterns
@@ -138,13 +146,14 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], NCWARP);
         }
+        S.abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == NCWARP) {
         // ---------------- producer: one stream of stages across all units ----------------
-        if (lane == 0) kivi_produce<NSTAGE, false, BK, BV>(P, P.Hq, S.stage, S.full, S.empty);
+        if (lane == 0) kivi_produce<NSTAGE, false, BK, BV>(P, P.Hq, S.stage, S.full, S.empty, &S.abort_flag);
         return;
     }
 
@@ -196,7 +205,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
             for (int s = 0; s < U.nstages; ++s, ++sg) {
                 const int slot = sg % NSTAGE;
-                ok = ok && mbar_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err);
+                ok = consumer_stage_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err, KIVI_WAIT_LIMIT(P), ok, &S.abort_flag);
                 const int tile = s * NCWARP + warp;
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];

@@ -58,7 +58,16 @@ struct SmemG {
     float st_acc[NCWARP][GMAX][ACC_ROW];
     float st_m[NCWARP][GMAX];
     float st_l[NCWARP][GMAX];
+    int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
+                                          // members before it keep their 16-byte alignment)
 };
+// members read with 16-byte vector loads stay 16-byte aligned
+using SmemG_223 = SmemG<2, 2, 3>;
+using SmemG_442 = SmemG<4, 4, 2>;
+static_assert(offsetof(SmemG_223, qhi) % 16 == 0 && offsetof(SmemG_223, qlo) % 16 == 0 &&
+                  offsetof(SmemG_223, qz) % 16 == 0 && offsetof(SmemG_223, st_acc) % 16 == 0 &&
+                  offsetof(SmemG_442, qhi) % 16 == 0 && offsetof(SmemG_442, st_acc) % 16 == 0,
+              "16-byte aligned shared-memory tables");
 
 }  // namespace
 
@@ -81,12 +90,13 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], NCWARP);
         }
+        S.abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kivi_produce<GQ_NSTAGE, true, BK, BV>(P, P.Hkv, S.stage, S.full, S.empty);
+        if (lane == 0) kivi_produce<GQ_NSTAGE, true, BK, BV>(P, P.Hkv, S.stage, S.full, S.empty, &S.abort_flag);
         return;
     }
 
@@ -175,7 +185,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
             const float unsig = S.unsig[r];
             for (int s = 0; s < U.nstages; ++s, ++sg) {
                 const int slot = sg % GQ_NSTAGE;
-                ok = ok && mbar_wait(&S.full[slot], (sg / GQ_NSTAGE) & 1, P.err);
+                ok = consumer_stage_wait(&S.full[slot], (sg / GQ_NSTAGE) & 1, P.err, KIVI_WAIT_LIMIT(P), ok, &S.abort_flag);
                 const int tile = s * NCWARP + warp;
                 if (ok && tile < U.nT) {
                     const uint8_t *st = S.stage[slot];

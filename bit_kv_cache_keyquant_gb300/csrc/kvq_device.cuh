@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/kvq.h"
@@ -104,14 +105,53 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(KVQ_SUSPEND_NS) : "memory");
     return ok != 0;
 }
-// Bounded wait (at most about KVQ_SPIN_LIMIT * KVQ_SUSPEND_NS): false, and the
+// Bounded wait (at most about limit * KVQ_SUSPEND_NS): false, and the
 // device error flag set, if the phase never completes.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
-    for (uint32_t i = 0; i < KVQ_SPIN_LIMIT; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err,
+                                          uint32_t limit = KVQ_SPIN_LIMIT) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicOr(err, 1u);
     return false;
 }
+// ---------------------------------------------------------------------------
+// The stage ring of the decode kernels: a producer fills slots with bulk
+// copies that complete on the slot's full barrier; consumer warps wait on it,
+// read the slot, then arrive on its empty barrier; the producer refills a slot
+// once its empty barrier completes.  A full barrier may be armed again only
+// after its armed phase has completed (a second arrive on one phase is not
+// allowed), and the consumers' successful waits are what guarantee that.  So
+// a consumer warp whose bounded wait gives up raises the ring's abort flag
+// before its next arrive on an empty barrier, the producer reads the flag
+// after each of its empty waits and stops filling, and before the CTA exits
+// the producer waits (bounded) for the last phase it armed on every slot, so
+// that no copy is in flight.
+// ---------------------------------------------------------------------------
+// Consumer side: the warp's bounded wait for a stage; false for the whole warp
+// if any lane gave up (the flag then raised), and false without waiting once
+// the warp has failed before.
+__device__ __forceinline__ bool consumer_stage_wait(uint64_t *full, uint32_t parity, unsigned *err, uint32_t limit,
+                                                    bool ok, int *abort_flag) {
+    if (!ok) return false;
+    const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(full, parity, err, limit));
+    if (!got) *reinterpret_cast<volatile int *>(abort_flag) = 1;
+    return got;
+}
+// Producer side: raised by a consumer (read after an empty wait, whose acquire
+// orders it after the consumer's flag store and arrive).
+__device__ __forceinline__ bool ring_aborted(const int *abort_flag) {
+    return *reinterpret_cast<const volatile int *>(abort_flag) != 0;
+}
+// Producer side: wait for the last armed phase of every slot (armed[j] phases
+// were armed on slot j).
+template <int NST>
+__device__ __forceinline__ void producer_drain(uint64_t *full, const int (&armed)[NST], unsigned *err,
+                                               uint32_t limit = KVQ_SPIN_LIMIT) {
+#pragma unroll
+    for (int j = 0; j < NST; ++j)
+        if (armed[j] > 0) mbar_wait(&full[j], (uint32_t)(armed[j] - 1) & 1u, err, limit);
+}
+
 // Global -> shared bulk copy completing on `bar`; src, dst 16-B aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

@@ -78,6 +78,18 @@ inline cudaError_t smem_opt_in(Kern *kernel, size_t smem, std::atomic<uint64_t> 
     return e;
 }
 
+#ifdef KVQ_FAULT_INJECT
+// Test builds only (never the product library): the KIVI decode producer of
+// CTA 0 leaves its stage skip_stage unfilled, and the KIVI decode waits give
+// up after spin_limit tries when it is nonzero, so that a test can watch the
+// bounded waits expire.  Set through kvq_test_inject_wait.
+struct TestInject {
+    int skip_stage = -1;
+    unsigned spin_limit = 0;
+};
+extern TestInject g_test_inject;
+#endif
+
 int num_sms();
 unsigned *device_error_ptr();   // device address of the error bitmask (current device)
 

@@ -188,24 +188,29 @@ __device__ __forceinline__ void kitty_residual(const Params &P, const Unit &U, c
 // unit order, into an NST-slot ring; returns after every issued copy landed.
 template <int NST, bool SPLIT_MAJOR = false>
 __device__ __forceinline__ void kitty_produce(const Params &P, int hpr, uint8_t (*stage)[STAGE_BYTES], uint64_t *full,
-                                              uint64_t *empty) {
+                                              uint64_t *empty, const int *abort_flag) {
     const int n_units = P.B * hpr * P.splits;
     bool ok = true;
     int sg = 0;
+    int armed[NST];
+#pragma unroll
+    for (int j = 0; j < NST; ++j) armed[j] = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit U = unit_of<SPLIT_MAJOR>(P, u, hpr);
         for (int s = 0; s < U.np; ++s, ++sg) {
             const int slot = sg % NST;
             if (sg >= NST) ok = mbar_wait(&empty[slot], ((sg / NST) - 1) & 1, P.err);
+            ok = ok && !ring_aborted(abort_flag);
             if (!ok) break;
             const int p = U.p0 + s;
             uint8_t *st = stage[slot];
+            ++armed[slot];
             mbar_expect_tx(&full[slot], (uint32_t)(P.kpb + P.vpb));
             bulk_g2s(st, key_page(P, U, p), (uint32_t)P.kpb, &full[slot]);
             bulk_g2s(st + VREC_OFF, value_page(P, U, p), (uint32_t)P.vpb, &full[slot]);
         }
     }
-    for (int s = max(0, sg - NST); s < sg; ++s) mbar_wait(&full[s % NST], (s / NST) & 1, P.err);
+    producer_drain<NST>(full, armed, P.err);
 }
 
 }  // namespace

@@ -55,7 +55,18 @@ struct Params {
     int pt_stride, n_pages;
     int64_t rec_bytes;
     int kc_bytes, vc_bytes;   // page record sections: key codes, key (s, z) (2048 B), value codes, value (s, z)
+#ifdef KVQ_FAULT_INJECT
+    int inj_skip;             // test builds: stage of CTA 0 the producer leaves unfilled (-1: none)
+    unsigned inj_spin;        // test builds: wait tries before giving up (0: KVQ_SPIN_LIMIT)
+#endif
 };
+
+// Tries of a bounded mbarrier wait in the KIVI decode kernels.
+#ifdef KVQ_FAULT_INJECT
+#define KIVI_WAIT_LIMIT(P) ((P).inj_spin ? (P).inj_spin : KVQ_SPIN_LIMIT)
+#else
+#define KIVI_WAIT_LIMIT(P) KVQ_SPIN_LIMIT
+#endif
 
 // Geometry of one work unit.  Splits 0 .. splits-2 of a (batch row, query
 // head) cover the staged quantized tiles [0, Qf) in chunks; split splits-1
@@ -297,12 +308,15 @@ __device__ __forceinline__ void kivi_residual(const Params &P, const Unit &U, co
 // unit order, into an NST-slot ring; returns after every issued copy landed.
 template <int NST, bool SPLIT_MAJOR = false, int BK = 2, int BV = 2>
 __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (*stage)[Geo<BK, BV>::BYTES],
-                                             uint64_t *full, uint64_t *empty) {
+                                             uint64_t *full, uint64_t *empty, const int *abort_flag) {
     using GG = Geo<BK, BV>;
     const int n_units = P.B * hpr * P.splits;
     const int G = P.G;
     bool ok = true;
     int sg = 0;
+    int armed[NST];
+#pragma unroll
+    for (int j = 0; j < NST; ++j) armed[j] = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit U = unit_of<SPLIT_MAJOR>(P, u, hpr);
         const uint8_t *kc_base = P.k_codes + U.bk * P.kgrp_cap * ((int64_t)G * KVQ_D * BK / 8);
@@ -311,8 +325,12 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
         const uint32_t *vsz_base = P.v_sz + U.bk * P.cap * P.ngv;
         for (int s = 0; s < U.nstages; ++s, ++sg) {
             const int slot = sg % NST;
-            if (sg >= NST) ok = mbar_wait(&empty[slot], ((sg / NST) - 1) & 1, P.err);
+            if (sg >= NST) ok = mbar_wait(&empty[slot], ((sg / NST) - 1) & 1, P.err, KIVI_WAIT_LIMIT(P));
+            ok = ok && !ring_aborted(abort_flag);
             if (!ok) break;
+#ifdef KVQ_FAULT_INJECT
+            if (blockIdx.x == 0 && sg == P.inj_skip) continue;   // test builds: this stage never fills
+#endif
             const int nt = min(NCWARP, U.nT - s * NCWARP);
             const int tok = U.t0 + s * STAGE_TOK;
             const uint32_t kc_b = nt * 512 * BK;
@@ -320,6 +338,7 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
             const uint32_t vc_b = nt * 32 * (KVQ_D * BV / 8);
             const uint32_t vsz_b = nt * 32 * P.ngv * 4;
             uint8_t *st = stage[slot];
+            ++armed[slot];
             if (P.page_table) {
                 // the page record is the stage: one copy (the tiles past nt are not read)
                 mbar_expect_tx(&full[slot], (uint32_t)GG::BYTES);
@@ -333,8 +352,8 @@ __device__ __forceinline__ void kivi_produce(const Params &P, int hpr, uint8_t (
             bulk_g2s(st + GG::KC + GG::KSZ + GG::VC, vsz_base + (int64_t)tok * P.ngv, vsz_b, &full[slot]);
         }
     }
-    // drain: every issued stage must have landed before the CTA exits
-    for (int s = max(0, sg - NST); s < sg; ++s) mbar_wait(&full[s % NST], (s / NST) & 1, P.err);
+    // drain: every issued copy must have landed before the CTA exits
+    producer_drain<NST>(full, armed, P.err, KIVI_WAIT_LIMIT(P));
 }
 
 // Kernel parameters common to the KIVI decode kernels, from a dense or paged cache.
@@ -373,6 +392,10 @@ inline Params kivi_params(const kvq_config *cfg, const KiviSrc &c, const void *q
     P.rec_bytes = kivi_page_bytes(cfg->bits_k, cfg->bits_v);
     P.kc_bytes = 16 * KVQ_D * cfg->bits_k;
     P.vc_bytes = 16 * KVQ_D * cfg->bits_v;
+#ifdef KVQ_FAULT_INJECT
+    P.inj_skip = g_test_inject.skip_stage;
+    P.inj_spin = g_test_inject.spin_limit;
+#endif
     return P;
 }
 
