@@ -105,14 +105,12 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     const int hB = q >> 1;                         // head of this lane's B column (n = q)
     const bool xB = (q & 1) != 0;                  // B column holds lo parts
     const int gl = (32 * warp) / P.G;              // key group of this warp's tile within a stage
-    // value unpacking: channel 16mt + q (+8) is byte 4mt + q/4 (+2) of a token row, bits 2(q%4)
-    const uint32_t vsel = (uint32_t)((q >> 2) | ((4 + (q >> 2)) << 4) | ((2 + (q >> 2)) << 8) | ((6 + (q >> 2)) << 12));
-    const uint32_t vshift = (q & 2) ? 4u : 0u;
-    const uint32_t vmask = (q & 1) ? 0x0C0C0C0Cu : 0x03030303u;
+    // 2-bit value unpacking: the lane's byte of value group g (32 channels) is byte 8g + q of a token row,
+    // channels 32g + 4q + p at bits 2p; bsel gathers that byte (byte q % 4 of its word) of two rows
+    const uint32_t bsel = (uint32_t)((q & 3) | ((4 + (q & 3)) << 4));
     // 4-bit values: channel 16mt + q (+8) is byte q/2 of the m-tile's first (second) word, bits 4(q%2)
     const uint32_t vsel4 = (uint32_t)((q >> 1) | ((4 + (q >> 1)) << 4));
     const uint32_t vshift4 = (q & 1) ? 4u : 0u;
-    const float vscale = BV == 4 ? 512.f : ((q & 1) ? 128.f : 512.f);
     const uint32_t *qown = xB ? S.qlo[hB] : S.qhi[hB];   // the part of B column n = q (zero-point products)
     const int jz = q % NGV;                               // value group of rows q, q + 8 of the zero-point product
     bool ok = true;
@@ -366,23 +364,27 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                                     mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0[j], bv1[j]);
                                 }
                             }
-                        } else
+                        } else {
+                            // m-tile 2g + pp, rows q | q + 8: channels 32g + 4q + 2pp + 0 | 1 (bit positions 2pp and
+                            // 2pp + 1 of the lane's byte of group g); one word X = that byte of the rows of tokens
+                            // t0, t0+4 | t0+8, t0+12 gives the A registers of both m-tiles
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 32 + 16 * hf);
-                            const uint4 rB = *reinterpret_cast<const uint4 *>(vc + (t0 + 4) * 32 + 16 * hf);
-                            const uint4 rC = *reinterpret_cast<const uint4 *>(vc + (t0 + 8) * 32 + 16 * hf);
-                            const uint4 rD = *reinterpret_cast<const uint4 *>(vc + (t0 + 12) * 32 + 16 * hf);
-                            const uint32_t wa[4] = {rA.x, rA.y, rA.z, rA.w}, wb[4] = {rB.x, rB.y, rB.z, rB.w};
-                            const uint32_t wc[4] = {rC.x, rC.y, rC.z, rC.w}, wd[4] = {rD.x, rD.y, rD.z, rD.w};
-#pragma unroll
-                            for (int m4 = 0; m4 < 4; ++m4) {
-                                const int mt = 4 * hf + m4;
-                                const int j = (16 * mt) / (KVQ_D / NGV);       // value group of the m-tile
-                                uint32_t c0l, c0h, c8l, c8h;
-                                e4m3x4_f16x2((prmt(wa[m4], wb[m4], vsel) >> vshift) & vmask, c0l, c0h);
-                                e4m3x4_f16x2((prmt(wc[m4], wd[m4], vsel) >> vshift) & vmask, c8l, c8h);
-                                mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0[j], bv1[j]);
+                            for (int g8 = 0; g8 < 4; ++g8) {
+                                const int wo = 8 * g8 + 4 * (q >> 2);            // the word holding byte 8g + q
+                                const uint32_t wA = *reinterpret_cast<const uint32_t *>(vc + t0 * 32 + wo);
+                                const uint32_t wB = *reinterpret_cast<const uint32_t *>(vc + (t0 + 4) * 32 + wo);
+                                const uint32_t wC = *reinterpret_cast<const uint32_t *>(vc + (t0 + 8) * 32 + wo);
+                                const uint32_t wD = *reinterpret_cast<const uint32_t *>(vc + (t0 + 12) * 32 + wo);
+                                const uint32_t X = prmt(prmt(wA, wB, bsel), prmt(wC, wD, bsel), 0x5410u);
+                                const uint32_t X4 = X >> 4;
+                                const int j = (32 * g8) / (KVQ_D / NGV);          // value group of both m-tiles
+                                uint32_t a0, a1, a2, a3;
+                                e4m3x4_f16x2(X & 0x03030303u, a0, a2);
+                                e4m3x4_f16x2(X & 0x0C0C0C0Cu, a1, a3);
+                                mma16816(vacc[2 * g8], a0, a1, a2, a3, bv0[j], bv1[j]);
+                                e4m3x4_f16x2(X4 & 0x03030303u, a0, a2);
+                                e4m3x4_f16x2(X4 & 0x0C0C0C0Cu, a1, a3);
+                                mma16816(vacc[2 * g8 + 1], a0, a1, a2, a3, bv0[j], bv1[j]);
                             }
                         }
                     }
@@ -412,11 +414,24 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                 }
             }
             float *acc = S.st_acc[warp][r];
+            if (BV == 4) {
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int j = (16 * mt) / (KVQ_D / NGV);
-                acc[16 * mt + q] = fmaf(vacc[mt][0] + vacc[mt][1], vscale, vz[j]);
-                acc[16 * mt + q + 8] = fmaf(vacc[mt][2] + vacc[mt][3], vscale, vz[j]);
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int j = (16 * mt) / (KVQ_D / NGV);
+                    acc[16 * mt + q] = fmaf(vacc[mt][0] + vacc[mt][1], 512.f, vz[j]);
+                    acc[16 * mt + q + 8] = fmaf(vacc[mt][2] + vacc[mt][3], 512.f, vz[j]);
+                }
+            } else {
+                // rows q of both m-tiles of group g carry codes x 2^-9, rows q + 8 codes x 2^-7
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const int j = (32 * g8) / (KVQ_D / NGV);
+                    *reinterpret_cast<float4 *>(&acc[32 * g8 + 4 * q]) =
+                        make_float4(fmaf(vacc[2 * g8][0] + vacc[2 * g8][1], 512.f, vz[j]),
+                                    fmaf(vacc[2 * g8][2] + vacc[2 * g8][3], 128.f, vz[j]),
+                                    fmaf(vacc[2 * g8 + 1][0] + vacc[2 * g8 + 1][1], 512.f, vz[j]),
+                                    fmaf(vacc[2 * g8 + 1][2] + vacc[2 * g8 + 1][3], 128.f, vz[j]));
+                }
             }
             if (q == 0) {
                 S.st_m[warp][r] = m_run;
