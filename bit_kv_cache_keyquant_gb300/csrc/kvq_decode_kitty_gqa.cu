@@ -37,7 +37,6 @@ struct SmemKG {
     uint32_t qhi[KG_MAX][64];             // fp16x2 hi parts of alpha q 2^sigma: [head][k/2][r][4]
     uint32_t qlo[KG_MAX][64];
     uint32_t qhl[KG_MAX][KVQ_D];          // channel order: fp16 hi | lo << 16 (the boosted rows' lookups)
-    float qz[KG_MAX][KVQ_D];              // alpha q (fp32): [head][k][r][4]
     float qv[KVQ_D];                      // alpha q of one head, channel order (residual unit)
     float unsig[KG_MAX];                  // 2^-sigma_h
     uint8_t hchan[NCWARP][KMAX + 16];     // channel of boosted row r (per warp copy)
@@ -48,8 +47,7 @@ struct SmemKG {
     int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
                                           // members before it keep their 16-byte alignment)
 };
-static_assert(offsetof(SmemKG, qhi) % 16 == 0 && offsetof(SmemKG, qlo) % 16 == 0 && offsetof(SmemKG, qz) % 16 == 0 &&
-                  offsetof(SmemKG, st_acc) % 16 == 0,
+static_assert(offsetof(SmemKG, qhi) % 16 == 0 && offsetof(SmemKG, qlo) % 16 == 0 && offsetof(SmemKG, st_acc) % 16 == 0,
               "16-byte aligned tables");
 
 }  // namespace
@@ -87,10 +85,10 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     const int rsw = r >> 1;
     const uint32_t bsel = rsw ? (uint32_t)(4 + (col & 3)) | ((uint32_t)(col & 3) << 4)
                               : (uint32_t)(col & 3) | ((uint32_t)(4 + (col & 3)) << 4);
-    const uint32_t vsel = (uint32_t)((q >> 2) | ((4 + (q >> 2)) << 4) | ((2 + (q >> 2)) << 8) | ((6 + (q >> 2)) << 12));
-    const uint32_t vshift = (q & 2) ? 4u : 0u;
-    const uint32_t vmask = (q & 1) ? 0x0C0C0C0Cu : 0x03030303u;
-    const float vscale = (q & 1) ? 128.f : 512.f;
+    // value unpacking: the lane's byte of each 32-channel block g is byte 8g + q of a token row (channels
+    // 32g + 4q + p at bits 2p); vbsel gathers that byte (byte q % 4 of its word) of two rows
+    const uint32_t vbsel = (uint32_t)((q & 3) | ((4 + (q & 3)) << 4));
+    const uint32_t *qown = xB ? S.qlo[hB] : S.qhi[hB];   // the part of B column n = q (zero-point products)
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -128,7 +126,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                 make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
             *reinterpret_cast<uint2 *>(&S.qlo[h][pw]) =
                 make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
-            *reinterpret_cast<float4 *>(&S.qz[h][tk * 16 + tr * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
             S.qhl[h][c0] = (uint32_t)hi[0] | ((uint32_t)lo[0] << 16);
             S.qhl[h][c0 + 1] = (uint32_t)hi[1] | ((uint32_t)lo[1] << 16);
             S.qhl[h][c0 + 8] = (uint32_t)hi[2] | ((uint32_t)lo[2] << 16);
@@ -158,7 +155,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                 asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
             }
         } else {
-            float m_run = -INFINITY, l_part = 0.f, vz = 0.f;   // head r
+            float m_run = -INFINITY, l_part = 0.f;   // head r
+            float vzacc[4] = {0.f, 0.f, 0.f, 0.f};   // sum_t p z_t of head r (hi, lo; rows q, q + 8 alike)
             float vacc[8][4];
 #pragma unroll
             for (int i = 0; i < 8; ++i) vacc[i][0] = vacc[i][1] = vacc[i][2] = vacc[i][3] = 0.f;
@@ -180,30 +178,12 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                         }
                         for (int rr = K + lane; rr < 16 * n_hk; rr += 32) S.hchan[warp][rr] = 0xFF;   // rows past K
                     }
-                    // ---- alpha sum_c q_hc z_c: the lanes of head hB split the lane's channels by xB ----
-                    float zr;
-                    {
-                        float zp = 0.f;
-#pragma unroll
-                        for (int n = 0; n < 4; ++n) {
-                            const int k = xB ? 7 - n : n;
-                            const int c0 = 16 * k + 2 * r;
-                            const uint32_t z01 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0);
-                            const uint32_t z89 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0 + 8);
-                            const float4 qa = *reinterpret_cast<const float4 *>(&S.qz[hB][k * 16 + 4 * r]);
-                            zp = fmaf(qa.x, h2f(lo16(z01)), zp);
-                            zp = fmaf(qa.y, h2f(hi16(z01)), zp);
-                            zp = fmaf(qa.z, h2f(lo16(z89)), zp);
-                            zp = fmaf(qa.w, h2f(hi16(z89)), zp);
-                        }
-                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
-                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
-                        zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
-                        zr = __shfl_sync(0xFFFFFFFFu, zp, 8 * r);
-                    }
                     __syncwarp();
                     // ---- low plane x W, then the boosted rows x 4W, on the tensor cores ----
                     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                    // alpha sum_c q_hc z_c as one more product per k-step: A = the page's z_c in every row,
+                    // B = the lane's part of alpha q 2^sigma (two chains)
+                    float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
                     {
                         const uint32_t *lw = reinterpret_cast<const uint32_t *>(low) + 2 * warp + (q >> 2);
 #pragma unroll
@@ -219,9 +199,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                             }
                             const uint32_t bk[4] = {split_prod(a.x, l.x, sv[0], xB), split_prod(a.y, l.y, sv[1], xB),
                                                     split_prod(a.z, l.z, sv[2], xB), split_prod(a.w, l.w, sv[3], xB)};
+                            const uint4 qo = *reinterpret_cast<const uint4 *>(qown + 16 * i + 4 * r);
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
                                 const int c0 = 16 * (2 * i + kk) + 2 * r;
+                                const uint32_t z01 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0);
+                                const uint32_t z89 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0 + 8);
+                                if (i & 1)
+                                    mma16816(z1, z01, z01, z89, z89, kk ? qo.z : qo.x, kk ? qo.w : qo.y);
+                                else
+                                    mma16816(z0, z01, z01, z89, z89, kk ? qo.z : qo.x, kk ? qo.w : qo.y);
                                 const uint32_t x01 = prmt(lw[(c0 + rsw) * 8], lw[(c0 + 1 - rsw) * 8], bsel);
                                 const uint32_t x89 = prmt(lw[(c0 + 8 + rsw) * 8], lw[(c0 + 9 - rsw) * 8], bsel);
                                 const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
@@ -268,6 +255,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                     }
                     // ---- logits of head r, tokens 32w + 4q + p; online softmax ----
                     const float f9 = unsig * 512.f, f7 = unsig * 128.f;
+                    const float zr = ((z0[0] + z1[0]) + (z0[1] + z1[1])) * unsig;
                     float lg[4];
                     lg[0] = fmaf(s0[0] + s0[1], f9, zr);
                     lg[1] = fmaf(s0[2] + s0[3], f7, zr);
@@ -278,19 +266,17 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
                     if (mt > m_run) {
-                        const float sc = exp2f(m_run - mt);
+                        const float sc = ex2_ftz(m_run - mt);
                         l_part *= sc;
-                        vz *= sc;
+                        scale4(vzacc, sc);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            vacc[i][0] *= sc; vacc[i][1] *= sc; vacc[i][2] *= sc; vacc[i][3] *= sc;
-                        }
+                        for (int i = 0; i < 8; ++i) scale4(vacc[i], sc);
                         m_run = mt;
                     }
                     float pr[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        pr[i] = exp2f(lg[i] - m_run);
+                        pr[i] = ex2_ftz(lg[i] - m_run);
                         l_part += pr[i];
                     }
                     // token t = 16k + 8hk + 4e + j of the tile sits at position 16k + 8hk + 2j + e
@@ -298,16 +284,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                     const int pbase = 16 * (q >> 2) + 8 * ((q >> 1) & 1) + (q & 1);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pb[r * KPB_ROW + pbase + 2 * i] = pr[i];
-                    // ---- value zero-point term of head r over the lane's four tokens ----
                     const uint8_t *vrec = st + VREC_OFF;
                     const uint16_t *vs = reinterpret_cast<const uint16_t *>(vrec + PG * KVQ_D / 4) + 32 * warp;
-                    {
-                        const uint2 z4 = *reinterpret_cast<const uint2 *>(vs + PG + 4 * q);
-                        vz = fmaf(pr[0], h2f(lo16(z4.x)), vz);
-                        vz = fmaf(pr[1], h2f(hi16(z4.x)), vz);
-                        vz = fmaf(pr[2], h2f(lo16(z4.y)), vz);
-                        vz = fmaf(pr[3], h2f(hi16(z4.y)), vz);
-                    }
                     __syncwarp();
                     // ---- values: k-column 2j + e + 8hk of k-step k is token 16k + 8hk + 4e + j ----
                     const uint8_t *vc = vrec + warp * 32 * (KVQ_D / 4);
@@ -322,22 +300,31 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                         const uint32_t sc8 = (uint32_t)vs[t0 + 8] | ((uint32_t)vs[t0 + 12] << 16);
                         const uint32_t bv0 = split_prod(pha, pla, sa, xB);
                         const uint32_t bv1 = split_prod(phc, plc, sc8, xB);
+                        {
+                            // value zero-point product: A rows hold z of the k-step's tokens, B the lane's part of p
+                            const uint32_t za = (uint32_t)vs[PG + t0] | ((uint32_t)vs[PG + t0 + 4] << 16);
+                            const uint32_t zc = (uint32_t)vs[PG + t0 + 8] | ((uint32_t)vs[PG + t0 + 12] << 16);
+                            mma16816(vzacc, za, za, zc, zc, xB ? pla : pha, xB ? plc : phc);
+                        }
+                        // m-tile 2g + pp, rows q | q + 8: channels 32g + 4q + 2pp + 0 | 1 (bit positions 2pp and
+                        // 2pp + 1 of the lane's byte of block g); one word X = that byte of the rows of tokens
+                        // t0, t0+4 | t0+8, t0+12 gives the A registers of both m-tiles
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 32 + 16 * hf);
-                            const uint4 rB = *reinterpret_cast<const uint4 *>(vc + (t0 + 4) * 32 + 16 * hf);
-                            const uint4 rC = *reinterpret_cast<const uint4 *>(vc + (t0 + 8) * 32 + 16 * hf);
-                            const uint4 rD = *reinterpret_cast<const uint4 *>(vc + (t0 + 12) * 32 + 16 * hf);
-                            const uint32_t wa[4] = {rA.x, rA.y, rA.z, rA.w}, wb[4] = {rB.x, rB.y, rB.z, rB.w};
-                            const uint32_t wc[4] = {rC.x, rC.y, rC.z, rC.w}, wd[4] = {rD.x, rD.y, rD.z, rD.w};
-#pragma unroll
-                            for (int m4 = 0; m4 < 4; ++m4) {
-                                const int mt = 4 * hf + m4;
-                                uint32_t c0l, c0h, c8l, c8h;
-                                e4m3x4_f16x2((prmt(wa[m4], wb[m4], vsel) >> vshift) & vmask, c0l, c0h);
-                                e4m3x4_f16x2((prmt(wc[m4], wd[m4], vsel) >> vshift) & vmask, c8l, c8h);
-                                mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0, bv1);
-                            }
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            const int wo = 8 * g8 + 4 * (q >> 2);            // the word holding byte 8g + q
+                            const uint32_t wA = *reinterpret_cast<const uint32_t *>(vc + t0 * 32 + wo);
+                            const uint32_t wB = *reinterpret_cast<const uint32_t *>(vc + (t0 + 4) * 32 + wo);
+                            const uint32_t wC = *reinterpret_cast<const uint32_t *>(vc + (t0 + 8) * 32 + wo);
+                            const uint32_t wD = *reinterpret_cast<const uint32_t *>(vc + (t0 + 12) * 32 + wo);
+                            const uint32_t X = prmt(prmt(wA, wB, vbsel), prmt(wC, wD, vbsel), 0x5410u);
+                            const uint32_t X4 = X >> 4;
+                            uint32_t a0, a1, a2, a3;
+                            e4m3x4_f16x2(X & 0x03030303u, a0, a2);
+                            e4m3x4_f16x2(X & 0x0C0C0C0Cu, a1, a3);
+                            mma16816(vacc[2 * g8], a0, a1, a2, a3, bv0, bv1);
+                            e4m3x4_f16x2(X4 & 0x03030303u, a0, a2);
+                            e4m3x4_f16x2(X4 & 0x0C0C0C0Cu, a1, a3);
+                            mma16816(vacc[2 * g8 + 1], a0, a1, a2, a3, bv0, bv1);
                         }
                     }
                     __syncwarp();
@@ -350,15 +337,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 4);
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
-            vz += __shfl_xor_sync(0xFFFFFFFFu, vz, 4);
-            vz += __shfl_xor_sync(0xFFFFFFFFu, vz, 8);
-            vz += __shfl_xor_sync(0xFFFFFFFFu, vz, 16);
+            const float vz = vzacc[0] + vzacc[1];
             float *acc = S.st_acc[warp][r];
+            // rows q of both m-tiles of block g carry codes x 2^-9, rows q + 8 codes x 2^-7
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                acc[16 * mt + q] = fmaf(vacc[mt][0] + vacc[mt][1], vscale, vz);
-                acc[16 * mt + q + 8] = fmaf(vacc[mt][2] + vacc[mt][3], vscale, vz);
-            }
+            for (int g8 = 0; g8 < 4; ++g8)
+                *reinterpret_cast<float4 *>(&acc[32 * g8 + 4 * q]) =
+                    make_float4(fmaf(vacc[2 * g8][0] + vacc[2 * g8][1], 512.f, vz),
+                                fmaf(vacc[2 * g8][2] + vacc[2 * g8][3], 128.f, vz),
+                                fmaf(vacc[2 * g8 + 1][0] + vacc[2 * g8 + 1][1], 512.f, vz),
+                                fmaf(vacc[2 * g8 + 1][2] + vacc[2 * g8 + 1][3], 128.f, vz));
             if (q == 0) {
                 S.st_m[warp][r] = m_run;
                 S.st_l[warp][r] = l_w;
