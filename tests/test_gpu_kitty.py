@@ -146,3 +146,20 @@ def test_kitty_offsets_beyond_2gib(K, orc):
         parts = orc.kitty_build_one(Kh, Vh)
         want = orc.kitty_decode_one(q[b, h * g:(h + 1) * g].cpu().numpy(), *parts, L=L)
         assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (8, 2)])
+def test_kitty_decode_big_query(K, orc, Hq, Hkv):
+    """A query of +-3000 in one channel over channels of about 1e-3 (logits of about 800; ties on the large
+    channel broken by the small ones) on the per-head and the grouped-query Kitty kernels."""
+    rng = np.random.default_rng(70 + Hq)
+    cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv, group_k=128, sink=32, residual=128, boost_k=16)
+    lens = [700, 1300]
+    Ks = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(Hkv)] for L in lens]
+    Vs = [[rng.standard_normal((L, 128)).astype(np.float16) for _ in range(Hkv)] for L in lens]
+    q = rng.standard_normal((2, Hq, 128)) * 1e-3
+    q[:, :, 5] = 3000.0
+    q[1, 0, 5] = -3000.0
+    q = q.astype(np.float16)
+    got = _run(K, cfg, Ks, Vs, q, 1300)
+    assert_attn_close(got, _oracle(orc, cfg, Ks, Vs, q))

@@ -151,7 +151,7 @@ def test_decode_wide_outlier_channels(K, orc, Hq, Hkv):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
-@pytest.mark.parametrize("case", ["zero_query", "wide_channels", "const_groups", "huge_query"])
+@pytest.mark.parametrize("case", ["zero_query", "wide_channels", "const_groups", "huge_query", "big_query"])
 def test_decode_key_weight_extremes(K, orc, Hq, Hkv, case):
     """Key weights alpha q s at the edges of the per-head kernel's fixed-point form (one power-of-two
     scale per 32-token group, set by the group's largest |weight|) and of the tensor-core hi / lo
@@ -159,8 +159,12 @@ def test_decode_key_weight_extremes(K, orc, Hq, Hkv, case):
     whose channels are constant (s = 0), and a query of +-300 in one channel over channels of about
     0.02, a range of 2^14 (the grouped-query path keeps every channel's weight a normal fp16 number
     up to that range; beyond it the smallest channels fall to fp16 subnormals and lose their key
-    contributions, and the logits' ties on the large channel are then broken without them)."""
-    rng = np.random.default_rng({"zero_query": 11, "wide_channels": 12, "const_groups": 13, "huge_query": 14}[case] + Hq)
+    contributions, and the logits' ties on the large channel are then broken without them), and a query of
+    +-3000 in one channel over channels of about 1e-3 (logits of about 800: the 2-bit codes tie many tokens on
+    the large channel and the small channels break the ties; beyond about 1e4 over 1e-3 even an fp32
+    accumulation of exact products misses 2e-3, see test_oracle_pins.py)."""
+    rng = np.random.default_rng({"zero_query": 11, "wide_channels": 12, "const_groups": 13, "huge_query": 14,
+                                 "big_query": 15}[case] + Hq)
     cfg = K.make_config(n_q_heads=Hq, n_kv_heads=Hkv)
     lens = [700, 1300]
     Ks, Vs = [], []
@@ -187,6 +191,10 @@ def test_decode_key_weight_extremes(K, orc, Hq, Hkv, case):
         q *= 0.02
         q[:, :, 5] = 300.0
         q[1, 0, 5] = -300.0
+    if case == "big_query":
+        q *= 1e-3
+        q[:, :, 5] = 3000.0
+        q[1, 0, 5] = -3000.0
     q = q.astype(np.float16)
     got = _run_decode(K, cfg, Ks, Vs, q, 1300)
     assert np.isfinite(got).all()

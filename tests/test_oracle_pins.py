@@ -558,6 +558,44 @@ def test_int8_decode_equals_attention_over_block_dequantized_tokens(orc):
     assert np.max(np.abs(textbook(q[0], khat, v_rel, 128 ** -0.5) - out[0])) > 1e-6
 
 
+def _fp32_decode(Kh, V, q, sm):
+    """Attention with every product exact and rounded once to fp32, the logits summed over channels in
+    fp32 in channel order, and the softmax in fp32: the best any fp32-accumulating decode can do."""
+    q32 = (q * sm).astype(np.float32)
+    K32 = Kh.astype(np.float32)
+    s = np.zeros(Kh.shape[0], np.float32)
+    for c in range(Kh.shape[1]):
+        s = (s + K32[:, c] * q32[c]).astype(np.float32)
+    p = np.exp((s - s.max()).astype(np.float32)).astype(np.float32)
+    return (p / p.sum()) @ V.astype(np.float32)
+
+
+def test_fp32_accumulation_limit_on_extreme_query_ranges(orc):
+    """Reading of the tolerance: max-abs 2e-3 with fp32 accumulation holds while the logits stay moderate.
+    A query of 6e4 in one channel over channels of 1e-2 makes logits of about 2e4 whose ties (2-bit codes
+    tie many tokens on the large channel) are broken by differences of about 1e-2: even exact products
+    summed in fp32 miss 2e-3 there, while at 3e3 over 1e-3 (logits of about 800) they stay within half of it."""
+    rng = np.random.default_rng(22)
+    L, sm = 1280, 128 ** -0.5
+    worst = {}
+    for big, small in ((6e4, 1e-2), (3e3, 1e-3)):
+        errs = []
+        for _ in range(3):
+            K = rng.standard_normal((L, 128)).astype(np.float16)
+            V = rng.standard_normal((L, 128)).astype(np.float16)
+            codes, sz = orc.kivi_key_codes(K.reshape(L // 32, 32, 128))
+            s_ = f16(sz[..., 0].copy()).astype(np.float64)
+            z_ = f16(sz[..., 1].copy()).astype(np.float64)
+            Kh = (codes.astype(np.float64) * s_[:, None, :] + z_[:, None, :]).reshape(L, 128)
+            q = rng.standard_normal(128) * small
+            q[5] = big
+            q = q.astype(np.float16).astype(np.float64)
+            errs.append(np.max(np.abs(_fp32_decode(Kh, V, q, sm) - textbook(q, Kh, V, sm))))
+        worst[big] = max(errs)
+    assert worst[6e4] > 2e-3
+    assert worst[3e3] < 1e-3
+
+
 # --------------------------------------------------------------------------
 # token-granular INT8 over a slot pool (WitCert, SGLang storage subsection)
 # --------------------------------------------------------------------------
