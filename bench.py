@@ -732,11 +732,12 @@ def run_gpu(args, w, rank, world, local_rank):
 def stage1_kernel(w):
     """Name and source files of the stage-1 kernel the library runs for workload w."""
     g = w.n_q_heads // w.n_kv_heads
-    if w.variant == "kivi" and 2 <= g <= 4:
+    gqa = 2 <= g <= 4 or (4 < g <= 8 and g % 2 == 0)        # up to 4 heads per unit, two units per kv head beyond
+    if w.variant == "kivi" and gqa:
         return "kivi_decode_gqa_kernel", ("kvq_decode_kivi_gqa.cu", "kvq_kivi.cuh", "kvq_mma.cuh", "kvq_device.cuh")
     if w.variant == "kivi":
         return "kivi_decode_kernel", ("kvq_decode_kivi.cu", "kvq_kivi.cuh", "kvq_device.cuh")
-    if w.variant == "kitty" and 2 <= g <= 4:
+    if w.variant == "kitty" and gqa:
         return "kitty_decode_gqa_kernel", ("kvq_decode_kitty_gqa.cu", "kvq_kitty.cuh", "kvq_mma.cuh", "kvq_device.cuh")
     if w.variant == "kitty":
         return "kitty_decode_kernel", ("kvq_decode_kitty.cu", "kvq_kitty.cuh", "kvq_device.cuh")
@@ -762,10 +763,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10],
                     help="3 (default: the headline line, the largest single-GPU workload); 1, 2, 4, 5 are the "
-                         "other synthetic workloads, 6-9 the variants (token-granular INT8, KIVI-4, paged KIVI, "
-                         "KIVI-4 grouped-query)")
+                         "other synthetic workloads, 6-10 the variants (token-granular INT8, KIVI-4, paged KIVI, "
+                         "KIVI-4 grouped-query, 64q/8kv grouped-query)")
     ap.add_argument("--score-mode", type=int, default=0, choices=[0, 1],
                     help="Kitty boost selection of workload 4: 0 = Eq. 2 sum of |x|, 1 = variance")
     ap.add_argument("--only", action="store_true",

@@ -67,7 +67,10 @@ kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_se
     const bool kivi = variant == KVQ_VARIANT_KIVI || variant == KVQ_VARIANT_KIVI_PAGED;
     const bool kv_units = int8 || (kivi && kivi_gqa_supported(cfg)) ||
                           (variant == KVQ_VARIANT_KITTY && kitty_gqa_supported(cfg));
-    const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads : rows;
+    const int vsub = kivi && kivi_gqa_supported(cfg)                               ? kivi_gqa_units_per_kv_head(cfg)
+                     : variant == KVQ_VARIANT_KITTY && kitty_gqa_supported(cfg) ? kitty_gqa_units_per_kv_head(cfg)
+                                                                                : 1;
+    const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads * vsub : rows;
     const int ctas = int8 ? 2 : 4;
     // units per CTA aimed at: fewer, longer units amortize the per-unit merge, more units balance the
     // static round-robin; measured on the MHA decode layer (B32, 32 heads, L4096) 6 beat 8 by 3.5 % and

@@ -290,6 +290,9 @@ cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
     P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + PG - 1) / PG;
     if (P.page_cap < 1) P.page_cap = 1;
     P.max_len = c->max_seq_len;
+    P.vsub = 1;
+    P.gall = cfg->n_q_heads / cfg->n_kv_heads;
+    P.gu = P.gall;
     P.kpb = KVQ_D * PG / 4 + cfg->boost_k * PG / 4 + KVQ_D + 4 * KVQ_D;
     P.vpb = PG * KVQ_D / 4 + 4 * PG;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;

@@ -56,8 +56,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SmemKG &S = *reinterpret_cast<SmemKG *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = P.Hq / P.Hkv;
-    const int n_units = P.B * P.Hkv * P.splits;
+    // query heads per kv head (P.gall) and per unit (P.gu), units per batch row and split (Hkv vsub):
+    // kernel parameters, read where used (no registers held across the tile loop)
+    const int n_units = P.B * P.Hkv * P.vsub * P.splits;
     const int K = P.K;
     const int n_hk = (K + 15) >> 4;               // high-plane k-steps
 
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kitty_produce<KQ_NSTAGE, true>(P, P.Hkv, S.stage, S.full, S.empty, &S.abort_flag);
+        if (lane == 0) kitty_produce<KQ_NSTAGE, true>(P, P.Hkv * P.vsub, S.stage, S.full, S.empty, &S.abort_flag);
         return;
     }
 
@@ -92,14 +93,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit U = unit_of<true>(P, u, P.Hkv);     // U.hq is the kv head
+        const Unit U = unit_of<true>(P, u, P.Hkv * P.vsub);
+        // first query row of the unit (recomputed where used: fewer live registers in the tile loop)
+        auto hrow0 = [&]() { return (int64_t)U.b * P.Hq + (int64_t)(U.kvh * P.gall + U.sub * P.gu); };
         // ---- per-unit query tables: warp w prepares head w ----
         {
             const int h = warp;
             const int c0 = 16 * (lane & 7) + 2 * (lane >> 3);
             float qv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (h < g) {
-                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+            if (h < P.gu) {
+                const uint16_t *qrow = P.q + (hrow0() + h) * KVQ_D;
                 const uint32_t q01 = *reinterpret_cast<const uint32_t *>(qrow + c0);
                 const uint32_t q89 = *reinterpret_cast<const uint32_t *>(qrow + c0 + 8);
                 qv[0] = h2f(lo16(q01)) * P.alpha;
@@ -135,9 +138,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
 
         if (U.residual) {
-            for (int h = 0; h < g; ++h) {
+            for (int h = 0; h < P.gu; ++h) {
                 if (warp == 0) {
-                    const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+                    const uint16_t *qrow = P.q + (hrow0() + h) * KVQ_D;
                     const uint2 qr = *reinterpret_cast<const uint2 *>(qrow + 4 * lane);
                     *reinterpret_cast<float4 *>(&S.qv[4 * lane]) =
                         make_float4(h2f(lo16(qr.x)) * P.alpha, h2f(hi16(qr.x)) * P.alpha, h2f(lo16(qr.y)) * P.alpha,
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
         // ---- warp w merges head w over the four warp states, writes (o_s, lse_s) ----
-        if (warp < g) {
+        if (warp < P.gu) {
             const int h = warp;
             float M = -INFINITY;
 #pragma unroll
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                     o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
                 }
             }
-            const int64_t row = (((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h)) * P.splits + U.split;
+            const int64_t row = (hrow0() + h) * P.splits + U.split;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
                 make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
@@ -380,9 +383,15 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     }
 }
 
+// 2 <= g <= 4 heads per kv head in one unit, or an even g <= 8 in two units of g / 2 heads
+int kitty_gqa_units_per_kv_head(const kvq_config *cfg) {
+    const int g = cfg->n_q_heads / cfg->n_kv_heads;
+    return g > KG_MAX ? 2 : 1;
+}
+
 bool kitty_gqa_supported(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;
-    return g >= 2 && g <= KG_MAX;
+    return g >= 2 && (g <= KG_MAX || (g <= 2 * KG_MAX && g % 2 == 0));
 }
 
 cudaError_t launch_decode_kitty_gqa(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,
@@ -422,7 +431,10 @@ cudaError_t launch_decode_kitty_gqa(const kvq_config *cfg, const kvq_kitty_cache
     const size_t smem = sizeof(SmemKG);
     static std::atomic<uint64_t> attr_done{0};
     if (cudaError_t e = smem_opt_in(kitty_decode_gqa_kernel, smem, attr_done)) return e;
-    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * p.splits;
+    P.vsub = kitty_gqa_units_per_kv_head(cfg);
+    P.gall = cfg->n_q_heads / cfg->n_kv_heads;
+    P.gu = P.gall / P.vsub;
+    const int64_t n_units = (int64_t)c->batch * cfg->n_kv_heads * P.vsub * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
     kitty_decode_gqa_kernel<<<(unsigned)grid, 32 * (NCWARP + 1), smem, st>>>(P);

@@ -82,8 +82,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SmemG<BK, BV, NST> &S = *reinterpret_cast<SmemG<BK, BV, NST> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = P.Hq / P.Hkv;
-    const int n_units = P.B * P.Hkv * P.splits;
+    // query heads per kv head (P.gall) and per unit (P.gu), units per batch row and split (Hkv vsub):
+    // kernel parameters, read where used (no registers held across the tile loop)
+    const int n_units = P.B * P.Hkv * P.vsub * P.splits;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < GQ_NSTAGE; ++i) {
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     __syncthreads();
 
     if (warp == NCWARP) {
-        if (lane == 0) kivi_produce<GQ_NSTAGE, true, BK, BV>(P, P.Hkv, S.stage, S.full, S.empty, &S.abort_flag);
+        if (lane == 0) kivi_produce<GQ_NSTAGE, true, BK, BV>(P, P.Hkv * P.vsub, S.stage, S.full, S.empty, &S.abort_flag);
         return;
     }
 
@@ -116,14 +117,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     bool ok = true;
     int sg = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit U = unit_of<true>(P, u, P.Hkv);     // U.hq is the kv head
+        const Unit U = unit_of<true>(P, u, P.Hkv * P.vsub);
+        // first query row of the unit (recomputed where used: fewer live registers in the tile loop)
+        auto hrow0 = [&]() { return (int64_t)U.b * P.Hq + (int64_t)(U.kvh * P.gall + U.sub * P.gu); };
         // ---- per-unit query tables: warp w prepares head w ----
         {
             const int h = warp;
             const int c0 = 16 * (lane & 7) + 2 * (lane >> 3);   // entries 4*lane..4*lane+3
             float qv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (h < g) {
-                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+            if (h < P.gu) {
+                const uint16_t *qrow = P.q + (hrow0() + h) * KVQ_D;
                 const uint32_t q01 = *reinterpret_cast<const uint32_t *>(qrow + c0);
                 const uint32_t q89 = *reinterpret_cast<const uint32_t *>(qrow + c0 + 8);
                 qv[0] = h2f(lo16(q01)) * P.alpha;
@@ -157,8 +160,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
 
         if (U.residual) {
-            for (int h = 0; h < g; ++h) {
-                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h) * KVQ_D;
+            for (int h = 0; h < P.gu; ++h) {
+                const uint16_t *qrow = P.q + (hrow0() + h) * KVQ_D;
                 const uint2 qr = *reinterpret_cast<const uint2 *>(qrow + 4 * lane);
                 const float qa[4] = {h2f(lo16(qr.x)) * P.alpha, h2f(hi16(qr.x)) * P.alpha, h2f(lo16(qr.y)) * P.alpha,
                                      h2f(hi16(qr.y)) * P.alpha};
@@ -195,18 +198,25 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     {
                         // BK = 4: plane 0 holds tokens p = 0, 1, plane 1 tokens p = 2, 3, a nibble each
                         const uint8_t *kt = st + warp * 512 * BK;
-                        const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
-                        const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
-                        const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                        uint32_t kw1[8];
+                        // plane-0 key words: at 2 bits loaded per k-step pair where used, at 4 bits all up front
+                        // (each measured faster for its width: register pressure differs)
+                        uint4 ka = make_uint4(0u, 0u, 0u, 0u), kb = make_uint4(0u, 0u, 0u, 0u);
                         if (BK == 4) {
-                            const uint4 kc = *reinterpret_cast<const uint4 *>(kt + 1024 + lane * 16);
-                            const uint4 kd = *reinterpret_cast<const uint4 *>(kt + 1536 + lane * 16);
-                            kw1[0] = kc.x; kw1[1] = kc.y; kw1[2] = kc.z; kw1[3] = kc.w;
-                            kw1[4] = kd.x; kw1[5] = kd.y; kw1[6] = kd.z; kw1[7] = kd.w;
+                            ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
+                            kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
                         }
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
+                            uint2 kw0;
+                            if (BK == 4)
+                                kw0 = i == 0 ? make_uint2(ka.x, ka.y) : i == 1 ? make_uint2(ka.z, ka.w)
+                                    : i == 2 ? make_uint2(kb.x, kb.y) : make_uint2(kb.z, kb.w);
+                            else
+                                kw0 = *reinterpret_cast<const uint2 *>(kt + 512 * (i >> 1) + lane * 16 + 8 * (i & 1));
+                            // BK = 4: the plane-1 words of k-steps 2i, 2i+1, loaded where used (registers)
+                            uint2 kw1 = make_uint2(0u, 0u);
+                            if (BK == 4)
+                                kw1 = *reinterpret_cast<const uint2 *>(kt + 1024 + 512 * (i >> 1) + lane * 16 + 8 * (i & 1));
                             const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
                             const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
                             const uint4 sv = *reinterpret_cast<const uint4 *>(ksz + (4 * i + r) * 8);
@@ -233,8 +243,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                                                     split_prod(a.z, l.z, sv.z, xB), split_prod(a.w, l.w, sv.w, xB)};
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
-                                const int k = 2 * i + kk;
-                                const uint32_t w = kw[k], w4 = kw[k] >> 4;
+                                const uint32_t w = kk ? kw0.y : kw0.x, w4 = w >> 4;
                                 uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
                                 if (BK == 2) {
                                     e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
@@ -245,8 +254,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                                     // a nibble in bits 0-3 is the e4m3 pattern of code * 2^-9 (exact, linear)
                                     e4m3x4_f16x2(w & 0x0F0F0F0Fu, a0l, a0h);
                                     e4m3x4_f16x2(w4 & 0x0F0F0F0Fu, a1l, a1h);
-                                    e4m3x4_f16x2(kw1[k] & 0x0F0F0F0Fu, a2l, a2h);
-                                    e4m3x4_f16x2((kw1[k] >> 4) & 0x0F0F0F0Fu, a3l, a3h);
+                                    const uint32_t w1 = kk ? kw1.y : kw1.x;
+                                    e4m3x4_f16x2(w1 & 0x0F0F0F0Fu, a2l, a2h);
+                                    e4m3x4_f16x2((w1 >> 4) & 0x0F0F0F0Fu, a3l, a3h);
                                 }
                                 mma16816(s0, a0l, a1l, a0h, a1h, bk[2 * kk], bk[2 * kk + 1]);
                                 mma16816(s1, a2l, a3l, a2h, a3h, bk[2 * kk], bk[2 * kk + 1]);
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
         // ---- warp w merges head w over the four warp states, writes (o_s, lse_s) ----
-        if (warp < g) {
+        if (warp < P.gu) {
             const int h = warp;
             float M = -INFINITY;
 #pragma unroll
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
                 }
             }
-            const int64_t row = (((int64_t)U.b * P.Hq + (int64_t)U.hq * g + h)) * P.splits + U.split;
+            const int64_t row = (hrow0() + h) * P.splits + U.split;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             *reinterpret_cast<float4 *>(P.ws_o + row * KVQ_D + 4 * lane) =
                 make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
@@ -466,11 +476,19 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     }
 }
 
+
+// 2 <= g <= 4 heads per kv head in one unit, or an even g <= 8 in two units of g / 2 heads (the second
+// unit of a kv head reads the same stages, mostly from L2: its units are neighbours in the unit order);
 // any value group at 2/2 bits; with a 4-bit width the value group must be 32 channels (other
 // 4-bit configurations run on the per-head kernel)
+int kivi_gqa_units_per_kv_head(const kvq_config *cfg) {
+    const int g = cfg->n_q_heads / cfg->n_kv_heads;
+    return g > GMAX ? 2 : 1;
+}
+
 bool kivi_gqa_supported(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;
-    if (g < 2 || g > GMAX) return false;
+    if (g < 2 || g > 2 * GMAX || (g > GMAX && g % 2 != 0)) return false;
     if (cfg->bits_k == 2 && cfg->bits_v == 2) return true;
     return cfg->group_v == 32;
 }
@@ -488,7 +506,9 @@ cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, cons
                                    void *ws, cudaStream_t st) {
     Params P = kivi_params(cfg, c, q, p, ws);
     if (!P.err) return cudaErrorInvalidDevicePointer;
-    const int64_t n_units = (int64_t)c.batch * cfg->n_kv_heads * p.splits;
+    P.vsub = kivi_gqa_units_per_kv_head(cfg);
+    P.gu = P.gall / P.vsub;
+    const int64_t n_units = (int64_t)c.batch * cfg->n_kv_heads * P.vsub * p.splits;
     int64_t grid = (int64_t)num_sms() * 4;
     if (grid > n_units) grid = n_units;
     const int ngv = P.ngv;

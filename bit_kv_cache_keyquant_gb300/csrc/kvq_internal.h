@@ -119,10 +119,12 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const KiviSrc &c, const vo
                                const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query KIVI decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
 bool kivi_gqa_supported(const kvq_config *cfg);
+int kivi_gqa_units_per_kv_head(const kvq_config *cfg);   // 1, or 2 for 4 < g <= 8
 cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, const void *q,
                                    const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query Kitty decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
 bool kitty_gqa_supported(const kvq_config *cfg);
+int kitty_gqa_units_per_kv_head(const kvq_config *cfg);
 cudaError_t launch_decode_kitty_gqa(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,
                                     const DecodePlan &p, void *ws, cudaStream_t st);
 cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c, const void *q,

@@ -24,6 +24,8 @@ struct Params {
     unsigned *err;
     int B, Hq, Hkv, S, R, K, splits, chunk, page_cap;
     int max_len;        // max_seq_len: seq_len[b] is read clamped into [0, max_len]
+    int vsub;           // grouped-query units per kv head (each takes Hq / Hkv / vsub query heads)
+    int gall, gu;       // query heads per kv head; per grouped-query unit (gall / vsub)
     int kpb, vpb;
     float alpha;
     int e0;
@@ -34,7 +36,7 @@ struct Params {
 };
 
 struct Unit {
-    int b, hq, kvh, split, p0, np, nKp, nVp, nkb, nvb, L;
+    int b, hq, kvh, sub, split, p0, np, nKp, nVp, nkb, nvb, L;
     bool residual;
     int64_t bk;
 };
@@ -80,7 +82,9 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
         U.p0 = U.split * cpp;
         U.np = max(0, min(U.p0 + cpp, Pf) - U.p0);
     }
-    U.kvh = hpr == P.Hkv ? U.hq : U.hq / (P.Hq / P.Hkv);
+    const int upk = hpr / P.Hkv;                       // units per kv head: Hq / Hkv, or vsub
+    U.kvh = U.hq / upk;
+    U.sub = U.hq - U.kvh * upk;
     U.bk = (int64_t)U.b * P.Hkv + U.kvh;
     return U;
 }

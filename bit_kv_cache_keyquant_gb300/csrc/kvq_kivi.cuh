@@ -43,6 +43,8 @@ struct Params {
     unsigned *err;
     int B, Hq, Hkv, G, Gv, R, splits, chunk;
     int ngv;            // D / Gv: value (s, z) pairs per token
+    int vsub;           // grouped-query units per kv head (each takes Hq / Hkv / vsub query heads)
+    int gall, gu;       // query heads per kv head; per grouped-query unit (gall / vsub)
     int max_len;        // max_seq_len: seq_len[b] is read clamped into [0, max_len]
     int64_t cap;        // token capacity per (b, kvh): max_seq_len rounded up to 128
     int64_t kgrp_cap;   // cap / G
@@ -73,13 +75,14 @@ struct Params {
 // covers every remaining token [Qf, L) (the fp16 residual and any tokens cut
 // off by a segment boundary), read straight from global memory.
 struct Unit {
-    int b, hq, kvh, split, t0, t1, nT, nstages, nKq, nVq;
+    int b, hq, kvh, sub, split, t0, t1, nT, nstages, nKq, nVq;
     bool residual;
     int64_t bk;
 };
 
 // hpr = units per batch row and split: P.Hq (one query head per unit) or
-// P.Hkv (all query heads of a kv head per unit; hq is then the kv head).
+// P.Hkv * P.vsub (a kv head's query heads in vsub units; hq then indexes
+// (kv head, sub)).
 // Units are numbered row-major (u = row * splits + split) or, for the long
 // units of the grouped-query kernels, split-major (u = split * rows + row),
 // which gives every CTA's round-robin share a mix of all splits (measured:
@@ -115,7 +118,9 @@ __device__ __forceinline__ Unit unit_of(const Params &P, int u, int hpr) {
         U.nT = (U.t1 - U.t0) / 32;
     }
     U.nstages = (U.nT + NCWARP - 1) / NCWARP;
-    U.kvh = hpr == P.Hkv ? U.hq : U.hq / (P.Hq / P.Hkv);
+    const int upk = hpr / P.Hkv;                       // units per kv head: Hq / Hkv, or vsub
+    U.kvh = U.hq / upk;
+    U.sub = U.hq - U.kvh * upk;
     U.bk = (int64_t)U.b * P.Hkv + U.kvh;
     return U;
 }
@@ -376,6 +381,9 @@ inline Params kivi_params(const kvq_config *cfg, const KiviSrc &c, const void *q
     P.G = cfg->group_k;
     P.Gv = cfg->group_v;
     P.ngv = KVQ_D / cfg->group_v;
+    P.vsub = 1;
+    P.gall = cfg->n_q_heads / cfg->n_kv_heads;
+    P.gu = P.gall;
     P.R = cfg->residual;
     P.max_len = c.max_seq_len;
     P.cap = ((int64_t)c.max_seq_len + 127) / 128 * 128;

@@ -84,6 +84,8 @@ WORKLOADS = {
     8: Workload(8, "paged KIVI Llama-2-7B-shaped MHA B32 H32 L4096", 32, 32, 32, 4096, "kivi", paged=True),
     9: Workload(9, "KIVI-4 Llama-3-8B-shaped GQA B64 32q/8kv L32768", 64, 32, 8, 32768, "kivi",
                 outlier_channels=1, outlier_gain=15.0, bits_k=4, bits_v=4),
+    10: Workload(10, "Llama-3-70B-shaped GQA B64 64q/8kv L32768", 64, 64, 8, 32768, "kivi",
+                 outlier_channels=1, outlier_gain=15.0),
 }
 
 

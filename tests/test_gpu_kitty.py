@@ -56,7 +56,9 @@ def _oracle(orc, cfg, Ks, Vs, q, score_mode=0):
     ([1300], 92, 0, 4, 2),          # the largest supported boost
     ([800, 1900], 16, 0, 6, 2),     # three heads per kv head (one dead tensor-core column pair)
     ([600, 1400], 16, 0, 2, 2),     # one head per kv head: per-head kernel
-    ([1234], 16, 0, 8, 1),          # eight heads per kv head: per-head kernel
+    ([1234], 16, 0, 8, 1),          # eight heads per kv head: two grouped-query units per kv head
+    ([1500], 16, 0, 12, 2),         # six heads per kv head
+    ([900], 16, 0, 64, 8),          # 64q/8kv
 ])
 def test_kitty_decode_parity(K, orc, lens, Kb, mode, Hq, Hkv):
     rng = np.random.default_rng(sum(lens) + Kb + mode + Hq)

@@ -118,8 +118,10 @@ def _oracle_decode(orc, cfg, Ks, Vs, q):
     (3, 6, 2, [97, 1024, 1333], 32, 32, 128),
     (2, 4, 2, [700, 1900], 32, 64, 64),
     (1, 8, 4, [1025], 64, 128, 128),
-    # more than 4 query heads per kv head: per-head kernel
+    # 8 and 6 query heads per kv head: two grouped-query units per kv head (64q/8kv: Llama-3-70B-shaped)
     (1, 8, 1, [1200], 32, 32, 128),
+    (2, 12, 2, [700, 1900], 32, 32, 128),
+    (1, 64, 8, [1100], 32, 32, 128),
 ])
 def test_decode_parity_small(K, orc, shape):
     B, Hq, Hkv, lens, G, Gv, R = shape
