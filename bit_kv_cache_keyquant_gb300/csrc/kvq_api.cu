@@ -398,7 +398,7 @@ extern "C" kvq_status kv_release_int8_token(const kvq_int8_token_cache *c, int32
 
 extern "C" size_t kvq_kitty_key_page_bytes(const kvq_config *cfg) {
     if (check_kitty(cfg)) return 0;
-    return (size_t)KVQ_D * cfg->group_k / 4 + (size_t)cfg->boost_k * cfg->group_k / 4 + KVQ_D + 4 * KVQ_D;
+    return (size_t)kitty_key_page_bytes(cfg->boost_k);   // group_k = 128 (check_kitty)
 }
 
 extern "C" size_t kvq_kitty_value_page_bytes(const kvq_config *cfg) {

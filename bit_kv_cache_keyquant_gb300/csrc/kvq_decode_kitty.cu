@@ -13,12 +13,12 @@
 // (batch row, query head, split) units; a producer warp streams one page
 // (key record + value record, 9856 B at K = 16) per stage with
 // cp.async.bulk into a 4-slot mbarrier ring; four consumer warps each take
-// 32 tokens of the page.  A key tile gathers, for each lane, the bytes of
-// its 32 channels x 4 tokens from the row-major low plane into packed
-// words, plus one word from the high plane (4 boosted rows, weights 4 q s),
-// and runs the exact fp32 denormal-code x fma.rn.f32x2 dot of the KIVI
-// kernel.  Values use the exact fp32 token-major path (value_token_accum)
-// with one (s, z) per token.
+// 32 tokens of the page.  The low plane is stored in the KIVI key-tile order,
+// so lane 4q + r finds its 32 channels (16k + 2r + {0, 1, 8, 9}) x 4 tokens
+// (q + 8p) in two 16-byte chunks, and one word per 16 boosted rows (rows
+// 16kh + 4r + {0..3}, weights 4 q s) in the high plane; the dot is the exact
+// fp32 denormal-code x fma.rn.f32x2 form.  Values use the exact fp32
+// token-major path (value_token_accum) with one (s, z) per token.
 // The last split of every row covers every token outside whole pages of
 // both sides (sink, buffers, local window, a key page whose values are
 // still in fp16): one token per lane for the keys (per-lane independent
@@ -116,7 +116,20 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_kernel(Para
                 S.st_l[warp] = l_w;
             }
         } else {
-            const float qp[4] = {qa[0] * pe, qa[1] * po, qa[2] * pe, qa[3] * po};
+            // lane = 8r + k writes the weights of channels c0 + {0, 1, 8, 9} = 16k + 2r + {0, 1, 8, 9}
+            // (row r, word k of the table), pre-scaled by the byte-parity power of two
+            const int c0 = 16 * (lane & 7) + 2 * (lane >> 3);
+            float qf[4];
+            {
+                const uint16_t *qrow = P.q + ((int64_t)U.b * P.Hq + U.hq) * KVQ_D;
+                const uint32_t q01 = *reinterpret_cast<const uint32_t *>(qrow + c0);
+                const uint32_t q89 = *reinterpret_cast<const uint32_t *>(qrow + c0 + 8);
+                qf[0] = h2f(lo16(q01)) * P.alpha;
+                qf[1] = h2f(hi16(q01)) * P.alpha;
+                qf[2] = h2f(lo16(q89)) * P.alpha;
+                qf[3] = h2f(hi16(q89)) * P.alpha;
+            }
+            const float qp[4] = {qf[0] * pe, qf[1] * po, qf[2] * pe, qf[3] * po};
             float m_run = -INFINITY, l_part = 0.f, vbias = 0.f;
             unsigned long long vacc2[16];
 #pragma unroll
@@ -126,37 +139,45 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                 ok = consumer_stage_wait(&S.full[slot], (sg / NSTAGE) & 1, P.err, KVQ_SPIN_LIMIT, ok, &S.abort_flag);
                 if (ok) {
                     const uint8_t *st = S.stage[slot];
-                    const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + K * PG / 4;
+                    const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + kitty_high_rows(K) * PG / 4;
                     const uint16_t *ps = reinterpret_cast<const uint16_t *>(idx + KVQ_D);
-                    // ---- pre-scaled weights of the page: low plane (channel order) and boosted rows ----
+                    // ---- pre-scaled weights of the page: low plane (table order) and boosted rows ----
                     {
-                        const uint2 s4 = *reinterpret_cast<const uint2 *>(ps + 4 * lane);
-                        const float sv[4] = {h2f(lo16(s4.x)), h2f(hi16(s4.x)), h2f(lo16(s4.y)), h2f(hi16(s4.y))};
+                        const uint32_t s01 = *reinterpret_cast<const uint32_t *>(ps + c0);
+                        const uint32_t s89 = *reinterpret_cast<const uint32_t *>(ps + c0 + 8);
+                        const float sv[4] = {h2f(lo16(s01)), h2f(hi16(s01)), h2f(lo16(s89)), h2f(hi16(s89))};
                         *reinterpret_cast<float4 *>(&S.qk[warp][(lane >> 3) * QK_ROW + 4 * (lane & 7)]) =
                             make_float4(qp[0] * sv[0], qp[1] * sv[1], qp[2] * sv[2], qp[3] * sv[3]);
-                        const uint32_t id4 = *reinterpret_cast<const uint32_t *>(idx + 4 * lane);
+                        const uint32_t i01 = *reinterpret_cast<const uint16_t *>(idx + c0);
+                        const uint32_t i89 = *reinterpret_cast<const uint16_t *>(idx + c0 + 8);
+                        const uint32_t id4 = i01 | (i89 << 16);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int r = (id4 >> (8 * i)) & 0xFF;
-                            // boosted row r sits at byte r & 3 of its gathered word: parity r & 1
-                            if (r < K) S.hw[warp][r] = 4.f * qa[i] * sv[i] * ((r & 1) ? po : pe);
+                            // boosted row r sits at byte r & 3 of its word: parity r & 1
+                            if (r < K) S.hw[warp][r] = 4.f * qf[i] * sv[i] * ((r & 1) ? po : pe);
                         }
                         for (int r = K + lane; r < n_hgrp * 16; r += 32) S.hw[warp][r] = 0.f;   // rows past K
                     }
-                    const float cb = warp_sum(qa[0] * h2f(ps[KVQ_D + 4 * lane]) + qa[1] * h2f(ps[KVQ_D + 4 * lane + 1]) +
-                                              qa[2] * h2f(ps[KVQ_D + 4 * lane + 2]) +
-                                              qa[3] * h2f(ps[KVQ_D + 4 * lane + 3]));
+                    const uint32_t z01 = *reinterpret_cast<const uint32_t *>(ps + KVQ_D + c0);
+                    const uint32_t z89 = *reinterpret_cast<const uint32_t *>(ps + KVQ_D + c0 + 8);
+                    const float cb = warp_sum(qf[0] * h2f(lo16(z01)) + qf[1] * h2f(hi16(z01)) + qf[2] * h2f(lo16(z89)) +
+                                              qf[3] * h2f(hi16(z89)));
                     __syncwarp();
-                    // ---- key dot: tokens 32*warp + 4*qd + j, channels 32*tq .. 32*tq+31 ----
-                    const int col = 8 * warp + qd;                  // byte column of the token quad
+                    // ---- key dot: tokens q + 8j (q = lane / 4), channels 16k + 2tq + {0, 1, 8, 9} ----
+                    uint32_t kw[8];
+                    {
+                        const uint8_t *kt = low + warp * 1024;
+                        const uint4 ka = *reinterpret_cast<const uint4 *>(kt + lane * 16);
+                        const uint4 kb = *reinterpret_cast<const uint4 *>(kt + 512 + lane * 16);
+                        kw[0] = ka.x; kw[1] = ka.y; kw[2] = ka.z; kw[3] = ka.w;
+                        kw[4] = kb.x; kw[5] = kb.y; kw[6] = kb.z; kw[7] = kb.w;
+                    }
                     const float4 *qs = reinterpret_cast<const float4 *>(&S.qk[warp][tq * QK_ROW]);
                     unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const int c0 = 32 * tq + 4 * k;
-                        const uint32_t w = (uint32_t)low[(c0 + 0) * 32 + col] | ((uint32_t)low[(c0 + 1) * 32 + col] << 8) |
-                                           ((uint32_t)low[(c0 + 2) * 32 + col] << 16) |
-                                           ((uint32_t)low[(c0 + 3) * 32 + col] << 24);
+                        const uint32_t w = kw[k];
                         const float4 qv = qs[k];
                         const uint32_t w16 = w >> 16;
                         const unsigned long long q01 = pack2f(qv.x, qv.y), q23 = pack2f(qv.z, qv.w);
@@ -167,13 +188,12 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
                             acc2[j] = ffma2(pack2u(w16 & m0, w16 & m1), q23, acc2[j]);
                         }
                     }
-                    // boosted rows 16*hg + 4*tq + b (b = 0..3): weights 4 alpha q s, zero past K
+                    // boosted rows 16hg + 4tq + b (b = 0..3) of this warp's tile block: weights 4 alpha q s,
+                    // zero past K (a word past the plane's rows holds finite bytes of the stage)
+                    const uint8_t *hb = high + warp * 8 * kitty_high_rows(K) + tq * 32 + qd * 4;
                     for (int hg = 0; hg < n_hgrp; ++hg) {
                         const int r0 = 16 * hg + 4 * tq;
-                        uint32_t w = 0;
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            if (r0 + b < K) w |= (uint32_t)high[(r0 + b) * 32 + col] << (8 * b);
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(hb + hg * 128);
                         const uint32_t w16 = w >> 16;
                         const unsigned long long q01 = pack2f(S.hw[warp][r0], S.hw[warp][r0 + 1]);
                         const unsigned long long q23 = pack2f(S.hw[warp][r0 + 2], S.hw[warp][r0 + 3]);
@@ -204,7 +224,7 @@ for (int i = 0; i < 16; ++i) vacc2[i] = 0ull;
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const int tau = 8 * r + ts;
-                        const float pt = __shfl_sync(0xFFFFFFFFu, p, tau);
+                        const float pt = __shfl_sync(0xFFFFFFFFu, p, 4 * ts + r);   // lane 4q + tq holds token q + 8tq
                         vbias += pt * h2f(vs[PG + tau]);
                         value_token_accum(*reinterpret_cast<const uint2 *>(vc + tau * (KVQ_D / 4) + jg * 8), pt * h2f(vs[tau]), vacc2);
                     }
@@ -293,7 +313,7 @@ cudaError_t launch_decode_kitty(const kvq_config *cfg, const kvq_kitty_cache *c,
     P.vsub = 1;
     P.gall = cfg->n_q_heads / cfg->n_kv_heads;
     P.gu = P.gall;
-    P.kpb = KVQ_D * PG / 4 + cfg->boost_k * PG / 4 + KVQ_D + 4 * KVQ_D;
+    P.kpb = (int)kitty_key_page_bytes(cfg->boost_k);
     P.vpb = PG * KVQ_D / 4 + 4 * PG;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
     P.e0 = 54 + (int)ceilf(log2f(P.alpha));

@@ -3,18 +3,25 @@
 // the tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation).
 //
 // A page (Kitty, "Page-Centric Memory Layout and Dense-Sparse
-// Decomposition") holds the key low plane [D][G/4] (byte (c, t/4), bits
-// 2(t%4)), the high plane of the K boosted channels, the boost index and a
-// per-channel (s, z); the value page holds token-major codes and a per-token
-// (s, z).  The key code is X = low + 4 high, so
+// Decomposition") holds the key low plane, the high plane of the K boosted
+// channels, the boost index and a per-channel (s, z); the value page holds
+// token-major codes and a per-token (s, z).  The key code is X = low + 4 high,
+// so
 //   logit_ht = sum_c low_tc W_hc + sum_{r<K} high_tr 4 W_h,c(r) + alpha sum_c q_hc z_c
 // with W_hc = alpha q_hc s_c: the dense low plane is eight 16-channel
 // k-steps, the sparse high plane ceil(K/16) more k-steps whose B rows are
 // the boosted channels' weights (dense-sparse decomposition on the tensor
-// cores).  The k-steps gather the low-plane bytes of a lane's token quad
-// from four channel rows; codes become exact fp16 operands through e4m3 bit
-// patterns, weights are fp16 hi / lo pairs (see kvq_mma.cuh), with
-// 2^sigma_h |alpha q| < 1/4 so that 4 W stays in fp16 range.
+// cores).  Both planes are stored in fragment order: the low plane as the
+// KIVI 2-bit key tiles (lane 4q + r finds tokens q + 8p x channels
+// 16k + 2r + {0, 1, 8, 9} of all eight k-steps in two 16-byte chunks), the
+// high plane as one word per lane and 16-row k-step (rows 16kh + 4r + b at
+// byte b; MMA k index 2r + e + 8h is row 4r + e + 2h).  Codes become exact
+// fp16 operands through e4m3 bit patterns, weights are fp16 hi / lo pairs
+// (see kvq_mma.cuh), with 2^sigma_h |alpha q| < 1/4 so that 4 W stays in
+// fp16 range.  The B operands and the zero-point dot depend on the page, not
+// on the tile: the four warps of a page build them once between them (warp
+// w the low k-steps 2w, 2w + 1 and the high k-steps w, w + 4, ...) into a
+// double-buffered shared copy, behind one barrier per page.
 // Values are the per-token 2-bit codes of the KIVI grouped-query kernel with
 // one (s, z) per token.  Tokens outside whole pages are the residual unit,
 // per head on CUDA cores.
@@ -27,7 +34,8 @@ namespace {
 
 constexpr int KQ_NSTAGE = 3;
 constexpr int KG_MAX = 4;                 // query heads per unit
-constexpr int KPB_ROW = 34;               // p exchange row (32 tokens + 2): conflict-free stores
+constexpr int KPB_ROW = 40;               // p exchange row (32 tokens + 8): conflict-free stores
+constexpr int KHK_MAX = (KMAX + 15) / 16;  // high-plane k-steps
 constexpr int KACC_ROW = KVQ_D + 8;
 
 struct SmemKG {
@@ -41,7 +49,14 @@ struct SmemKG {
     float unsig[KG_MAX];                  // 2^-sigma_h
     uint8_t hchan[NCWARP][KMAX + 16];     // channel of boosted row r (per warp copy)
     float pbuf[NCWARP][KG_MAX * KPB_ROW];
-    float st_acc[NCWARP][KG_MAX][KACC_ROW];
+    union {
+        float st_acc[NCWARP][KG_MAX][KACC_ROW];   // warp states at the end of a unit
+        struct {                                  // per page (double-buffered by stage parity)
+            uint4 bk[2][4][32];                   // B words of low k-steps 2i, 2i+1: [buf][i][lane]
+            uint2 bh[2][KHK_MAX][32];             // B words of high k-step hk: [buf][hk][lane]
+            float zp[2][KG_MAX][NCWARP];          // zero-point dot of head h over k-steps 2w, 2w+1: [buf][h][w]
+        } pg;
+    };
     float st_m[NCWARP][KG_MAX];
     float st_l[NCWARP][KG_MAX];
     int abort_flag;                       // raised by a consumer warp whose wait gave up (last: the
@@ -49,6 +64,7 @@ struct SmemKG {
 };
 static_assert(offsetof(SmemKG, qhi) % 16 == 0 && offsetof(SmemKG, qlo) % 16 == 0 && offsetof(SmemKG, st_acc) % 16 == 0,
               "16-byte aligned tables");
+static_assert(sizeof(((SmemKG *)0)->pg) <= sizeof(((SmemKG *)0)->st_acc), "the page area fits the warp states");
 
 }  // namespace
 
@@ -80,12 +96,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     const int q = lane >> 2, r = lane & 3;
     const int hB = q >> 1;
     const bool xB = (q & 1) != 0;
-    const int col = 8 * warp + q;                 // low-plane byte column: tokens 32w + 4q + p, bits 2p
-    // Lanes r >= 2 load the odd channel row of a pair first (rows 4 apart share banks); the
-    // selector puts the byte col%4 of the even row in byte 0 and of the odd row in byte 1 either way.
-    const int rsw = r >> 1;
-    const uint32_t bsel = rsw ? (uint32_t)(4 + (col & 3)) | ((uint32_t)(col & 3) << 4)
-                              : (uint32_t)(col & 3) | ((uint32_t)(4 + (col & 3)) << 4);
     // value unpacking: the lane's byte of each 32-channel block g is byte 8g + q of a token row (channels
     // 32g + 4q + p at bits 2p); vbsel gathers that byte (byte q % 4 of its word) of two rows
     const uint32_t vbsel = (uint32_t)((q & 3) | ((4 + (q & 3)) << 4));
@@ -167,12 +177,36 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
             for (int s = 0; s < U.np; ++s, ++sg) {
                 const int slot = sg % KQ_NSTAGE;
                 ok = consumer_stage_wait(&S.full[slot], (sg / KQ_NSTAGE) & 1, P.err, KVQ_SPIN_LIMIT, ok, &S.abort_flag);
+                const int buf = sg & 1;
+                const uint8_t *st = S.stage[slot];
+                const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + kitty_high_rows(K) * PG / 4;
+                const uint16_t *ks = reinterpret_cast<const uint16_t *>(idx + KVQ_D);   // s [D], then z [D]
                 if (ok) {
-                    const uint8_t *st = S.stage[slot];
-                    const uint8_t *low = st, *high = st + KVQ_D * PG / 4, *idx = high + K * PG / 4;
-                    const uint16_t *ks = reinterpret_cast<const uint16_t *>(idx + KVQ_D);   // s [D], then z [D]
-                    // ---- boosted-row channel table of this page ----
+                    // ---- this warp's share of the page's B operands (column n = q: head hB, part xB) ----
                     {
+                        const int i = warp;                       // low k-steps 2i, 2i + 1
+                        const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
+                        const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
+                        const uint4 qo = *reinterpret_cast<const uint4 *>(qown + 16 * i + 4 * r);
+                        uint32_t sv[4];
+                        float zd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int c0 = 16 * (2 * i + kk) + 2 * r;
+                            sv[2 * kk] = *reinterpret_cast<const uint32_t *>(ks + c0);
+                            sv[2 * kk + 1] = *reinterpret_cast<const uint32_t *>(ks + c0 + 8);
+                            // alpha sum_c q_hc z_c as a product: A = the page's z_c in every row, B = the lane's part
+                            // of alpha q 2^sigma
+                            const uint32_t z01 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0);
+                            const uint32_t z89 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0 + 8);
+                            mma16816(zd, z01, z01, z89, z89, kk ? qo.z : qo.x, kk ? qo.w : qo.y);
+                        }
+                        S.pg.bk[buf][i][lane] = make_uint4(split_prod(a.x, l.x, sv[0], xB), split_prod(a.y, l.y, sv[1], xB),
+                                                           split_prod(a.z, l.z, sv[2], xB), split_prod(a.w, l.w, sv[3], xB));
+                        if (q == 0) S.pg.zp[buf][r][warp] = zd[0] + zd[1];   // head r: hi + lo parts
+                    }
+                    if (warp < n_hk) {
+                        // boosted-row channel table of this page
                         const uint32_t id4 = *reinterpret_cast<const uint32_t *>(idx + 4 * lane);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -180,41 +214,40 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                             if (rr < K) S.hchan[warp][rr] = (uint8_t)(4 * lane + i);
                         }
                         for (int rr = K + lane; rr < 16 * n_hk; rr += 32) S.hchan[warp][rr] = 0xFF;   // rows past K
+                        __syncwarp();
+                        for (int hk = warp; hk < n_hk; hk += NCWARP) {
+                            // rows 16hk + 4r + {0, 1} (first register) and + {2, 3} (second): B = 4 W of their
+                            // channels, 0 past K
+                            const int r0 = 16 * hk + 4 * r;
+                            uint32_t bw[2];
+#pragma unroll
+                            for (int jp = 0; jp < 2; ++jp) {
+                                const int ca = S.hchan[warp][r0 + 2 * jp], cb = S.hchan[warp][r0 + 2 * jp + 1];
+                                const uint32_t ha = ca < KVQ_D ? S.qhl[hB][ca] : 0u, hb = cb < KVQ_D ? S.qhl[hB][cb] : 0u;
+                                const uint32_t sa = ca < KVQ_D ? (uint32_t)ks[ca] : 0u, sb = cb < KVQ_D ? (uint32_t)ks[cb] : 0u;
+                                // 4 W = (4 qhi) s + ...: scaling the query parts by 4 is exact
+                                bw[jp] = split_prod(hmul2(prmt(ha, hb, 0x5410u), 0x44004400u),
+                                                    hmul2(prmt(ha, hb, 0x7632u), 0x44004400u), sa | (sb << 16), xB);
+                            }
+                            S.pg.bh[buf][hk][lane] = make_uint2(bw[0], bw[1]);
+                        }
                     }
-                    __syncwarp();
+                }
+                // every warp at every page, also one whose wait gave up: the page's B operands are complete
+                asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
+                if (ok) {
                     // ---- low plane x W, then the boosted rows x 4W, on the tensor cores ----
                     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-                    // alpha sum_c q_hc z_c as one more product per k-step: A = the page's z_c in every row,
-                    // B = the lane's part of alpha q 2^sigma (two chains)
-                    float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
                     {
-                        const uint32_t *lw = reinterpret_cast<const uint32_t *>(low) + 2 * warp + (q >> 2);
+                        const uint8_t *kt = low + warp * 1024;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const uint4 a = *reinterpret_cast<const uint4 *>(&S.qhi[hB][16 * i + 4 * r]);
-                            const uint4 l = *reinterpret_cast<const uint4 *>(&S.qlo[hB][16 * i + 4 * r]);
-                            uint32_t sv[4];
+                            const uint2 kw = *reinterpret_cast<const uint2 *>(kt + 512 * (i >> 1) + lane * 16 + 8 * (i & 1));
+                            const uint4 b = S.pg.bk[buf][i][lane];
+                            const uint32_t bk[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
-                                const int c0 = 16 * (2 * i + kk) + 2 * r;
-                                sv[2 * kk] = *reinterpret_cast<const uint32_t *>(ks + c0);
-                                sv[2 * kk + 1] = *reinterpret_cast<const uint32_t *>(ks + c0 + 8);
-                            }
-                            const uint32_t bk[4] = {split_prod(a.x, l.x, sv[0], xB), split_prod(a.y, l.y, sv[1], xB),
-                                                    split_prod(a.z, l.z, sv[2], xB), split_prod(a.w, l.w, sv[3], xB)};
-                            const uint4 qo = *reinterpret_cast<const uint4 *>(qown + 16 * i + 4 * r);
-#pragma unroll
-                            for (int kk = 0; kk < 2; ++kk) {
-                                const int c0 = 16 * (2 * i + kk) + 2 * r;
-                                const uint32_t z01 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0);
-                                const uint32_t z89 = *reinterpret_cast<const uint32_t *>(ks + KVQ_D + c0 + 8);
-                                if (i & 1)
-                                    mma16816(z1, z01, z01, z89, z89, kk ? qo.z : qo.x, kk ? qo.w : qo.y);
-                                else
-                                    mma16816(z0, z01, z01, z89, z89, kk ? qo.z : qo.x, kk ? qo.w : qo.y);
-                                const uint32_t x01 = prmt(lw[(c0 + rsw) * 8], lw[(c0 + 1 - rsw) * 8], bsel);
-                                const uint32_t x89 = prmt(lw[(c0 + 8 + rsw) * 8], lw[(c0 + 9 - rsw) * 8], bsel);
-                                const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
+                                const uint32_t w = kk ? kw.y : kw.x, w4 = w >> 4;
                                 uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
                                 e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
                                 e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
@@ -224,41 +257,28 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                                 mma16816(s1, a2l, a3l, a2h, a3h, bk[2 * kk], bk[2 * kk + 1]);
                             }
                         }
-                        // boosted rows 16hk + {2r, 2r+1, 2r+8, 2r+9}: B = 4 W of their channels, 0 past K
-                        const uint32_t *hw = reinterpret_cast<const uint32_t *>(high) + 2 * warp + (q >> 2);
+                        // boosted rows: one word of this warp's tile block per 16-row k-step (a word past the
+                        // plane's rows holds finite bytes of the stage; its B rows are zero)
+                        const uint8_t *hw = high + warp * 8 * kitty_high_rows(K) + r * 32 + q * 4;
                         for (int hk = 0; hk < n_hk; ++hk) {
-                            const int r0 = 16 * hk + 2 * r;
-                            const int rows[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
-                            uint32_t qh2[2], ql2[2], s2[2];
-#pragma unroll
-                            for (int jp = 0; jp < 2; ++jp) {
-                                // rows past K (channel 0xFF) take weight 0
-                                const int ca = S.hchan[warp][rows[2 * jp]], cb = S.hchan[warp][rows[2 * jp + 1]];
-                                const uint32_t ha = ca < KVQ_D ? S.qhl[hB][ca] : 0u, hb = cb < KVQ_D ? S.qhl[hB][cb] : 0u;
-                                const uint32_t sa = ca < KVQ_D ? (uint32_t)ks[ca] : 0u, sb = cb < KVQ_D ? (uint32_t)ks[cb] : 0u;
-                                qh2[jp] = prmt(ha, hb, 0x5410u);
-                                ql2[jp] = prmt(ha, hb, 0x7632u);
-                                s2[jp] = sa | (sb << 16);
-                            }
-                            // 4 W = (4 qhi) s + ...: scaling the query parts by 4 is exact
-                            const uint32_t b0 = split_prod(hmul2(qh2[0], 0x44004400u), hmul2(ql2[0], 0x44004400u), s2[0], xB);
-                            const uint32_t b1 = split_prod(hmul2(qh2[1], 0x44004400u), hmul2(ql2[1], 0x44004400u), s2[1], xB);
-                            // rows past K read finite bytes; their B rows are zero
-                            const uint32_t x01 = prmt(hw[(r0 + rsw) * 8], hw[(r0 + 1 - rsw) * 8], bsel);
-                            const uint32_t x89 = prmt(hw[(r0 + 8 + rsw) * 8], hw[(r0 + 9 - rsw) * 8], bsel);
-                            const uint32_t w = prmt(x01, x89, 0x5410u), w4 = w >> 4;
+                            const uint32_t w = *reinterpret_cast<const uint32_t *>(hw + hk * 128), w4 = w >> 4;
+                            const uint2 b = S.pg.bh[buf][hk][lane];
                             uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
                             e4m3x4_f16x2(w & 0x03030303u, a0l, a0h);
                             e4m3x4_f16x2(w & 0x0C0C0C0Cu, a1l, a1h);
                             e4m3x4_f16x2(w4 & 0x03030303u, a2l, a2h);
                             e4m3x4_f16x2(w4 & 0x0C0C0C0Cu, a3l, a3h);
-                            mma16816(s0, a0l, a1l, a0h, a1h, b0, b1);
-                            mma16816(s1, a2l, a3l, a2h, a3h, b0, b1);
+                            mma16816(s0, a0l, a1l, a0h, a1h, b.x, b.y);
+                            mma16816(s1, a2l, a3l, a2h, a3h, b.x, b.y);
                         }
                     }
-                    // ---- logits of head r, tokens 32w + 4q + p; online softmax ----
+                    // ---- logits of head r, tokens q, q + 8, q + 16, q + 24; online softmax ----
                     const float f9 = unsig * 512.f, f7 = unsig * 128.f;
-                    const float zr = ((z0[0] + z1[0]) + (z0[1] + z1[1])) * unsig;
+                    float zr;
+                    {
+                        const float4 zq = *reinterpret_cast<const float4 *>(S.pg.zp[buf][r]);
+                        zr = ((zq.x + zq.y) + (zq.z + zq.w)) * unsig;
+                    }
                     float lg[4];
                     lg[0] = fmaf(s0[0] + s0[1], f9, zr);
                     lg[1] = fmaf(s0[2] + s0[3], f7, zr);
@@ -282,11 +302,11 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                         pr[i] = ex2_ftz(lg[i] - m_run);
                         l_part += pr[i];
                     }
-                    // token t = 16k + 8hk + 4e + j of the tile sits at position 16k + 8hk + 2j + e
+                    // token 16k + 8hk + 4e + j (k-step k, k-column 2j + e + 8hk of the value products) at
+                    // position 16k + 8hk + 2j + e: each B register's two tokens are adjacent
                     float *pb = S.pbuf[warp];
-                    const int pbase = 16 * (q >> 2) + 8 * ((q >> 1) & 1) + (q & 1);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) pb[r * KPB_ROW + pbase + 2 * i] = pr[i];
+                    for (int i = 0; i < 4; ++i) pb[r * KPB_ROW + 8 * i + 2 * (q & 3) + (q >> 2)] = pr[i];
                     const uint8_t *vrec = st + VREC_OFF;
                     const uint16_t *vs = reinterpret_cast<const uint16_t *>(vrec + PG * KVQ_D / 4) + 32 * warp;
                     __syncwarp();
@@ -335,7 +355,8 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
-            // ---- warp state (head r) -> shared memory ----
+            // ---- warp state (head r) -> shared memory (over the page area: every warp is past its last page) ----
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * NCWARP) : "memory");
             float l_w = l_part;
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 4);
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 8);
@@ -422,7 +443,7 @@ cudaError_t launch_decode_kitty_gqa(const kvq_config *cfg, const kvq_kitty_cache
     P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + PG - 1) / PG;
     if (P.page_cap < 1) P.page_cap = 1;
     P.max_len = c->max_seq_len;
-    P.kpb = KVQ_D * PG / 4 + cfg->boost_k * PG / 4 + KVQ_D + 4 * KVQ_D;
+    P.kpb = (int)kitty_key_page_bytes(cfg->boost_k);
     P.vpb = PG * KVQ_D / 4 + 4 * PG;
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
     P.e0 = 0;

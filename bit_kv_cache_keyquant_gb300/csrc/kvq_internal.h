@@ -57,6 +57,15 @@ inline KiviSrc kivi_src(const kvq_kivi_paged_cache *c) {
     return s;
 }
 
+// Rows of a Kitty key page's high plane: the K boosted channels rounded up to
+// a multiple of 4 (each 4-byte word of the plane holds a group of four rows).
+__host__ __device__ constexpr int kitty_high_rows(int K) { return (K + 3) & ~3; }
+
+// bytes of one Kitty key page record of 128 tokens (D = 128): low plane, high plane, idx [D], s [D], z [D]
+__host__ __device__ constexpr int64_t kitty_key_page_bytes(int K) {
+    return 128LL * 128 / 4 + (int64_t)kitty_high_rows(K) * 128 / 4 + 128 + 4 * 128;
+}
+
 // bytes of one paged KIVI page record: key codes, key (s, z), value codes, value (s, z) of 128 tokens
 inline int64_t kivi_page_bytes(int bits_k, int bits_v) {
     return 16LL * 128 * bits_k + 2048 + 16LL * 128 * bits_v + 2048;   // D = 128

@@ -110,6 +110,19 @@ __device__ __forceinline__ const uint8_t *value_page(const Params &P, const Unit
     return P.v_pages + page_record(P, U, p) * (int64_t)P.vpb;
 }
 
+// Byte of token tt (0..127) of a key page's planes, bit position 2 * ((tt % 32) / 8):
+// the low plane in the KIVI 2-bit key-tile order (channel c = 16k + 2r + e + 8h of
+// token q + 8p of tile j at byte j*1024 + (k/4)*512 + (4q + r)*16 + (k%4)*4 + e + 2h),
+// the high plane in blocks of kp * 8 bytes per 32-token tile (row 16kh + 4rb + b at
+// byte 128kh + 32rb + 4q + b of its tile's block; kp = the plane's rows).
+__device__ __forceinline__ int kitty_low_byte(int tt, int c) {
+    const int q = tt & 7, k = c >> 4, cc = c & 15;
+    return (tt >> 5) * 1024 + (k >> 2) * 512 + (4 * q + ((cc & 7) >> 1)) * 16 + (k & 3) * 4 + (cc & 1) + 2 * (cc >> 3);
+}
+__device__ __forceinline__ int kitty_high_byte(int kp, int tt, int row) {
+    return (tt >> 5) * 8 * kp + (row >> 4) * 128 + ((row & 15) >> 2) * 32 + 4 * (tt & 7) + (row & 3);
+}
+
 // Tokens of one query head outside whole pages (sink, Q-buffers, local
 // window, a key page whose values are still fp16): lane = token for the keys
 // (independent per-lane loads), four channels per lane for the values.
@@ -150,12 +163,13 @@ __device__ __forceinline__ void kitty_residual(const Params &P, const Unit &U, c
         } else {
             const int p = (t - P.S) / PG, tt = (t - P.S) % PG;
             const uint8_t *pg = key_page(P, U, p);
-            const uint8_t *low = pg, *high = pg + KVQ_D * PG / 4, *idx = high + (int64_t)K * PG / 4;
+            const int kp = kitty_high_rows(K), sh = 2 * ((tt & 31) >> 3);
+            const uint8_t *low = pg, *high = pg + KVQ_D * PG / 4, *idx = high + (int64_t)kp * PG / 4;
             const uint16_t *ps = reinterpret_cast<const uint16_t *>(idx + KVQ_D);
             for (int c = 0; c < KVQ_D; ++c) {
-                int code = (low[c * (PG / 4) + tt / 4] >> (2 * (tt & 3))) & 3;
+                int code = (low[kitty_low_byte(tt, c)] >> sh) & 3;
                 const int r = idx[c];
-                if (r < K) code |= ((high[r * (PG / 4) + tt / 4] >> (2 * (tt & 3))) & 3) << 2;
+                if (r < K) code |= ((high[kitty_high_byte(kp, tt, r)] >> sh) & 3) << 2;
                 logit += qv[c] * ((float)code * h2f(ps[c]) + h2f(ps[KVQ_D + c]));
             }
         }

@@ -325,8 +325,37 @@ __device__ __forceinline__ long long abs_units(uint16_t h) {
     return e == 0 ? (long long)m : ((long long)(1024 + m) << (e - 1));
 }
 
+// The codes of channel c of a key page into the shared copy of its planes:
+// for tile j and token quad q, the low bits of tokens 32j + q + 8p (p = 0..3,
+// bits 2p) at byte j*1024 + 64q + pos, and for a boosted channel of rank r
+// the high bits at byte 4096 + j*8Kp + 4q + hpos.  With EXACT false the
+// product form (affine_code_fast); the return value reports a near-tie.
+template <bool EXACT>
+__device__ __forceinline__ bool kitty_channel_codes(const uint16_t *xs, int c, float zf, float sf, float rf, int qmax,
+                                                    uint8_t *cw, int pos, bool boosted, int hpos, int kp8) {
+    bool tie = false;
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float x = h2f(xs[(32 * j + q + 8 * p) * KVQ_D + c]);
+                const uint32_t code = EXACT ? (uint32_t)affine_code(x, zf, sf, rf, qmax)
+                                            : (uint32_t)affine_code_fast(x, zf, rf, tie);
+                lo |= (code & 3u) << (2 * p);
+                hi |= (code >> 2) << (2 * p);
+            }
+            cw[j * 1024 + q * 64 + pos] = (uint8_t)lo;
+            if (boosted) cw[4096 + j * kp8 + q * 4 + hpos] = (uint8_t)hi;
+        }
+    return tie;
+}
+
 // One Kitty key page (G = 128 tokens) by a 128-thread block (thread =
-// channel), staged through `smem` (G*D fp16 plus three D-sized arrays).
+// channel), staged through `smem` (G*D fp16, three D-sized arrays and the
+// planes' bytes, which the block then stores with 16-byte stores).
 __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict__ src, int K, int score_mode,
                                                      uint8_t *__restrict__ pg, uint8_t *smem) {
     constexpr int G = 128;
@@ -334,9 +363,12 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
     long long *si = reinterpret_cast<long long *>(xs + G * KVQ_D);     // [D]
     float *sf = reinterpret_cast<float *>(si + KVQ_D);                 // [D]
     int *boost = reinterpret_cast<int *>(sf + KVQ_D);                   // [D]
+    uint8_t *cw = reinterpret_cast<uint8_t *>(boost + KVQ_D);          // the planes: low 4096 B, high Kp * 32 B
+    const int Kp = kitty_high_rows(K);
     const int c = threadIdx.x;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
     for (int i = c; i < G * KVQ_D / 8; i += 128) reinterpret_cast<uint4 *>(xs)[i] = s4[i];
+    for (int i = c; i < Kp * 8; i += 128) reinterpret_cast<uint32_t *>(cw + 4096)[i] = 0u;   // rows past K stay 0
     __syncthreads();
     long long a = 0;
     float mn = INFINITY, mx = -INFINITY, var = 0.f;
@@ -380,52 +412,28 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
     uint16_t s, z;
     affine_fit(mn, mx, qmax, s, z);
     const float sv = h2f(s), zv = h2f(z), rv = sv != 0.0f ? __frcp_rn(sv) : 0.0f;
-    uint8_t *low = pg;
-    uint8_t *high = pg + KVQ_D * G / 4;
-    uint8_t *idx = high + (int64_t)K * G / 4;
+    // channel c = 16k + 2rr + e + 8h: byte (k/4)*512 + 16rr + (k%4)*4 + e + 2h of chunk row 4q + rr (the
+    // KIVI key-tile order); boosted row r = 16kh + 4rb + b: byte 128kh + 32rb + b of a tile's high block
+    const int k = c >> 4, cc = c & 15;
+    const int pos = (k >> 2) * 512 + ((cc & 7) >> 1) * 16 + (k & 3) * 4 + (cc & 1) + 2 * (cc >> 3);
+    const int hpos = (r >> 4) * 128 + ((r & 15) >> 2) * 32 + (r & 3);
+    // the product form; a channel that met a near-tie is coded again with the quotient
+    if (kitty_channel_codes<false>(xs, c, zv, sv, rv, qmax, cw, pos, boosted, hpos, 8 * Kp))
+        kitty_channel_codes<true>(xs, c, zv, sv, rv, qmax, cw, pos, boosted, hpos, 8 * Kp);
+    uint8_t *idx = pg + KVQ_D * G / 4 + (int64_t)Kp * G / 4;
     uint16_t *ps = reinterpret_cast<uint16_t *>(idx + KVQ_D);
-    uint32_t lw[8], hw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { lw[i] = 0; hw[i] = 0; }
-    // word i of the planes holds tokens 16i..16i+15 (indices fixed at compile time: no local memory)
-    bool tie = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint32_t code = (uint32_t)affine_code_fast(h2f(xs[(16 * i + j) * KVQ_D + c]), zv, rv, tie);
-            lw[i] |= (code & 3u) << (2 * j);
-            hw[i] |= ((code >> 2) & 3u) << (2 * j);
-        }
-
-    uint4 *lrow = reinterpret_cast<uint4 *>(low + c * (G / 4));
-    lrow[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    lrow[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-    uint4 *hrow = reinterpret_cast<uint4 *>(high + (int64_t)r * (G / 4));
-    if (boosted) {
-        hrow[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        hrow[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-    }
-    if (tie) {                           // a near-tie: the channel's rows again with the quotient
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-            uint32_t l = 0u, hh = 0u;
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t code = (uint32_t)affine_code(h2f(xs[(16 * i + j) * KVQ_D + c]), zv, sv, rv, qmax);
-                l |= (code & 3u) << (2 * j);
-                hh |= ((code >> 2) & 3u) << (2 * j);
-            }
-            reinterpret_cast<uint32_t *>(lrow)[i] = l;
-            if (boosted) reinterpret_cast<uint32_t *>(hrow)[i] = hh;
-        }
-    }
     idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
     ps[c] = s;
     ps[KVQ_D + c] = z;
     __syncthreads();
+    // both planes (4096 + Kp * 32 bytes, a multiple of 16) with 16-byte stores
+    const uint4 *c4 = reinterpret_cast<const uint4 *>(cw);
+    uint4 *o4 = reinterpret_cast<uint4 *>(pg);
+    for (int i = c; i < (4096 + Kp * 32) / 16; i += 128) o4[i] = c4[i];
+    __syncthreads();
 }
 
-constexpr size_t KITTY_KEY_SMEM = (size_t)128 * KVQ_D * 2 + KVQ_D * (8 + 4 + 4);
+constexpr size_t KITTY_KEY_SMEM = (size_t)128 * KVQ_D * 2 + KVQ_D * (8 + 4 + 4) + 4096 + 128 * 32;
 
 __global__ void __launch_bounds__(128) quant_key_kitty_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
                                                               int K, int score_mode, uint8_t *__restrict__ pages,
@@ -587,7 +595,7 @@ cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t
                                    void *pages, cudaStream_t st) {
     if (n_pages == 0) return cudaSuccess;
     const int G = cfg->group_k, K = cfg->boost_k;
-    const int64_t pb = (int64_t)KVQ_D * G / 4 + (int64_t)K * G / 4 + KVQ_D + 4LL * KVQ_D;
+    const int64_t pb = kitty_key_page_bytes(K);
     const size_t smem = KITTY_KEY_SMEM;
     static std::atomic<uint64_t> attr_done{0};
     if (cudaError_t e = smem_opt_in(quant_key_kitty_kernel, smem, attr_done)) return e;
@@ -1084,7 +1092,7 @@ static KittyPagedDst kitty_paged_dst(const kvq_config *cfg, const kvq_kitty_cach
 
 cudaError_t launch_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_cache *c, const void *k, int64_t n,
                                          int page0, int row, int kvh, int score_mode, cudaStream_t st) {
-    const int64_t kpb = (int64_t)KVQ_D * 128 / 4 + (int64_t)cfg->boost_k * 128 / 4 + KVQ_D + 4LL * KVQ_D;
+    const int64_t kpb = kitty_key_page_bytes(cfg->boost_k);
     const KittyPagedDst D = kitty_paged_dst(cfg, c, c->k_pages, kpb, page0, row, kvh);
     if (!D.err) return cudaErrorInvalidDevicePointer;
     static std::atomic<uint64_t> attr_done{0};
@@ -1229,7 +1237,7 @@ static cudaError_t launch_append_kitty_impl(const kvq_config *cfg, const kvq_kit
     P.max_seq_len = c->max_seq_len;
     P.page_cap = (int)((c->max_seq_len - cfg->sink > 0 ? c->max_seq_len - cfg->sink : 0) + 127) / 128;
     if (P.page_cap < 1) P.page_cap = 1;
-    P.kpb = (int64_t)KVQ_D * 128 / 4 + (int64_t)cfg->boost_k * 128 / 4 + KVQ_D + 4LL * KVQ_D;
+    P.kpb = kitty_key_page_bytes(cfg->boost_k);
     P.vpb = 128LL * KVQ_D / 4 + 4LL * 128;
     static std::atomic<uint64_t> attr_done{0};
     if (cudaError_t e = smem_opt_in(append_kitty_kernel, KITTY_KEY_SMEM, attr_done)) return e;

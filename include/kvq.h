@@ -51,10 +51,18 @@
  *   KIVI value token: D*b/8 bytes for b-bit codes, channel c in bits
  *     b*(c % (8/b)) of byte c/(8/b).  Parameters: fp16x2 (s, z) [D/Gv] per token.
  *   Kitty key page (G = 128 tokens, K boosted channels), one record of
- *     kvq_kitty_key_page_bytes() bytes: low plane [D][G/4] (byte (c, t/4),
- *     bits 2*(t%4), code & 3), high plane [K][G/4] (row r = r-th boosted
- *     channel in ascending channel order, code >> 2), idx uint8 [D] (r, or
- *     K+1 for channels that are not boosted), s fp16 [D], z fp16 [D].
+ *     kvq_kitty_key_page_bytes() bytes: low plane (D*G/4 bytes, code & 3 of
+ *     every channel), high plane (Kp*G/4 bytes, Kp = K rounded up to a
+ *     multiple of 4; row r = r-th boosted channel in ascending channel order,
+ *     code >> 2; rows K..Kp-1 zero), idx uint8 [D] (r, or K+1 for channels
+ *     that are not boosted), s fp16 [D], z fp16 [D].  Both planes are in
+ *     the fragment order of the KIVI key tiles: the low plane is the KIVI
+ *     2-bit key layout above over the page's 128 tokens (token t, channel c
+ *     at bits 2p of byte (t/32)*1024 + (k/4)*512 + (4q + r)*16 + (k%4)*4 +
+ *     (e + 2h)); the high plane gives each 32-token tile t/32 a block of
+ *     Kp*8 bytes, row r = 16kh + 4rb + b of token t = q + 8p (mod 32) at
+ *     bits 2p of byte (t/32)*Kp*8 + kh*128 + 32*rb + 4q + b, so one 4-byte
+ *     word holds four rows at four tokens.
  *   Kitty value page: codes [G][D/4] token-major as above, s fp16 [G],
  *     z fp16 [G].
  *   INT8 cache: codes int8 [tokens][D]; scale fp16 [blocks][D].

@@ -347,7 +347,41 @@ static int tokenmajor_code_at(int bits, const uint8_t *tok_bytes, int c)
 /* Kitty pages                                                          */
 /* ------------------------------------------------------------------ */
 
-ORC_API long orc_kitty_key_page_bytes(int D, int G, int K) { return (long)D * G / 4 + (long)K * G / 4 + D + 4L * D; }
+/* Rows of the high plane: K rounded up to a multiple of 4 (rows K..Kp-1 hold
+ * zero bytes), so that every 4-byte word of the plane belongs to one group of
+ * four rows. */
+ORC_API int orc_kitty_high_rows(int K) { return (K + 3) & ~3; }
+
+ORC_API long orc_kitty_key_page_bytes(int D, int G, int K)
+{
+    return (long)D * G / 4 + (long)orc_kitty_high_rows(K) * G / 4 + D + 4L * D;
+}
+
+/* Storage order of the two code planes of a key page (D = 128, G a multiple
+ * of 32).  The Kitty page (section "Page-Centric Memory Layout and
+ * Dense-Sparse Decomposition") fixes which planes a page holds, not the order
+ * of the bytes inside a plane; this one is a design choice.
+ * Low plane: the page's low code bits (code & 3) of every channel in the
+ * KIVI 2-bit key-tile order (orc_kivi_key_byte_offset): tile t/32 of 1024
+ * bytes, token t % 32 = q + 8p of channel c = 16k + 2r + e + 8h at bits 2p
+ * of byte (k/4)*512 + (4q + r)*16 + (k%4)*4 + e + 2h. */
+ORC_API long orc_kitty_low_byte_offset(int t, int c) { return orc_kivi_key_byte_offset(t, c); }
+
+/* High plane: the high code bits (code >> 2) of the boosted channels, row rho
+ * = the rank of the channel among the boosted ones (ascending channel order).
+ * Each 32-token tile owns a block of Kp * 8 bytes (Kp = orc_kitty_high_rows);
+ * inside it, row rho = 16 kh + 4 r + b and token t % 32 = q + 8p sit at bits
+ * 2p of byte kh*128 + 32 r + 4 q + b.  A 4-byte word thus holds four rows
+ * 4r..4r+3 of a 16-row block at tokens q, q+8, q+16, q+24, and a partial last
+ * block (Kp % 16 rows) is a compact prefix. */
+ORC_API long orc_kitty_high_byte_offset(int K, int t, int rho)
+{
+    int kh = rho / 16, r = (rho % 16) / 4, b = rho % 4, q = (t % 32) % 8;
+    return (long)(t / 32) * orc_kitty_high_rows(K) * 8 + kh * 128 + 32 * r + 4 * q + b;
+}
+
+/* Bit position of token t inside its byte, in both planes. */
+ORC_API int orc_kitty_code_bit(int t) { return 2 * ((t % 32) / 8); }
 ORC_API long orc_kitty_value_page_bytes(int D, int G) { return (long)G * D / 4 + 4L * G; }
 
 /* Eq. 2 channel score, exactly: sum_t |x| in units of 2^-24 (every finite
@@ -408,19 +442,23 @@ ORC_API void orc_kitty_select(int D, int G, int K, int score_mode, const uint16_
 
 /* Quantize one key page: x fp16 [G][D] -> packed record of
  * orc_kitty_key_page_bytes(D, G, K) bytes:
- *   low  [D][G/4]  code & 3, byte (c, t/4), bits 2*(t%4)
- *   high [K][G/4]  code >> 2 of the r-th boosted channel (ascending order)
- *   idx  [D]       r for boosted channels, K + 1 otherwise
+ *   low  D*G/4 bytes   code & 3 of every channel (orc_kitty_low_byte_offset)
+ *   high Kp*G/4 bytes  code >> 2 of the r-th boosted channel (ascending order;
+ *                      orc_kitty_high_byte_offset), Kp = K rounded up to 4
+ *   idx  [D]           r for boosted channels, K + 1 otherwise
  *   s    fp16 [D], z fp16 [D]
- * Boosted channels use 4-bit codes, the rest 2-bit codes. */
+ * Boosted channels use 4-bit codes, the rest 2-bit codes.  D = 128 and G a
+ * multiple of 32 (the plane order); other shapes leave the page zero. */
 ORC_API void orc_kitty_key_page(int D, int G, int K, int score_mode, const uint16_t *x, uint8_t *page)
 {
+    memset(page, 0, (size_t)orc_kitty_key_page_bytes(D, G, K));
+    if (D != 128 || G % 32 != 0)
+        return;
     uint8_t *boosted = (uint8_t *)malloc((size_t)D);
     orc_kitty_select(D, G, K, score_mode, x, boosted);
-    memset(page, 0, (size_t)orc_kitty_key_page_bytes(D, G, K));
     uint8_t *low = page;
     uint8_t *high = page + (long)D * G / 4;
-    uint8_t *idx = high + (long)K * G / 4;
+    uint8_t *idx = high + (long)orc_kitty_high_rows(K) * G / 4;
     uint16_t *s = (uint16_t *)(idx + D);
     uint16_t *z = s + D;
     int r = 0;
@@ -430,9 +468,9 @@ ORC_API void orc_kitty_key_page(int D, int G, int K, int score_mode, const uint1
         idx[c] = boosted[c] ? (uint8_t)r : (uint8_t)(K + 1);
         for (int t = 0; t < G; ++t) {
             int code = orc_affine_code(x[(long)t * D + c], s[c], z[c], bits);
-            low[(long)c * (G / 4) + t / 4] |= (uint8_t)((code & 3) << (2 * (t % 4)));
+            low[orc_kitty_low_byte_offset(t, c)] |= (uint8_t)((code & 3) << orc_kitty_code_bit(t));
             if (boosted[c])
-                high[(long)r * (G / 4) + t / 4] |= (uint8_t)(((code >> 2) & 3) << (2 * (t % 4)));
+                high[orc_kitty_high_byte_offset(K, t, r)] |= (uint8_t)(((code >> 2) & 3) << orc_kitty_code_bit(t));
         }
         if (boosted[c])
             ++r;
@@ -446,19 +484,21 @@ ORC_API void orc_kitty_key_page(int D, int G, int K, int score_mode, const uint1
 ORC_API void orc_kitty_key_page_decode(int D, int G, int K, const uint8_t *page,
                                        uint8_t *codes, uint16_t *s_out, uint16_t *z_out)
 {
+    if (D != 128 || G % 32 != 0)
+        return;
     const uint8_t *low = page;
     const uint8_t *high = page + (long)D * G / 4;
-    const uint8_t *idx = high + (long)K * G / 4;
+    const uint8_t *idx = high + (long)orc_kitty_high_rows(K) * G / 4;
     const uint16_t *s = (const uint16_t *)(idx + D);
     const uint16_t *z = s + D;
     for (int c = 0; c < D; ++c) {
         s_out[c] = s[c];
         z_out[c] = z[c];
         for (int t = 0; t < G; ++t) {
-            int lo = (low[(long)c * (G / 4) + t / 4] >> (2 * (t % 4))) & 3;
+            int lo = (low[orc_kitty_low_byte_offset(t, c)] >> orc_kitty_code_bit(t)) & 3;
             int hi = 0;
             if (idx[c] < K)
-                hi = (high[(long)idx[c] * (G / 4) + t / 4] >> (2 * (t % 4))) & 3;
+                hi = (high[orc_kitty_high_byte_offset(K, t, idx[c])] >> orc_kitty_code_bit(t)) & 3;
             codes[(long)t * D + c] = (uint8_t)(lo | (hi << 2));
         }
     }

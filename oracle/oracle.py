@@ -73,6 +73,10 @@ def _declare(l):
         "orc_kivi_value_codes": (None, [I, I, I, P, L, P, P]),
         "orc_tokenmajor_pack": (None, [I, P, L, P]),
         "orc_kitty_key_page_bytes": (L, [I, I, I]),
+        "orc_kitty_high_rows": (I, [I]),
+        "orc_kitty_low_byte_offset": (L, [I, I]),
+        "orc_kitty_high_byte_offset": (L, [I, I, I]),
+        "orc_kitty_code_bit": (I, [I]),
         "orc_kitty_value_page_bytes": (L, [I, I]),
         "orc_kitty_select": (None, [I, I, I, I, P, P]),
         "orc_kitty_key_page": (None, [I, I, I, I, P, P]),
@@ -208,6 +212,22 @@ def kivi_quant_value(x: np.ndarray, group: int = 32, bits: int = 2):
 # ---------------------------------------------------------------------------
 def kitty_key_page_bytes(D: int, G: int, K: int) -> int:
     return lib().orc_kitty_key_page_bytes(D, G, K)
+
+
+def kitty_high_rows(K: int) -> int:
+    return lib().orc_kitty_high_rows(K)
+
+
+def kitty_low_byte_offset(t: int, c: int) -> int:
+    return lib().orc_kitty_low_byte_offset(t, c)
+
+
+def kitty_high_byte_offset(K: int, t: int, rho: int) -> int:
+    return lib().orc_kitty_high_byte_offset(K, t, rho)
+
+
+def kitty_code_bit(t: int) -> int:
+    return lib().orc_kitty_code_bit(t)
 
 
 def kitty_value_page_bytes(D: int, G: int) -> int:

@@ -68,6 +68,10 @@ def test_kitty_mixed_key_layer(K):
     assert round(total / 1e6, 1) == 1302.8
     cfg_pro = K.make_config(n_q_heads=32, n_kv_heads=8, group_k=128, boost_k=32)
     assert K.kvq_kitty_key_page_bytes(cfg_pro) == 4096 + 32 * 32 + 128 + 512
+    # the high plane holds K rounded up to a multiple of 4 rows
+    for Kb, rows in ((1, 4), (13, 16), (92, 92), (128, 128)):
+        cfg_k = K.make_config(n_q_heads=32, n_kv_heads=8, group_k=128, boost_k=Kb)
+        assert K.kvq_kitty_key_page_bytes(cfg_k) == 4096 + rows * 32 + 128 + 512
 
 
 def test_int8_block_scale(K):

@@ -54,6 +54,9 @@ def _oracle(orc, cfg, Ks, Vs, q, score_mode=0):
     ([900, 1300], 0, 0, 8, 2),
     ([1700], 48, 0, 8, 2),          # three boosted k-steps
     ([1300], 92, 0, 4, 2),          # the largest supported boost
+    ([1300], 13, 0, 8, 2),          # K not a multiple of 4: a padded row group, a partial k-step
+    ([1100], 21, 1, 2, 2),          # the same on the per-head kernel (two high k-steps)
+    ([1250], 90, 0, 8, 2),          # six high k-steps, two padded rows
     ([800, 1900], 16, 0, 6, 2),     # three heads per kv head (one dead tensor-core column pair)
     ([600, 1400], 16, 0, 2, 2),     # one head per kv head: per-head kernel
     ([1234], 16, 0, 8, 1),          # eight heads per kv head: two grouped-query units per kv head

@@ -22,7 +22,7 @@ def _pages(rng, n, heavy=True):
     return x
 
 
-@pytest.mark.parametrize("Kb", [0, 16, 32, 128])
+@pytest.mark.parametrize("Kb", [0, 13, 16, 32, 128])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_kitty_key_pages_bitexact(K, orc, Kb, mode):
     rng = np.random.default_rng(300 + Kb + mode)

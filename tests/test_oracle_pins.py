@@ -313,6 +313,60 @@ def test_kitty_planes_combine_to_4bit_codes(orc):
             assert codes[t, c] == orc.affine_code(int(x[t, c].view(np.uint16)), sc, zc, bits)
 
 
+def test_kitty_plane_order_is_lane_friendly(orc):
+    """Key-page planes in the fragment order of the KIVI 2-bit key tiles (the Kitty page fixes the
+    planes, not the byte order inside them): the low plane of a 128-token page is four 1024-byte
+    tiles where a byte holds tokens q, q+8, q+16, q+24 of one channel and lane 4q + r's 16-byte
+    chunks hold channels 16k + 2r + {0, 1, 8, 9}; the high plane gives each 32-token tile a block of
+    Kp * 8 bytes (Kp = K rounded up to 4) whose 4-byte word 8r + q of 16-row block kh holds rows
+    16kh + 4r + {0..3} at tokens q + 8p."""
+    seen = set()
+    for t in range(128):
+        for c in range(128):
+            off, bit = orc.kitty_low_byte_offset(t, c), orc.kitty_code_bit(t)
+            q, p, r, k = t % 8, (t % 32) // 8, (c % 8) // 2, c // 16
+            e, h = c % 2, (c % 16) // 8
+            assert off // 1024 == t // 32 and bit == 2 * p
+            assert (off % 1024) // 512 == k // 4 and (off % 512) // 16 == 4 * q + r
+            assert (off % 16) // 4 == k % 4 and off % 4 == e + 2 * h
+            seen.add((off, bit))
+    assert len(seen) == 128 * 128 and {o for o, _ in seen} == set(range(4096))
+    for K in (1, 3, 4, 13, 16, 17, 32, 92):
+        Kp = orc.kitty_high_rows(K)
+        assert Kp % 4 == 0 and K <= Kp < K + 4
+        seen = set()
+        for t in range(128):
+            for rho in range(Kp):
+                off = orc.kitty_high_byte_offset(K, t, rho)
+                j, q = t // 32, t % 8
+                assert j * Kp * 8 <= off < (j + 1) * Kp * 8           # the tile's block
+                o = off - j * Kp * 8
+                assert o // 128 == rho // 16 and (o % 128) // 32 == (rho % 16) // 4
+                assert (o % 32) // 4 == q and o % 4 == rho % 4
+                seen.add((off, orc.kitty_code_bit(t)))
+        assert len(seen) == 128 * Kp and {o for o, _ in seen} == set(range(Kp * 32))
+
+
+def test_kitty_page_planes_are_kivi_tiles_of_the_codes(orc):
+    """The low plane equals the KIVI 2-bit key packing of the page's low code bits; the high plane
+    holds the high bits of the boosted channels by rank, zero in rows K..Kp-1."""
+    rng = np.random.default_rng(12)
+    x = _page(rng)
+    for K in (13, 16):
+        page = orc.kitty_key_page(x, K)
+        Kp = orc.kitty_high_rows(K)
+        assert page.size == 4096 + Kp * 32 + 128 + 512
+        codes, _, _ = orc.kitty_key_page_decode(page, 128, 128, K)
+        low = orc.kivi_key_pack((codes & 3).reshape(1, 128, 128), 2).reshape(-1)
+        assert np.array_equal(page[:4096], low)
+        boosted = np.flatnonzero(orc.kitty_select(x, K, 0))
+        high = page[4096:4096 + Kp * 32]
+        for rho in range(Kp):
+            for t in range(128):
+                v = (int(high[orc.kitty_high_byte_offset(K, t, rho)]) >> orc.kitty_code_bit(t)) & 3
+                assert v == (codes[t, boosted[rho]] >> 2 if rho < K else 0)
+
+
 def test_kitty_alpha_limits(orc):
     rng = np.random.default_rng(10)
     x = _page(rng)
@@ -338,6 +392,7 @@ def test_page_byte_accounts(orc):
         assert code_bits == g[key]["value"]
     assert g["kitty_boosted_channels"]["K"] == [int(a * 128) for a in g["kitty_boosted_channels"]["alpha"]]
     assert orc.kitty_key_page_bytes(128, 128, 16) == 4096 + 512 + 128 + 512
+    assert orc.kitty_key_page_bytes(128, 128, 13) == orc.kitty_key_page_bytes(128, 128, 16)
     assert orc.kitty_value_page_bytes(128, 128) == 4096 + 512
     # INT8 block cache: 128 one-byte codes plus 128 fp16 scales per 256 tokens
     assert 128 + 128 * 2 / 256 == g["int8_block_bytes_per_token_per_side"]["value"]
