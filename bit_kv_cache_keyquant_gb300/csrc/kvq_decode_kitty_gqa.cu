@@ -96,9 +96,9 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
     const int q = lane >> 2, r = lane & 3;
     const int hB = q >> 1;
     const bool xB = (q & 1) != 0;
-    // value unpacking: the lane's byte of each 32-channel block g is byte 8g + q of a token row (channels
-    // 32g + 4q + p at bits 2p); vbsel gathers that byte (byte q % 4 of its word) of two rows
-    const uint32_t vbsel = (uint32_t)((q & 3) | ((4 + (q & 3)) << 4));
+    // value codes: row address of this lane in the transposing matrix loads (matrix lane / 8: tokens
+    // 8 (m % 2) + lane % 8 of a k-step, bytes 16 (m / 2) .. + 15 of their rows)
+    const int vrow = 8 * ((lane >> 3) & 1) + (lane & 7), vcol = 16 * (lane >> 4);
     const uint32_t *qown = xB ? S.qlo[hB] : S.qhi[hB];   // the part of B column n = q (zero-point products)
     bool ok = true;
     int sg = 0;
@@ -288,13 +288,16 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 4));
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
-                    if (mt > m_run) {
-                        const float sc = ex2_ftz(m_run - mt);
+                    // rescale when a head of the warp raised its maximum: a warp-uniform branch (the heads'
+                    // lanes would diverge), the other heads' lanes multiplying by 1
+                    if (__any_sync(0xFFFFFFFFu, mt > m_run)) {
+                        const float mn = fmaxf(m_run, mt);
+                        const float sc = ex2_ftz(m_run - mn);
                         l_part *= sc;
                         scale4(vzacc, sc);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) scale4(vacc[i], sc);
-                        m_run = mt;
+                        m_run = mn;
                     }
                     float pr[4];
 #pragma unroll
@@ -302,52 +305,49 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
                         pr[i] = ex2_ftz(lg[i] - m_run);
                         l_part += pr[i];
                     }
-                    // token 16k + 8hk + 4e + j (k-step k, k-column 2j + e + 8hk of the value products) at
-                    // position 16k + 8hk + 2j + e: each B register's two tokens are adjacent
+                    // p of head r, token q + 8i, at position q + 8i of row r
                     float *pb = S.pbuf[warp];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) pb[r * KPB_ROW + 8 * i + 2 * (q & 3) + (q >> 2)] = pr[i];
+                    for (int i = 0; i < 4; ++i) pb[r * KPB_ROW + q + 8 * i] = pr[i];
                     const uint8_t *vrec = st + VREC_OFF;
                     const uint16_t *vs = reinterpret_cast<const uint16_t *>(vrec + PG * KVQ_D / 4) + 32 * warp;
                     __syncwarp();
-                    // ---- values: k-column 2j + e + 8hk of k-step k is token 16k + 8hk + 4e + j ----
+                    // ---- values: k-column k of k-step kv is token 16kv + k; A from transposing matrix loads of
+                    //      the token-major code rows: a lane's word holds bytes 2q, 2q + 1 of tokens 2r, 2r + 1
+                    //      (channels 8q .. 8q + 7 of a 64-channel half), m-tile 4hh + j takes channel 8q + j
+                    //      (row q) and 8q + 4 + j (row q + 8) of half hh ----
                     const uint8_t *vc = vrec + warp * 32 * (KVQ_D / 4);
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
-                        const int t0 = 16 * kv + r;             // tokens t0, t0+4 | t0+8, t0+12
                         const float2 pa = *reinterpret_cast<const float2 *>(&pb[hB * KPB_ROW + 16 * kv + 2 * r]);
                         const float2 pc = *reinterpret_cast<const float2 *>(&pb[hB * KPB_ROW + 16 * kv + 8 + 2 * r]);
                         const uint32_t pha = split_pair(pa.x, pa.y, false), pla = split_pair(pa.x, pa.y, true);
                         const uint32_t phc = split_pair(pc.x, pc.y, false), plc = split_pair(pc.x, pc.y, true);
-                        const uint32_t sa = (uint32_t)vs[t0] | ((uint32_t)vs[t0 + 4] << 16);
-                        const uint32_t sc8 = (uint32_t)vs[t0 + 8] | ((uint32_t)vs[t0 + 12] << 16);
+                        const uint32_t sa = *reinterpret_cast<const uint32_t *>(vs + 16 * kv + 2 * r);
+                        const uint32_t sc8 = *reinterpret_cast<const uint32_t *>(vs + 16 * kv + 8 + 2 * r);
                         const uint32_t bv0 = split_prod(pha, pla, sa, xB);
                         const uint32_t bv1 = split_prod(phc, plc, sc8, xB);
                         {
                             // value zero-point product: A rows hold z of the k-step's tokens, B the lane's part of p
-                            const uint32_t za = (uint32_t)vs[PG + t0] | ((uint32_t)vs[PG + t0 + 4] << 16);
-                            const uint32_t zc = (uint32_t)vs[PG + t0 + 8] | ((uint32_t)vs[PG + t0 + 12] << 16);
+                            const uint32_t za = *reinterpret_cast<const uint32_t *>(vs + PG + 16 * kv + 2 * r);
+                            const uint32_t zc = *reinterpret_cast<const uint32_t *>(vs + PG + 16 * kv + 8 + 2 * r);
                             mma16816(vzacc, za, za, zc, zc, xB ? pla : pha, xB ? plc : phc);
                         }
-                        // m-tile 2g + pp, rows q | q + 8: channels 32g + 4q + 2pp + 0 | 1 (bit positions 2pp and
-                        // 2pp + 1 of the lane's byte of block g); one word X = that byte of the rows of tokens
-                        // t0, t0+4 | t0+8, t0+12 gives the A registers of both m-tiles
+                        uint32_t m4[4];
+                        ldsm_x4_trans(m4, vc + (16 * kv + vrow) * 32 + vcol);
 #pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            const int wo = 8 * g8 + 4 * (q >> 2);            // the word holding byte 8g + q
-                            const uint32_t wA = *reinterpret_cast<const uint32_t *>(vc + t0 * 32 + wo);
-                            const uint32_t wB = *reinterpret_cast<const uint32_t *>(vc + (t0 + 4) * 32 + wo);
-                            const uint32_t wC = *reinterpret_cast<const uint32_t *>(vc + (t0 + 8) * 32 + wo);
-                            const uint32_t wD = *reinterpret_cast<const uint32_t *>(vc + (t0 + 12) * 32 + wo);
-                            const uint32_t X = prmt(prmt(wA, wB, vbsel), prmt(wC, wD, vbsel), 0x5410u);
-                            const uint32_t X4 = X >> 4;
-                            uint32_t a0, a1, a2, a3;
-                            e4m3x4_f16x2(X & 0x03030303u, a0, a2);
-                            e4m3x4_f16x2(X & 0x0C0C0C0Cu, a1, a3);
-                            mma16816(vacc[2 * g8], a0, a1, a2, a3, bv0, bv1);
-                            e4m3x4_f16x2(X4 & 0x03030303u, a0, a2);
-                            e4m3x4_f16x2(X4 & 0x0C0C0C0Cu, a1, a3);
-                            mma16816(vacc[2 * g8 + 1], a0, a1, a2, a3, bv0, bv1);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            // tokens 2r, 2r + 1 (x) and 2r + 8, 2r + 9 (y): bytes 2q of both, then 2q + 1 of both
+                            const uint32_t x = prmt(m4[2 * hh], 0u, 0x3120u), y = prmt(m4[2 * hh + 1], 0u, 0x3120u);
+                            const uint32_t x4 = x >> 4, y4 = y >> 4;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t mk = (j & 1) ? 0x0C0C0C0Cu : 0x03030303u;
+                                uint32_t a0, a1, a2, a3;
+                                e4m3x4_f16x2((j < 2 ? x : x4) & mk, a0, a1);
+                                e4m3x4_f16x2((j < 2 ? y : y4) & mk, a2, a3);
+                                mma16816(vacc[4 * hh + j], a0, a1, a2, a3, bv0, bv1);
+                            }
                         }
                     }
                     __syncwarp();
@@ -363,14 +363,18 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kitty_decode_gqa_kernel(
             l_w += __shfl_xor_sync(0xFFFFFFFFu, l_w, 16);
             const float vz = vzacc[0] + vzacc[1];
             float *acc = S.st_acc[warp][r];
-            // rows q of both m-tiles of block g carry codes x 2^-9, rows q + 8 codes x 2^-7
+            // m-tile 4hh + j: row q is channel 64hh + 8q + j, row q + 8 channel 64hh + 8q + 4 + j, codes
+            // x 2^-9 (j even) or 2^-7 (j odd)
 #pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8)
-                *reinterpret_cast<float4 *>(&acc[32 * g8 + 4 * q]) =
-                    make_float4(fmaf(vacc[2 * g8][0] + vacc[2 * g8][1], 512.f, vz),
-                                fmaf(vacc[2 * g8][2] + vacc[2 * g8][3], 128.f, vz),
-                                fmaf(vacc[2 * g8 + 1][0] + vacc[2 * g8 + 1][1], 512.f, vz),
-                                fmaf(vacc[2 * g8 + 1][2] + vacc[2 * g8 + 1][3], 128.f, vz));
+            for (int hh = 0; hh < 2; ++hh) {
+                const float (*v)[4] = &vacc[4 * hh];
+                *reinterpret_cast<float4 *>(&acc[64 * hh + 8 * q]) =
+                    make_float4(fmaf(v[0][0] + v[0][1], 512.f, vz), fmaf(v[1][0] + v[1][1], 128.f, vz),
+                                fmaf(v[2][0] + v[2][1], 512.f, vz), fmaf(v[3][0] + v[3][1], 128.f, vz));
+                *reinterpret_cast<float4 *>(&acc[64 * hh + 8 * q + 4]) =
+                    make_float4(fmaf(v[0][2] + v[0][3], 512.f, vz), fmaf(v[1][2] + v[1][3], 128.f, vz),
+                                fmaf(v[2][2] + v[2][3], 512.f, vz), fmaf(v[3][2] + v[3][3], 128.f, vz));
+            }
             if (q == 0) {
                 S.st_m[warp][r] = m_run;
                 S.st_l[warp][r] = l_w;

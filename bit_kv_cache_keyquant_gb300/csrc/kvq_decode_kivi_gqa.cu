@@ -285,15 +285,18 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 4));
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
                     mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
-                    if (mt > m_run) {
-                        const float sc = ex2_ftz(m_run - mt);
+                    // rescale when a head of the warp raised its maximum: a warp-uniform branch (the heads'
+                    // lanes would diverge), the other heads' lanes multiplying by 1
+                    if (__any_sync(0xFFFFFFFFu, mt > m_run)) {
+                        const float mn = fmaxf(m_run, mt);
+                        const float sc = ex2_ftz(m_run - mn);
                         l_part *= sc;
                         scale4(vzacc, sc);
 #pragma unroll
                         for (int i = 0; i < NGV; ++i) vzc[i] *= sc;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) scale4(vacc[i], sc);
-                        m_run = mt;
+                        m_run = mn;
                     }
                     float pr[4];
 #pragma unroll

@@ -42,6 +42,17 @@ __device__ __forceinline__ uint32_t hneg2(uint32_t a) {
     asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
     return d;
 }
+// ldmatrix of four 8 x 8 matrices of 16-bit elements, transposed: lanes 8m .. 8m + 7 give the
+// 16-byte row addresses of matrix m; lane 4q + r receives in d[m] the elements (rows 2r, 2r + 1;
+// column q) of matrix m, row 2r in the low half.  Volatile with a memory clobber: it reads
+// bytes that a bulk copy wrote, so it stays behind the barrier wait that announced them.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t d[4], const void *row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(smem_addr(row))
+                 : "memory");
+}
+
 // fp16x2 product a*b as its hi part (x == 0) or its lo part (x == 1):
 // hi = fl(ah b); lo = fl(al b + fl(ah b - hi)), the inner FMA being exact.
 // The negation is a floating-point one, which the FMA can take as an
