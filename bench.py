@@ -305,7 +305,7 @@ def build_state(w, device, appends: int = 1024):
         st.update(n_vtok=n_vtok, n_kgrp=n_kgrp,
                   vnew=I.gen_slice_torch(w.seed, I.T_V, 9999, 0, n_vtok, 128, device),
                   knew=I.gen_slice_torch(w.seed, I.T_K, 9999, 1, n_kgrp * cfg.group_k, 128, device),
-                  scratch=[torch.empty((n_vtok, 128 * w.bits_v // 8), dtype=torch.uint8, device=device),
+                  scratch=[torch.empty(((n_vtok + 31) // 32 * 32, 128 * w.bits_v // 8), dtype=torch.uint8, device=device),
                            torch.empty((n_vtok, 128 // cfg.group_v), dtype=torch.int32, device=device),
                            torch.empty((n_kgrp, cfg.group_k * 128 * w.bits_k // 8), dtype=torch.uint8,
                                        device=device),
@@ -439,7 +439,7 @@ def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
             us = timed(lambda: kvq.kv_quant_key(cfg, x, ng, kc, ks, stream))
             out["kv_quant_key"] = entry(us, ng, f"{G}-token key groups", total + kc.numel() + ks.numel() * 4)
             nt = total // 256
-            vc = torch.empty(nt * 128 * w.bits_v // 8, dtype=torch.uint8, device=dev)
+            vc = torch.empty((nt + 31) // 32 * 32 * 128 * w.bits_v // 8, dtype=torch.uint8, device=dev)   # whole tiles
             vs = torch.empty((nt, 128 // Gv), dtype=torch.int32, device=dev)
             us = timed(lambda: kvq.kv_quant_value(cfg, x, nt, vc, vs, stream))
             out["kv_quant_value"] = entry(us, nt, "value tokens", total + vc.numel() + vs.numel() * 4)

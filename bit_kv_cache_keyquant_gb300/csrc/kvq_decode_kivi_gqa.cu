@@ -106,9 +106,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     const int hB = q >> 1;                         // head of this lane's B column (n = q)
     const bool xB = (q & 1) != 0;                  // B column holds lo parts
     const int gl = (32 * warp) / P.G;              // key group of this warp's tile within a stage
-    // 2-bit value unpacking: the lane's byte of value group g (32 channels) is byte 8g + q of a token row,
-    // channels 32g + 4q + p at bits 2p; bsel gathers that byte (byte q % 4 of its word) of two rows
-    const uint32_t bsel = (uint32_t)((q & 3) | ((4 + (q & 3)) << 4));
     // 4-bit values: channel 16mt + q (+8) is byte q/2 of the m-tile's first (second) word, bits 4(q%2)
     const uint32_t vsel4 = (uint32_t)((q >> 1) | ((4 + (q >> 1)) << 4));
     const uint32_t vshift4 = (q & 1) ? 4u : 0u;
@@ -379,16 +376,14 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                             }
                         } else {
                             // m-tile 2g + pp, rows q | q + 8: channels 32g + 4q + 2pp + 0 | 1 (bit positions 2pp and
-                            // 2pp + 1 of the lane's byte of group g); one word X = that byte of the rows of tokens
-                            // t0, t0+4 | t0+8, t0+12 gives the A registers of both m-tiles
+                            // 2pp + 1 of byte 8g + q); the value tile stores, for lane 4q + r, that byte of the
+                            // tokens t0, t0+4 | t0+8, t0+12 as word g of its 16-byte chunk: the A registers of both
+                            // m-tiles of group g
+                            const uint4 v4 = *reinterpret_cast<const uint4 *>(vc + ks * 512 + lane * 16);
+                            const uint32_t vx[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                             for (int g8 = 0; g8 < 4; ++g8) {
-                                const int wo = 8 * g8 + 4 * (q >> 2);            // the word holding byte 8g + q
-                                const uint32_t wA = *reinterpret_cast<const uint32_t *>(vc + t0 * 32 + wo);
-                                const uint32_t wB = *reinterpret_cast<const uint32_t *>(vc + (t0 + 4) * 32 + wo);
-                                const uint32_t wC = *reinterpret_cast<const uint32_t *>(vc + (t0 + 8) * 32 + wo);
-                                const uint32_t wD = *reinterpret_cast<const uint32_t *>(vc + (t0 + 12) * 32 + wo);
-                                const uint32_t X = prmt(prmt(wA, wB, bsel), prmt(wC, wD, bsel), 0x5410u);
+                                const uint32_t X = vx[g8];
                                 const uint32_t X4 = X >> 4;
                                 const int j = (32 * g8) / (KVQ_D / NGV);          // value group of both m-tiles
                                 uint32_t a0, a1, a2, a3;
@@ -488,6 +483,8 @@ int kivi_gqa_units_per_kv_head(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;
     return g > GMAX ? 2 : 1;
 }
+
+bool kivi_value_tiles(const kvq_config *cfg) { return cfg->bits_v == 2 && kivi_gqa_supported(cfg); }
 
 bool kivi_gqa_supported(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;

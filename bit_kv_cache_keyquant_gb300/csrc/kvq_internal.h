@@ -57,6 +57,15 @@ inline KiviSrc kivi_src(const kvq_kivi_paged_cache *c) {
     return s;
 }
 
+// Byte offset of channel quad c4 (channels 4 c4 .. 4 c4 + 3, c4 = 8g + q) of token t in 2-bit KIVI value
+// codes stored in value tiles (kivi_value_tiles), of one (batch row, kv head) or page record: 32-token tiles
+// of 1024 bytes in the fragment order of the grouped-query kernel's tensor-core value products.  With t % 32 = 16 kv + 4 i + r the byte is
+// tile * 1024 + kv * 512 + (4q + r) * 16 + 4g + i, so lane 4q + r of a warp finds byte c4 of the tokens
+// r, r + 4, r + 8, r + 12 of a 16-token half (for g = 0..3) in one 16-byte chunk.
+__host__ __device__ constexpr int64_t kivi_value_byte(int64_t t, int c4) {
+    return (t >> 5) * 1024 + ((t >> 4) & 1) * 512 + (4 * (c4 & 7) + (int)(t & 3)) * 16 + 4 * (c4 >> 3) + (int)((t >> 2) & 3);
+}
+
 // Rows of a Kitty key page's high plane: the K boosted channels rounded up to
 // a multiple of 4 (each 4-byte word of the plane holds a group of four rows).
 __host__ __device__ constexpr int kitty_high_rows(int K) { return (K + 3) & ~3; }
@@ -128,6 +137,9 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const KiviSrc &c, const vo
                                const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query KIVI decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
 bool kivi_gqa_supported(const kvq_config *cfg);
+// 2-bit KIVI value codes of a config that decodes on the grouped-query kernel are stored in its value
+// tiles (kivi_value_byte); every other KIVI value cache is token-major
+bool kivi_value_tiles(const kvq_config *cfg);
 int kivi_gqa_units_per_kv_head(const kvq_config *cfg);   // 1, or 2 for 4 < g <= 8
 cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, const void *q,
                                    const DecodePlan &p, void *ws, cudaStream_t st);

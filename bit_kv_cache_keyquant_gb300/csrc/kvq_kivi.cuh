@@ -50,6 +50,7 @@ struct Params {
     int64_t kgrp_cap;   // cap / G
     float alpha;
     int bits_k, bits_v; // code widths (2 or 4)
+    int vtiles;         // 2-bit values stored in value tiles (kivi_value_tiles), else token-major
     // paged cache (page_table non-null): token t of row b is in page record
     // pages + (page_table[b * pt_stride + t / 128] * Hkv + kv head) * rec_bytes
     const int32_t *page_table;
@@ -193,18 +194,23 @@ __device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, 
     if (t < U.nVq) {
         // the lane's 4 channels: one byte at 2 bits, two at 4 bits (channel c at bits bits*(c % (8/bits)))
         const int bits = P.bits_v;
-        const uint8_t *tb;
+        // the byte (2 bits) or 16-bit word (4 bits) of channel quad `lane`: in the value tiles, or token-major
+        const uint8_t *vb;
         const uint32_t *szr;
+        int64_t tl;                                            // the token within vb's tiles or rows
         if (P.page_table) {
             const uint8_t *rec = kivi_page(P, U, t);
-            const int tp = t & 127;
-            tb = rec + P.kc_bytes + 2048 + tp * (KVQ_D * bits / 8);
-            szr = reinterpret_cast<const uint32_t *>(rec + P.kc_bytes + 2048 + P.vc_bytes) + tp * P.ngv;
+            tl = t & 127;
+            vb = rec + P.kc_bytes + 2048;
+            szr = reinterpret_cast<const uint32_t *>(rec + P.kc_bytes + 2048 + P.vc_bytes) + tl * P.ngv;
         } else {
-            tb = P.v_codes + (U.bk * P.cap + t) * (KVQ_D * bits / 8);
+            tl = t;
+            vb = P.v_codes + U.bk * P.cap * (KVQ_D * bits / 8);
             szr = P.v_sz + (U.bk * P.cap + t) * P.ngv;
         }
-        const uint32_t w = bits == 2 ? (uint32_t)tb[lane] : (uint32_t)reinterpret_cast<const uint16_t *>(tb)[lane];
+        const uint32_t w = P.vtiles    ? (uint32_t)vb[kivi_value_byte(tl, lane)]
+                           : bits == 2 ? (uint32_t)vb[tl * (KVQ_D / 4) + lane]
+                                       : (uint32_t)reinterpret_cast<const uint16_t *>(vb + tl * (KVQ_D / 2))[lane];
         const uint32_t sz = szr[(4 * lane) / P.Gv];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -393,6 +399,7 @@ inline Params kivi_params(const kvq_config *cfg, const KiviSrc &c, const void *q
     P.alpha = sm_scale_of(cfg) * 1.4426950408889634f;
     P.bits_k = cfg->bits_k;
     P.bits_v = cfg->bits_v;
+    P.vtiles = kivi_value_tiles(cfg);
     P.page_table = c.page_table;
     P.pages = static_cast<const uint8_t *>(c.pages);
     P.pt_stride = (int)(P.cap / 128);

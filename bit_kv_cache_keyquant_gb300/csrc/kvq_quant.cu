@@ -210,12 +210,25 @@ __device__ __forceinline__ void value_token_quant(const uint16_t *__restrict__ s
     value_token_quant_x<GV>(*reinterpret_cast<const uint2 *>(src + 4 * lane), lane, wv, s, z, bits);
 }
 
-// Store of one token's packed codes by the lanes that hold a full word.
+// Store of one token's packed codes by the lanes that hold a full word: token-major (the Kitty value pages,
+// and KIVI values unless tiled), or into the KIVI value tiles of `codes` (token t of the row, lanes 4j
+// holding channel quads 4j .. 4j + 3, one byte each).
 __device__ __forceinline__ void value_token_store(uint8_t *__restrict__ tok, int lane, uint32_t wv, int bits) {
     if (bits == 2) {
         if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(tok)[lane >> 2] = wv;
     } else {
         if ((lane & 1) == 0) reinterpret_cast<uint32_t *>(tok)[lane >> 1] = wv;
+    }
+}
+__device__ __forceinline__ void value_token_store_kivi(uint8_t *__restrict__ codes, int64_t t, int lane, uint32_t wv,
+                                                       int bits, bool tiles) {
+    if (tiles) {
+        if ((lane & 3) == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) codes[kivi_value_byte(t, lane + k)] = (uint8_t)(wv >> (8 * k));
+        }
+    } else {
+        value_token_store(codes + t * (KVQ_D * bits / 8), lane, wv, bits);
     }
 }
 
@@ -232,7 +245,7 @@ __device__ __forceinline__ void value_token_store(uint8_t *__restrict__ tok, int
 template <int GV, bool KITTY, int BITS>
 __global__ void __launch_bounds__(256, 3) quant_value_kernel(const uint16_t *__restrict__ v, int64_t n_tokens,
                                                           uint8_t *__restrict__ out, uint32_t *__restrict__ sz,
-                                                          int page_tokens, int64_t page_bytes) {
+                                                          int page_tokens, int64_t page_bytes, bool tiles) {
     constexpr int LG = GV / 16, QMAX = (1 << BITS) - 1;   // lanes per group
     const int lane = threadIdx.x & 31, ts = lane >> 3, cb = lane & 7;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -295,9 +308,15 @@ __global__ void __launch_bounds__(256, 3) quant_value_kernel(const uint16_t *__r
         }
         if (!live) continue;
         if (!KITTY) {
-            uint8_t *row = out + t * (KVQ_D * BITS / 8);
-            if (BITS == 2) reinterpret_cast<uint32_t *>(row)[cb] = w[0];
-            else reinterpret_cast<uint2 *>(row)[cb] = make_uint2(w[0], w[BITS / 2 - 1]);
+            if (BITS == 2 && tiles) {
+                // channel quads 4cb .. 4cb + 3 of token t into the 32-token value tiles
+#pragma unroll
+                for (int k = 0; k < 4; ++k) out[kivi_value_byte(t, 4 * cb + k)] = (uint8_t)(w[0] >> (8 * k));
+            } else if (BITS == 2) {
+                reinterpret_cast<uint32_t *>(out + t * (KVQ_D / 4))[cb] = w[0];
+            } else {
+                reinterpret_cast<uint2 *>(out + t * (KVQ_D * BITS / 8))[cb] = make_uint2(w[0], w[BITS / 2 - 1]);
+            }
             if (cb % LG == 0) sz[t * (KVQ_D / GV) + cb / LG] = (uint32_t)s | ((uint32_t)z << 16);
         } else {
             const int64_t p = t / page_tokens;
@@ -568,7 +587,8 @@ cudaError_t launch_quant_value_kivi(const kvq_config *cfg, const void *v, int64_
     const uint16_t *vp = static_cast<const uint16_t *>(v);
     uint8_t *cp = static_cast<uint8_t *>(codes);
     uint32_t *zp = static_cast<uint32_t *>(sz);
-#define KVQ_QV(GV, B) quant_value_kernel<GV, false, B><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0)
+    const bool tiles = kivi_value_tiles(cfg);
+#define KVQ_QV(GV, B) quant_value_kernel<GV, false, B><<<grid, 256, 0, st>>>(vp, n_tokens, cp, zp, 0, 0, tiles)
     const bool b4 = cfg->bits_v == 4;
     switch (cfg->group_v) {
         case 32: if (b4) KVQ_QV(32, 4); else KVQ_QV(32, 2); break;
@@ -587,14 +607,14 @@ cudaError_t launch_quant_value_kitty(const kvq_config *cfg, const void *v, int64
     const int grid = grid_cap((n_tokens + 31) / 32, 3);
     const int64_t pb = (int64_t)G * KVQ_D / 4 + 4LL * G;
     quant_value_kernel<128, true, 2><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(v), n_tokens,
-                                                           static_cast<uint8_t *>(pages), nullptr, G, pb);
+                                                           static_cast<uint8_t *>(pages), nullptr, G, pb, false);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t n_pages, int score_mode,
                                    void *pages, cudaStream_t st) {
     if (n_pages == 0) return cudaSuccess;
-    const int G = cfg->group_k, K = cfg->boost_k;
+    const int K = cfg->boost_k;
     const int64_t pb = kitty_key_page_bytes(K);
     const size_t smem = KITTY_KEY_SMEM;
     static std::atomic<uint64_t> attr_done{0};
@@ -639,6 +659,7 @@ struct AppendParams {
     uint16_t *k_res, *v_res;
     unsigned *err;
     int Hkv, R, G, ngv, max_seq_len, bits_k, bits_v;
+    int vtiles;                  // 2-bit values stored in value tiles (kivi_value_tiles)
     int64_t cap, kgrp_cap;
 };
 
@@ -667,7 +688,7 @@ __global__ void __launch_bounds__(128) append_kivi_kernel(AppendParams P) {
         uint32_t wv;
         uint16_t s, z;
         value_token_quant<GV>(vres + (t % P.R) * KVQ_D, lane, wv, s, z, P.bits_v);
-        value_token_store(P.v_codes + (bk * P.cap + t) * (KVQ_D * P.bits_v / 8), lane, wv, P.bits_v);
+        value_token_store_kivi(P.v_codes + bk * P.cap * (KVQ_D * P.bits_v / 8), t, lane, wv, P.bits_v, P.vtiles);
         if ((lane % (GV / 4)) == 0)
             P.v_sz[(bk * P.cap + t) * P.ngv + lane / (GV / 4)] = (uint32_t)s | ((uint32_t)z << 16);
     }
@@ -707,6 +728,7 @@ cudaError_t launch_append_kivi(const kvq_config *cfg, const kvq_kivi_cache *c, c
     P.ngv = KVQ_D / cfg->group_v;
     P.bits_k = cfg->bits_k;
     P.bits_v = cfg->bits_v;
+    P.vtiles = kivi_value_tiles(cfg);
     P.max_seq_len = c->max_seq_len;
     P.cap = ((int64_t)c->max_seq_len + 127) / 128 * 128;
     P.kgrp_cap = P.cap / cfg->group_k;
@@ -736,6 +758,7 @@ struct PagedDst {
     int pt_stride, n_pages, Hkv;
     int64_t rec_bytes;
     int kc_bytes, vc_bytes;
+    int vtiles;                  // 2-bit values stored in value tiles (kivi_value_tiles)
     unsigned *err;
 };
 
@@ -773,7 +796,7 @@ __device__ __forceinline__ void value_token_paged(const uint16_t *__restrict__ s
     uint16_t s, z;
     value_token_quant<GV>(src, lane, wv, s, z, bits);
     const int tp = tg & 127;
-    value_token_store(rec + D.kc_bytes + 2048 + tp * (KVQ_D * bits / 8), lane, wv, bits);
+    value_token_store_kivi(rec + D.kc_bytes + 2048, tp, lane, wv, bits, D.vtiles);
     if ((lane % LG) == 0)
         reinterpret_cast<uint32_t *>(rec + D.kc_bytes + 2048 + D.vc_bytes)[tp * ngv + lane / LG] =
             (uint32_t)s | ((uint32_t)z << 16);
@@ -807,6 +830,7 @@ static PagedDst paged_dst(const kvq_config *cfg, const kvq_kivi_paged_cache *c) 
     D.rec_bytes = kivi_page_bytes(cfg->bits_k, cfg->bits_v);
     D.kc_bytes = 16 * KVQ_D * cfg->bits_k;
     D.vc_bytes = 16 * KVQ_D * cfg->bits_v;
+    D.vtiles = kivi_value_tiles(cfg);
     D.err = device_error_ptr();
     return D;
 }
@@ -920,6 +944,7 @@ cudaError_t launch_append_kivi_paged(const kvq_config *cfg, const kvq_kivi_paged
     P.ngv = KVQ_D / cfg->group_v;
     P.bits_k = cfg->bits_k;
     P.bits_v = cfg->bits_v;
+    P.vtiles = kivi_value_tiles(cfg);
     P.max_seq_len = c->max_seq_len;
     P.cap = 0;
     P.kgrp_cap = 0;

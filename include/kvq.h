@@ -48,8 +48,19 @@
  *     At 4 bits (KIVI-4) a tile is 2048 bytes, two planes of 1024: token
  *     q + 8p goes to plane p/2, at bits 4*(p%2) of the byte that the 2-bit
  *     layout above gives inside the plane (t%8 in place of t).
- *   KIVI value token: D*b/8 bytes for b-bit codes, channel c in bits
- *     b*(c % (8/b)) of byte c/(8/b).  Parameters: fp16x2 (s, z) [D/Gv] per token.
+ *   KIVI value codes, token-major: D*b/8 bytes per token for b-bit codes,
+ *     channel c in bits b*(c % (8/b)) of byte c/(8/b).  Parameters: fp16x2
+ *     (s, z) [D/Gv] per token.
+ *   KIVI value tiles: a config whose query heads decode on the grouped-query
+ *     tensor-core kernel (2 <= n_q_heads / n_kv_heads <= 4, or an even ratio
+ *     up to 8) with 2-bit values stores its value codes in 32-token tiles of
+ *     1024 bytes instead (the tile of token t is tile t/32 of its (batch row,
+ *     kv head) or page record).  With t % 32 = 16kv + 4i + r and
+ *     c = 32g + 4q + p, the code sits in bits 2p of byte
+ *     (t/32)*1024 + kv*512 + (4q + r)*16 + 4g + i: a byte holds four channels
+ *     of one token, and lane 4q + r of a warp finds byte 8g + q of the tokens
+ *     r, r+4, r+8, r+12 of each 16-token half, g = 0..3, in one 16-byte chunk
+ *     (the A operands of the tensor-core value products).
  *   Kitty key page (G = 128 tokens, K boosted channels), one record of
  *     kvq_kitty_key_page_bytes() bytes: low plane (D*G/4 bytes, code & 3 of
  *     every channel), high plane (Kp*G/4 bytes, Kp = K rounded up to a
@@ -154,7 +165,10 @@ KVQ_API kvq_status kv_quant_key(const kvq_config *cfg, const void *k, int64_t n_
 /* a2: quantize n_tokens KIVI values, per token over groups of Gv channels,
  * at b = cfg->bits_v bits (2 or 4).
  *   v       fp16 [n_tokens][D]
- *   codes   uint8 [n_tokens][D*b/8] (token-major)
+ *   codes   token-major uint8 [n_tokens][D*b/8], or, for a config stored in
+ *           value tiles, ceil(n_tokens/32) tiles of 1024 bytes (token 0 of
+ *           the call starts a tile; bytes of the last tile's tokens past
+ *           n_tokens are left unchanged)
  *   sz      fp16x2 [n_tokens][D/Gv]
  * Same rounding rules as kv_quant_key.  (KIVI section 3.3 value split.) */
 KVQ_API kvq_status kv_quant_value(const kvq_config *cfg, const void *v, int64_t n_tokens,

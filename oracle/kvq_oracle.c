@@ -337,6 +337,55 @@ ORC_API void orc_tokenmajor_pack(int D, const uint8_t *codes, long n_tok, uint8_
     orc_tokenmajor_pack_w(D, 2, codes, n_tok, packed);
 }
 
+/* KIVI value codes at 2 bits (D = 128) in value tiles: 32-token tiles of
+ * 1024 bytes.  KIVI fixes the per-token grouping, not the storage order; this
+ * order is a design choice (the fragment order of a tensor-core value product
+ * whose rows are channels and whose k index runs over tokens), used by the
+ * caches whose grouped-query heads decode on the tensor cores; the others keep
+ * the token-major order (orc_tokenmajor_pack_w).  Token t, with
+ * tt = t % 32 = 16 kv + 4 i + r (kv < 2, i < 4, r < 4), and channel
+ * c = 32 g + 4 q + p (g < 4, q < 8, p < 4) sit at bits 2p of byte
+ *   (t / 32) * 1024 + kv * 512 + (4q + r) * 16 + 4g + i,
+ * so a byte holds four channels of one token, the 4-byte word 4q + r of a
+ * 16-token half holds byte 8g + q of the tokens r, r + 4, r + 8, r + 12, and
+ * the 16 bytes at (4q + r) * 16 are those words for g = 0..3. */
+ORC_API long orc_kivi_value_byte_offset(int t, int c)
+{
+    int tt = t % 32, kv = tt / 16, i = (tt % 16) / 4, r = tt % 4;
+    int g = c / 32, q = (c % 32) / 4;
+    return (long)(t / 32) * 1024 + kv * 512 + (4 * q + r) * 16 + 4 * g + i;
+}
+
+ORC_API int orc_kivi_value_bit(int c) { return 2 * (c % 4); }
+
+/* Value codes [n_tok][D] -> packed bytes: with tiles (2 bits only) the tile
+ * order above (ceil(n_tok / 32) tiles; bytes of tokens past n_tok stay 0),
+ * otherwise token-major (orc_tokenmajor_pack_w).  Returns 1 for other shapes. */
+ORC_API int orc_kivi_value_pack_w(int D, int bits, int tiles, const uint8_t *codes, long n_tok, uint8_t *packed)
+{
+    if (D != 128 || (bits != 2 && bits != 4) || (tiles && bits != 2))
+        return 1;
+    if (!tiles) {
+        orc_tokenmajor_pack_w(D, bits, codes, n_tok, packed);
+        return 0;
+    }
+    memset(packed, 0, (size_t)((n_tok + 31) / 32 * 1024));
+    for (long t = 0; t < n_tok; ++t)
+        for (int c = 0; c < D; ++c)
+            packed[orc_kivi_value_byte_offset((int)(t % 32), c) + (t / 32) * 1024] |=
+                (uint8_t)((codes[t * D + c] & 3) << orc_kivi_value_bit(c));
+    return 0;
+}
+
+static int tokenmajor_code_at(int bits, const uint8_t *tok_bytes, int c);
+
+static int kivi_value_code_at(int bits, int tiles, const uint8_t *vc, long t, int c)
+{
+    if (tiles)
+        return (vc[(t / 32) * 1024 + orc_kivi_value_byte_offset((int)(t % 32), c)] >> orc_kivi_value_bit(c)) & 3;
+    return tokenmajor_code_at(bits, vc + t * ((long)128 * bits / 8), c);
+}
+
 static int tokenmajor_code_at(int bits, const uint8_t *tok_bytes, int c)
 {
     int cpb = 8 / bits;
@@ -691,10 +740,11 @@ ORC_API void orc_attend_fp16(int D, int n, const uint16_t *q, const uint16_t *k,
  *   Residual token t lives at slot t % R.
  * Arrays (this (b, kvh) only), b_K / b_V-bit codes:
  *   kc   packed key groups, G*D*b_K/8 bytes each   ksz fp16 [grp][D][2]
- *   vc   packed value tokens, D*b_V/8 bytes each   vsz fp16 [tok][D/Gv][2]
+ *   vc   packed value codes (orc_kivi_value_pack_w: value tiles when
+ *        vtiles, else token-major)                vsz fp16 [tok][D/Gv][2]
  *   kres, vres fp16 [R][D]
  * out: binary64 [g][D] for the g query heads q fp16 [g][D]. */
-ORC_API void orc_kivi_decode_one_w(int D, int G, int Gv, int R, int L, int bits_k, int bits_v, int n_heads,
+ORC_API void orc_kivi_decode_one_w(int D, int G, int Gv, int R, int L, int bits_k, int bits_v, int vtiles, int n_heads,
                                    double sm_scale, const uint16_t *q, const uint8_t *kc, const uint16_t *ksz,
                                    const uint8_t *vc, const uint16_t *vsz,
                                    const uint16_t *kres, const uint16_t *vres, double *out)
@@ -717,7 +767,7 @@ ORC_API void orc_kivi_decode_one_w(int D, int G, int Gv, int R, int L, int bits_
                 k[(long)t * D + c] = orc_half_to_double(kres[(long)(t % R) * D + c]);
             }
             if (t < nVq) {
-                int code = tokenmajor_code_at(bits_v, vc + (long)t * ((long)D * bits_v / 8), c);
+                int code = kivi_value_code_at(bits_v, vtiles, vc, t, c);
                 long j = (long)t * ngv + c / Gv;
                 v[(long)t * D + c] = orc_affine_dequant(code, vsz[j * 2], vsz[j * 2 + 1]);
             } else {
@@ -738,7 +788,7 @@ ORC_API void orc_kivi_decode_one(int D, int G, int Gv, int R, int L, int n_heads
                                  const uint8_t *vc, const uint16_t *vsz,
                                  const uint16_t *kres, const uint16_t *vres, double *out)
 {
-    orc_kivi_decode_one_w(D, G, Gv, R, L, 2, 2, n_heads, sm_scale, q, kc, ksz, vc, vsz, kres, vres, out);
+    orc_kivi_decode_one_w(D, G, Gv, R, L, 2, 2, 0, n_heads, sm_scale, q, kc, ksz, vc, vsz, kres, vres, out);
 }
 
 /* Kitty cache of one (batch row, kv head) with L tokens, sink S, page G,

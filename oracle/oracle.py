@@ -67,7 +67,10 @@ def _declare(l):
         "orc_kivi_key_bit_w": (I, [I, I]),
         "orc_kivi_key_pack_w": (I, [I, I, I, P, L, P]),
         "orc_tokenmajor_pack_w": (None, [I, I, P, L, P]),
-        "orc_kivi_decode_one_w": (None, [I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P]),
+        "orc_kivi_value_byte_offset": (L, [I, I]),
+        "orc_kivi_value_bit": (I, [I]),
+        "orc_kivi_value_pack_w": (I, [I, I, I, P, L, P]),
+        "orc_kivi_decode_one_w": (None, [I, I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P]),
         "orc_kivi_key_sz_index": (I, [I]),
         "orc_kivi_key_sz_pack": (I, [I, P, L, P]),
         "orc_kivi_value_codes": (None, [I, I, I, P, L, P, P]),
@@ -202,9 +205,28 @@ def tokenmajor_pack(codes: np.ndarray, bits: int = 2) -> np.ndarray:
     return out
 
 
-def kivi_quant_value(x: np.ndarray, group: int = 32, bits: int = 2):
+def kivi_value_byte_offset(t: int, c: int) -> int:
+    return lib().orc_kivi_value_byte_offset(t, c)
+
+
+def kivi_value_bit(c: int) -> int:
+    return lib().orc_kivi_value_bit(c)
+
+
+def kivi_value_pack(codes: np.ndarray, bits: int = 2, tiles: bool = False) -> np.ndarray:
+    """Value codes [n][D] -> the stored bytes as rows of D*bits/8: token-major (one row per token), or with
+    tiles (2 bits) ceil(n/32) 32-token value tiles (32 rows each, in the tile order)."""
+    n, Dm = codes.shape
+    rows = (n + 31) // 32 * 32 if tiles else n
+    out = np.zeros((rows, Dm * bits // 8), np.uint8)
+    if lib().orc_kivi_value_pack_w(Dm, bits, int(tiles), _p(np.ascontiguousarray(codes)), n, _p(out)):
+        raise ValueError("KIVI value packing needs D == 128, 2 or 4 bits, and 2 bits for tiles")
+    return out
+
+
+def kivi_quant_value(x: np.ndarray, group: int = 32, bits: int = 2, tiles: bool = False):
     codes, sz = kivi_value_codes(x, group, bits)
-    return tokenmajor_pack(codes, bits), sz
+    return kivi_value_pack(codes, bits, tiles), sz
 
 
 # ---------------------------------------------------------------------------
@@ -343,12 +365,13 @@ def attend_fp16(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: float) ->
     return out
 
 
-def kivi_decode_one(q, kc, ksz, vc, vsz, kres, vres, L, G=32, Gv=32, R=128, sm_scale=None, bits_k=2, bits_v=2):
+def kivi_decode_one(q, kc, ksz, vc, vsz, kres, vres, L, G=32, Gv=32, R=128, sm_scale=None, bits_k=2, bits_v=2,
+                    value_tiles=False):
     """One (batch row, kv head): q fp16 [g][D] -> binary64 [g][D]."""
     g, Dm = q.shape
     sm = (1.0 / np.sqrt(Dm)) if sm_scale is None else sm_scale
     out = np.zeros((g, Dm), np.float64)
-    lib().orc_kivi_decode_one_w(Dm, G, Gv, R, L, bits_k, bits_v, g, sm, _p(_h16(q)), _p(np.ascontiguousarray(kc)),
+    lib().orc_kivi_decode_one_w(Dm, G, Gv, R, L, bits_k, bits_v, int(value_tiles), g, sm, _p(_h16(q)), _p(np.ascontiguousarray(kc)),
                                 _p(_h16(ksz)), _p(np.ascontiguousarray(vc)), _p(_h16(vsz)),
                                 _p(_h16(kres)), _p(_h16(vres)), _p(out))
     return out
@@ -390,7 +413,7 @@ def kivi_segments(L: int, R: int = 128):
 
 
 def kivi_build_one(K: np.ndarray, V: np.ndarray, G: int = 32, Gv: int = 32, R: int = 128, bits_k: int = 2,
-                   bits_v: int = 2):
+                   bits_v: int = 2, value_tiles: bool = False):
     """fp16 K, V [L][D] -> (kc, ksz, vc, vsz, kres, vres) for one (b, kvh)."""
     L, Dm = K.shape
     nkq, nvq = kivi_segments(L, R)
@@ -401,7 +424,7 @@ def kivi_build_one(K: np.ndarray, V: np.ndarray, G: int = 32, Gv: int = 32, R: i
         kc = np.zeros((0, G * Dm * bits_k // 8), np.uint8)
         ksz = np.zeros((0, Dm, 2), np.uint16)
     if nvq:
-        vc, vsz = kivi_quant_value(V[:nvq], Gv, bits_v)
+        vc, vsz = kivi_quant_value(V[:nvq], Gv, bits_v, value_tiles)
     else:
         vc = np.zeros((0, Dm * bits_v // 8), np.uint8)
         vsz = np.zeros((0, Dm // Gv, 2), np.uint16)

@@ -64,15 +64,25 @@ def test_quant_value_bitexact(K, orc, Gv, kind):
     rng = np.random.default_rng(200 + Gv)
     n = 333
     x = _rand_fp16(rng, (n, 128), kind)
-    cfg = K.make_config(group_v=Gv)
-    xd = torch.from_numpy(x).to(DEV)
-    codes = torch.full((n, 32), 0xAB, dtype=torch.uint8, device=DEV)
-    sz = torch.full((n, 128 // Gv), -1, dtype=torch.int32, device=DEV)
-    K.kv_quant_value(cfg, xd, n, codes, sz)
-    torch.cuda.synchronize()
-    ref_codes, ref_sz = orc.kivi_quant_value(x, Gv)
-    assert np.array_equal(codes.cpu().numpy(), ref_codes)
-    assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, 128 // Gv, 2), ref_sz)
+    for Hq, Hkv in ((4, 4), (8, 2)):                # one query head per kv head: token-major; four: value tiles
+        tiles = Hq // Hkv == 4
+        cfg = K.make_config(group_v=Gv, n_q_heads=Hq, n_kv_heads=Hkv)
+        xd = torch.from_numpy(x).to(DEV)
+        rows = (n + 31) // 32 * 32 if tiles else n  # whole 32-token value tiles
+        codes = torch.full((rows, 32), 0xAB, dtype=torch.uint8, device=DEV)
+        sz = torch.full((n, 128 // Gv), -1, dtype=torch.int32, device=DEV)
+        K.kv_quant_value(cfg, xd, n, codes, sz)
+        torch.cuda.synchronize()
+        ref_codes, ref_sz = orc.kivi_quant_value(x, Gv, tiles=tiles)
+        got = codes.cpu().numpy().reshape(-1)
+        if tiles:
+            written = np.zeros(got.size, bool)
+            written[[orc.kivi_value_byte_offset(t, c) for t in range(n) for c in range(0, 128, 4)]] = True
+            assert np.array_equal(got[written], ref_codes.reshape(-1)[written])
+            assert np.all(got[~written] == 0xAB)    # the last tile's bytes past token n are left unchanged
+        else:
+            assert np.array_equal(got, ref_codes.reshape(-1))
+        assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, 128 // Gv, 2), ref_sz)
 
 
 def _run_decode(K, cfg, Ks, Vs, q, max_seq_len):

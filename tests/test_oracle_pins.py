@@ -187,6 +187,60 @@ def test_kivi_key_layout_4bit_is_a_lane_friendly_bijection(orc):
     assert all(len(v) == 1 for v in seen.values()) and len(seen) == 64 * 128
 
 
+def test_kivi_value_layout_is_a_lane_friendly_bijection(orc):
+    """2-bit KIVI values in 32-token tiles in the fragment order of a tensor-core value product: a byte
+    holds four channels 32g + 4q + {0..3} of one token; word 4q + r of a 16-token half holds that byte
+    (g, q) of tokens r, r + 4, r + 8, r + 12; lane 4q + r's 16 bytes are its words for g = 0..3."""
+    seen = set()
+    for t in range(64):
+        for c in range(128):
+            off, bit = orc.kivi_value_byte_offset(t, c), orc.kivi_value_bit(c)
+            tt, g, q = t % 32, c // 32, (c % 32) // 4
+            assert off // 1024 == t // 32 and (off % 1024) // 512 == tt // 16
+            assert (off % 512) // 16 == 4 * q + tt % 4            # the lane's 16 bytes
+            assert (off % 16) // 4 == g and off % 4 == (tt % 16) // 4
+            assert bit == 2 * (c % 4)
+            seen.add((off, bit))
+    assert len(seen) == 64 * 128 and {o for o, _ in seen} == set(range(2048))
+
+
+def test_kivi_value_pack_roundtrip_and_tail(orc):
+    rng = np.random.default_rng(66)
+    for n in (1, 31, 32, 45, 96):
+        codes = rng.integers(0, 4, (n, 128)).astype(np.uint8)
+        packed = orc.kivi_value_pack(codes, 2, tiles=True)
+        assert packed.shape == ((n + 31) // 32 * 32, 32)
+        flat = packed.reshape(-1)
+        got = np.zeros_like(codes)
+        written = np.zeros(flat.size, bool)
+        for t in range(n):
+            for c in range(128):
+                o = orc.kivi_value_byte_offset(t, c)
+                got[t, c] = (flat[o] >> orc.kivi_value_bit(c)) & 3
+                written[o] = True
+        assert np.array_equal(got, codes)
+        assert not flat[~written].any()                        # tokens past n leave zero bytes
+        # without tiles: one token-major row per token, as tokenmajor_pack
+        assert np.array_equal(orc.kivi_value_pack(codes, 2), orc.tokenmajor_pack(codes, 2))
+        c4 = rng.integers(0, 16, (n, 128)).astype(np.uint8)
+        assert np.array_equal(orc.kivi_value_pack(c4, 4), orc.tokenmajor_pack(c4, 4))
+
+
+def test_kivi_decode_reads_both_value_layouts(orc):
+    """The same cache stored with value tiles or token-major decodes to the same binary64 output."""
+    rng = np.random.default_rng(67)
+    L = 333
+    K = rng.standard_normal((L, 128)).astype(np.float16)
+    V = (rng.standard_normal((L, 128)) * 10 ** rng.uniform(-1, 1, 128)).astype(np.float16)
+    q = rng.standard_normal((2, 128)).astype(np.float16)
+    a = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V), L=L)
+    b = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V, value_tiles=True), L=L, value_tiles=True)
+    assert np.array_equal(a, b)
+    # and the tile bytes are read as tiles: a decode told the wrong layout differs
+    c = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V, value_tiles=True), L=L)
+    assert not np.allclose(a, c, atol=1e-3)
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_kivi_key_pack_roundtrip_any_width(orc, bits):
     rng = np.random.default_rng(60 + bits)
