@@ -19,7 +19,10 @@
 //   (fp16, exact) in every row, B = the hi / lo parts of alpha q_hc 2^sigma_h.
 // Values:
 //   O[c, n]  = sum_t A[c, t] B[t, n]
-//   A[c, t] = code_tc * 2^-9 or 2^-7 (same unpacking, channel rows);
+//   A[c, t] = code_tc * 2^-9 or 2^-7 (same unpacking, channel rows; at 2 bits
+//             the cache's value tiles hold each lane's A words of a 16-token
+//             k-step in one 16-byte chunk, at 4 bits they are gathered from
+//             the token-major rows);
 //   B[t, n] = hi / lo parts of p_ht s_tg (p kept as fp16 hi + lo);
 //   o_hc     = (O[c, 2h] + O[c, 2h+1]) 2^(9|7) + sum_t p_ht z_tg,
 //   the zero-point term again on the tensor cores: A row g = z_tg (rows
