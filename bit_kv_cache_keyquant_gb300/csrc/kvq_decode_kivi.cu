@@ -296,22 +296,12 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_kernel(Param
             // ---- warp state -> shared memory (channel order) ----
             {
                 const float l_w = warp_sum(l_part);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float a = lo2f(vacc2[i]), c = hi2f(vacc2[i]);
-#pragma unroll
-                    for (int o = 4; o <= 16; o <<= 1) {
-                        a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-                        c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-                    }
-                    vacc2[i] = pack2f(a, c);
-                }
                 float vb = vbias;
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 8);
                 vb += __shfl_xor_sync(0xFFFFFFFFu, vb, 16);
                 // lane (ts, jg) writes channels 32jg + 4ts + i (i = 0..3) plus the zero-point term
-                float4 w4 = BV == 2 ? value_block_channels(vacc2, ts) : value_block_channels4(vacc2, ts);
+                float4 w4 = value_block_reduce<BV>(vacc2, ts);
                 w4.x += vb; w4.y += vb; w4.z += vb; w4.w += vb;
                 *reinterpret_cast<float4 *>(&S.st_acc[warp][32 * jg + 4 * ts]) = w4;
                 if (lane == 0) {

@@ -166,7 +166,7 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // is the denormal code * 2^(k-149) (k = 2i, or 8 + 2i for odd bytes).  One
 // weight pair ps * (2^(149-EV), 2^(141-EV)) serves every bit position, so a
 // packed fma.rn.f32x2 adds code * ps * 2^(2i-EV): accumulator i carries an
-// extra 2^(2i), removed once per unit by value_block_channels.
+// extra 2^(2i), removed once per unit by value_block_reduce.
 // acc2[8*wi + 4*ab + i] holds channels (16 wi + 8 ab + i, 16 wi + 8 ab + 4 + i)
 // of the block.  |p s| < 2^16 keeps the weights below 2^127.
 // ---------------------------------------------------------------------------
@@ -185,28 +185,6 @@ __device__ __forceinline__ void value_token_accum(uint2 codes, float ps, unsigne
             acc2[8 * wi + 4 + i] = ffma2(pack2u(w16 & m0, w16 & m1), wt, acc2[8 * wi + 4 + i]);
         }
     }
-}
-
-// Channels 4*ts .. 4*ts+3 of the 32-channel block (ts = 0..7) from acc2,
-// scaled back by 2^(KVQ_EV - 2i) (compile-time indices only).
-__device__ __forceinline__ float4 value_block_channels(const unsigned long long acc2[16], int ts) {
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int t8 = 0; t8 < 8; ++t8) {
-        if (ts == t8) {
-            // offset 4*t8: wi = t8 / 4, ab = (t8 / 2) % 2, odd byte = t8 % 2
-            const int base = 8 * (t8 / 4) + 4 * ((t8 / 2) % 2);
-            if (t8 % 2 == 0)
-                r = make_float4(lo2f(acc2[base]), lo2f(acc2[base + 1]), lo2f(acc2[base + 2]), lo2f(acc2[base + 3]));
-            else
-                r = make_float4(hi2f(acc2[base]), hi2f(acc2[base + 1]), hi2f(acc2[base + 2]), hi2f(acc2[base + 3]));
-        }
-    }
-    r.x *= __int_as_float((127 + KVQ_EV) << 23);
-    r.y *= __int_as_float((127 + KVQ_EV - 2) << 23);
-    r.z *= __int_as_float((127 + KVQ_EV - 4) << 23);
-    r.w *= __int_as_float((127 + KVQ_EV - 6) << 23);
-    return r;
 }
 
 // The 4-bit form: the token's 16 bytes (32 4-bit codes, channel 2b + i of
@@ -230,20 +208,48 @@ __device__ __forceinline__ void value_token_accum4(uint4 codes, float ps, unsign
     }
 }
 
-// Channels 4*ts .. 4*ts+3 of the block from the 4-bit accumulators: channel
-// 4ts + x is acc2[2ts + (x & 1)], low half for x < 2, scaled by 2^(KVQ_EV - 4(x & 1)).
-__device__ __forceinline__ float4 value_block_channels4(const unsigned long long acc2[16], int ts) {
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+// Packed fp32 add, and a 64-bit register pair exchanged across lanes.
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long shfl_xor2(unsigned long long v, int o) {
+    return pack2f(__shfl_xor_sync(0xFFFFFFFFu, lo2f(v), o), __shfl_xor_sync(0xFFFFFFFFu, hi2f(v), o));
+}
+
+// The value accumulators summed over the eight lanes of a channel block (lanes 4ts + jg, ts = 0..7),
+// with the result scattered: lane ts keeps channels 4ts .. 4ts + 3 of the block, scaled back by their
+// bit-position powers.  At 2 bits channel 4ts + i is half ts % 2 of acc2[8 (ts / 4) + 4 ((ts / 2) % 2) + i]
+// carrying 2^(2i - EV); at 4 bits channel 4ts + x is acc2[2ts + (x & 1)], low half for x < 2, carrying
+// 2^(4 (x & 1) - EV).  Three exchange levels over the lane bits 4, 3, 2 (ts bits 2, 1, 0), each keeping
+// the half of the remaining floats that the lane's side owns: pairs 8b .. 8b + 7 (b = ts bit 2), then four
+// of them (ts bit 1), then one half of each of the four pairs (2 bits) or two of the pairs (4 bits).
+template <int BV>
+__device__ __forceinline__ float4 value_block_reduce(const unsigned long long acc2[16], int ts) {
+    const bool b2 = (ts & 4) != 0, b1 = (ts & 2) != 0, b0 = (ts & 1) != 0;
+    unsigned long long a8[8], a4[4];
 #pragma unroll
-    for (int t8 = 0; t8 < 8; ++t8) {
-        if (ts == t8)
-            r = make_float4(lo2f(acc2[2 * t8]), lo2f(acc2[2 * t8 + 1]), hi2f(acc2[2 * t8]), hi2f(acc2[2 * t8 + 1]));
+    for (int k = 0; k < 8; ++k)
+        a8[k] = add2(b2 ? acc2[8 + k] : acc2[k], shfl_xor2(b2 ? acc2[k] : acc2[8 + k], 16));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a4[k] = add2(b1 ? a8[4 + k] : a8[k], shfl_xor2(b1 ? a8[k] : a8[4 + k], 8));
+    if (BV == 2) {
+        float f[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            f[k] = (b0 ? hi2f(a4[k]) : lo2f(a4[k])) + __shfl_xor_sync(0xFFFFFFFFu, b0 ? lo2f(a4[k]) : hi2f(a4[k]), 4);
+        return make_float4(f[0] * __int_as_float((127 + KVQ_EV) << 23), f[1] * __int_as_float((127 + KVQ_EV - 2) << 23),
+                           f[2] * __int_as_float((127 + KVQ_EV - 4) << 23), f[3] * __int_as_float((127 + KVQ_EV - 6) << 23));
+    } else {
+        unsigned long long a2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) a2[k] = add2(b0 ? a4[2 + k] : a4[k], shfl_xor2(b0 ? a4[k] : a4[2 + k], 4));
+        return make_float4(lo2f(a2[0]) * __int_as_float((127 + KVQ_EV) << 23),
+                           lo2f(a2[1]) * __int_as_float((127 + KVQ_EV - 4) << 23),
+                           hi2f(a2[0]) * __int_as_float((127 + KVQ_EV) << 23),
+                           hi2f(a2[1]) * __int_as_float((127 + KVQ_EV - 4) << 23));
     }
-    r.x *= __int_as_float((127 + KVQ_EV) << 23);
-    r.y *= __int_as_float((127 + KVQ_EV - 4) << 23);
-    r.z *= __int_as_float((127 + KVQ_EV) << 23);
-    r.w *= __int_as_float((127 + KVQ_EV - 4) << 23);
-    return r;
 }
 
 __device__ __forceinline__ void scale_pairs(unsigned long long acc2[16], float sc) {
