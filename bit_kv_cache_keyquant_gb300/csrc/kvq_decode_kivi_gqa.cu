@@ -19,10 +19,9 @@
 //   (fp16, exact) in every row, B = the hi / lo parts of alpha q_hc 2^sigma_h.
 // Values:
 //   O[c, n]  = sum_t A[c, t] B[t, n]
-//   A[c, t] = code_tc * 2^-9 or 2^-7 (same unpacking, channel rows; at 2 bits
-//             the cache's value tiles hold each lane's A words of a 16-token
-//             k-step in one 16-byte chunk, at 4 bits they are gathered from
-//             the token-major rows);
+//   A[c, t] = code_tc * 2^-9 or 2^-7 (same unpacking, channel rows; the
+//             cache's value tiles hold each lane's A words of a 16-token
+//             k-step in one 16-byte chunk at 2 bits, two at 4 bits);
 //   B[t, n] = hi / lo parts of p_ht s_tg (p kept as fp16 hi + lo);
 //   o_hc     = (O[c, 2h] + O[c, 2h+1]) 2^(9|7) + sum_t p_ht z_tg,
 //   the zero-point term again on the tensor cores: A row g = z_tg (rows
@@ -109,9 +108,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
     const int hB = q >> 1;                         // head of this lane's B column (n = q)
     const bool xB = (q & 1) != 0;                  // B column holds lo parts
     const int gl = (32 * warp) / P.G;              // key group of this warp's tile within a stage
-    // 4-bit values: channel 16mt + q (+8) is byte q/2 of the m-tile's first (second) word, bits 4(q%2)
-    const uint32_t vsel4 = (uint32_t)((q >> 1) | ((4 + (q >> 1)) << 4));
-    const uint32_t vshift4 = (q & 1) ? 4u : 0u;
     const uint32_t *qown = xB ? S.qlo[hB] : S.qhi[hB];   // the part of B column n = q (zero-point products)
     const int jz = q % NGV;                               // value group of rows q, q + 8 of the zero-point product
     bool ok = true;
@@ -353,29 +349,23 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(P
                             }
                         }
                         if (BV == 4) {
-                            // 32 channels (two m-tiles) per quarter: 16 bytes of each of the lane's token rows
+                            // the 4-bit value tile: lane 4q + r's 32 bytes of k-step ks are words 2m + w, m-tile m
+                            // (channels 16m + q | + 8) in the low nibbles and m-tile m + 4 in the high nibbles, tokens
+                            // t0, t0+4 (w = 0: k-columns 2r, 2r+1) and t0+8, t0+12 (w = 1: 2r+8, 2r+9)
+                            const uint4 va = *reinterpret_cast<const uint4 *>(vc + ks * 1024 + lane * 32);
+                            const uint4 vb4 = *reinterpret_cast<const uint4 *>(vc + ks * 1024 + lane * 32 + 16);
+                            const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb4.x, vb4.y, vb4.z, vb4.w};
 #pragma unroll
-                            for (int qt = 0; qt < 4; ++qt) {
-                                const uint4 rA = *reinterpret_cast<const uint4 *>(vc + t0 * 64 + 16 * qt);
-                                const uint4 rB = *reinterpret_cast<const uint4 *>(vc + (t0 + 4) * 64 + 16 * qt);
-                                const uint4 rC = *reinterpret_cast<const uint4 *>(vc + (t0 + 8) * 64 + 16 * qt);
-                                const uint4 rD = *reinterpret_cast<const uint4 *>(vc + (t0 + 12) * 64 + 16 * qt);
-                                const uint32_t wa[4] = {rA.x, rA.y, rA.z, rA.w}, wb[4] = {rB.x, rB.y, rB.z, rB.w};
-                                const uint32_t wc[4] = {rC.x, rC.y, rC.z, rC.w}, wd[4] = {rD.x, rD.y, rD.z, rD.w};
-#pragma unroll
-                                for (int m2 = 0; m2 < 2; ++m2) {
-                                    const int mt = 2 * qt + m2;
-                                    const int j = (16 * mt) / (KVQ_D / NGV);
-                                    // channel q of tokens (a, b) | channel q + 8 of tokens (a, b)
-                                    const uint32_t x0 = prmt(prmt(wa[2 * m2], wb[2 * m2], vsel4),
-                                                             prmt(wa[2 * m2 + 1], wb[2 * m2 + 1], vsel4), 0x5410u);
-                                    const uint32_t x1 = prmt(prmt(wc[2 * m2], wd[2 * m2], vsel4),
-                                                             prmt(wc[2 * m2 + 1], wd[2 * m2 + 1], vsel4), 0x5410u);
-                                    uint32_t c0l, c0h, c8l, c8h;
-                                    e4m3x4_f16x2((x0 >> vshift4) & 0x0F0F0F0Fu, c0l, c0h);
-                                    e4m3x4_f16x2((x1 >> vshift4) & 0x0F0F0F0Fu, c8l, c8h);
-                                    mma16816(vacc[mt], c0l, c0h, c8l, c8h, bv0[j], bv1[j]);
-                                }
+                            for (int m = 0; m < 4; ++m) {
+                                const uint32_t x0 = vw[2 * m], x1 = vw[2 * m + 1];
+                                const int jl = (16 * m) / (KVQ_D / NGV), jh = (16 * (m + 4)) / (KVQ_D / NGV);
+                                uint32_t a0, a1, a2, a3;
+                                e4m3x4_f16x2(x0 & 0x0F0F0F0Fu, a0, a1);
+                                e4m3x4_f16x2(x1 & 0x0F0F0F0Fu, a2, a3);
+                                mma16816(vacc[m], a0, a1, a2, a3, bv0[jl], bv1[jl]);
+                                e4m3x4_f16x2((x0 >> 4) & 0x0F0F0F0Fu, a0, a1);
+                                e4m3x4_f16x2((x1 >> 4) & 0x0F0F0F0Fu, a2, a3);
+                                mma16816(vacc[m + 4], a0, a1, a2, a3, bv0[jh], bv1[jh]);
                             }
                         } else {
                             // m-tile 2g + pp, rows q | q + 8: channels 32g + 4q + 2pp + 0 | 1 (bit positions 2pp and
@@ -487,7 +477,7 @@ int kivi_gqa_units_per_kv_head(const kvq_config *cfg) {
     return g > GMAX ? 2 : 1;
 }
 
-bool kivi_value_tiles(const kvq_config *cfg) { return cfg->bits_v == 2 && kivi_gqa_supported(cfg); }
+bool kivi_value_tiles(const kvq_config *cfg) { return kivi_gqa_supported(cfg); }
 
 bool kivi_gqa_supported(const kvq_config *cfg) {
     const int g = cfg->n_q_heads / cfg->n_kv_heads;

@@ -66,6 +66,16 @@ __host__ __device__ constexpr int64_t kivi_value_byte(int64_t t, int c4) {
     return (t >> 5) * 1024 + ((t >> 4) & 1) * 512 + (4 * (c4 & 7) + (int)(t & 3)) * 16 + 4 * (c4 >> 3) + (int)((t >> 2) & 3);
 }
 
+// Byte offset of channel c of token t in 4-bit KIVI value tiles (32-token tiles of 2048 bytes); the code is
+// nibble c / 64 of the byte, which holds channels c % 64 and c % 64 + 64 of one token.  With
+// t % 32 = 16 kv + 8 w + 4 s + r and c % 64 = 16 m + 8 h + q the byte is
+// tile * 2048 + kv * 1024 + (4q + r) * 32 + (2m + w) * 4 + 2h + s: lane 4q + r finds in its 32 bytes of a
+// 16-token half the A words of m-tiles m (low nibbles) and m + 4 (high nibbles), two words each.
+__host__ __device__ constexpr int64_t kivi_value_byte4(int64_t t, int c) {
+    return (t >> 5) * 2048 + ((t >> 4) & 1) * 1024 + (4 * (c & 7) + (int)(t & 3)) * 32 +
+           (2 * ((c & 63) >> 4) + (int)((t >> 3) & 1)) * 4 + 2 * ((c >> 3) & 1) + (int)((t >> 2) & 1);
+}
+
 // Rows of a Kitty key page's high plane: the K boosted channels rounded up to
 // a multiple of 4 (each 4-byte word of the plane holds a group of four rows).
 __host__ __device__ constexpr int kitty_high_rows(int K) { return (K + 3) & ~3; }
@@ -137,8 +147,8 @@ cudaError_t launch_decode_kivi(const kvq_config *cfg, const KiviSrc &c, const vo
                                const DecodePlan &p, void *ws, cudaStream_t st);
 // grouped-query KIVI decode on the tensor cores (2 <= n_q_heads / n_kv_heads <= 4)
 bool kivi_gqa_supported(const kvq_config *cfg);
-// 2-bit KIVI value codes of a config that decodes on the grouped-query kernel are stored in its value
-// tiles (kivi_value_byte); every other KIVI value cache is token-major
+// KIVI value codes of a config that decodes on the grouped-query kernel are stored in its value tiles
+// (kivi_value_byte at 2 bits, kivi_value_byte4 at 4 bits); every other KIVI value cache is token-major
 bool kivi_value_tiles(const kvq_config *cfg);
 int kivi_gqa_units_per_kv_head(const kvq_config *cfg);   // 1, or 2 for 4 < g <= 8
 cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, const void *q,

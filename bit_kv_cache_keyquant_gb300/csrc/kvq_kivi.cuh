@@ -50,7 +50,7 @@ struct Params {
     int64_t kgrp_cap;   // cap / G
     float alpha;
     int bits_k, bits_v; // code widths (2 or 4)
-    int vtiles;         // 2-bit values stored in value tiles (kivi_value_tiles), else token-major
+    int vtiles;         // values stored in value tiles (kivi_value_tiles), else token-major
     // paged cache (page_table non-null): token t of row b is in page record
     // pages + (page_table[b * pt_stride + t / 128] * Hkv + kv head) * rec_bytes
     const int32_t *page_table;
@@ -208,9 +208,17 @@ __device__ __forceinline__ void fetch_v4(const Params &P, const Unit &U, int t, 
             vb = P.v_codes + U.bk * P.cap * (KVQ_D * bits / 8);
             szr = P.v_sz + (U.bk * P.cap + t) * P.ngv;
         }
-        const uint32_t w = P.vtiles    ? (uint32_t)vb[kivi_value_byte(tl, lane)]
-                           : bits == 2 ? (uint32_t)vb[tl * (KVQ_D / 4) + lane]
-                                       : (uint32_t)reinterpret_cast<const uint16_t *>(vb + tl * (KVQ_D / 2))[lane];
+        uint32_t w;
+        if (P.vtiles && bits == 2) {
+            w = vb[kivi_value_byte(tl, lane)];
+        } else if (P.vtiles) {
+            w = 0u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w |= ((uint32_t)(vb[kivi_value_byte4(tl, 4 * lane + i)] >> (4 * (lane >> 4))) & 15u) << (4 * i);
+        } else {
+            w = bits == 2 ? (uint32_t)vb[tl * (KVQ_D / 4) + lane]
+                          : (uint32_t)reinterpret_cast<const uint16_t *>(vb + tl * (KVQ_D / 2))[lane];
+        }
         const uint32_t sz = szr[(4 * lane) / P.Gv];
 #pragma unroll
         for (int i = 0; i < 4; ++i)

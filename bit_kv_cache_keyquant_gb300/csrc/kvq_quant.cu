@@ -220,12 +220,21 @@ __device__ __forceinline__ void value_token_store(uint8_t *__restrict__ tok, int
         if ((lane & 1) == 0) reinterpret_cast<uint32_t *>(tok)[lane >> 1] = wv;
     }
 }
+// Every lane calls it (a shuffle at 4 bits): there lanes 2j hold channels 8j .. 8j + 7 as nibbles, and lane
+// 2j < 16 writes the bytes of channels 8j + k with 8j + k + 64 (from lane 2j + 16) in the high nibble.
 __device__ __forceinline__ void value_token_store_kivi(uint8_t *__restrict__ codes, int64_t t, int lane, uint32_t wv,
                                                        int bits, bool tiles) {
-    if (tiles) {
+    if (tiles && bits == 2) {
         if ((lane & 3) == 0) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) codes[kivi_value_byte(t, lane + k)] = (uint8_t)(wv >> (8 * k));
+        }
+    } else if (tiles) {
+        const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, wv, 16);
+        if ((lane & 1) == 0 && lane < 16) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                codes[kivi_value_byte4(t, 4 * lane + k)] = (uint8_t)(((wv >> (4 * k)) & 15u) | (((hi >> (4 * k)) & 15u) << 4));
         }
     } else {
         value_token_store(codes + t * (KVQ_D * bits / 8), lane, wv, bits);
@@ -306,16 +315,35 @@ __global__ void __launch_bounds__(256, 3) quant_value_kernel(const uint16_t *__r
                 else w[i / 8] |= code << (4 * (i % 8));
             }
         }
+        // 4-bit tiles pair channel c with c + 64 in a byte: lane cb < 4 takes the codes of lane cb + 4
+        uint32_t w64[2] = {0u, 0u};
+        if constexpr (BITS == 4 && !KITTY) {
+            if (tiles) {
+                w64[0] = __shfl_down_sync(0xFFFFFFFFu, w[0], 4);
+                w64[1] = __shfl_down_sync(0xFFFFFFFFu, w[1], 4);
+            }
+        }
         if (!live) continue;
         if (!KITTY) {
-            if (BITS == 2 && tiles) {
+            if constexpr (BITS == 4) {
+                if (tiles) {
+                    // channels 16cb + k with 16cb + k + 64 in one byte of the 4-bit value tiles
+                    if (cb < 4) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const uint32_t lo = (w[k / 8] >> (4 * (k % 8))) & 15u, hi = (w64[k / 8] >> (4 * (k % 8))) & 15u;
+                            out[kivi_value_byte4(t, 16 * cb + k)] = (uint8_t)(lo | (hi << 4));
+                        }
+                    }
+                } else {
+                    reinterpret_cast<uint2 *>(out + t * (KVQ_D / 2))[cb] = make_uint2(w[0], w[1]);
+                }
+            } else if (tiles) {
                 // channel quads 4cb .. 4cb + 3 of token t into the 32-token value tiles
 #pragma unroll
                 for (int k = 0; k < 4; ++k) out[kivi_value_byte(t, 4 * cb + k)] = (uint8_t)(w[0] >> (8 * k));
-            } else if (BITS == 2) {
-                reinterpret_cast<uint32_t *>(out + t * (KVQ_D / 4))[cb] = w[0];
             } else {
-                reinterpret_cast<uint2 *>(out + t * (KVQ_D * BITS / 8))[cb] = make_uint2(w[0], w[BITS / 2 - 1]);
+                reinterpret_cast<uint32_t *>(out + t * (KVQ_D / 4))[cb] = w[0];
             }
             if (cb % LG == 0) sz[t * (KVQ_D / GV) + cb / LG] = (uint32_t)s | ((uint32_t)z << 16);
         } else {
@@ -659,7 +687,7 @@ struct AppendParams {
     uint16_t *k_res, *v_res;
     unsigned *err;
     int Hkv, R, G, ngv, max_seq_len, bits_k, bits_v;
-    int vtiles;                  // 2-bit values stored in value tiles (kivi_value_tiles)
+    int vtiles;                  // values stored in value tiles (kivi_value_tiles)
     int64_t cap, kgrp_cap;
 };
 
@@ -758,7 +786,7 @@ struct PagedDst {
     int pt_stride, n_pages, Hkv;
     int64_t rec_bytes;
     int kc_bytes, vc_bytes;
-    int vtiles;                  // 2-bit values stored in value tiles (kivi_value_tiles)
+    int vtiles;                  // values stored in value tiles (kivi_value_tiles)
     unsigned *err;
 };
 

@@ -53,14 +53,18 @@
  *     (s, z) [D/Gv] per token.
  *   KIVI value tiles: a config whose query heads decode on the grouped-query
  *     tensor-core kernel (2 <= n_q_heads / n_kv_heads <= 4, or an even ratio
- *     up to 8) with 2-bit values stores its value codes in 32-token tiles of
- *     1024 bytes instead (the tile of token t is tile t/32 of its (batch row,
- *     kv head) or page record).  With t % 32 = 16kv + 4i + r and
- *     c = 32g + 4q + p, the code sits in bits 2p of byte
- *     (t/32)*1024 + kv*512 + (4q + r)*16 + 4g + i: a byte holds four channels
- *     of one token, and lane 4q + r of a warp finds byte 8g + q of the tokens
- *     r, r+4, r+8, r+12 of each 16-token half, g = 0..3, in one 16-byte chunk
- *     (the A operands of the tensor-core value products).
+ *     up to 8; at 4-bit widths with Gv = 32) stores its value codes in
+ *     32-token tiles instead (the tile of token t is tile t/32 of its (batch
+ *     row, kv head) or page record), in the order of the A operands of the
+ *     tensor-core value products.  2 bits, tiles of 1024 bytes: with
+ *     t % 32 = 16kv + 4i + r and c = 32g + 4q + p, the code sits in bits 2p
+ *     of byte (t/32)*1024 + kv*512 + (4q + r)*16 + 4g + i (a byte holds four
+ *     channels of one token; lane 4q + r finds byte 8g + q of the tokens r,
+ *     r+4, r+8, r+12 of each 16-token half, g = 0..3, in one 16-byte chunk).
+ *     4 bits, tiles of 2048 bytes: with t % 32 = 16kv + 8w + 4s + r and
+ *     c % 64 = 16m + 8h + q, the code sits in nibble c/64 of byte
+ *     (t/32)*2048 + kv*1024 + (4q + r)*32 + (2m + w)*4 + 2h + s (a byte holds
+ *     channels c % 64 and c % 64 + 64 of one token).
  *   Kitty key page (G = 128 tokens, K boosted channels), one record of
  *     kvq_kitty_key_page_bytes() bytes: low plane (D*G/4 bytes, code & 3 of
  *     every channel), high plane (Kp*G/4 bytes, Kp = K rounded up to a
@@ -166,8 +170,8 @@ KVQ_API kvq_status kv_quant_key(const kvq_config *cfg, const void *k, int64_t n_
  * at b = cfg->bits_v bits (2 or 4).
  *   v       fp16 [n_tokens][D]
  *   codes   token-major uint8 [n_tokens][D*b/8], or, for a config stored in
- *           value tiles, ceil(n_tokens/32) tiles of 1024 bytes (token 0 of
- *           the call starts a tile; bytes of the last tile's tokens past
+ *           value tiles, ceil(n_tokens/32) tiles of 32*D*b/8 bytes (token 0
+ *           of the call starts a tile; bytes of the last tile's tokens past
  *           n_tokens are left unchanged)
  *   sz      fp16x2 [n_tokens][D/Gv]
  * Same rounding rules as kv_quant_key.  (KIVI section 3.3 value split.) */

@@ -358,22 +358,48 @@ ORC_API long orc_kivi_value_byte_offset(int t, int c)
 
 ORC_API int orc_kivi_value_bit(int c) { return 2 * (c % 4); }
 
-/* Value codes [n_tok][D] -> packed bytes: with tiles (2 bits only) the tile
- * order above (ceil(n_tok / 32) tiles; bytes of tokens past n_tok stay 0),
- * otherwise token-major (orc_tokenmajor_pack_w).  Returns 1 for other shapes. */
+/* The 4-bit value tiles: 32-token tiles of 2048 bytes.  A byte holds channels
+ * c and c + 64 (c < 64, low and high nibble) of one token.  With
+ * t % 32 = 16 kv + 8 w + 4 s + r (kv, w, s < 2, r < 4) and
+ * c % 64 = 16 m + 8 h + q (m < 4, h < 2, q < 8) the byte is
+ *   (t / 32) * 2048 + kv * 1024 + (4q + r) * 32 + (2m + w) * 4 + 2h + s
+ * and the nibble is c / 64: lane 4q + r's 32 bytes of a 16-token half are
+ * eight words, word 2m + w holding channels 16m + q (bytes 0, 1) and
+ * 16m + q + 8 (bytes 2, 3) of tokens r + 8w and r + 8w + 4 in its low nibbles
+ * and channels 64 + 16m + q, 64 + 16m + q + 8 in its high nibbles. */
+ORC_API long orc_kivi_value_byte_offset4(int t, int c)
+{
+    int tt = t % 32, kv = tt / 16, w = (tt / 8) % 2, s = (tt / 4) % 2, r = tt % 4;
+    int c64 = c % 64, m = c64 / 16, h = (c64 / 8) % 2, q = c64 % 8;
+    return (long)(t / 32) * 2048 + kv * 1024 + (4 * q + r) * 32 + (2 * m + w) * 4 + 2 * h + s;
+}
+
+ORC_API int orc_kivi_value_bit4(int c) { return 4 * (c / 64); }
+
+/* Value codes [n_tok][D] -> packed bytes: with tiles the tile orders above
+ * (ceil(n_tok / 32) tiles of 1024 or 2048 bytes; bytes of tokens past n_tok
+ * stay 0), otherwise token-major (orc_tokenmajor_pack_w).  Returns 1 for
+ * other shapes. */
 ORC_API int orc_kivi_value_pack_w(int D, int bits, int tiles, const uint8_t *codes, long n_tok, uint8_t *packed)
 {
-    if (D != 128 || (bits != 2 && bits != 4) || (tiles && bits != 2))
+    if (D != 128 || (bits != 2 && bits != 4))
         return 1;
     if (!tiles) {
         orc_tokenmajor_pack_w(D, bits, codes, n_tok, packed);
         return 0;
     }
-    memset(packed, 0, (size_t)((n_tok + 31) / 32 * 1024));
+    long tile = 16L * 32 * bits;
+    memset(packed, 0, (size_t)((n_tok + 31) / 32 * tile));
     for (long t = 0; t < n_tok; ++t)
-        for (int c = 0; c < D; ++c)
-            packed[orc_kivi_value_byte_offset((int)(t % 32), c) + (t / 32) * 1024] |=
-                (uint8_t)((codes[t * D + c] & 3) << orc_kivi_value_bit(c));
+        for (int c = 0; c < D; ++c) {
+            int code = codes[t * D + c] & ((1 << bits) - 1);
+            if (bits == 2)
+                packed[orc_kivi_value_byte_offset((int)(t % 32), c) + (t / 32) * tile] |=
+                    (uint8_t)(code << orc_kivi_value_bit(c));
+            else
+                packed[orc_kivi_value_byte_offset4((int)(t % 32), c) + (t / 32) * tile] |=
+                    (uint8_t)(code << orc_kivi_value_bit4(c));
+        }
     return 0;
 }
 
@@ -381,8 +407,10 @@ static int tokenmajor_code_at(int bits, const uint8_t *tok_bytes, int c);
 
 static int kivi_value_code_at(int bits, int tiles, const uint8_t *vc, long t, int c)
 {
-    if (tiles)
+    if (tiles && bits == 2)
         return (vc[(t / 32) * 1024 + orc_kivi_value_byte_offset((int)(t % 32), c)] >> orc_kivi_value_bit(c)) & 3;
+    if (tiles)
+        return (vc[(t / 32) * 2048 + orc_kivi_value_byte_offset4((int)(t % 32), c)] >> orc_kivi_value_bit4(c)) & 15;
     return tokenmajor_code_at(bits, vc + t * ((long)128 * bits / 8), c);
 }
 

@@ -69,6 +69,8 @@ def _declare(l):
         "orc_tokenmajor_pack_w": (None, [I, I, P, L, P]),
         "orc_kivi_value_byte_offset": (L, [I, I]),
         "orc_kivi_value_bit": (I, [I]),
+        "orc_kivi_value_byte_offset4": (L, [I, I]),
+        "orc_kivi_value_bit4": (I, [I]),
         "orc_kivi_value_pack_w": (I, [I, I, I, P, L, P]),
         "orc_kivi_decode_one_w": (None, [I, I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P]),
         "orc_kivi_key_sz_index": (I, [I]),
@@ -213,14 +215,22 @@ def kivi_value_bit(c: int) -> int:
     return lib().orc_kivi_value_bit(c)
 
 
+def kivi_value_byte_offset4(t: int, c: int) -> int:
+    return lib().orc_kivi_value_byte_offset4(t, c)
+
+
+def kivi_value_bit4(c: int) -> int:
+    return lib().orc_kivi_value_bit4(c)
+
+
 def kivi_value_pack(codes: np.ndarray, bits: int = 2, tiles: bool = False) -> np.ndarray:
     """Value codes [n][D] -> the stored bytes as rows of D*bits/8: token-major (one row per token), or with
-    tiles (2 bits) ceil(n/32) 32-token value tiles (32 rows each, in the tile order)."""
+    tiles ceil(n/32) 32-token value tiles (32 rows each, in the tile order)."""
     n, Dm = codes.shape
     rows = (n + 31) // 32 * 32 if tiles else n
     out = np.zeros((rows, Dm * bits // 8), np.uint8)
     if lib().orc_kivi_value_pack_w(Dm, bits, int(tiles), _p(np.ascontiguousarray(codes)), n, _p(out)):
-        raise ValueError("KIVI value packing needs D == 128, 2 or 4 bits, and 2 bits for tiles")
+        raise ValueError("KIVI value packing needs D == 128 and 2 or 4 bits")
     return out
 
 

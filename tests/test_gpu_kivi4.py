@@ -49,14 +49,26 @@ def test_quant_value_4bit_bitexact(K, orc, Gv, kind):
     rng = np.random.default_rng(500 + Gv)
     n = 257
     x = _data(rng, (n, D), kind)
-    cfg = K.make_config(group_v=Gv, bits_v=4)
-    codes = torch.full((n, D // 2), 0xAB, dtype=torch.uint8, device=DEV)
-    sz = torch.full((n, D // Gv), -1, dtype=torch.int32, device=DEV)
-    K.kv_quant_value(cfg, torch.from_numpy(x).to(DEV), n, codes, sz)
-    torch.cuda.synchronize()
-    ref_codes, ref_sz = orc.kivi_quant_value(x, Gv, 4)
-    assert np.array_equal(codes.cpu().numpy(), ref_codes)
-    assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, D // Gv, 2), ref_sz)
+    # one query head per kv head: token-major; four (the grouped-query kernel, 4-bit values at Gv = 32):
+    # 4-bit value tiles
+    for Hq, Hkv in ((4, 4), (8, 2)):
+        tiles = Hq // Hkv == 4 and Gv == 32
+        cfg = K.make_config(group_v=Gv, bits_v=4, bits_k=4, n_q_heads=Hq, n_kv_heads=Hkv)
+        rows = (n + 31) // 32 * 32 if tiles else n
+        codes = torch.full((rows, D // 2), 0xAB, dtype=torch.uint8, device=DEV)
+        sz = torch.full((n, D // Gv), -1, dtype=torch.int32, device=DEV)
+        K.kv_quant_value(cfg, torch.from_numpy(x).to(DEV), n, codes, sz)
+        torch.cuda.synchronize()
+        ref_codes, ref_sz = orc.kivi_quant_value(x, Gv, 4, tiles=tiles)
+        got = codes.cpu().numpy().reshape(-1)
+        if tiles:
+            written = np.zeros(got.size, bool)
+            written[[orc.kivi_value_byte_offset4(t, c) for t in range(n) for c in range(64)]] = True
+            assert np.array_equal(got[written], ref_codes.reshape(-1)[written])
+            assert np.all(got[~written] == 0xAB)    # the last tile's bytes past token n are left unchanged
+        else:
+            assert np.array_equal(got, ref_codes.reshape(-1))
+        assert np.array_equal(sz.cpu().numpy().view(np.uint16).reshape(n, D // Gv, 2), ref_sz)
 
 
 def _fill(cfg, Ks, Vs, L_each, max_seq_len):

@@ -204,6 +204,29 @@ def test_kivi_value_layout_is_a_lane_friendly_bijection(orc):
     assert len(seen) == 64 * 128 and {o for o, _ in seen} == set(range(2048))
 
 
+def test_kivi_value_layout_4bit_pairs_channels_of_one_token(orc):
+    """4-bit KIVI value tiles: a byte holds channels c and c + 64 of one token (so tokens are written
+    independently); word 2m + w of lane 4q + r's 32 bytes of a 16-token half holds channels 16m + q
+    (bytes 0, 1) and 16m + q + 8 (bytes 2, 3) of tokens r + 8w, r + 8w + 4 in its low nibbles, the same
+    channels + 64 in its high nibbles."""
+    seen = set()
+    for t in range(64):
+        for c in range(128):
+            off, bit = orc.kivi_value_byte_offset4(t, c), orc.kivi_value_bit4(c)
+            tt, c64 = t % 32, c % 64
+            assert off // 2048 == t // 32 and (off % 2048) // 1024 == tt // 16
+            assert (off % 1024) // 32 == 4 * (c64 % 8) + tt % 4                # the lane's 32 bytes
+            assert (off % 32) // 4 == 2 * (c64 // 16) + (tt // 8) % 2          # word 2m + w
+            assert off % 4 == 2 * ((c64 // 8) % 2) + (tt // 4) % 2 and bit == 4 * (c // 64)
+            seen.add((off, bit))
+    assert len(seen) == 64 * 128 and {o for o, _ in seen} == set(range(4096))
+    by_byte = {}
+    for t in range(32):
+        for c in range(128):
+            by_byte.setdefault(orc.kivi_value_byte_offset4(t, c), set()).add(t)
+    assert all(len(v) == 1 for v in by_byte.values())                     # one token per byte
+
+
 def test_kivi_value_pack_roundtrip_and_tail(orc):
     rng = np.random.default_rng(66)
     for n in (1, 31, 32, 45, 96):
@@ -224,6 +247,18 @@ def test_kivi_value_pack_roundtrip_and_tail(orc):
         assert np.array_equal(orc.kivi_value_pack(codes, 2), orc.tokenmajor_pack(codes, 2))
         c4 = rng.integers(0, 16, (n, 128)).astype(np.uint8)
         assert np.array_equal(orc.kivi_value_pack(c4, 4), orc.tokenmajor_pack(c4, 4))
+        # 4-bit tiles
+        p4 = orc.kivi_value_pack(c4, 4, tiles=True)
+        assert p4.shape == ((n + 31) // 32 * 32, 64)
+        f4 = p4.reshape(-1)
+        got4 = np.zeros_like(c4)
+        written4 = np.zeros(f4.size, bool)
+        for t in range(n):
+            for c in range(128):
+                o = orc.kivi_value_byte_offset4(t, c)
+                got4[t, c] = (f4[o] >> orc.kivi_value_bit4(c)) & 15
+                written4[o] = True
+        assert np.array_equal(got4, c4) and not f4[~written4].any()
 
 
 def test_kivi_decode_reads_both_value_layouts(orc):
@@ -236,6 +271,10 @@ def test_kivi_decode_reads_both_value_layouts(orc):
     a = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V), L=L)
     b = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V, value_tiles=True), L=L, value_tiles=True)
     assert np.array_equal(a, b)
+    a4 = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V, bits_v=4), L=L, bits_v=4)
+    b4 = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V, bits_v=4, value_tiles=True), L=L, bits_v=4,
+                             value_tiles=True)
+    assert np.array_equal(a4, b4)
     # and the tile bytes are read as tiles: a decode told the wrong layout differs
     c = orc.kivi_decode_one(q, *orc.kivi_build_one(K, V, value_tiles=True), L=L)
     assert not np.allclose(a, c, atol=1e-3)
