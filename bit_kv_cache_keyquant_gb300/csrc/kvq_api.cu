@@ -54,15 +54,15 @@ float sm_scale_of(const kvq_config *cfg) {
 }
 
 // Splits: chunks of a multiple of 128 tokens (the stage), sized so that the
-// persistent decode grid (4 CTAs per SM, 2 for INT8) gets about 6 (per-head units) or 8 (kv-head units)
-// units per CTA, within
-// [128, 4096] tokens and at most 256 + 1 splits per row (the last split of
+// persistent decode grid (4 CTAs per SM; 3 for grouped-query KIVI, 2 for
+// INT8) gets about 6 (per-head units) or 8 (kv-head units) units per CTA,
+// within [128, 4096] tokens and at most 256 + 1 splits per row (the last split of
 // a row holds the tokens outside the quantized tiles, e.g. the fp16 residual;
 // the token-granular INT8 cache has none and leaves that split empty).
 kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_seq_len, DecodePlan *p) {
     const int64_t rows = (int64_t)batch * cfg->n_q_heads;
-    // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI and Kitty kernels (4 CTAs per SM)
-    // handle all query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
+    // the INT8 kernel (2 CTAs per SM) and the grouped-query KIVI (3) and Kitty (4) kernels handle all
+    // query heads of a kv head in one unit; the per-head kernels run 4 CTAs per SM
     const bool int8 = variant == KVQ_VARIANT_INT8 || variant == KVQ_VARIANT_INT8_TOKEN;
     const bool kivi = variant == KVQ_VARIANT_KIVI || variant == KVQ_VARIANT_KIVI_PAGED;
     const bool kv_units = int8 || (kivi && kivi_gqa_supported(cfg)) ||
@@ -71,10 +71,13 @@ kvq_status plan_decode(const kvq_config *cfg, int variant, int batch, int max_se
                      : variant == KVQ_VARIANT_KITTY && kitty_gqa_supported(cfg) ? kitty_gqa_units_per_kv_head(cfg)
                                                                                 : 1;
     const int64_t unit_rows = kv_units ? (int64_t)batch * cfg->n_kv_heads * vsub : rows;
-    const int ctas = int8 ? 2 : 4;
+    const int ctas = int8 ? 2 : (kivi && kivi_gqa_supported(cfg)) ? 3 : 4;
     // units per CTA aimed at: fewer, longer units amortize the per-unit merge, more units balance the
     // static round-robin; measured on the MHA decode layer (B32, 32 heads, L4096) 6 beat 8 by 3.5 % and
-    // 5 lost 19 %, on the grouped-query layer (B64, 32q/8kv, L32768) 8 beat 6 and 10
+    // 5 lost 19 %, on the grouped-query layer (B64, 32q/8kv, L32768) 8 beat 6 and 10.  A dynamic
+    // schedule (a ticket counter in the workspace, largest units first) measured 2-11 % slower on
+    // both layers: the SM's issue slots pass to its other CTAs as one drains, so the static imbalance
+    // costs less than the tickets' round trips and the spills they added
     const int64_t per_cta = kv_units ? 8 : 6;
     const int64_t target_units = per_cta * num_sms() * ctas;
     int64_t chunk = (unit_rows * max_seq_len + target_units - 1) / target_units;

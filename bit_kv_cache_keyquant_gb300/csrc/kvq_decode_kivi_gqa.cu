@@ -34,7 +34,9 @@
 // stages with bulk async copies into an mbarrier ring; four consumer warps
 // each take one 32-token tile (two 16-token m-tiles) per stage; the last
 // split of every row is the residual unit, done per head on CUDA cores.
-// Four CTAs per SM with a three-stage ring keep 16 consumer warps resident.
+// Three CTAs per SM with a three-stage ring: 12 consumer warps at 128
+// registers, no spills (measured 3-6 % faster on the grouped-query layers
+// than four CTAs at 96 registers, which spill in the tile loop).
 #include "kvq_kivi.cuh"
 #include "kvq_mma.cuh"
 
@@ -75,7 +77,7 @@ static_assert(offsetof(SmemG_223, qhi) % 16 == 0 && offsetof(SmemG_223, qlo) % 1
 
 // BK-bit keys and BV-bit values (2 or 4) in an NST-stage ring.
 template <int NGV, int BK, int BV, int NST>
-__global__ void __launch_bounds__(32 * (NCWARP + 1), 4) kivi_decode_gqa_kernel(Params P) {
+__global__ void __launch_bounds__(32 * (NCWARP + 1), 3) kivi_decode_gqa_kernel(Params P) {
     using GG = Geo<BK, BV>;
     constexpr int GQ_NSTAGE = NST;
     // zero-point terms as tensor-core products (2-bit widths) or as CUDA-core dots (4-bit widths: the
@@ -502,7 +504,7 @@ cudaError_t launch_decode_kivi_gqa(const kvq_config *cfg, const KiviSrc &c, cons
     P.vsub = kivi_gqa_units_per_kv_head(cfg);
     P.gu = P.gall / P.vsub;
     const int64_t n_units = (int64_t)c.batch * cfg->n_kv_heads * P.vsub * p.splits;
-    int64_t grid = (int64_t)num_sms() * 4;
+    int64_t grid = (int64_t)num_sms() * 3;
     if (grid > n_units) grid = n_units;
     const int ngv = P.ngv;
     // 2/2 bits: three 12 KiB stages; with 4-bit codes (Gv = 32 only) two stages of up to 20 KiB
