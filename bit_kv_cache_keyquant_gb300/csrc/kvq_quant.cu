@@ -379,10 +379,11 @@ __device__ __forceinline__ long long abs_units(uint16_t h) {
 // product form (affine_code_fast); the return value reports a near-tie.
 template <bool EXACT>
 __device__ __forceinline__ bool kitty_channel_codes(const uint16_t *xs, int c, float zf, float sf, float rf, int qmax,
-                                                    uint8_t *cw, int pos, bool boosted, int hpos, int kp8) {
+                                                    uint8_t *cw, int pos, bool boosted, int hpos, int kp8, int j0,
+                                                    int j1) {
     bool tie = false;
 #pragma unroll 1
-    for (int j = 0; j < 4; ++j)
+    for (int j = j0; j < j1; ++j)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             uint32_t lo = 0u, hi = 0u;
@@ -400,35 +401,46 @@ __device__ __forceinline__ bool kitty_channel_codes(const uint16_t *xs, int c, f
     return tie;
 }
 
-// One Kitty key page (G = 128 tokens) by a 128-thread block (thread =
-// channel), staged through `smem` (G*D fp16, three D-sized arrays and the
-// planes' bytes, which the block then stores with 16-byte stores).
-__device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict__ src, int K, int score_mode,
-                                                     uint8_t *__restrict__ pg, uint8_t *smem) {
-    constexpr int G = 128;
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);                 // [G][D]
-    long long *si = reinterpret_cast<long long *>(xs + G * KVQ_D);     // [D]
-    float *sf = reinterpret_cast<float *>(si + KVQ_D);                 // [D]
-    int *boost = reinterpret_cast<int *>(sf + KVQ_D);                   // [D]
-    uint8_t *cw = reinterpret_cast<uint8_t *>(boost + KVQ_D);          // the planes: low 4096 B, high Kp * 32 B
+// Work area of a Kitty key page beside its fp16 copy, for a block of NT = 128 J threads (J threads per
+// channel): the channels' rank keys and scores, the warps' boosted counts, the J threads' partial
+// scores, extrema and ranks, and the planes' bytes (low 4096 B, high Kp * 32 B).
+__host__ __device__ constexpr size_t kitty_key_work(int J) {
+    return (size_t)KVQ_D * (8 + 4 + 4) + (size_t)J * KVQ_D * (8 + 4 + 4 + 4) + 4096 + 128 * 32;
+}
+
+// One Kitty key page (G = 128 tokens) by a block of NT threads from its fp16 copy xs [G][D] in shared
+// memory, with `work` (kitty_key_work(NT / 128) bytes).  Thread (j, c) = (tid / 128, tid % 128) serves
+// channel c and tokens [32 J' j, 32 J' (j + 1)), J' = 4 / J: its part of the exact score sum and the
+// extrema (combined over the channel's J threads: integer sums and min / max do not depend on the order),
+// its share of the rank comparisons, and the codes of its tiles.  The variance score (score_mode 1) is a
+// sequential fp32 sum in token order, taken by the channel's thread j = 0.
+template <int NT>
+__device__ __forceinline__ void kitty_key_page_from_smem(const uint16_t *__restrict__ xs, int K, int score_mode,
+                                                         uint8_t *__restrict__ pg, uint8_t *work) {
+    constexpr int G = 128, J = NT / 128, TQ = G / J;
+    unsigned long long *si = reinterpret_cast<unsigned long long *>(work);   // [D] rank keys (score mode 0)
+    float *sf = reinterpret_cast<float *>(si + KVQ_D);                 // [D] variances (score mode 1)
+    int *boost = reinterpret_cast<int *>(sf + KVQ_D);                   // [D] boosted channels per warp (4 used)
+    long long *pa = reinterpret_cast<long long *>(boost + KVQ_D);      // [J][D] partial score sums
+    float *pmn = reinterpret_cast<float *>(pa + J * KVQ_D);            // [J][D] partial minima
+    float *pmx = pmn + J * KVQ_D;                                       // [J][D] partial maxima
+    int *prk = reinterpret_cast<int *>(pmx + J * KVQ_D);                // [J][D] partial ranks
+    uint8_t *cw = reinterpret_cast<uint8_t *>(prk + J * KVQ_D);        // the planes: low 4096 B, high Kp * 32 B
     const int Kp = kitty_high_rows(K);
-    const int c = threadIdx.x;
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-    for (int i = c; i < G * KVQ_D / 8; i += 128) reinterpret_cast<uint4 *>(xs)[i] = s4[i];
-    for (int i = c; i < Kp * 8; i += 128) reinterpret_cast<uint32_t *>(cw + 4096)[i] = 0u;   // rows past K stay 0
-    __syncthreads();
+    const int tid = threadIdx.x, c = tid & (KVQ_D - 1), j = tid / KVQ_D;
+    for (int i = tid; i < Kp * 8; i += NT) reinterpret_cast<uint32_t *>(cw + 4096)[i] = 0u;   // rows past K stay 0
     long long a = 0;
     float mn = INFINITY, mx = -INFINITY, var = 0.f;
     if (score_mode == 0) {
 #pragma unroll 4
-        for (int t = 0; t < G; ++t) {
-            uint16_t h = xs[t * KVQ_D + c];
-            float x = h2f(h);
+        for (int t = j * TQ; t < (j + 1) * TQ; ++t) {
+            const uint16_t h = xs[t * KVQ_D + c];
+            const float x = h2f(h);
             a += abs_units(h);
             mn = fminf(mn, x);
             mx = fmaxf(mx, x);
         }
-    } else {
+    } else if (j == 0) {
         float s1 = 0.f, s2 = 0.f;
         for (int t = 0; t < G; ++t) {
             float x = h2f(xs[t * KVQ_D + c]);
@@ -439,19 +451,53 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
         }
         float mean = __fdiv_rn(s1, (float)G);
         var = __fsub_rn(__fdiv_rn(s2, (float)G), __fmul_rn(mean, mean));
+        sf[c] = var;
     }
-    si[c] = a;
-    sf[c] = var;
+    if (J > 1) {
+        pa[j * KVQ_D + c] = a;
+        pmn[j * KVQ_D + c] = mn;
+        pmx[j * KVQ_D + c] = mx;
+        __syncthreads();
+        if (score_mode == 0) {
+            a = 0;
+            mn = INFINITY;
+            mx = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < J; ++jj) {
+                a += pa[jj * KVQ_D + c];
+                mn = fminf(mn, pmn[jj * KVQ_D + c]);
+                mx = fmaxf(mx, pmx[jj * KVQ_D + c]);
+            }
+        } else {
+            mn = pmn[c];
+            mx = pmx[c];
+            var = sf[c];
+        }
+    }
+    // mode 0: the score (below 2^47) and the channel as one key, (a << 7) | (127 - c): a larger key is a
+    // larger score or, on a tie, a lower channel, so a channel's rank is the number of larger keys
+    const unsigned long long key = ((unsigned long long)a << 7) | (unsigned long long)(127 - c);
+    if (j == 0) si[c] = key;
     __syncthreads();
     int rank = 0;
-    for (int o = 0; o < KVQ_D; ++o) {
-        bool better = score_mode == 0 ? (si[o] > a || (si[o] == a && o < c)) : (sf[o] > var || (sf[o] == var && o < c));
-        rank += better ? 1 : 0;
+    if (score_mode == 0) {
+#pragma unroll 8
+        for (int o = j * TQ; o < (j + 1) * TQ; ++o) rank += si[o] > key ? 1 : 0;
+    } else {
+        for (int o = j * TQ; o < (j + 1) * TQ; ++o) rank += (sf[o] > var || (sf[o] == var && o < c)) ? 1 : 0;
+    }
+    if (J > 1) {
+        prk[j * KVQ_D + c] = rank;
+        __syncthreads();
+        rank = 0;
+#pragma unroll
+        for (int jj = 0; jj < J; ++jj) rank += prk[jj * KVQ_D + c];
     }
     const int boosted = rank < K;
-    // r = boosted channels below c: a ballot within the warp plus the counts of the warps below
+    // r = boosted channels below c: a ballot within the warp (every warp holds 32 consecutive channels)
+    // plus the counts of the channel warps below
     const unsigned bm = __ballot_sync(0xFFFFFFFFu, boosted);
-    if ((c & 31) == 0) boost[c >> 5] = __popc(bm);
+    if (j == 0 && (c & 31) == 0) boost[c >> 5] = __popc(bm);
     __syncthreads();
     int r = __popc(bm & ((1u << (c & 31)) - 1u));
     for (int w = 0; w < (c >> 5); ++w) r += boost[w];
@@ -464,30 +510,50 @@ __device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict_
     const int k = c >> 4, cc = c & 15;
     const int pos = (k >> 2) * 512 + ((cc & 7) >> 1) * 16 + (k & 3) * 4 + (cc & 1) + 2 * (cc >> 3);
     const int hpos = (r >> 4) * 128 + ((r & 15) >> 2) * 32 + (r & 3);
-    // the product form; a channel that met a near-tie is coded again with the quotient
-    if (kitty_channel_codes<false>(xs, c, zv, sv, rv, qmax, cw, pos, boosted, hpos, 8 * Kp))
-        kitty_channel_codes<true>(xs, c, zv, sv, rv, qmax, cw, pos, boosted, hpos, 8 * Kp);
-    uint8_t *idx = pg + KVQ_D * G / 4 + (int64_t)Kp * G / 4;
-    uint16_t *ps = reinterpret_cast<uint16_t *>(idx + KVQ_D);
-    idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
-    ps[c] = s;
-    ps[KVQ_D + c] = z;
+    // the product form; tiles that met a near-tie are coded again with the quotient
+    const int j0 = j * (4 / J), j1 = (j + 1) * (4 / J);
+    if (kitty_channel_codes<false>(xs, c, zv, sv, rv, qmax, cw, pos, boosted, hpos, 8 * Kp, j0, j1))
+        kitty_channel_codes<true>(xs, c, zv, sv, rv, qmax, cw, pos, boosted, hpos, 8 * Kp, j0, j1);
+    if (j == 0) {
+        uint8_t *idx = pg + KVQ_D * G / 4 + (int64_t)Kp * G / 4;
+        uint16_t *ps = reinterpret_cast<uint16_t *>(idx + KVQ_D);
+        idx[c] = boosted ? (uint8_t)r : (uint8_t)(K + 1);
+        ps[c] = s;
+        ps[KVQ_D + c] = z;
+    }
     __syncthreads();
     // both planes (4096 + Kp * 32 bytes, a multiple of 16) with 16-byte stores
     const uint4 *c4 = reinterpret_cast<const uint4 *>(cw);
     uint4 *o4 = reinterpret_cast<uint4 *>(pg);
-    for (int i = c; i < (4096 + Kp * 32) / 16; i += 128) o4[i] = c4[i];
+    for (int i = tid; i < (4096 + Kp * 32) / 16; i += NT) o4[i] = c4[i];
     __syncthreads();
 }
 
-constexpr size_t KITTY_KEY_SMEM = (size_t)128 * KVQ_D * 2 + KVQ_D * (8 + 4 + 4) + 4096 + 128 * 32;
+// Shared memory of a block of NT threads quantizing key pages: the page's fp16 copy, then the work area.
+__host__ __device__ constexpr size_t kitty_key_smem(int NT) { return (size_t)128 * KVQ_D * 2 + kitty_key_work(NT / 128); }
+constexpr size_t KITTY_KEY_SMEM = kitty_key_smem(128);
+constexpr int KITTY_KEY_BULK_NT = 256;   // the bulk and paged entry points: two threads per channel, 4 blocks per SM
 
-__global__ void __launch_bounds__(128) quant_key_kitty_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
-                                                              int K, int score_mode, uint8_t *__restrict__ pages,
-                                                              int64_t page_bytes) {
+// The same from global memory: the block copies the page into `smem` (G*D fp16, then the work area).
+template <int NT>
+__device__ __forceinline__ void kitty_key_page_quant(const uint16_t *__restrict__ src, int K, int score_mode,
+                                                     uint8_t *__restrict__ pg, uint8_t *smem) {
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int i = threadIdx.x; i < 128 * KVQ_D / 8; i += NT) reinterpret_cast<uint4 *>(xs)[i] = s4[i];
+    __syncthreads();
+    kitty_key_page_from_smem<NT>(xs, K, score_mode, pg, smem + (size_t)128 * KVQ_D * 2);
+}
+
+__global__ void __launch_bounds__(KITTY_KEY_BULK_NT, 4) quant_key_kitty_kernel(const uint16_t *__restrict__ k,
+                                                                               int64_t n_pages, int K, int score_mode,
+                                                                               uint8_t *__restrict__ pages,
+                                                                               int64_t page_bytes) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     for (int64_t p = blockIdx.x; p < n_pages; p += gridDim.x)
-        kitty_key_page_quant(k + p * (int64_t)128 * KVQ_D, K, score_mode, pages + p * page_bytes, smem_raw);
+        kitty_key_page_quant<KITTY_KEY_BULK_NT>(k + p * (int64_t)128 * KVQ_D, K, score_mode, pages + p * page_bytes,
+                                                smem_raw);
 }
 
 // ---------------------------------------------------------------------------
@@ -644,12 +710,12 @@ cudaError_t launch_quant_key_kitty(const kvq_config *cfg, const void *k, int64_t
     if (n_pages == 0) return cudaSuccess;
     const int K = cfg->boost_k;
     const int64_t pb = kitty_key_page_bytes(K);
-    const size_t smem = KITTY_KEY_SMEM;
+    const size_t smem = kitty_key_smem(KITTY_KEY_BULK_NT);
     static std::atomic<uint64_t> attr_done{0};
     if (cudaError_t e = smem_opt_in(quant_key_kitty_kernel, smem, attr_done)) return e;
     const int grid = grid_cap(n_pages, 4);
-    quant_key_kitty_kernel<<<grid, 128, smem, st>>>(static_cast<const uint16_t *>(k), n_pages, K, score_mode,
-                                                    static_cast<uint8_t *>(pages), pb);
+    quant_key_kitty_kernel<<<grid, KITTY_KEY_BULK_NT, smem, st>>>(static_cast<const uint16_t *>(k), n_pages, K,
+                                                                  score_mode, static_cast<uint8_t *>(pages), pb);
     return cudaGetLastError();
 }
 
@@ -1089,8 +1155,9 @@ __device__ __forceinline__ uint8_t *kitty_paged_record(const KittyPagedDst &D, i
     return D.pool + ((int64_t)pg * D.Hkv + D.kvh) * D.rec_bytes;
 }
 
-__global__ void __launch_bounds__(128) quant_key_kitty_paged_kernel(const uint16_t *__restrict__ k, int64_t n_pages,
-                                                                    int K, int score_mode, KittyPagedDst D) {
+__global__ void __launch_bounds__(KITTY_KEY_BULK_NT, 4) quant_key_kitty_paged_kernel(const uint16_t *__restrict__ k,
+                                                                                     int64_t n_pages, int K,
+                                                                                     int score_mode, KittyPagedDst D) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     for (int64_t p = blockIdx.x; p < n_pages; p += gridDim.x) {
         uint8_t *rec = kitty_paged_record(D, (int)p);
@@ -1098,7 +1165,7 @@ __global__ void __launch_bounds__(128) quant_key_kitty_paged_kernel(const uint16
             if (threadIdx.x == 0) atomicOr(D.err, KVQ_DEVICE_ERR_POOL);
             continue;
         }
-        kitty_key_page_quant(k + p * (int64_t)128 * KVQ_D, K, score_mode, rec, smem_raw);
+        kitty_key_page_quant<KITTY_KEY_BULK_NT>(k + p * (int64_t)128 * KVQ_D, K, score_mode, rec, smem_raw);
     }
 }
 
@@ -1149,10 +1216,11 @@ cudaError_t launch_quant_key_kitty_paged(const kvq_config *cfg, const kvq_kitty_
     const KittyPagedDst D = kitty_paged_dst(cfg, c, c->k_pages, kpb, page0, row, kvh);
     if (!D.err) return cudaErrorInvalidDevicePointer;
     static std::atomic<uint64_t> attr_done{0};
-    if (cudaError_t e = smem_opt_in(quant_key_kitty_paged_kernel, KITTY_KEY_SMEM, attr_done)) return e;
+    const size_t smem = kitty_key_smem(KITTY_KEY_BULK_NT);
+    if (cudaError_t e = smem_opt_in(quant_key_kitty_paged_kernel, smem, attr_done)) return e;
     const int grid = grid_cap(n, 4);
-    quant_key_kitty_paged_kernel<<<grid, 128, KITTY_KEY_SMEM, st>>>(static_cast<const uint16_t *>(k), n, cfg->boost_k,
-                                                                    score_mode, D);
+    quant_key_kitty_paged_kernel<<<grid, KITTY_KEY_BULK_NT, smem, st>>>(static_cast<const uint16_t *>(k), n,
+                                                                        cfg->boost_k, score_mode, D);
     return cudaGetLastError();
 }
 
@@ -1225,7 +1293,7 @@ __global__ void __launch_bounds__(128) append_kitty_kernel(AppendKittyParams P) 
     uint16_t *vloc = P.v_local + bk * (int64_t)R * KVQ_D;
     if (L > S && (L - S) % G == 0) {
         const int64_t rec = kitty_record(P, b, h, (L - S) / G - 1);
-        if (rec >= 0) kitty_key_page_quant(kqb, P.K, P.score_mode, P.k_pages + rec * P.kpb, smem_raw);
+        if (rec >= 0) kitty_key_page_quant<128>(kqb, P.K, P.score_mode, P.k_pages + rec * P.kpb, smem_raw);
     }
     const int E = L - S - R;
     const int64_t vrec = E > 0 && E % G == 0 ? kitty_record(P, b, h, E / G - 1) : -1;

@@ -289,6 +289,47 @@ def test_workload_full_size_sampled(K, orc, widx):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("widx", [2, 3, 9, 10])
+def test_workload_shapes_gaussian_sampled(K, orc, widx):
+    """The workloads' head counts, code widths and full lengths with Gaussian activations (N(0, 1)
+    rounded to fp16, one key channel per kv head scaled by 15): the tails and off-grid values that the
+    workload generator's bounded grid never produces.  Two batch rows; sampled (row, kv head) pairs
+    against the oracle, in the launch shape of the full workload's kernel."""
+    from bit_kv_cache_keyquant_gb300 import cache as C
+    w = I.WORKLOADS[widx]
+    B, L, Hkv = 2, w.seq_len, w.n_kv_heads
+    cfg = K.make_config(n_q_heads=w.n_q_heads, n_kv_heads=Hkv, bits_k=w.bits_k, bits_v=w.bits_v)
+    rng = np.random.default_rng(1000 + widx)
+    pairs = {(0, 0), (1, Hkv - 1), (0, Hkv // 2)}
+    cache = C.KiviCache(cfg, B, L, device=DEV)
+    kept = {}
+    for b in range(B):
+        for h in range(Hkv):
+            k = rng.standard_normal((L, 128), dtype=np.float32)
+            k[:, (7 * h + 3) % 128] *= 15.0
+            Kh = k.astype(np.float16)
+            Vh = rng.standard_normal((L, 128), dtype=np.float32).astype(np.float16)
+            cache.fill(b, h, torch.from_numpy(Kh).to(DEV), torch.from_numpy(Vh).to(DEV))
+            if (b, h) in pairs:
+                kept[(b, h)] = (Kh, Vh)
+    q = torch.from_numpy(rng.standard_normal((B, w.n_q_heads, 128), dtype=np.float32).astype(np.float16)).to(DEV)
+    n, wsb = K.kv_decode_attn_plan(cfg, K.KVQ_VARIANT_KIVI, B, L)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty((B, w.n_q_heads, 128), dtype=torch.float16, device=DEV)
+    K.kv_decode_attn(cfg, cache.desc(), q, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert K.kvq_get_device_error() == 0
+    outn = out.float().cpu().numpy()
+    assert np.isfinite(outn).all()
+    qn = q.cpu().numpy()
+    g = w.n_q_heads // Hkv
+    for (b, h), (Kh, Vh) in kept.items():
+        parts = orc.kivi_build_one(Kh, Vh, bits_k=w.bits_k, bits_v=w.bits_v)
+        want = orc.kivi_decode_one(qn[b, h * g:(h + 1) * g], *parts, L=L, bits_k=w.bits_k, bits_v=w.bits_v)
+        assert_attn_close(outn[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
+
+
+@pytest.mark.slow
 def test_decode_offsets_beyond_2gib(K, orc):
     """Maximum-size addressing: a cache whose code and parameter arrays span 4.3 GB (B32, 64 query / 16 kv
     heads, 262144 tokens).  Random bytes fill every row; the first and the last (row, kv head) hold real
