@@ -109,6 +109,29 @@ def test_kitty_workload_full_size_sampled(K, orc):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("mode", [0, 1])
+def test_kitty_workload_shape_gaussian_sampled(K, orc, mode):
+    """The mixed-key workload's heads and full length with Gaussian activations (per-channel sigma
+    log-uniform over [0.5, 8], as the workload states its key channels): two batch rows, both boost
+    selections, sampled (row, kv head) pairs against the oracle."""
+    w = I.WORKLOADS[4]
+    B, L, Hkv = 2, w.seq_len, w.n_kv_heads
+    cfg = K.make_config(n_q_heads=w.n_q_heads, n_kv_heads=Hkv, group_k=128, sink=32, residual=128, boost_k=16)
+    rng = np.random.default_rng(4000 + mode)
+    sig = 2.0 ** rng.uniform(-1.0, 3.0, (Hkv, 128))
+    Ks = [[(rng.standard_normal((L, 128), dtype=np.float32) * sig[h]).astype(np.float16) for h in range(Hkv)]
+          for _ in range(B)]
+    Vs = [[rng.standard_normal((L, 128), dtype=np.float32).astype(np.float16) for h in range(Hkv)] for _ in range(B)]
+    q = rng.standard_normal((B, w.n_q_heads, 128), dtype=np.float32).astype(np.float16)
+    got = _run(K, cfg, Ks, Vs, q, L, mode)
+    g = w.n_q_heads // Hkv
+    for b, h in ((0, 0), (1, Hkv - 1), (0, Hkv // 2)):
+        parts = orc.kitty_build_one(Ks[b][h], Vs[b][h], 128, 16, 32, 128, mode)
+        want = orc.kitty_decode_one(q[b, h * g:(h + 1) * g], *parts, L=L, K=16, S=32, R=128)
+        assert_attn_close(got[b, h * g:(h + 1) * g], want, f"row {b}, kv head {h}")
+
+
+@pytest.mark.slow
 def test_kitty_offsets_beyond_2gib(K, orc):
     """Maximum-size addressing: key page records spanning 2.2 GB (B32, 64 query / 16 kv heads, 104992 tokens).
     Random bytes fill every page; the first and the last (row, kv head) hold real data (the last at byte
