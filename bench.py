@@ -403,8 +403,11 @@ def decode_step(st, stream, ev=None, q=None, vnew=None, knew=None, out=None):
 
 def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
     """The workload's quantization kernels on their own, outside the timed step, at 256 MB of fp16 input
-    per call (twice the L2): us per call, and HBM GB/s of the bytes each call must move (fp16 input read,
-    codes and scales written) against the measured copy peak."""
+    per call (twice the L2): us per call, HBM GB/s of the bytes each call must move (fp16 input read,
+    codes and scales written) against the measured copy peak, and the call's time amortized over a
+    layer-step: the units one decode step needs on average (one value token per (row, kv head); a key
+    flush of R/G groups every R steps; a Kitty key and value page every 128 steps; an INT8 block per side
+    every 256 steps), times the time per unit."""
     import torch
     from bit_kv_cache_keyquant_gb300 import kvq
     peak, _ = _peaks()
@@ -424,9 +427,12 @@ def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / reps
 
-    def entry(us, units, unit, nbytes):
+    pairs = w.batch * w.n_kv_heads
+
+    def entry(us, units, unit, nbytes, per_step):
         gbs = nbytes / (us * 1e-6) / 1e9
-        return {"us_per_call": us, "units": units, "unit": unit, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak}
+        return {"us_per_call": us, "units": units, "unit": unit, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak,
+                "units_per_step": per_step, "amortized_us_per_step": us * per_step / units}
 
     x = torch.randn(total // 2, generator=gen, device=dev).half()
     out = {}
@@ -437,21 +443,22 @@ def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
             kc = torch.empty(ng * G * 128 * w.bits_k // 8, dtype=torch.uint8, device=dev)
             ks = torch.empty((ng, 128), dtype=torch.int32, device=dev)
             us = timed(lambda: kvq.kv_quant_key(cfg, x, ng, kc, ks, stream))
-            out["kv_quant_key"] = entry(us, ng, f"{G}-token key groups", total + kc.numel() + ks.numel() * 4)
+            out["kv_quant_key"] = entry(us, ng, f"{G}-token key groups", total + kc.numel() + ks.numel() * 4,
+                                        pairs / G)
             nt = total // 256
             vc = torch.empty((nt + 31) // 32 * 32 * 128 * w.bits_v // 8, dtype=torch.uint8, device=dev)   # whole tiles
             vs = torch.empty((nt, 128 // Gv), dtype=torch.int32, device=dev)
             us = timed(lambda: kvq.kv_quant_value(cfg, x, nt, vc, vs, stream))
-            out["kv_quant_value"] = entry(us, nt, "value tokens", total + vc.numel() + vs.numel() * 4)
+            out["kv_quant_value"] = entry(us, nt, "value tokens", total + vc.numel() + vs.numel() * 4, pairs)
         elif w.variant == "kitty":
             npg = total // (128 * 128 * 2)
             kp = torch.empty(npg * kvq.kvq_kitty_key_page_bytes(cfg), dtype=torch.uint8, device=dev)
             us = timed(lambda: kvq.kv_quant_key_kitty(cfg, x, npg, w.score_mode, kp, stream))
-            out["kv_quant_key_kitty"] = entry(us, npg, "128-token key pages", total + kp.numel())
+            out["kv_quant_key_kitty"] = entry(us, npg, "128-token key pages", total + kp.numel(), pairs / 128)
             out["kv_quant_key_kitty"]["score_mode"] = w.score_mode
             vp = torch.empty(npg * kvq.kvq_kitty_value_page_bytes(cfg), dtype=torch.uint8, device=dev)
             us = timed(lambda: kvq.kv_quant_value_kitty(cfg, x, npg, vp, stream))
-            out["kv_quant_value_kitty"] = entry(us, npg, "128-token value pages", total + vp.numel())
+            out["kv_quant_value_kitty"] = entry(us, npg, "128-token value pages", total + vp.numel(), pairs / 128)
         elif w.variant == "int8":
             nb = total // (256 * 128 * 2)
             blk = torch.arange(nb, dtype=torch.int32, device=dev)
@@ -460,7 +467,8 @@ def quant_kernels_bench(w, cfg, dev, stream, reps: int = 10):
             scale = torch.empty((nb, 128), dtype=torch.float16, device=dev)
             us = timed(lambda: kvq.kv_quant_int8_dither(cfg, x, nb, meta[0], meta[1], meta[2], 5, 0, w.seed, codes,
                                                         scale, stream))
-            out["kv_quant_int8_dither"] = entry(us, nb, "256-token blocks", total + codes.numel() + scale.numel() * 2)
+            out["kv_quant_int8_dither"] = entry(us, nb, "256-token blocks", total + codes.numel() + scale.numel() * 2,
+                                                2 * pairs / 256)
     torch.cuda.synchronize()
     return out
 
