@@ -219,8 +219,12 @@ __device__ __forceinline__ void write_unit(SM &S, const HeadState &H, float *ws_
 
 // One tile of n <= 32 tokens.  kfn(tt, kv[4]) / vfn(tt, vv[4]) return this
 // lane's four dequantized channels of token tt of the tile; wk2[j][i] holds
-// the key weights (alpha q) of heads 2j, 2j+1 for channel i.
-template <typename KF, typename VF>
+// the key weights (alpha q) of heads 2j, 2j+1 for channel i.  KU key batches
+// of four tokens and VU value tokens are unrolled together, so that as many
+// Philox chains are in flight (block INT8: KU = 2, VU = 8 measured 871.7 ->
+// 823.8 us on its workload; the slot-pool kernel, bound by its gathering
+// producer, measured best at 1 and 4).
+template <int KU, int VU, typename KF, typename VF>
 __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 2][4], KF kfn, VF vfn, HeadState &H,
                                      float (*pw)[GMAX], float (*red)[32], int lane) {
     // ---- keys: 8 batches of 4 tokens; per lane 4 x 8 head partials over its 4 channels, then a
@@ -228,7 +232,7 @@ __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 
     float sc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) sc[c] = -INFINITY;
-#pragma unroll 1
+#pragma unroll KU
     for (int c4 = 0; c4 < 8; ++c4) {
         float v[32];
 #pragma unroll
@@ -290,7 +294,7 @@ __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 
     }
     __syncwarp();
     // ---- values: lane = channels, head weights broadcast from shared memory ----
-#pragma unroll 4
+#pragma unroll VU
     for (int tt = 0; tt < 32; ++tt) {
         if (tt >= n) break;
         float vv[4];
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                     const uint2 x = __ldg(reinterpret_cast<const uint2 *>(vt + (int64_t)((r0 + tt) % T) * KVQ_D));
                     vv[0] = h2f(lo16(x.x)); vv[1] = h2f(hi16(x.x)); vv[2] = h2f(lo16(x.y)); vv[3] = h2f(hi16(x.y));
                 };
-                tile(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
+                tile<2, 8>(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
             }
         } else {
             const int nst = (U.t1 - U.t0 + STAGE_TOK - 1) / STAGE_TOK;
@@ -422,7 +426,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_decode_kernel(Param
                         vv[2] = vs2 * d[2];
                         vv[3] = vs3 * d[3];
                     };
-                    tile(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
+                    tile<2, 8>(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -661,7 +665,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
                     vv[2] = sc * d[2];
                     vv[3] = sc * d[3];
                 };
-                tile(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
+                tile<1, 4>(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[buf]);
