@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&S.full[i], 32);
+            mbar_init(&S.full[i], 64);      // per producer lane: its slots and scales, then its code copies
             mbar_init(&S.empty[i], NCWARP);
         }
         S.abort_flag = 0;
@@ -587,7 +587,6 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
                 const int tok = U.t0 + s * STAGE_TOK;
                 const int nt = min(STAGE_TOK, U.t1 - tok);
                 int64_t rec[4];
-                uint32_t bytes = 0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int i = lane + 32 * j;
@@ -604,18 +603,27 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
                         const uint2 b = load_scales(P.v_scale + rec[j] * P.nsc, P.nsc);
                         *reinterpret_cast<uint2 *>(&S.ks[buf][i][0]) = a;
                         *reinterpret_cast<uint2 *>(&S.vs[buf][i][0]) = b;
-                        bytes += 2 * KVQ_D;
                     }
                 }
-                mbar_expect_tx(&S.full[buf], bytes);
+                mbar_arrive(&S.full[buf]);                 // the slots and scales this lane stored
+                // the tokens' code rows, 16 bytes per copy from every lane (no per-lane serialization of
+                // bulk copies); the stage barrier counts this lane's arrival once all of them landed
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (rec[j] >= 0) {
                         const int i = lane + 32 * j;
-                        bulk_g2s(S.kc[buf] + i * KVQ_D, P.k_codes + rec[j] * KVQ_D, KVQ_D, &S.full[buf]);
-                        bulk_g2s(S.vc[buf] + i * KVQ_D, P.v_codes + rec[j] * KVQ_D, KVQ_D, &S.full[buf]);
+                        const int8_t *kg = P.k_codes + rec[j] * KVQ_D, *vg = P.v_codes + rec[j] * KVQ_D;
+#pragma unroll
+                        for (int c = 0; c < KVQ_D / 16; ++c) {
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                                         ::"r"(smem_addr(S.kc[buf] + i * KVQ_D + 16 * c)), "l"(kg + 16 * c) : "memory");
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                                         ::"r"(smem_addr(S.vc[buf] + i * KVQ_D + 16 * c)), "l"(vg + 16 * c) : "memory");
+                        }
                     }
                 }
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&S.full[buf]))
+                             : "memory");
             }
         }
         // no copy may be in flight when the CTA exits
