@@ -220,10 +220,9 @@ __device__ __forceinline__ void write_unit(SM &S, const HeadState &H, float *ws_
 // One tile of n <= 32 tokens.  kfn(tt, kv[4]) / vfn(tt, vv[4]) return this
 // lane's four dequantized channels of token tt of the tile; wk2[j][i] holds
 // the key weights (alpha q) of heads 2j, 2j+1 for channel i.  KU key batches
-// of four tokens and VU value tokens are unrolled together, so that as many
-// Philox chains are in flight (block INT8: KU = 2, VU = 8 measured 871.7 ->
-// 823.8 us on its workload; the slot-pool kernel, bound by its gathering
-// producer, measured best at 1 and 4).
+// of four tokens and VU value tokens are unrolled together, so that more
+// Philox chains are in flight (KU = 2, VU = 8 measured 871.7 -> 823.8 us on
+// the block-INT8 workload, 1178.6 -> 1137.9 us on the slot-pool one).
 template <int KU, int VU, typename KF, typename VF>
 __device__ __forceinline__ void tile(int n, const unsigned long long wk2[GMAX / 2][4], KF kfn, VF vfn, HeadState &H,
                                      float (*pw)[GMAX], float (*red)[32], int lane) {
@@ -673,7 +672,7 @@ __global__ void __launch_bounds__(32 * (NCWARP + 1), 2) int8_token_decode_kernel
                     vv[2] = sc * d[2];
                     vv[3] = sc * d[3];
                 };
-                tile<1, 4>(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
+                tile<2, 8>(n, wk2, kfn, vfn, H, S.pw[warp], S.red[warp], lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[buf]);
